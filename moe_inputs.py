@@ -1,0 +1,159 @@
+"""Seeded synthetic inputs for the MoE layer, shared by the CUDA path and the oracle.
+
+This module holds none of the layer's arithmetic: it only draws tensors and
+names the workloads.  Both sides of a parity check receive the very same
+tensors from here (drawn once, on the device under test, then copied to the
+host for the oracle), so no generator has to be re-implemented bit-exactly.
+
+Recipe (every workload):
+  * one torch.Generator per tensor, on the target device, seeded with
+    ``(seed << 8) | tensor_index`` so that a tensor's values depend only on the
+    seed, its index and its own shape (decode sizes with different T share the
+    expert weights);
+  * x ~ N(0, 1); router and expert weights ~ N(0, 1/fan_in) with fan_in = d for
+    W_gate, W1, W3 (and their shared-expert copies) and fan_in = F for W2;
+  * values are drawn in fp32 and, for bf16 workloads, rounded to bf16 (round to
+    nearest even);
+  * the selection-only bias (DeepSeek-V3-shaped layer) ~ U(-0.1, 0.1), fp32;
+  * the skewed layer adds to every token's logits the log-probability of a
+    Zipf(s) rank distribution over the experts (expert 0 the most popular).
+
+Weights are stored as the layer consumes them: W_gate [E, d], W1 and W3
+[E, F, d], W2 [E, d, F], shared W1/W3 [F_s, d], shared W2 [d, F_s].
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+
+TENSOR_INDEX = {"x": 0, "w_gate": 1, "w1": 2, "w3": 3, "w2": 4, "ws1": 5, "ws3": 6, "ws2": 7,
+                "select_bias": 8}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    d: int
+    E: int
+    F: int
+    k: int
+    dtype: str = "bf16"          # "bf16" or "f32" (x, weights and y)
+    n_shared: int = 0
+    F_s: int = 0
+    renormalize: bool = True
+    capacity: int = -1           # < 0: unlimited
+    alpha: float = 0.01
+    select_bias: bool = False    # draw a selection-only bias ~ U(-0.1, 0.1)
+    zipf_s: float = 0.0          # > 0: add Zipf(s) log-probabilities to the logits
+    seed: int = 0
+    notes: str = field(default="", compare=False)
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+def _cap(T, k, E, factor=1.25):
+    return int(math.floor(factor * T * k / E))
+
+
+WORKLOADS = {
+    "tiny_f32": Workload("tiny_f32", T=256, d=256, E=8, F=512, k=2, dtype="f32"),
+    "mixtral_prefill": Workload("mixtral_prefill", T=4096, d=4096, E=8, F=14336, k=2),
+    "mixtral_decode_t1": Workload("mixtral_decode_t1", T=1, d=4096, E=8, F=14336, k=2),
+    "mixtral_decode_t8": Workload("mixtral_decode_t8", T=8, d=4096, E=8, F=14336, k=2),
+    "mixtral_decode_t32": Workload("mixtral_decode_t32", T=32, d=4096, E=8, F=14336, k=2),
+    "mixtral_decode_t128": Workload("mixtral_decode_t128", T=128, d=4096, E=8, F=14336, k=2),
+    "deepseek_v3": Workload("deepseek_v3", T=8192, d=7168, E=256, F=2048, k=8, n_shared=1, F_s=2048,
+                            select_bias=True),
+    "skewed_capacity": Workload("skewed_capacity", T=16384, d=2048, E=64, F=1408, k=2,
+                                capacity=_cap(16384, 2, 64), zipf_s=1.2),
+}
+
+
+def zipf_log_probs(E: int, s: float) -> torch.Tensor:
+    """log of the Zipf(s) probability of rank r = e + 1 among E ranks (fp64 -> fp32)."""
+    r = torch.arange(1, E + 1, dtype=torch.float64)
+    w = r.pow(-s)
+    return (w / w.sum()).log().to(torch.float32)
+
+
+def _gen(device, seed, name):
+    g = torch.Generator(device=device)
+    g.manual_seed((int(seed) << 8) | TENSOR_INDEX[name])
+    return g
+
+
+def _normal(shape, std, device, dtype, seed, name, chunk_dim0=False):
+    g = _gen(device, seed, name)
+    if chunk_dim0 and len(shape) == 3:
+        out = torch.empty(shape, dtype=dtype, device=device)
+        for e in range(shape[0]):
+            out[e] = (torch.randn(shape[1:], generator=g, device=device) * std).to(dtype)
+        return out
+    return (torch.randn(shape, generator=g, device=device) * std).to(dtype)
+
+
+def make_layer(w: Workload, device="cpu") -> dict:
+    """Draw every input tensor of workload ``w`` on ``device``."""
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dev = torch.device(device)
+    s = w.seed
+    L = {
+        "x": _normal((w.T, w.d), 1.0, dev, dt, s, "x"),
+        "w_gate": _normal((w.E, w.d), 1.0 / math.sqrt(w.d), dev, dt, s, "w_gate"),
+        "w1": _normal((w.E, w.F, w.d), 1.0 / math.sqrt(w.d), dev, dt, s, "w1", True),
+        "w3": _normal((w.E, w.F, w.d), 1.0 / math.sqrt(w.d), dev, dt, s, "w3", True),
+        "w2": _normal((w.E, w.d, w.F), 1.0 / math.sqrt(w.F), dev, dt, s, "w2", True),
+        "ws1": None, "ws3": None, "ws2": None, "logit_bias": None, "select_bias": None,
+    }
+    if w.n_shared:
+        L["ws1"] = _normal((w.F_s, w.d), 1.0 / math.sqrt(w.d), dev, dt, s, "ws1")
+        L["ws3"] = _normal((w.F_s, w.d), 1.0 / math.sqrt(w.d), dev, dt, s, "ws3")
+        L["ws2"] = _normal((w.d, w.F_s), 1.0 / math.sqrt(w.F_s), dev, dt, s, "ws2")
+    if w.select_bias:
+        g = _gen(dev, s, "select_bias")
+        L["select_bias"] = (torch.rand((w.E,), generator=g, device=dev) * 0.2 - 0.1).float()
+    if w.zipf_s > 0:
+        L["logit_bias"] = zipf_log_probs(w.E, w.zipf_s).to(dev)
+    return L
+
+
+def to_numpy(t):
+    """Host numpy view for the oracle: float32 stays float32, bf16 becomes uint16 bits."""
+    if t is None:
+        return None
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view("uint16")
+    return t.numpy()
+
+
+def layer_numpy(L: dict) -> dict:
+    return {k: to_numpy(v) for k, v in L.items()}
+
+
+# ---- work accounting (what counts as the layer's algorithmic work) ----------
+
+def expert_params(d: int, F: int) -> int:
+    """Parameters of one SwiGLU expert: W1, W3 (F x d) and W2 (d x F)."""
+    return 3 * d * F
+
+
+def algorithmic_flops(w: Workload, kept_total: int) -> float:
+    """FLOPs of one layer call: routed (kept) expert work, shared expert, router.
+
+    Counts 2 FLOPs per multiply-add; no padded tile rows, no dropped entries.
+    """
+    routed = 2.0 * expert_params(w.d, w.F) * kept_total
+    shared = 2.0 * expert_params(w.d, w.F_s) * w.T * w.n_shared
+    router = 2.0 * w.T * w.d * w.E
+    return routed + shared + router
+
+
+def expert_weight_bytes(w: Workload, n_touched: int) -> float:
+    """Bytes of expert weights a call must read: touched routed experts + shared."""
+    eb = 2 if w.dtype == "bf16" else 4
+    return float(eb * (expert_params(w.d, w.F) * n_touched + expert_params(w.d, w.F_s) * w.n_shared))

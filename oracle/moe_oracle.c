@@ -1,0 +1,341 @@
+/*
+ * moe_oracle.c -- TEST INFRASTRUCTURE, not product code.
+ *
+ * The plain, slow fp64 CPU oracle for the forward pass of a Mixture-of-Experts
+ * SwiGLU FFN layer.  Only the test suite, the package's smoke check and the
+ * benchmark's CPU-baseline leg load it.  It shares no code, header, table or
+ * helper with the CUDA library; the two meet only in the seeded inputs that the
+ * test harness hands to both.
+ *
+ * Every floating-point step is done in IEEE double from the exact stored input
+ * values (fp32, or bf16 widened exactly), with no intermediate rounding to a
+ * narrower type.  Loops are written in the per-token form that the pages use as
+ * the definition of the layer; nothing is blocked, fused or reordered beyond an
+ * OpenMP split over independent tokens.
+ *
+ * Sources, by page title and section:
+ *  [MoE-Arch]   "MoE Architecture" (infra.bea.ai), section 2 "The Router" /
+ *               "Gating Function" and "Load Balancing"; section 3 "Shared
+ *               Experts"; section 1 "The Core Idea" (y = sum_i g_i Expert_i(x)).
+ *  [MoE-Notes]  "Mixture of Experts" (avinashkadimisetty.com notes), "How it
+ *               works": routing math g(x) = softmax(W_g x), keep top-k and
+ *               renormalise "in many implementations"; capacity and dropping.
+ *  [Handbook]   "Mixture of experts (MoE)" (anrans ai-infra-handbooks),
+ *               "Structure" (router d->E, top-k, SwiGLU experts, weighted sum,
+ *               shared expert), "Implementation: token by token vs. grouped by
+ *               expert" (the naive per-token form; the stable sort by expert,
+ *               per-expert counts and running start), "Load balancing"
+ *               (E * sum f_i P_i, bias used only for selection).
+ *  [DeepDive]   "MoE (Mixture of Experts) Deep Dive: Principles, Formulas, and
+ *               Implementation", "Weighted Sum Output" (normalise the selected
+ *               probabilities), "Load Balancing Loss Derivation" (N sum F_i P_i).
+ *  [OneDeep]    "One Deep Concept #04 -- Mixture of Experts", section 4 "Core
+ *               Innovation -- Routing" (un-renormalised y = sum_{i in T} p_i E_i).
+ *
+ * Parity status of each function is stated beside it; the pins live in the
+ * test suite (tests/test_oracle_pins.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+/* Exact widening of a stored element to double.  bf16 is the top half of an
+ * IEEE binary32, so shifting its 16 bits up gives the same value exactly. */
+static double elem(const void *base, int dtype, size_t i) {
+    if (dtype == ORACLE_F32) return (double)((const float *)base)[i];
+    uint32_t u = (uint32_t)((const uint16_t *)base)[i] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Router for every token t:
+ *   l   = W_g x_t (+ logit_bias)          [MoE-Notes] g(x) = softmax(W_g x), W_g in R^{E x d}
+ *   p   = softmax(l)                      [MoE-Arch] Gating Function; [OneDeep] s4
+ *   s   = l + select_bias                 [Handbook] Load balancing: the bias enters only
+ *                                         the choice of the top-k, never the weights
+ *   ids = the k largest s, descending,    [Handbook] Structure step 2; ties go to the lower
+ *         ties to the lower expert index  expert index (the pages are silent on ties)
+ *   g_j = p[ids_j], divided by sum_j g_j  [DeepDive] Weighted Sum Output (0.55, 0.3 -> /0.85);
+ *         when renormalize != 0           [Handbook] route(): weights / weights.sum
+ * W_g is stored [E][d] (one row of d weights per expert).
+ * Outputs: topk_ids [T][k], gates [T][k], probs [T][E] (nullable), and
+ * margin [T] = s_(k) - s_(k+1) (the gap between the k-th and (k+1)-th
+ * selection score; +inf when k == E), nullable.
+ * Pinned: worked examples, brute-force top-k, softmax special cases.
+ */
+int oracle_route(int T, int d, int E, int k, int dtype, const void *x, const void *w_gate,
+                 const float *logit_bias, const float *select_bias, int renormalize,
+                 int32_t *topk_ids, double *gates, double *probs, double *margin) {
+    if (T < 0 || d < 1 || E < 1 || k < 1 || k > E) return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *l = (double *)malloc(sizeof(double) * (size_t)E);
+        double *p = (double *)malloc(sizeof(double) * (size_t)E);
+        double *s = (double *)malloc(sizeof(double) * (size_t)E);
+        char *taken = (char *)malloc((size_t)E);
+        int ok = l && p && s && taken;
+        /* every thread reaches the work-sharing loop, so a failed malloc
+         * cannot leave the others waiting at its barrier */
+#pragma omp for schedule(static)
+        for (int t = 0; t < T; ++t) {
+            if (!ok) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i)
+                    acc += elem(w_gate, dtype, (size_t)e * d + i) * elem(x, dtype, (size_t)t * d + i);
+                l[e] = acc + (logit_bias ? (double)logit_bias[e] : 0.0);
+            }
+            double m = l[0];
+            for (int e = 1; e < E; ++e)
+                if (l[e] > m) m = l[e];
+            double z = 0.0;
+            for (int e = 0; e < E; ++e) {
+                p[e] = exp(l[e] - m);
+                z += p[e];
+            }
+            for (int e = 0; e < E; ++e) p[e] /= z;
+            for (int e = 0; e < E; ++e) {
+                s[e] = l[e] + (select_bias ? (double)select_bias[e] : 0.0);
+                taken[e] = 0;
+            }
+            /* k passes of "largest remaining score, lowest index on ties". */
+            double gsum = 0.0, kth = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int best = -1;
+                for (int e = 0; e < E; ++e)
+                    if (!taken[e] && (best < 0 || s[e] > s[best])) best = e;
+                taken[best] = 1;
+                topk_ids[(size_t)t * k + j] = best;
+                gates[(size_t)t * k + j] = p[best];
+                gsum += p[best];
+                kth = s[best];
+            }
+            if (renormalize)
+                for (int j = 0; j < k; ++j) gates[(size_t)t * k + j] /= gsum;
+            if (margin) {
+                if (k == E) {
+                    margin[t] = INFINITY;
+                } else {
+                    int nxt = -1;
+                    for (int e = 0; e < E; ++e)
+                        if (!taken[e] && (nxt < 0 || s[e] > s[nxt])) nxt = e;
+                    margin[t] = kth - s[nxt];
+                }
+            }
+            if (probs)
+                for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = p[e];
+        }
+        free(l);
+        free(p);
+        free(s);
+        free(taken);
+    }
+    return bad ? -2 : 0;
+}
+
+/*
+ * Gates for a given set of ids: g_j = p[t, ids_j], renormalised over the k
+ * chosen when renormalize != 0.  Same rule as oracle_route; used when the ids
+ * come from elsewhere (a near-tie token the other side resolved differently).
+ */
+int oracle_gates_for_ids(int T, int E, int k, const double *probs, const int32_t *ids,
+                         int renormalize, double *gates) {
+    for (int t = 0; t < T; ++t) {
+        double gsum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            if (e < 0 || e >= E) return -1;
+            gates[(size_t)t * k + j] = probs[(size_t)t * E + e];
+            gsum += gates[(size_t)t * k + j];
+        }
+        if (renormalize)
+            for (int j = 0; j < k; ++j) gates[(size_t)t * k + j] /= gsum;
+    }
+    return 0;
+}
+
+/*
+ * Grouping by expert.  [Handbook] "Implementation": flatten the (token, slot)
+ * pairs in the order t*k + j, sort them by expert with a STABLE sort, count
+ * each expert's entries and give each expert a running start (the prefix sum
+ * of the counts).  A stable sort keeps entries of one expert in flat order, so
+ * an entry's rank inside its expert is the number of earlier entries (in flat
+ * order) with the same expert -- which is what the single forward pass below
+ * counts.
+ * Capacity ([MoE-Notes] capacity and dropping; [MoE-Arch] "Tokens routed to a
+ * full expert are dropped"): capacity < 0 means unlimited; otherwise an entry
+ * whose rank is >= capacity is dropped.  Dropped entries get no position.
+ * Outputs:
+ *   counts[e]  entries routed to e (before the capacity cut)
+ *   kept[e]    min(counts[e], capacity)
+ *   offsets[E+1] exclusive running sum of kept
+ *   rank[t*k+j]  rank inside its expert
+ *   slot_pos[t*k+j] offsets[e] + rank when kept, else -1
+ *   sorted_token_ids[pos] = t for every kept entry; positions past offsets[E]
+ *                   are set to -1
+ *   n_dropped  sum(counts) - sum(kept)
+ * Pinned: brute force over tiny inputs, count/offset invariants, naive == grouped.
+ */
+int oracle_group(int T, int E, int k, int capacity, const int32_t *ids, int32_t *counts,
+                 int32_t *kept, int32_t *offsets, int32_t *rank, int32_t *slot_pos,
+                 int32_t *sorted_token_ids, int32_t *n_dropped) {
+    size_t n = (size_t)T * (size_t)k;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (size_t i = 0; i < n; ++i) {
+        int e = ids[i];
+        if (e < 0 || e >= E) return -1;
+        rank[i] = counts[e];
+        counts[e] += 1;
+    }
+    int32_t total = 0;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        kept[e] = (capacity >= 0 && counts[e] > capacity) ? capacity : counts[e];
+        total += kept[e];
+        offsets[e + 1] = offsets[e] + kept[e];
+    }
+    *n_dropped = (int32_t)n - total;
+    for (size_t i = 0; i < n; ++i) sorted_token_ids[i] = -1;
+    for (size_t i = 0; i < n; ++i) {
+        int e = ids[i];
+        if (capacity >= 0 && rank[i] >= capacity) {
+            slot_pos[i] = -1;
+        } else {
+            int32_t pos = offsets[e] + rank[i];
+            slot_pos[i] = pos;
+            sorted_token_ids[pos] = (int32_t)(i / (size_t)k);
+        }
+    }
+    return 0;
+}
+
+/*
+ * One SwiGLU expert on one token, [Handbook] Structure / Expert.forward and
+ * [MoE-Arch] "Each expert is a standard SwiGLU FFN":
+ *   out = W2 ( silu(W1 x) (.) W3 x ),  silu(z) = z / (1 + e^{-z})
+ * W1 (gate_proj) and W3 (up_proj) are stored [F][d], W2 (down_proj) [d][F]
+ * (the nn.Linear [out][in] layout), each at element offset `base`.
+ * h is a caller-provided scratch row of F doubles.
+ */
+static void swiglu_expert(int d, int F, int dtype, const void *w1, const void *w3, const void *w2,
+                          size_t base1, size_t base2, const double *xt, double *h, double *out) {
+    for (int f = 0; f < F; ++f) {
+        double a = 0.0, b = 0.0;
+        for (int i = 0; i < d; ++i) {
+            a += elem(w1, dtype, base1 + (size_t)f * d + i) * xt[i];
+            b += elem(w3, dtype, base1 + (size_t)f * d + i) * xt[i];
+        }
+        h[f] = a / (1.0 + exp(-a)) * b;
+    }
+    for (int o = 0; o < d; ++o) {
+        double acc = 0.0;
+        for (int f = 0; f < F; ++f) acc += elem(w2, dtype, base2 + (size_t)o * F + f) * h[f];
+        out[o] = acc;
+    }
+}
+
+/*
+ * Layer output for the tokens listed in `tokens` (n_tok of them), in the naive
+ * per-token form of [Handbook] "Implementation" (outer loop over tokens, inner
+ * over the k chosen experts) and [DeepDive] Code Implementation Essentials 3+5:
+ *   y_t = sum_{j : slot_pos[t,j] >= 0} g_{t,j} Expert_{ids[t,j]}(x_t)
+ *         + sum over shared experts of Shared(x_t)          ([MoE-Arch] s3)
+ * A dropped entry (slot_pos < 0) contributes nothing ([MoE-Arch] "they
+ * contribute nothing to the forward pass"); the other gates are not
+ * renormalised again.  slot_pos may be NULL (nothing dropped).
+ * Expert e's W1/W3 start at element e*F*d, its W2 at e*d*F.  The shared
+ * expert (n_shared 0 or 1) has its own hidden size F_s.
+ * y is [n_tok][d].
+ */
+int oracle_layer_tokens(int T, int d, int E, int k, int F, int n_shared, int F_s, int dtype,
+                        const void *x, const void *w1, const void *w3, const void *w2,
+                        const void *ws1, const void *ws3, const void *ws2, const int32_t *ids,
+                        const double *gates, const int32_t *slot_pos, const int32_t *tokens,
+                        int n_tok, double *y) {
+    if (n_shared < 0 || n_shared > 1) return -1;
+    int bad = 0;
+    int Fmax = F > F_s ? F : F_s;
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)d);
+        double *h = (double *)malloc(sizeof(double) * (size_t)(Fmax > 0 ? Fmax : 1));
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+        int ok = xt && h && o;
+#pragma omp for schedule(dynamic, 1)
+        for (int n = 0; n < n_tok; ++n) {
+            int t = tokens ? tokens[n] : n;
+            double *yt = y + (size_t)n * d;
+            if (!ok || t < 0 || t >= T) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            for (int i = 0; i < d; ++i) {
+                xt[i] = elem(x, dtype, (size_t)t * d + i);
+                yt[i] = 0.0;
+            }
+            for (int j = 0; j < k; ++j) {
+                size_t fi = (size_t)t * k + j;
+                if (slot_pos && slot_pos[fi] < 0) continue;
+                int e = ids[fi];
+                if (e < 0 || e >= E) continue;
+                swiglu_expert(d, F, dtype, w1, w3, w2, (size_t)e * F * d, (size_t)e * d * F, xt, h, o);
+                for (int i = 0; i < d; ++i) yt[i] += gates[fi] * o[i];
+            }
+            if (n_shared == 1) {
+                swiglu_expert(d, F_s, dtype, ws1, ws3, ws2, 0, 0, xt, h, o);
+                for (int i = 0; i < d; ++i) yt[i] += o[i];
+            }
+        }
+        free(xt);
+        free(h);
+        free(o);
+    }
+    return bad ? -2 : 0;
+}
+
+/*
+ * Load statistics.  [MoE-Arch] Load Balancing: L = alpha * E * sum_i f_i p_i,
+ * f_i the fraction of routing decisions sent to expert i, p_i the mean router
+ * probability of expert i.  [Handbook] Load balancing / aux_loss: f is the
+ * per-expert count over the number of (token, slot) decisions T*k, P is the
+ * mean over tokens of the softmax row.  f counts decisions before any capacity
+ * cut.  probs is [T][E] (the unbiased softmax, logit_bias included).
+ * Pinned: closed forms (uniform p or uniform f give alpha; the handbook's
+ * skewed example gives 4 with alpha = 1), random router near 1.
+ */
+int oracle_load_stats(int T, int E, int k, const int32_t *counts, const double *probs,
+                      double alpha, double *f, double *p, double *L) {
+    double acc = 0.0;
+    for (int e = 0; e < E; ++e) {
+        f[e] = (double)counts[e] / ((double)T * (double)k);
+        double s = 0.0;
+        for (int t = 0; t < T; ++t) s += probs[(size_t)t * E + e];
+        p[e] = s / (double)T;
+        acc += f[e] * p[e];
+    }
+    *L = alpha * (double)E * acc;
+    return 0;
+}
