@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE SwiGLU layer forward on B300 GPUs; prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full layer call (router, top-k, grouping, both grouped expert
+GEMMs, combine, load statistics) over one batch of synthetic tokens whose
+inputs are resident in HBM.  N > 1 runs under torchrun as N independent
+replicas (one per GPU, weak scaling): the layer's token batch has no exchange
+step on one GPU, so the only collectives are the harness's barrier and the
+max-over-ranks of the timed region.
+
+`value` is whole-job tokens/s.  `roofline` describes the dominant kernel (the
+up-projection grouped GEMM with the fused SwiGLU), timed live with the
+library's per-stage CUDA events inside the timed region.  `e2e` repeats the
+measurement through the public Python API with the token batch copied from
+pinned host memory each step and the output copied back.  `cpu_baseline`
+times the fp64 CPU oracle on a bounded sample of the same workload.
+
+--impl reference times that oracle (the only reference implementation this
+method has) on the same workload, a bounded token sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 B300; % of bf16 tensor peak or HBM roofline"
+UNIT = "tokens/s"
+FALLBACK = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0)
+TC_SOURCE = os.path.join(ROOT, "mixture_experts_layer_95_b300", "csrc", "gemm_tc.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral_prefill")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))), "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def source_hash(path=TC_SOURCE):
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the up GEMM from a committed ncu summary, or None
+    when the summary is missing or was taken on a different kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as fh:
+        d = json.load(fh)
+    e = d.get(workload)
+    if not e or e.get("source_sha256_16") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.window = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.monotonic(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        t0, t1 = self.window or (0, float("inf"))
+        inside = [p for t, p in self.samples if t0 - 0.06 <= t <= t1 + 0.06]
+        use = inside or [min(self.samples, key=lambda s: abs(s[0] - t1))[1]]
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in use if num(p[0]) is not None]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for p in use:
+            for name, v in zip(names, p[3:7]):
+                if v.strip().lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(use[0][1]),
+                "reasons": sorted(reasons), "samples": len(inside), "power_w_max": max(
+                    (num(p[2]) for p in use if num(p[2]) is not None), default=None)}
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def time_oracle(w, Ln, budget_s, n_tokens=None):
+    """Times the fp64 oracle on the full routing + grouping and the expert
+    FFNs of a token sample; returns (tokens/s extrapolated to T, info)."""
+    import numpy as np
+
+    import oracle
+    threads = oracle.num_threads()
+    t0 = time.perf_counter()
+    r = oracle.route(Ln["x"], Ln["w_gate"], w.k, Ln["logit_bias"], Ln["select_bias"], w.renormalize)
+    g = oracle.group(r["ids"], w.E, w.capacity)
+    t_rg = time.perf_counter() - t0
+    shared = (Ln["ws1"], Ln["ws3"], Ln["ws2"]) if w.n_shared else None
+    if n_tokens is None:
+        # calibrate on one token per thread, then size the sample to the budget
+        n0 = min(w.T, threads)
+        t1 = time.perf_counter()
+        oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], r["ids"], r["gates"], g["slot_pos"],
+                            np.arange(n0, dtype=np.int32), shared)
+        per_round = time.perf_counter() - t1
+        rounds = max(1, int(budget_s / max(per_round, 1e-6)))
+        n_tokens = min(w.T, n0 * rounds)
+    toks = np.arange(n_tokens, dtype=np.int32)
+    t2 = time.perf_counter()
+    oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], r["ids"], r["gates"], g["slot_pos"], toks, shared)
+    t_ffn = time.perf_counter() - t2
+    total = t_rg + t_ffn * (w.T / n_tokens)
+    info = dict(cores=threads, n_tokens=int(n_tokens), t_route_group_s=round(t_rg, 3), t_ffn_s=round(t_ffn, 3))
+    return w.T / total, info
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------------ our arm
+
+def layer_of(w):
+    import mixture_experts_layer_95_b300 as moe
+    return moe.Layer(T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.F, n_shared=w.n_shared, d_ff_shared=w.F_s, dtype=w.dtype,
+                     renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    from mixture_experts_layer_95_b300 import _build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    w = moe_inputs.WORKLOADS[args.workload]
+    layer = layer_of(w)
+    L = moe_inputs.make_layer(w, dev)
+    fw = moe.Forward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
+                     L["ws3"], L["ws2"], stats=True, device=dev)
+    x = L["x"]
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        fw(x, y)
+    torch.cuda.synchronize(dev)
+    st = fw.device_status()
+    if st != 0:
+        raise moe.MoeError(st, "warm-up device status")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    try:  # nvidia-smi numbers GPUs physically; the UUID names ours regardless of CUDA_VISIBLE_DEVICES
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
+    except Exception:
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.15)
+    barrier()
+    launches0 = moe.launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.monotonic()
+    with moe.StageTimer() as timer:
+        start.record(stream)
+        for _ in range(args.steps):
+            timer.begin_call()
+            fw(x, y)
+        end.record(stream)
+    end.synchronize()
+    wall1 = time.monotonic()
+    barrier()
+    clocks.mark(wall0, wall1)
+    clocks.stop()
+    launches = moe.launch_count() - launches0
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st = fw.device_status()
+    if st != 0:
+        raise moe.MoeError(st, "timed-region device status")
+    stage_ms, stage_n = timer.ms()
+    kept_total = int(fw.stats["kept"].sum().item())
+    n_dropped = int(fw.stats["n_dropped"].item())
+    touched = int((fw.stats["counts"] > 0).sum().item())
+
+    ms_per_step = ms / args.steps
+    value = world * w.T * args.steps / (ms / 1e3)
+
+    # roofline of the dominant kernel (up GEMM + fused SwiGLU)
+    peaks, peak_src = load_peaks()
+    up_flops = 2.0 * kept_total * w.d * 2 * w.F + 2.0 * w.T * w.d * 2 * w.F_s * w.n_shared
+    down_flops = 2.0 * kept_total * w.d * w.F + 2.0 * w.T * w.d * w.F_s * w.n_shared
+    per = {s: (stage_ms[s] / stage_n[s] if stage_n[s] else None) for s in moe.STAGES}
+    up_ms = per["up_gemm"]
+    layer_flops = moe_inputs.algorithmic_flops(w, kept_total)
+    wbytes = moe_inputs.expert_weight_bytes(w, touched)
+    tensor_bound = w.T * w.k >= 512  # below that the GEMMs stream weights from HBM
+    if tensor_bound:
+        achieved = up_flops / (up_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": recorded_traffic(args.workload),
+                "kernel": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)", "peak_source": f"{peak_src} bf16 burst",
+                "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4)}
+    else:
+        up_bytes = wbytes * 2.0 / 3.0
+        achieved = up_bytes / (up_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": recorded_traffic(args.workload),
+                "kernel": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)", "peak_source": f"{peak_src} HBM copy",
+                "algorithmic_bytes_per_launch": up_bytes, "launch_ms": round(up_ms, 4)}
+
+    # end to end through the public API: host batch in, host result out
+    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_h.copy_(x)
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    for _ in range(2):
+        x_dev.copy_(x_h, non_blocking=True)
+        fw(x_dev, y)
+        y_h.copy_(y, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_h, non_blocking=True)
+        fw(x_dev, y)
+        y_h.copy_(y, non_blocking=True)
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(world * w.T * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
+           "d2h_bytes_per_step": y_h.numel() * y_h.element_size()}
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded, N(0,1) tokens, N(0,1/fan_in) weights)",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F, "n_shared": w.n_shared,
+                   "d_ff_shared": w.F_s, "capacity": w.capacity, "parallelism": f"replicas x{world}",
+                   "l2": "working set larger than L2 (expert weights %.2f GB)" % (wbytes / 1e9)},
+        "roofline": roof,
+        "layer": {"algorithmic_tflop_per_step": round(layer_flops / 1e12, 4),
+                  "tflops": round(layer_flops / (ms_per_step / 1e3) / 1e12, 1),
+                  "frac_bf16_peak": round(layer_flops / (ms_per_step / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                  "expert_weight_gbs": round(wbytes / (ms_per_step / 1e3) / 1e9, 1),
+                  "frac_hbm": round(wbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                  "stage_ms": {s: (round(v, 4) if v is not None else None) for s, v in per.items()},
+                  "kept_entries": kept_total, "dropped_entries": n_dropped, "experts_touched": touched},
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        Ln = moe_inputs.layer_numpy(L)
+        tps, info = time_oracle(w, Ln, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(tps, 3), "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+                               "sample": f"full routing+grouping of {w.T} tokens, expert FFNs of the first "
+                                         f"{info['n_tokens']} tokens, extrapolated to {w.T}",
+                               "cpu": cpu_model(), **{k: v for k, v in info.items() if k != "cores"}}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The fp64 CPU oracle as the reference implementation, rank 0 only."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    import moe_inputs
+    w = moe_inputs.WORKLOADS[args.workload]
+    L = moe_inputs.make_layer(w, "cuda" if torch.cuda.is_available() else "cpu")
+    Ln = moe_inputs.layer_numpy(L)
+    del L
+    # size each step to a few seconds so the whole run stays within minutes
+    _, cal = time_oracle(w, Ln, budget_s=0.0)
+    per_token = cal["t_ffn_s"] / max(cal["n_tokens"], 1)
+    n_tokens = max(cal["n_tokens"], min(w.T, int(4.0 / max(per_token, 1e-9))))
+    for _ in range(args.warmup):
+        time_oracle(w, Ln, 0.0, n_tokens=min(n_tokens, cal["n_tokens"]))
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, info = time_oracle(w, Ln, 0.0, n_tokens=n_tokens)
+        vals.append(v)
+    elapsed = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    sample = (f"per step: full routing+grouping of {w.T} tokens, expert FFNs of {n_tokens} tokens, "
+              f"extrapolated to {w.T}")
+    out = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(1e3 * elapsed / args.steps, 1), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F,
+                      "n_shared": w.n_shared, "capacity": w.capacity},
+           "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+                            "sample": sample, "cpu": cpu_model()},
+           "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+/*
+ * moe_b300.h -- C ABI of libmoe_b300.so: the forward pass of a Mixture-of-Experts
+ * SwiGLU FFN layer on one NVIDIA B300 (sm_103a).
+ *
+ * What the layer computes (sources by page title and section):
+ *   1. router logits  l = W_g x (+ logit_bias)      "Mixture of Experts" notes, How it works
+ *                                                    (g(x) = softmax(W_g x), W_g in R^{E x d});
+ *                                                    "MoE Architecture" s2 Gating Function
+ *   2. p = softmax(l)                                same; "One Deep Concept #04" s4
+ *   3. top-k of l + select_bias, gates g_j = p[id_j] "Mixture of experts (MoE)" handbook,
+ *      renormalised to sum 1 (optional)             Structure and Load balancing (bias used
+ *                                                    only for the choice); "MoE Deep Dive",
+ *                                                    Weighted Sum Output (divide by the sum)
+ *   4. grouping by expert: counts, stable ranks,    handbook, "Implementation: token by token
+ *      capacity cut, offsets, permutation           vs. grouped by expert" (stable argsort,
+ *                                                    bincount, running start); notes,
+ *                                                    capacity and token dropping
+ *   5. per expert segment: H = silu(X W1^T) * (X W3^T), Y = H W2^T   handbook Structure
+ *                                                    (Expert: down(silu(gate(x)) * up(x)));
+ *                                                    "MoE Architecture" s3 (SwiGLU experts)
+ *   6. y_t = sum_j g_j Y[pos(t,j)] + Shared(x_t)     handbook forward_grouped / forward_naive;
+ *                                                    "MoE Architecture" s3 Shared Experts
+ *   7. f_i = counts_i/(T k), p_i = mean_t p[t,i],   "MoE Architecture" s2 Load Balancing;
+ *      L_balance = alpha E sum_i f_i p_i             handbook Load balancing (aux_loss)
+ *
+ * Conventions for every entry point
+ *   - Every pointer argument except `cfg` and `stats` (a host struct of device
+ *     pointers) is a DEVICE pointer unless stated otherwise.  The caller owns all
+ *     memory; the library never allocates, frees or keeps a pointer past the call.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and the call returns without synchronising.  Results are valid
+ *     once the stream has reached that point.
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  Argument errors
+ *     are detected on the host before anything is enqueued.  MOE_ERR_CUDA
+ *     reports a launch failure (cudaGetLastError after the launches).
+ *     Failures found by a kernel (a bounded wait that ran out, an index out of
+ *     range) are recorded in the workspace's status word and are read with
+ *     moe_last_device_status after the stream is synchronised.
+ *   - Layouts are row-major.  x is [T][d]; W_g is [E][d] (one row per expert,
+ *     the notes' W_g in R^{E x d}, i.e. an nn.Linear(d, E) weight);
+ *     W1 (gate_proj) and W3 (up_proj) are [E][F][d]; W2 (down_proj) is
+ *     [E][d][F]; the shared expert's Ws1/Ws3 are [F_s][d] and Ws2 is [d][F_s].
+ *   - dtype MOE_BF16: x, weights and y are bf16; accumulation is fp32; the
+ *     hidden activation H is stored as bf16 between the two expert GEMMs.
+ *     dtype MOE_F32: everything is fp32 (IEEE fp32 FMA, no TF32).
+ *   - Alignment: every device pointer must be 16-byte aligned and the
+ *     workspace 256-byte aligned; d, F and F_s must be multiples of 8.
+ *   - Limits: 1 <= k <= min(E, 32); E <= 1024; T >= 0 (T = 0 enqueues
+ *     nothing); T * k < 2^31; n_shared is 0 or 1; d, F, F_s >= 8.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st *moe_stream_t;
+
+enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_NULL = -1,          /* a required pointer is NULL                          */
+    MOE_ERR_SHAPE = -2,         /* sizes out of range or misaligned (see Limits)       */
+    MOE_ERR_DTYPE = -3,         /* unknown dtype                                       */
+    MOE_ERR_WORKSPACE = -4,     /* ws_bytes < moe_workspace_size(cfg) or ws misaligned */
+    MOE_ERR_CUDA = -5,          /* a kernel launch or CUDA runtime call failed         */
+    MOE_ERR_DEVICE = -6,        /* current device is not a compute-capability 10.3 GPU */
+    MOE_ERR_TIMEOUT = -7,       /* device: a bounded wait ran out (kernel gave up)     */
+    MOE_ERR_DEVICE_BOUNDS = -8, /* device: an index read from memory was out of range  */
+    MOE_ERR_ALIGN = -9          /* a device pointer is not 16-byte aligned             */
+};
+
+/* Layer description.  T tokens, model width d, E routed experts, top-k, expert
+ * hidden size d_ff (F); n_shared (0 or 1) always-on shared experts of hidden
+ * size d_ff_shared (F_s).  capacity < 0: no limit; otherwise each expert keeps
+ * at most `capacity` (token, slot) entries, the ones with the lowest token
+ * index, and drops the rest (a dropped entry contributes nothing; the other
+ * gates are not renormalised again).  alpha scales L_balance. */
+typedef struct moe_config {
+    int32_t T, d, E, k, d_ff;
+    int32_t n_shared, d_ff_shared;
+    int32_t dtype;       /* enum moe_dtype                                     */
+    int32_t renormalize; /* 1: divide the k gates of a token by their sum     */
+    int32_t capacity;    /* < 0: unlimited                                     */
+    float alpha;         /* L_balance = alpha * E * sum_i f_i p_i              */
+} moe_config;
+
+/* Optional statistics outputs of moe_forward (device pointers, each nullable). */
+typedef struct moe_stats {
+    int32_t *counts;    /* [E]  routing decisions per expert, before the capacity cut */
+    int32_t *kept;      /* [E]  min(counts, capacity)                                */
+    float *f;           /* [E]  counts / (T k)                                       */
+    float *p;           /* [E]  mean over tokens of the softmax row                  */
+    float *L;           /* [1]  alpha * E * sum f p                                  */
+    int32_t *n_dropped; /* [1]  T k - sum kept                                       */
+} moe_stats;
+
+/* Bytes of device workspace every entry point below may use for `cfg`.
+ * Returns 0 when cfg is invalid.  The workspace needs 256-byte alignment. */
+MOE_API size_t moe_workspace_size(const moe_config *cfg);
+
+/* Prepares a freshly allocated workspace: zeroes its device status word
+ * (enqueued on `stream`).  Call once per workspace before the first entry
+ * point; moe_last_device_status clears the word again after reading it.
+ * Errors: MOE_ERR_NULL, MOE_ERR_WORKSPACE, MOE_ERR_CUDA. */
+MOE_API int moe_workspace_init(const moe_config *cfg, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Router, softmax and top-k (steps 1-3).
+ *   x [T][d], w_gate [E][d] (dtype), logit_bias [E] fp32 or NULL (added to the
+ *   logits everywhere: selection, gates and p), select_bias [E] fp32 or NULL
+ *   (added to the logits for the top-k choice only).
+ *   Outputs: topk_ids int32 [T][k] (descending selection score, ties to the lower
+ *   expert index), gates fp32 [T][k] (unbiased softmax at those ids, renormalised
+ *   when cfg->renormalize), p_mean fp32 [E] or NULL (mean softmax row). */
+MOE_API int moe_route(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
+              const float *select_bias, int32_t *topk_ids, float *gates, float *p_mean, void *ws,
+              size_t ws_bytes, moe_stream_t stream);
+
+/* Grouping by expert (step 4).  Entries are the (t, j) pairs in flat order
+ * t*k + j; an entry's rank is the number of earlier entries of the same expert.
+ *   In:  topk_ids int32 [T][k], gates fp32 [T][k], x [T][d] (dtype).
+ *   Out: counts [E], kept [E], offsets [E+1] (exclusive running sum of kept),
+ *        sorted_token_ids [T*k] (token of the entry at each position; positions
+ *        >= offsets[E] are set to -1), slot_pos [T][k] (position of the entry,
+ *        -1 if dropped), gates_perm fp32 [T*k] (gate at each position, 0 past the
+ *        end), x_perm [T*k][d] (dtype; row pos = x[sorted_token_ids[pos]];
+ *        rows past offsets[E] are left untouched), n_dropped [1].
+ * All outputs are required (non-NULL). */
+MOE_API int moe_permute(const moe_config *cfg, const int32_t *topk_ids, const float *gates, const void *x,
+                int32_t *counts, int32_t *kept, int32_t *offsets, int32_t *sorted_token_ids,
+                int32_t *slot_pos, float *gates_perm, void *x_perm, int32_t *n_dropped, void *ws,
+                size_t ws_bytes, moe_stream_t stream);
+
+/* Expert FFNs over the grouped rows (step 5), gate applied in the epilogue.
+ *   x_perm [T*k][d] and offsets [E+1] as produced by moe_permute; gates_perm fp32
+ *   [T*k]; w1, w3 [E][F][d], w2 [E][d][F] (dtype).
+ *   y_perm fp32 [T*k][d]: row pos = gates_perm[pos] * W2_e(silu(W1_e x) * W3_e x)
+ *   for pos < offsets[E] (rows past the end are left untouched).
+ *   Shared expert (when cfg->n_shared == 1): x [T][d], ws1, ws3 [F_s][d],
+ *   ws2 [d][F_s] and y_shared fp32 [T][d] = Shared(x) (gate 1) are required;
+ *   when n_shared == 0 those five may be NULL. */
+MOE_API int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets,
+                   const float *gates_perm, const void *w1, const void *w3, const void *w2,
+                   const void *x, const void *ws1, const void *ws3, const void *ws2, float *y_perm,
+                   float *y_shared, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Combine (step 6): y[t] = sum over j = 0..k-1 with slot_pos[t][j] >= 0 of
+ * y_perm[slot_pos[t][j]], in that order, plus y_shared[t] when y_shared is
+ * non-NULL; accumulated in fp32 and stored in cfg->dtype.  A token whose
+ * entries were all dropped gets only its shared row (or 0). */
+MOE_API int moe_combine(const moe_config *cfg, const float *y_perm, const int32_t *slot_pos,
+                const float *y_shared, void *y, moe_stream_t stream);
+
+/* Load statistics (step 7) from counts [E] (moe_permute) and p_mean [E]
+ * (moe_route): f [E] = counts/(T k), L [1] = alpha * E * sum f p_mean.
+ * f or L may be NULL. */
+MOE_API int moe_load_stats(const moe_config *cfg, const int32_t *counts, const float *p_mean, float *f,
+                   float *L, moe_stream_t stream);
+
+/* The whole layer (steps 1-7) in one call, fused where the steps allow.
+ *   y [T][d] (dtype) receives the layer output; stats (host struct, nullable)
+ *   names optional device outputs.  ws1/ws3/ws2 are the shared expert's weights
+ *   (required iff cfg->n_shared == 1). */
+MOE_API int moe_forward(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
+                const float *select_bias, const void *w1, const void *w3, const void *w2,
+                const void *ws1, const void *ws3, const void *ws2, void *y, const moe_stats *stats,
+                void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Reads (and clears) the device status word kept in the workspace: MOE_OK,
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  Synchronises `stream` first.
+ * Returns MOE_ERR_CUDA if the copy itself fails. */
+MOE_API int moe_last_device_status(const moe_config *cfg, void *ws, moe_stream_t stream);
+
+/* ---- diagnostics ---------------------------------------------------------
+ * Stage timing hook.  While set (per host thread), every entry point records
+ * events[2*s] on its stream just before the launches of stage s and
+ * events[2*s+1] just after them, for s = 0 router (logits, softmax, top-k),
+ * 1 grouping scan (ranks, offsets, permutation; includes the histogram
+ * kernel of moe_permute), 2 row gather (x_perm), 3 up GEMM (SwiGLU), 4 down
+ * GEMM, 5 combine.  `events` holds n (<= 12) cudaEvent_t handles owned by
+ * the caller; NULL entries are skipped.  Pass events = NULL to clear.
+ * Returns MOE_OK, or MOE_ERR_SHAPE if n is out of range. */
+MOE_API int moe_set_stage_events(void *const *events, int n);
+
+/* Number of kernels this library has launched in this process so far. */
+MOE_API uint64_t moe_launch_count(void);
+
+/* Static text for a status code (never NULL). */
+MOE_API const char *moe_strerror(int status);
+
+/* Library version as "major.minor.patch". */
+MOE_API const char *moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

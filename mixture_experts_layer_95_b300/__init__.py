@@ -1,0 +1,370 @@
+"""Python binding of libmoe_b300.so -- the MoE SwiGLU layer forward on a B300.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch supplies device memory (tensors) and streams; the functions
+below check shapes/dtypes, allocate outputs with ``torch.empty`` and pass raw
+pointers through ctypes to the C entry points of ``include/moe_b300.h`` of the
+same names.  There is no CPU path: if the shared library is missing, importing
+succeeds but every call raises ``MoeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+MOE_F32, MOE_BF16 = 0, 1
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTYPE", -4: "MOE_ERR_WORKSPACE",
+          -5: "MOE_ERR_CUDA", -6: "MOE_ERR_DEVICE", -7: "MOE_ERR_TIMEOUT", -8: "MOE_ERR_DEVICE_BOUNDS",
+          -9: "MOE_ERR_ALIGN"}
+
+EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
+            "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
+            "moe_version", "moe_set_stage_events", "moe_launch_count")
+STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({strerror(code) if _lib else ''})")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("capacity", ctypes.c_int32),
+                ("alpha", ctypes.c_float)]
+
+
+class MoeStats(ctypes.Structure):
+    _fields_ = [("counts", ctypes.c_void_p), ("kept", ctypes.c_void_p), ("f", ctypes.c_void_p),
+                ("p", ctypes.c_void_p), ("L", ctypes.c_void_p), ("n_dropped", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded shared library; raises MoeError if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MoeError(-5, f"{LIB_PATH} is missing; build it with `python -m mixture_experts_layer_95_b300._build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        cfgp = ctypes.POINTER(MoeConfig)
+        L.moe_workspace_size.argtypes = [cfgp]
+        L.moe_workspace_size.restype = sz
+        L.moe_workspace_init.argtypes = [cfgp, vp, sz, vp]
+        L.moe_route.argtypes = [cfgp] + [vp] * 7 + [vp, sz, vp]
+        L.moe_permute.argtypes = [cfgp] + [vp] * 11 + [vp, sz, vp]
+        L.moe_expert_ffn.argtypes = [cfgp] + [vp] * 12 + [vp, sz, vp]
+        L.moe_combine.argtypes = [cfgp] + [vp] * 4 + [vp]
+        L.moe_load_stats.argtypes = [cfgp] + [vp] * 4 + [vp]
+        L.moe_forward.argtypes = [cfgp] + [vp] * 10 + [vp, ctypes.POINTER(MoeStats), vp, sz, vp]
+        L.moe_last_device_status.argtypes = [cfgp, vp, vp]
+        L.moe_strerror.argtypes = [i32]
+        L.moe_strerror.restype = ctypes.c_char_p
+        L.moe_version.restype = ctypes.c_char_p
+        L.moe_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+        L.moe_set_stage_events.restype = i32
+        L.moe_launch_count.restype = ctypes.c_uint64
+        for f in ("moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+                  "moe_load_stats", "moe_forward", "moe_last_device_status"):
+            getattr(L, f).restype = i32
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().moe_strerror(int(code)).decode()
+
+
+def version() -> str:
+    return lib().moe_version().decode()
+
+
+def launch_count() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(lib().moe_launch_count())
+
+
+class StageTimer:
+    """Per-stage CUDA-event timing of the library's launches (diagnostics).
+
+    ``with StageTimer() as st: ...`` makes every library call inside the block
+    record a start/stop event pair around each stage's launches; ``st.ms()``
+    returns the summed milliseconds per stage over all calls made inside the
+    block.  Events are recorded on the stream each call runs on.
+    """
+
+    def __init__(self):
+        self._pairs = []
+
+    def begin_call(self):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(STAGES))]
+        self._pairs.append(ev)
+        arr = (ctypes.c_void_p * len(ev))(*[e.cuda_event for e in ev])
+        self._arr = arr  # keep alive while set
+        _check(lib().moe_set_stage_events(arr, len(ev)), "moe_set_stage_events")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        lib().moe_set_stage_events(None, 0)
+        return False
+
+    def ms(self):
+        torch.cuda.synchronize()
+        out = {s: 0.0 for s in STAGES}
+        counts = {s: 0 for s in STAGES}
+        for ev in self._pairs:
+            for i, s in enumerate(STAGES):
+                a, b = ev[2 * i], ev[2 * i + 1]
+                if a.query() and b.query():
+                    try:
+                        out[s] += a.elapsed_time(b)
+                        counts[s] += 1
+                    except RuntimeError:  # stage not recorded in this call
+                        pass
+        return out, counts
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise MoeError(rc, what)
+
+
+@dataclass
+class Layer:
+    """Static description of a layer (sizes and routing options)."""
+    T: int
+    d: int
+    E: int
+    k: int
+    d_ff: int
+    n_shared: int = 0
+    d_ff_shared: int = 0
+    dtype: str = "bf16"
+    renormalize: bool = True
+    capacity: int = -1
+    alpha: float = 0.01
+
+    def cfg(self) -> MoeConfig:
+        return MoeConfig(self.T, self.d, self.E, self.k, self.d_ff, self.n_shared, self.d_ff_shared,
+                         MOE_BF16 if self.dtype == "bf16" else MOE_F32, int(bool(self.renormalize)),
+                         int(self.capacity), float(self.alpha))
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, shape, dtype, name):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{name}: expected {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+    return t
+
+
+def workspace_size(layer: Layer) -> int:
+    c = layer.cfg()
+    n = lib().moe_workspace_size(ctypes.byref(c))
+    if n == 0:
+        raise MoeError(-2, "moe_workspace_size")
+    return int(n)
+
+
+def workspace(layer: Layer, device=None, stream=None) -> torch.Tensor:
+    """Allocates (with torch) and initialises a workspace for `layer`."""
+    ws = torch.empty(workspace_size(layer), dtype=torch.uint8, device=device or "cuda")
+    c = layer.cfg()
+    _check(lib().moe_workspace_init(ctypes.byref(c), _ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
+    return ws
+
+
+def last_device_status(layer: Layer, ws: torch.Tensor, stream=None) -> int:
+    c = layer.cfg()
+    return int(lib().moe_last_device_status(ctypes.byref(c), _ptr(ws), _stream(stream)))
+
+
+def route(layer: Layer, x, w_gate, logit_bias=None, select_bias=None, ws=None, stream=None):
+    """moe_route: returns (topk_ids int32 [T,k], gates fp32 [T,k], p_mean fp32 [E])."""
+    dt, dev = layer.torch_dtype, x.device
+    _need(x, (layer.T, layer.d), dt, "x")
+    _need(w_gate, (layer.E, layer.d), dt, "w_gate")
+    if logit_bias is not None:
+        _need(logit_bias, (layer.E,), torch.float32, "logit_bias")
+    if select_bias is not None:
+        _need(select_bias, (layer.E,), torch.float32, "select_bias")
+    ws = ws if ws is not None else workspace(layer, dev, stream)
+    ids = torch.empty((layer.T, layer.k), dtype=torch.int32, device=dev)
+    gates = torch.empty((layer.T, layer.k), dtype=torch.float32, device=dev)
+    p_mean = torch.empty((layer.E,), dtype=torch.float32, device=dev)
+    c = layer.cfg()
+    _check(lib().moe_route(ctypes.byref(c), _ptr(x), _ptr(w_gate), _ptr(logit_bias), _ptr(select_bias), _ptr(ids),
+                           _ptr(gates), _ptr(p_mean), _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
+    return ids, gates, p_mean
+
+
+def permute(layer: Layer, topk_ids, gates, x, ws=None, stream=None):
+    """moe_permute: returns a dict of the grouping outputs and x_perm."""
+    dev = x.device
+    n = layer.T * layer.k
+    _need(topk_ids, (layer.T, layer.k), torch.int32, "topk_ids")
+    _need(gates, (layer.T, layer.k), torch.float32, "gates")
+    _need(x, (layer.T, layer.d), layer.torch_dtype, "x")
+    ws = ws if ws is not None else workspace(layer, dev, stream)
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(counts=torch.empty(layer.E, **i32), kept=torch.empty(layer.E, **i32),
+               offsets=torch.empty(layer.E + 1, **i32), sorted_token_ids=torch.empty(n, **i32),
+               slot_pos=torch.empty((layer.T, layer.k), **i32),
+               gates_perm=torch.empty(n, dtype=torch.float32, device=dev),
+               x_perm=torch.empty((n, layer.d), dtype=layer.torch_dtype, device=dev),
+               n_dropped=torch.empty(1, **i32))
+    c = layer.cfg()
+    _check(lib().moe_permute(ctypes.byref(c), _ptr(topk_ids), _ptr(gates), _ptr(x), _ptr(out["counts"]),
+                             _ptr(out["kept"]), _ptr(out["offsets"]), _ptr(out["sorted_token_ids"]),
+                             _ptr(out["slot_pos"]), _ptr(out["gates_perm"]), _ptr(out["x_perm"]),
+                             _ptr(out["n_dropped"]), _ptr(ws), ws.numel(), _stream(stream)), "moe_permute")
+    return out
+
+
+def expert_ffn(layer: Layer, x_perm, offsets, gates_perm, w1, w3, w2, x=None, ws1=None, ws3=None, ws2=None,
+               ws=None, stream=None):
+    """moe_expert_ffn: returns (y_perm fp32 [T*k, d], y_shared fp32 [T, d] or None)."""
+    dt, dev = layer.torch_dtype, x_perm.device
+    n = layer.T * layer.k
+    _need(x_perm, (n, layer.d), dt, "x_perm")
+    _need(offsets, (layer.E + 1,), torch.int32, "offsets")
+    _need(gates_perm, (n,), torch.float32, "gates_perm")
+    _need(w1, (layer.E, layer.d_ff, layer.d), dt, "w1")
+    _need(w3, (layer.E, layer.d_ff, layer.d), dt, "w3")
+    _need(w2, (layer.E, layer.d, layer.d_ff), dt, "w2")
+    y_shared = None
+    if layer.n_shared:
+        _need(x, (layer.T, layer.d), dt, "x")
+        _need(ws1, (layer.d_ff_shared, layer.d), dt, "ws1")
+        _need(ws3, (layer.d_ff_shared, layer.d), dt, "ws3")
+        _need(ws2, (layer.d, layer.d_ff_shared), dt, "ws2")
+        y_shared = torch.empty((layer.T, layer.d), dtype=torch.float32, device=dev)
+    ws = ws if ws is not None else workspace(layer, dev, stream)
+    y_perm = torch.empty((n, layer.d), dtype=torch.float32, device=dev)
+    c = layer.cfg()
+    _check(lib().moe_expert_ffn(ctypes.byref(c), _ptr(x_perm), _ptr(offsets), _ptr(gates_perm), _ptr(w1), _ptr(w3),
+                                _ptr(w2), _ptr(x), _ptr(ws1), _ptr(ws3), _ptr(ws2), _ptr(y_perm), _ptr(y_shared),
+                                _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
+    return y_perm, y_shared
+
+
+def combine(layer: Layer, y_perm, slot_pos, y_shared=None, stream=None):
+    """moe_combine: returns y [T, d] in the layer dtype."""
+    dev = y_perm.device
+    _need(y_perm, (layer.T * layer.k, layer.d), torch.float32, "y_perm")
+    _need(slot_pos, (layer.T, layer.k), torch.int32, "slot_pos")
+    if y_shared is not None:
+        _need(y_shared, (layer.T, layer.d), torch.float32, "y_shared")
+    y = torch.empty((layer.T, layer.d), dtype=layer.torch_dtype, device=dev)
+    c = layer.cfg()
+    _check(lib().moe_combine(ctypes.byref(c), _ptr(y_perm), _ptr(slot_pos), _ptr(y_shared), _ptr(y),
+                             _stream(stream)), "moe_combine")
+    return y
+
+
+def load_stats(layer: Layer, counts, p_mean, stream=None):
+    """moe_load_stats: returns (f fp32 [E], L fp32 [1])."""
+    dev = counts.device
+    _need(counts, (layer.E,), torch.int32, "counts")
+    _need(p_mean, (layer.E,), torch.float32, "p_mean")
+    f = torch.empty(layer.E, dtype=torch.float32, device=dev)
+    L = torch.empty(1, dtype=torch.float32, device=dev)
+    c = layer.cfg()
+    _check(lib().moe_load_stats(ctypes.byref(c), _ptr(counts), _ptr(p_mean), _ptr(f), _ptr(L), _stream(stream)),
+           "moe_load_stats")
+    return f, L
+
+
+class Forward:
+    """Reusable moe_forward call: checks the weights once, owns the workspace,
+    and enqueues the whole layer per call (the form the benchmark times)."""
+
+    def __init__(self, layer: Layer, w_gate, w1, w3, w2, logit_bias=None, select_bias=None, ws1=None, ws3=None,
+                 ws2=None, stats: bool = False, device=None, stream=None):
+        dt = layer.torch_dtype
+        self.layer = layer
+        self.cfg = layer.cfg()
+        self.w = dict(w_gate=_need(w_gate, (layer.E, layer.d), dt, "w_gate"),
+                      w1=_need(w1, (layer.E, layer.d_ff, layer.d), dt, "w1"),
+                      w3=_need(w3, (layer.E, layer.d_ff, layer.d), dt, "w3"),
+                      w2=_need(w2, (layer.E, layer.d, layer.d_ff), dt, "w2"),
+                      logit_bias=logit_bias, select_bias=select_bias, ws1=ws1, ws3=ws3, ws2=ws2)
+        if logit_bias is not None:
+            _need(logit_bias, (layer.E,), torch.float32, "logit_bias")
+        if select_bias is not None:
+            _need(select_bias, (layer.E,), torch.float32, "select_bias")
+        if layer.n_shared:
+            _need(ws1, (layer.d_ff_shared, layer.d), dt, "ws1")
+            _need(ws3, (layer.d_ff_shared, layer.d), dt, "ws3")
+            _need(ws2, (layer.d, layer.d_ff_shared), dt, "ws2")
+        dev = device or w1.device
+        self.ws = workspace(layer, dev, stream)
+        self.stats = None
+        self._stats_struct = None
+        if stats:
+            E = layer.E
+            i32 = dict(dtype=torch.int32, device=dev)
+            f32 = dict(dtype=torch.float32, device=dev)
+            self.stats = dict(counts=torch.zeros(E, **i32), kept=torch.zeros(E, **i32), f=torch.zeros(E, **f32),
+                              p=torch.zeros(E, **f32), L=torch.zeros(1, **f32), n_dropped=torch.zeros(1, **i32))
+            s = self.stats
+            self._stats_struct = MoeStats(s["counts"].data_ptr(), s["kept"].data_ptr(), s["f"].data_ptr(),
+                                          s["p"].data_ptr(), s["L"].data_ptr(), s["n_dropped"].data_ptr())
+        self._args = [_ptr(self.w[n]) for n in ("w_gate", "logit_bias", "select_bias", "w1", "w3", "w2", "ws1",
+                                                "ws3", "ws2")]
+
+    def __call__(self, x, y=None, stream=None):
+        L = self.layer
+        _need(x, (L.T, L.d), L.torch_dtype, "x")
+        if y is None:
+            y = torch.empty((L.T, L.d), dtype=L.torch_dtype, device=x.device)
+        else:
+            _need(y, (L.T, L.d), L.torch_dtype, "y")
+        wg, lb, sb, w1, w3, w2, s1, s3, s2 = self._args
+        st = ctypes.byref(self._stats_struct) if self._stats_struct is not None else None
+        _check(lib().moe_forward(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(y), st,
+                                 _ptr(self.ws), self.ws.numel(), _stream(stream)), "moe_forward")
+        return y
+
+    def device_status(self, stream=None) -> int:
+        return last_device_status(self.layer, self.ws, stream)
+
+
+def forward(layer: Layer, x, w_gate, w1, w3, w2, logit_bias=None, select_bias=None, ws1=None, ws3=None, ws2=None,
+            stats: bool = False, stream=None):
+    """One moe_forward call; returns y (and the statistics dict when stats=True)."""
+    fw = Forward(layer, w_gate, w1, w3, w2, logit_bias, select_bias, ws1, ws3, ws2, stats=stats, device=x.device,
+                 stream=stream)
+    y = fw(x, stream=stream)
+    rc = fw.device_status(stream)
+    if rc != 0:
+        raise MoeError(rc, "moe_forward (device status)")
+    return (y, fw.stats) if stats else y

@@ -1,0 +1,487 @@
+// api.cu -- the C ABI of libmoe_b300.so (declared in include/moe_b300.h).
+//
+// Validates arguments on the host, carves the caller's workspace and enqueues
+// the kernels of each step on the caller's stream.  No call allocates device
+// memory, synchronises (except moe_last_device_status, which must) or keeps a
+// pointer after returning.
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxTopK = 32;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool use_gemm_router(const moe_config& c) { return c.E > kWarpRouterMaxE; }
+
+size_t esize(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
+
+// Byte offsets of every workspace region; `total` is the size.
+struct Layout {
+    size_t status, topk_ids, gates, p_part, block_hist, counts, kept, offsets, n_dropped, sorted, slot_pos,
+        gates_perm, p_mean, f, L, logits, x_perm, h, h_shared, y_perm, y_shared, total;
+};
+
+Layout layout(const moe_config& c) {
+    Layout l{};
+    const size_t n = (size_t)c.T * c.k;
+    const size_t nblk = ((size_t)c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+    const size_t E = (size_t)c.E;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes);
+        return at;
+    };
+    l.status = take(16);
+    l.topk_ids = take(4 * n);
+    l.gates = take(4 * n);
+    l.p_part = take(4 * nblk * E);
+    l.block_hist = take(4 * nblk * E);
+    l.counts = take(4 * E);
+    l.kept = take(4 * E);
+    l.offsets = take(4 * (E + 1));
+    l.n_dropped = take(4);
+    l.sorted = take(4 * n);
+    l.slot_pos = take(4 * n);
+    l.gates_perm = take(4 * n);
+    l.p_mean = take(4 * E);
+    l.f = take(4 * E);
+    l.L = take(4);
+    l.logits = take(use_gemm_router(c) ? 4 * (size_t)c.T * E : 0);
+    l.x_perm = take(n * c.d * esize(c));
+    l.h = take(n * c.d_ff * esize(c));
+    l.h_shared = take(c.n_shared ? (size_t)c.T * c.d_ff_shared * esize(c) : 0);
+    l.y_perm = take(4 * n * c.d);
+    l.y_shared = take(c.n_shared ? 4 * (size_t)c.T * c.d : 0);
+    l.total = off;
+    return l;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+    return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_config(const moe_config* c) {
+    if (!c) return MOE_ERR_NULL;
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_DTYPE;
+    if (c->T < 0 || c->d < 8 || c->E < 1 || c->E > kMaxExperts || c->k < 1 || c->k > c->E || c->k > kMaxTopK ||
+        c->d_ff < 8)
+        return MOE_ERR_SHAPE;
+    if ((long long)c->T * c->k >= (1LL << 31)) return MOE_ERR_SHAPE;
+    if (c->n_shared != 0 && c->n_shared != 1) return MOE_ERR_SHAPE;
+    if (c->n_shared == 1 && c->d_ff_shared < 8) return MOE_ERR_SHAPE;
+    if (c->d % 8 || c->d_ff % 8 || (c->n_shared && c->d_ff_shared % 8)) return MOE_ERR_SHAPE;
+    // the grouped GEMM tile list holds at most kMaxExperts row groups
+    return MOE_OK;
+}
+
+int check_ws(const moe_config* c, const void* ws, size_t ws_bytes) {
+    if (!ws) return MOE_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < layout(*c).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+// Device capability (10.3) and SM count, cached per ordinal.
+int device_sms(int* sms_out) {
+    static int cache_sms[64] = {0};
+    static int cache_ok[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 64 && cache_ok[dev]) {
+        *sms_out = cache_sms[dev];
+        return cache_ok[dev] > 0 ? MOE_OK : MOE_ERR_DEVICE;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const bool ok = (major == 10 && minor == 3);
+    if (dev < 64) {
+        cache_sms[dev] = sms;
+        cache_ok[dev] = ok ? 1 : -1;
+    }
+    *sms_out = sms;
+    return ok ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ---- diagnostics: stage events and launch count ----
+constexpr int kStageEvents = 12;
+thread_local cudaEvent_t g_stage_events[kStageEvents] = {};
+thread_local int g_stage_n = 0;
+std::atomic<uint64_t> g_launches{0};
+
+enum Stage { kStageRouter = 0, kStageScan = 1, kStageGather = 2, kStageUp = 3, kStageDown = 4, kStageCombine = 5 };
+
+void stage_mark(int idx, cudaStream_t s) {
+    if (idx < g_stage_n && g_stage_events[idx]) cudaEventRecord(g_stage_events[idx], s);
+}
+
+// Records the stage's start event on construction and its stop event on scope exit.
+struct StageScope {
+    int stage;
+    cudaStream_t stream;
+    StageScope(int st, cudaStream_t s) : stage(st), stream(s) { stage_mark(2 * stage, stream); }
+    ~StageScope() { stage_mark(2 * stage + 1, stream); }
+};
+
+#define MOE_TRY(expr)               \
+    do {                            \
+        const int _rc = (expr);     \
+        if (_rc != MOE_OK) return _rc; \
+    } while (0)
+
+#define MOE_CUDA(expr) MOE_TRY(cuda_rc(expr))
+
+// One kernel launch: fails with MOE_ERR_CUDA, counts successful launches.
+#define MOE_LAUNCH(expr)                                        \
+    do {                                                        \
+        if ((expr) != cudaSuccess) return MOE_ERR_CUDA;         \
+        g_launches.fetch_add(1, std::memory_order_relaxed);     \
+    } while (0)
+
+int enqueue_route(const moe_config& c, const Layout& L, void* ws, const void* x, const void* w_gate,
+                  const float* logit_bias, const float* select_bias, int32_t* topk_ids, float* gates,
+                  int32_t* block_hist, int sms, cudaStream_t s) {
+    float* p_part = at<float>(ws, L.p_part);
+    StageScope scope(kStageRouter, s);
+    if (!use_gemm_router(c)) {
+        MOE_LAUNCH(launch_router_warp(c.dtype, c.T, c.d, c.E, c.k, x, w_gate, logit_bias, select_bias, c.renormalize,
+                                    topk_ids, gates, p_part, block_hist, s));
+        return MOE_OK;
+    }
+    float* logits = at<float>(ws, L.logits);
+    GemmProblem g{};
+    g.A = x;
+    g.a_rows = c.T;
+    g.B1 = w_gate;
+    g.G = 1;
+    g.M = c.T;
+    g.N = c.E;
+    g.K = c.d;
+    g.out = logits;
+    if (c.dtype == MOE_BF16)
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, &g, 1, at<int>(ws, L.status), sms, s));
+    else
+        MOE_LAUNCH(launch_gemm_simt_f32(kGemmPlain, &g, 1, s));
+    MOE_LAUNCH(launch_router_from_logits(c.T, c.E, c.k, logits, logit_bias, select_bias, c.renormalize, topk_ids,
+                                       gates, p_part, block_hist, s));
+    return MOE_OK;
+}
+
+int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_perm, const int32_t* offsets,
+                const float* gates_perm, const void* w1, const void* w3, const void* w2, const void* x,
+                const void* ws1, const void* ws3, const void* ws2, float* y_perm, float* y_shared, int sms,
+                cudaStream_t s) {
+    const int n = c.T * c.k;
+    void* h = at<void>(ws, L.h);
+    void* hs = at<void>(ws, L.h_shared);
+    GemmProblem up[2] = {}, down[2] = {};
+    up[0].A = x_perm;
+    up[0].a_rows = n;
+    up[0].B1 = w1;
+    up[0].B2 = w3;
+    up[0].offsets = offsets;
+    up[0].G = c.E;
+    up[0].N = c.d_ff;
+    up[0].K = c.d;
+    up[0].out = h;
+    down[0].A = h;
+    down[0].a_rows = n;
+    down[0].B1 = w2;
+    down[0].offsets = offsets;
+    down[0].G = c.E;
+    down[0].N = c.d;
+    down[0].K = c.d_ff;
+    down[0].out = y_perm;
+    down[0].row_scale = gates_perm;
+    int np = 1;
+    if (c.n_shared) {
+        up[1].A = x;
+        up[1].a_rows = c.T;
+        up[1].B1 = ws1;
+        up[1].B2 = ws3;
+        up[1].G = 1;
+        up[1].M = c.T;
+        up[1].N = c.d_ff_shared;
+        up[1].K = c.d;
+        up[1].out = hs;
+        down[1].A = hs;
+        down[1].a_rows = c.T;
+        down[1].B1 = ws2;
+        down[1].G = 1;
+        down[1].M = c.T;
+        down[1].N = c.d;
+        down[1].K = c.d_ff_shared;
+        down[1].out = y_shared;
+        np = 2;
+    }
+    int* status = at<int>(ws, L.status);
+    {
+        StageScope scope(kStageUp, s);
+        if (c.dtype == MOE_BF16)
+            MOE_LAUNCH(launch_gemm_tc(kGemmSwiGLU, up, np, status, sms, s));
+        else
+            MOE_LAUNCH(launch_gemm_simt_f32(kGemmSwiGLU, up, np, s));
+    }
+    {
+        StageScope scope(kStageDown, s);
+        if (c.dtype == MOE_BF16)
+            MOE_LAUNCH(launch_gemm_tc(kGemmScale, down, np, status, sms, s));
+        else
+            MOE_LAUNCH(launch_gemm_simt_f32(kGemmScale, down, np, s));
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config* cfg) {
+    if (check_config(cfg) != MOE_OK) return 0;
+    return layout(*cfg).total;
+}
+
+int moe_workspace_init(const moe_config* cfg, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    const Layout L = layout(*cfg);
+    MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.status), 0, 16, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+int moe_route(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+              const float* select_bias, int32_t* topk_ids, float* gates, float* p_mean, void* ws, size_t ws_bytes,
+              moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (!x || !w_gate || !topk_ids || !gates) return MOE_ERR_NULL;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    for (const void* p : {x, w_gate, (const void*)topk_ids, (const void*)gates})
+        if (!aligned16(p)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    if (c.T == 0) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Layout L = layout(c);
+    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, nullptr, sms, s));
+    if (p_mean) {
+        const int nblk = (c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+        StageScope scope(kStageRouter, s);
+        MOE_LAUNCH(launch_p_mean(c.T, c.E, nblk, at<float>(ws, L.p_part), p_mean, s));
+    }
+    return MOE_OK;
+}
+
+int moe_permute(const moe_config* cfg, const int32_t* topk_ids, const float* gates, const void* x, int32_t* counts,
+                int32_t* kept, int32_t* offsets, int32_t* sorted_token_ids, int32_t* slot_pos, float* gates_perm,
+                void* x_perm, int32_t* n_dropped, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (!topk_ids || !gates || !x || !counts || !kept || !offsets || !sorted_token_ids || !slot_pos ||
+        !gates_perm || !x_perm || !n_dropped)
+        return MOE_ERR_NULL;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    if (c.T == 0) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Layout L = layout(c);
+    int* status = at<int>(ws, L.status);
+    int32_t* block_hist = at<int32_t>(ws, L.block_hist);
+    GroupOut o{};
+    o.counts = counts;
+    o.kept = kept;
+    o.offsets = offsets;
+    o.sorted_token_ids = sorted_token_ids;
+    o.slot_pos = slot_pos;
+    o.gates_perm = gates_perm;
+    o.n_dropped = n_dropped;
+    {
+        StageScope scope(kStageScan, s);
+        MOE_LAUNCH(launch_group_hist(c.T, c.E, c.k, topk_ids, block_hist, status, s));
+        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, c.capacity, topk_ids, gates, block_hist, o, status, s));
+    }
+    StageScope scope(kStageGather, s);
+    MOE_LAUNCH(launch_gather_rows(c.dtype, c.T, c.d, c.T * c.k, offsets + c.E, sorted_token_ids, x, x_perm, status, s));
+    return MOE_OK;
+}
+
+int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets, const float* gates_perm,
+                   const void* w1, const void* w3, const void* w2, const void* x, const void* ws1, const void* ws3,
+                   const void* ws2, float* y_perm, float* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (!x_perm || !offsets || !gates_perm || !w1 || !w3 || !w2 || !y_perm) return MOE_ERR_NULL;
+    if (c.n_shared && (!x || !ws1 || !ws3 || !ws2 || !y_shared)) return MOE_ERR_NULL;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    for (const void* p : {x_perm, w1, w3, w2, (const void*)y_perm})
+        if (!aligned16(p)) return MOE_ERR_ALIGN;
+    if (c.n_shared)
+        for (const void* p : {x, ws1, ws3, ws2, (const void*)y_shared})
+            if (!aligned16(p)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    if (c.T == 0) return MOE_OK;
+    const Layout L = layout(c);
+    return enqueue_ffn(c, L, ws, x_perm, offsets, gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared, sms,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_pos, const float* y_shared, void* y,
+                moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (!y_perm || !slot_pos || !y) return MOE_ERR_NULL;
+    if (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared))) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    if (c.T == 0) return MOE_OK;
+    StageScope scope(kStageCombine, reinterpret_cast<cudaStream_t>(stream));
+    MOE_LAUNCH(launch_combine(c.dtype, c.T, c.d, c.k, y_perm, slot_pos, y_shared, y,
+                              reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+int moe_load_stats(const moe_config* cfg, const int32_t* counts, const float* p_mean, float* f, float* L,
+                   moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (!counts || !p_mean) return MOE_ERR_NULL;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    if (c.T == 0) return MOE_OK;
+    MOE_LAUNCH(launch_load_stats(c.T, c.E, c.k, c.alpha, counts, p_mean, f, L, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                const void* ws3, const void* ws2, void* y, const moe_stats* stats, void* ws, size_t ws_bytes,
+                moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (!x || !w_gate || !w1 || !w3 || !w2 || !y) return MOE_ERR_NULL;
+    if (c.n_shared && (!ws1 || !ws3 || !ws2)) return MOE_ERR_NULL;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    for (const void* p : {x, w_gate, w1, w3, w2, (const void*)y})
+        if (!aligned16(p)) return MOE_ERR_ALIGN;
+    if (c.n_shared)
+        for (const void* p : {ws1, ws3, ws2})
+            if (!aligned16(p)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    if (c.T == 0) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Layout L = layout(c);
+    int* status = at<int>(ws, L.status);
+    int32_t* topk_ids = at<int32_t>(ws, L.topk_ids);
+    float* gates = at<float>(ws, L.gates);
+    int32_t* block_hist = at<int32_t>(ws, L.block_hist);
+    const int nblk = (c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+
+    // 1-3: router, softmax, top-k; the router blocks also emit their id histograms
+    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, block_hist, sms, s));
+
+    // 4: grouping (+ load statistics from the router's partial sums)
+    GroupOut o{};
+    o.counts = (stats && stats->counts) ? stats->counts : at<int32_t>(ws, L.counts);
+    o.kept = (stats && stats->kept) ? stats->kept : at<int32_t>(ws, L.kept);
+    o.offsets = at<int32_t>(ws, L.offsets);
+    o.sorted_token_ids = at<int32_t>(ws, L.sorted);
+    o.slot_pos = at<int32_t>(ws, L.slot_pos);
+    o.gates_perm = at<float>(ws, L.gates_perm);
+    o.n_dropped = (stats && stats->n_dropped) ? stats->n_dropped : at<int32_t>(ws, L.n_dropped);
+    if (stats && (stats->f || stats->p || stats->L)) {
+        o.p_part = at<float>(ws, L.p_part);
+        o.p_nblk = nblk;
+        o.f = stats->f;
+        o.p_mean = stats->p;
+        o.L = stats->L;
+        o.alpha = c.alpha;
+    }
+    {
+        StageScope scope(kStageScan, s);
+        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, c.capacity, topk_ids, gates, block_hist, o, status, s));
+    }
+    void* x_perm = at<void>(ws, L.x_perm);
+    {
+        StageScope scope(kStageGather, s);
+        MOE_LAUNCH(launch_gather_rows(c.dtype, c.T, c.d, c.T * c.k, o.offsets + c.E, o.sorted_token_ids, x, x_perm,
+                                      status, s));
+    }
+
+    // 5: expert FFNs (routed groups + shared expert in the same launches)
+    float* y_perm = at<float>(ws, L.y_perm);
+    float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
+    MOE_TRY(enqueue_ffn(c, L, ws, x_perm, o.offsets, o.gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared,
+                        sms, s));
+
+    // 6: combine
+    StageScope scope(kStageCombine, s);
+    MOE_LAUNCH(launch_combine(c.dtype, c.T, c.d, c.k, y_perm, o.slot_pos, y_shared, y, s));
+    return MOE_OK;
+}
+
+int moe_last_device_status(const moe_config* cfg, void* ws, moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    if (!ws) return MOE_ERR_NULL;
+    const Layout L = layout(*cfg);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(&v, at<int>(ws, L.status), sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (v != 0 && cudaMemset(at<int>(ws, L.status), 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    return v;
+}
+
+const char* moe_strerror(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_NULL: return "a required pointer is NULL";
+        case MOE_ERR_SHAPE: return "sizes out of range or not multiples of 8";
+        case MOE_ERR_DTYPE: return "unknown dtype";
+        case MOE_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+        case MOE_ERR_CUDA: return "a CUDA launch or runtime call failed";
+        case MOE_ERR_DEVICE: return "the current device is not a compute-capability 10.3 GPU";
+        case MOE_ERR_TIMEOUT: return "a kernel's bounded wait ran out (device status)";
+        case MOE_ERR_DEVICE_BOUNDS: return "a kernel read an index out of range (device status)";
+        case MOE_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+        default: return "unknown status";
+    }
+}
+
+const char* moe_version(void) { return "0.1.0"; }
+
+int moe_set_stage_events(void* const* events, int n) {
+    if (!events) {
+        g_stage_n = 0;
+        return MOE_OK;
+    }
+    if (n < 0 || n > kStageEvents) return MOE_ERR_SHAPE;
+    for (int i = 0; i < n; ++i) g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_stage_n = n;
+    return MOE_OK;
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

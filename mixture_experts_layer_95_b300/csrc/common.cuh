@@ -1,0 +1,168 @@
+// common.cuh -- internal declarations shared by the kernels of libmoe_b300.so.
+//
+// Nothing here is part of the C ABI (include/moe_b300.h is).  The launchers
+// declared at the bottom are called only by api.cu, which validates every
+// argument before a launch.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_b300.h"
+
+namespace moe {
+
+// Upper bound on E handled by the kernels (shared-memory histograms, scans).
+constexpr int kMaxExperts = 1024;
+// Tokens handled by one router block; the grouping kernels chunk the flat
+// (token, slot) entries by the same blocks so the router can emit the
+// per-block expert histograms the scan needs.
+constexpr int kRouterTokensPerBlock = 64;
+constexpr int kRouterThreads = 256;
+// The fused warp router keeps E logits per lane in registers.
+constexpr int kWarpRouterMaxE = 16;
+
+// Device status word values (mirror enum moe_status).
+constexpr int kStatusTimeout = MOE_ERR_TIMEOUT;
+constexpr int kStatusBounds = MOE_ERR_DEVICE_BOUNDS;
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Arg-max over a warp with ties resolved to the lower index; every lane gets
+// the winner.  Lanes with idx < 0 hold no candidate.
+__device__ __forceinline__ void warp_argmax(float& v, int& idx) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        bool take = (oi >= 0) && (idx < 0 || ov > v || (ov == v && oi < idx));
+        if (take) {
+            v = ov;
+            idx = oi;
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------
+// Launchers (one per kernel family).  All return cudaError_t of the launch.
+// ---------------------------------------------------------------------------
+
+// Fused router for E <= kWarpRouterMaxE: logits, softmax, top-k, gates, a
+// per-block partial sum of the softmax rows (p_part [nblk][E]) and, when
+// block_hist != nullptr, the per-block expert histogram of the chosen ids
+// (block_hist [nblk][E]).
+cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
+                               const float* logit_bias, const float* select_bias, int renormalize,
+                               int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
+                               cudaStream_t s);
+
+// Softmax / top-k over precomputed fp32 logits [T][E] (any E <= kMaxExperts);
+// same outputs as the fused router.
+cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, const float* logit_bias,
+                                      const float* select_bias, int renormalize, int32_t* topk_ids,
+                                      float* gates, float* p_part, int32_t* block_hist, cudaStream_t s);
+
+// p_mean[e] = (sum over blocks of p_part[b][e]) / T, fixed order.
+cudaError_t launch_p_mean(int T, int E, int nblk, const float* p_part, float* p_mean, cudaStream_t s);
+
+// Per-block expert histogram of topk_ids, chunked like the router.
+cudaError_t launch_group_hist(int T, int E, int k, const int32_t* topk_ids, int32_t* block_hist, int* status,
+                              cudaStream_t s);
+
+struct GroupOut {
+    int32_t* counts;
+    int32_t* kept;
+    int32_t* offsets;
+    int32_t* sorted_token_ids;
+    int32_t* slot_pos;
+    float* gates_perm;
+    int32_t* n_dropped;
+    // optional load statistics, written by block 0 when p_part != nullptr
+    const float* p_part;
+    int p_nblk;
+    float* f;
+    float* p_mean;
+    float* L;
+    float alpha;
+};
+
+// Scan of the block histograms, stable ranks, capacity cut, permutation.
+cudaError_t launch_group_scan(int T, int E, int k, int capacity, const int32_t* topk_ids, const float* gates,
+                              const int32_t* block_hist, const GroupOut& o, int* status, cudaStream_t s);
+
+// x_perm[pos] = x[sorted_token_ids[pos]] for pos < offsets[E].
+cudaError_t launch_gather_rows(int dtype, int T, int d, int rows_max, const int32_t* offsets_end,
+                               const int32_t* sorted_token_ids, const void* x, void* x_perm, int* status,
+                               cudaStream_t s);
+
+// y[t] = sum_j y_perm[slot_pos[t][j]] (slot_pos >= 0) + y_shared[t].
+cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, const int32_t* slot_pos,
+                           const float* y_shared, void* y, cudaStream_t s);
+
+// f = counts/(T k), L = alpha E sum f p.
+cudaError_t launch_load_stats(int T, int E, int k, float alpha, const int32_t* counts, const float* p_mean,
+                              float* f, float* L, cudaStream_t s);
+
+// ---- grouped GEMMs ----------------------------------------------------------
+
+enum GemmMode : int {
+    kGemmSwiGLU = 0,  // out(dtype) = silu(A W1^T) * (A W3^T), N = F columns
+    kGemmScale = 1,   // out(fp32)  = row_scale[row] * (A B^T)  (row_scale may be null: 1)
+    kGemmPlain = 2,   // out(fp32)  = A B^T
+};
+
+// One grouped problem: rows of A are split into groups by offsets (G+1
+// entries, device) or form a single group of M rows when offsets is null.
+// Group g multiplies its rows by B rows [g*N, (g+1)*N) (B is [G*N][K]).
+struct GemmProblem {
+    const void* A;        // [rows][K]
+    int a_rows;           // allocated rows of A (bounds the loads)
+    const void* B1;       // [G*N][K]
+    const void* B2;       // SwiGLU only: W3 with B1's layout
+    const int32_t* offsets;
+    int G;
+    int M;                // rows when offsets == nullptr
+    int N;
+    int K;
+    void* out;            // [rows][N]
+    const float* row_scale;
+};
+
+// Tensor-core (tcgen05) path, bf16 operands, fp32 accumulate.  Runs up to two
+// problems (a routed one and a shared-expert one) in one persistent launch.
+cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
+                           cudaStream_t s);
+
+// CUDA-core fp32 path with the same semantics (dtype MOE_F32).
+cudaError_t launch_gemm_simt_f32(int mode, const GemmProblem* probs, int nprob, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,581 @@
+// gemm_tc.cu -- grouped expert GEMMs on the 5th-generation tensor cores.
+//
+// "Mixture of experts (MoE)" handbook, "Implementation: token by token vs.
+// grouped by expert": each expert does one matrix multiplication over all the
+// tokens assigned to it (its contiguous segment after grouping), and "one
+// grouped GEMM computes all the experts at once".  The expert itself is the
+// handbook's SwiGLU Expert (down(silu(gate(x)) * up(x))), so one layer call
+// runs two grouped GEMMs:
+//   up:   H[r, :]  = silu(X[r] W1_g^T) * (X[r] W3_g^T)     (bf16 out)
+//   down: Y[r, :]  = gate[r] * (H[r] W2_g^T)                (fp32 out)
+// for every row r of group g's segment, plus the same for the shared expert
+// as a second problem in the same launch.  The router's logits (x W_g^T,
+// fp32 out) reuse the kernel with a single group.
+//
+// Design (sm_103a):
+//  * persistent: one CTA per SM walks a device-side tile list derived from the
+//    group offsets (no host sync); tiles are 128 rows x 256 accumulator
+//    columns; consecutive tiles share a weight tile (row blocks vary fastest)
+//    so that each weight tile is fetched from HBM once and re-read from L2.
+//  * warp 0: TMA producer (cp.async.bulk.tensor, 128-byte swizzle, 4-stage
+//    mbarrier ring; rows past a segment's end are loaded but never stored,
+//    rows past the tensor are zero-filled by the TMA unit).
+//  * warp 1: allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//    one lane issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128,
+//    N=256, K=16 per instruction); tcgen05.commit frees smem stages and
+//    hands finished accumulators to the epilogue.
+//  * warps 2-5: epilogue; tcgen05.ld 32 columns at a time, fused SwiGLU /
+//    gate scaling, 16-byte stores.  The two accumulators let the epilogue of
+//    tile i overlap the main loop of tile i+1.
+//  * every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
+//    MOE_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded)
+//    for its copies in flight, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int MAX_GROUPS = kMaxExperts;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr uint64_t kDrainLimitNs = 10000000ull;   // 10 ms to drain copies after an abort
+
+struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
+    CUtensorMap tmA[2];
+    CUtensorMap tmB1[2];
+    CUtensorMap tmB2[2];
+    const int32_t* offsets[2];
+    void* out[2];
+    const float* row_scale[2];
+    int G[2], M[2], N[2], K[2], a_rows[2];
+    int nprob;
+    int* status;
+};
+
+struct SmemTail {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint32_t tmem_base;
+    int abort_flag;
+    int total[2];
+    int tile_start[2][MAX_GROUPS + 1];
+    int row0[2][MAX_GROUPS];
+    int rows[2][MAX_GROUPS];
+};
+
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(SmemTail);
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Returns false when the CTA is
+// aborting (another role gave up) or this wait ran out of time.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            *abort_flag = 1;
+            record_status(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core groups 1024 bytes apart (SBO); LBO is unused for a
+// swizzled K-major operand whose K extent per instruction (32 bytes) stays
+// inside one swizzle row.  Bits 46-47 hold the descriptor version (1).
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(16u >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, dense, M x N.
+constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                                  // D format: f32
+           | (1u << 7)                                // A format: bf16
+           | (1u << 10)                               // B format: bf16
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------- tile schedule
+
+struct Tile {
+    int prob, g, m, n;
+    int a_row0, rows_valid;
+};
+
+template <int MODE>
+__device__ __forceinline__ int out_cols_per_tile() {
+    return MODE == kGemmSwiGLU ? BN / 2 : BN;
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& p, int id) {
+    Tile t;
+    t.prob = (id < st.total[0]) ? 0 : 1;
+    const int local = id - (t.prob ? st.total[0] : 0);
+    const int* ts = st.tile_start[t.prob];
+    int lo = 0, hi = p.G[t.prob] - 1;  // largest g with ts[g] <= local
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ts[mid] <= local) lo = mid;
+        else hi = mid - 1;
+    }
+    t.g = lo;
+    const int rows = st.rows[t.prob][lo];
+    const int mt = (rows + BM - 1) / BM;
+    const int r = local - ts[lo];
+    t.n = r / mt;
+    t.m = r - t.n * mt;
+    t.a_row0 = st.row0[t.prob][lo] + t.m * BM;
+    t.rows_valid = min(BM, rows - t.m * BM);
+    return t;
+}
+
+// --------------------------------------------------------------- epilogues
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile) {
+    const int N = p.N[t.prob];
+    const bool valid = row_in_tile < t.rows_valid;
+    const size_t grow = static_cast<size_t>(t.a_row0 + row_in_tile);
+    if (MODE == kGemmSwiGLU) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.prob]);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+            uint32_t g[32], u[32];
+            __syncwarp();  // tcgen05.ld is warp-aligned: reconverge after the per-lane stores
+            tmem_ld32(tacc + c0, g);
+            tmem_ld32(tacc + BN / 2 + c0, u);
+            tmem_ld_wait();
+            const int col = t.n * (BN / 2) + c0;
+            if (!valid || col >= N) continue;
+            __nv_bfloat16* dst = out + grow * N + col;
+            if (col + 32 <= N) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 pk;
+                    uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int i = q * 8 + h * 2;
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                            silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i])),
+                            silu_mul(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1])));
+                        w[h] = *reinterpret_cast<uint32_t*>(&b2);
+                    }
+                    reinterpret_cast<uint4*>(dst)[q] = pk;
+                }
+            } else {
+                for (int i = 0; i < 32 && col + i < N; ++i)
+                    dst[i] = __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i])));
+            }
+        }
+    } else {
+        float* out = static_cast<float*>(p.out[t.prob]);
+        float scale = 1.0f;
+        if (MODE == kGemmScale && valid && p.row_scale[t.prob] != nullptr) scale = __ldg(p.row_scale[t.prob] + grow);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            __syncwarp();
+            tmem_ld32(tacc + c0, v);
+            tmem_ld_wait();
+            const int col = t.n * BN + c0;
+            if (!valid || col >= N) continue;
+            float* dst = out + grow * N + col;
+            if (col + 32 <= N) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4*>(dst)[q] =
+                        make_float4(scale * __uint_as_float(v[4 * q]), scale * __uint_as_float(v[4 * q + 1]),
+                                    scale * __uint_as_float(v[4 * q + 2]), scale * __uint_as_float(v[4 * q + 3]));
+            } else {
+                for (int i = 0; i < 32 && col + i < N; ++i) dst[i] = scale * __uint_as_float(v[i]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)STAGES * STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* abort_flag = &st.abort_flag;
+
+    // ---- prologue: barriers, TMEM, tile prefix ----
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&st.full[s], 1);
+            mbar_init(&st.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&st.tmem_full[a], 1);
+            mbar_init(&st.tmem_empty[a], 4);
+        }
+        st.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        for (int q = 0; q < p.nprob; ++q) {
+            prefetch_tmap(&p.tmA[q]);
+            prefetch_tmap(&p.tmB1[q]);
+            if (MODE == kGemmSwiGLU) prefetch_tmap(&p.tmB2[q]);
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&st.tmem_base)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (warp == 2) {
+        // tiles per group: ceil(rows / BM) * column blocks; warp-wide prefix sum
+        for (int q = 0; q < 2; ++q) {
+            int carry = 0;
+            if (q < p.nprob) {
+                const int ncb = (p.N[q] + out_cols_per_tile<MODE>() - 1) / out_cols_per_tile<MODE>();
+                for (int base = 0; base < p.G[q]; base += 32) {
+                    const int g = base + lane;
+                    int tiles = 0;
+                    if (g < p.G[q]) {
+                        int lo = 0, hi = p.M[q];
+                        if (p.offsets[q]) {
+                            lo = p.offsets[q][g];
+                            hi = p.offsets[q][g + 1];
+                        }
+                        if (lo < 0 || hi < lo || hi > p.a_rows[q]) {
+                            record_status(p.status, kStatusBounds);
+                            lo = hi = 0;
+                        }
+                        st.row0[q][g] = lo;
+                        st.rows[q][g] = hi - lo;
+                        tiles = ((hi - lo + BM - 1) / BM) * ncb;
+                    }
+                    int incl = tiles;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    if (g < p.G[q]) st.tile_start[q][g] = carry + incl - tiles;
+                    carry += __shfl_sync(0xffffffffu, incl, 31);
+                }
+            }
+            if (lane == 0) st.total[q] = carry;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = st.tmem_base;
+    const int total_tiles = st.total[0] + st.total[1];
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_parity[STAGES];
+            bool used[STAGES];
+            for (int i = 0; i < STAGES; ++i) used[i] = false;
+            bool dead = false;
+            for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
+                const Tile t = decode_tile<MODE>(st, p, id);
+                const int K = p.K[t.prob];
+                const int nk = (K + BK - 1) / BK;
+                const int b_row0 = t.g * p.N[t.prob] + t.n * out_cols_per_tile<MODE>();
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status)) {
+                        dead = true;
+                        break;
+                    }
+                    uint8_t* sa = smem + (size_t)s * STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    mbar_expect_tx(&st.full[s], STAGE_BYTES);
+                    tma_load_2d(sa, &p.tmA[t.prob], kb * BK, t.a_row0, &st.full[s]);
+                    if (MODE == kGemmSwiGLU) {
+                        tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
+                        tma_load_2d(sb + B_BYTES / 2, &p.tmB2[t.prob], kb * BK, b_row0, &st.full[s]);
+                    } else {
+                        tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
+                    }
+                    issued_parity[s] = ph;
+                    used[s] = true;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // make sure no copy is still landing in shared memory before the CTA exits
+            volatile int no_abort = 0;
+            for (int i = 0; i < STAGES; ++i)
+                if (used[i]) mbar_wait(&st.full[i], issued_parity[i], &no_abort, nullptr, kDrainLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool dead = false;
+            for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x, ++it) {
+                const Tile t = decode_tile<MODE>(st, p, id);
+                const int nk = (p.K[t.prob] + BK - 1) / BK;
+                const int acc = it & 1;
+                const uint32_t use = static_cast<uint32_t>(it >> 1);
+                if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t dtm = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&st.full[s], ph, abort_flag, p.status)) {
+                        dead = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        umma_bf16(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2), sdesc_k_sw128(sb + kk * UMMA_K * 2), idesc,
+                                  (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(&st.empty[s]);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (dead) break;
+                umma_commit(&st.tmem_full[acc]);
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row_in_tile = quarter * 32 + lane;
+        int it = 0;
+        for (int id = blockIdx.x; id < total_tiles; id += gridDim.x, ++it) {
+            const Tile t = decode_tile<MODE>(st, p, id);
+            const int acc = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            epilogue_tile<MODE>(p, t, tacc, row_in_tile);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&st.tmem_empty[acc]);
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        // an aborted main loop may leave MMAs in flight: give them time to land
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {
+        }
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    }
+}
+
+// ----------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows][K] (K contiguous), box = 64 x box_rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap* tm, const void* base, int rows, int K, int box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
+    // the shared-memory opt-in is per device; remember it for the first 64 ordinals
+    static uint64_t attr_set_mask = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (!bit || !(attr_set_mask & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attr_set_mask |= bit;
+    }
+    grouped_gemm_tc_kernel<MODE><<<grid, NUM_THREADS, kSmemBytes, s>>>(prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
+                           cudaStream_t s) {
+    if (nprob < 1 || nprob > 2) return cudaErrorInvalidValue;
+    TcParams prm;
+    memset(&prm, 0, sizeof(prm));
+    const int b_box = (mode == kGemmSwiGLU) ? BN / 2 : BN;
+    for (int q = 0; q < nprob; ++q) {
+        const GemmProblem& g = probs[q];
+        if (g.G < 1 || g.G > MAX_GROUPS) return cudaErrorInvalidValue;
+        if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
+        if (!make_tmap(&prm.tmB1[q], g.B1, g.G * g.N, g.K, b_box)) return cudaErrorInvalidValue;
+        if (mode == kGemmSwiGLU && !make_tmap(&prm.tmB2[q], g.B2, g.G * g.N, g.K, b_box))
+            return cudaErrorInvalidValue;
+        prm.offsets[q] = g.offsets;
+        prm.out[q] = g.out;
+        prm.row_scale[q] = g.row_scale;
+        prm.G[q] = g.G;
+        prm.M[q] = g.M;
+        prm.N[q] = g.N;
+        prm.K[q] = g.K;
+        prm.a_rows[q] = g.a_rows;
+    }
+    prm.nprob = nprob;
+    prm.status = status;
+    const int grid = num_sms > 0 ? num_sms : 148;
+    switch (mode) {
+        case kGemmSwiGLU: return launch_mode<kGemmSwiGLU>(prm, grid, s);
+        case kGemmScale: return launch_mode<kGemmScale>(prm, grid, s);
+        case kGemmPlain: return launch_mode<kGemmPlain>(prm, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,153 @@
+"""GPU-vs-oracle parity harness (test infrastructure).
+
+``check_layer`` draws a workload's inputs on the GPU, runs the CUDA library
+through its C entry points (step by step and fused), runs the fp64 oracle on
+the very same tensors and returns a report of every comparison:
+
+* routing: for every token whose oracle margin between the k-th and (k+1)-th
+  selection score exceeds 1e-3, the GPU's set of ids equals the oracle's;
+  tokens inside the margin must still be a valid top-k (every chosen score
+  >= every unchosen score - 1e-3).  Gates are compared by id (abs 1e-5).
+* grouping: counts, kept, offsets, sorted_token_ids, slot_pos, n_dropped are
+  compared BIT-EXACTLY with the oracle's grouping of the GPU's ids, and with
+  the oracle's own grouping when no token is inside the margin.
+* x_perm: bit-exact row gather.
+* y: max |y_gpu - y_oracle| <= tol * RMS(y_oracle) over the checked tokens
+  (all tokens, or a seeded sample for the large workloads), with tol = 2e-2
+  for bf16 and 1e-4 for fp32; the oracle evaluates y with the GPU's ids.
+* statistics: f exact, p and L within fp32 summation error.
+* determinism: two fused calls give bit-identical y; the fused call equals
+  the chain of separate entry points bit for bit.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import mixture_experts_layer_95_b300 as moe
+import moe_inputs
+import oracle
+
+MARGIN = 1e-3
+TOL = {"bf16": 2e-2, "f32": 1e-4}
+
+
+def layer_of(w: moe_inputs.Workload) -> moe.Layer:
+    return moe.Layer(T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.F, n_shared=w.n_shared, d_ff_shared=w.F_s, dtype=w.dtype,
+                     renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha)
+
+
+def sample_tokens(T: int, n: int, seed: int = 1234, must=()) -> np.ndarray:
+    if n >= T:
+        return np.arange(T, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(T, n, replace=False).tolist()) | {0, T - 1} | set(int(t) for t in must if 0 <= t < T)
+    return np.array(sorted(pick), dtype=np.int32)
+
+
+def run_gpu(w: moe_inputs.Workload, L: dict, layer: moe.Layer):
+    """Separate entry points, then the fused call twice."""
+    ws = moe.workspace(layer)
+    ids, gates, p_mean = moe.route(layer, L["x"], L["w_gate"], L["logit_bias"], L["select_bias"], ws=ws)
+    g = moe.permute(layer, ids, gates, L["x"], ws=ws)
+    y_perm, y_shared = moe.expert_ffn(layer, g["x_perm"], g["offsets"], g["gates_perm"], L["w1"], L["w3"], L["w2"],
+                                      L["x"], L["ws1"], L["ws3"], L["ws2"], ws=ws)
+    y_steps = moe.combine(layer, y_perm, g["slot_pos"], y_shared)
+    f, Lb = moe.load_stats(layer, g["counts"], p_mean)
+    status_steps = moe.last_device_status(layer, ws)
+    fw = moe.Forward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
+                     L["ws3"], L["ws2"], stats=True)
+    y1 = fw(L["x"])
+    y2 = fw(L["x"])
+    status_fused = fw.device_status()
+    torch.cuda.synchronize()
+    return dict(ids=ids, gates=gates, p_mean=p_mean, group=g, y_perm=y_perm, y_steps=y_steps, f=f, L=Lb,
+                y1=y1, y2=y2, stats=fw.stats, status_steps=status_steps, status_fused=status_fused)
+
+
+def check_layer(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | None = None) -> dict:
+    """Runs one workload on cuda:0 and the oracle; returns a report dict with
+    'ok' and the individual measurements."""
+    layer = layer_of(w)
+    if L is None:
+        L = moe_inputs.make_layer(w, "cuda")
+    G = run_gpu(w, L, layer)
+    rep = dict(workload=w.name, status_steps=G["status_steps"], status_fused=G["status_fused"])
+    Ln = moe_inputs.layer_numpy(L)
+
+    # ---- routing ----
+    r = oracle.route(Ln["x"], Ln["w_gate"], w.k, Ln["logit_bias"], Ln["select_bias"], w.renormalize)
+    gids = G["ids"].cpu().numpy()
+    ggates = G["gates"].cpu().numpy()
+    outside = r["margin"] > MARGIN
+    same_set = np.array([set(a) == set(b) for a, b in zip(gids.tolist(), r["ids"].tolist())])
+    rep["ids_mismatch_outside_margin"] = int((~same_set & outside).sum())
+    rep["tokens_inside_margin"] = int((~outside).sum())
+    # validity of every GPU choice against the oracle's scores
+    scores = np.log(np.maximum(r["probs"], 1e-300))  # softmax is monotone: compare via log p + select_bias
+    if Ln["select_bias"] is not None:
+        scores = scores + Ln["select_bias"][None, :].astype(np.float64)
+    chosen = np.zeros_like(scores, dtype=bool)
+    np.put_along_axis(chosen, gids.astype(np.int64), True, axis=1)
+    min_chosen = np.where(chosen, scores, np.inf).min(1)
+    max_unchosen = np.where(chosen, -np.inf, scores).max(1)
+    rep["invalid_topk_tokens"] = int((min_chosen < max_unchosen - MARGIN).sum())
+    rep["duplicate_ids"] = int(sum(len(set(row)) != len(row) for row in gids.tolist()))
+    ogates_for_gpu = oracle.gates_for_ids(r["probs"], gids, w.renormalize)
+    rep["gates_max_abs_err"] = float(np.abs(ggates - ogates_for_gpu).max()) if gids.size else 0.0
+
+    # ---- grouping (bit-exact, as a function of the GPU's ids) ----
+    og = oracle.group(gids, w.E, w.capacity)
+    gg = {k_: v.cpu().numpy() for k_, v in G["group"].items() if k_ != "x_perm"}
+    grouping_equal = all(np.array_equal(gg[name].reshape(-1), og[name].reshape(-1))
+                         for name in ("counts", "kept", "offsets", "sorted_token_ids", "slot_pos"))
+    grouping_equal = grouping_equal and int(gg["n_dropped"][0]) == og["n_dropped"]
+    rep["grouping_bit_exact"] = bool(grouping_equal)
+    if rep["tokens_inside_margin"] == 0:
+        og_own = oracle.group(r["ids"], w.E, w.capacity)
+        rep["grouping_matches_oracle_routing"] = bool(
+            all(np.array_equal(gg[name].reshape(-1), og_own[name].reshape(-1))
+                for name in ("counts", "kept", "offsets", "sorted_token_ids", "slot_pos")))
+    total = int(og["offsets"][-1])
+    xp = G["group"]["x_perm"][:total]
+    src = L["x"][torch.from_numpy(og["sorted_token_ids"][:total].astype(np.int64)).to(xp.device)]
+    rep["x_perm_bit_exact"] = bool(torch.equal(xp, src))
+    rep["n_dropped"] = og["n_dropped"]
+
+    # ---- layer output ----
+    must = np.nonzero((og["slot_pos"] < 0).any(1))[0][:8] if og["n_dropped"] else ()
+    toks = sample_tokens(w.T, n_sample if n_sample else w.T, must=must)
+    y_or = oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], gids, ogates_for_gpu, og["slot_pos"], toks,
+                               (Ln["ws1"], Ln["ws3"], Ln["ws2"]) if w.n_shared else None)
+    y_gpu = G["y1"].float().cpu().numpy()[toks].astype(np.float64)
+    rms = float(np.sqrt(np.mean(y_or ** 2))) if y_or.size else 0.0
+    err = float(np.abs(y_gpu - y_or).max()) if y_or.size else 0.0
+    rep.update(y_rms=rms, y_max_abs_err=err, y_rel=err / rms if rms > 0 else err, tol=TOL[w.dtype],
+               y_tokens_checked=int(len(toks)))
+    rep["y_deterministic"] = bool(torch.equal(G["y1"], G["y2"]))
+    rep["fused_equals_steps"] = bool(torch.equal(G["y1"], G["y_steps"]))
+
+    # ---- statistics ----
+    st = oracle.load_stats(og["counts"], r["probs"], w.k, w.alpha)
+    s = {k_: v.cpu().numpy() for k_, v in G["stats"].items()}
+    rep["stats_counts_exact"] = bool(np.array_equal(s["counts"], og["counts"]) and
+                                     np.array_equal(s["kept"], og["kept"]) and
+                                     int(s["n_dropped"][0]) == og["n_dropped"])
+    rep["f_max_abs_err"] = float(np.abs(s["f"] - st["f"]).max())
+    rep["p_max_abs_err"] = float(np.abs(s["p"] - st["p"]).max())
+    rep["L_abs_err"] = float(abs(float(s["L"][0]) - st["L"]))
+    rep["L"] = float(s["L"][0])
+    rep["steps_stats_equal"] = bool(np.allclose(G["f"].cpu().numpy(), s["f"], rtol=0, atol=0) and
+                                    abs(float(G["L"].cpu().numpy()[0]) - float(s["L"][0])) <= 1e-6 * max(1.0, abs(st["L"])))
+    p_tol = 1e-5 + 1e-6 * math.sqrt(w.T)
+    rep["ok"] = bool(
+        rep["status_steps"] == 0 and rep["status_fused"] == 0 and rep["ids_mismatch_outside_margin"] == 0
+        and rep["invalid_topk_tokens"] == 0 and rep["duplicate_ids"] == 0 and rep["gates_max_abs_err"] < 1e-5
+        and rep["grouping_bit_exact"] and rep.get("grouping_matches_oracle_routing", True)
+        and rep["x_perm_bit_exact"] and rep["y_rel"] <= rep["tol"] and rep["y_deterministic"]
+        and rep["fused_equals_steps"] and rep["stats_counts_exact"] and rep["f_max_abs_err"] <= 1e-7
+        and rep["p_max_abs_err"] <= p_tol and rep["L_abs_err"] <= 1e-5 * max(1.0, abs(st["L"]))
+        and rep["steps_stats_equal"])
+    return rep

@@ -1,0 +1,82 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI (GPU only).
+
+Small workloads span several 128-row tiles, ragged segment ends, K and N
+tails, empty experts, dropped entries and every routing variant; the
+BASELINE-sized workloads are checked on every routing and grouping output and
+on a seeded sample of output rows, in the same launch configuration the
+benchmark times.  See tests/_parity.py for the comparison rules.
+"""
+import pytest
+import torch
+
+from moe_inputs import WORKLOADS, Workload
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    WORKLOADS["tiny_f32"],
+    Workload("small_bf16", T=300, d=512, E=8, F=384, k=2),
+    Workload("ragged_bf16", T=77, d=264, E=6, F=200, k=3),
+    Workload("ragged_f32", T=77, d=264, E=6, F=200, k=3, dtype="f32"),
+    Workload("gemm_router_capacity_zipf_bf16", T=520, d=384, E=64, F=256, k=4, capacity=40, zipf_s=1.2),
+    Workload("gemm_router_f32", T=150, d=128, E=20, F=96, k=3, dtype="f32"),
+    Workload("shared_selectbias_bf16", T=200, d=256, E=32, F=128, k=8, n_shared=1, F_s=192, select_bias=True),
+    Workload("dense_limit_bf16", T=64, d=128, E=8, F=128, k=8, renormalize=False),
+    Workload("single_expert_bf16", T=130, d=128, E=1, F=256, k=1),
+    Workload("capacity_zero_shared_bf16", T=40, d=128, E=4, F=64, k=2, capacity=0, n_shared=1, F_s=64),
+    Workload("decode_like_t1_bf16", T=1, d=512, E=8, F=512, k=2),
+    Workload("decode_like_t5_bf16", T=5, d=512, E=8, F=512, k=2),
+    Workload("many_tiles_bf16", T=1000, d=256, E=4, F=640, k=2),
+]
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mixture_experts_layer_95_b300 as moe
+    moe.lib()  # fail loudly if the library is missing
+    return torch.device("cuda")
+
+
+def _assert_ok(rep):
+    assert rep["ok"], rep
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_workloads_match_oracle(cuda, w):
+    from tests._parity import check_layer
+    _assert_ok(check_layer(w))
+
+
+def test_all_tokens_to_one_expert(cuda):
+    """Empty groups and one long segment (six 128-row tiles)."""
+    import moe_inputs
+    from tests._parity import check_layer
+    w = Workload("all_to_one_bf16", T=700, d=128, E=8, F=192, k=1)
+    L = moe_inputs.make_layer(w, "cuda")
+    L["logit_bias"] = torch.tensor([30.0] + [0.0] * 7, device="cuda")
+    rep = check_layer(w, L=L)
+    _assert_ok(rep)
+
+
+def test_zero_tokens_is_a_no_op(cuda):
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    w = Workload("empty", T=0, d=128, E=4, F=64, k=2)
+    L = moe_inputs.make_layer(w, "cuda")
+    layer = moe.Layer(T=0, d=128, E=4, k=2, d_ff=64)
+    y = moe.forward(layer, L["x"], L["w_gate"], L["w1"], L["w3"], L["w2"])
+    assert y.shape == (0, 128)
+
+
+FULL = [("mixtral_decode_t1", None), ("mixtral_decode_t8", None), ("mixtral_decode_t32", None),
+        ("mixtral_decode_t128", 48), ("mixtral_prefill", 48), ("skewed_capacity", 96), ("deepseek_v3", 24)]
+
+
+@pytest.mark.parametrize("name,n_sample", FULL, ids=[n for n, _ in FULL])
+def test_full_size_workloads_match_oracle(cuda, name, n_sample):
+    from tests._parity import check_layer
+    rep = check_layer(WORKLOADS[name], n_sample=n_sample)
+    print(rep)
+    _assert_ok(rep)
