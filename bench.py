@@ -245,7 +245,7 @@ def run_ours(args):
     launches0 = moe.launch_count()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.monotonic()
-    with moe.StageTimer() as timer:
+    with moe.StageTimer(args.steps) as timer:
         start.record(stream)
         for _ in range(args.steps):
             timer.begin_call()
@@ -266,6 +266,7 @@ def run_ours(args):
     if st != 0:
         raise moe.MoeError(st, "timed-region device status")
     stage_ms, stage_n = timer.ms()
+    timer.close()
     kept_total = int(fw.stats["kept"].sum().item())
     n_dropped = int(fw.stats["n_dropped"].item())
     touched = int((fw.stats["counts"] > 0).sum().item())

@@ -45,8 +45,9 @@
  *     dtype MOE_F32: everything is fp32 (IEEE fp32 FMA, no TF32).
  *   - Alignment: every device pointer must be 16-byte aligned and the
  *     workspace 256-byte aligned; d, F and F_s must be multiples of 8.
- *   - Limits: 1 <= k <= min(E, 32); E <= 1024; T >= 0 (T = 0 enqueues
- *     nothing); T * k < 2^31; n_shared is 0 or 1; d, F, F_s >= 8.
+ *   - Limits: 1 <= k <= min(E, 32); E <= 1024; T >= 0; T * k < 2^31;
+ *     n_shared is 0 or 1; d, F, F_s >= 8.  With T = 0 a call validates cfg
+ *     only and enqueues nothing (pointers may then be NULL).
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -95,6 +96,8 @@ typedef struct moe_config {
     int32_t renormalize; /* 1: divide the k gates of a token by their sum     */
     int32_t capacity;    /* < 0: unlimited                                     */
     float alpha;         /* L_balance = alpha * E * sum_i f_i p_i              */
+    int32_t y_fp32;      /* 0: y in `dtype`; 1: y in fp32 (the combine's fp32
+                            sum, before any rounding to bf16)                  */
 } moe_config;
 
 /* Optional statistics outputs of moe_forward (device pointers, each nullable). */
@@ -158,8 +161,9 @@ MOE_API int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int3
 
 /* Combine (step 6): y[t] = sum over j = 0..k-1 with slot_pos[t][j] >= 0 of
  * y_perm[slot_pos[t][j]], in that order, plus y_shared[t] when y_shared is
- * non-NULL; accumulated in fp32 and stored in cfg->dtype.  A token whose
- * entries were all dropped gets only its shared row (or 0). */
+ * non-NULL; accumulated in fp32 and stored in cfg->dtype (round to nearest
+ * even for bf16), or in fp32 when cfg->y_fp32.  A token whose entries were
+ * all dropped gets only its shared row (or 0). */
 MOE_API int moe_combine(const moe_config *cfg, const float *y_perm, const int32_t *slot_pos,
                 const float *y_shared, void *y, moe_stream_t stream);
 
@@ -170,7 +174,7 @@ MOE_API int moe_load_stats(const moe_config *cfg, const int32_t *counts, const f
                    float *L, moe_stream_t stream);
 
 /* The whole layer (steps 1-7) in one call, fused where the steps allow.
- *   y [T][d] (dtype) receives the layer output; stats (host struct, nullable)
+ *   y [T][d] (dtype, or fp32 when cfg->y_fp32) receives the layer output; stats (host struct, nullable)
  *   names optional device outputs.  ws1/ws3/ws2 are the shared expert's weights
  *   (required iff cfg->n_shared == 1). */
 MOE_API int moe_forward(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,

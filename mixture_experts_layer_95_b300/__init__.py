@@ -39,7 +39,7 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("capacity", ctypes.c_int32),
-                ("alpha", ctypes.c_float)]
+                ("alpha", ctypes.c_float), ("y_fp32", ctypes.c_int32)]
 
 
 class MoeStats(ctypes.Structure):
@@ -98,21 +98,38 @@ def launch_count() -> int:
 class StageTimer:
     """Per-stage CUDA-event timing of the library's launches (diagnostics).
 
-    ``with StageTimer() as st: ...`` makes every library call inside the block
-    record a start/stop event pair around each stage's launches; ``st.ms()``
-    returns the summed milliseconds per stage over all calls made inside the
-    block.  Events are recorded on the stream each call runs on.
+    Inside ``with StageTimer() as st:``, call ``st.begin_call()`` before each
+    library call; the call then records a start/stop event pair around each
+    stage's launches (``moe_set_stage_events``) on its own stream.  ``st.ms()``
+    returns the summed milliseconds per stage and how many calls recorded it.
+    The events are plain cudart events owned by this object.
     """
 
-    def __init__(self):
-        self._pairs = []
+    def __init__(self, n_calls: int = 0):
+        from cuda.bindings import runtime as cudart
+        self._rt = cudart
+        self._events = []
+        self._used = 0
+        for _ in range(n_calls):  # create up front so timed loops pay no creation cost
+            self._events.append(self._new_set())
+
+    def _new_set(self):
+        rt = self._rt
+        ev = []
+        for _ in range(2 * len(STAGES)):
+            err, e = rt.cudaEventCreate()
+            if err != rt.cudaError_t.cudaSuccess:
+                raise MoeError(-5, f"cudaEventCreate: {err}")
+            ev.append(e)
+        return ev
 
     def begin_call(self):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(STAGES))]
-        self._pairs.append(ev)
-        arr = (ctypes.c_void_p * len(ev))(*[e.cuda_event for e in ev])
-        self._arr = arr  # keep alive while set
-        _check(lib().moe_set_stage_events(arr, len(ev)), "moe_set_stage_events")
+        if self._used == len(self._events):
+            self._events.append(self._new_set())
+        ev = self._events[self._used]
+        self._used += 1
+        self._arr = (ctypes.c_void_p * len(ev))(*[int(e) for e in ev])  # kept alive while set
+        _check(lib().moe_set_stage_events(self._arr, len(ev)), "moe_set_stage_events")
 
     def __enter__(self):
         return self
@@ -122,19 +139,24 @@ class StageTimer:
         return False
 
     def ms(self):
+        """(summed ms per stage, number of calls that recorded the stage)."""
+        rt = self._rt
         torch.cuda.synchronize()
         out = {s: 0.0 for s in STAGES}
         counts = {s: 0 for s in STAGES}
-        for ev in self._pairs:
+        for ev in self._events[:self._used]:
             for i, s in enumerate(STAGES):
-                a, b = ev[2 * i], ev[2 * i + 1]
-                if a.query() and b.query():
-                    try:
-                        out[s] += a.elapsed_time(b)
-                        counts[s] += 1
-                    except RuntimeError:  # stage not recorded in this call
-                        pass
+                err, ms = rt.cudaEventElapsedTime(ev[2 * i], ev[2 * i + 1])
+                if err == rt.cudaError_t.cudaSuccess:  # stages a call did not run stay unrecorded
+                    out[s] += ms
+                    counts[s] += 1
         return out, counts
+
+    def close(self):
+        for ev in self._events:
+            for e in ev:
+                self._rt.cudaEventDestroy(e)
+        self._events = []
 
 
 def _check(rc: int, what: str):
@@ -156,15 +178,20 @@ class Layer:
     renormalize: bool = True
     capacity: int = -1
     alpha: float = 0.01
+    y_fp32: bool = False  # return y in fp32 (before rounding to the layer dtype)
 
     def cfg(self) -> MoeConfig:
         return MoeConfig(self.T, self.d, self.E, self.k, self.d_ff, self.n_shared, self.d_ff_shared,
                          MOE_BF16 if self.dtype == "bf16" else MOE_F32, int(bool(self.renormalize)),
-                         int(self.capacity), float(self.alpha))
+                         int(self.capacity), float(self.alpha), int(bool(self.y_fp32)))
 
     @property
     def torch_dtype(self):
         return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def y_dtype(self):
+        return torch.float32 if self.y_fp32 else self.torch_dtype
 
 
 def _ptr(t):
@@ -283,7 +310,7 @@ def combine(layer: Layer, y_perm, slot_pos, y_shared=None, stream=None):
     _need(slot_pos, (layer.T, layer.k), torch.int32, "slot_pos")
     if y_shared is not None:
         _need(y_shared, (layer.T, layer.d), torch.float32, "y_shared")
-    y = torch.empty((layer.T, layer.d), dtype=layer.torch_dtype, device=dev)
+    y = torch.empty((layer.T, layer.d), dtype=layer.y_dtype, device=dev)
     c = layer.cfg()
     _check(lib().moe_combine(ctypes.byref(c), _ptr(y_perm), _ptr(slot_pos), _ptr(y_shared), _ptr(y),
                              _stream(stream)), "moe_combine")
@@ -345,9 +372,9 @@ class Forward:
         L = self.layer
         _need(x, (L.T, L.d), L.torch_dtype, "x")
         if y is None:
-            y = torch.empty((L.T, L.d), dtype=L.torch_dtype, device=x.device)
+            y = torch.empty((L.T, L.d), dtype=L.y_dtype, device=x.device)
         else:
-            _need(y, (L.T, L.d), L.torch_dtype, "y")
+            _need(y, (L.T, L.d), L.y_dtype, "y")
         wg, lb, sb, w1, w3, w2, s1, s3, s2 = self._args
         st = ctypes.byref(self._stats_struct) if self._stats_struct is not None else None
         _check(lib().moe_forward(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(y), st,

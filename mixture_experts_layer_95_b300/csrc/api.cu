@@ -81,6 +81,7 @@ int check_config(const moe_config* c) {
     if (c->n_shared != 0 && c->n_shared != 1) return MOE_ERR_SHAPE;
     if (c->n_shared == 1 && c->d_ff_shared < 8) return MOE_ERR_SHAPE;
     if (c->d % 8 || c->d_ff % 8 || (c->n_shared && c->d_ff_shared % 8)) return MOE_ERR_SHAPE;
+    if (c->y_fp32 != 0 && c->y_fp32 != 1) return MOE_ERR_DTYPE;
     // the grouped GEMM tile list holds at most kMaxExperts row groups
     return MOE_OK;
 }
@@ -272,13 +273,13 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_gate, const fl
               moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
     if (!x || !w_gate || !topk_ids || !gates) return MOE_ERR_NULL;
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     for (const void* p : {x, w_gate, (const void*)topk_ids, (const void*)gates})
         if (!aligned16(p)) return MOE_ERR_ALIGN;
     int sms = 0;
     MOE_TRY(device_sms(&sms));
-    if (c.T == 0) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const Layout L = layout(c);
     MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, nullptr, sms, s));
@@ -295,6 +296,7 @@ int moe_permute(const moe_config* cfg, const int32_t* topk_ids, const float* gat
                 void* x_perm, int32_t* n_dropped, void* ws, size_t ws_bytes, moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
     if (!topk_ids || !gates || !x || !counts || !kept || !offsets || !sorted_token_ids || !slot_pos ||
         !gates_perm || !x_perm || !n_dropped)
         return MOE_ERR_NULL;
@@ -302,7 +304,6 @@ int moe_permute(const moe_config* cfg, const int32_t* topk_ids, const float* gat
     if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_ALIGN;
     int sms = 0;
     MOE_TRY(device_sms(&sms));
-    if (c.T == 0) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const Layout L = layout(c);
     int* status = at<int>(ws, L.status);
@@ -330,6 +331,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* off
                    const void* ws2, float* y_perm, float* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
     if (!x_perm || !offsets || !gates_perm || !w1 || !w3 || !w2 || !y_perm) return MOE_ERR_NULL;
     if (c.n_shared && (!x || !ws1 || !ws3 || !ws2 || !y_shared)) return MOE_ERR_NULL;
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
@@ -340,7 +342,6 @@ int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* off
             if (!aligned16(p)) return MOE_ERR_ALIGN;
     int sms = 0;
     MOE_TRY(device_sms(&sms));
-    if (c.T == 0) return MOE_OK;
     const Layout L = layout(c);
     return enqueue_ffn(c, L, ws, x_perm, offsets, gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared, sms,
                        reinterpret_cast<cudaStream_t>(stream));
@@ -350,13 +351,13 @@ int moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_
                 moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
     if (!y_perm || !slot_pos || !y) return MOE_ERR_NULL;
     if (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared))) return MOE_ERR_ALIGN;
     int sms = 0;
     MOE_TRY(device_sms(&sms));
-    if (c.T == 0) return MOE_OK;
     StageScope scope(kStageCombine, reinterpret_cast<cudaStream_t>(stream));
-    MOE_LAUNCH(launch_combine(c.dtype, c.T, c.d, c.k, y_perm, slot_pos, y_shared, y,
+    MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, c.k, y_perm, slot_pos, y_shared, y,
                               reinterpret_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
@@ -365,10 +366,10 @@ int moe_load_stats(const moe_config* cfg, const int32_t* counts, const float* p_
                    moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
     if (!counts || !p_mean) return MOE_ERR_NULL;
     int sms = 0;
     MOE_TRY(device_sms(&sms));
-    if (c.T == 0) return MOE_OK;
     MOE_LAUNCH(launch_load_stats(c.T, c.E, c.k, c.alpha, counts, p_mean, f, L, reinterpret_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
@@ -379,6 +380,7 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
                 moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
     if (!x || !w_gate || !w1 || !w3 || !w2 || !y) return MOE_ERR_NULL;
     if (c.n_shared && (!ws1 || !ws3 || !ws2)) return MOE_ERR_NULL;
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
@@ -389,7 +391,6 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
             if (!aligned16(p)) return MOE_ERR_ALIGN;
     int sms = 0;
     MOE_TRY(device_sms(&sms));
-    if (c.T == 0) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const Layout L = layout(c);
     int* status = at<int>(ws, L.status);
@@ -437,7 +438,7 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
 
     // 6: combine
     StageScope scope(kStageCombine, s);
-    MOE_LAUNCH(launch_combine(c.dtype, c.T, c.d, c.k, y_perm, o.slot_pos, y_shared, y, s));
+    MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, c.k, y_perm, o.slot_pos, y_shared, y, s));
     return MOE_OK;
 }
 

@@ -31,6 +31,7 @@
 //    MOE_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded)
 //    for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 
@@ -61,6 +62,8 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     int G[2], M[2], N[2], K[2], a_rows[2];
     int nprob;
     int* status;
+    uint64_t wait_limit_ns;  // bound on every mbarrier wait
+    int stall_producer;      // test switch: issue no loads, so the consumers' bounded waits run out
 };
 
 struct SmemTail {
@@ -387,14 +390,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
             uint32_t issued_parity[STAGES];
             bool used[STAGES];
             for (int i = 0; i < STAGES; ++i) used[i] = false;
-            bool dead = false;
+            bool dead = p.stall_producer != 0;
             for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
                 const Tile t = decode_tile<MODE>(st, p, id);
                 const int K = p.K[t.prob];
                 const int nk = (K + BK - 1) / BK;
                 const int b_row0 = t.g * p.N[t.prob] + t.n * out_cols_per_tile<MODE>();
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status)) {
+                    if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
                         dead = true;
                         break;
                     }
@@ -434,11 +437,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                 const int nk = (p.K[t.prob] + BK - 1) / BK;
                 const int acc = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
-                if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+                if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
                 tc_fence_after();
                 const uint32_t dtm = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(&st.full[s], ph, abort_flag, p.status)) {
+                    if (!mbar_wait(&st.full[s], ph, abort_flag, p.status, p.wait_limit_ns)) {
                         dead = true;
                         break;
                     }
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
             const Tile t = decode_tile<MODE>(st, p, id);
             const int acc = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
-            if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status)) break;
+            if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status, p.wait_limit_ns)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
             epilogue_tile<MODE>(p, t, tacc, row_in_tile);
@@ -569,6 +572,15 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     }
     prm.nprob = nprob;
     prm.status = status;
+    prm.wait_limit_ns = kWaitLimitNs;
+    // Test switch for the failure path: MOE_TEST_STALL_GEMM=1 makes the
+    // producer issue no loads; every CTA with work then gives up after a
+    // short bounded wait and reports MOE_ERR_TIMEOUT in the status word.
+    const char* stall = getenv("MOE_TEST_STALL_GEMM");
+    if (stall && stall[0] == '1') {
+        prm.stall_producer = 1;
+        prm.wait_limit_ns = 20000000ull;  // 20 ms
+    }
     const int grid = num_sms > 0 ? num_sms : 148;
     switch (mode) {
         case kGemmSwiGLU: return launch_mode<kGemmSwiGLU>(prm, grid, s);

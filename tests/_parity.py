@@ -15,12 +15,18 @@ the very same tensors and returns a report of every comparison:
 * y: max |y_gpu - y_oracle| <= tol * RMS(y_oracle) over the checked tokens
   (all tokens, or a seeded sample for the large workloads), with tol = 2e-2
   for bf16 and 1e-4 for fp32; the oracle evaluates y with the GPU's ids.
+  For bf16 layers the tolerance applies to the layer's fp32 result (the
+  library's y_fp32 output): rounding the output itself to bf16 costs up to
+  half an ulp, 2^-8 |y|, which alone exceeds 2e-2 RMS(y) wherever
+  |y| > 5.1 RMS(y).  The stored bf16 output must then equal the
+  round-to-nearest-even of that fp32 result bit for bit.
 * statistics: f exact, p and L within fp32 summation error.
 * determinism: two fused calls give bit-identical y; the fused call equals
   the chain of separate entry points bit for bit.
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 
 import numpy as np
@@ -62,9 +68,14 @@ def run_gpu(w: moe_inputs.Workload, L: dict, layer: moe.Layer):
     y1 = fw(L["x"])
     y2 = fw(L["x"])
     status_fused = fw.device_status()
+    layer32 = dataclasses.replace(layer, y_fp32=True)
+    fw32 = moe.Forward(layer32, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
+                       L["ws3"], L["ws2"])
+    y32 = fw32(L["x"])
+    status_fused |= fw32.device_status()
     torch.cuda.synchronize()
     return dict(ids=ids, gates=gates, p_mean=p_mean, group=g, y_perm=y_perm, y_steps=y_steps, f=f, L=Lb,
-                y1=y1, y2=y2, stats=fw.stats, status_steps=status_steps, status_fused=status_fused)
+                y1=y1, y2=y2, y32=y32, stats=fw.stats, status_steps=status_steps, status_fused=status_fused)
 
 
 def check_layer(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | None = None) -> dict:
@@ -121,11 +132,15 @@ def check_layer(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | N
     toks = sample_tokens(w.T, n_sample if n_sample else w.T, must=must)
     y_or = oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], gids, ogates_for_gpu, og["slot_pos"], toks,
                                (Ln["ws1"], Ln["ws3"], Ln["ws2"]) if w.n_shared else None)
-    y_gpu = G["y1"].float().cpu().numpy()[toks].astype(np.float64)
+    y_gpu = G["y32"].cpu().numpy()[toks].astype(np.float64)
+    y_stored = G["y1"].float().cpu().numpy()[toks].astype(np.float64)
     rms = float(np.sqrt(np.mean(y_or ** 2))) if y_or.size else 0.0
     err = float(np.abs(y_gpu - y_or).max()) if y_or.size else 0.0
+    err_stored = float(np.abs(y_stored - y_or).max()) if y_or.size else 0.0
     rep.update(y_rms=rms, y_max_abs_err=err, y_rel=err / rms if rms > 0 else err, tol=TOL[w.dtype],
-               y_tokens_checked=int(len(toks)))
+               y_rel_stored=err_stored / rms if rms > 0 else err_stored, y_tokens_checked=int(len(toks)),
+               y_max_over_rms=float(np.abs(y_or).max() / rms) if rms > 0 else 0.0)
+    rep["y_stored_is_rne_of_fp32"] = bool(torch.equal(G["y1"], G["y32"].to(G["y1"].dtype)))
     rep["y_deterministic"] = bool(torch.equal(G["y1"], G["y2"]))
     rep["fused_equals_steps"] = bool(torch.equal(G["y1"], G["y_steps"]))
 
@@ -146,7 +161,8 @@ def check_layer(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | N
         rep["status_steps"] == 0 and rep["status_fused"] == 0 and rep["ids_mismatch_outside_margin"] == 0
         and rep["invalid_topk_tokens"] == 0 and rep["duplicate_ids"] == 0 and rep["gates_max_abs_err"] < 1e-5
         and rep["grouping_bit_exact"] and rep.get("grouping_matches_oracle_routing", True)
-        and rep["x_perm_bit_exact"] and rep["y_rel"] <= rep["tol"] and rep["y_deterministic"]
+        and rep["x_perm_bit_exact"] and rep["y_rel"] <= rep["tol"] and rep["y_stored_is_rne_of_fp32"]
+        and rep["y_deterministic"]
         and rep["fused_equals_steps"] and rep["stats_counts_exact"] and rep["f_max_abs_err"] <= 1e-7
         and rep["p_max_abs_err"] <= p_tol and rep["L_abs_err"] <= 1e-5 * max(1.0, abs(st["L"]))
         and rep["steps_stats_equal"])

@@ -6,6 +6,8 @@ BASELINE-sized workloads are checked on every routing and grouping output and
 on a seeded sample of output rows, in the same launch configuration the
 benchmark times.  See tests/_parity.py for the comparison rules.
 """
+import json
+
 import pytest
 import torch
 
@@ -40,7 +42,7 @@ def cuda():
 
 
 def _assert_ok(rep):
-    assert rep["ok"], rep
+    assert rep["ok"], json.dumps(rep, indent=1)
 
 
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
@@ -78,5 +80,5 @@ FULL = [("mixtral_decode_t1", None), ("mixtral_decode_t8", None), ("mixtral_deco
 def test_full_size_workloads_match_oracle(cuda, name, n_sample):
     from tests._parity import check_layer
     rep = check_layer(WORKLOADS[name], n_sample=n_sample)
-    print(rep)
+    print(json.dumps(rep))
     _assert_ok(rep)
