@@ -146,6 +146,29 @@ MOE_API int moe_permute(const moe_config *cfg, const int32_t *topk_ids, const fl
                 int32_t *slot_pos, float *gates_perm, void *x_perm, int32_t *n_dropped, void *ws,
                 size_t ws_bytes, moe_stream_t stream);
 
+/* Allocation-free variant of moe_permute (the pages have no counterpart; it
+ * exists for callers, not for the method).  Same arguments and outputs as
+ * moe_permute, minus the workspace: for callers that are handed only their
+ * input and output buffers (a plug-in slot with a fixed signature) or that
+ * run where device allocation is forbidden after start-up, and so cannot
+ * obtain a workspace.  The per-block histogram scratch lives instead in a
+ * fixed device array inside the library: 65,536 int32 (256 KiB), held on
+ * every device that loads the library until the process exits.
+ *   Limit: ceil(T / 64) * E must not exceed 65,536, else MOE_ERR_SHAPE and
+ *   nothing is enqueued (e.g. T = 16384 with E <= 256, T = 4096 with E <= 1024).
+ *   The call allocates nothing and calls no allocating routine.  Its first
+ *   call on a device looks up the array's device address (once per device,
+ *   with that device current); make that first call before any stream capture.
+ *   All calls on a device share the one array and each call overwrites what
+ *   the previous one left there, so calls whose kernels overlap on the GPU
+ *   (different streams without ordering) race and give wrong results;
+ *   serialise them.  There is no workspace status word: ids outside [0, E)
+ *   are skipped, not reported. */
+MOE_API int moe_permute_static(const moe_config *cfg, const int32_t *topk_ids, const float *gates,
+                               const void *x, int32_t *counts, int32_t *kept, int32_t *offsets,
+                               int32_t *sorted_token_ids, int32_t *slot_pos, float *gates_perm,
+                               void *x_perm, int32_t *n_dropped, moe_stream_t stream);
+
 /* Expert FFNs over the grouped rows (step 5), gate applied in the epilogue.
  *   x_perm [T*k][d] and offsets [E+1] as produced by moe_permute; gates_perm fp32
  *   [T*k]; w1, w3 [E][F][d], w2 [E][d][F] (dtype).

@@ -25,7 +25,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTY
 
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
-            "moe_version", "moe_set_stage_events", "moe_launch_count")
+            "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static")
 STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
 
 
@@ -64,6 +64,8 @@ def lib():
         L.moe_workspace_init.argtypes = [cfgp, vp, sz, vp]
         L.moe_route.argtypes = [cfgp] + [vp] * 7 + [vp, sz, vp]
         L.moe_permute.argtypes = [cfgp] + [vp] * 11 + [vp, sz, vp]
+        L.moe_permute_static.argtypes = [cfgp] + [vp] * 11 + [vp]
+        L.moe_permute_static.restype = i32
         L.moe_expert_ffn.argtypes = [cfgp] + [vp] * 12 + [vp, sz, vp]
         L.moe_combine.argtypes = [cfgp] + [vp] * 4 + [vp]
         L.moe_load_stats.argtypes = [cfgp] + [vp] * 4 + [vp]
@@ -273,6 +275,32 @@ def permute(layer: Layer, topk_ids, gates, x, ws=None, stream=None):
                              _ptr(out["kept"]), _ptr(out["offsets"]), _ptr(out["sorted_token_ids"]),
                              _ptr(out["slot_pos"]), _ptr(out["gates_perm"]), _ptr(out["x_perm"]),
                              _ptr(out["n_dropped"]), _ptr(ws), ws.numel(), _stream(stream)), "moe_permute")
+    return out
+
+
+def permute_static(layer: Layer, topk_ids, gates, x, stream=None):
+    """moe_permute_static: moe_permute without a workspace (fixed library scratch).
+
+    For callers that cannot allocate device memory; see include/moe_b300.h for
+    the size limit and the rule that concurrent calls on one device race.
+    """
+    dev = x.device
+    n = layer.T * layer.k
+    _need(topk_ids, (layer.T, layer.k), torch.int32, "topk_ids")
+    _need(gates, (layer.T, layer.k), torch.float32, "gates")
+    _need(x, (layer.T, layer.d), layer.torch_dtype, "x")
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(counts=torch.empty(layer.E, **i32), kept=torch.empty(layer.E, **i32),
+               offsets=torch.empty(layer.E + 1, **i32), sorted_token_ids=torch.empty(n, **i32),
+               slot_pos=torch.empty((layer.T, layer.k), **i32),
+               gates_perm=torch.empty(n, dtype=torch.float32, device=dev),
+               x_perm=torch.empty((n, layer.d), dtype=layer.torch_dtype, device=dev),
+               n_dropped=torch.empty(1, **i32))
+    c = layer.cfg()
+    _check(lib().moe_permute_static(ctypes.byref(c), _ptr(topk_ids), _ptr(gates), _ptr(x), _ptr(out["counts"]),
+                                    _ptr(out["kept"]), _ptr(out["offsets"]), _ptr(out["sorted_token_ids"]),
+                                    _ptr(out["slot_pos"]), _ptr(out["gates_perm"]), _ptr(out["x_perm"]),
+                                    _ptr(out["n_dropped"]), _stream(stream)), "moe_permute_static")
     return out
 
 
