@@ -197,7 +197,7 @@ def cpu_model():
 def layer_of(w):
     import mixture_experts_layer_95_b300 as moe
     return moe.Layer(T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.F, n_shared=w.n_shared, d_ff_shared=w.F_s, dtype=w.dtype,
-                     renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha)
+                     renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha, h_split=w.h_split)
 
 
 def run_ours(args):

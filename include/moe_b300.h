@@ -41,7 +41,8 @@
  *     W1 (gate_proj) and W3 (up_proj) are [E][F][d]; W2 (down_proj) is
  *     [E][d][F]; the shared expert's Ws1/Ws3 are [F_s][d] and Ws2 is [d][F_s].
  *   - dtype MOE_BF16: x, weights and y are bf16; accumulation is fp32; the
- *     hidden activation H is stored as bf16 between the two expert GEMMs.
+ *     hidden activation H is stored as bf16 between the two expert GEMMs (or
+ *     as a hi + lo bf16 pair when cfg->h_split).
  *     dtype MOE_F32: everything is fp32 (IEEE fp32 FMA, no TF32).
  *   - Alignment: every device pointer must be 16-byte aligned and the
  *     workspace 256-byte aligned; d, F and F_s must be multiples of 8.
@@ -98,6 +99,12 @@ typedef struct moe_config {
     float alpha;         /* L_balance = alpha * E * sum_i f_i p_i              */
     int32_t y_fp32;      /* 0: y in `dtype`; 1: y in fp32 (the combine's fp32
                             sum, before any rounding to bf16)                  */
+    int32_t h_split;     /* bf16 layers: 1 keeps the SwiGLU activation H as a
+                            pair of bf16 values (hi + lo, ~16 significant bits)
+                            and runs the down GEMM on both halves, for layers
+                            whose outputs are too heavy-tailed for a bf16 H;
+                            costs a second pass of the down GEMM's MMAs.
+                            Ignored for fp32 layers.                           */
 } moe_config;
 
 /* Optional statistics outputs of moe_forward (device pointers, each nullable). */

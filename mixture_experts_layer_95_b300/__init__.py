@@ -39,7 +39,7 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("capacity", ctypes.c_int32),
-                ("alpha", ctypes.c_float), ("y_fp32", ctypes.c_int32)]
+                ("alpha", ctypes.c_float), ("y_fp32", ctypes.c_int32), ("h_split", ctypes.c_int32)]
 
 
 class MoeStats(ctypes.Structure):
@@ -181,11 +181,12 @@ class Layer:
     capacity: int = -1
     alpha: float = 0.01
     y_fp32: bool = False  # return y in fp32 (before rounding to the layer dtype)
+    h_split: bool = False  # bf16: keep H as a hi + lo bf16 pair (heavy-tailed layers)
 
     def cfg(self) -> MoeConfig:
         return MoeConfig(self.T, self.d, self.E, self.k, self.d_ff, self.n_shared, self.d_ff_shared,
                          MOE_BF16 if self.dtype == "bf16" else MOE_F32, int(bool(self.renormalize)),
-                         int(self.capacity), float(self.alpha), int(bool(self.y_fp32)))
+                         int(self.capacity), float(self.alpha), int(bool(self.y_fp32)), int(bool(self.h_split)))
 
     @property
     def torch_dtype(self):

@@ -18,14 +18,16 @@ constexpr int kMaxTopK = 32;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
-bool use_gemm_router(const moe_config& c) { return c.E > kWarpRouterMaxE; }
+bool use_gemm_router(const moe_config& c) { return !use_warp_router(c.E, c.d, c.dtype); }
 
 size_t esize(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
+
+bool use_h_split(const moe_config& c) { return c.dtype == MOE_BF16 && c.h_split == 1; }
 
 // Byte offsets of every workspace region; `total` is the size.
 struct Layout {
     size_t status, topk_ids, gates, p_part, block_hist, counts, kept, offsets, n_dropped, sorted, slot_pos,
-        gates_perm, p_mean, f, L, logits, x_perm, h, h_shared, y_perm, y_shared, total;
+        gates_perm, p_mean, f, L, logits, x_perm, h, h_shared, h_lo, h_shared_lo, y_perm, y_shared, total;
 };
 
 Layout layout(const moe_config& c) {
@@ -58,6 +60,9 @@ Layout layout(const moe_config& c) {
     l.x_perm = take(n * c.d * esize(c));
     l.h = take(n * c.d_ff * esize(c));
     l.h_shared = take(c.n_shared ? (size_t)c.T * c.d_ff_shared * esize(c) : 0);
+    const bool split = use_h_split(c);
+    l.h_lo = take(split ? n * c.d_ff * esize(c) : 0);
+    l.h_shared_lo = take(split && c.n_shared ? (size_t)c.T * c.d_ff_shared * esize(c) : 0);
     l.y_perm = take(4 * n * c.d);
     l.y_shared = take(c.n_shared ? 4 * (size_t)c.T * c.d : 0);
     l.total = off;
@@ -82,6 +87,7 @@ int check_config(const moe_config* c) {
     if (c->n_shared == 1 && c->d_ff_shared < 8) return MOE_ERR_SHAPE;
     if (c->d % 8 || c->d_ff % 8 || (c->n_shared && c->d_ff_shared % 8)) return MOE_ERR_SHAPE;
     if (c->y_fp32 != 0 && c->y_fp32 != 1) return MOE_ERR_DTYPE;
+    if (c->h_split != 0 && c->h_split != 1) return MOE_ERR_DTYPE;
     // the grouped GEMM tile list holds at most kMaxExperts row groups
     return MOE_OK;
 }
@@ -190,6 +196,9 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     const int n = c.T * c.k;
     void* h = at<void>(ws, L.h);
     void* hs = at<void>(ws, L.h_shared);
+    const bool split = use_h_split(c);
+    void* h_lo = split ? at<void>(ws, L.h_lo) : nullptr;
+    void* hs_lo = split && c.n_shared ? at<void>(ws, L.h_shared_lo) : nullptr;
     GemmProblem up[2] = {}, down[2] = {};
     up[0].A = x_perm;
     up[0].a_rows = n;
@@ -200,7 +209,9 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     up[0].N = c.d_ff;
     up[0].K = c.d;
     up[0].out = h;
+    up[0].out2 = h_lo;
     down[0].A = h;
+    down[0].A2 = h_lo;
     down[0].a_rows = n;
     down[0].B1 = w2;
     down[0].offsets = offsets;
@@ -220,7 +231,9 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
         up[1].N = c.d_ff_shared;
         up[1].K = c.d;
         up[1].out = hs;
+        up[1].out2 = hs_lo;
         down[1].A = hs;
+        down[1].A2 = hs_lo;
         down[1].a_rows = c.T;
         down[1].B1 = ws2;
         down[1].G = 1;
@@ -241,7 +254,7 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     {
         StageScope scope(kStageDown, s);
         if (c.dtype == MOE_BF16)
-            MOE_LAUNCH(launch_gemm_tc(kGemmScale, down, np, status, sms, s));
+            MOE_LAUNCH(launch_gemm_tc(split ? kGemmScaleSplit : kGemmScale, down, np, status, sms, s));
         else
             MOE_LAUNCH(launch_gemm_simt_f32(kGemmScale, down, np, s));
     }

@@ -30,6 +30,17 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v
     *reinterpret_cast<uint2*>(p) = u;
 }
 
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+
+// One warp per token.  Lane j < k holds slot_pos[t][j] (k <= 32) and
+// broadcasts it; every lane then sums 8 consecutive columns per step (two
+// 16-byte loads per row, all rows' loads issued before the adds) in the
+// fixed order j = 0..k-1, then the shared row.
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, const float* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_pos,
@@ -37,26 +48,28 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (t >= Tn) return;
-    const int32_t* sp = slot_pos + (size_t)t * k;
-    for (int c = lane * 4; c < d; c += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int my_pos = lane < k ? __ldg(slot_pos + (size_t)t * k + lane) : -1;
+    // the loop bound is the same for every lane, so the shuffles below always
+    // run with the whole warp; lanes past the row end skip only the memory work
+    for (int c0 = 0; c0 < d; c0 += 256) {
+        const int c = c0 + lane * 8;
+        const bool active = c < d;  // d is a multiple of 8: an active lane owns 8 columns
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
         for (int j = 0; j < k; ++j) {
-            const int pos = __ldg(sp + j);
-            if (pos < 0) continue;
-            const float4 v = __ldg(reinterpret_cast<const float4*>(y_perm + (size_t)pos * d + c));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            const int pos = __shfl_sync(0xffffffffu, my_pos, j);
+            if (pos < 0 || !active) continue;
+            const float4* src = reinterpret_cast<const float4*>(y_perm + (size_t)pos * d + c);
+            add4(a0, __ldg(src));
+            add4(a1, __ldg(src + 1));
         }
+        if (!active) continue;
         if (y_shared) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            const float4* src = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
+            add4(a0, __ldg(src));
+            add4(a1, __ldg(src + 1));
         }
-        store4<T>(y + (size_t)t * d + c, acc);
+        store4<T>(y + (size_t)t * d + c, a0);
+        store4<T>(y + (size_t)t * d + c + 4, a1);
     }
 }
 

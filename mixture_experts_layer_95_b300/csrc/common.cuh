@@ -20,8 +20,23 @@ constexpr int kMaxExperts = 1024;
 // per-block expert histograms the scan needs.
 constexpr int kRouterTokensPerBlock = 64;
 constexpr int kRouterThreads = 256;
-// The fused warp router keeps E logits per lane in registers.
+// The fused warp router keeps E logits per lane in registers and W_g in
+// shared memory (padded to 8 or 16 rows); larger routers go through the
+// tensor-core GEMM.
 constexpr int kWarpRouterMaxE = 16;
+constexpr int kWarpRouterThreads = 512;
+constexpr size_t kWarpRouterMaxSmem = 160 * 1024;
+
+inline int warp_router_width(int E) { return E <= 8 ? 8 : 16; }
+
+inline size_t warp_router_smem_bytes(int E, int d, int dtype) {
+    return (size_t)warp_router_width(E) * d * (dtype == MOE_BF16 ? 2 : 4);
+}
+
+// True when the fused warp router handles this layer.
+inline bool use_warp_router(int E, int d, int dtype) {
+    return E <= kWarpRouterMaxE && warp_router_smem_bytes(E, d, dtype) <= kWarpRouterMaxSmem;
+}
 
 // Device status word values (mirror enum moe_status).
 constexpr int kStatusTimeout = MOE_ERR_TIMEOUT;
@@ -138,6 +153,7 @@ enum GemmMode : int {
     kGemmSwiGLU = 0,  // out(dtype) = silu(A W1^T) * (A W3^T), N = F columns
     kGemmScale = 1,   // out(fp32)  = row_scale[row] * (A B^T)  (row_scale may be null: 1)
     kGemmPlain = 2,   // out(fp32)  = A B^T
+    kGemmScaleSplit = 3,  // out(fp32) = row_scale[row] * ((A + A2) B^T), A and A2 bf16 (hi and lo halves)
 };
 
 // One grouped problem: rows of A are split into groups by offsets (G+1
@@ -155,6 +171,8 @@ struct GemmProblem {
     int K;
     void* out;            // [rows][N]
     const float* row_scale;
+    const void* A2;       // kGemmScaleSplit: the lo half of A, same layout
+    void* out2;           // kGemmSwiGLU: optional lo half of H (H - bf16(H)), same layout as out
 };
 
 // Tensor-core (tcgen05) path, bf16 operands, fp32 accumulate.  Runs up to two

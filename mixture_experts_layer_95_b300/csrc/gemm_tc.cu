@@ -42,10 +42,19 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;  // ring depth; 3 for the split-A down GEMM (64 KB stages)
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+
+// Per-mode stage layout: [A | (A_lo) | B].  The split mode multiplies two A
+// operands (the hi and lo bf16 halves of H) by the same B tile.
+template <int MODE>
+struct StageCfg {
+    static constexpr bool kSplit = MODE == kGemmScaleSplit;
+    static constexpr int kStages = kSplit ? 3 : STAGES;
+    static constexpr int kBOff = kSplit ? 2 * A_BYTES : A_BYTES;
+    static constexpr int kBytes = kBOff + B_BYTES;
+};
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = kMaxExperts;
@@ -54,10 +63,12 @@ constexpr uint64_t kDrainLimitNs = 10000000ull;   // 10 ms to drain copies after
 
 struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     CUtensorMap tmA[2];
+    CUtensorMap tmA2[2];  // split mode: the lo half of A
     CUtensorMap tmB1[2];
     CUtensorMap tmB2[2];
     const int32_t* offsets[2];
     void* out[2];
+    void* out2[2];  // SwiGLU: when non-null, the lo half of H (H - bf16(H)) goes here
     const float* row_scale[2];
     int G[2], M[2], N[2], K[2], a_rows[2];
     int nprob;
@@ -79,7 +90,10 @@ struct SmemTail {
     int rows[2][MAX_GROUPS];
 };
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(SmemTail);
+template <int MODE>
+constexpr size_t smem_bytes() {
+    return 1024 /*align slack*/ + (size_t)StageCfg<MODE>::kStages * StageCfg<MODE>::kBytes + sizeof(SmemTail);
+}
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -248,6 +262,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
     const size_t grow = static_cast<size_t>(t.a_row0 + row_in_tile);
     if (MODE == kGemmSwiGLU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.prob]);
+        __nv_bfloat16* out_lo = static_cast<__nv_bfloat16*>(p.out2[t.prob]);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN / 2; c0 += 32) {
             uint32_t g[32], u[32];
@@ -258,30 +273,41 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             const int col = t.n * (BN / 2) + c0;
             if (!valid || col >= N) continue;
             __nv_bfloat16* dst = out + grow * N + col;
+            __nv_bfloat16* dst_lo = out_lo ? out_lo + grow * N + col : nullptr;
             if (col + 32 <= N) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    uint4 pk;
+                    uint4 pk, pk_lo;
                     uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+                    uint32_t* w_lo = reinterpret_cast<uint32_t*>(&pk_lo);
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         const int i = q * 8 + h * 2;
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                            silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i])),
-                            silu_mul(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1])));
+                        const float h0 = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
+                        const float h1 = silu_mul(__uint_as_float(g[i + 1]), __uint_as_float(u[i + 1]));
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
                         w[h] = *reinterpret_cast<uint32_t*>(&b2);
+                        const float2 back = __bfloat1622float2(b2);
+                        __nv_bfloat162 l2 = __floats2bfloat162_rn(h0 - back.x, h1 - back.y);
+                        w_lo[h] = *reinterpret_cast<uint32_t*>(&l2);
                     }
                     reinterpret_cast<uint4*>(dst)[q] = pk;
+                    if (dst_lo) reinterpret_cast<uint4*>(dst_lo)[q] = pk_lo;
                 }
             } else {
-                for (int i = 0; i < 32 && col + i < N; ++i)
-                    dst[i] = __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i])));
+                for (int i = 0; i < 32 && col + i < N; ++i) {
+                    const float hv = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
+                    const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
+                    dst[i] = hb;
+                    if (dst_lo) dst_lo[i] = __float2bfloat16_rn(hv - __bfloat162float(hb));
+                }
             }
         }
     } else {
         float* out = static_cast<float*>(p.out[t.prob]);
         float scale = 1.0f;
-        if (MODE == kGemmScale && valid && p.row_scale[t.prob] != nullptr) scale = __ldg(p.row_scale[t.prob] + grow);
+        if ((MODE == kGemmScale || MODE == kGemmScaleSplit) && valid && p.row_scale[t.prob] != nullptr)
+            scale = __ldg(p.row_scale[t.prob] + grow);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t v[32];
@@ -310,13 +336,15 @@ template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)STAGES * STAGE_BYTES);
+    using SC = StageCfg<MODE>;
+    constexpr int NST = SC::kStages;
+    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)NST * SC::kBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &st.abort_flag;
 
     // ---- prologue: barriers, TMEM, tile prefix ----
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(&st.full[s], 1);
             mbar_init(&st.empty[s], 1);
         }
@@ -333,6 +361,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
             prefetch_tmap(&p.tmA[q]);
             prefetch_tmap(&p.tmB1[q]);
             if (MODE == kGemmSwiGLU) prefetch_tmap(&p.tmB2[q]);
+            if (SC::kSplit) prefetch_tmap(&p.tmA2[q]);
         }
     }
     if (warp == 1) {
@@ -387,9 +416,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            uint32_t issued_parity[STAGES];
-            bool used[STAGES];
-            for (int i = 0; i < STAGES; ++i) used[i] = false;
+            uint32_t issued_parity[NST];
+            bool used[NST];
+            for (int i = 0; i < NST; ++i) used[i] = false;
             bool dead = p.stall_producer != 0;
             for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
                 const Tile t = decode_tile<MODE>(st, p, id);
@@ -401,10 +430,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                         dead = true;
                         break;
                     }
-                    uint8_t* sa = smem + (size_t)s * STAGE_BYTES;
-                    uint8_t* sb = sa + A_BYTES;
-                    mbar_expect_tx(&st.full[s], STAGE_BYTES);
+                    uint8_t* sa = smem + (size_t)s * SC::kBytes;
+                    uint8_t* sb = sa + SC::kBOff;
+                    mbar_expect_tx(&st.full[s], SC::kBytes);
                     tma_load_2d(sa, &p.tmA[t.prob], kb * BK, t.a_row0, &st.full[s]);
+                    if (SC::kSplit) tma_load_2d(sa + A_BYTES, &p.tmA2[t.prob], kb * BK, t.a_row0, &st.full[s]);
                     if (MODE == kGemmSwiGLU) {
                         tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
                         tma_load_2d(sb + B_BYTES / 2, &p.tmB2[t.prob], kb * BK, b_row0, &st.full[s]);
@@ -413,7 +443,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                     }
                     issued_parity[s] = ph;
                     used[s] = true;
-                    if (++s == STAGES) {
+                    if (++s == NST) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -421,7 +451,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
             }
             // make sure no copy is still landing in shared memory before the CTA exits
             volatile int no_abort = 0;
-            for (int i = 0; i < STAGES; ++i)
+            for (int i = 0; i < NST; ++i)
                 if (used[i]) mbar_wait(&st.full[i], issued_parity[i], &no_abort, nullptr, kDrainLimitNs);
         }
     } else if (warp == 1) {
@@ -446,15 +476,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)s * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t sa = smem_u32(smem + (size_t)s * SC::kBytes);
+                    const uint32_t sb = sa + SC::kBOff;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        umma_bf16(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2), sdesc_k_sw128(sb + kk * UMMA_K * 2), idesc,
-                                  (kb | kk) != 0 ? 1u : 0u);
+                        const uint64_t bdesc = sdesc_k_sw128(sb + kk * UMMA_K * 2);
+                        umma_bf16(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2), bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        if (SC::kSplit) umma_bf16(dtm, sdesc_k_sw128(sa + A_BYTES + kk * UMMA_K * 2), bdesc, idesc, 1u);
                     }
                     umma_commit(&st.empty[s]);
-                    if (++s == STAGES) {
+                    if (++s == NST) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -538,11 +569,11 @@ cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (!bit || !(attr_set_mask & bit)) {
         cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+                                             static_cast<int>(smem_bytes<MODE>()));
         if (e != cudaSuccess) return e;
         attr_set_mask |= bit;
     }
-    grouped_gemm_tc_kernel<MODE><<<grid, NUM_THREADS, kSmemBytes, s>>>(prm);
+    grouped_gemm_tc_kernel<MODE><<<grid, NUM_THREADS, smem_bytes<MODE>(), s>>>(prm);
     return cudaGetLastError();
 }
 
@@ -561,8 +592,10 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         if (!make_tmap(&prm.tmB1[q], g.B1, g.G * g.N, g.K, b_box)) return cudaErrorInvalidValue;
         if (mode == kGemmSwiGLU && !make_tmap(&prm.tmB2[q], g.B2, g.G * g.N, g.K, b_box))
             return cudaErrorInvalidValue;
+        if (mode == kGemmScaleSplit && !make_tmap(&prm.tmA2[q], g.A2, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
         prm.offsets[q] = g.offsets;
         prm.out[q] = g.out;
+        prm.out2[q] = g.out2;
         prm.row_scale[q] = g.row_scale;
         prm.G[q] = g.G;
         prm.M[q] = g.M;
@@ -586,6 +619,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         case kGemmSwiGLU: return launch_mode<kGemmSwiGLU>(prm, grid, s);
         case kGemmScale: return launch_mode<kGemmScale>(prm, grid, s);
         case kGemmPlain: return launch_mode<kGemmPlain>(prm, grid, s);
+        case kGemmScaleSplit: return launch_mode<kGemmScaleSplit>(prm, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }

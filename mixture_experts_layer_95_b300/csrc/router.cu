@@ -12,10 +12,10 @@
 // probability p_i) and the histogram of the chosen ids (for the grouping scan).
 //
 // Two kernels:
-//  * router_warp_kernel -- one warp per token, E <= 32 experts.  Each lane
-//    streams 16-byte vectors of x and of the E rows of W_g (which stay hot in
-//    L1 for small E*d), keeps E fp32 partial dots in registers and finishes
-//    them with butterfly shuffles; afterwards lane e owns expert e.
+//  * router_warp_kernel -- one warp per token, E <= 16 experts, W_g staged in
+//    shared memory.  Each lane streams 16-byte vectors of x, keeps E fp32
+//    partial dots in registers and finishes them with butterfly shuffles;
+//    afterwards lane e owns expert e.
 //  * router_logits_kernel -- softmax/top-k over fp32 logits produced by a
 //    tensor-core GEMM (large E); lane owns experts lane, lane+32, ...
 #include <float.h>
@@ -27,24 +27,6 @@ namespace {
 
 constexpr int kWarps = kRouterThreads / 32;
 constexpr int kTokensPerWarp = kRouterTokensPerBlock / kWarps;
-
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
-    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f = __bfloat1622float2(h[i]);
-        v[2 * i] = f.x;
-        v[2 * i + 1] = f.y;
-    }
-}
-
-__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
-    float4 a = __ldg(reinterpret_cast<const float4*>(p));
-    float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
 
 // Softmax, top-k and gate epilogue shared by both kernels.  Lane L holds the
 // logit (already including logit_bias) of experts L + 32*j in l[j]; absent
@@ -116,7 +98,7 @@ __device__ __forceinline__ void softmax_topk(int t, int E, int k, const float (&
 }
 
 // Writes the per-block partial sums of p and the per-block id histogram.
-template <int NJ>
+template <int NJ, int NW>
 __device__ __forceinline__ void block_epilogue(int E, const float (&psum)[NJ], const int (&hcnt)[NJ],
                                                float* p_part, int32_t* block_hist, float* s_p, int* s_h) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,7 +114,7 @@ __device__ __forceinline__ void block_epilogue(int E, const float (&psum)[NJ], c
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float ps = 0.f;
         int hs = 0;
-        for (int w = 0; w < kWarps; ++w) {  // fixed order: deterministic
+        for (int w = 0; w < NW; ++w) {  // fixed order: deterministic
             ps += s_p[w * E + e];
             hs += s_h[w * E + e];
         }
@@ -141,49 +123,95 @@ __device__ __forceinline__ void block_epilogue(int E, const float (&psum)[NJ], c
     }
 }
 
+// 16-byte vector of T: 8 bf16 or 4 fp32.
+template <typename T>
+struct Vec {
+    static constexpr int kElems = 16 / sizeof(T);
+};
+
+__device__ __forceinline__ void widen(const uint4& u, float (&v)[8], const __nv_bfloat16*) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ void widen(const uint4& u, float (&v)[4], const float*) {
+    v[0] = __uint_as_float(u.x);
+    v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z);
+    v[3] = __uint_as_float(u.w);
+}
+
+// Fused router for E <= NE.  W_g is copied once per block into shared memory
+// (rows E..NE-1 zero-filled, so the inner loop has no branches).  Each warp
+// owns kTpw consecutive tokens and works on all of them at once: every
+// 16-byte vector of W_g read from shared memory feeds kTpw tokens, and the x
+// vectors of all kTpw tokens are in flight together.  Lanes accumulate NE fp32
+// partial dots per token, finished with butterfly shuffles.
 template <typename T, int NE>
-__global__ void __launch_bounds__(kRouterThreads) router_warp_kernel(
+__global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
     int Tn, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ wg,
     const float* __restrict__ logit_bias, const float* __restrict__ select_bias, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
     int32_t* __restrict__ block_hist) {
-    __shared__ float s_p[kWarps * NE];
-    __shared__ int s_h[kWarps * NE];
+    constexpr int kW = kWarpRouterThreads / 32;
+    constexpr int kTpw = kRouterTokensPerBlock / kW;
+    constexpr int VE = Vec<T>::kElems;
+    extern __shared__ uint4 s_w[];  // [NE][d / VE] 16-byte vectors
+    __shared__ float s_p[kW * NE];
+    __shared__ int s_h[kW * NE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nv = d / VE;  // vectors per row
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(wg);
+        for (int i = threadIdx.x; i < NE * nv; i += blockDim.x)
+            s_w[i] = (i < E * nv) ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
+    const int t0 = blockIdx.x * kRouterTokensPerBlock + warp * kTpw;
+    const uint4* xr[kTpw];
+#pragma unroll
+    for (int q = 0; q < kTpw; ++q) {
+        const int t = t0 + q < Tn ? t0 + q : Tn - 1;  // clamp: rows past T are read but never used
+        xr[q] = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    }
+    float acc[kTpw][NE];
+#pragma unroll
+    for (int q = 0; q < kTpw; ++q)
+#pragma unroll
+        for (int e = 0; e < NE; ++e) acc[q][e] = 0.f;
+    for (int v = lane; v < nv; v += 32) {
+        float xv[kTpw][VE];
+#pragma unroll
+        for (int q = 0; q < kTpw; ++q) widen(__ldg(xr[q] + v), xv[q], static_cast<const T*>(nullptr));
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            float wv[VE];
+            widen(s_w[e * nv + v], wv, static_cast<const T*>(nullptr));
+#pragma unroll
+            for (int q = 0; q < kTpw; ++q)
+#pragma unroll
+                for (int i = 0; i < VE; ++i) acc[q][e] = fmaf(xv[q][i], wv[i], acc[q][e]);
+        }
+    }
     float psum[1] = {0.f};
     int hcnt[1] = {0};
-    for (int i = 0; i < kTokensPerWarp; ++i) {
-        const int t = blockIdx.x * kRouterTokensPerBlock + warp * kTokensPerWarp + i;
-        if (t >= Tn) break;  // warp-uniform
-        const T* xr = x + (size_t)t * d;
-        float acc[NE];
 #pragma unroll
-        for (int e = 0; e < NE; ++e) acc[e] = 0.f;
-#pragma unroll 2
-        for (int c = lane * 8; c < d; c += 256) {
-            float xv[8];
-            load8(xr + c, xv);
-#pragma unroll
-            for (int e = 0; e < NE; ++e) {
-                if (e < E) {
-                    float wv[8];
-                    load8(wg + (size_t)e * d + c, wv);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[e] = fmaf(xv[q], wv[q], acc[e]);
-                }
-            }
-        }
+    for (int q = 0; q < kTpw; ++q) {
+        if (t0 + q >= Tn) break;  // warp-uniform
         float l[1] = {-FLT_MAX};
 #pragma unroll
         for (int e = 0; e < NE; ++e) {
-            if (e < E) {
-                const float v = warp_sum(acc[e]);
-                if (lane == e) l[0] = v + (logit_bias ? __ldg(logit_bias + e) : 0.f);
-            }
+            const float v = warp_sum(acc[q][e]);
+            if (lane == e && e < E) l[0] = v + (logit_bias ? __ldg(logit_bias + e) : 0.f);
         }
-        softmax_topk<1>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
+        softmax_topk<1>(t0 + q, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
     }
-    block_epilogue<1>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
+    block_epilogue<1, kW>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
 }
 
 template <int NJ>
@@ -213,7 +241,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
         }
         softmax_topk<NJ>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
     }
-    block_epilogue<NJ>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
+    block_epilogue<NJ, kWarps>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
 }
 
 __global__ void p_mean_kernel(int Tn, int E, int nblk, const float* __restrict__ p_part, float* __restrict__ p_mean) {
@@ -232,19 +260,25 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
                                cudaStream_t s) {
     const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
     if (nblk == 0) return cudaSuccess;
-    const dim3 grid(nblk), block(kRouterThreads);
-#define MOE_ROUTER_CASE(TY, NE)                                                                              \
-    router_warp_kernel<TY, NE><<<grid, block, 0, s>>>(T, d, E, k, static_cast<const TY*>(x),                \
-                                                      static_cast<const TY*>(w_gate), logit_bias, select_bias, \
-                                                      renormalize, topk_ids, gates, p_part, block_hist)
+    const int ne = warp_router_width(E);
+    const size_t smem = warp_router_smem_bytes(E, d, dtype);
+    const dim3 grid(nblk), block(kWarpRouterThreads);
+#define MOE_ROUTER_CASE(TY, NE)                                                                                 \
+    do {                                                                                                        \
+        cudaError_t e_ = cudaFuncSetAttribute(router_warp_kernel<TY, NE>,                                       \
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);          \
+        if (e_ != cudaSuccess) return e_;                                                                       \
+        router_warp_kernel<TY, NE><<<grid, block, smem, s>>>(T, d, E, k, static_cast<const TY*>(x),           \
+                                                             static_cast<const TY*>(w_gate), logit_bias,       \
+                                                             select_bias, renormalize, topk_ids, gates, p_part, \
+                                                             block_hist);                                       \
+    } while (0)
     if (dtype == MOE_BF16) {
-        if (E <= 8) MOE_ROUTER_CASE(__nv_bfloat16, 8);
-        else if (E <= 16) MOE_ROUTER_CASE(__nv_bfloat16, 16);
-        else MOE_ROUTER_CASE(__nv_bfloat16, 32);
+        if (ne == 8) MOE_ROUTER_CASE(__nv_bfloat16, 8);
+        else MOE_ROUTER_CASE(__nv_bfloat16, 16);
     } else {
-        if (E <= 8) MOE_ROUTER_CASE(float, 8);
-        else if (E <= 16) MOE_ROUTER_CASE(float, 16);
-        else MOE_ROUTER_CASE(float, 32);
+        if (ne == 8) MOE_ROUTER_CASE(float, 8);
+        else MOE_ROUTER_CASE(float, 16);
     }
 #undef MOE_ROUTER_CASE
     return cudaGetLastError();

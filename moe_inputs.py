@@ -48,6 +48,7 @@ class Workload:
     alpha: float = 0.01
     select_bias: bool = False    # draw a selection-only bias ~ U(-0.1, 0.1)
     zipf_s: float = 0.0          # > 0: add Zipf(s) log-probabilities to the logits
+    h_split: bool = False        # layer option: keep H as a hi + lo bf16 pair
     seed: int = 0
     notes: str = field(default="", compare=False)
 
@@ -66,10 +67,16 @@ WORKLOADS = {
     "mixtral_decode_t8": Workload("mixtral_decode_t8", T=8, d=4096, E=8, F=14336, k=2),
     "mixtral_decode_t32": Workload("mixtral_decode_t32", T=32, d=4096, E=8, F=14336, k=2),
     "mixtral_decode_t128": Workload("mixtral_decode_t128", T=128, d=4096, E=8, F=14336, k=2),
+    # same expert shapes and tokens per expert as mixtral_prefill at half the
+    # memory (4 experts, 2048 tokens): the case profiled with ncu --set full
+    "mixtral_prefill_e4": Workload("mixtral_prefill_e4", T=2048, d=4096, E=4, F=14336, k=2),
     "deepseek_v3": Workload("deepseek_v3", T=8192, d=7168, E=256, F=2048, k=8, n_shared=1, F_s=2048,
                             select_bias=True),
+    # the capacity cut leaves most tokens with small outputs and a few with
+    # outputs ~12x RMS(y); a bf16 H then costs ~2% of RMS(y) at those tokens,
+    # so this layer keeps H as a hi + lo pair
     "skewed_capacity": Workload("skewed_capacity", T=16384, d=2048, E=64, F=1408, k=2,
-                                capacity=_cap(16384, 2, 64), zipf_s=1.2),
+                                capacity=_cap(16384, 2, 64), zipf_s=1.2, h_split=True),
 }
 
 

@@ -20,7 +20,10 @@ SMALL = [
     Workload("small_bf16", T=300, d=512, E=8, F=384, k=2),
     Workload("ragged_bf16", T=77, d=264, E=6, F=200, k=3),
     Workload("ragged_f32", T=77, d=264, E=6, F=200, k=3, dtype="f32"),
-    Workload("gemm_router_capacity_zipf_bf16", T=520, d=384, E=64, F=256, k=4, capacity=40, zipf_s=1.2),
+    Workload("gemm_router_capacity_zipf_bf16", T=520, d=384, E=64, F=256, k=4, capacity=40, zipf_s=1.2,
+             h_split=True),
+    Workload("split_h_shared_ragged_bf16", T=150, d=264, E=6, F=200, k=2, n_shared=1, F_s=136, capacity=30,
+             h_split=True),
     Workload("gemm_router_f32", T=150, d=128, E=20, F=96, k=3, dtype="f32"),
     Workload("shared_selectbias_bf16", T=200, d=256, E=32, F=128, k=8, n_shared=1, F_s=192, select_bias=True),
     Workload("dense_limit_bf16", T=64, d=128, E=8, F=128, k=8, renormalize=False),
