@@ -24,10 +24,75 @@ size_t esize(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
 
 bool use_h_split(const moe_config& c) { return c.dtype == MOE_BF16 && c.h_split == 1; }
 
+// ---- split-K for decode-sized batches ----------------------------------------
+// When a grouped GEMM has too few output tiles to keep every SM streaming
+// weights, each tile's K range is split into S slices (fp32 partials, summed
+// in slice order afterwards).  S is a function of the configuration only (a
+// nominal 148-SM B300), so the workspace size does not depend on the device.
+constexpr int kNominalSms = 148;
+constexpr int kMaxKSplit = 16;
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Smallest S whose waves are >= 90% full, else the fullest; 1 when the tile
+// list already covers several waves.  max_s bounds S so that the slices'
+// fp32 traffic stays small next to the weight bytes the split helps stream.
+int choose_ksplit(long long est_tiles, int nk, long long max_s) {
+    if (est_tiles <= 0 || est_tiles >= 4LL * kNominalSms || max_s < 2) return 1;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int S = 1; S <= kMaxKSplit && S <= nk && S <= max_s; ++S) {
+        const long long units = est_tiles * S;
+        const double eff = (double)units / ((double)ceil_div(units, kNominalSms) * kNominalSms);
+        if (eff >= 0.9) return S;
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = S;
+        }
+    }
+    return best;
+}
+
+struct Splits {
+    int up = 1, down = 1;
+};
+
+// Tiles a grouped GEMM will have at least: every touched expert owns one or
+// more 128-row tiles.
+long long est_row_tiles(const moe_config& c) {
+    const long long n = (long long)c.T * c.k;
+    const long long touched = n < c.E ? n : c.E;
+    const long long by_rows = ceil_div(n, 128);
+    return by_rows > touched ? by_rows : touched;
+}
+
+Splits choose_splits(const moe_config& c) {
+    Splits sp;
+    if (c.dtype != MOE_BF16 || c.T == 0) return sp;
+    const long long rt = est_row_tiles(c);
+    const long long st = c.n_shared ? ceil_div(c.T, 128) : 0;
+    const long long up = rt * ceil_div(c.d_ff, 128) + st * (c.n_shared ? ceil_div(c.d_ff_shared, 128) : 0);
+    const long long dn = (rt + st) * ceil_div(c.d, 256);
+    int nk_up = ceil_div(c.d, 64);
+    int nk_dn = ceil_div(c.d_ff, 64);
+    if (c.n_shared) nk_dn = nk_dn < ceil_div(c.d_ff_shared, 64) ? nk_dn : ceil_div(c.d_ff_shared, 64);
+    // bytes: weights streamed vs one slice's fp32 partials written and read back
+    const long long n = (long long)c.T * c.k;
+    const long long touched = n < c.E ? n : c.E;
+    const long long w_up = touched * 2LL * c.d_ff * c.d * 2 + (long long)c.n_shared * 2LL * c.d_ff_shared * c.d * 2;
+    const long long p_up = 8LL * (n * 2 * c.d_ff + (long long)c.n_shared * c.T * 2 * c.d_ff_shared);
+    const long long w_dn = touched * (long long)c.d * c.d_ff * 2 + (long long)c.n_shared * c.d * c.d_ff_shared * 2;
+    const long long p_dn = 8LL * (n + (long long)c.n_shared * c.T) * c.d;
+    sp.up = choose_ksplit(up, nk_up, w_up / (10 * p_up));
+    sp.down = choose_ksplit(dn, nk_dn, w_dn / (10 * p_dn));
+    return sp;
+}
+
 // Byte offsets of every workspace region; `total` is the size.
 struct Layout {
     size_t status, topk_ids, gates, p_part, block_hist, counts, kept, offsets, n_dropped, sorted, slot_pos,
-        gates_perm, p_mean, f, L, logits, x_perm, h, h_shared, h_lo, h_shared_lo, y_perm, y_shared, total;
+        gates_perm, p_mean, f, L, logits, x_perm, h, h_shared, h_lo, h_shared_lo, y_perm, y_shared, part_up,
+        part_up_shared, part_dn, part_dn_shared, total;
 };
 
 Layout layout(const moe_config& c) {
@@ -65,6 +130,12 @@ Layout layout(const moe_config& c) {
     l.h_shared_lo = take(split && c.n_shared ? (size_t)c.T * c.d_ff_shared * esize(c) : 0);
     l.y_perm = take(4 * n * c.d);
     l.y_shared = take(c.n_shared ? 4 * (size_t)c.T * c.d : 0);
+    const Splits sp = choose_splits(c);
+    const size_t su = sp.up > 1 ? sp.up : 0, sd = sp.down > 1 ? sp.down : 0;
+    l.part_up = take(4 * su * n * 2 * c.d_ff);
+    l.part_up_shared = take(c.n_shared ? 4 * su * (size_t)c.T * 2 * c.d_ff_shared : 0);
+    l.part_dn = take(4 * sd * n * c.d);
+    l.part_dn_shared = take(c.n_shared ? 4 * sd * (size_t)c.T * c.d : 0);
     l.total = off;
     return l;
 }
@@ -189,10 +260,14 @@ int enqueue_route(const moe_config& c, const Layout& L, void* ws, const void* x,
     return MOE_OK;
 }
 
+// Both expert GEMMs.  With split-K on the down GEMM, reduce_down = true sums
+// the slices into y_perm / y_shared (moe_expert_ffn); otherwise the slices are
+// left in the workspace for the split-aware combine (moe_forward).
 int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_perm, const int32_t* offsets,
                 const float* gates_perm, const void* w1, const void* w3, const void* w2, const void* x,
                 const void* ws1, const void* ws3, const void* ws2, float* y_perm, float* y_shared, int sms,
-                cudaStream_t s) {
+                cudaStream_t s, bool reduce_down) {
+    const Splits sp = choose_splits(c);
     const int n = c.T * c.k;
     void* h = at<void>(ws, L.h);
     void* hs = at<void>(ws, L.h_shared);
@@ -243,20 +318,40 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
         down[1].out = y_shared;
         np = 2;
     }
+    if (sp.up > 1) {
+        up[0].part = at<float>(ws, L.part_up);
+        up[1].part = at<float>(ws, L.part_up_shared);
+    }
+    if (sp.down > 1) {
+        down[0].part = at<float>(ws, L.part_dn);
+        down[1].part = at<float>(ws, L.part_dn_shared);
+    }
     int* status = at<int>(ws, L.status);
     {
         StageScope scope(kStageUp, s);
-        if (c.dtype == MOE_BF16)
-            MOE_LAUNCH(launch_gemm_tc(kGemmSwiGLU, up, np, status, sms, s));
-        else
+        if (c.dtype == MOE_BF16) {
+            MOE_LAUNCH(launch_gemm_tc(kGemmSwiGLU, up, np, status, sms, s, sp.up));
+            if (sp.up > 1) {
+                MOE_LAUNCH(launch_swiglu_finalize(n, offsets + c.E, c.d_ff, sp.up, up[0].part, h, h_lo, s));
+                if (c.n_shared)
+                    MOE_LAUNCH(launch_swiglu_finalize(c.T, nullptr, c.d_ff_shared, sp.up, up[1].part, hs, hs_lo, s));
+            }
+        } else {
             MOE_LAUNCH(launch_gemm_simt_f32(kGemmSwiGLU, up, np, s));
+        }
     }
     {
         StageScope scope(kStageDown, s);
-        if (c.dtype == MOE_BF16)
-            MOE_LAUNCH(launch_gemm_tc(split ? kGemmScaleSplit : kGemmScale, down, np, status, sms, s));
-        else
+        if (c.dtype == MOE_BF16) {
+            MOE_LAUNCH(launch_gemm_tc(split ? kGemmScaleSplit : kGemmScale, down, np, status, sms, s, sp.down));
+            if (sp.down > 1 && reduce_down) {
+                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
+                if (c.n_shared)
+                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s));
+            }
+        } else {
             MOE_LAUNCH(launch_gemm_simt_f32(kGemmScale, down, np, s));
+        }
     }
     return MOE_OK;
 }
@@ -357,7 +452,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* off
     MOE_TRY(device_sms(&sms));
     const Layout L = layout(c);
     return enqueue_ffn(c, L, ws, x_perm, offsets, gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared, sms,
-                       reinterpret_cast<cudaStream_t>(stream));
+                       reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 int moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_pos, const float* y_shared, void* y,
@@ -447,11 +542,24 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
     float* y_perm = at<float>(ws, L.y_perm);
     float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
     MOE_TRY(enqueue_ffn(c, L, ws, x_perm, o.offsets, o.gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared,
-                        sms, s));
+                        sms, s, false));
 
-    // 6: combine
+    // 6: combine (straight from the down GEMM's split-K slices when it was split)
+    const Splits sp = choose_splits(c);
+    const float* yp = y_perm;
+    const float* ys = y_shared;
+    size_t yp_stride = 0, ys_stride = 0;
+    if (sp.down > 1) {
+        yp = at<float>(ws, L.part_dn);
+        yp_stride = (size_t)c.T * c.k * c.d;
+        if (c.n_shared) {
+            ys = at<float>(ws, L.part_dn_shared);
+            ys_stride = (size_t)c.T * c.d;
+        }
+    }
     StageScope scope(kStageCombine, s);
-    MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, c.k, y_perm, o.slot_pos, y_shared, y, s));
+    MOE_LAUNCH(launch_combine_split(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, c.k, yp, yp_stride, sp.down, o.slot_pos,
+                                    ys, ys_stride, sp.down, y, s));
     return MOE_OK;
 }
 

@@ -37,40 +37,115 @@ __device__ __forceinline__ void add4(float4& a, const float4& b) {
     a.w += b.w;
 }
 
-// One warp per token.  Lane j < k holds slot_pos[t][j] (k <= 32) and
-// broadcasts it; every lane then sums 8 consecutive columns per step (two
-// 16-byte loads per row, all rows' loads issued before the adds) in the
-// fixed order j = 0..k-1, then the shared row.
+// One warp per (token, 256-column chunk), so that even a single token is
+// spread over d/256 warps.  Lane j < k holds slot_pos[t][j] (k <= 32) and
+// broadcasts it; each lane owns 8 consecutive columns.  Rows of y_perm (and
+// y_shared) may be split into `nsplit` fp32 slices `stride` elements apart:
+// each entry's slices are summed in slice order first, then the entries in
+// fixed j order, then the shared row -- the same order in which a reduction
+// of the slices followed by the plain combine adds them.
 template <typename T>
 __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, const float* __restrict__ y_perm,
+                                                      size_t perm_stride, int nsplit,
                                                       const int32_t* __restrict__ slot_pos,
-                                                      const float* __restrict__ y_shared, T* __restrict__ y) {
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+                                                      const float* __restrict__ y_shared, size_t shared_stride,
+                                                      int shared_nsplit, T* __restrict__ y) {
+    const int chunks = (d + 255) / 256;
+    const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (t >= Tn) return;
+    if (item >= Tn * chunks) return;
+    const int t = item / chunks;
+    const int c = (item - t * chunks) * 256 + lane * 8;
+    const bool active = c < d;  // d is a multiple of 8: an active lane owns 8 columns
     const int my_pos = lane < k ? __ldg(slot_pos + (size_t)t * k + lane) : -1;
-    // the loop bound is the same for every lane, so the shuffles below always
-    // run with the whole warp; lanes past the row end skip only the memory work
-    for (int c0 = 0; c0 < d; c0 += 256) {
-        const int c = c0 + lane * 8;
-        const bool active = c < d;  // d is a multiple of 8: an active lane owns 8 columns
-        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-        for (int j = 0; j < k; ++j) {
-            const int pos = __shfl_sync(0xffffffffu, my_pos, j);
-            if (pos < 0 || !active) continue;
-            const float4* src = reinterpret_cast<const float4*>(y_perm + (size_t)pos * d + c);
-            add4(a0, __ldg(src));
-            add4(a1, __ldg(src + 1));
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    for (int j = 0; j < k; ++j) {
+        const int pos = __shfl_sync(0xffffffffu, my_pos, j);
+        if (pos < 0 || !active) continue;
+        const float4* src = reinterpret_cast<const float4*>(y_perm + (size_t)pos * d + c);
+        float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+        for (int sl = 1; sl < nsplit; ++sl) {
+            const float4* q = reinterpret_cast<const float4*>(y_perm + sl * perm_stride + (size_t)pos * d + c);
+            add4(p0, __ldg(q));
+            add4(p1, __ldg(q + 1));
         }
-        if (!active) continue;
-        if (y_shared) {
-            const float4* src = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
-            add4(a0, __ldg(src));
-            add4(a1, __ldg(src + 1));
-        }
-        store4<T>(y + (size_t)t * d + c, a0);
-        store4<T>(y + (size_t)t * d + c + 4, a1);
+        add4(a0, p0);
+        add4(a1, p1);
     }
+    if (!active) return;
+    if (y_shared) {
+        const float4* src = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
+        float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+        for (int sl = 1; sl < shared_nsplit; ++sl) {
+            const float4* q = reinterpret_cast<const float4*>(y_shared + sl * shared_stride + (size_t)t * d + c);
+            add4(p0, __ldg(q));
+            add4(p1, __ldg(q + 1));
+        }
+        add4(a0, p0);
+        add4(a1, p1);
+    }
+    store4<T>(y + (size_t)t * d + c, a0);
+    store4<T>(y + (size_t)t * d + c + 4, a1);
+}
+
+// SwiGLU over split-K partials of the up GEMM: one thread per 4 columns.
+__global__ void __launch_bounds__(256) swiglu_finalize_kernel(int rows_max, const int32_t* __restrict__ rows_dev,
+                                                              int N, int ksplit, const float* __restrict__ part,
+                                                              __nv_bfloat16* __restrict__ h,
+                                                              __nv_bfloat16* __restrict__ h_lo) {
+    const int rows = rows_dev ? min(*rows_dev, rows_max) : rows_max;
+    const size_t stride = (size_t)rows_max * 2 * N;
+    const int q4 = N / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)rows * q4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / q4;
+        const int f = (int)(i - r * q4) * 4;
+        const float* gp = part + r * 2 * N + f;
+        float4 g = __ldg(reinterpret_cast<const float4*>(gp));
+        float4 u = __ldg(reinterpret_cast<const float4*>(gp + N));
+        for (int sl = 1; sl < ksplit; ++sl) {
+            add4(g, __ldg(reinterpret_cast<const float4*>(gp + sl * stride)));
+            add4(u, __ldg(reinterpret_cast<const float4*>(gp + sl * stride + N)));
+        }
+        const float hv[4] = {g.x / (1.0f + __expf(-g.x)) * u.x, g.y / (1.0f + __expf(-g.y)) * u.y,
+                             g.z / (1.0f + __expf(-g.z)) * u.z, g.w / (1.0f + __expf(-g.w)) * u.w};
+        __nv_bfloat162 a = __floats2bfloat162_rn(hv[0], hv[1]);
+        __nv_bfloat162 b = __floats2bfloat162_rn(hv[2], hv[3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&a);
+        pk.y = *reinterpret_cast<uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(h + r * N + f) = pk;
+        if (h_lo) {
+            const float2 ba = __bfloat1622float2(a), bb = __bfloat1622float2(b);
+            __nv_bfloat162 la = __floats2bfloat162_rn(hv[0] - ba.x, hv[1] - ba.y);
+            __nv_bfloat162 lb = __floats2bfloat162_rn(hv[2] - bb.x, hv[3] - bb.y);
+            pk.x = *reinterpret_cast<uint32_t*>(&la);
+            pk.y = *reinterpret_cast<uint32_t*>(&lb);
+            *reinterpret_cast<uint2*>(h_lo + r * N + f) = pk;
+        }
+    }
+}
+
+// out[r][c] = sum over slices of part[s][r][c], slices in order.
+__global__ void __launch_bounds__(256) reduce_partials_kernel(int rows_max, const int32_t* __restrict__ rows_dev,
+                                                              int N, int ksplit, const float* __restrict__ part,
+                                                              float* __restrict__ out) {
+    const int rows = rows_dev ? min(*rows_dev, rows_max) : rows_max;
+    const size_t stride = (size_t)rows_max * N;
+    const int q4 = N / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)rows * q4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / q4;
+        const int c = (int)(i - r * q4) * 4;
+        float4 acc = __ldg(reinterpret_cast<const float4*>(part + r * N + c));
+        for (int sl = 1; sl < ksplit; ++sl) add4(acc, __ldg(reinterpret_cast<const float4*>(part + sl * stride + r * N + c)));
+        *reinterpret_cast<float4*>(out + r * N + c) = acc;
+    }
+}
+
+int grid_for(size_t work, int per_block) {
+    const size_t b = (work + per_block - 1) / per_block;
+    return (int)(b < 148 * 16 ? (b > 0 ? b : 1) : 148 * 16);
 }
 
 __global__ void load_stats_kernel(int Tn, int E, int k, float alpha, const int32_t* __restrict__ counts,
@@ -93,15 +168,40 @@ __global__ void load_stats_kernel(int Tn, int E, int k, float alpha, const int32
 
 }  // namespace
 
-cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, const int32_t* slot_pos,
-                           const float* y_shared, void* y, cudaStream_t s) {
+cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_perm, size_t perm_stride,
+                                 int nsplit, const int32_t* slot_pos, const float* y_shared, size_t shared_stride,
+                                 int shared_nsplit, void* y, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const int grid = (T + 7) / 8;
+    const long long warps = (long long)T * ((d + 255) / 256);
+    const int grid = (int)((warps + 7) / 8);
     if (dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(T, d, k, y_perm, slot_pos, y_shared,
+        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
+                                                           shared_stride, shared_nsplit,
                                                            static_cast<__nv_bfloat16*>(y));
     else
-        combine_kernel<float><<<grid, 256, 0, s>>>(T, d, k, y_perm, slot_pos, y_shared, static_cast<float*>(y));
+        combine_kernel<float><<<grid, 256, 0, s>>>(T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
+                                                   shared_stride, shared_nsplit, static_cast<float*>(y));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, const int32_t* slot_pos,
+                           const float* y_shared, void* y, cudaStream_t s) {
+    return launch_combine_split(dtype, T, d, k, y_perm, 0, 1, slot_pos, y_shared, 0, 1, y, s);
+}
+
+cudaError_t launch_swiglu_finalize(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
+                                   void* h, void* h_lo, cudaStream_t s) {
+    if (rows_max == 0) return cudaSuccess;
+    swiglu_finalize_kernel<<<grid_for((size_t)rows_max * (N / 4), 256), 256, 0, s>>>(
+        rows_max, rows_dev, N, ksplit, part, static_cast<__nv_bfloat16*>(h), static_cast<__nv_bfloat16*>(h_lo));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_partials(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
+                                   float* out, cudaStream_t s) {
+    if (rows_max == 0) return cudaSuccess;
+    reduce_partials_kernel<<<grid_for((size_t)rows_max * (N / 4), 256), 256, 0, s>>>(rows_max, rows_dev, N, ksplit,
+                                                                                     part, out);
     return cudaGetLastError();
 }
 

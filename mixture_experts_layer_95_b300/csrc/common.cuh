@@ -173,12 +173,30 @@ struct GemmProblem {
     const float* row_scale;
     const void* A2;       // kGemmScaleSplit: the lo half of A, same layout
     void* out2;           // kGemmSwiGLU: optional lo half of H (H - bf16(H)), same layout as out
+    float* part;          // split-K: fp32 partials [ksplit][a_rows][2N (SwiGLU) or N]
 };
 
 // Tensor-core (tcgen05) path, bf16 operands, fp32 accumulate.  Runs up to two
 // problems (a routed one and a shared-expert one) in one persistent launch.
+// ksplit > 1 splits every tile's K range into ksplit slices that write fp32
+// partials to GemmProblem::part instead of `out` (finish with
+// launch_swiglu_finalize or the split-aware combine / reduce).
 cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
-                           cudaStream_t s);
+                           cudaStream_t s, int ksplit = 1);
+
+// H[r][f] = silu(sum_s P[s][r][f]) * sum_s P[s][r][N + f] (bf16, and the lo
+// half when h_lo != nullptr) for r < rows, rows = *rows_dev when non-null.
+cudaError_t launch_swiglu_finalize(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
+                                   void* h, void* h_lo, cudaStream_t s);
+
+// out[r][c] = sum_s P[s][r][c] (fp32) for r < rows (rows_dev as above).
+cudaError_t launch_reduce_partials(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
+                                   float* out, cudaStream_t s);
+
+// Combine over split-K partials: y[t] = sum_j (sum_s Yp[s][pos_j]) + sum_s Ys[s][t].
+cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_perm, size_t perm_stride,
+                                 int nsplit, const int32_t* slot_pos, const float* y_shared, size_t shared_stride,
+                                 int shared_nsplit, void* y, cudaStream_t s);
 
 // CUDA-core fp32 path with the same semantics (dtype MOE_F32).
 cudaError_t launch_gemm_simt_f32(int mode, const GemmProblem* probs, int nprob, cudaStream_t s);

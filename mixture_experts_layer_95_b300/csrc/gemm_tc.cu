@@ -72,6 +72,9 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     const float* row_scale[2];
     int G[2], M[2], N[2], K[2], a_rows[2];
     int nprob;
+    int ksplit;                // K slices per tile (1: no split)
+    float* part[2];            // ksplit > 1: fp32 partials [ksplit][a_rows][part_cols]
+    int part_cols[2];          // 2N for SwiGLU (gate half, then up half), N otherwise
     int* status;
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
     int stall_producer;      // test switch: issue no loads, so the consumers' bounded waits run out
@@ -221,6 +224,7 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 struct Tile {
     int prob, g, m, n;
     int a_row0, rows_valid;
+    int ks, kb0, kb1;  // K slice and its k-block range [kb0, kb1)
 };
 
 template <int MODE>
@@ -243,11 +247,16 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& 
     t.g = lo;
     const int rows = st.rows[t.prob][lo];
     const int mt = (rows + BM - 1) / BM;
-    const int r = local - ts[lo];
+    int r = local - ts[lo];
+    t.ks = r % p.ksplit;  // K slices of one output tile are adjacent in the list
+    r /= p.ksplit;
     t.n = r / mt;
     t.m = r - t.n * mt;
     t.a_row0 = st.row0[t.prob][lo] + t.m * BM;
     t.rows_valid = min(BM, rows - t.m * BM);
+    const int nk = (p.K[t.prob] + BK - 1) / BK;
+    t.kb0 = t.ks * nk / p.ksplit;
+    t.kb1 = (t.ks + 1) * nk / p.ksplit;
     return t;
 }
 
@@ -255,8 +264,52 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& 
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
+// Split-K epilogue: the raw fp32 accumulator of this K slice goes to the
+// partial buffer (scaled by the row's gate in the scale modes); a later pass
+// sums the slices in slice order.  For SwiGLU the gate half lands in columns
+// [0, N) and the up half in [N, 2N).
+template <int MODE>
+__device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile) {
+    const int N = p.N[t.prob];
+    const bool valid = row_in_tile < t.rows_valid;
+    const size_t grow = static_cast<size_t>(t.a_row0 + row_in_tile);
+    const size_t pc = static_cast<size_t>(p.part_cols[t.prob]);
+    float* base = p.part[t.prob] + (static_cast<size_t>(t.ks) * p.a_rows[t.prob] + grow) * pc;
+    float scale = 1.0f;
+    if ((MODE == kGemmScale || MODE == kGemmScaleSplit) && valid && p.row_scale[t.prob] != nullptr)
+        scale = __ldg(p.row_scale[t.prob] + grow);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(tacc + c0, v);
+        tmem_ld_wait();
+        int col;
+        if (MODE == kGemmSwiGLU)
+            col = (c0 < BN / 2) ? t.n * (BN / 2) + c0 : N + t.n * (BN / 2) + (c0 - BN / 2);
+        else
+            col = t.n * BN + c0;
+        const int lim = (MODE == kGemmSwiGLU && c0 >= BN / 2) ? 2 * N : N;
+        if (!valid || col >= lim) continue;
+        float* dst = base + col;
+        if (col + 32 <= lim) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(dst)[q] =
+                    make_float4(scale * __uint_as_float(v[4 * q]), scale * __uint_as_float(v[4 * q + 1]),
+                                scale * __uint_as_float(v[4 * q + 2]), scale * __uint_as_float(v[4 * q + 3]));
+        } else {
+            for (int i = 0; i < 32 && col + i < lim; ++i) dst[i] = scale * __uint_as_float(v[i]);
+        }
+    }
+}
+
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile) {
+    if (p.ksplit > 1) {
+        epilogue_partial<MODE>(p, t, tacc, row_in_tile);
+        return;
+    }
     const int N = p.N[t.prob];
     const bool valid = row_in_tile < t.rows_valid;
     const size_t grow = static_cast<size_t>(t.a_row0 + row_in_tile);
@@ -390,7 +443,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                         }
                         st.row0[q][g] = lo;
                         st.rows[q][g] = hi - lo;
-                        tiles = ((hi - lo + BM - 1) / BM) * ncb;
+                        tiles = ((hi - lo + BM - 1) / BM) * ncb * p.ksplit;
                     }
                     int incl = tiles;
 #pragma unroll
@@ -422,10 +475,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
             bool dead = p.stall_producer != 0;
             for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
                 const Tile t = decode_tile<MODE>(st, p, id);
-                const int K = p.K[t.prob];
-                const int nk = (K + BK - 1) / BK;
                 const int b_row0 = t.g * p.N[t.prob] + t.n * out_cols_per_tile<MODE>();
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
                         dead = true;
                         break;
@@ -464,13 +515,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
             bool dead = false;
             for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x, ++it) {
                 const Tile t = decode_tile<MODE>(st, p, id);
-                const int nk = (p.K[t.prob] + BK - 1) / BK;
                 const int acc = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
                 if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
                 tc_fence_after();
                 const uint32_t dtm = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(&st.full[s], ph, abort_flag, p.status, p.wait_limit_ns)) {
                         dead = true;
                         break;
@@ -481,7 +531,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t bdesc = sdesc_k_sw128(sb + kk * UMMA_K * 2);
-                        umma_bf16(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2), bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_bf16(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2), bdesc, idesc,
+                                  (kb != t.kb0 || kk != 0) ? 1u : 0u);
                         if (SC::kSplit) umma_bf16(dtm, sdesc_k_sw128(sa + A_BYTES + kk * UMMA_K * 2), bdesc, idesc, 1u);
                     }
                     umma_commit(&st.empty[s]);
@@ -580,10 +631,11 @@ cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
-                           cudaStream_t s) {
-    if (nprob < 1 || nprob > 2) return cudaErrorInvalidValue;
+                           cudaStream_t s, int ksplit) {
+    if (nprob < 1 || nprob > 2 || ksplit < 1) return cudaErrorInvalidValue;
     TcParams prm;
     memset(&prm, 0, sizeof(prm));
+    prm.ksplit = ksplit;
     const int b_box = (mode == kGemmSwiGLU) ? BN / 2 : BN;
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
@@ -593,6 +645,12 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         if (mode == kGemmSwiGLU && !make_tmap(&prm.tmB2[q], g.B2, g.G * g.N, g.K, b_box))
             return cudaErrorInvalidValue;
         if (mode == kGemmScaleSplit && !make_tmap(&prm.tmA2[q], g.A2, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
+        if (ksplit > 1) {
+            // every slice needs at least one k-block
+            if (ksplit > (g.K + BK - 1) / BK || g.part == nullptr) return cudaErrorInvalidValue;
+            prm.part[q] = g.part;
+            prm.part_cols[q] = mode == kGemmSwiGLU ? 2 * g.N : g.N;
+        }
         prm.offsets[q] = g.offsets;
         prm.out[q] = g.out;
         prm.out2[q] = g.out2;

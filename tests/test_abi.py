@@ -72,10 +72,23 @@ def test_workspace_size_validation(lib):
 
 
 def test_workspace_grows_with_tokens_and_shared_expert(lib):
-    a = lib.moe_workspace_size(ctypes.byref(_cfg(T=16)))
-    b = lib.moe_workspace_size(ctypes.byref(_cfg(T=1600)))
-    c = lib.moe_workspace_size(ctypes.byref(_cfg(T=1600, n_shared=1, d_ff_shared=32)))
+    # large batches (no split-K slices in the workspace)
+    a = lib.moe_workspace_size(ctypes.byref(_cfg(T=16000)))
+    b = lib.moe_workspace_size(ctypes.byref(_cfg(T=32000)))
+    c = lib.moe_workspace_size(ctypes.byref(_cfg(T=32000, n_shared=1, d_ff_shared=32)))
     assert a < b < c
+
+
+def test_decode_sized_batches_reserve_split_k_slices(lib):
+    """A one-token batch cannot fill the SMs with output tiles, so the expert
+    GEMMs split K and the workspace holds their fp32 partial slices."""
+    one = moe.Layer(T=1, d=4096, E=8, k=2, d_ff=14336).cfg()
+    n, d, F = 2, 4096, 14336
+    plain = 4 * n * (d + 2 + 2 + 3 + 1) + 2 * n * (d + F)  # rough lower bound without slices
+    assert lib.moe_workspace_size(ctypes.byref(one)) > plain + 4 * n * (2 * F + d)
+
+
+def test_bf16_workspace_is_smaller_than_fp32(lib):
     # bf16 activations take half the bytes of fp32 in the large regions
     f32 = moe.Layer(T=4096, d=1024, E=8, k=2, d_ff=2048, dtype="f32").cfg()
     bf = moe.Layer(T=4096, d=1024, E=8, k=2, d_ff=2048, dtype="bf16").cfg()

@@ -30,6 +30,10 @@ SMALL = [
     Workload("single_expert_bf16", T=130, d=128, E=1, F=256, k=1),
     Workload("capacity_zero_shared_bf16", T=40, d=128, E=4, F=64, k=2, capacity=0, n_shared=1, F_s=64),
     Workload("decode_like_t1_bf16", T=1, d=512, E=8, F=512, k=2),
+    # a few tokens: the expert GEMMs split K into fp32 slices (shared expert,
+    # ragged F and the hi + lo H included)
+    Workload("split_k_shared_t3_bf16", T=3, d=256, E=16, F=320, k=2, n_shared=1, F_s=192, select_bias=True,
+             h_split=True),
     Workload("decode_like_t5_bf16", T=5, d=512, E=8, F=512, k=2),
     Workload("many_tiles_bf16", T=1000, d=256, E=4, F=640, k=2),
 ]
