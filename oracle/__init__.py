@@ -53,8 +53,9 @@ def _L():
         _lib.oracle_group.argtypes = [ip, ip, ip, ip, vp, vp, vp, vp, vp, vp, vp, vp]
         _lib.oracle_layer_tokens.argtypes = [ip] * 8 + [vp] * 11 + [ip, vp]
         _lib.oracle_load_stats.argtypes = [ip, ip, ip, vp, vp, ctypes.c_double, vp, vp, vp]
+        _lib.oracle_bias_update.argtypes = [ip, ip, ip, vp, ctypes.c_double, vp, vp]
         for f in ("oracle_route", "oracle_gates_for_ids", "oracle_group", "oracle_layer_tokens",
-                  "oracle_load_stats", "oracle_num_threads"):
+                  "oracle_load_stats", "oracle_num_threads", "oracle_bias_update"):
             getattr(_lib, f).restype = ctypes.c_int
     return _lib
 
@@ -184,6 +185,16 @@ def load_stats(counts, probs, k, alpha):
     _check(_L().oracle_load_stats(T, E, k, _p(counts), _p(probs), float(alpha), _p(f), _p(p), _p(L)),
            "load_stats")
     return dict(f=f, p=p, L=float(L[0]))
+
+
+def bias_update(counts, bias, T, k, gamma):
+    """Selection-bias step b_e - gamma * sign(load_e - T k / E); returns float64 [E]."""
+    counts = _c(counts, np.int32)
+    bias = _c(bias, np.float32)
+    E = counts.shape[0]
+    out = np.empty(E, np.float64)
+    _check(_L().oracle_bias_update(int(T), E, int(k), _p(counts), float(gamma), _p(bias), _p(out)), "bias_update")
+    return out
 
 
 def forward(layer, k, renormalize=True, capacity=-1, alpha=0.01, ids=None, tokens=None):

@@ -339,3 +339,27 @@ int oracle_load_stats(int T, int E, int k, const int32_t *counts, const double *
     *L = alpha * (double)E * acc;
     return 0;
 }
+
+/*
+ * Auxiliary-loss-free balancing: the selection-only per-expert bias moves
+ * against the load.  [MoE-Arch] s2 Load Balancing ("Over-loaded experts get a
+ * negative bias"); [Handbook] Load balancing ("the bias of an overloaded
+ * expert is lowered and that of an idle one raised").  The pages give the
+ * direction but no step size: gamma is a parameter.
+ *   load_e = counts_e (routing decisions, before any capacity cut)
+ *   mean   = T k / E
+ *   b_e   <- b_e - gamma * sign(load_e - mean)       (sign(0) = 0)
+ * The comparison with the mean is done exactly in integers (load_e E vs T k).
+ * bias_out is the exact double b_e -/+ gamma.
+ * Pinned: closed forms on hand-made loads (tests/golden/bias_update_direction.txt).
+ */
+int oracle_bias_update(int T, int E, int k, const int32_t *counts, double gamma, const float *bias_in,
+                       double *bias_out) {
+    const long long total = (long long)T * (long long)k;
+    for (int e = 0; e < E; ++e) {
+        const long long scaled = (long long)counts[e] * (long long)E;
+        const double sgn = scaled > total ? 1.0 : (scaled < total ? -1.0 : 0.0);
+        bias_out[e] = (double)bias_in[e] - gamma * sgn;
+    }
+    return 0;
+}

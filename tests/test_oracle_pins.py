@@ -335,3 +335,44 @@ def test_expert_parameter_arithmetic_matches_the_handbook_exercise():
     active = g["k"][0] * pe * g["layers"][0]
     assert round(total / 1e9, 2) == g["total_billions"][0]
     assert round(active / 1e9, 2) == g["active_billions"][0]
+
+
+# ------------------------------------------------------- selection-bias update pins
+
+def test_bias_update_direction_matches_the_pages():
+    g = _golden.load("bias_update_direction.txt")
+    out = oracle.bias_update(np.array(g["counts"]), np.array(g["bias"], np.float32), g["T"][0], g["k"][0],
+                             g["gamma"][0])
+    expected = np.array(g["bias"]) + g["gamma"][0] * np.array(g["direction"], np.float64)
+    np.testing.assert_array_equal(out, expected)
+
+
+def test_bias_update_leaves_balanced_loads_alone_and_is_exact_in_integers():
+    E, T, k = 8, 64, 2
+    counts = np.full(E, T * k // E, np.int32)
+    b = np.linspace(-1, 1, E).astype(np.float32)
+    np.testing.assert_array_equal(oracle.bias_update(counts, b, T, k, 0.01), b.astype(np.float64))
+    # the mean T*k/E = 16.5 is fractional: loads 16 and 17 sit on either side of it
+    T, k, E = 33, 2, 4
+    counts = np.array([17, 16, 17, 16], np.int32)
+    out = oracle.bias_update(counts, np.zeros(E, np.float32), T, k, 0.5)
+    np.testing.assert_array_equal(out, [-0.5, 0.5, -0.5, 0.5])
+
+
+def test_bias_update_moves_routing_towards_balance():
+    """Iterating route -> count -> update on a skewed router lowers the load of
+    the most popular expert (the purpose the pages give for the bias)."""
+    rng = np.random.default_rng(21)
+    T, d, E, k = 512, 16, 8, 2
+    x = _f32(rng.standard_normal((T, d)))
+    wg = _f32(rng.standard_normal((E, d)) / math.sqrt(d))
+    lb = _f32(np.log(np.arange(1, E + 1) ** -1.5))  # Zipf-like skew on the logits
+    bias = np.zeros(E, np.float32)
+    first = None
+    for _ in range(40):
+        r = oracle.route(x, wg, k, logit_bias=lb, select_bias=bias)
+        counts = oracle.group(r["ids"], E)["counts"]
+        first = counts.copy() if first is None else first
+        bias = oracle.bias_update(counts, bias, T, k, 0.05).astype(np.float32)
+    assert counts.max() < first.max()
+    assert np.abs(counts - T * k / E).sum() < np.abs(first - T * k / E).sum()
