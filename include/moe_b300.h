@@ -203,6 +203,19 @@ MOE_API int moe_combine(const moe_config *cfg, const float *y_perm, const int32_
 MOE_API int moe_load_stats(const moe_config *cfg, const int32_t *counts, const float *p_mean, float *f,
                    float *L, moe_stream_t stream);
 
+/* Selection-bias update of auxiliary-loss-free balancing ("MoE Architecture"
+ * s2 Load Balancing: over-loaded experts get a negative bias; "Mixture of
+ * experts (MoE)" handbook, Load balancing: an overloaded expert's bias is
+ * lowered and an idle one's raised).  A training-time step between layer
+ * calls, not part of the forward pass:
+ *   select_bias[e] -= gamma * sign(counts[e] - T k / E)      (sign(0) = 0)
+ * with counts [E] int32 as produced by moe_permute / moe_forward (routing
+ * decisions before the capacity cut; the comparison with the mean is exact).
+ * select_bias [E] fp32 is updated in place.  The pages give no step size:
+ * gamma is the caller's. */
+MOE_API int moe_bias_update(const moe_config *cfg, const int32_t *counts, float gamma, float *select_bias,
+                            moe_stream_t stream);
+
 /* The whole layer (steps 1-7) in one call, fused where the steps allow.
  *   y [T][d] (dtype, or fp32 when cfg->y_fp32) receives the layer output; stats (host struct, nullable)
  *   names optional device outputs.  ws1/ws3/ws2 are the shared expert's weights

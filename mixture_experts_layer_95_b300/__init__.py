@@ -25,7 +25,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTY
 
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
-            "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static")
+            "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static", "moe_bias_update")
 STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
 
 
@@ -66,6 +66,8 @@ def lib():
         L.moe_permute.argtypes = [cfgp] + [vp] * 11 + [vp, sz, vp]
         L.moe_permute_static.argtypes = [cfgp] + [vp] * 11 + [vp]
         L.moe_permute_static.restype = i32
+        L.moe_bias_update.argtypes = [cfgp, vp, ctypes.c_float, vp, vp]
+        L.moe_bias_update.restype = i32
         L.moe_expert_ffn.argtypes = [cfgp] + [vp] * 12 + [vp, sz, vp]
         L.moe_combine.argtypes = [cfgp] + [vp] * 4 + [vp]
         L.moe_load_stats.argtypes = [cfgp] + [vp] * 4 + [vp]
@@ -357,6 +359,16 @@ def load_stats(layer: Layer, counts, p_mean, stream=None):
     _check(lib().moe_load_stats(ctypes.byref(c), _ptr(counts), _ptr(p_mean), _ptr(f), _ptr(L), _stream(stream)),
            "moe_load_stats")
     return f, L
+
+
+def bias_update(layer: Layer, counts, select_bias, gamma: float, stream=None):
+    """moe_bias_update: select_bias[e] -= gamma * sign(counts[e] - T k / E), in place."""
+    _need(counts, (layer.E,), torch.int32, "counts")
+    _need(select_bias, (layer.E,), torch.float32, "select_bias")
+    c = layer.cfg()
+    _check(lib().moe_bias_update(ctypes.byref(c), _ptr(counts), ctypes.c_float(gamma), _ptr(select_bias),
+                                 _stream(stream)), "moe_bias_update")
+    return select_bias
 
 
 class Forward:

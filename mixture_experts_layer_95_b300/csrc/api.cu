@@ -24,6 +24,14 @@ size_t esize(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
 
 bool use_h_split(const moe_config& c) { return c.dtype == MOE_BF16 && c.h_split == 1; }
 
+// Decode-sized bf16 batches (at most 32 rows per touched expert on average):
+// the up GEMM gathers x rows itself, so the layer skips the permuted copy.
+bool use_gather_a(const moe_config& c) {
+    const long long n = (long long)c.T * c.k;
+    const long long touched = n < c.E ? n : c.E;
+    return c.dtype == MOE_BF16 && n <= 32 * touched;
+}
+
 // ---- split-K for decode-sized batches ----------------------------------------
 // When a grouped GEMM has too few output tiles to keep every SM streaming
 // weights, each tile's K range is split into S slices (fp32 partials, summed
@@ -98,7 +106,11 @@ struct Layout {
 Layout layout(const moe_config& c) {
     Layout l{};
     const size_t n = (size_t)c.T * c.k;
-    const size_t nblk = ((size_t)c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+    // histogram / p rows: the router's chunks, and moe_permute's 64-token chunks
+    const size_t ch = (size_t)router_chunk(c.T, c.E, c.d, c.dtype);
+    const size_t nblk_r = ((size_t)c.T + ch - 1) / ch;
+    const size_t nblk_p = ((size_t)c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+    const size_t nblk = nblk_r > nblk_p ? nblk_r : nblk_p;
     const size_t E = (size_t)c.E;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -122,7 +134,7 @@ Layout layout(const moe_config& c) {
     l.f = take(4 * E);
     l.L = take(4);
     l.logits = take(use_gemm_router(c) ? 4 * (size_t)c.T * E : 0);
-    l.x_perm = take(n * c.d * esize(c));
+    l.x_perm = take(use_gather_a(c) ? 0 : n * c.d * esize(c));  // not needed when the up GEMM gathers x
     l.h = take(n * c.d_ff * esize(c));
     l.h_shared = take(c.n_shared ? (size_t)c.T * c.d_ff_shared * esize(c) : 0);
     const bool split = use_h_split(c);
@@ -236,6 +248,11 @@ int enqueue_route(const moe_config& c, const Layout& L, void* ws, const void* x,
                   int32_t* block_hist, int sms, cudaStream_t s) {
     float* p_part = at<float>(ws, L.p_part);
     StageScope scope(kStageRouter, s);
+    if (use_split_d_router(c.T, c.E)) {
+        MOE_LAUNCH(launch_router_split_d(c.dtype, c.T, c.d, c.E, c.k, x, w_gate, logit_bias, select_bias,
+                                         c.renormalize, topk_ids, gates, p_part, block_hist, s));
+        return MOE_OK;
+    }
     if (!use_gemm_router(c)) {
         MOE_LAUNCH(launch_router_warp(c.dtype, c.T, c.d, c.E, c.k, x, w_gate, logit_bias, select_bias, c.renormalize,
                                     topk_ids, gates, p_part, block_hist, s));
@@ -266,7 +283,7 @@ int enqueue_route(const moe_config& c, const Layout& L, void* ws, const void* x,
 int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_perm, const int32_t* offsets,
                 const float* gates_perm, const void* w1, const void* w3, const void* w2, const void* x,
                 const void* ws1, const void* ws3, const void* ws2, float* y_perm, float* y_shared, int sms,
-                cudaStream_t s, bool reduce_down) {
+                cudaStream_t s, bool reduce_down, const int32_t* gather_idx) {
     const Splits sp = choose_splits(c);
     const int n = c.T * c.k;
     void* h = at<void>(ws, L.h);
@@ -277,6 +294,11 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     GemmProblem up[2] = {}, down[2] = {};
     up[0].A = x_perm;
     up[0].a_rows = n;
+    if (gather_idx) {  // rows come straight from x, in permuted order
+        up[0].A = x;
+        up[0].a_gather = gather_idx;
+        up[0].a_src_rows = c.T;
+    }
     up[0].B1 = w1;
     up[0].B2 = w3;
     up[0].offsets = offsets;
@@ -392,7 +414,8 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_gate, const fl
     const Layout L = layout(c);
     MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, nullptr, sms, s));
     if (p_mean) {
-        const int nblk = (c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+        const int ch = router_chunk(c.T, c.E, c.d, c.dtype);
+        const int nblk = (c.T + ch - 1) / ch;
         StageScope scope(kStageRouter, s);
         MOE_LAUNCH(launch_p_mean(c.T, c.E, nblk, at<float>(ws, L.p_part), p_mean, s));
     }
@@ -426,8 +449,9 @@ int moe_permute(const moe_config* cfg, const int32_t* topk_ids, const float* gat
     o.n_dropped = n_dropped;
     {
         StageScope scope(kStageScan, s);
-        MOE_LAUNCH(launch_group_hist(c.T, c.E, c.k, topk_ids, block_hist, status, s));
-        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, c.capacity, topk_ids, gates, block_hist, o, status, s));
+        const int chunk = kRouterTokensPerBlock;
+        MOE_LAUNCH(launch_group_hist(c.T, c.E, c.k, chunk, topk_ids, block_hist, status, s));
+        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, block_hist, o, status, s));
     }
     StageScope scope(kStageGather, s);
     MOE_LAUNCH(launch_gather_rows(c.dtype, c.T, c.d, c.T * c.k, offsets + c.E, sorted_token_ids, x, x_perm, status, s));
@@ -452,7 +476,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* off
     MOE_TRY(device_sms(&sms));
     const Layout L = layout(c);
     return enqueue_ffn(c, L, ws, x_perm, offsets, gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared, sms,
-                       reinterpret_cast<cudaStream_t>(stream), true);
+                       reinterpret_cast<cudaStream_t>(stream), true, nullptr);
 }
 
 int moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_pos, const float* y_shared, void* y,
@@ -482,6 +506,18 @@ int moe_load_stats(const moe_config* cfg, const int32_t* counts, const float* p_
     return MOE_OK;
 }
 
+int moe_bias_update(const moe_config* cfg, const int32_t* counts, float gamma, float* select_bias,
+                    moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (!counts || !select_bias) return MOE_ERR_NULL;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    MOE_LAUNCH(launch_bias_update(c.T, c.E, c.k, counts, gamma, select_bias, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
 int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
                 const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
                 const void* ws3, const void* ws2, void* y, const moe_stats* stats, void* ws, size_t ws_bytes,
@@ -505,7 +541,8 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
     int32_t* topk_ids = at<int32_t>(ws, L.topk_ids);
     float* gates = at<float>(ws, L.gates);
     int32_t* block_hist = at<int32_t>(ws, L.block_hist);
-    const int nblk = (c.T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+    const int chunk = router_chunk(c.T, c.E, c.d, c.dtype);
+    const int nblk = (c.T + chunk - 1) / chunk;
 
     // 1-3: router, softmax, top-k; the router blocks also emit their id histograms
     MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, block_hist, sms, s));
@@ -529,10 +566,16 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
     }
     {
         StageScope scope(kStageScan, s);
-        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, c.capacity, topk_ids, gates, block_hist, o, status, s));
+        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, block_hist, o, status, s));
     }
-    void* x_perm = at<void>(ws, L.x_perm);
-    {
+    // decode-sized bf16 batches: the up GEMM gathers x rows itself (TMA
+    // gather4); otherwise an explicit copy into expert order
+    void* x_perm = nullptr;
+    const int32_t* gather_idx = nullptr;
+    if (use_gather_a(c)) {
+        gather_idx = o.sorted_token_ids;
+    } else {
+        x_perm = at<void>(ws, L.x_perm);
         StageScope scope(kStageGather, s);
         MOE_LAUNCH(launch_gather_rows(c.dtype, c.T, c.d, c.T * c.k, o.offsets + c.E, o.sorted_token_ids, x, x_perm,
                                       status, s));
@@ -542,7 +585,7 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
     float* y_perm = at<float>(ws, L.y_perm);
     float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
     MOE_TRY(enqueue_ffn(c, L, ws, x_perm, o.offsets, o.gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared,
-                        sms, s, false));
+                        sms, s, false, gather_idx));
 
     // 6: combine (straight from the down GEMM's split-K slices when it was split)
     const Splits sp = choose_splits(c);

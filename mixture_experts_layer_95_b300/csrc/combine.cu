@@ -11,6 +11,10 @@
 //
 // Load statistics ("MoE Architecture" s2 Load Balancing; handbook aux_loss):
 //   f_i = counts_i / (T k),   L = alpha * E * sum_i f_i p_i.
+// Selection-bias update of auxiliary-loss-free balancing ("MoE Architecture"
+// s2: over-loaded experts get a negative bias; handbook Load balancing: an
+// overloaded expert's bias is lowered and an idle one's raised):
+//   b_e -= gamma * sign(counts_e - T k / E), compared exactly in integers.
 #include "common.cuh"
 
 namespace moe {
@@ -166,7 +170,21 @@ __global__ void load_stats_kernel(int Tn, int E, int k, float alpha, const int32
     }
 }
 
+__global__ void bias_update_kernel(int Tn, int E, int k, const int32_t* __restrict__ counts, float gamma,
+                                   float* __restrict__ bias) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    const long long scaled = (long long)counts[e] * E, total = (long long)Tn * k;
+    if (scaled > total) bias[e] = bias[e] - gamma;
+    else if (scaled < total) bias[e] = bias[e] + gamma;
+}
+
 }  // namespace
+
+cudaError_t launch_bias_update(int T, int E, int k, const int32_t* counts, float gamma, float* bias, cudaStream_t s) {
+    bias_update_kernel<<<(E + 255) / 256, 256, 0, s>>>(T, E, k, counts, gamma, bias);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_perm, size_t perm_stride,
                                  int nsplit, const int32_t* slot_pos, const float* y_shared, size_t shared_stride,

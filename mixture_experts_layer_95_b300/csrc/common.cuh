@@ -15,10 +15,12 @@ namespace moe {
 
 // Upper bound on E handled by the kernels (shared-memory histograms, scans).
 constexpr int kMaxExperts = 1024;
-// Tokens handled by one router block; the grouping kernels chunk the flat
-// (token, slot) entries by the same blocks so the router can emit the
-// per-block expert histograms the scan needs.
-constexpr int kRouterTokensPerBlock = 64;
+// The router emits one expert histogram (and one partial sum of p) per chunk
+// of consecutive tokens; the grouping scan reads those rows, chunked the same
+// way.  Chunk sizes per router kernel:
+constexpr int kRouterTokensPerBlock = 64;  // logits router; the stand-alone moe_permute histograms
+constexpr int kWarpRouterChunk = 32;       // warp router (prefill-sized batches, small E)
+constexpr int kSplitDRouterMaxT = 256;     // up to this many tokens: one block per token
 constexpr int kRouterThreads = 256;
 // The fused warp router keeps E logits per lane in registers and W_g in
 // shared memory (padded to 8 or 16 rows); larger routers go through the
@@ -36,6 +38,17 @@ inline size_t warp_router_smem_bytes(int E, int d, int dtype) {
 // True when the fused warp router handles this layer.
 inline bool use_warp_router(int E, int d, int dtype) {
     return E <= kWarpRouterMaxE && warp_router_smem_bytes(E, d, dtype) <= kWarpRouterMaxSmem;
+}
+
+// True when the one-block-per-token router handles this layer (decode-sized
+// batches: every token gets a whole block, d split across its threads).
+inline bool use_split_d_router(int T, int E) { return T <= kSplitDRouterMaxT && E <= 32; }
+
+// Tokens per histogram row for the router a layer uses (T, E, d, dtype).
+inline int router_chunk(int T, int E, int d, int dtype) {
+    if (use_split_d_router(T, E)) return 1;
+    if (use_warp_router(E, d, dtype)) return kWarpRouterChunk;
+    return kRouterTokensPerBlock;
 }
 
 // Device status word values (mirror enum moe_status).
@@ -100,6 +113,13 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
                                int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
                                cudaStream_t s);
 
+// Router for T <= kSplitDRouterMaxT and E <= 32: one block per token, same
+// outputs with one histogram row per token.
+cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
+                                  const float* logit_bias, const float* select_bias, int renormalize,
+                                  int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
+                                  cudaStream_t s);
+
 // Softmax / top-k over precomputed fp32 logits [T][E] (any E <= kMaxExperts);
 // same outputs as the fused router.
 cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, const float* logit_bias,
@@ -109,9 +129,9 @@ cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, 
 // p_mean[e] = (sum over blocks of p_part[b][e]) / T, fixed order.
 cudaError_t launch_p_mean(int T, int E, int nblk, const float* p_part, float* p_mean, cudaStream_t s);
 
-// Per-block expert histogram of topk_ids, chunked like the router.
-cudaError_t launch_group_hist(int T, int E, int k, const int32_t* topk_ids, int32_t* block_hist, int* status,
-                              cudaStream_t s);
+// Expert histogram of topk_ids per chunk of `chunk` tokens.
+cudaError_t launch_group_hist(int T, int E, int k, int chunk, const int32_t* topk_ids, int32_t* block_hist,
+                              int* status, cudaStream_t s);
 
 struct GroupOut {
     int32_t* counts;
@@ -131,8 +151,10 @@ struct GroupOut {
 };
 
 // Scan of the block histograms, stable ranks, capacity cut, permutation.
-cudaError_t launch_group_scan(int T, int E, int k, int capacity, const int32_t* topk_ids, const float* gates,
-                              const int32_t* block_hist, const GroupOut& o, int* status, cudaStream_t s);
+// block_hist holds one row per chunk of `chunk` tokens.
+cudaError_t launch_group_scan(int T, int E, int k, int chunk, int capacity, const int32_t* topk_ids,
+                              const float* gates, const int32_t* block_hist, const GroupOut& o, int* status,
+                              cudaStream_t s);
 
 // x_perm[pos] = x[sorted_token_ids[pos]] for pos < offsets[E].
 cudaError_t launch_gather_rows(int dtype, int T, int d, int rows_max, const int32_t* offsets_end,
@@ -142,6 +164,9 @@ cudaError_t launch_gather_rows(int dtype, int T, int d, int rows_max, const int3
 // y[t] = sum_j y_perm[slot_pos[t][j]] (slot_pos >= 0) + y_shared[t].
 cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, const int32_t* slot_pos,
                            const float* y_shared, void* y, cudaStream_t s);
+
+// bias[e] -= gamma * sign(counts[e] - T k / E).
+cudaError_t launch_bias_update(int T, int E, int k, const int32_t* counts, float gamma, float* bias, cudaStream_t s);
 
 // f = counts/(T k), L = alpha E sum f p.
 cudaError_t launch_load_stats(int T, int E, int k, float alpha, const int32_t* counts, const float* p_mean,
@@ -174,6 +199,8 @@ struct GemmProblem {
     const void* A2;       // kGemmScaleSplit: the lo half of A, same layout
     void* out2;           // kGemmSwiGLU: optional lo half of H (H - bf16(H)), same layout as out
     float* part;          // split-K: fp32 partials [ksplit][a_rows][2N (SwiGLU) or N]
+    const int32_t* a_gather;  // non-null: A row r is row a_gather[r] of A, which has a_src_rows rows
+    int a_src_rows;
 };
 
 // Tensor-core (tcgen05) path, bf16 operands, fp32 accumulate.  Runs up to two

@@ -19,7 +19,12 @@
 //    so that each weight tile is fetched from HBM once and re-read from L2.
 //  * warp 0: TMA producer (cp.async.bulk.tensor, 128-byte swizzle, 4-stage
 //    mbarrier ring; rows past a segment's end are loaded but never stored,
-//    rows past the tensor are zero-filled by the TMA unit).
+//    rows past the tensor are zero-filled by the TMA unit).  For decode-sized
+//    batches the up GEMM of the fused layer gathers its A rows straight from
+//    the token matrix with tile::gather4 (4 rows per load, indices from the
+//    permutation, only the tile's valid rows), so no permuted copy of x is
+//    written; large batches load A as plain tiles of that copy, because 32
+//    gather4 loads per 16 KB stage cannot keep up with the tensor cores.
 //  * warp 1: allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
 //    one lane issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128,
 //    N=256, K=16 per instruction); tcgen05.commit frees smem stages and
@@ -71,6 +76,8 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     void* out2[2];  // SwiGLU: when non-null, the lo half of H (H - bf16(H)) goes here
     const float* row_scale[2];
     int G[2], M[2], N[2], K[2], a_rows[2];
+    const int32_t* a_gather[2];  // non-null: A row r is row a_gather[r] of tmA's tensor (gather4 loads)
+    int a_src_rows[2];           // rows of the tensor tmA describes when gathering
     int nprob;
     int ksplit;                // K slices per tile (1: no split)
     float* part[2];            // ksplit > 1: fp32 partials [ksplit][a_rows][part_cols]
@@ -157,6 +164,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Four rows (r0..r3) x 64 columns starting at column c0 of a 2-D tensor whose
+// map has a one-row box; lands in shared memory as four consecutive 128-byte
+// rows, swizzled like a tiled load to the same address.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, int c0, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -466,25 +485,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            uint32_t issued_parity[NST];
-            bool used[NST];
-            for (int i = 0; i < NST; ++i) used[i] = false;
-            bool dead = p.stall_producer != 0;
-            for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
-                const Tile t = decode_tile<MODE>(st, p, id);
-                const int b_row0 = t.g * p.N[t.prob] + t.n * out_cols_per_tile<MODE>();
-                for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
-                        dead = true;
-                        break;
+        // Lane 0 arms each stage's barrier and loads B (and A when A is a plain
+        // tile); when A rows are gathered, every lane loads 4 of the tile's
+        // 128 rows with one gather4 per k-block.
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t issued_parity[NST];
+        bool used[NST];
+        for (int i = 0; i < NST; ++i) used[i] = false;
+        bool dead = p.stall_producer != 0;
+        for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
+            const Tile t = decode_tile<MODE>(st, p, id);
+            const int b_row0 = t.g * p.N[t.prob] + t.n * out_cols_per_tile<MODE>();
+            const int32_t* gidx = p.a_gather[t.prob];
+            int rows4[4] = {0, 0, 0, 0};
+            if (gidx) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = lane * 4 + i;
+                    int v = r < t.rows_valid ? __ldg(gidx + t.a_row0 + r) : 0;
+                    if (v < 0 || v >= p.a_src_rows[t.prob]) {
+                        if (r < t.rows_valid) record_status(p.status, kStatusBounds);
+                        v = 0;
                     }
-                    uint8_t* sa = smem + (size_t)s * SC::kBytes;
-                    uint8_t* sb = sa + SC::kBOff;
-                    mbar_expect_tx(&st.full[s], SC::kBytes);
-                    tma_load_2d(sa, &p.tmA[t.prob], kb * BK, t.a_row0, &st.full[s]);
+                    rows4[i] = v;
+                }
+            }
+            for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
+                    dead = true;
+                    break;
+                }
+                uint8_t* sa = smem + (size_t)s * SC::kBytes;
+                uint8_t* sb = sa + SC::kBOff;
+                if (lane == 0) {
+                    // gathered A: only the groups of 4 rows that hold valid rows are
+                    // loaded; the other rows of the tile are never stored
+                    const uint32_t a_bytes = gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : A_BYTES;
+                    mbar_expect_tx(&st.full[s], SC::kBytes - A_BYTES + a_bytes);
+                    if (!gidx) tma_load_2d(sa, &p.tmA[t.prob], kb * BK, t.a_row0, &st.full[s]);
                     if (SC::kSplit) tma_load_2d(sa + A_BYTES, &p.tmA2[t.prob], kb * BK, t.a_row0, &st.full[s]);
                     if (MODE == kGemmSwiGLU) {
                         tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
@@ -492,15 +531,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                     } else {
                         tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
                     }
-                    issued_parity[s] = ph;
-                    used[s] = true;
-                    if (++s == NST) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                }
+                if (gidx && lane * 4 < t.rows_valid)
+                    tma_gather4(sa + lane * 4 * (BK * 2), &p.tmA[t.prob], kb * BK, rows4[0], rows4[1], rows4[2],
+                                rows4[3], &st.full[s]);
+                issued_parity[s] = ph;
+                used[s] = true;
+                if (++s == NST) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
-            // make sure no copy is still landing in shared memory before the CTA exits
+        }
+        // make sure no copy is still landing in shared memory before the CTA exits
+        __syncwarp();
+        if (lane == 0) {
             volatile int no_abort = 0;
             for (int i = 0; i < NST; ++i)
                 if (used[i]) mbar_wait(&st.full[i], issued_parity[i], &no_abort, nullptr, kDrainLimitNs);
@@ -640,7 +685,14 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
         if (g.G < 1 || g.G > MAX_GROUPS) return cudaErrorInvalidValue;
-        if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
+        if (g.a_gather) {
+            // A rows are gathered from a [a_src_rows][K] tensor, 4 rows per load
+            if (!make_tmap(&prm.tmA[q], g.A, g.a_src_rows, g.K, 1)) return cudaErrorInvalidValue;
+            prm.a_gather[q] = g.a_gather;
+            prm.a_src_rows[q] = g.a_src_rows;
+        } else if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) {
+            return cudaErrorInvalidValue;
+        }
         if (!make_tmap(&prm.tmB1[q], g.B1, g.G * g.N, g.K, b_box)) return cudaErrorInvalidValue;
         if (mode == kGemmSwiGLU && !make_tmap(&prm.tmB2[q], g.B2, g.G * g.N, g.K, b_box))
             return cudaErrorInvalidValue;

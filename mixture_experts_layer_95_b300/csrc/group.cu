@@ -8,8 +8,9 @@
 // order and drops the rest.
 //
 // GPU form (reduce-then-scan, no spin-waits):
-//  1. a per-block shared-memory histogram of the chosen ids (emitted by the
-//     router for free, or by group_hist_kernel) -> block_hist [nblk][E];
+//  1. a shared-memory histogram of the chosen ids per chunk of tokens
+//     (emitted by the router for free, or by group_hist_kernel) ->
+//     block_hist [nchunk][E];
 //  2. group_scan_kernel: every block re-reads the whole (small) block_hist,
 //     derives the global counts, the capacity cut, the expert offsets and its
 //     own per-expert starting ranks, then ranks its entries stably with warp
@@ -26,7 +27,7 @@ namespace {
 constexpr int kScanThreads = 256;
 constexpr int kScanWarps = kScanThreads / 32;
 
-__global__ void __launch_bounds__(kRouterThreads) group_hist_kernel(int Tn, int E, int k,
+__global__ void __launch_bounds__(kRouterThreads) group_hist_kernel(int Tn, int E, int k, int chunk,
                                                                      const int32_t* __restrict__ ids,
                                                                      int32_t* __restrict__ block_hist,
                                                                      int* status) {
@@ -34,8 +35,8 @@ __global__ void __launch_bounds__(kRouterThreads) group_hist_kernel(int Tn, int 
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
     const size_t n = (size_t)Tn * k;
-    const size_t lo = (size_t)blockIdx.x * kRouterTokensPerBlock * k;
-    const size_t hi = min(n, lo + (size_t)kRouterTokensPerBlock * k);
+    const size_t lo = (size_t)blockIdx.x * chunk * k;
+    const size_t hi = min(n, lo + (size_t)chunk * k);
     for (size_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
         const int e = ids[i];
         if (e < 0 || e >= E) {
@@ -87,7 +88,7 @@ __device__ void block_exclusive_scan(const int* v, int* out, int n, int* s_warp)
 }
 
 struct ScanArgs {
-    int T, E, k, capacity, nblk;
+    int T, E, k, chunk, capacity, nblk;
     const int32_t* ids;
     const float* gates;
     const int32_t* block_hist;
@@ -110,8 +111,9 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
     // 1. global counts, this block's prefix, capacity cut
     for (int e = threadIdx.x; e < E; e += kScanThreads) {
         int tot = 0, before = 0;
-        for (int b = 0; b < a.nblk; ++b) {
-            const int v = a.block_hist[(size_t)b * E + e];
+#pragma unroll 8
+        for (int b = 0; b < a.nblk; ++b) {  // independent loads: keep several in flight
+            const int v = __ldg(a.block_hist + (size_t)b * E + e);
             before += (b < (int)blockIdx.x) ? v : 0;
             tot += v;
         }
@@ -135,7 +137,8 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
             float part = 0.f;
             for (int e = threadIdx.x; e < E; e += kScanThreads) {
                 float ps = 0.f;
-                for (int b = 0; b < a.o.p_nblk; ++b) ps += a.o.p_part[(size_t)b * E + e];
+#pragma unroll 8
+                for (int b = 0; b < a.o.p_nblk; ++b) ps += __ldg(a.o.p_part + (size_t)b * E + e);
                 const float pm = ps / (float)a.T;
                 const float f = (float)s_wcnt[e] / ((float)a.T * (float)a.k);
                 if (a.o.p_mean) a.o.p_mean[e] = pm;
@@ -159,8 +162,8 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
     __syncthreads();
 
     // 3. stable ranks: warp w owns a contiguous sub-range of this block's entries
-    const int lo = blockIdx.x * kRouterTokensPerBlock * a.k;
-    const int hi = min(n, lo + kRouterTokensPerBlock * a.k);
+    const int lo = blockIdx.x * a.chunk * a.k;
+    const int hi = min(n, lo + a.chunk * a.k);
     const int per_warp = (hi - lo + kScanWarps - 1) / kScanWarps;
     const int wlo = min(hi, lo + warp * per_warp);
     const int whi = min(hi, wlo + per_warp);
@@ -234,19 +237,20 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int Tn, int d, const i
 
 }  // namespace
 
-cudaError_t launch_group_hist(int T, int E, int k, const int32_t* topk_ids, int32_t* block_hist, int* status,
-                              cudaStream_t s) {
-    const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+cudaError_t launch_group_hist(int T, int E, int k, int chunk, const int32_t* topk_ids, int32_t* block_hist,
+                              int* status, cudaStream_t s) {
+    const int nblk = (T + chunk - 1) / chunk;
     if (nblk == 0) return cudaSuccess;
-    group_hist_kernel<<<nblk, kRouterThreads, E * sizeof(int), s>>>(T, E, k, topk_ids, block_hist, status);
+    group_hist_kernel<<<nblk, kRouterThreads, E * sizeof(int), s>>>(T, E, k, chunk, topk_ids, block_hist, status);
     return cudaGetLastError();
 }
 
-cudaError_t launch_group_scan(int T, int E, int k, int capacity, const int32_t* topk_ids, const float* gates,
-                              const int32_t* block_hist, const GroupOut& o, int* status, cudaStream_t s) {
-    const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+cudaError_t launch_group_scan(int T, int E, int k, int chunk, int capacity, const int32_t* topk_ids,
+                              const float* gates, const int32_t* block_hist, const GroupOut& o, int* status,
+                              cudaStream_t s) {
+    const int nblk = (T + chunk - 1) / chunk;
     if (nblk == 0) return cudaSuccess;
-    ScanArgs a{T, E, k, capacity, nblk, topk_ids, gates, block_hist, o, status};
+    ScanArgs a{T, E, k, chunk, capacity, nblk, topk_ids, gates, block_hist, o, status};
     const size_t smem = sizeof(int) * ((size_t)3 * E + 1 + (size_t)kScanWarps * E + kScanWarps + 1) +
                         sizeof(float) * kScanThreads;
     cudaFuncSetAttribute(group_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

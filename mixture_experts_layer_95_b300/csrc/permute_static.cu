@@ -85,8 +85,10 @@ extern "C" int moe_permute_static(const moe_config* cfg, const int32_t* topk_ids
     o.slot_pos = slot_pos;
     o.gates_perm = gates_perm;
     o.n_dropped = n_dropped;
-    if (launch_group_hist(c.T, c.E, c.k, topk_ids, block_hist, nullptr, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_group_scan(c.T, c.E, c.k, c.capacity, topk_ids, gates, block_hist, o, nullptr, s) != cudaSuccess)
+    const int chunk = kRouterTokensPerBlock;
+    if (launch_group_hist(c.T, c.E, c.k, chunk, topk_ids, block_hist, nullptr, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, block_hist, o, nullptr, s) !=
+        cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_gather_rows(c.dtype, c.T, c.d, c.T * c.k, offsets + c.E, sorted_token_ids, x, x_perm, nullptr, s) !=
         cudaSuccess)

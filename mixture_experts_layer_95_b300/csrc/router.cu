@@ -11,11 +11,12 @@
 // plus, per block, the partial column sums of p (for the mean router
 // probability p_i) and the histogram of the chosen ids (for the grouping scan).
 //
-// Two kernels:
+// Three kernels:
 //  * router_warp_kernel -- one warp per token, E <= 16 experts, W_g staged in
 //    shared memory.  Each lane streams 16-byte vectors of x, keeps E fp32
 //    partial dots in registers and finishes them with butterfly shuffles;
 //    afterwards lane e owns expert e.
+//  * router_split_d_kernel -- decode-sized batches: one block per token.
 //  * router_logits_kernel -- softmax/top-k over fp32 logits produced by a
 //    tensor-core GEMM (large E); lane owns experts lane, lane+32, ...
 #include <float.h>
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
     int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
     int32_t* __restrict__ block_hist) {
     constexpr int kW = kWarpRouterThreads / 32;
-    constexpr int kTpw = kRouterTokensPerBlock / kW;
+    constexpr int kTpw = kWarpRouterChunk / kW;
     constexpr int VE = Vec<T>::kElems;
     extern __shared__ uint4 s_w[];  // [NE][d / VE] 16-byte vectors
     __shared__ float s_p[kW * NE];
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
             s_w[i] = (i < E * nv) ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
-    const int t0 = blockIdx.x * kRouterTokensPerBlock + warp * kTpw;
+    const int t0 = blockIdx.x * kWarpRouterChunk + warp * kTpw;
     const uint4* xr[kTpw];
 #pragma unroll
     for (int q = 0; q < kTpw; ++q) {
@@ -212,6 +213,63 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
         softmax_topk<1>(t0 + q, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
     }
     block_epilogue<1, kW>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
+}
+
+// Router for decode-sized batches: one block per token, the d dimension split
+// over the block's threads (each thread owns 16-byte vectors v = tid,
+// tid + 256, ...), W_g read straight from L2/L1.  The E partial dots are
+// reduced across the block in a fixed order; warp 0 then runs the shared
+// softmax/top-k epilogue.  Histogram and p rows are per token (chunk = 1).
+template <typename T, int NE>
+__global__ void __launch_bounds__(kRouterThreads) router_split_d_kernel(
+    int Tn, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ wg,
+    const float* __restrict__ logit_bias, const float* __restrict__ select_bias, int renormalize,
+    int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
+    int32_t* __restrict__ block_hist) {
+    constexpr int VE = Vec<T>::kElems;
+    constexpr int kW = kRouterThreads / 32;
+    __shared__ float s_red[kW][NE];
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nv = d / VE;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    const uint4* w = reinterpret_cast<const uint4*>(wg);
+    float acc[NE];
+#pragma unroll
+    for (int e = 0; e < NE; ++e) acc[e] = 0.f;
+    for (int v = threadIdx.x; v < nv; v += kRouterThreads) {
+        float xv[VE];
+        widen(__ldg(xr + v), xv, static_cast<const T*>(nullptr));
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            if (e < E) {
+                float wv[VE];
+                widen(__ldg(w + (size_t)e * nv + v), wv, static_cast<const T*>(nullptr));
+#pragma unroll
+                for (int i = 0; i < VE; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+        const float v = warp_sum(acc[e]);
+        if (lane == 0) s_red[warp][e] = v;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float l[1] = {-FLT_MAX};
+    if (lane < E) {
+        float v = 0.f;
+        for (int q = 0; q < kW; ++q) v += s_red[q][lane];  // fixed order
+        l[0] = v + (logit_bias ? __ldg(logit_bias + lane) : 0.f);
+    }
+    float psum[1] = {0.f};
+    int hcnt[1] = {0};
+    softmax_topk<1>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
+    if (lane < E) {
+        if (p_part) p_part[(size_t)t * E + lane] = psum[0];
+        if (block_hist) block_hist[(size_t)t * E + lane] = hcnt[0];
+    }
 }
 
 template <int NJ>
@@ -258,7 +316,7 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
                                const float* logit_bias, const float* select_bias, int renormalize,
                                int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
                                cudaStream_t s) {
-    const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
+    const int nblk = (T + kWarpRouterChunk - 1) / kWarpRouterChunk;
     if (nblk == 0) return cudaSuccess;
     const int ne = warp_router_width(E);
     const size_t smem = warp_router_smem_bytes(E, d, dtype);
@@ -281,6 +339,29 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
         else MOE_ROUTER_CASE(float, 16);
     }
 #undef MOE_ROUTER_CASE
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
+                                  const float* logit_bias, const float* select_bias, int renormalize,
+                                  int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
+                                  cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+#define MOE_SPLITD_CASE(TY, NE)                                                                              \
+    router_split_d_kernel<TY, NE><<<T, kRouterThreads, 0, s>>>(T, d, E, k, static_cast<const TY*>(x),       \
+                                                               static_cast<const TY*>(w_gate), logit_bias,  \
+                                                               select_bias, renormalize, topk_ids, gates,  \
+                                                               p_part, block_hist)
+    if (dtype == MOE_BF16) {
+        if (E <= 8) MOE_SPLITD_CASE(__nv_bfloat16, 8);
+        else if (E <= 16) MOE_SPLITD_CASE(__nv_bfloat16, 16);
+        else MOE_SPLITD_CASE(__nv_bfloat16, 32);
+    } else {
+        if (E <= 8) MOE_SPLITD_CASE(float, 8);
+        else if (E <= 16) MOE_SPLITD_CASE(float, 16);
+        else MOE_SPLITD_CASE(float, 32);
+    }
+#undef MOE_SPLITD_CASE
     return cudaGetLastError();
 }
 

@@ -15,6 +15,9 @@ from moe_inputs import WORKLOADS, Workload
 
 pytestmark = pytest.mark.gpu
 
+# Router kernels by shape: T <= 256 and E <= 32 -> one block per token;
+# E <= 16 -> warp router (32-token chunks); otherwise tensor-core (bf16) or
+# CUDA-core (fp32) logits GEMM + softmax/top-k pass (64-token chunks).
 SMALL = [
     WORKLOADS["tiny_f32"],
     Workload("small_bf16", T=300, d=512, E=8, F=384, k=2),
@@ -24,7 +27,8 @@ SMALL = [
              h_split=True),
     Workload("split_h_shared_ragged_bf16", T=150, d=264, E=6, F=200, k=2, n_shared=1, F_s=136, capacity=30,
              h_split=True),
-    Workload("gemm_router_f32", T=150, d=128, E=20, F=96, k=3, dtype="f32"),
+    Workload("gemm_router_f32", T=300, d=128, E=20, F=96, k=3, dtype="f32"),
+    Workload("warp_router_f32", T=300, d=264, E=8, F=96, k=2, dtype="f32"),
     Workload("shared_selectbias_bf16", T=200, d=256, E=32, F=128, k=8, n_shared=1, F_s=192, select_bias=True),
     Workload("dense_limit_bf16", T=64, d=128, E=8, F=128, k=8, renormalize=False),
     Workload("single_expert_bf16", T=130, d=128, E=1, F=256, k=1),
