@@ -95,9 +95,14 @@ struct SmemTail {
     uint32_t tmem_base;
     int abort_flag;
     int total[2];
-    int tile_start[2][MAX_GROUPS + 1];
-    int row0[2][MAX_GROUPS];
-    int rows[2][MAX_GROUPS];
+    int gbase[2];  // first entry of each problem's groups in the arrays below
+    // per group (both problems back to back; the launcher keeps G0 + G1 <= MAX_GROUPS + 1)
+    int tile_start[MAX_GROUPS + 1];
+    int row0[MAX_GROUPS + 1];
+    int rows[MAX_GROUPS + 1];
+    // epilogue staging: each epilogue warp transposes 32 rows x 32 fp32 columns
+    // so that its global stores are whole 128-byte row segments
+    float stage[4][32][33];
 };
 
 template <int MODE>
@@ -256,7 +261,8 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& 
     Tile t;
     t.prob = (id < st.total[0]) ? 0 : 1;
     const int local = id - (t.prob ? st.total[0] : 0);
-    const int* ts = st.tile_start[t.prob];
+    const int gb = st.gbase[t.prob];
+    const int* ts = st.tile_start + gb;
     int lo = 0, hi = p.G[t.prob] - 1;  // largest g with ts[g] <= local
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -264,14 +270,14 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& 
         else hi = mid - 1;
     }
     t.g = lo;
-    const int rows = st.rows[t.prob][lo];
+    const int rows = st.rows[gb + lo];
     const int mt = (rows + BM - 1) / BM;
     int r = local - ts[lo];
     t.ks = r % p.ksplit;  // K slices of one output tile are adjacent in the list
     r /= p.ksplit;
     t.n = r / mt;
     t.m = r - t.n * mt;
-    t.a_row0 = st.row0[t.prob][lo] + t.m * BM;
+    t.a_row0 = st.row0[gb + lo] + t.m * BM;
     t.rows_valid = min(BM, rows - t.m * BM);
     const int nk = (p.K[t.prob] + BK - 1) / BK;
     t.kb0 = t.ks * nk / p.ksplit;
@@ -324,7 +330,8 @@ __device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& 
 }
 
 template <int MODE>
-__device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile) {
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile,
+                                              float (*stage)[33]) {
     if (p.ksplit > 1) {
         epilogue_partial<MODE>(p, t, tacc, row_in_tile);
         return;
@@ -376,10 +383,16 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             }
         }
     } else {
+        // fp32 output: each 32x32 block of the warp's rows goes through shared
+        // memory (thread = row on the way in, lane = column on the way out), so
+        // that every store instruction writes one 128-byte row segment.
         float* out = static_cast<float*>(p.out[t.prob]);
         float scale = 1.0f;
         if ((MODE == kGemmScale || MODE == kGemmScaleSplit) && valid && p.row_scale[t.prob] != nullptr)
             scale = __ldg(p.row_scale[t.prob] + grow);
+        const int lane = threadIdx.x & 31;
+        const int wrow0 = row_in_tile - lane;  // first tile row of this warp
+        const int nvalid = min(32, t.rows_valid - wrow0);  // rows of this warp that exist
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t v[32];
@@ -387,17 +400,14 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             tmem_ld32(tacc + c0, v);
             tmem_ld_wait();
             const int col = t.n * BN + c0;
-            if (!valid || col >= N) continue;
-            float* dst = out + grow * N + col;
-            if (col + 32 <= N) {
+            if (col >= N || nvalid <= 0) continue;  // uniform across the warp
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    reinterpret_cast<float4*>(dst)[q] =
-                        make_float4(scale * __uint_as_float(v[4 * q]), scale * __uint_as_float(v[4 * q + 1]),
-                                    scale * __uint_as_float(v[4 * q + 2]), scale * __uint_as_float(v[4 * q + 3]));
-            } else {
-                for (int i = 0; i < 32 && col + i < N; ++i) dst[i] = scale * __uint_as_float(v[i]);
-            }
+            for (int i = 0; i < 32; ++i) stage[lane][i] = scale * __uint_as_float(v[i]);
+            __syncwarp();
+            const bool col_ok = col + lane < N;
+            float* dst = out + (size_t)(t.a_row0 + wrow0) * N + col + lane;
+            for (int r = 0; r < nvalid; ++r)
+                if (col_ok) dst[(size_t)r * N] = stage[r][lane];
         }
     }
 }
@@ -445,6 +455,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
         // tiles per group: ceil(rows / BM) * column blocks; warp-wide prefix sum
         for (int q = 0; q < 2; ++q) {
             int carry = 0;
+            const int gb = q == 0 ? 0 : p.G[0];
+            if (lane == 0) st.gbase[q] = gb;
             if (q < p.nprob) {
                 const int ncb = (p.N[q] + out_cols_per_tile<MODE>() - 1) / out_cols_per_tile<MODE>();
                 for (int base = 0; base < p.G[q]; base += 32) {
@@ -460,8 +472,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                             record_status(p.status, kStatusBounds);
                             lo = hi = 0;
                         }
-                        st.row0[q][g] = lo;
-                        st.rows[q][g] = hi - lo;
+                        st.row0[gb + g] = lo;
+                        st.rows[gb + g] = hi - lo;
                         tiles = ((hi - lo + BM - 1) / BM) * ncb * p.ksplit;
                     }
                     int incl = tiles;
@@ -470,7 +482,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                         const int y = __shfl_up_sync(0xffffffffu, incl, o);
                         if (lane >= o) incl += y;
                     }
-                    if (g < p.G[q]) st.tile_start[q][g] = carry + incl - tiles;
+                    if (g < p.G[q]) st.tile_start[gb + g] = carry + incl - tiles;
                     carry += __shfl_sync(0xffffffffu, incl, 31);
                 }
             }
@@ -602,7 +614,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
             if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status, p.wait_limit_ns)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_tile<MODE>(p, t, tacc, row_in_tile);
+            epilogue_tile<MODE>(p, t, tacc, row_in_tile, st.stage[quarter]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.tmem_empty[acc]);
@@ -682,6 +694,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     memset(&prm, 0, sizeof(prm));
     prm.ksplit = ksplit;
     const int b_box = (mode == kGemmSwiGLU) ? BN / 2 : BN;
+    if (probs[0].G + (nprob > 1 ? probs[1].G : 0) > MAX_GROUPS + 1) return cudaErrorInvalidValue;
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
         if (g.G < 1 || g.G > MAX_GROUPS) return cudaErrorInvalidValue;
