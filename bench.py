@@ -88,66 +88,108 @@ def recorded_traffic(workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling during the timed region."""
+    """SM clock, power and throttle reasons sampled every 50 ms on a thread.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    Uses NVML in-process (read-only queries; no GPU setting is touched).  It
+    is started before the warm-up so that its set-up never overlaps the timed
+    region; `mark` records the timed window and `summary` keeps the samples
+    inside it.  Falls back to `nvidia-smi -lms 50` when NVML is unavailable.
+    """
 
-    def __init__(self, gpu_index):
-        self.samples = []
+    REASONS = {"hw_slowdown": "nvmlClocksEventReasonHwSlowdown",
+               "hw_thermal_slowdown": "nvmlClocksEventReasonHwThermalSlowdown",
+               "sw_thermal_slowdown": "nvmlClocksEventReasonSwThermalSlowdown",
+               "sw_power_cap": "nvmlClocksEventReasonSwPowerCap"}
+
+    def __init__(self, gpu_uuid, pci_bus_id=None, period_s=0.05):
+        self.samples = []  # (time, sm_mhz, max_mhz, power_w, reasons)
         self.window = None
         self.proc = None
+        self._stop = threading.Event()
+        self.source = "nvml"
+        self.error = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            try:
+                self._h = pynvml.nvmlDeviceGetHandleByUUID(gpu_uuid)
+            except Exception as e:  # some drivers want the PCI address instead
+                if not pci_bus_id:
+                    raise
+                self.error = f"uuid lookup: {e!r}"
+                self._h = pynvml.nvmlDeviceGetHandleByPciBusId(pci_bus_id)
+            self._max = float(pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM))
+            self._masks = {k: getattr(pynvml, v) for k, v in self.REASONS.items()}
+            self.thread = threading.Thread(target=self._poll_nvml, args=(period_s,), daemon=True)
+        except Exception as e:
+            self.error = repr(e)
+            self.source = "nvidia-smi"
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", gpu_uuid, "--query-gpu=clocks.sm,clocks.max.sm,power.draw,"
+                     "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", str(int(period_s * 1000))],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.thread = threading.Thread(target=self._read_smi, daemon=True)
+            except OSError:
+                self.thread = None
+        if self.thread:
             self.thread.start()
-        except OSError:
-            self.proc = None
 
-    def _read(self):
+    def _poll_nvml(self, period_s):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                sm = float(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                pw = nv.nvmlDeviceGetPowerUsage(self._h) / 1000.0
+                bits = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                reasons = [k for k, m in self._masks.items() if bits & m]
+                self.samples.append((time.monotonic(), sm, self._max, pw, reasons))
+            except Exception:
+                pass
+            self._stop.wait(period_s)
+
+    def _read_smi(self):
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 7:
-                self.samples.append((time.monotonic(), parts))
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 7:
+                continue
+            try:
+                self.samples.append((time.monotonic(), float(p[0]), float(p[1]), float(p[2]),
+                                     [n for n, v in zip(names, p[3:7]) if v.lower() in ("active", "1", "yes")]))
+            except ValueError:
+                pass
 
     def mark(self, t0, t1):
         self.window = (t0, t1)
 
     def stop(self):
+        self._stop.set()
         if self.proc:
-            time.sleep(0.12)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=2)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "source": self.source, "error": self.error}
         t0, t1 = self.window or (0, float("inf"))
-        inside = [p for t, p in self.samples if t0 - 0.06 <= t <= t1 + 0.06]
-        use = inside or [min(self.samples, key=lambda s: abs(s[0] - t1))[1]]
-
-        def num(v):
-            try:
-                return float(v)
-            except ValueError:
-                return None
-
-        sm = [num(p[0]) for p in use if num(p[0]) is not None]
-        reasons = set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for p in use:
-            for name, v in zip(names, p[3:7]):
-                if v.strip().lower() in ("active", "1", "yes"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(use[0][1]),
-                "reasons": sorted(reasons), "samples": len(inside), "power_w_max": max(
-                    (num(p[2]) for p in use if num(p[2]) is not None), default=None)}
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        use = inside or [min(self.samples, key=lambda x: abs(x[0] - t1))]
+        reasons = sorted({r for x in use for r in x[4]})
+        out = {"sm_mhz": statistics.median(x[1] for x in use), "sm_max_mhz": use[0][2], "reasons": reasons,
+               "samples": len(inside), "power_w_max": max(x[3] for x in use), "source": self.source}
+        if self.error:
+            out["nvml_error"] = self.error
+        return out
 
 
 # ------------------------------------------------------------------ oracle leg
@@ -223,6 +265,17 @@ def run_ours(args):
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream(dev)
 
+    props = torch.cuda.get_device_properties(dev)
+    try:  # NVML numbers GPUs physically; the UUID names ours regardless of CUDA_VISIBLE_DEVICES
+        gpu_id = "GPU-" + str(props.uuid).replace("GPU-", "")
+    except Exception:
+        gpu_id = str(local)
+    try:
+        pci = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+    except Exception:
+        pci = None
+    clocks = ClockSampler(gpu_id, pci)  # started before the warm-up: its set-up never overlaps the timed region
+
     for _ in range(args.warmup):
         fw(x, y)
     torch.cuda.synchronize(dev)
@@ -235,12 +288,6 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    try:  # nvidia-smi numbers GPUs physically; the UUID names ours regardless of CUDA_VISIBLE_DEVICES
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
-    except Exception:
-        gpu_id = str(local)
-    clocks = ClockSampler(gpu_id)
-    time.sleep(0.15)
     barrier()
     launches0 = moe.launch_count()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -255,7 +302,6 @@ def run_ours(args):
     wall1 = time.monotonic()
     barrier()
     clocks.mark(wall0, wall1)
-    clocks.stop()
     launches = moe.launch_count() - launches0
     ms = start.elapsed_time(end)
     if world > 1:
@@ -286,7 +332,9 @@ def run_ours(args):
     if tensor_bound:
         achieved = up_flops / (up_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": recorded_traffic(args.workload),
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "traffic": recorded_traffic(args.workload),
                 "kernel": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)", "peak_source": f"{peak_src} bf16 burst",
                 "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4)}
     else:
@@ -320,6 +368,7 @@ def run_ours(args):
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    clocks.stop()
     e2e = {"value": round(world * w.T * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
            "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
            "d2h_bytes_per_step": y_h.numel() * y_h.element_size()}

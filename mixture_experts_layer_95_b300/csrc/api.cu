@@ -24,6 +24,16 @@ size_t esize(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
 
 bool use_h_split(const moe_config& c) { return c.dtype == MOE_BF16 && c.h_split == 1; }
 
+// Large expert segments (at least 512 rows per touched expert on average,
+// bf16, a single bf16 H): both grouped GEMMs run on CTA pairs with 256-row
+// tiles (2-SM tensor-core MMAs).  Smaller segments keep 128-row tiles, which
+// waste fewer rows at segment ends.
+bool use_pair_gemm(const moe_config& c) {
+    const long long n = (long long)c.T * c.k;
+    const long long touched = n < c.E ? n : c.E;
+    return c.dtype == MOE_BF16 && c.h_split == 0 && n >= 512 * touched;
+}
+
 // Decode-sized bf16 batches (at most 32 rows per touched expert on average):
 // the up GEMM gathers x rows itself, so the layer skips the permuted copy.
 bool use_gather_a(const moe_config& c) {
@@ -352,7 +362,8 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     {
         StageScope scope(kStageUp, s);
         if (c.dtype == MOE_BF16) {
-            MOE_LAUNCH(launch_gemm_tc(kGemmSwiGLU, up, np, status, sms, s, sp.up));
+            MOE_LAUNCH(launch_gemm_tc(kGemmSwiGLU, up, np, status, sms, s, sp.up,
+                                      use_pair_gemm(c) && sp.up == 1 && !up[0].a_gather));
             if (sp.up > 1) {
                 MOE_LAUNCH(launch_swiglu_finalize(n, offsets + c.E, c.d_ff, sp.up, up[0].part, h, h_lo, s));
                 if (c.n_shared)
@@ -365,7 +376,8 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     {
         StageScope scope(kStageDown, s);
         if (c.dtype == MOE_BF16) {
-            MOE_LAUNCH(launch_gemm_tc(split ? kGemmScaleSplit : kGemmScale, down, np, status, sms, s, sp.down));
+            MOE_LAUNCH(launch_gemm_tc(split ? kGemmScaleSplit : kGemmScale, down, np, status, sms, s, sp.down,
+                                      use_pair_gemm(c) && sp.down == 1));
             if (sp.down > 1 && reduce_down) {
                 MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
                 if (c.n_shared)

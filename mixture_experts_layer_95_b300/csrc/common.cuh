@@ -208,8 +208,10 @@ struct GemmProblem {
 // ksplit > 1 splits every tile's K range into ksplit slices that write fp32
 // partials to GemmProblem::part instead of `out` (finish with
 // launch_swiglu_finalize or the split-aware combine / reduce).
+// pair = true runs the 2-SM kernel (256-row tiles on CTA pairs; SwiGLU and
+// Scale modes, ksplit 1, plain A) for large expert segments.
 cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
-                           cudaStream_t s, int ksplit = 1);
+                           cudaStream_t s, int ksplit = 1, bool pair = false);
 
 // H[r][f] = silu(sum_s P[s][r][f]) * sum_s P[s][r][N + f] (bf16, and the lo
 // half when h_lo != nullptr) for r < rows, rows = *rows_dev when non-null.

@@ -87,9 +87,11 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     int stall_producer;      // test switch: issue no loads, so the consumers' bounded waits run out
 };
 
+constexpr int kMaxRing = 6;  // deepest ring of any kernel here (the 2-SM kernel)
+
 struct SmemTail {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[kMaxRing];
+    uint64_t empty[kMaxRing];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
@@ -636,6 +638,299 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
     }
 }
 
+// ------------------------------------------------------- 2-SM (CTA pair) kernel
+//
+// For large expert segments: a cluster of two CTAs on two SMs computes one
+// 256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256: each CTA owns 128
+// rows of A and of the accumulator; N = 256: each CTA holds half of the B
+// tile and the pair's tensor cores share the halves).  Every SM therefore
+// reads 32 KB of operands per 64-deep k-block instead of 48 KB, and the ring
+// holds 6 stages instead of 4, which is what the 1-SM kernel lacks to keep
+// its tensor cores fed.  Roles as in the 1-SM kernel; the leader CTA (rank 0)
+// issues the MMAs, both CTAs load their own halves, both TMA streams signal
+// the leader's stage barrier, MMA completion is multicast to both CTAs, and
+// both CTAs' epilogue warps release the accumulator on the leader's barrier.
+
+constexpr int PAIR_STAGES = kMaxRing;
+constexpr int PAIR_STAGE_BYTES = A_BYTES + B_BYTES / 2;  // this CTA's 128 rows of A + half of B
+
+constexpr size_t pair_smem_bytes() { return 1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + sizeof(SmemTail); }
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the same variable in the leader CTA (rank 0)
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(out) : "r"(smem_u32(p)));
+    return out;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// arrive on the barrier at this offset in both CTAs of the pair
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)0x3)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+// Pair tile: 256 rows of one group (128 per CTA) x 256 accumulator columns.
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile_pair(const SmemTail& st, const TcParams& p, int id, int rank) {
+    Tile t;
+    t.prob = (id < st.total[0]) ? 0 : 1;
+    const int local = id - (t.prob ? st.total[0] : 0);
+    const int gb = st.gbase[t.prob];
+    const int* ts = st.tile_start + gb;
+    int lo = 0, hi = p.G[t.prob] - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ts[mid] <= local) lo = mid;
+        else hi = mid - 1;
+    }
+    t.g = lo;
+    const int rows = st.rows[gb + lo];
+    const int mt = (rows + 2 * BM - 1) / (2 * BM);
+    const int r = local - ts[lo];
+    t.ks = 0;
+    t.n = r / mt;
+    t.m = r - t.n * mt;
+    const int first = t.m * 2 * BM + rank * BM;  // this CTA's first row inside the group
+    t.a_row0 = st.row0[gb + lo] + first;
+    t.rows_valid = min(BM, rows - first);  // may be <= 0 for the upper half of a tail tile
+    t.kb0 = 0;
+    t.kb1 = (p.K[t.prob] + BK - 1) / BK;
+    return t;
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_tc_pair_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int NST = PAIR_STAGES;
+    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)NST * PAIR_STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (int)cluster_rank();
+    const bool leader = rank == 0;
+    const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    volatile int* abort_flag = &st.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&st.full[s], 1);   // leader: one arrive (with the pair's bytes)
+            mbar_init(&st.empty[s], 1);  // one multicast MMA commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&st.tmem_full[a], 1);
+            mbar_init(&st.tmem_empty[a], 8);  // leader: 4 epilogue warps in each CTA
+        }
+        st.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        for (int q = 0; q < p.nprob; ++q) {
+            prefetch_tmap(&p.tmA[q]);
+            prefetch_tmap(&p.tmB1[q]);
+            if (MODE == kGemmSwiGLU) prefetch_tmap(&p.tmB2[q]);
+        }
+    }
+    if (warp == 1) {  // both CTAs of the pair allocate together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&st.tmem_base)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    if (warp == 2) {
+        for (int q = 0; q < 2; ++q) {
+            int carry = 0;
+            const int gb = q == 0 ? 0 : p.G[0];
+            if (lane == 0) st.gbase[q] = gb;
+            if (q < p.nprob) {
+                const int ncb = (p.N[q] + out_cols_per_tile<MODE>() - 1) / out_cols_per_tile<MODE>();
+                for (int base = 0; base < p.G[q]; base += 32) {
+                    const int g = base + lane;
+                    int tiles = 0;
+                    if (g < p.G[q]) {
+                        int lo = 0, hi = p.M[q];
+                        if (p.offsets[q]) {
+                            lo = p.offsets[q][g];
+                            hi = p.offsets[q][g + 1];
+                        }
+                        if (lo < 0 || hi < lo || hi > p.a_rows[q]) {
+                            record_status(p.status, kStatusBounds);
+                            lo = hi = 0;
+                        }
+                        st.row0[gb + g] = lo;
+                        st.rows[gb + g] = hi - lo;
+                        tiles = ((hi - lo + 2 * BM - 1) / (2 * BM)) * ncb;
+                    }
+                    int incl = tiles;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    if (g < p.G[q]) st.tile_start[gb + g] = carry + incl - tiles;
+                    carry += __shfl_sync(0xffffffffu, incl, 31);
+                }
+            }
+            if (lane == 0) st.total[q] = carry;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers are initialised before anyone signals them
+    tc_fence_after();
+    const uint32_t tmem_base = st.tmem_base;
+    const int total_tiles = st.total[0] + st.total[1];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_parity[NST];
+            bool used[NST];
+            for (int i = 0; i < NST; ++i) used[i] = false;
+            bool dead = p.stall_producer != 0;
+            for (int id = cluster_id; id < total_tiles && !dead; id += nclusters) {
+                const Tile t = decode_tile_pair<MODE>(st, p, id, rank);
+                int b_row;  // this CTA's half of the B tile
+                const CUtensorMap* tmb;
+                if (MODE == kGemmSwiGLU) {  // rank 0: the W1 (gate) rows, rank 1: the W3 (up) rows
+                    b_row = t.g * p.N[t.prob] + t.n * (BN / 2);
+                    tmb = rank == 0 ? &p.tmB1[t.prob] : &p.tmB2[t.prob];
+                } else {
+                    b_row = t.g * p.N[t.prob] + t.n * BN + rank * (BN / 2);
+                    tmb = &p.tmB1[t.prob];
+                }
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
+                        dead = true;
+                        break;
+                    }
+                    uint8_t* sa = smem + (size_t)s * PAIR_STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    const uint32_t full_leader = leader_addr(&st.full[s]);
+                    if (leader) mbar_expect_tx(&st.full[s], 2 * PAIR_STAGE_BYTES);
+                    tma_load_2d_pair(sa, &p.tmA[t.prob], kb * BK, t.a_row0, full_leader);
+                    tma_load_2d_pair(sb, tmb, kb * BK, b_row, full_leader);
+                    issued_parity[s] = ph;
+                    used[s] = true;
+                    if (++s == NST) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // Copies of the leader land on its own barrier; wait for those.  The
+            // peer's copies are covered by the leader's wait and the final
+            // cluster barrier.
+            if (leader) {
+                volatile int no_abort = 0;
+                for (int i = 0; i < NST; ++i)
+                    if (used[i]) mbar_wait(&st.full[i], issued_parity[i], &no_abort, nullptr, kDrainLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool dead = false;
+            for (int id = cluster_id; id < total_tiles && !dead; id += nclusters, ++it) {
+                const Tile t = decode_tile_pair<MODE>(st, p, id, 0);
+                const int acc = it & 1;
+                const uint32_t use = static_cast<uint32_t>(it >> 1);
+                if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
+                tc_fence_after();
+                const uint32_t dtm = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(&st.full[s], ph, abort_flag, p.status, p.wait_limit_ns)) {
+                        dead = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * PAIR_STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        umma_bf16_pair(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2), sdesc_k_sw128(sb + kk * UMMA_K * 2),
+                                       idesc, (kb != t.kb0 || kk != 0) ? 1u : 0u);
+                    umma_commit_pair(&st.empty[s]);
+                    if (++s == NST) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (dead) break;
+                umma_commit_pair(&st.tmem_full[acc]);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int row_in_tile = quarter * 32 + lane;
+        int it = 0;
+        for (int id = cluster_id; id < total_tiles; id += nclusters, ++it) {
+            const Tile t = decode_tile_pair<MODE>(st, p, id, rank);
+            const int acc = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status, p.wait_limit_ns)) break;
+            tc_fence_after();
+            const uint32_t tacc =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            epilogue_tile<MODE>(p, t, tacc, row_in_tile, st.stage[quarter]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_addr(&st.tmem_empty[acc]));
+        }
+    }
+
+    // ---- teardown: neither CTA leaves while its peer may still touch its
+    // shared memory or barriers; then the pair frees its TMEM together ----
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {
+        }
+    }
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    }
+}
+
 // ----------------------------------------------------------------- host side
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -685,15 +980,46 @@ cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <int MODE>
+cudaError_t launch_pair_mode(const TcParams& prm, int num_sms, cudaStream_t s) {
+    static uint64_t attr_set_mask = 0;
+    static int max_clusters[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (!bit || !(attr_set_mask & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_pair_kernel<MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(pair_smem_bytes()));
+        if (e != cudaSuccess) return e;
+        // persistent grid: only as many pairs as can be resident at once
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms / 2));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = pair_smem_bytes();
+        int nc = 0;
+        e = cudaOccupancyMaxActiveClusters(&nc, grouped_gemm_tc_pair_kernel<MODE>, &cfg);
+        if (e != cudaSuccess || nc < 1) return e != cudaSuccess ? e : cudaErrorLaunchOutOfResources;
+        if (dev < 64) max_clusters[dev] = nc;
+        attr_set_mask |= bit;
+    }
+    const int nc = dev < 64 ? max_clusters[dev] : 1;
+    const int clusters = nc < num_sms / 2 ? nc : num_sms / 2;
+    grouped_gemm_tc_pair_kernel<MODE><<<2 * clusters, NUM_THREADS, pair_smem_bytes(), s>>>(prm);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
-                           cudaStream_t s, int ksplit) {
+                           cudaStream_t s, int ksplit, bool pair) {
     if (nprob < 1 || nprob > 2 || ksplit < 1) return cudaErrorInvalidValue;
     TcParams prm;
     memset(&prm, 0, sizeof(prm));
     prm.ksplit = ksplit;
-    const int b_box = (mode == kGemmSwiGLU) ? BN / 2 : BN;
+    // rows of B per TMA box: half the tile for SwiGLU (the W1 / W3 halves) and,
+    // in either mode, on a CTA pair (each CTA holds half of the N columns)
+    const int b_box = (mode == kGemmSwiGLU || pair) ? BN / 2 : BN;
     if (probs[0].G + (nprob > 1 ? probs[1].G : 0) > MAX_GROUPS + 1) return cudaErrorInvalidValue;
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
@@ -738,6 +1064,15 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         prm.wait_limit_ns = 20000000ull;  // 20 ms
     }
     const int grid = num_sms > 0 ? num_sms : 148;
+    if (pair) {
+        // 2-SM tiles: plain A tiles only (no split-K, no gathered or split A)
+        if (ksplit != 1 || prm.a_gather[0] || prm.a_gather[1]) return cudaErrorInvalidValue;
+        switch (mode) {
+            case kGemmSwiGLU: return launch_pair_mode<kGemmSwiGLU>(prm, grid, s);
+            case kGemmScale: return launch_pair_mode<kGemmScale>(prm, grid, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (mode) {
         case kGemmSwiGLU: return launch_mode<kGemmSwiGLU>(prm, grid, s);
         case kGemmScale: return launch_mode<kGemmScale>(prm, grid, s);

@@ -40,6 +40,9 @@ SMALL = [
              h_split=True),
     Workload("decode_like_t5_bf16", T=5, d=512, E=8, F=512, k=2),
     Workload("many_tiles_bf16", T=1000, d=256, E=4, F=640, k=2),
+    # >= 512 rows per expert: both GEMMs run on CTA pairs (256-row tiles whose
+    # upper half may be empty at a segment end; N tail of 64 in the down GEMM)
+    Workload("pair_tiles_shared_bf16", T=1100, d=320, E=4, F=384, k=2, n_shared=1, F_s=256),
 ]
 
 
