@@ -59,6 +59,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch of tokens_per_rank
+    per step (weak scaling), and the job takes the slowest rank's time."""
+    return world * tokens_per_rank * steps / (elapsed_ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -303,11 +320,7 @@ def run_ours(args):
     barrier()
     clocks.mark(wall0, wall1)
     launches = moe.launch_count() - launches0
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), world, dev)
     st = fw.device_status()
     if st != 0:
         raise moe.MoeError(st, "timed-region device status")
@@ -318,7 +331,7 @@ def run_ours(args):
     touched = int((fw.stats["counts"] > 0).sum().item())
 
     ms_per_step = ms / args.steps
-    value = world * w.T * args.steps / (ms / 1e3)
+    value = job_throughput(w.T, world, args.steps, ms)
 
     # roofline of the dominant kernel (up GEMM + fused SwiGLU)
     peaks, peak_src = load_peaks()
@@ -363,13 +376,9 @@ def run_ours(args):
         y_h.copy_(y, non_blocking=True)
     e1.record(stream)
     e1.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     clocks.stop()
-    e2e = {"value": round(world * w.T * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+    e2e = {"value": round(job_throughput(w.T, world, args.steps, e2e_ms), 1), "unit": UNIT,
            "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
            "d2h_bytes_per_step": y_h.numel() * y_h.element_size()}
 
