@@ -309,7 +309,9 @@ def run_ours(args):
     launches0 = moe.launch_count()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.monotonic()
-    with moe.StageTimer(args.steps) as timer:
+    # timed region: only the dominant kernel (up GEMM) is bracketed by events,
+    # so the other launches keep their programmatic overlap
+    with moe.StageTimer(args.steps, stages=("up_gemm",)) as timer:
         start.record(stream)
         for _ in range(args.steps):
             timer.begin_call()
@@ -319,13 +321,20 @@ def run_ours(args):
     wall1 = time.monotonic()
     barrier()
     clocks.mark(wall0, wall1)
-    launches = moe.launch_count() - launches0
+    launches = moe.launch_count() - launches0  # kernels launched inside the timed region
+    up_ms_live, up_n = timer.ms()
+    timer.close()
+    # per-stage breakdown in a separate loop (every stage bracketed)
+    with moe.StageTimer(args.steps) as br:
+        for _ in range(args.steps):
+            br.begin_call()
+            fw(x, y)
+    stage_ms, stage_n = br.ms()
+    br.close()
     ms = max_over_ranks(start.elapsed_time(end), world, dev)
     st = fw.device_status()
     if st != 0:
         raise moe.MoeError(st, "timed-region device status")
-    stage_ms, stage_n = timer.ms()
-    timer.close()
     kept_total = int(fw.stats["kept"].sum().item())
     n_dropped = int(fw.stats["n_dropped"].item())
     touched = int((fw.stats["counts"] > 0).sum().item())
@@ -338,7 +347,7 @@ def run_ours(args):
     up_flops = 2.0 * kept_total * w.d * 2 * w.F + 2.0 * w.T * w.d * 2 * w.F_s * w.n_shared
     down_flops = 2.0 * kept_total * w.d * w.F + 2.0 * w.T * w.d * w.F_s * w.n_shared
     per = {s: (stage_ms[s] / stage_n[s] if stage_n[s] else None) for s in moe.STAGES}
-    up_ms = per["up_gemm"]
+    up_ms = up_ms_live["up_gemm"] / up_n["up_gemm"]  # live, inside the timed region
     layer_flops = moe_inputs.algorithmic_flops(w, kept_total)
     wbytes = moe_inputs.expert_weight_bytes(w, touched)
     tensor_bound = w.T * w.k >= 512  # below that the GEMMs stream weights from HBM

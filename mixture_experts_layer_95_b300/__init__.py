@@ -109,11 +109,12 @@ class StageTimer:
     The events are plain cudart events owned by this object.
     """
 
-    def __init__(self, n_calls: int = 0):
+    def __init__(self, n_calls: int = 0, stages=STAGES):
         from cuda.bindings import runtime as cudart
         self._rt = cudart
         self._events = []
         self._used = 0
+        self._want = set(stages)  # stages not listed get no events (their launches stay back to back)
         for _ in range(n_calls):  # create up front so timed loops pay no creation cost
             self._events.append(self._new_set())
 
@@ -132,7 +133,8 @@ class StageTimer:
             self._events.append(self._new_set())
         ev = self._events[self._used]
         self._used += 1
-        self._arr = (ctypes.c_void_p * len(ev))(*[int(e) for e in ev])  # kept alive while set
+        handles = [int(e) if STAGES[i // 2] in self._want else None for i, e in enumerate(ev)]
+        self._arr = (ctypes.c_void_p * len(ev))(*handles)  # kept alive while set
         _check(lib().moe_set_stage_events(self._arr, len(ev)), "moe_set_stage_events")
 
     def __enter__(self):
@@ -150,6 +152,8 @@ class StageTimer:
         counts = {s: 0 for s in STAGES}
         for ev in self._events[:self._used]:
             for i, s in enumerate(STAGES):
+                if s not in self._want:
+                    continue
                 err, ms = rt.cudaEventElapsedTime(ev[2 * i], ev[2 * i + 1])
                 if err == rt.cudaError_t.cudaSuccess:  # stages a call did not run stay unrecorded
                     out[s] += ms

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
                                                       const int32_t* __restrict__ slot_pos,
                                                       const float* __restrict__ y_shared, size_t shared_stride,
                                                       int shared_nsplit, T* __restrict__ y) {
+    pdl_wait();
     const int chunks = (d + 255) / 256;
     const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(int rows_max, cons
                                                               int N, int ksplit, const float* __restrict__ part,
                                                               __nv_bfloat16* __restrict__ h,
                                                               __nv_bfloat16* __restrict__ h_lo) {
+    pdl_wait();
     const int rows = rows_dev ? min(*rows_dev, rows_max) : rows_max;
     const size_t stride = (size_t)rows_max * 2 * N;
     const int q4 = N / 4;
@@ -128,12 +130,15 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(int rows_max, cons
             *reinterpret_cast<uint2*>(h_lo + r * N + f) = pk;
         }
     }
+    __syncthreads();
+    pdl_trigger();
 }
 
 // out[r][c] = sum over slices of part[s][r][c], slices in order.
 __global__ void __launch_bounds__(256) reduce_partials_kernel(int rows_max, const int32_t* __restrict__ rows_dev,
                                                               int N, int ksplit, const float* __restrict__ part,
                                                               float* __restrict__ out) {
+    pdl_wait();
     const int rows = rows_dev ? min(*rows_dev, rows_max) : rows_max;
     const size_t stride = (size_t)rows_max * N;
     const int q4 = N / 4;
@@ -145,6 +150,8 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(int rows_max, cons
         for (int sl = 1; sl < ksplit; ++sl) add4(acc, __ldg(reinterpret_cast<const float4*>(part + sl * stride + r * N + c)));
         *reinterpret_cast<float4*>(out + r * N + c) = acc;
     }
+    __syncthreads();
+    pdl_trigger();
 }
 
 int grid_for(size_t work, int per_block) {
@@ -154,6 +161,7 @@ int grid_for(size_t work, int per_block) {
 
 __global__ void load_stats_kernel(int Tn, int E, int k, float alpha, const int32_t* __restrict__ counts,
                                   const float* __restrict__ p_mean, float* __restrict__ f, float* __restrict__ L) {
+    pdl_wait();
     __shared__ float s_red[256];
     float part = 0.f;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -172,6 +180,7 @@ __global__ void load_stats_kernel(int Tn, int E, int k, float alpha, const int32
 
 __global__ void bias_update_kernel(int Tn, int E, int k, const int32_t* __restrict__ counts, float gamma,
                                    float* __restrict__ bias) {
+    pdl_wait();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E) return;
     const long long scaled = (long long)counts[e] * E, total = (long long)Tn * k;
@@ -182,7 +191,7 @@ __global__ void bias_update_kernel(int Tn, int E, int k, const int32_t* __restri
 }  // namespace
 
 cudaError_t launch_bias_update(int T, int E, int k, const int32_t* counts, float gamma, float* bias, cudaStream_t s) {
-    bias_update_kernel<<<(E + 255) / 256, 256, 0, s>>>(T, E, k, counts, gamma, bias);
+    launch_pdl(bias_update_kernel, dim3((E + 255) / 256), dim3(256), 0, s, T, E, k, counts, gamma, bias);
     return cudaGetLastError();
 }
 
@@ -193,11 +202,11 @@ cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_
     const long long warps = (long long)T * ((d + 255) / 256);
     const int grid = (int)((warps + 7) / 8);
     if (dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
+        launch_pdl(combine_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
                                                            shared_stride, shared_nsplit,
                                                            static_cast<__nv_bfloat16*>(y));
     else
-        combine_kernel<float><<<grid, 256, 0, s>>>(T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
+        launch_pdl(combine_kernel<float>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
                                                    shared_stride, shared_nsplit, static_cast<float*>(y));
     return cudaGetLastError();
 }
@@ -210,7 +219,7 @@ cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, 
 cudaError_t launch_swiglu_finalize(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
                                    void* h, void* h_lo, cudaStream_t s) {
     if (rows_max == 0) return cudaSuccess;
-    swiglu_finalize_kernel<<<grid_for((size_t)rows_max * (N / 4), 256), 256, 0, s>>>(
+    launch_pdl(swiglu_finalize_kernel, dim3(grid_for((size_t)rows_max * (N / 4), 256)), dim3(256), 0, s, 
         rows_max, rows_dev, N, ksplit, part, static_cast<__nv_bfloat16*>(h), static_cast<__nv_bfloat16*>(h_lo));
     return cudaGetLastError();
 }
@@ -218,14 +227,14 @@ cudaError_t launch_swiglu_finalize(int rows_max, const int32_t* rows_dev, int N,
 cudaError_t launch_reduce_partials(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
                                    float* out, cudaStream_t s) {
     if (rows_max == 0) return cudaSuccess;
-    reduce_partials_kernel<<<grid_for((size_t)rows_max * (N / 4), 256), 256, 0, s>>>(rows_max, rows_dev, N, ksplit,
+    launch_pdl(reduce_partials_kernel, dim3(grid_for((size_t)rows_max * (N / 4), 256)), dim3(256), 0, s, rows_max, rows_dev, N, ksplit,
                                                                                      part, out);
     return cudaGetLastError();
 }
 
 cudaError_t launch_load_stats(int T, int E, int k, float alpha, const int32_t* counts, const float* p_mean,
                               float* f, float* L, cudaStream_t s) {
-    load_stats_kernel<<<1, 256, 0, s>>>(T, E, k, alpha, counts, p_mean, f, L);
+    launch_pdl(load_stats_kernel, dim3(1), dim3(256), 0, s, T, E, k, alpha, counts, p_mean, f, L);
     return cudaGetLastError();
 }
 

@@ -55,6 +55,32 @@ inline int router_chunk(int T, int E, int d, int dtype) {
 constexpr int kStatusTimeout = MOE_ERR_TIMEOUT;
 constexpr int kStatusBounds = MOE_ERR_DEVICE_BOUNDS;
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with launch_pdl and calls pdl_wait() before its first global-memory access.
+// A dependent may rely only on what its predecessor wrote before triggering,
+// so a kernel triggers (pdl_trigger) only after its CTA's last global write
+// -- or not at all, which triggers at exit.  What overlaps is the successor's
+// launch and its memory-free prologue (barrier set-up, TMEM allocation,
+// tensor-map prefetch) with the predecessor's last CTAs.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ void record_status(int* status, int code) {
     if (status) atomicCAS(status, 0, code);
 }

@@ -29,6 +29,7 @@ struct SimtParams {
 
 template <int MODE>
 __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams p) {
+    pdl_wait();
     __shared__ int s_start[2][SMAXG + 1];
     __shared__ int s_row0[2][SMAXG];
     __shared__ int s_rows[2][SMAXG];
@@ -126,6 +127,8 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams
             }
         }
     }
+    __syncthreads();
+    pdl_trigger();
 }
 
 }  // namespace
@@ -155,9 +158,9 @@ cudaError_t launch_gemm_simt_f32(int mode, const GemmProblem* probs, int nprob, 
     if (tiles_max == 0) return cudaSuccess;
     const int grid = static_cast<int>(tiles_max < 65535 ? tiles_max : 65535);
     switch (mode) {
-        case kGemmSwiGLU: grouped_gemm_simt_kernel<kGemmSwiGLU><<<grid, 256, 0, s>>>(prm); break;
-        case kGemmScale: grouped_gemm_simt_kernel<kGemmScale><<<grid, 256, 0, s>>>(prm); break;
-        case kGemmPlain: grouped_gemm_simt_kernel<kGemmPlain><<<grid, 256, 0, s>>>(prm); break;
+        case kGemmSwiGLU: launch_pdl(grouped_gemm_simt_kernel<kGemmSwiGLU>, dim3(grid), dim3(256), 0, s, prm); break;
+        case kGemmScale: launch_pdl(grouped_gemm_simt_kernel<kGemmScale>, dim3(grid), dim3(256), 0, s, prm); break;
+        case kGemmPlain: launch_pdl(grouped_gemm_simt_kernel<kGemmPlain>, dim3(grid), dim3(256), 0, s, prm); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

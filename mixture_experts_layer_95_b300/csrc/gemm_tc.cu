@@ -453,6 +453,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    // everything above touched no global memory: overlap it with the predecessor
+    pdl_wait();
     if (warp == 2) {
         // tiles per group: ceil(rows / BM) * column blocks; warp-wide prefix sum
         for (int q = 0; q < 2; ++q) {
@@ -636,6 +638,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
     }
+    pdl_trigger();  // every epilogue store of this CTA precedes the teardown barrier
 }
 
 // ------------------------------------------------------- 2-SM (CTA pair) kernel
@@ -769,6 +772,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
     }
+    pdl_wait();
     if (warp == 2) {
         for (int q = 0; q < 2; ++q) {
             int carry = 0;
@@ -929,6 +933,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
     }
+    pdl_trigger();
 }
 
 // ----------------------------------------------------------------- host side
@@ -976,7 +981,7 @@ cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set_mask |= bit;
     }
-    grouped_gemm_tc_kernel<MODE><<<grid, NUM_THREADS, smem_bytes<MODE>(), s>>>(prm);
+    launch_pdl(grouped_gemm_tc_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), smem_bytes<MODE>(), s, prm);
     return cudaGetLastError();
 }
 
@@ -1005,7 +1010,7 @@ cudaError_t launch_pair_mode(const TcParams& prm, int num_sms, cudaStream_t s) {
     }
     const int nc = dev < 64 ? max_clusters[dev] : 1;
     const int clusters = nc < num_sms / 2 ? nc : num_sms / 2;
-    grouped_gemm_tc_pair_kernel<MODE><<<2 * clusters, NUM_THREADS, pair_smem_bytes(), s>>>(prm);
+    launch_pdl(grouped_gemm_tc_pair_kernel<MODE>, dim3(2 * clusters), dim3(NUM_THREADS), pair_smem_bytes(), s, prm);
     return cudaGetLastError();
 }
 

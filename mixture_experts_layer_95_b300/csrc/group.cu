@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kRouterThreads) group_hist_kernel(int Tn, int 
                                                                      const int32_t* __restrict__ ids,
                                                                      int32_t* __restrict__ block_hist,
                                                                      int* status) {
+    pdl_wait();
     extern __shared__ int s_hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
@@ -47,6 +48,8 @@ __global__ void __launch_bounds__(kRouterThreads) group_hist_kernel(int Tn, int 
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) block_hist[(size_t)blockIdx.x * E + e] = s_hist[e];
+    __syncthreads();
+    pdl_trigger();
 }
 
 // Exclusive scan over v[0..n) in shared memory (n <= kMaxExperts), result in
@@ -97,6 +100,7 @@ struct ScanArgs {
 };
 
 __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs a) {
+    pdl_wait();
     extern __shared__ int s_mem[];
     const int E = a.E;
     int* s_before = s_mem;                 // [E]   this block's starting rank per expert
@@ -212,6 +216,8 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
             }
         }
     }
+    __syncthreads();
+    pdl_trigger();
 }
 
 template <typename T>
@@ -219,6 +225,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int Tn, int d, const i
                                                           const int32_t* __restrict__ sorted_token_ids,
                                                           const T* __restrict__ x, T* __restrict__ x_perm,
                                                           int rows_max, int* status) {
+    pdl_wait();
     const int total = min(*offsets_end, rows_max);
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -233,6 +240,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int Tn, int d, const i
         uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)row * d);
         for (int c = lane; c < d / vec; c += 32) dst[c] = __ldg(src + c);
     }
+    __syncthreads();
+    pdl_trigger();
 }
 
 }  // namespace
@@ -241,7 +250,7 @@ cudaError_t launch_group_hist(int T, int E, int k, int chunk, const int32_t* top
                               int* status, cudaStream_t s) {
     const int nblk = (T + chunk - 1) / chunk;
     if (nblk == 0) return cudaSuccess;
-    group_hist_kernel<<<nblk, kRouterThreads, E * sizeof(int), s>>>(T, E, k, chunk, topk_ids, block_hist, status);
+    launch_pdl(group_hist_kernel, dim3(nblk), dim3(kRouterThreads), E * sizeof(int), s, T, E, k, chunk, topk_ids, block_hist, status);
     return cudaGetLastError();
 }
 
@@ -254,7 +263,7 @@ cudaError_t launch_group_scan(int T, int E, int k, int chunk, int capacity, cons
     const size_t smem = sizeof(int) * ((size_t)3 * E + 1 + (size_t)kScanWarps * E + kScanWarps + 1) +
                         sizeof(float) * kScanThreads;
     cudaFuncSetAttribute(group_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    group_scan_kernel<<<nblk, kScanThreads, smem, s>>>(a);
+    launch_pdl(group_scan_kernel, dim3(nblk), dim3(kScanThreads), smem, s, a);
     return cudaGetLastError();
 }
 
@@ -268,11 +277,11 @@ cudaError_t launch_gather_rows(int dtype, int T, int d, int rows_max, const int3
     const int want = (rows_max + 7) / 8;  // 8 warps per block, one row per warp
     const int grid = want < sms * 8 ? want : sms * 8;
     if (dtype == MOE_BF16)
-        gather_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(T, d, offsets_end, sorted_token_ids,
+        launch_pdl(gather_rows_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, T, d, offsets_end, sorted_token_ids,
                                                                static_cast<const __nv_bfloat16*>(x),
                                                                static_cast<__nv_bfloat16*>(x_perm), rows_max, status);
     else
-        gather_rows_kernel<float><<<grid, 256, 0, s>>>(T, d, offsets_end, sorted_token_ids,
+        launch_pdl(gather_rows_kernel<float>, dim3(grid), dim3(256), 0, s, T, d, offsets_end, sorted_token_ids,
                                                        static_cast<const float*>(x), static_cast<float*>(x_perm),
                                                        rows_max, status);
     return cudaGetLastError();

@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
     const float* __restrict__ logit_bias, const float* __restrict__ select_bias, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
     int32_t* __restrict__ block_hist) {
+    pdl_wait();
     constexpr int kW = kWarpRouterThreads / 32;
     constexpr int kTpw = kWarpRouterChunk / kW;
     constexpr int VE = Vec<T>::kElems;
@@ -213,6 +214,8 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
         softmax_topk<1>(t0 + q, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
     }
     block_epilogue<1, kW>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
+    __syncthreads();
+    pdl_trigger();  // after this block's last global write
 }
 
 // Router for decode-sized batches: one block per token, the d dimension split
@@ -226,6 +229,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_split_d_kernel(
     const float* __restrict__ logit_bias, const float* __restrict__ select_bias, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
     int32_t* __restrict__ block_hist) {
+    pdl_wait();
     constexpr int VE = Vec<T>::kElems;
     constexpr int kW = kRouterThreads / 32;
     __shared__ float s_red[kW][NE];
@@ -277,6 +281,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
     int Tn, int E, int k, const float* __restrict__ logits, const float* __restrict__ logit_bias,
     const float* __restrict__ select_bias, int renormalize, int32_t* __restrict__ topk_ids,
     float* __restrict__ gates, float* __restrict__ p_part, int32_t* __restrict__ block_hist) {
+    pdl_wait();
     extern __shared__ float s_dyn[];
     float* s_p = s_dyn;
     int* s_h = reinterpret_cast<int*>(s_dyn + kWarps * E);
@@ -300,9 +305,12 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
         softmax_topk<NJ>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
     }
     block_epilogue<NJ, kWarps>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
+    __syncthreads();
+    pdl_trigger();
 }
 
 __global__ void p_mean_kernel(int Tn, int E, int nblk, const float* __restrict__ p_part, float* __restrict__ p_mean) {
+    pdl_wait();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E) return;
     float s = 0.f;
@@ -326,7 +334,7 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
         cudaError_t e_ = cudaFuncSetAttribute(router_warp_kernel<TY, NE>,                                       \
                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);          \
         if (e_ != cudaSuccess) return e_;                                                                       \
-        router_warp_kernel<TY, NE><<<grid, block, smem, s>>>(T, d, E, k, static_cast<const TY*>(x),           \
+        launch_pdl(router_warp_kernel<TY, NE>, dim3(grid), dim3(block), smem, s, T, d, E, k, static_cast<const TY*>(x),           \
                                                              static_cast<const TY*>(w_gate), logit_bias,       \
                                                              select_bias, renormalize, topk_ids, gates, p_part, \
                                                              block_hist);                                       \
@@ -348,7 +356,7 @@ cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const v
                                   cudaStream_t s) {
     if (T == 0) return cudaSuccess;
 #define MOE_SPLITD_CASE(TY, NE)                                                                              \
-    router_split_d_kernel<TY, NE><<<T, kRouterThreads, 0, s>>>(T, d, E, k, static_cast<const TY*>(x),       \
+    launch_pdl(router_split_d_kernel<TY, NE>, dim3(T), dim3(kRouterThreads), 0, s, T, d, E, k, static_cast<const TY*>(x),       \
                                                                static_cast<const TY*>(w_gate), logit_bias,  \
                                                                select_bias, renormalize, topk_ids, gates,  \
                                                                p_part, block_hist)
@@ -375,7 +383,7 @@ cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, 
 #define MOE_LOGITS_CASE(NJ)                                                                                  \
     do {                                                                                                     \
         cudaFuncSetAttribute(router_logits_kernel<NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-        router_logits_kernel<NJ><<<grid, block, smem, s>>>(T, E, k, logits, logit_bias, select_bias,       \
+        launch_pdl(router_logits_kernel<NJ>, dim3(grid), dim3(block), smem, s, T, E, k, logits, logit_bias, select_bias,       \
                                                            renormalize, topk_ids, gates, p_part, block_hist); \
     } while (0)
     if (E <= 64) MOE_LOGITS_CASE(2);
@@ -386,7 +394,7 @@ cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, 
 }
 
 cudaError_t launch_p_mean(int T, int E, int nblk, const float* p_part, float* p_mean, cudaStream_t s) {
-    p_mean_kernel<<<(E + 255) / 256, 256, 0, s>>>(T, E, nblk, p_part, p_mean);
+    launch_pdl(p_mean_kernel, dim3((E + 255) / 256), dim3(256), 0, s, T, E, nblk, p_part, p_mean);
     return cudaGetLastError();
 }
 
