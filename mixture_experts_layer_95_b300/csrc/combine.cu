@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
         if (pos < 0 || !active) continue;
         const float4* src = reinterpret_cast<const float4*>(y_perm + (size_t)pos * d + c);
         float4 p0 = __ldg(src), p1 = __ldg(src + 1);
-        for (int sl = 1; sl < nsplit; ++sl) {
+#pragma unroll 8
+        for (int sl = 1; sl < nsplit; ++sl) {  // independent loads: keep them in flight together
             const float4* q = reinterpret_cast<const float4*>(y_perm + sl * perm_stride + (size_t)pos * d + c);
             add4(p0, __ldg(q));
             add4(p1, __ldg(q + 1));
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
     if (y_shared) {
         const float4* src = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
         float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+#pragma unroll 8
         for (int sl = 1; sl < shared_nsplit; ++sl) {
             const float4* q = reinterpret_cast<const float4*>(y_shared + sl * shared_stride + (size_t)t * d + c);
             add4(p0, __ldg(q));
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(int rows_max, cons
         const float* gp = part + r * 2 * N + f;
         float4 g = __ldg(reinterpret_cast<const float4*>(gp));
         float4 u = __ldg(reinterpret_cast<const float4*>(gp + N));
+#pragma unroll 8
         for (int sl = 1; sl < ksplit; ++sl) {
             add4(g, __ldg(reinterpret_cast<const float4*>(gp + sl * stride)));
             add4(u, __ldg(reinterpret_cast<const float4*>(gp + sl * stride + N)));
@@ -147,7 +150,9 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(int rows_max, cons
         const size_t r = i / q4;
         const int c = (int)(i - r * q4) * 4;
         float4 acc = __ldg(reinterpret_cast<const float4*>(part + r * N + c));
-        for (int sl = 1; sl < ksplit; ++sl) add4(acc, __ldg(reinterpret_cast<const float4*>(part + sl * stride + r * N + c)));
+#pragma unroll 8
+        for (int sl = 1; sl < ksplit; ++sl)
+            add4(acc, __ldg(reinterpret_cast<const float4*>(part + sl * stride + r * N + c)));
         *reinterpret_cast<float4*>(out + r * N + c) = acc;
     }
     __syncthreads();

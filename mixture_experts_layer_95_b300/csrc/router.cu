@@ -27,6 +27,7 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = kRouterThreads / 32;
+constexpr int kSplitDThreads = 512;  // one-block-per-token router: d split over 512 threads
 constexpr int kTokensPerWarp = kRouterTokensPerBlock / kWarps;
 
 // Softmax, top-k and gate epilogue shared by both kernels.  Lane L holds the
@@ -224,14 +225,14 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
 // reduced across the block in a fixed order; warp 0 then runs the shared
 // softmax/top-k epilogue.  Histogram and p rows are per token (chunk = 1).
 template <typename T, int NE>
-__global__ void __launch_bounds__(kRouterThreads) router_split_d_kernel(
+__global__ void __launch_bounds__(kSplitDThreads) router_split_d_kernel(
     int Tn, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ wg,
     const float* __restrict__ logit_bias, const float* __restrict__ select_bias, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
     int32_t* __restrict__ block_hist) {
     pdl_wait();
     constexpr int VE = Vec<T>::kElems;
-    constexpr int kW = kRouterThreads / 32;
+    constexpr int kW = kSplitDThreads / 32;
     __shared__ float s_red[kW][NE];
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_split_d_kernel(
     float acc[NE];
 #pragma unroll
     for (int e = 0; e < NE; ++e) acc[e] = 0.f;
-    for (int v = threadIdx.x; v < nv; v += kRouterThreads) {
+    for (int v = threadIdx.x; v < nv; v += kSplitDThreads) {
         float xv[VE];
         widen(__ldg(xr + v), xv, static_cast<const T*>(nullptr));
 #pragma unroll
@@ -356,7 +357,7 @@ cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const v
                                   cudaStream_t s) {
     if (T == 0) return cudaSuccess;
 #define MOE_SPLITD_CASE(TY, NE)                                                                              \
-    launch_pdl(router_split_d_kernel<TY, NE>, dim3(T), dim3(kRouterThreads), 0, s, T, d, E, k, static_cast<const TY*>(x),       \
+    launch_pdl(router_split_d_kernel<TY, NE>, dim3(T), dim3(kSplitDThreads), 0, s, T, d, E, k, static_cast<const TY*>(x),       \
                                                                static_cast<const TY*>(w_gate), logit_bias,  \
                                                                select_bias, renormalize, topk_ids, gates,  \
                                                                p_part, block_hist)
