@@ -351,20 +351,24 @@ def run_ours(args):
     layer_flops = moe_inputs.algorithmic_flops(w, kept_total)
     wbytes = moe_inputs.expert_weight_bytes(w, touched)
     tensor_bound = w.T * w.k >= 512  # below that the GEMMs stream weights from HBM
+    plan = moe.plan_describe(layer_of(w).cfg())
+    up_kernel = {"tc_pair": "grouped_gemm_tc_pair_kernel<SwiGLU> (up GEMM, CTA pairs)",
+                 "tc": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)",
+                 "simt": "grouped_gemm_simt_kernel<SwiGLU> (up GEMM)"}[plan["up"]]
     if tensor_bound:
         achieved = up_flops / (up_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4),
                 "traffic": recorded_traffic(args.workload),
-                "kernel": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)", "peak_source": f"{peak_src} bf16 burst",
+                "kernel": up_kernel, "peak_source": f"{peak_src} bf16 burst",
                 "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4)}
     else:
         up_bytes = wbytes * 2.0 / 3.0
         achieved = up_bytes / (up_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": recorded_traffic(args.workload),
-                "kernel": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)", "peak_source": f"{peak_src} HBM copy",
+                "kernel": up_kernel, "peak_source": f"{peak_src} HBM copy",
                 "algorithmic_bytes_per_launch": up_bytes, "launch_ms": round(up_ms, 4)}
 
     # end to end through the public API: host batch in, host result out
@@ -405,7 +409,8 @@ def run_ours(args):
                   "expert_weight_gbs": round(wbytes / (ms_per_step / 1e3) / 1e9, 1),
                   "frac_hbm": round(wbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                   "stage_ms": {s: (round(v, 4) if v is not None else None) for s, v in per.items()},
-                  "kept_entries": kept_total, "dropped_entries": n_dropped, "experts_touched": touched},
+                  "kept_entries": kept_total, "dropped_entries": n_dropped, "experts_touched": touched,
+                  "plan": plan},
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),

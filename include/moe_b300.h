@@ -247,6 +247,16 @@ MOE_API uint64_t moe_launch_count(void);
 /* Static text for a status code (never NULL). */
 MOE_API const char *moe_strerror(int status);
 
+/* Diagnostic: the kernels moe_forward picks for this configuration, as one
+ * line of "key=value" words written into buf (NUL-terminated, truncated to
+ * len bytes): router=split_d|warp|gemm, up=/down= tc|tc_pair|simt (tc_pair =
+ * CTA-pair tensor-core GEMM with 256-row tiles), ksplit_up=/ksplit_down= the
+ * split-K factor, gather_a=1 when the up GEMM gathers x rows itself, h= the
+ * storage of the SwiGLU output.  The choice depends on the configuration
+ * only, never on the data.  No counterpart on the pages.  Returns MOE_OK,
+ * MOE_ERR_NULL (buf NULL or len 0) or a configuration error. */
+MOE_API int moe_plan_describe(const moe_config *cfg, char *buf, size_t len);
+
 /* Library version as "major.minor.patch". */
 MOE_API const char *moe_version(void);
 

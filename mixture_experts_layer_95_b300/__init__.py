@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTY
 
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
-            "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static", "moe_bias_update")
+            "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static", "moe_bias_update",
+            "moe_plan_describe")
 STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
 
 
@@ -79,6 +80,8 @@ def lib():
         L.moe_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         L.moe_set_stage_events.restype = i32
         L.moe_launch_count.restype = ctypes.c_uint64
+        L.moe_plan_describe.argtypes = [cfgp, ctypes.c_char_p, sz]
+        L.moe_plan_describe.restype = i32
         for f in ("moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
                   "moe_load_stats", "moe_forward", "moe_last_device_status"):
             getattr(L, f).restype = i32
@@ -92,6 +95,14 @@ def strerror(code: int) -> str:
 
 def version() -> str:
     return lib().moe_version().decode()
+
+
+def plan_describe(cfg: MoeConfig) -> dict:
+    """The kernels moe_forward picks for `cfg`, as a dict of the library's
+    "key=value" words (router, up, down, ksplit_up, ksplit_down, gather_a, h)."""
+    buf = ctypes.create_string_buffer(256)
+    _check(lib().moe_plan_describe(ctypes.byref(cfg), buf, 256), "moe_plan_describe")
+    return dict(w.split("=", 1) for w in buf.value.decode().split())
 
 
 def launch_count() -> int:

@@ -4,6 +4,7 @@
 // the kernels of each step on the caller's stream.  No call allocates device
 // memory, synchronises (except moe_last_device_status, which must) or keeps a
 // pointer after returning.
+#include <stdio.h>
 #include <string.h>
 
 #include <atomic>
@@ -647,6 +648,24 @@ const char* moe_strerror(int status) {
 }
 
 const char* moe_version(void) { return "0.1.0"; }
+
+int moe_plan_describe(const moe_config* cfg, char* buf, size_t len) {
+    MOE_TRY(check_config(cfg));
+    if (!buf || len == 0) return MOE_ERR_NULL;
+    const moe_config& c = *cfg;
+    const char* router = use_split_d_router(c.T, c.E) ? "split_d"
+                         : use_warp_router(c.E, c.d, c.dtype) ? "warp"
+                                                              : "gemm";
+    const char* gemm = c.dtype != MOE_BF16 ? "simt" : "tc";
+    const Splits sp = choose_splits(c);
+    const bool gather = use_gather_a(c);
+    const bool pair_up = use_pair_gemm(c) && sp.up == 1 && !gather;
+    const bool pair_dn = use_pair_gemm(c) && sp.down == 1;
+    snprintf(buf, len, "router=%s up=%s%s ksplit_up=%d down=%s%s ksplit_down=%d gather_a=%d h=%s", router, gemm,
+             pair_up ? "_pair" : "", sp.up, gemm, pair_dn ? "_pair" : "", sp.down, gather ? 1 : 0,
+             use_h_split(c) ? "bf16_hi_lo" : (c.dtype == MOE_BF16 ? "bf16" : "f32"));
+    return MOE_OK;
+}
 
 int moe_set_stage_events(void* const* events, int n) {
     if (!events) {
