@@ -54,8 +54,12 @@ def _L():
         _lib.oracle_layer_tokens.argtypes = [ip] * 8 + [vp] * 11 + [ip, vp]
         _lib.oracle_load_stats.argtypes = [ip, ip, ip, vp, vp, ctypes.c_double, vp, vp, vp]
         _lib.oracle_bias_update.argtypes = [ip, ip, ip, vp, ctypes.c_double, vp, vp]
+        _lib.oracle_load_stats_n.argtypes = [ip, ip, ctypes.c_longlong, vp, vp, ctypes.c_double, vp, vp, vp]
+        _lib.oracle_ec_select.argtypes = [ip, ip, ip, vp, vp, vp]
+        _lib.oracle_ec_slots.argtypes = [ip, ip, ip, vp, vp, vp, vp, vp, vp]
         for f in ("oracle_route", "oracle_gates_for_ids", "oracle_group", "oracle_layer_tokens",
-                  "oracle_load_stats", "oracle_num_threads", "oracle_bias_update"):
+                  "oracle_load_stats", "oracle_num_threads", "oracle_bias_update", "oracle_ec_select",
+                  "oracle_ec_slots", "oracle_load_stats_n"):
             getattr(_lib, f).restype = ctypes.c_int
     return _lib
 
@@ -223,3 +227,72 @@ def forward(layer, k, renormalize=True, capacity=-1, alpha=0.01, ids=None, token
                      tokens, shared)
     st = load_stats(g["counts"], r["probs"], k, alpha)
     return dict(y=y, ids=ids, gates=gates, probs=r["probs"], margin=r["margin"], **g, **st)
+
+
+# ---------------------------------------------------------------- expert choice
+
+def ec_bucket(T, E, k, capacity=-1):
+    """Bucket size C of expert-choice routing: `capacity` when positive, else
+    floor(T k / E) (k read as the average number of experts per token), at
+    least 1 and at most T."""
+    if T == 0:
+        return 0
+    C = int(capacity) if capacity > 0 else (T * k) // E
+    return max(1, min(C, T))
+
+
+def ec_select(probs, C):
+    """Each expert's C highest-scoring tokens (ties to the lower token index),
+    ascending.  probs f64 [T, E].  Returns (sel int32 [E, C], margin f64 [E])."""
+    probs = _c(probs, np.float64)
+    T, E = probs.shape
+    sel = np.empty((E, C), np.int32)
+    margin = np.empty(E, np.float64)
+    _check(_L().oracle_ec_select(T, E, int(C), _p(probs), _p(sel), _p(margin)), "ec_select")
+    return sel, margin
+
+
+def ec_slots(sel, probs):
+    """[T, E] slot form of an expert-choice assignment: ids, gates (p or 0),
+    slot_pos (e*C + i or -1) and the number of tokens no expert chose."""
+    sel, probs = _c(sel, np.int32), _c(probs, np.float64)
+    T, E = probs.shape
+    C = sel.shape[1]
+    ids = np.empty((T, E), np.int32)
+    gates = np.empty((T, E), np.float64)
+    slot_pos = np.empty((T, E), np.int32)
+    ne = np.zeros(1, np.int32)
+    _check(_L().oracle_ec_slots(T, E, C, _p(sel), _p(probs), _p(ids), _p(gates), _p(slot_pos), _p(ne)), "ec_slots")
+    return dict(ids=ids, gates=gates, slot_pos=slot_pos, n_empty=int(ne[0]))
+
+
+def forward_expert_choice(layer, C, alpha=0.01, sel=None, tokens=None):
+    """The layer under expert-choice routing, from the steps above.
+
+    The router scores are the token-choice softmax probabilities (one route
+    call with k = 1 supplies them); every expert keeps C tokens; each chosen
+    (token, expert) pair adds p[t, e] * Expert_e(x_t); the shared expert is
+    added unweighted.  sel: optional int32 [E, C] selection to use instead of
+    the oracle's own (gates still come from the oracle's probabilities).
+    Statistics: counts_e = C, f_e = C / (E C), p_e = mean score, L as usual.
+    """
+    r = route(layer["x"], layer["w_gate"], 1, layer.get("logit_bias"), None, True)
+    probs = r["probs"]
+    T, E = probs.shape
+    own_sel, margin = ec_select(probs, C)
+    use = own_sel if sel is None else np.ascontiguousarray(sel, np.int32)
+    sl = ec_slots(use, probs)
+    shared = None
+    if layer.get("ws1") is not None:
+        shared = (layer["ws1"], layer["ws3"], layer["ws2"])
+    y = layer_tokens(layer["x"], layer["w1"], layer["w3"], layer["w2"], sl["ids"], sl["gates"], sl["slot_pos"],
+                     tokens, shared)
+    counts = np.full(E, C, np.int32)
+    f = np.zeros(E, np.float64)
+    pm = np.zeros(E, np.float64)
+    Lb = np.zeros(1, np.float64)
+    if T > 0:
+        _check(_L().oracle_load_stats_n(T, E, E * C, _p(counts), _p(probs), float(alpha), _p(f), _p(pm), _p(Lb)),
+               "load_stats_n")
+    st = dict(f=f, p=pm, L=float(Lb[0]))
+    return dict(y=y, probs=probs, sel=use, own_sel=own_sel, margin=margin, counts=counts, **sl, **st)

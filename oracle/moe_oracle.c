@@ -325,12 +325,14 @@ int oracle_layer_tokens(int T, int d, int E, int k, int F, int n_shared, int F_s
  * cut.  probs is [T][E] (the unbiased softmax, logit_bias included).
  * Pinned: closed forms (uniform p or uniform f give alpha; the handbook's
  * skewed example gives 4 with alpha = 1), random router near 1.
+ * oracle_load_stats_n takes the number of decisions n explicitly (f = counts
+ * / n); expert-choice routing makes E*C decisions instead of T*k.
  */
-int oracle_load_stats(int T, int E, int k, const int32_t *counts, const double *probs,
-                      double alpha, double *f, double *p, double *L) {
+int oracle_load_stats_n(int T, int E, long long n_decisions, const int32_t *counts, const double *probs,
+                        double alpha, double *f, double *p, double *L) {
     double acc = 0.0;
     for (int e = 0; e < E; ++e) {
-        f[e] = (double)counts[e] / ((double)T * (double)k);
+        f[e] = (double)counts[e] / (double)n_decisions;
         double s = 0.0;
         for (int t = 0; t < T; ++t) s += probs[(size_t)t * E + e];
         p[e] = s / (double)T;
@@ -338,6 +340,12 @@ int oracle_load_stats(int T, int E, int k, const int32_t *counts, const double *
     }
     *L = alpha * (double)E * acc;
     return 0;
+}
+
+/* The token-choice form: T*k decisions. */
+int oracle_load_stats(int T, int E, int k, const int32_t *counts, const double *probs, double alpha, double *f,
+                      double *p, double *L) {
+    return oracle_load_stats_n(T, E, (long long)T * k, counts, probs, alpha, f, p, L);
 }
 
 /*
@@ -361,5 +369,102 @@ int oracle_bias_update(int T, int E, int k, const int32_t *counts, double gamma,
         const double sgn = scaled > total ? 1.0 : (scaled < total ? -1.0 : 0.0);
         bias_out[e] = (double)bias_in[e] - gamma * sgn;
     }
+    return 0;
+}
+
+/*
+ * Expert-choice routing ("One Deep Concept #04", section 11 "Expert Choice --
+ * Reverse Who Selects Whom"): instead of each token choosing its experts, each
+ * expert chooses its tokens, and every expert's bucket has the same fixed size
+ * C, so the load is balanced by construction while a token may end up with any
+ * number of experts (none included).  The page gives the idea, not the
+ * formulas; the reading taken here:
+ *   scores  p[t][e] = softmax over experts of the router logits (the same p as
+ *           token choice, logit_bias included);
+ *   expert e keeps the C tokens with the largest p[t][e], ties to the lower
+ *           token index, listed in ascending token order;
+ *   gate of (t, e) = p[t][e] (no renormalisation: a token's gates need not sum
+ *           to one).
+ * Selection is a library sort on (score descending, token ascending) per
+ * expert -- a total order, so the chosen set is unique -- followed by a sort of
+ * the C chosen token indices.
+ * Outputs: sel[e*C + i] (i-th chosen token of expert e, ascending) and
+ * margin[e] = p_(C) - p_(C+1), the gap between the C-th and (C+1)-th largest
+ * score of expert e (+inf when C == T).  Requires 0 <= C <= T.
+ * Pinned: brute force over all C-subsets on tiny tie-heavy inputs, a hand
+ * example, the C = T dense limit, the closed-form balance loss.
+ */
+struct ec_key {
+    double p;
+    int t;
+};
+
+static int ec_key_cmp(const void *a, const void *b) {
+    const struct ec_key *x = (const struct ec_key *)a, *y = (const struct ec_key *)b;
+    if (x->p > y->p) return -1;
+    if (x->p < y->p) return 1;
+    return (x->t > y->t) - (x->t < y->t);
+}
+
+static int int_cmp(const void *a, const void *b) {
+    const int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+int oracle_ec_select(int T, int E, int C, const double *probs, int32_t *sel, double *margin) {
+    if (T < 0 || E < 1 || C < 0 || C > T) return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        struct ec_key *keys = (struct ec_key *)malloc(sizeof(struct ec_key) * (size_t)(T > 0 ? T : 1));
+#pragma omp for schedule(static)
+        for (int e = 0; e < E; ++e) {
+            if (!keys) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            for (int t = 0; t < T; ++t) {
+                keys[t].p = probs[(size_t)t * E + e];
+                keys[t].t = t;
+            }
+            qsort(keys, (size_t)T, sizeof(struct ec_key), ec_key_cmp);
+            for (int i = 0; i < C; ++i) sel[(size_t)e * C + i] = keys[i].t;
+            qsort(sel + (size_t)e * C, (size_t)C, sizeof(int32_t), int_cmp);
+            if (margin) margin[e] = (C == T || C == 0) ? INFINITY : keys[C - 1].p - keys[C].p;
+        }
+        free(keys);
+    }
+    return bad ? -2 : 0;
+}
+
+/*
+ * Token-side view of an expert-choice assignment, in the [T][E] slot form the
+ * per-token layer loop takes: slot (t, e) is live iff expert e chose token t;
+ * then ids[t][e] = e, gates[t][e] = p[t][e] and slot_pos[t][e] = e*C + i, the
+ * row of X_perm it occupies (expert segments of C rows, in expert order).
+ * Dead slots get gates 0 and slot_pos -1.  n_empty = tokens no expert chose.
+ */
+int oracle_ec_slots(int T, int E, int C, const int32_t *sel, const double *probs, int32_t *ids, double *gates,
+                    int32_t *slot_pos, int32_t *n_empty) {
+    for (size_t i = 0; i < (size_t)T * E; ++i) {
+        ids[i] = (int32_t)(i % (size_t)E);
+        gates[i] = 0.0;
+        slot_pos[i] = -1;
+    }
+    for (int e = 0; e < E; ++e)
+        for (int i = 0; i < C; ++i) {
+            const int t = sel[(size_t)e * C + i];
+            if (t < 0 || t >= T) return -1;
+            gates[(size_t)t * E + e] = probs[(size_t)t * E + e];
+            slot_pos[(size_t)t * E + e] = e * C + i;
+        }
+    int empty = 0;
+    for (int t = 0; t < T; ++t) {
+        int any = 0;
+        for (int e = 0; e < E; ++e) any |= slot_pos[(size_t)t * E + e] >= 0;
+        empty += !any;
+    }
+    *n_empty = empty;
     return 0;
 }
