@@ -219,22 +219,29 @@ def time_oracle(w, Ln, budget_s, n_tokens=None):
     import oracle
     threads = oracle.num_threads()
     t0 = time.perf_counter()
-    r = oracle.route(Ln["x"], Ln["w_gate"], w.k, Ln["logit_bias"], Ln["select_bias"], w.renormalize)
-    g = oracle.group(r["ids"], w.E, w.capacity)
+    if w.routing == "expert":  # every expert picks its bucket of C tokens
+        r = oracle.route(Ln["x"], Ln["w_gate"], 1, Ln["logit_bias"], None, True)
+        sel, _ = oracle.ec_select(r["probs"], oracle.ec_bucket(w.T, w.E, w.k, w.capacity))
+        sl = oracle.ec_slots(sel, r["probs"])
+        ids, gates, slot_pos = sl["ids"], sl["gates"], sl["slot_pos"]
+    else:
+        r = oracle.route(Ln["x"], Ln["w_gate"], w.k, Ln["logit_bias"], Ln["select_bias"], w.renormalize)
+        g = oracle.group(r["ids"], w.E, w.capacity)
+        ids, gates, slot_pos = r["ids"], r["gates"], g["slot_pos"]
     t_rg = time.perf_counter() - t0
     shared = (Ln["ws1"], Ln["ws3"], Ln["ws2"]) if w.n_shared else None
     if n_tokens is None:
         # calibrate on one token per thread, then size the sample to the budget
         n0 = min(w.T, threads)
         t1 = time.perf_counter()
-        oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], r["ids"], r["gates"], g["slot_pos"],
+        oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], ids, gates, slot_pos,
                             np.arange(n0, dtype=np.int32), shared)
         per_round = time.perf_counter() - t1
         rounds = max(1, int(budget_s / max(per_round, 1e-6)))
         n_tokens = min(w.T, n0 * rounds)
     toks = np.arange(n_tokens, dtype=np.int32)
     t2 = time.perf_counter()
-    oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], r["ids"], r["gates"], g["slot_pos"], toks, shared)
+    oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], ids, gates, slot_pos, toks, shared)
     t_ffn = time.perf_counter() - t2
     total = t_rg + t_ffn * (w.T / n_tokens)
     info = dict(cores=threads, n_tokens=int(n_tokens), t_route_group_s=round(t_rg, 3), t_ffn_s=round(t_ffn, 3))
@@ -256,7 +263,8 @@ def cpu_model():
 def layer_of(w):
     import mixture_experts_layer_95_b300 as moe
     return moe.Layer(T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.F, n_shared=w.n_shared, d_ff_shared=w.F_s, dtype=w.dtype,
-                     renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha, h_split=w.h_split)
+                     renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha, h_split=w.h_split,
+                     routing=w.routing)
 
 
 def run_ours(args):
@@ -400,7 +408,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded, N(0,1) tokens, N(0,1/fan_in) weights)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F, "n_shared": w.n_shared,
-                   "d_ff_shared": w.F_s, "capacity": w.capacity, "parallelism": f"replicas x{world}",
+                   "d_ff_shared": w.F_s, "capacity": w.capacity, "routing": w.routing,
+                   "parallelism": f"replicas x{world}",
                    "l2": "working set larger than L2 (expert weights %.2f GB)" % (wbytes / 1e9)},
         "roofline": roof,
         "layer": {"algorithmic_tflop_per_step": round(layer_flops / 1e12, 4),
@@ -409,7 +418,8 @@ def run_ours(args):
                   "expert_weight_gbs": round(wbytes / (ms_per_step / 1e3) / 1e9, 1),
                   "frac_hbm": round(wbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                   "stage_ms": {s: (round(v, 4) if v is not None else None) for s, v in per.items()},
-                  "kept_entries": kept_total, "dropped_entries": n_dropped, "experts_touched": touched,
+                  "kept_entries": kept_total, "experts_touched": touched,
+                  ("tokens_without_expert" if w.routing == "expert" else "dropped_entries"): n_dropped,
                   "plan": plan},
         "e2e": e2e,
         "gpu_launches": int(launches),

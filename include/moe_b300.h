@@ -23,6 +23,14 @@
  *   7. f_i = counts_i/(T k), p_i = mean_t p[t,i],   "MoE Architecture" s2 Load Balancing;
  *      L_balance = alpha E sum_i f_i p_i             handbook Load balancing (aux_loss)
  *
+ * Expert-choice routing (cfg->routing = MOE_ROUTE_EXPERT_CHOICE; "One Deep
+ * Concept #04" s11, Expert Choice -- Reverse Who Selects Whom) replaces steps
+ * 3-4: every expert takes a fixed bucket of C tokens, those with the largest
+ * p[t][e] (ties to the lower token index), so each expert's load is exactly C
+ * and a token gets any number of experts, zero included; the gate of a chosen
+ * (t, e) is p[t][e] (never renormalised).  Steps 5-7 are unchanged, with the
+ * E*C chosen pairs in place of the T*k routing decisions.
+ *
  * Conventions for every entry point
  *   - Every pointer argument except `cfg` and `stats` (a host struct of device
  *     pointers) is a DEVICE pointer unless stated otherwise.  The caller owns all
@@ -46,7 +54,8 @@
  *     dtype MOE_F32: everything is fp32 (IEEE fp32 FMA, no TF32).
  *   - Alignment: every device pointer must be 16-byte aligned and the
  *     workspace 256-byte aligned; d, F and F_s must be multiples of 8.
- *   - Limits: 1 <= k <= min(E, 32); E <= 1024; T >= 0; T * k < 2^31;
+ *   - Limits: 1 <= k <= min(E, 32); E <= 1024; T >= 0; T * k < 2^31 (expert
+ *     choice: also T * E < 2^31 and E * C < 2^31);
  *     n_shared is 0 or 1; d, F, F_s >= 8.  With T = 0 a call validates cfg
  *     only and enqueues nothing (pointers may then be NULL).
  */
@@ -70,6 +79,9 @@ extern "C" {
 typedef struct CUstream_st *moe_stream_t;
 
 enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
+
+/* Who chooses whom (moe_config.routing). */
+enum moe_routing { MOE_ROUTE_TOKEN_CHOICE = 0, MOE_ROUTE_EXPERT_CHOICE = 1 };
 
 enum moe_status {
     MOE_OK = 0,
@@ -105,6 +117,13 @@ typedef struct moe_config {
                             whose outputs are too heavy-tailed for a bf16 H;
                             costs a second pass of the down GEMM's MMAs.
                             Ignored for fp32 layers.                           */
+    int32_t routing;     /* enum moe_routing.  MOE_ROUTE_EXPERT_CHOICE: each
+                            expert takes a bucket of C tokens, C = capacity
+                            when capacity > 0, else floor(T k / E) (k read as
+                            the average number of experts per token), clamped
+                            to [1, T]; renormalize and select_bias have no
+                            effect (a per-expert constant does not change an
+                            expert's ranking of the tokens).                   */
 } moe_config;
 
 /* Optional statistics outputs of moe_forward (device pointers, each nullable). */
@@ -116,6 +135,9 @@ typedef struct moe_stats {
     float *L;           /* [1]  alpha * E * sum f p                                  */
     int32_t *n_dropped; /* [1]  T k - sum kept                                       */
 } moe_stats;
+/* Under expert choice: counts = kept = C for every expert, f = C / (E C) =
+ * 1/E (so L = alpha * sum_e p_e = alpha), and n_dropped counts the tokens that
+ * no expert took (they receive only the shared expert's output, or 0). */
 
 /* Bytes of device workspace every entry point below may use for `cfg`.
  * Returns 0 when cfg is invalid.  The workspace needs 256-byte alignment. */
@@ -137,6 +159,25 @@ MOE_API int moe_workspace_init(const moe_config *cfg, void *ws, size_t ws_bytes,
 MOE_API int moe_route(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
               const float *select_bias, int32_t *topk_ids, float *gates, float *p_mean, void *ws,
               size_t ws_bytes, moe_stream_t stream);
+
+/* Expert-choice routing and grouping in one step (requires cfg->routing ==
+ * MOE_ROUTE_EXPERT_CHOICE; token-choice configurations get MOE_ERR_SHAPE, as
+ * do moe_route, moe_permute, moe_permute_static and moe_bias_update under
+ * expert choice).  Router logits and softmax as in moe_route (logit_bias
+ * nullable), then every expert e takes its C tokens (bucket size in
+ * moe_config.routing) as rows [e*C, (e+1)*C) of the permuted layout, in
+ * ascending token order.
+ *   Outputs: probs fp32 [T][E] (the softmax rows; nullable -- the workspace
+ *   keeps a copy), sorted_token_ids int32 [E*C], gates_perm fp32 [E*C] (p of
+ *   each chosen pair), slot_pos int32 [T][E] (row of pair (t, e), -1 when
+ *   expert e did not take t), offsets int32 [E+1] (= e*C), p_mean fp32 [E]
+ *   (nullable), x_perm [E*C][d] (dtype; nullable: row r = x[sorted_token_ids[r]]).
+ * moe_expert_ffn then takes x_perm, offsets and gates_perm unchanged, and
+ * moe_combine takes slot_pos as its [T][E] slot map. */
+MOE_API int moe_route_expert_choice(const moe_config *cfg, const void *x, const void *w_gate,
+                                    const float *logit_bias, float *probs, int32_t *sorted_token_ids,
+                                    float *gates_perm, int32_t *slot_pos, int32_t *offsets, float *p_mean,
+                                    void *x_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Grouping by expert (step 4).  Entries are the (t, j) pairs in flat order
  * t*k + j; an entry's rank is the number of earlier entries of the same expert.
@@ -177,7 +218,8 @@ MOE_API int moe_permute_static(const moe_config *cfg, const int32_t *topk_ids, c
                                void *x_perm, int32_t *n_dropped, moe_stream_t stream);
 
 /* Expert FFNs over the grouped rows (step 5), gate applied in the epilogue.
- *   x_perm [T*k][d] and offsets [E+1] as produced by moe_permute; gates_perm fp32
+ *   x_perm [T*k][d] and offsets [E+1] as produced by moe_permute (expert
+ *   choice: [E*C][d] from moe_route_expert_choice); gates_perm fp32
  *   [T*k]; w1, w3 [E][F][d], w2 [E][d][F] (dtype).
  *   y_perm fp32 [T*k][d]: row pos = gates_perm[pos] * W2_e(silu(W1_e x) * W3_e x)
  *   for pos < offsets[E] (rows past the end are left untouched).
@@ -193,13 +235,15 @@ MOE_API int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int3
  * y_perm[slot_pos[t][j]], in that order, plus y_shared[t] when y_shared is
  * non-NULL; accumulated in fp32 and stored in cfg->dtype (round to nearest
  * even for bf16), or in fp32 when cfg->y_fp32.  A token whose entries were
- * all dropped gets only its shared row (or 0). */
+ * all dropped gets only its shared row (or 0).  Under expert choice slot_pos
+ * is [T][E] and the sum runs over j = 0..E-1. */
 MOE_API int moe_combine(const moe_config *cfg, const float *y_perm, const int32_t *slot_pos,
                 const float *y_shared, void *y, moe_stream_t stream);
 
 /* Load statistics (step 7) from counts [E] (moe_permute) and p_mean [E]
  * (moe_route): f [E] = counts/(T k), L [1] = alpha * E * sum f p_mean.
- * f or L may be NULL. */
+ * f or L may be NULL.  Under expert choice the denominator is E*C (the
+ * number of chosen pairs) instead of T k. */
 MOE_API int moe_load_stats(const moe_config *cfg, const int32_t *counts, const float *p_mean, float *f,
                    float *L, moe_stream_t stream);
 

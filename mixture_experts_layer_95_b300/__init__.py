@@ -19,6 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_F32, MOE_BF16 = 0, 1
+MOE_ROUTE_TOKEN_CHOICE, MOE_ROUTE_EXPERT_CHOICE = 0, 1
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTYPE", -4: "MOE_ERR_WORKSPACE",
           -5: "MOE_ERR_CUDA", -6: "MOE_ERR_DEVICE", -7: "MOE_ERR_TIMEOUT", -8: "MOE_ERR_DEVICE_BOUNDS",
           -9: "MOE_ERR_ALIGN"}
@@ -26,7 +27,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTY
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
             "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static", "moe_bias_update",
-            "moe_plan_describe")
+            "moe_plan_describe", "moe_route_expert_choice")
 STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
 
 
@@ -40,7 +41,8 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("capacity", ctypes.c_int32),
-                ("alpha", ctypes.c_float), ("y_fp32", ctypes.c_int32), ("h_split", ctypes.c_int32)]
+                ("alpha", ctypes.c_float), ("y_fp32", ctypes.c_int32), ("h_split", ctypes.c_int32),
+                ("routing", ctypes.c_int32)]
 
 
 class MoeStats(ctypes.Structure):
@@ -80,6 +82,8 @@ def lib():
         L.moe_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         L.moe_set_stage_events.restype = i32
         L.moe_launch_count.restype = ctypes.c_uint64
+        L.moe_route_expert_choice.argtypes = [cfgp] + [vp] * 10 + [vp, sz, vp]
+        L.moe_route_expert_choice.restype = i32
         L.moe_plan_describe.argtypes = [cfgp, ctypes.c_char_p, sz]
         L.moe_plan_describe.restype = i32
         for f in ("moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
@@ -199,11 +203,33 @@ class Layer:
     alpha: float = 0.01
     y_fp32: bool = False  # return y in fp32 (before rounding to the layer dtype)
     h_split: bool = False  # bf16: keep H as a hi + lo bf16 pair (heavy-tailed layers)
+    routing: str = "token"  # "token": tokens choose top-k experts; "expert": experts choose C tokens
 
     def cfg(self) -> MoeConfig:
+        if self.routing not in ("token", "expert"):
+            raise ValueError(f"routing must be 'token' or 'expert', got {self.routing!r}")
         return MoeConfig(self.T, self.d, self.E, self.k, self.d_ff, self.n_shared, self.d_ff_shared,
                          MOE_BF16 if self.dtype == "bf16" else MOE_F32, int(bool(self.renormalize)),
-                         int(self.capacity), float(self.alpha), int(bool(self.y_fp32)), int(bool(self.h_split)))
+                         int(self.capacity), float(self.alpha), int(bool(self.y_fp32)), int(bool(self.h_split)),
+                         MOE_ROUTE_EXPERT_CHOICE if self.routing == "expert" else MOE_ROUTE_TOKEN_CHOICE)
+
+    @property
+    def bucket(self) -> int:
+        """Expert choice: tokens per expert, C (the header's rule); 0 for token choice."""
+        if self.routing != "expert" or self.T == 0:
+            return 0
+        C = self.capacity if self.capacity > 0 else (self.T * self.k) // self.E
+        return max(1, min(C, self.T))
+
+    @property
+    def perm_rows(self) -> int:
+        """Rows of the permuted layout: T*k, or E*C under expert choice."""
+        return self.E * self.bucket if self.routing == "expert" else self.T * self.k
+
+    @property
+    def slots(self) -> int:
+        """Slots per token in slot_pos: k, or E under expert choice."""
+        return self.E if self.routing == "expert" else self.k
 
     @property
     def torch_dtype(self):
@@ -273,6 +299,32 @@ def route(layer: Layer, x, w_gate, logit_bias=None, select_bias=None, ws=None, s
     return ids, gates, p_mean
 
 
+def route_expert_choice(layer: Layer, x, w_gate, logit_bias=None, ws=None, stream=None, gather=True):
+    """moe_route_expert_choice: every expert takes its C tokens.  Returns a dict
+    with probs [T,E], sorted_token_ids / gates_perm [E*C], slot_pos [T,E],
+    offsets [E+1], p_mean [E] and (gather=True) x_perm [E*C, d]."""
+    dt, dev = layer.torch_dtype, x.device
+    _need(x, (layer.T, layer.d), dt, "x")
+    _need(w_gate, (layer.E, layer.d), dt, "w_gate")
+    if logit_bias is not None:
+        _need(logit_bias, (layer.E,), torch.float32, "logit_bias")
+    ws = ws if ws is not None else workspace(layer, dev, stream)
+    n = layer.perm_rows
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(probs=torch.empty((layer.T, layer.E), **f32), sorted_token_ids=torch.empty(n, **i32),
+               gates_perm=torch.empty(n, **f32), slot_pos=torch.empty((layer.T, layer.E), **i32),
+               offsets=torch.empty(layer.E + 1, **i32), p_mean=torch.empty(layer.E, **f32),
+               x_perm=torch.empty((n, layer.d), dtype=dt, device=dev) if gather else None)
+    c = layer.cfg()
+    _check(lib().moe_route_expert_choice(ctypes.byref(c), _ptr(x), _ptr(w_gate), _ptr(logit_bias),
+                                         _ptr(out["probs"]), _ptr(out["sorted_token_ids"]), _ptr(out["gates_perm"]),
+                                         _ptr(out["slot_pos"]), _ptr(out["offsets"]), _ptr(out["p_mean"]),
+                                         _ptr(out["x_perm"]), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_route_expert_choice")
+    return out
+
+
 def permute(layer: Layer, topk_ids, gates, x, ws=None, stream=None):
     """moe_permute: returns a dict of the grouping outputs and x_perm."""
     dev = x.device
@@ -324,9 +376,10 @@ def permute_static(layer: Layer, topk_ids, gates, x, stream=None):
 
 def expert_ffn(layer: Layer, x_perm, offsets, gates_perm, w1, w3, w2, x=None, ws1=None, ws3=None, ws2=None,
                ws=None, stream=None):
-    """moe_expert_ffn: returns (y_perm fp32 [T*k, d], y_shared fp32 [T, d] or None)."""
+    """moe_expert_ffn: returns (y_perm fp32 [rows, d], y_shared fp32 [T, d] or None);
+    rows = T*k (token choice) or E*C (expert choice)."""
     dt, dev = layer.torch_dtype, x_perm.device
-    n = layer.T * layer.k
+    n = layer.perm_rows
     _need(x_perm, (n, layer.d), dt, "x_perm")
     _need(offsets, (layer.E + 1,), torch.int32, "offsets")
     _need(gates_perm, (n,), torch.float32, "gates_perm")
@@ -352,8 +405,8 @@ def expert_ffn(layer: Layer, x_perm, offsets, gates_perm, w1, w3, w2, x=None, ws
 def combine(layer: Layer, y_perm, slot_pos, y_shared=None, stream=None):
     """moe_combine: returns y [T, d] in the layer dtype."""
     dev = y_perm.device
-    _need(y_perm, (layer.T * layer.k, layer.d), torch.float32, "y_perm")
-    _need(slot_pos, (layer.T, layer.k), torch.int32, "slot_pos")
+    _need(y_perm, (layer.perm_rows, layer.d), torch.float32, "y_perm")
+    _need(slot_pos, (layer.T, layer.slots), torch.int32, "slot_pos")
     if y_shared is not None:
         _need(y_shared, (layer.T, layer.d), torch.float32, "y_shared")
     y = torch.empty((layer.T, layer.d), dtype=layer.y_dtype, device=dev)

@@ -25,12 +25,30 @@ size_t esize(const moe_config& c) { return c.dtype == MOE_BF16 ? 2 : 4; }
 
 bool use_h_split(const moe_config& c) { return c.dtype == MOE_BF16 && c.h_split == 1; }
 
+bool expert_choice(const moe_config& c) { return c.routing == MOE_ROUTE_EXPERT_CHOICE; }
+
+// Bucket size C of expert-choice routing: capacity when positive, else
+// floor(T k / E), clamped to [1, T].
+int ec_bucket(const moe_config& c) {
+    if (c.T == 0) return 0;
+    long long C = c.capacity > 0 ? c.capacity : (long long)c.T * c.k / c.E;
+    if (C < 1) C = 1;
+    if (C > c.T) C = c.T;
+    return (int)C;
+}
+
+// Rows of the permuted layout: T k routing decisions, or E C chosen pairs.
+long long perm_rows(const moe_config& c) { return expert_choice(c) ? (long long)c.E * ec_bucket(c) : (long long)c.T * c.k; }
+
+// Slots per token in slot_pos: k, or E under expert choice.
+int slots_per_token(const moe_config& c) { return expert_choice(c) ? c.E : c.k; }
+
 // Large expert segments (at least 512 rows per touched expert on average,
 // bf16, a single bf16 H): both grouped GEMMs run on CTA pairs with 256-row
 // tiles (2-SM tensor-core MMAs).  Smaller segments keep 128-row tiles, which
 // waste fewer rows at segment ends.
 bool use_pair_gemm(const moe_config& c) {
-    const long long n = (long long)c.T * c.k;
+    const long long n = perm_rows(c);
     const long long touched = n < c.E ? n : c.E;
     return c.dtype == MOE_BF16 && c.h_split == 0 && n >= 512 * touched;
 }
@@ -38,7 +56,7 @@ bool use_pair_gemm(const moe_config& c) {
 // Decode-sized bf16 batches (at most 32 rows per touched expert on average):
 // the up GEMM gathers x rows itself, so the layer skips the permuted copy.
 bool use_gather_a(const moe_config& c) {
-    const long long n = (long long)c.T * c.k;
+    const long long n = perm_rows(c);
     const long long touched = n < c.E ? n : c.E;
     return c.dtype == MOE_BF16 && n <= 32 * touched;
 }
@@ -79,7 +97,7 @@ struct Splits {
 // Tiles a grouped GEMM will have at least: every touched expert owns one or
 // more 128-row tiles.
 long long est_row_tiles(const moe_config& c) {
-    const long long n = (long long)c.T * c.k;
+    const long long n = perm_rows(c);
     const long long touched = n < c.E ? n : c.E;
     const long long by_rows = ceil_div(n, 128);
     return by_rows > touched ? by_rows : touched;
@@ -96,7 +114,7 @@ Splits choose_splits(const moe_config& c) {
     int nk_dn = ceil_div(c.d_ff, 64);
     if (c.n_shared) nk_dn = nk_dn < ceil_div(c.d_ff_shared, 64) ? nk_dn : ceil_div(c.d_ff_shared, 64);
     // bytes: weights streamed vs one slice's fp32 partials written and read back
-    const long long n = (long long)c.T * c.k;
+    const long long n = perm_rows(c);
     const long long touched = n < c.E ? n : c.E;
     const long long w_up = touched * 2LL * c.d_ff * c.d * 2 + (long long)c.n_shared * 2LL * c.d_ff_shared * c.d * 2;
     const long long p_up = 8LL * (n * 2 * c.d_ff + (long long)c.n_shared * c.T * 2 * c.d_ff_shared);
@@ -110,13 +128,14 @@ Splits choose_splits(const moe_config& c) {
 // Byte offsets of every workspace region; `total` is the size.
 struct Layout {
     size_t status, topk_ids, gates, p_part, block_hist, counts, kept, offsets, n_dropped, sorted, slot_pos,
-        gates_perm, p_mean, f, L, logits, x_perm, h, h_shared, h_lo, h_shared_lo, y_perm, y_shared, part_up,
+        gates_perm, p_mean, f, L, logits, probs, x_perm, h, h_shared, h_lo, h_shared_lo, y_perm, y_shared, part_up,
         part_up_shared, part_dn, part_dn_shared, total;
 };
 
 Layout layout(const moe_config& c) {
     Layout l{};
-    const size_t n = (size_t)c.T * c.k;
+    const size_t n = (size_t)perm_rows(c);
+    const size_t nk = (size_t)c.T * c.k;  // token-choice routing outputs
     // histogram / p rows: the router's chunks, and moe_permute's 64-token chunks
     const size_t ch = (size_t)router_chunk(c.T, c.E, c.d, c.dtype);
     const size_t nblk_r = ((size_t)c.T + ch - 1) / ch;
@@ -130,8 +149,8 @@ Layout layout(const moe_config& c) {
         return at;
     };
     l.status = take(16);
-    l.topk_ids = take(4 * n);
-    l.gates = take(4 * n);
+    l.topk_ids = take(4 * nk);
+    l.gates = take(4 * nk);
     l.p_part = take(4 * nblk * E);
     l.block_hist = take(4 * nblk * E);
     l.counts = take(4 * E);
@@ -139,12 +158,13 @@ Layout layout(const moe_config& c) {
     l.offsets = take(4 * (E + 1));
     l.n_dropped = take(4);
     l.sorted = take(4 * n);
-    l.slot_pos = take(4 * n);
+    l.slot_pos = take(4 * (size_t)c.T * slots_per_token(c));
     l.gates_perm = take(4 * n);
     l.p_mean = take(4 * E);
     l.f = take(4 * E);
     l.L = take(4);
     l.logits = take(use_gemm_router(c) ? 4 * (size_t)c.T * E : 0);
+    l.probs = take(expert_choice(c) ? 4 * (size_t)c.T * E : 0);
     l.x_perm = take(use_gather_a(c) ? 0 : n * c.d * esize(c));  // not needed when the up GEMM gathers x
     l.h = take(n * c.d_ff * esize(c));
     l.h_shared = take(c.n_shared ? (size_t)c.T * c.d_ff_shared * esize(c) : 0);
@@ -182,6 +202,11 @@ int check_config(const moe_config* c) {
     if (c->d % 8 || c->d_ff % 8 || (c->n_shared && c->d_ff_shared % 8)) return MOE_ERR_SHAPE;
     if (c->y_fp32 != 0 && c->y_fp32 != 1) return MOE_ERR_DTYPE;
     if (c->h_split != 0 && c->h_split != 1) return MOE_ERR_DTYPE;
+    if (c->routing != MOE_ROUTE_TOKEN_CHOICE && c->routing != MOE_ROUTE_EXPERT_CHOICE) return MOE_ERR_SHAPE;
+    if (c->routing == MOE_ROUTE_EXPERT_CHOICE) {
+        if ((long long)c->T * c->E >= (1LL << 31)) return MOE_ERR_SHAPE;
+        if ((long long)c->E * ec_bucket(*c) >= (1LL << 31)) return MOE_ERR_SHAPE;
+    }
     // the grouped GEMM tile list holds at most kMaxExperts row groups
     return MOE_OK;
 }
@@ -254,19 +279,22 @@ struct StageScope {
         g_launches.fetch_add(1, std::memory_order_relaxed);     \
     } while (0)
 
+// Router: logits, softmax, top-k (k = c.k), per-block partial sums of p and
+// id histograms.  Expert choice calls it with k = 0 (softmax only) and a
+// probs [T][E] output.
 int enqueue_route(const moe_config& c, const Layout& L, void* ws, const void* x, const void* w_gate,
                   const float* logit_bias, const float* select_bias, int32_t* topk_ids, float* gates,
-                  int32_t* block_hist, int sms, cudaStream_t s) {
+                  int32_t* block_hist, int sms, cudaStream_t s, int k, float* probs = nullptr) {
     float* p_part = at<float>(ws, L.p_part);
     StageScope scope(kStageRouter, s);
     if (use_split_d_router(c.T, c.E)) {
-        MOE_LAUNCH(launch_router_split_d(c.dtype, c.T, c.d, c.E, c.k, x, w_gate, logit_bias, select_bias,
-                                         c.renormalize, topk_ids, gates, p_part, block_hist, s));
+        MOE_LAUNCH(launch_router_split_d(c.dtype, c.T, c.d, c.E, k, x, w_gate, logit_bias, select_bias,
+                                         c.renormalize, topk_ids, gates, p_part, block_hist, s, probs));
         return MOE_OK;
     }
     if (!use_gemm_router(c)) {
-        MOE_LAUNCH(launch_router_warp(c.dtype, c.T, c.d, c.E, c.k, x, w_gate, logit_bias, select_bias, c.renormalize,
-                                    topk_ids, gates, p_part, block_hist, s));
+        MOE_LAUNCH(launch_router_warp(c.dtype, c.T, c.d, c.E, k, x, w_gate, logit_bias, select_bias, c.renormalize,
+                                    topk_ids, gates, p_part, block_hist, s, probs));
         return MOE_OK;
     }
     float* logits = at<float>(ws, L.logits);
@@ -283,8 +311,20 @@ int enqueue_route(const moe_config& c, const Layout& L, void* ws, const void* x,
         MOE_LAUNCH(launch_gemm_tc(kGemmPlain, &g, 1, at<int>(ws, L.status), sms, s));
     else
         MOE_LAUNCH(launch_gemm_simt_f32(kGemmPlain, &g, 1, s));
-    MOE_LAUNCH(launch_router_from_logits(c.T, c.E, c.k, logits, logit_bias, select_bias, c.renormalize, topk_ids,
-                                       gates, p_part, block_hist, s));
+    MOE_LAUNCH(launch_router_from_logits(c.T, c.E, k, logits, logit_bias, select_bias, c.renormalize, topk_ids,
+                                       gates, p_part, block_hist, s, probs));
+    return MOE_OK;
+}
+
+// Expert-choice routing + grouping: softmax rows into probs, then every
+// expert's bucket.  counts / kept / n_empty nullable.
+int enqueue_route_ec(const moe_config& c, const Layout& L, void* ws, const void* x, const void* w_gate,
+                     const float* logit_bias, float* probs, int32_t* sorted, float* gates_perm, int32_t* slot_pos,
+                     int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* n_empty, int sms, cudaStream_t s) {
+    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, nullptr, nullptr, nullptr, nullptr, sms, s, 0, probs));
+    StageScope scope(kStageScan, s);
+    MOE_LAUNCH(launch_ec_select(c.T, c.E, ec_bucket(c), probs, sorted, gates_perm, slot_pos, counts, kept, offsets,
+                                n_empty, s));
     return MOE_OK;
 }
 
@@ -296,7 +336,7 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
                 const void* ws1, const void* ws3, const void* ws2, float* y_perm, float* y_shared, int sms,
                 cudaStream_t s, bool reduce_down, const int32_t* gather_idx) {
     const Splits sp = choose_splits(c);
-    const int n = c.T * c.k;
+    const int n = (int)perm_rows(c);
     void* h = at<void>(ws, L.h);
     void* hs = at<void>(ws, L.h_shared);
     const bool split = use_h_split(c);
@@ -391,6 +431,74 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     return MOE_OK;
 }
 
+// Expert-FFN rows in place (explicit gather, or the up GEMM's own gather
+// for decode-sized batches), both GEMMs, combine over `slots` slots per
+// token -- the part of moe_forward shared by both routings.
+int forward_tail(const moe_config& c, const Layout& L, void* ws, const void* x, const int32_t* offsets,
+                 const int32_t* sorted, const float* gates_perm, const int32_t* slot_pos, int slots, const void* w1,
+                 const void* w3, const void* w2, const void* ws1, const void* ws3, const void* ws2, void* y,
+                 int32_t* n_empty, int sms, cudaStream_t s) {
+    int* status = at<int>(ws, L.status);
+    void* x_perm = nullptr;
+    const int32_t* gather_idx = nullptr;
+    if (use_gather_a(c)) {
+        gather_idx = sorted;
+    } else {
+        x_perm = at<void>(ws, L.x_perm);
+        StageScope scope(kStageGather, s);
+        MOE_LAUNCH(launch_gather_rows(c.dtype, c.T, c.d, (int)perm_rows(c), offsets + c.E, sorted, x, x_perm,
+                                      status, s));
+    }
+    float* y_perm = at<float>(ws, L.y_perm);
+    float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
+    MOE_TRY(enqueue_ffn(c, L, ws, x_perm, offsets, gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared, sms,
+                        s, false, gather_idx));
+    // combine (straight from the down GEMM's split-K slices when it was split)
+    const Splits sp = choose_splits(c);
+    const float* yp = y_perm;
+    const float* ys = y_shared;
+    size_t yp_stride = 0, ys_stride = 0;
+    if (sp.down > 1) {
+        yp = at<float>(ws, L.part_dn);
+        yp_stride = (size_t)perm_rows(c) * c.d;
+        if (c.n_shared) {
+            ys = at<float>(ws, L.part_dn_shared);
+            ys_stride = (size_t)c.T * c.d;
+        }
+    }
+    StageScope scope(kStageCombine, s);
+    MOE_LAUNCH(launch_combine_split(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, slots, yp, yp_stride, sp.down, slot_pos,
+                                    ys, ys_stride, sp.down, y, s, n_empty));
+    return MOE_OK;
+}
+
+int forward_expert_choice(const moe_config& c, const Layout& L, void* ws, const void* x, const void* w_gate,
+                          const float* logit_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                          const void* ws3, const void* ws2, void* y, const moe_stats* stats, int nblk, int sms,
+                          cudaStream_t s) {
+    const int C = ec_bucket(c);
+    float* probs = at<float>(ws, L.probs);
+    int32_t* sorted = at<int32_t>(ws, L.sorted);
+    float* gates_perm = at<float>(ws, L.gates_perm);
+    int32_t* slot_pos = at<int32_t>(ws, L.slot_pos);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* counts = (stats && stats->counts) ? stats->counts : at<int32_t>(ws, L.counts);
+    int32_t* kept = (stats && stats->kept) ? stats->kept : at<int32_t>(ws, L.kept);
+    int32_t* n_empty = stats ? stats->n_dropped : nullptr;
+    MOE_TRY(enqueue_route_ec(c, L, ws, x, w_gate, logit_bias, probs, sorted, gates_perm, slot_pos, counts, kept,
+                             offsets, n_empty, sms, s));
+    if (stats && (stats->f || stats->p || stats->L)) {
+        float* p_mean = stats->p ? stats->p : at<float>(ws, L.p_mean);
+        StageScope scope(kStageScan, s);
+        MOE_LAUNCH(launch_p_mean(c.T, c.E, nblk, at<float>(ws, L.p_part), p_mean, s));
+        // f = counts / (E C): the E*C chosen pairs are the decisions
+        if (stats->f || stats->L)
+            MOE_LAUNCH(launch_load_stats(c.E * C, c.E, 1, c.alpha, counts, p_mean, stats->f, stats->L, s));
+    }
+    return forward_tail(c, L, ws, x, offsets, sorted, gates_perm, slot_pos, c.E, w1, w3, w2, ws1, ws3, ws2, y,
+                        n_empty, sms, s);
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -415,6 +523,7 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_gate, const fl
               const float* select_bias, int32_t* topk_ids, float* gates, float* p_mean, void* ws, size_t ws_bytes,
               moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
+    if (expert_choice(*cfg)) return MOE_ERR_SHAPE;  // token-choice step
     const moe_config& c = *cfg;
     if (c.T == 0) return MOE_OK;
     if (!x || !w_gate || !topk_ids || !gates) return MOE_ERR_NULL;
@@ -425,7 +534,7 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_gate, const fl
     MOE_TRY(device_sms(&sms));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const Layout L = layout(c);
-    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, nullptr, sms, s));
+    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, nullptr, sms, s, c.k));
     if (p_mean) {
         const int ch = router_chunk(c.T, c.E, c.d, c.dtype);
         const int nblk = (c.T + ch - 1) / ch;
@@ -435,10 +544,42 @@ int moe_route(const moe_config* cfg, const void* x, const void* w_gate, const fl
     return MOE_OK;
 }
 
+int moe_route_expert_choice(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                            float* probs, int32_t* sorted_token_ids, float* gates_perm, int32_t* slot_pos,
+                            int32_t* offsets, float* p_mean, void* x_perm, void* ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (!expert_choice(c)) return MOE_ERR_SHAPE;
+    if (c.T == 0) return MOE_OK;
+    if (!x || !w_gate || !sorted_token_ids || !gates_perm || !slot_pos || !offsets) return MOE_ERR_NULL;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    if (!aligned16(x) || !aligned16(w_gate) || (x_perm && !aligned16(x_perm))) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Layout L = layout(c);
+    float* pr = probs ? probs : at<float>(ws, L.probs);
+    MOE_TRY(enqueue_route_ec(c, L, ws, x, w_gate, logit_bias, pr, sorted_token_ids, gates_perm, slot_pos, nullptr,
+                             nullptr, offsets, nullptr, sms, s));
+    if (p_mean) {
+        const int ch = router_chunk(c.T, c.E, c.d, c.dtype);
+        StageScope scope(kStageRouter, s);
+        MOE_LAUNCH(launch_p_mean(c.T, c.E, (c.T + ch - 1) / ch, at<float>(ws, L.p_part), p_mean, s));
+    }
+    if (x_perm) {
+        StageScope scope(kStageGather, s);
+        MOE_LAUNCH(launch_gather_rows(c.dtype, c.T, c.d, (int)perm_rows(c), offsets + c.E, sorted_token_ids, x,
+                                      x_perm, at<int>(ws, L.status), s));
+    }
+    return MOE_OK;
+}
+
 int moe_permute(const moe_config* cfg, const int32_t* topk_ids, const float* gates, const void* x, int32_t* counts,
                 int32_t* kept, int32_t* offsets, int32_t* sorted_token_ids, int32_t* slot_pos, float* gates_perm,
                 void* x_perm, int32_t* n_dropped, void* ws, size_t ws_bytes, moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
+    if (expert_choice(*cfg)) return MOE_ERR_SHAPE;  // token-choice step
     const moe_config& c = *cfg;
     if (c.T == 0) return MOE_OK;
     if (!topk_ids || !gates || !x || !counts || !kept || !offsets || !sorted_token_ids || !slot_pos ||
@@ -502,7 +643,7 @@ int moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_
     int sms = 0;
     MOE_TRY(device_sms(&sms));
     StageScope scope(kStageCombine, reinterpret_cast<cudaStream_t>(stream));
-    MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, c.k, y_perm, slot_pos, y_shared, y,
+    MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, slots_per_token(c), y_perm, slot_pos, y_shared, y,
                               reinterpret_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
@@ -515,13 +656,16 @@ int moe_load_stats(const moe_config* cfg, const int32_t* counts, const float* p_
     if (!counts || !p_mean) return MOE_ERR_NULL;
     int sms = 0;
     MOE_TRY(device_sms(&sms));
-    MOE_LAUNCH(launch_load_stats(c.T, c.E, c.k, c.alpha, counts, p_mean, f, L, reinterpret_cast<cudaStream_t>(stream)));
+    // decisions: T k, or the E C chosen pairs under expert choice
+    const int tn = expert_choice(c) ? (int)perm_rows(c) : c.T, kk = expert_choice(c) ? 1 : c.k;
+    MOE_LAUNCH(launch_load_stats(tn, c.E, kk, c.alpha, counts, p_mean, f, L, reinterpret_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 
 int moe_bias_update(const moe_config* cfg, const int32_t* counts, float gamma, float* select_bias,
                     moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
+    if (expert_choice(*cfg)) return MOE_ERR_SHAPE;  // token-choice step
     const moe_config& c = *cfg;
     if (c.T == 0) return MOE_OK;
     if (!counts || !select_bias) return MOE_ERR_NULL;
@@ -556,9 +700,12 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
     int32_t* block_hist = at<int32_t>(ws, L.block_hist);
     const int chunk = router_chunk(c.T, c.E, c.d, c.dtype);
     const int nblk = (c.T + chunk - 1) / chunk;
+    if (expert_choice(c))
+        return forward_expert_choice(c, L, ws, x, w_gate, logit_bias, w1, w3, w2, ws1, ws3, ws2, y, stats, nblk,
+                                     sms, s);
 
     // 1-3: router, softmax, top-k; the router blocks also emit their id histograms
-    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, block_hist, sms, s));
+    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, block_hist, sms, s, c.k));
 
     // 4: grouping (+ load statistics from the router's partial sums)
     GroupOut o{};
@@ -581,42 +728,11 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
         StageScope scope(kStageScan, s);
         MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, block_hist, o, status, s));
     }
-    // decode-sized bf16 batches: the up GEMM gathers x rows itself (TMA
-    // gather4); otherwise an explicit copy into expert order
-    void* x_perm = nullptr;
-    const int32_t* gather_idx = nullptr;
-    if (use_gather_a(c)) {
-        gather_idx = o.sorted_token_ids;
-    } else {
-        x_perm = at<void>(ws, L.x_perm);
-        StageScope scope(kStageGather, s);
-        MOE_LAUNCH(launch_gather_rows(c.dtype, c.T, c.d, c.T * c.k, o.offsets + c.E, o.sorted_token_ids, x, x_perm,
-                                      status, s));
-    }
-
-    // 5: expert FFNs (routed groups + shared expert in the same launches)
-    float* y_perm = at<float>(ws, L.y_perm);
-    float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
-    MOE_TRY(enqueue_ffn(c, L, ws, x_perm, o.offsets, o.gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared,
-                        sms, s, false, gather_idx));
-
-    // 6: combine (straight from the down GEMM's split-K slices when it was split)
-    const Splits sp = choose_splits(c);
-    const float* yp = y_perm;
-    const float* ys = y_shared;
-    size_t yp_stride = 0, ys_stride = 0;
-    if (sp.down > 1) {
-        yp = at<float>(ws, L.part_dn);
-        yp_stride = (size_t)c.T * c.k * c.d;
-        if (c.n_shared) {
-            ys = at<float>(ws, L.part_dn_shared);
-            ys_stride = (size_t)c.T * c.d;
-        }
-    }
-    StageScope scope(kStageCombine, s);
-    MOE_LAUNCH(launch_combine_split(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, c.k, yp, yp_stride, sp.down, o.slot_pos,
-                                    ys, ys_stride, sp.down, y, s));
-    return MOE_OK;
+    // 5-6: rows in expert order (decode-sized bf16 batches: the up GEMM
+    // gathers x rows itself with TMA gather4), expert FFNs (routed groups +
+    // shared expert in the same launches), combine
+    return forward_tail(c, L, ws, x, o.offsets, o.sorted_token_ids, o.gates_perm, o.slot_pos, c.k, w1, w3, w2, ws1,
+                        ws3, ws2, y, nullptr, sms, s);
 }
 
 int moe_last_device_status(const moe_config* cfg, void* ws, moe_stream_t stream) {
@@ -661,7 +777,8 @@ int moe_plan_describe(const moe_config* cfg, char* buf, size_t len) {
     const bool gather = use_gather_a(c);
     const bool pair_up = use_pair_gemm(c) && sp.up == 1 && !gather;
     const bool pair_dn = use_pair_gemm(c) && sp.down == 1;
-    snprintf(buf, len, "router=%s up=%s%s ksplit_up=%d down=%s%s ksplit_down=%d gather_a=%d h=%s", router, gemm,
+    snprintf(buf, len, "routing=%s router=%s up=%s%s ksplit_up=%d down=%s%s ksplit_down=%d gather_a=%d h=%s",
+             expert_choice(c) ? "expert_choice" : "token_choice", router, gemm,
              pair_up ? "_pair" : "", sp.up, gemm, pair_dn ? "_pair" : "", sp.down, gather ? 1 : 0,
              use_h_split(c) ? "bf16_hi_lo" : (c.dtype == MOE_BF16 ? "bf16" : "f32"));
     return MOE_OK;

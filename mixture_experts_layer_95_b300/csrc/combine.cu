@@ -42,8 +42,12 @@ __device__ __forceinline__ void add4(float4& a, const float4& b) {
 }
 
 // One warp per (token, 256-column chunk), so that even a single token is
-// spread over d/256 warps.  Lane j < k holds slot_pos[t][j] (k <= 32) and
-// broadcasts it; each lane owns 8 consecutive columns.  Rows of y_perm (and
+// spread over d/256 warps.  The warp reads the token's k slot positions 32 at
+// a time (lane j holds slot j of the batch), finds the live ones (>= 0) with
+// a ballot and broadcasts them in ascending slot order; each lane owns 8
+// consecutive columns.  k is the top-k of token choice, or E for expert
+// choice (slot e live iff expert e took the token; n_empty, when given,
+// counts the tokens with no live slot).  Rows of y_perm (and
 // y_shared) may be split into `nsplit` fp32 slices `stride` elements apart:
 // each entry's slices are summed in slice order first, then the entries in
 // fixed j order, then the shared row -- the same order in which a reduction
@@ -53,7 +57,8 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
                                                       size_t perm_stride, int nsplit,
                                                       const int32_t* __restrict__ slot_pos,
                                                       const float* __restrict__ y_shared, size_t shared_stride,
-                                                      int shared_nsplit, T* __restrict__ y) {
+                                                      int shared_nsplit, T* __restrict__ y,
+                                                      int32_t* __restrict__ n_empty) {
     pdl_wait();
     const int chunks = (d + 255) / 256;
     const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -62,22 +67,30 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
     const int t = item / chunks;
     const int c = (item - t * chunks) * 256 + lane * 8;
     const bool active = c < d;  // d is a multiple of 8: an active lane owns 8 columns
-    const int my_pos = lane < k ? __ldg(slot_pos + (size_t)t * k + lane) : -1;
     float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-    for (int j = 0; j < k; ++j) {
-        const int pos = __shfl_sync(0xffffffffu, my_pos, j);
-        if (pos < 0 || !active) continue;
-        const float4* src = reinterpret_cast<const float4*>(y_perm + (size_t)pos * d + c);
-        float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+    bool any = false;
+    for (int j0 = 0; j0 < k; j0 += 32) {  // 32 slots at a time; live ones in ascending j
+        const int my_pos = j0 + lane < k ? __ldg(slot_pos + (size_t)t * k + j0 + lane) : -1;
+        unsigned live = __ballot_sync(0xffffffffu, my_pos >= 0);
+        any |= live != 0u;
+        while (live) {
+            const int j = __ffs(live) - 1;
+            live &= live - 1u;
+            const int pos = __shfl_sync(0xffffffffu, my_pos, j);
+            if (!active) continue;
+            const float4* src = reinterpret_cast<const float4*>(y_perm + (size_t)pos * d + c);
+            float4 p0 = __ldg(src), p1 = __ldg(src + 1);
 #pragma unroll 8
-        for (int sl = 1; sl < nsplit; ++sl) {  // independent loads: keep them in flight together
-            const float4* q = reinterpret_cast<const float4*>(y_perm + sl * perm_stride + (size_t)pos * d + c);
-            add4(p0, __ldg(q));
-            add4(p1, __ldg(q + 1));
+            for (int sl = 1; sl < nsplit; ++sl) {  // independent loads: keep them in flight together
+                const float4* q = reinterpret_cast<const float4*>(y_perm + sl * perm_stride + (size_t)pos * d + c);
+                add4(p0, __ldg(q));
+                add4(p1, __ldg(q + 1));
+            }
+            add4(a0, p0);
+            add4(a1, p1);
         }
-        add4(a0, p0);
-        add4(a1, p1);
     }
+    if (n_empty && !any && lane == 0 && c == 0) atomicAdd(n_empty, 1);  // a token no expert took
     if (!active) return;
     if (y_shared) {
         const float4* src = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
@@ -202,23 +215,23 @@ cudaError_t launch_bias_update(int T, int E, int k, const int32_t* counts, float
 
 cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_perm, size_t perm_stride,
                                  int nsplit, const int32_t* slot_pos, const float* y_shared, size_t shared_stride,
-                                 int shared_nsplit, void* y, cudaStream_t s) {
+                                 int shared_nsplit, void* y, cudaStream_t s, int32_t* n_empty) {
     if (T == 0) return cudaSuccess;
     const long long warps = (long long)T * ((d + 255) / 256);
     const int grid = (int)((warps + 7) / 8);
     if (dtype == MOE_BF16)
         launch_pdl(combine_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
                                                            shared_stride, shared_nsplit,
-                                                           static_cast<__nv_bfloat16*>(y));
+                                                           static_cast<__nv_bfloat16*>(y), n_empty);
     else
         launch_pdl(combine_kernel<float>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
-                                                   shared_stride, shared_nsplit, static_cast<float*>(y));
+                                                   shared_stride, shared_nsplit, static_cast<float*>(y), n_empty);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, const int32_t* slot_pos,
-                           const float* y_shared, void* y, cudaStream_t s) {
-    return launch_combine_split(dtype, T, d, k, y_perm, 0, 1, slot_pos, y_shared, 0, 1, y, s);
+                           const float* y_shared, void* y, cudaStream_t s, int32_t* n_empty) {
+    return launch_combine_split(dtype, T, d, k, y_perm, 0, 1, slot_pos, y_shared, 0, 1, y, s, n_empty);
 }
 
 cudaError_t launch_swiglu_finalize(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,

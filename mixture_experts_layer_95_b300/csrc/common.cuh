@@ -133,24 +133,26 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { retu
 // Fused router for E <= kWarpRouterMaxE: logits, softmax, top-k, gates, a
 // per-block partial sum of the softmax rows (p_part [nblk][E]) and, when
 // block_hist != nullptr, the per-block expert histogram of the chosen ids
-// (block_hist [nblk][E]).
+// (block_hist [nblk][E]); when probs != nullptr, every softmax row (probs
+// [T][E]).  k = 0 computes the softmax only (no ids, no gates).
 cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
                                const float* logit_bias, const float* select_bias, int renormalize,
                                int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
-                               cudaStream_t s);
+                               cudaStream_t s, float* probs = nullptr);
 
 // Router for T <= kSplitDRouterMaxT and E <= 32: one block per token, same
 // outputs with one histogram row per token.
 cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
                                   const float* logit_bias, const float* select_bias, int renormalize,
                                   int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
-                                  cudaStream_t s);
+                                  cudaStream_t s, float* probs = nullptr);
 
 // Softmax / top-k over precomputed fp32 logits [T][E] (any E <= kMaxExperts);
 // same outputs as the fused router.
 cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, const float* logit_bias,
                                       const float* select_bias, int renormalize, int32_t* topk_ids,
-                                      float* gates, float* p_part, int32_t* block_hist, cudaStream_t s);
+                                      float* gates, float* p_part, int32_t* block_hist, cudaStream_t s,
+                                      float* probs = nullptr);
 
 // p_mean[e] = (sum over blocks of p_part[b][e]) / T, fixed order.
 cudaError_t launch_p_mean(int T, int E, int nblk, const float* p_part, float* p_mean, cudaStream_t s);
@@ -189,7 +191,16 @@ cudaError_t launch_gather_rows(int dtype, int T, int d, int rows_max, const int3
 
 // y[t] = sum_j y_perm[slot_pos[t][j]] (slot_pos >= 0) + y_shared[t].
 cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, const int32_t* slot_pos,
-                           const float* y_shared, void* y, cudaStream_t s);
+                           const float* y_shared, void* y, cudaStream_t s, int32_t* n_empty = nullptr);
+
+// Expert-choice routing: expert e takes the C tokens with the largest
+// probs[t][e] (ties to the lower token index), in ascending token order, as
+// rows [e*C, (e+1)*C) of the permuted layout; writes sorted_token_ids and
+// gates_perm [E*C], slot_pos [T][E] (row or -1), counts/kept [E] (= C,
+// nullable), offsets [E+1] (= e*C) and zeroes *n_empty (nullable).
+cudaError_t launch_ec_select(int T, int E, int C, const float* probs, int32_t* sorted_token_ids, float* gates_perm,
+                             int32_t* slot_pos, int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* n_empty,
+                             cudaStream_t s);
 
 // bias[e] -= gamma * sign(counts[e] - T k / E).
 cudaError_t launch_bias_update(int T, int E, int k, const int32_t* counts, float gamma, float* bias, cudaStream_t s);
@@ -251,7 +262,7 @@ cudaError_t launch_reduce_partials(int rows_max, const int32_t* rows_dev, int N,
 // Combine over split-K partials: y[t] = sum_j (sum_s Yp[s][pos_j]) + sum_s Ys[s][t].
 cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_perm, size_t perm_stride,
                                  int nsplit, const int32_t* slot_pos, const float* y_shared, size_t shared_stride,
-                                 int shared_nsplit, void* y, cudaStream_t s);
+                                 int shared_nsplit, void* y, cudaStream_t s, int32_t* n_empty = nullptr);
 
 // CUDA-core fp32 path with the same semantics (dtype MOE_F32).
 cudaError_t launch_gemm_simt_f32(int mode, const GemmProblem* probs, int nprob, cudaStream_t s);

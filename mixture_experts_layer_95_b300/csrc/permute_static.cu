@@ -37,6 +37,7 @@ int static_check(const moe_config* c) {
     if (c->T < 0 || c->d < 8 || c->d % 8 || c->E < 1 || c->E > kMaxExperts || c->k < 1 || c->k > c->E ||
         c->k > 32 || (long long)c->T * c->k >= (1LL << 31))
         return MOE_ERR_SHAPE;
+    if (c->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_SHAPE;  // token-choice grouping only
     return MOE_OK;
 }
 

@@ -9,7 +9,9 @@
 //   ids = top-k of l + select_bias, descending, ties to the lower index
 //   g_j = p[ids_j] / sum_j p[ids_j]   (or p[ids_j] without renormalisation)
 // plus, per block, the partial column sums of p (for the mean router
-// probability p_i) and the histogram of the chosen ids (for the grouping scan).
+// probability p_i) and the histogram of the chosen ids (for the grouping scan),
+// and optionally the whole row p (expert-choice routing ranks tokens by it;
+// it then calls the router with k = 0, which skips the top-k).
 //
 // Three kernels:
 //  * router_warp_kernel -- one warp per token, E <= 16 experts, W_g staged in
@@ -37,7 +39,7 @@ constexpr int kTokensPerWarp = kRouterTokensPerBlock / kWarps;
 template <int NJ>
 __device__ __forceinline__ void softmax_topk(int t, int E, int k, const float (&l)[NJ], const float* select_bias,
                                              int renormalize, int32_t* topk_ids, float* gates, float (&psum)[NJ],
-                                             int (&hcnt)[NJ]) {
+                                             int (&hcnt)[NJ], float* probs_out) {
     const int lane = threadIdx.x & 31;
     float m = -FLT_MAX;
 #pragma unroll
@@ -59,6 +61,7 @@ __device__ __forceinline__ void softmax_topk(int t, int E, int k, const float (&
         const int e = lane + 32 * j;
         p[j] = ex[j] * inv_z;
         psum[j] += p[j];
+        if (probs_out && e < E) probs_out[(size_t)t * E + e] = p[j];
         s[j] = (e < E) ? l[j] + (select_bias ? __ldg(select_bias + e) : 0.f) : -FLT_MAX;
     }
     uint32_t taken = 0;
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
     int Tn, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ wg,
     const float* __restrict__ logit_bias, const float* __restrict__ select_bias, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
-    int32_t* __restrict__ block_hist) {
+    int32_t* __restrict__ block_hist, float* __restrict__ probs) {
     pdl_wait();
     constexpr int kW = kWarpRouterThreads / 32;
     constexpr int kTpw = kWarpRouterChunk / kW;
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
             const float v = warp_sum(acc[q][e]);
             if (lane == e && e < E) l[0] = v + (logit_bias ? __ldg(logit_bias + e) : 0.f);
         }
-        softmax_topk<1>(t0 + q, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
+        softmax_topk<1>(t0 + q, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
     }
     block_epilogue<1, kW>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
     __syncthreads();
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kSplitDThreads) router_split_d_kernel(
     int Tn, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ wg,
     const float* __restrict__ logit_bias, const float* __restrict__ select_bias, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
-    int32_t* __restrict__ block_hist) {
+    int32_t* __restrict__ block_hist, float* __restrict__ probs) {
     pdl_wait();
     constexpr int VE = Vec<T>::kElems;
     constexpr int kW = kSplitDThreads / 32;
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kSplitDThreads) router_split_d_kernel(
     }
     float psum[1] = {0.f};
     int hcnt[1] = {0};
-    softmax_topk<1>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
+    softmax_topk<1>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
     if (lane < E) {
         if (p_part) p_part[(size_t)t * E + lane] = psum[0];
         if (block_hist) block_hist[(size_t)t * E + lane] = hcnt[0];
@@ -281,7 +284,8 @@ template <int NJ>
 __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
     int Tn, int E, int k, const float* __restrict__ logits, const float* __restrict__ logit_bias,
     const float* __restrict__ select_bias, int renormalize, int32_t* __restrict__ topk_ids,
-    float* __restrict__ gates, float* __restrict__ p_part, int32_t* __restrict__ block_hist) {
+    float* __restrict__ gates, float* __restrict__ p_part, int32_t* __restrict__ block_hist,
+    float* __restrict__ probs) {
     pdl_wait();
     extern __shared__ float s_dyn[];
     float* s_p = s_dyn;
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
             const int e = lane + 32 * j;
             l[j] = (e < E) ? logits[(size_t)t * E + e] + (logit_bias ? __ldg(logit_bias + e) : 0.f) : -FLT_MAX;
         }
-        softmax_topk<NJ>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt);
+        softmax_topk<NJ>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
     }
     block_epilogue<NJ, kWarps>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
     __syncthreads();
@@ -324,7 +328,7 @@ __global__ void p_mean_kernel(int Tn, int E, int nblk, const float* __restrict__
 cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
                                const float* logit_bias, const float* select_bias, int renormalize,
                                int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
-                               cudaStream_t s) {
+                               cudaStream_t s, float* probs) {
     const int nblk = (T + kWarpRouterChunk - 1) / kWarpRouterChunk;
     if (nblk == 0) return cudaSuccess;
     const int ne = warp_router_width(E);
@@ -338,7 +342,7 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
         launch_pdl(router_warp_kernel<TY, NE>, dim3(grid), dim3(block), smem, s, T, d, E, k, static_cast<const TY*>(x),           \
                                                              static_cast<const TY*>(w_gate), logit_bias,       \
                                                              select_bias, renormalize, topk_ids, gates, p_part, \
-                                                             block_hist);                                       \
+                                                             block_hist, probs);                                \
     } while (0)
     if (dtype == MOE_BF16) {
         if (ne == 8) MOE_ROUTER_CASE(__nv_bfloat16, 8);
@@ -354,13 +358,13 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
 cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
                                   const float* logit_bias, const float* select_bias, int renormalize,
                                   int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, float* probs) {
     if (T == 0) return cudaSuccess;
 #define MOE_SPLITD_CASE(TY, NE)                                                                              \
     launch_pdl(router_split_d_kernel<TY, NE>, dim3(T), dim3(kSplitDThreads), 0, s, T, d, E, k, static_cast<const TY*>(x),       \
                                                                static_cast<const TY*>(w_gate), logit_bias,  \
                                                                select_bias, renormalize, topk_ids, gates,  \
-                                                               p_part, block_hist)
+                                                               p_part, block_hist, probs)
     if (dtype == MOE_BF16) {
         if (E <= 8) MOE_SPLITD_CASE(__nv_bfloat16, 8);
         else if (E <= 16) MOE_SPLITD_CASE(__nv_bfloat16, 16);
@@ -376,7 +380,8 @@ cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const v
 
 cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, const float* logit_bias,
                                       const float* select_bias, int renormalize, int32_t* topk_ids,
-                                      float* gates, float* p_part, int32_t* block_hist, cudaStream_t s) {
+                                      float* gates, float* p_part, int32_t* block_hist, cudaStream_t s,
+                                      float* probs) {
     const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
     if (nblk == 0) return cudaSuccess;
     const size_t smem = (size_t)kWarps * E * (sizeof(float) + sizeof(int));
@@ -385,7 +390,7 @@ cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, 
     do {                                                                                                     \
         cudaFuncSetAttribute(router_logits_kernel<NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
         launch_pdl(router_logits_kernel<NJ>, dim3(grid), dim3(block), smem, s, T, E, k, logits, logit_bias, select_bias,       \
-                                                           renormalize, topk_ids, gates, p_part, block_hist); \
+                                                           renormalize, topk_ids, gates, p_part, block_hist, probs); \
     } while (0)
     if (E <= 64) MOE_LOGITS_CASE(2);
     else if (E <= 256) MOE_LOGITS_CASE(8);

@@ -49,6 +49,7 @@ class Workload:
     select_bias: bool = False    # draw a selection-only bias ~ U(-0.1, 0.1)
     zipf_s: float = 0.0          # > 0: add Zipf(s) log-probabilities to the logits
     h_split: bool = False        # layer option: keep H as a hi + lo bf16 pair
+    routing: str = "token"       # "token": tokens pick top-k experts; "expert": experts pick C tokens
     seed: int = 0
     notes: str = field(default="", compare=False)
 
@@ -70,6 +71,9 @@ WORKLOADS = {
     # same expert shapes and tokens per expert as mixtral_prefill at half the
     # memory (4 experts, 2048 tokens): the case profiled with ncu --set full
     "mixtral_prefill_e4": Workload("mixtral_prefill_e4", T=2048, d=4096, E=4, F=14336, k=2),
+    # expert-choice routing on the Mixtral prefill shape: every expert takes
+    # C = T k / E = 1024 tokens (the same GEMM work as token choice)
+    "mixtral_prefill_ec": Workload("mixtral_prefill_ec", T=4096, d=4096, E=8, F=14336, k=2, routing="expert"),
     "deepseek_v3": Workload("deepseek_v3", T=8192, d=7168, E=256, F=2048, k=8, n_shared=1, F_s=2048,
                             select_bias=True),
     # the capacity cut leaves most tokens with small outputs and a few with

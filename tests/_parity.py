@@ -42,7 +42,8 @@ TOL = {"bf16": 2e-2, "f32": 1e-4}
 
 def layer_of(w: moe_inputs.Workload) -> moe.Layer:
     return moe.Layer(T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.F, n_shared=w.n_shared, d_ff_shared=w.F_s, dtype=w.dtype,
-                     renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha, h_split=w.h_split)
+                     renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha, h_split=w.h_split,
+                     routing=w.routing)
 
 
 def sample_tokens(T: int, n: int, seed: int = 1234, must=()) -> np.ndarray:
@@ -166,4 +167,120 @@ def check_layer(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | N
         and rep["fused_equals_steps"] and rep["stats_counts_exact"] and rep["f_max_abs_err"] <= 1e-7
         and rep["p_max_abs_err"] <= p_tol and rep["L_abs_err"] <= 1e-5 * max(1.0, abs(st["L"]))
         and rep["steps_stats_equal"])
+    return rep
+
+
+# ---------------------------------------------------------------- expert choice
+
+EC_MARGIN = 1e-5  # score gap at a bucket boundary beyond fp32-vs-fp64 softmax error
+
+
+def run_gpu_ec(L: dict, layer: moe.Layer):
+    """Expert choice: the step entry points, then the fused call twice (+ fp32 y)."""
+    ws = moe.workspace(layer)
+    r = moe.route_expert_choice(layer, L["x"], L["w_gate"], L["logit_bias"], ws=ws)
+    y_perm, y_shared = moe.expert_ffn(layer, r["x_perm"], r["offsets"], r["gates_perm"], L["w1"], L["w3"], L["w2"],
+                                      L["x"], L["ws1"], L["ws3"], L["ws2"], ws=ws)
+    y_steps = moe.combine(layer, y_perm, r["slot_pos"], y_shared)
+    counts = torch.full((layer.E,), layer.bucket, dtype=torch.int32, device=L["x"].device)
+    f, Lb = moe.load_stats(layer, counts, r["p_mean"])
+    status_steps = moe.last_device_status(layer, ws)
+    fw = moe.Forward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], None, L["ws1"], L["ws3"],
+                     L["ws2"], stats=True)
+    y1 = fw(L["x"])
+    y2 = fw(L["x"])
+    status_fused = fw.device_status()
+    layer32 = dataclasses.replace(layer, y_fp32=True)
+    fw32 = moe.Forward(layer32, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], None, L["ws1"], L["ws3"],
+                       L["ws2"])
+    y32 = fw32(L["x"])
+    status_fused |= fw32.device_status()
+    torch.cuda.synchronize()
+    return dict(route=r, y_steps=y_steps, f=f, L=Lb, y1=y1, y2=y2, y32=y32, stats=fw.stats,
+                status_steps=status_steps, status_fused=status_fused)
+
+
+def check_layer_ec(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | None = None) -> dict:
+    """Expert-choice parity.  Selection: for every expert whose oracle gap
+    between its C-th and (C+1)-th score exceeds EC_MARGIN, the GPU's bucket
+    equals the oracle's; every bucket must be valid (each chosen score >=
+    each unchosen score - EC_MARGIN), distinct and ascending.  The slot map,
+    offsets, x_perm and the empty-token count are compared bit-exactly with
+    the oracle's slot form of the GPU's buckets; y against the oracle
+    evaluated on those buckets; statistics against the closed forms."""
+    layer = layer_of(w)
+    C = layer.bucket
+    assert C == oracle.ec_bucket(w.T, w.E, w.k, w.capacity)
+    if L is None:
+        L = moe_inputs.make_layer(w, "cuda")
+    G = run_gpu_ec(L, layer)
+    rep = dict(workload=w.name, C=C, status_steps=G["status_steps"], status_fused=G["status_fused"])
+    Ln = moe_inputs.layer_numpy(L)
+    r = oracle.route(Ln["x"], Ln["w_gate"], 1, Ln["logit_bias"], None, True)
+    probs = r["probs"]
+    own_sel, margin = oracle.ec_select(probs, C)
+    R = {k_: v.cpu().numpy() for k_, v in G["route"].items() if k_ != "x_perm"}
+    rep["probs_max_abs_err"] = float(np.abs(R["probs"] - probs).max())
+    gsel = R["sorted_token_ids"].reshape(w.E, C)
+    outside = margin > EC_MARGIN
+    same = np.array([np.array_equal(gsel[e], own_sel[e]) for e in range(w.E)])
+    rep["experts_inside_margin"] = int((~outside).sum())
+    rep["bucket_mismatch_outside_margin"] = int((~same & outside).sum())
+    rep["buckets_equal_oracle"] = bool(same.all())
+    bad = 0
+    for e in range(w.E):
+        row = gsel[e]
+        if not (np.all(np.diff(row) > 0) and row.min() >= 0 and row.max() < w.T):
+            bad += 1
+            continue
+        chosen = np.zeros(w.T, bool)
+        chosen[row] = True
+        if chosen.all():
+            continue
+        if probs[chosen, e].min() < probs[~chosen, e].max() - EC_MARGIN:
+            bad += 1
+    rep["invalid_buckets"] = bad
+    sl = oracle.ec_slots(gsel, probs)
+    rep["slots_bit_exact"] = bool(np.array_equal(R["slot_pos"], sl["slot_pos"]))
+    rep["offsets_exact"] = bool(np.array_equal(R["offsets"], np.arange(w.E + 1) * C))
+    # gates: the GPU's own scores at the chosen pairs, and close to the oracle's
+    gp = R["gates_perm"].reshape(w.E, C)
+    own = np.array([R["probs"][gsel[e], e] for e in range(w.E)])
+    rep["gates_are_gpu_scores"] = bool(np.array_equal(gp, own))
+    xp = G["route"]["x_perm"]
+    src = L["x"][torch.from_numpy(R["sorted_token_ids"].astype(np.int64)).to(xp.device)]
+    rep["x_perm_bit_exact"] = bool(torch.equal(xp, src))
+
+    toks = sample_tokens(w.T, n_sample if n_sample else w.T)
+    y_or = oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], sl["ids"], sl["gates"], sl["slot_pos"], toks,
+                               (Ln["ws1"], Ln["ws3"], Ln["ws2"]) if w.n_shared else None)
+    y_gpu = G["y32"].cpu().numpy()[toks].astype(np.float64)
+    rms = float(np.sqrt(np.mean(y_or ** 2))) if y_or.size else 0.0
+    err = float(np.abs(y_gpu - y_or).max()) if y_or.size else 0.0
+    rep.update(y_rms=rms, y_max_abs_err=err, y_rel=err / rms if rms > 0 else err, tol=TOL[w.dtype],
+               y_tokens_checked=int(len(toks)))
+    rep["y_stored_is_rne_of_fp32"] = bool(torch.equal(G["y1"], G["y32"].to(G["y1"].dtype)))
+    rep["y_deterministic"] = bool(torch.equal(G["y1"], G["y2"]))
+    rep["fused_equals_steps"] = bool(torch.equal(G["y1"], G["y_steps"]))
+
+    s = {k_: v.cpu().numpy() for k_, v in G["stats"].items()}
+    rep["n_empty"] = sl["n_empty"]
+    rep["stats_counts_exact"] = bool(np.all(s["counts"] == C) and np.all(s["kept"] == C)
+                                     and int(s["n_dropped"][0]) == sl["n_empty"])
+    st_p = probs.mean(axis=0)
+    rep["f_max_abs_err"] = float(np.abs(s["f"] - 1.0 / w.E).max())
+    rep["p_max_abs_err"] = float(np.abs(s["p"] - st_p).max())
+    rep["L"] = float(s["L"][0])
+    rep["L_abs_err"] = float(abs(rep["L"] - w.alpha))  # closed form: alpha * sum_e p_e = alpha
+    rep["steps_stats_equal"] = bool(np.array_equal(G["f"].cpu().numpy(), s["f"]) and
+                                    float(G["L"].cpu().numpy()[0]) == float(s["L"][0]))
+    p_tol = 1e-5 + 1e-6 * math.sqrt(w.T)
+    rep["ok"] = bool(
+        rep["status_steps"] == 0 and rep["status_fused"] == 0 and rep["probs_max_abs_err"] < 1e-5
+        and rep["bucket_mismatch_outside_margin"] == 0 and rep["invalid_buckets"] == 0
+        and rep["slots_bit_exact"] and rep["offsets_exact"] and rep["gates_are_gpu_scores"]
+        and rep["x_perm_bit_exact"] and rep["y_rel"] <= rep["tol"] and rep["y_stored_is_rne_of_fp32"]
+        and rep["y_deterministic"] and rep["fused_equals_steps"] and rep["stats_counts_exact"]
+        and rep["f_max_abs_err"] <= 1e-7 and rep["p_max_abs_err"] <= p_tol
+        and rep["L_abs_err"] <= 1e-5 and rep["steps_stats_equal"])
     return rep
