@@ -27,7 +27,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle_moe.so")
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -56,10 +56,16 @@ def _L():
         _lib.oracle_bias_update.argtypes = [ip, ip, ip, vp, ctypes.c_double, vp, vp]
         _lib.oracle_load_stats_n.argtypes = [ip, ip, ctypes.c_longlong, vp, vp, ctypes.c_double, vp, vp, vp]
         _lib.oracle_ec_select.argtypes = [ip, ip, ip, vp, vp, vp]
+        ll = ctypes.c_longlong
+        _lib.oracle_e4m3_encode.argtypes = [ip, vp, vp]
+        _lib.oracle_e4m3_decode.argtypes = [ip, vp, vp]
+        _lib.oracle_quantize_fp8.argtypes = [ll, ip, ip, vp, vp, vp]
+        _lib.oracle_dequant_fp8.argtypes = [ll, ip, vp, vp, vp]
         _lib.oracle_ec_slots.argtypes = [ip, ip, ip, vp, vp, vp, vp, vp, vp]
         for f in ("oracle_route", "oracle_gates_for_ids", "oracle_group", "oracle_layer_tokens",
                   "oracle_load_stats", "oracle_num_threads", "oracle_bias_update", "oracle_ec_select",
-                  "oracle_ec_slots", "oracle_load_stats_n"):
+                  "oracle_ec_slots", "oracle_load_stats_n", "oracle_e4m3_encode", "oracle_e4m3_decode",
+                  "oracle_quantize_fp8", "oracle_dequant_fp8"):
             getattr(_lib, f).restype = ctypes.c_int
     return _lib
 
@@ -77,7 +83,9 @@ def _dtype_of(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits), got {a.dtype}")
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"oracle takes float32, uint16 (bf16 bits) or float64, got {a.dtype}")
 
 
 def _c(a, dt=None):
@@ -296,3 +304,52 @@ def forward_expert_choice(layer, C, alpha=0.01, sel=None, tokens=None):
                "load_stats_n")
     st = dict(f=f, p=pm, L=float(Lb[0]))
     return dict(y=y, probs=probs, sel=use, own_sel=own_sel, margin=margin, counts=counts, **sl, **st)
+
+
+# ------------------------------------------------------------ FP8 weights
+
+def widen(a):
+    """Exact float64 copy of a float32 array or of bf16 bits held as uint16."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def e4m3_encode(v):
+    """float32 values -> E4M3 codes (round to nearest even, saturating)."""
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _check(_L().oracle_e4m3_encode(v.size, _p(v), _p(out)), "e4m3_encode")
+    return out
+
+
+def e4m3_decode(c):
+    """E4M3 codes -> float64 values (NaN for the two NaN codes)."""
+    c = _c(c, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _check(_L().oracle_e4m3_decode(c.size, _p(c), _p(out)), "e4m3_decode")
+    return out
+
+
+def quantize_fp8(w):
+    """Per-row E4M3 quantisation of a [..., cols] weight array (float32 or bf16
+    bits): returns (codes uint8 of the same shape, scales float32 [rows])."""
+    w = _c(w)
+    dt = _dtype_of(w)
+    cols = w.shape[-1]
+    rows = w.size // cols
+    q = np.empty(w.shape, np.uint8)
+    sc = np.empty(w.shape[:-1], np.float32)
+    _check(_L().oracle_quantize_fp8(rows, cols, dt, _p(w), _p(q), _p(sc)), "quantize_fp8")
+    return q, sc
+
+
+def dequant_fp8(q, scale):
+    """value(q) * scale per row, exactly, as float64."""
+    q, scale = _c(q, np.uint8), _c(scale, np.float32)
+    cols = q.shape[-1]
+    rows = q.size // cols
+    out = np.empty(q.shape, np.float64)
+    _check(_L().oracle_dequant_fp8(rows, cols, _p(q), _p(scale), _p(out)), "dequant_fp8")
+    return out

@@ -45,11 +45,14 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F64 2
 
 /* Exact widening of a stored element to double.  bf16 is the top half of an
- * IEEE binary32, so shifting its 16 bits up gives the same value exactly. */
+ * IEEE binary32, so shifting its 16 bits up gives the same value exactly.
+ * ORACLE_F64 inputs (e.g. dequantised FP8 weights) are used as they are. */
 static double elem(const void *base, int dtype, size_t i) {
     if (dtype == ORACLE_F32) return (double)((const float *)base)[i];
+    if (dtype == ORACLE_F64) return ((const double *)base)[i];
     uint32_t u = (uint32_t)((const uint16_t *)base)[i] << 16;
     float f;
     memcpy(&f, &u, sizeof f);
@@ -466,5 +469,94 @@ int oracle_ec_slots(int T, int E, int C, const int32_t *sel, const double *probs
         empty += !any;
     }
     *n_empty = empty;
+    return 0;
+}
+
+
+/*
+ * FP8 expert weights.  The pages name FP8 (and INT4) quantisation as the way
+ * to fit every expert in memory ("Mixture of Experts" notes, serving: "INT4/FP8
+ * quantization is especially valuable here"; handbook, deployment: DeepSeek-V3's
+ * FP8 weights) and warn that experts calibrate unevenly ("One Deep Concept
+ * #04" s13), but give no format or scaling scheme.  The reading taken here:
+ * OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; largest finite 448; subnormals m/8 * 2^-6)
+ * with one fp32 scale per output channel (per row of every weight matrix), so
+ * each expert -- and each channel -- gets its own range:
+ *   scale = max_i |w_i| / 448    (fp32; 1 for an all-zero row)
+ *   q_i   = E4M3(w_i / scale)    (fp32 quotient, round to nearest even,
+ *                                 saturating to +-448)
+ *   w~_i  = value(q_i) * scale   (the weight the layer then uses; exact in fp64)
+ * The quotient and the rounding are taken in fp32, as the GPU takes them, so
+ * both sides choose the same code.
+ * Pinned: every code's value and the rounding of random, tie and boundary
+ * inputs against PyTorch's float8_e4m3fn cast; the per-row maximum maps to 448;
+ * the error bound of round-to-nearest.
+ */
+static double e4m3_value(uint8_t c) {
+    const int e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+static uint8_t e4m3_encode(float f) {
+    if (isnan(f)) return 0x7F;
+    const uint8_t sign = signbit(f) ? 0x80 : 0;
+    const double a = fabs((double)f);
+    if (a >= 448.0) return sign | 0x7E;  /* saturate (ties at 464 also round to 448) */
+    if (a < ldexp(1.0, -6)) {           /* subnormal grid: multiples of 2^-9 */
+        const double k = nearbyint(a * 512.0);   /* exact scaling; ties to even */
+        return sign | (uint8_t)k;               /* k == 8 is 2^-6, code 0x08 */
+    }
+    int e;
+    const double fr = frexp(a, &e);   /* a = fr * 2^e, fr in [0.5, 1) */
+    const int E = e - 1;              /* a = (2 fr) * 2^E, 2 fr in [1, 2) */
+    double k = nearbyint((2.0 * fr - 1.0) * 8.0);  /* 3-bit mantissa, ties to even */
+    int Eb = E + 7;
+    if (k == 8.0) {
+        k = 0.0;
+        Eb += 1;
+    }
+    if (Eb > 15 || (Eb == 15 && k == 7.0)) return sign | 0x7E;
+    return sign | (uint8_t)((Eb << 3) | (int)k);
+}
+
+int oracle_e4m3_encode(int n, const float *in, uint8_t *out) {
+    for (int i = 0; i < n; ++i) out[i] = e4m3_encode(in[i]);
+    return 0;
+}
+
+int oracle_e4m3_decode(int n, const uint8_t *in, double *out) {
+    for (int i = 0; i < n; ++i) out[i] = e4m3_value(in[i]);
+    return 0;
+}
+
+int oracle_quantize_fp8(long long rows, int cols, int dtype, const void *w, uint8_t *q, float *scale) {
+    if (rows < 0 || cols < 1 || (dtype != ORACLE_F32 && dtype != ORACLE_BF16)) return -1;
+#pragma omp parallel for schedule(static)
+    for (long long r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int i = 0; i < cols; ++i) {
+            const float v = (float)fabs(elem(w, dtype, (size_t)r * cols + i));
+            if (v > amax) amax = v;
+        }
+        volatile float sc = amax > 0.0f ? amax / 448.0f : 1.0f;  /* fp32 quotient */
+        scale[r] = sc;
+        for (int i = 0; i < cols; ++i) {
+            volatile float quot = (float)elem(w, dtype, (size_t)r * cols + i) / sc;  /* fp32 quotient */
+            q[(size_t)r * cols + i] = e4m3_encode(quot);
+        }
+    }
+    return 0;
+}
+
+int oracle_dequant_fp8(long long rows, int cols, const uint8_t *q, const float *scale, double *out) {
+#pragma omp parallel for schedule(static)
+    for (long long r = 0; r < rows; ++r)
+        for (int i = 0; i < cols; ++i)
+            out[(size_t)r * cols + i] = e4m3_value(q[(size_t)r * cols + i]) * (double)scale[r];
     return 0;
 }
