@@ -269,6 +269,46 @@ MOE_API int moe_forward(const moe_config *cfg, const void *x, const void *w_gate
                 const void *ws1, const void *ws3, const void *ws2, void *y, const moe_stats *stats,
                 void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---- FP8 expert weights ------------------------------------------------
+ * The pages name FP8 quantisation of the experts as the way to fit every
+ * expert in memory ("Mixture of Experts" notes, serving; handbook, DeepSeek-V3
+ * in FP8) without fixing a scheme.  Here: OCP E4M3 codes (bias 7, largest
+ * finite 448, no infinities) with one fp32 scale per output channel, i.e. per
+ * row of every weight matrix:
+ *   scale_r = max_i |w_ri| / 448 (1 for an all-zero row),
+ *   q_ri    = E4M3(w_ri / scale_r)  (IEEE fp32 quotient, round to nearest
+ *             even, saturating), and the layer uses w~_ri = value(q_ri) scale_r.
+ * The expert GEMMs stream the one-byte codes (half the bytes of bf16 weights:
+ * the decode-time bound), widen them exactly to bf16 in shared memory and
+ * apply scale_r to the fp32 accumulator of output channel r. */
+
+/* Quantises a [rows][cols] matrix (dtype MOE_BF16 or MOE_F32; cols a multiple
+ * of 16) row by row: q [rows][cols] uint8 codes, scale [rows] fp32.  Device
+ * pointers, 16-byte aligned.  Quantise W1 and W3 as [E*F][d] and W2 as
+ * [E*d][F] (and the shared expert's matrices the same way).
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_ALIGN, MOE_ERR_CUDA. */
+MOE_API int moe_quantize_fp8(const void *w, int32_t dtype, int64_t rows, int32_t cols, uint8_t *q, float *scale,
+                             moe_stream_t stream);
+
+/* FP8 weights of the routed experts (and of the shared expert when
+ * cfg->n_shared == 1; those six pointers may be NULL otherwise). */
+typedef struct moe_fp8_weights {
+    const uint8_t *w1, *w3; /* [E][F][d] codes               */
+    const uint8_t *w2;      /* [E][d][F] codes               */
+    const float *s1, *s3;   /* [E][F] scales (rows of W1/W3) */
+    const float *s2;        /* [E][d] scales (rows of W2)    */
+    const uint8_t *ws1, *ws3, *ws2; /* shared: [F_s][d], [F_s][d], [d][F_s] codes */
+    const float *ss1, *ss3, *ss2;   /* shared: [F_s], [F_s], [d] scales          */
+} moe_fp8_weights;
+
+/* moe_forward with FP8 expert weights (host struct of device pointers).
+ * cfg->dtype must be MOE_BF16 (x, w_gate and y stay bf16; the router is
+ * unchanged) and cfg->h_split 0; d, F and F_s must be multiples of 16.  Both
+ * routings; same workspace, statistics and errors as moe_forward. */
+MOE_API int moe_forward_fp8(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
+                            const float *select_bias, const moe_fp8_weights *w, void *y, const moe_stats *stats,
+                            void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Reads (and clears) the device status word kept in the workspace: MOE_OK,
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  Synchronises `stream` first.
  * Returns MOE_ERR_CUDA if the copy itself fails. */

@@ -27,7 +27,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTY
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
             "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static", "moe_bias_update",
-            "moe_plan_describe", "moe_route_expert_choice")
+            "moe_plan_describe", "moe_route_expert_choice", "moe_quantize_fp8", "moe_forward_fp8")
 STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
 
 
@@ -43,6 +43,11 @@ class MoeConfig(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("capacity", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("y_fp32", ctypes.c_int32), ("h_split", ctypes.c_int32),
                 ("routing", ctypes.c_int32)]
+
+
+class MoeFp8Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w1", "w3", "w2", "s1", "s3", "s2", "ws1", "ws3", "ws2", "ss1", "ss3",
+                                               "ss2")]
 
 
 class MoeStats(ctypes.Structure):
@@ -83,6 +88,11 @@ def lib():
         L.moe_set_stage_events.restype = i32
         L.moe_launch_count.restype = ctypes.c_uint64
         L.moe_route_expert_choice.argtypes = [cfgp] + [vp] * 10 + [vp, sz, vp]
+        L.moe_quantize_fp8.argtypes = [vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, vp, vp, vp]
+        L.moe_quantize_fp8.restype = i32
+        L.moe_forward_fp8.argtypes = [cfgp, vp, vp, vp, vp, ctypes.POINTER(MoeFp8Weights), vp,
+                                      ctypes.POINTER(MoeStats), vp, sz, vp]
+        L.moe_forward_fp8.restype = i32
         L.moe_route_expert_choice.restype = i32
         L.moe_plan_describe.argtypes = [cfgp, ctypes.c_char_p, sz]
         L.moe_plan_describe.restype = i32
@@ -439,29 +449,74 @@ def bias_update(layer: Layer, counts, select_bias, gamma: float, stream=None):
     return select_bias
 
 
+def quantize_fp8(w, stream=None):
+    """moe_quantize_fp8 over the last axis of w (bf16 or fp32, last dim a
+    multiple of 16): returns (codes uint8 of w's shape, scales fp32 w.shape[:-1])."""
+    if not w.is_cuda or not w.is_contiguous() or w.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("w must be a contiguous bf16 or fp32 CUDA tensor")
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sc = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _check(lib().moe_quantize_fp8(_ptr(w), MOE_BF16 if w.dtype == torch.bfloat16 else MOE_F32, rows, cols, _ptr(q),
+                                  _ptr(sc), _stream(stream)), "moe_quantize_fp8")
+    return q, sc
+
+
+def quantize_experts_fp8(layer: "Layer", w1, w3, w2, ws1=None, ws3=None, ws2=None, stream=None) -> dict:
+    """FP8 weight set for moe_forward_fp8: codes and per-row scales of W1, W3,
+    W2 (and of the shared expert when the layer has one)."""
+    out = {}
+    for n, t in (("w1", w1), ("w3", w3), ("w2", w2), ("ws1", ws1), ("ws3", ws3), ("ws2", ws2)):
+        if t is None:
+            continue
+        q, sc = quantize_fp8(t, stream)
+        out[n] = q
+        out["s" + n[1:]] = sc  # w1 -> s1, ws1 -> ss1
+    return out
+
+
 class Forward:
     """Reusable moe_forward call: checks the weights once, owns the workspace,
     and enqueues the whole layer per call (the form the benchmark times)."""
 
     def __init__(self, layer: Layer, w_gate, w1, w3, w2, logit_bias=None, select_bias=None, ws1=None, ws3=None,
-                 ws2=None, stats: bool = False, device=None, stream=None):
+                 ws2=None, stats: bool = False, device=None, stream=None, fp8: dict | None = None):
+        """fp8: an FP8 weight set from quantize_experts_fp8 (then w1/w3/w2 and
+        ws1/ws3/ws2 are ignored and may be None; the call is moe_forward_fp8)."""
         dt = layer.torch_dtype
         self.layer = layer
         self.cfg = layer.cfg()
-        self.w = dict(w_gate=_need(w_gate, (layer.E, layer.d), dt, "w_gate"),
-                      w1=_need(w1, (layer.E, layer.d_ff, layer.d), dt, "w1"),
-                      w3=_need(w3, (layer.E, layer.d_ff, layer.d), dt, "w3"),
-                      w2=_need(w2, (layer.E, layer.d, layer.d_ff), dt, "w2"),
+        E, F, d, Fs = layer.E, layer.d_ff, layer.d, layer.d_ff_shared
+        self.fp8 = None
+        if fp8 is not None:
+            u8, f32 = torch.uint8, torch.float32
+            for n, shape, t in (("w1", (E, F, d), u8), ("w3", (E, F, d), u8), ("w2", (E, d, F), u8),
+                                ("s1", (E, F), f32), ("s3", (E, F), f32), ("s2", (E, d), f32)):
+                _need(fp8.get(n), shape, t, "fp8 " + n)
+            if layer.n_shared:
+                for n, shape, t in (("ws1", (Fs, d), u8), ("ws3", (Fs, d), u8), ("ws2", (d, Fs), u8),
+                                    ("ss1", (Fs,), f32), ("ss3", (Fs,), f32), ("ss2", (d,), f32)):
+                    _need(fp8.get(n), shape, t, "fp8 " + n)
+            self.fp8 = dict(fp8)
+            self._fp8_struct = MoeFp8Weights(*[(self.fp8[n].data_ptr() if self.fp8.get(n) is not None else None)
+                                               for n, _ in MoeFp8Weights._fields_])
+            w1 = w3 = w2 = ws1 = ws3 = ws2 = None
+        else:
+            _need(w1, (E, F, d), dt, "w1")
+            _need(w3, (E, F, d), dt, "w3")
+            _need(w2, (E, d, F), dt, "w2")
+            if layer.n_shared:
+                _need(ws1, (Fs, d), dt, "ws1")
+                _need(ws3, (Fs, d), dt, "ws3")
+                _need(ws2, (d, Fs), dt, "ws2")
+        self.w = dict(w_gate=_need(w_gate, (E, d), dt, "w_gate"), w1=w1, w3=w3, w2=w2,
                       logit_bias=logit_bias, select_bias=select_bias, ws1=ws1, ws3=ws3, ws2=ws2)
         if logit_bias is not None:
             _need(logit_bias, (layer.E,), torch.float32, "logit_bias")
         if select_bias is not None:
             _need(select_bias, (layer.E,), torch.float32, "select_bias")
-        if layer.n_shared:
-            _need(ws1, (layer.d_ff_shared, layer.d), dt, "ws1")
-            _need(ws3, (layer.d_ff_shared, layer.d), dt, "ws3")
-            _need(ws2, (layer.d, layer.d_ff_shared), dt, "ws2")
-        dev = device or w1.device
+        dev = device or w_gate.device
         self.ws = workspace(layer, dev, stream)
         self.stats = None
         self._stats_struct = None
@@ -486,6 +541,11 @@ class Forward:
             _need(y, (L.T, L.d), L.y_dtype, "y")
         wg, lb, sb, w1, w3, w2, s1, s3, s2 = self._args
         st = ctypes.byref(self._stats_struct) if self._stats_struct is not None else None
+        if self.fp8 is not None:
+            _check(lib().moe_forward_fp8(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, ctypes.byref(self._fp8_struct),
+                                         _ptr(y), st, _ptr(self.ws), self.ws.numel(), _stream(stream)),
+                   "moe_forward_fp8")
+            return y
         _check(lib().moe_forward(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(y), st,
                                  _ptr(self.ws), self.ws.numel(), _stream(stream)), "moe_forward")
         return y

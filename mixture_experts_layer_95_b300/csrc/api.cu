@@ -334,7 +334,7 @@ int enqueue_route_ec(const moe_config& c, const Layout& L, void* ws, const void*
 int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_perm, const int32_t* offsets,
                 const float* gates_perm, const void* w1, const void* w3, const void* w2, const void* x,
                 const void* ws1, const void* ws3, const void* ws2, float* y_perm, float* y_shared, int sms,
-                cudaStream_t s, bool reduce_down, const int32_t* gather_idx) {
+                cudaStream_t s, bool reduce_down, const int32_t* gather_idx, const moe_fp8_weights* w8 = nullptr) {
     const Splits sp = choose_splits(c);
     const int n = (int)perm_rows(c);
     void* h = at<void>(ws, L.h);
@@ -399,10 +399,31 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
         down[0].part = at<float>(ws, L.part_dn);
         down[1].part = at<float>(ws, L.part_dn_shared);
     }
+    if (w8) {  // FP8 codes in place of the bf16 weights, plus their row scales
+        up[0].B1 = w8->w1;
+        up[0].B2 = w8->w3;
+        up[0].wscale1 = w8->s1;
+        up[0].wscale2 = w8->s3;
+        down[0].B1 = w8->w2;
+        down[0].wscale1 = w8->s2;
+        up[1].B1 = w8->ws1;
+        up[1].B2 = w8->ws3;
+        up[1].wscale1 = w8->ss1;
+        up[1].wscale2 = w8->ss3;
+        down[1].B1 = w8->ws2;
+        down[1].wscale1 = w8->ss2;
+    }
     int* status = at<int>(ws, L.status);
     {
         StageScope scope(kStageUp, s);
-        if (c.dtype == MOE_BF16) {
+        if (w8) {
+            MOE_LAUNCH(launch_gemm_tc_w8(kGemmSwiGLU, up, np, status, sms, s, sp.up));
+            if (sp.up > 1) {
+                MOE_LAUNCH(launch_swiglu_finalize(n, offsets + c.E, c.d_ff, sp.up, up[0].part, h, nullptr, s));
+                if (c.n_shared)
+                    MOE_LAUNCH(launch_swiglu_finalize(c.T, nullptr, c.d_ff_shared, sp.up, up[1].part, hs, nullptr, s));
+            }
+        } else if (c.dtype == MOE_BF16) {
             MOE_LAUNCH(launch_gemm_tc(kGemmSwiGLU, up, np, status, sms, s, sp.up,
                                       use_pair_gemm(c) && sp.up == 1 && !up[0].a_gather));
             if (sp.up > 1) {
@@ -416,7 +437,14 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     }
     {
         StageScope scope(kStageDown, s);
-        if (c.dtype == MOE_BF16) {
+        if (w8) {
+            MOE_LAUNCH(launch_gemm_tc_w8(kGemmScale, down, np, status, sms, s, sp.down));
+            if (sp.down > 1 && reduce_down) {
+                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
+                if (c.n_shared)
+                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s));
+            }
+        } else if (c.dtype == MOE_BF16) {
             MOE_LAUNCH(launch_gemm_tc(split ? kGemmScaleSplit : kGemmScale, down, np, status, sms, s, sp.down,
                                       use_pair_gemm(c) && sp.down == 1));
             if (sp.down > 1 && reduce_down) {
@@ -437,7 +465,7 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
 int forward_tail(const moe_config& c, const Layout& L, void* ws, const void* x, const int32_t* offsets,
                  const int32_t* sorted, const float* gates_perm, const int32_t* slot_pos, int slots, const void* w1,
                  const void* w3, const void* w2, const void* ws1, const void* ws3, const void* ws2, void* y,
-                 int32_t* n_empty, int sms, cudaStream_t s) {
+                 int32_t* n_empty, int sms, cudaStream_t s, const moe_fp8_weights* w8) {
     int* status = at<int>(ws, L.status);
     void* x_perm = nullptr;
     const int32_t* gather_idx = nullptr;
@@ -452,7 +480,7 @@ int forward_tail(const moe_config& c, const Layout& L, void* ws, const void* x, 
     float* y_perm = at<float>(ws, L.y_perm);
     float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
     MOE_TRY(enqueue_ffn(c, L, ws, x_perm, offsets, gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared, sms,
-                        s, false, gather_idx));
+                        s, false, gather_idx, w8));
     // combine (straight from the down GEMM's split-K slices when it was split)
     const Splits sp = choose_splits(c);
     const float* yp = y_perm;
@@ -475,7 +503,7 @@ int forward_tail(const moe_config& c, const Layout& L, void* ws, const void* x, 
 int forward_expert_choice(const moe_config& c, const Layout& L, void* ws, const void* x, const void* w_gate,
                           const float* logit_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
                           const void* ws3, const void* ws2, void* y, const moe_stats* stats, int nblk, int sms,
-                          cudaStream_t s) {
+                          cudaStream_t s, const moe_fp8_weights* w8) {
     const int C = ec_bucket(c);
     float* probs = at<float>(ws, L.probs);
     int32_t* sorted = at<int32_t>(ws, L.sorted);
@@ -496,7 +524,7 @@ int forward_expert_choice(const moe_config& c, const Layout& L, void* ws, const 
             MOE_LAUNCH(launch_load_stats(c.E * C, c.E, 1, c.alpha, counts, p_mean, stats->f, stats->L, s));
     }
     return forward_tail(c, L, ws, x, offsets, sorted, gates_perm, slot_pos, c.E, w1, w3, w2, ws1, ws3, ws2, y,
-                        n_empty, sms, s);
+                        n_empty, sms, s, w8);
 }
 
 }  // namespace
@@ -675,24 +703,11 @@ int moe_bias_update(const moe_config* cfg, const int32_t* counts, float gamma, f
     return MOE_OK;
 }
 
-int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
-                const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
-                const void* ws3, const void* ws2, void* y, const moe_stats* stats, void* ws, size_t ws_bytes,
-                moe_stream_t stream) {
-    MOE_TRY(check_config(cfg));
-    const moe_config& c = *cfg;
-    if (c.T == 0) return MOE_OK;
-    if (!x || !w_gate || !w1 || !w3 || !w2 || !y) return MOE_ERR_NULL;
-    if (c.n_shared && (!ws1 || !ws3 || !ws2)) return MOE_ERR_NULL;
-    MOE_TRY(check_ws(cfg, ws, ws_bytes));
-    for (const void* p : {x, w_gate, w1, w3, w2, (const void*)y})
-        if (!aligned16(p)) return MOE_ERR_ALIGN;
-    if (c.n_shared)
-        for (const void* p : {ws1, ws3, ws2})
-            if (!aligned16(p)) return MOE_ERR_ALIGN;
-    int sms = 0;
-    MOE_TRY(device_sms(&sms));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+// Steps 1-7 after argument checks; w8 != nullptr: FP8 expert weights.
+static int forward_body(const moe_config& c, const void* x, const void* w_gate, const float* logit_bias,
+                        const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                        const void* ws3, const void* ws2, const moe_fp8_weights* w8, void* y, const moe_stats* stats,
+                        void* ws, cudaStream_t s, int sms) {
     const Layout L = layout(c);
     int* status = at<int>(ws, L.status);
     int32_t* topk_ids = at<int32_t>(ws, L.topk_ids);
@@ -702,7 +717,7 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
     const int nblk = (c.T + chunk - 1) / chunk;
     if (expert_choice(c))
         return forward_expert_choice(c, L, ws, x, w_gate, logit_bias, w1, w3, w2, ws1, ws3, ws2, y, stats, nblk,
-                                     sms, s);
+                                     sms, s, w8);
 
     // 1-3: router, softmax, top-k; the router blocks also emit their id histograms
     MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, block_hist, sms, s, c.k));
@@ -732,7 +747,65 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
     // gathers x rows itself with TMA gather4), expert FFNs (routed groups +
     // shared expert in the same launches), combine
     return forward_tail(c, L, ws, x, o.offsets, o.sorted_token_ids, o.gates_perm, o.slot_pos, c.k, w1, w3, w2, ws1,
-                        ws3, ws2, y, nullptr, sms, s);
+                        ws3, ws2, y, nullptr, sms, s, w8);
+}
+
+int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                const void* ws3, const void* ws2, void* y, const moe_stats* stats, void* ws, size_t ws_bytes,
+                moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (c.T == 0) return MOE_OK;
+    if (!x || !w_gate || !w1 || !w3 || !w2 || !y) return MOE_ERR_NULL;
+    if (c.n_shared && (!ws1 || !ws3 || !ws2)) return MOE_ERR_NULL;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    for (const void* p : {x, w_gate, w1, w3, w2, (const void*)y})
+        if (!aligned16(p)) return MOE_ERR_ALIGN;
+    if (c.n_shared)
+        for (const void* p : {ws1, ws3, ws2})
+            if (!aligned16(p)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    return forward_body(c, x, w_gate, logit_bias, select_bias, w1, w3, w2, ws1, ws3, ws2, nullptr, y, stats, ws,
+                        reinterpret_cast<cudaStream_t>(stream), sms);
+}
+
+int moe_forward_fp8(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                    const float* select_bias, const moe_fp8_weights* w, void* y, const moe_stats* stats, void* ws,
+                    size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (c.dtype != MOE_BF16 || c.h_split != 0) return MOE_ERR_DTYPE;
+    if (c.d % 16 || c.d_ff % 16 || (c.n_shared && c.d_ff_shared % 16)) return MOE_ERR_SHAPE;
+    if (c.T == 0) return MOE_OK;
+    if (!w || !x || !w_gate || !y || !w->w1 || !w->w3 || !w->w2 || !w->s1 || !w->s3 || !w->s2) return MOE_ERR_NULL;
+    if (c.n_shared && (!w->ws1 || !w->ws3 || !w->ws2 || !w->ss1 || !w->ss3 || !w->ss2)) return MOE_ERR_NULL;
+    MOE_TRY(check_ws(cfg, ws, ws_bytes));
+    for (const void* p : {x, w_gate, (const void*)y, (const void*)w->w1, (const void*)w->w3, (const void*)w->w2,
+                          (const void*)w->s1, (const void*)w->s3, (const void*)w->s2})
+        if (!aligned16(p)) return MOE_ERR_ALIGN;
+    if (c.n_shared)
+        for (const void* p : {(const void*)w->ws1, (const void*)w->ws3, (const void*)w->ws2, (const void*)w->ss1,
+                              (const void*)w->ss3, (const void*)w->ss2})
+            if (!aligned16(p)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    return forward_body(c, x, w_gate, logit_bias, select_bias, w->w1, w->w3, w->w2, w->ws1, w->ws3, w->ws2, w, y,
+                        stats, ws, reinterpret_cast<cudaStream_t>(stream), sms);
+}
+
+int moe_quantize_fp8(const void* w, int32_t dtype, int64_t rows, int32_t cols, uint8_t* q, float* scale,
+                     moe_stream_t stream) {
+    if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_DTYPE;
+    if (rows < 0 || cols < 16 || cols % 16) return MOE_ERR_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !q || !scale) return MOE_ERR_NULL;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(scale)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    MOE_LAUNCH(launch_quantize_fp8(dtype, rows, cols, w, q, scale, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
 }
 
 int moe_last_device_status(const moe_config* cfg, void* ws, moe_stream_t stream) {

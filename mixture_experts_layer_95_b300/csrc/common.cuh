@@ -238,6 +238,10 @@ struct GemmProblem {
     float* part;          // split-K: fp32 partials [ksplit][a_rows][2N (SwiGLU) or N]
     const int32_t* a_gather;  // non-null: A row r is row a_gather[r] of A, which has a_src_rows rows
     int a_src_rows;
+    // FP8 (E4M3) weights (launch_gemm_tc_w8): B1/B2 hold one-byte codes and
+    // these the fp32 scale of every weight row ([G*N]), applied per column
+    const float* wscale1;
+    const float* wscale2;
 };
 
 // Tensor-core (tcgen05) path, bf16 operands, fp32 accumulate.  Runs up to two
@@ -249,6 +253,19 @@ struct GemmProblem {
 // Scale modes, ksplit 1, plain A) for large expert segments.
 cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
                            cudaStream_t s, int ksplit = 1, bool pair = false);
+
+// Same grouped GEMM with FP8 (E4M3) B operands: raw one-byte tiles stream in
+// through a deep TMA ring, four converter warps widen them (exactly) to the
+// bf16 swizzled layout the MMA reads, and the epilogue multiplies column n by
+// wscale[n] (per weight row).  SwiGLU and Scale modes, 1-CTA tiles, split-K
+// and gathered A as in launch_gemm_tc; K must be a multiple of 16.
+cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
+                              cudaStream_t s, int ksplit = 1);
+
+// Per-row E4M3 quantisation of a [rows][cols] bf16 or fp32 matrix (cols a
+// multiple of 16): q [rows][cols] codes, scale [rows] fp32.
+cudaError_t launch_quantize_fp8(int dtype, long long rows, int cols, const void* w, uint8_t* q, float* scale,
+                                cudaStream_t s);
 
 // H[r][f] = silu(sum_s P[s][r][f]) * sum_s P[s][r][N + f] (bf16, and the lo
 // half when h_lo != nullptr) for r < rows, rows = *rows_dev when non-null.

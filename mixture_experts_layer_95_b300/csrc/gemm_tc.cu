@@ -36,6 +36,7 @@
 //    MOE_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded)
 //    for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -61,6 +62,11 @@ struct StageCfg {
     static constexpr int kBytes = kBOff + B_BYTES;
 };
 constexpr int NUM_THREADS = 192;
+// FP8-weight variant: 4 more warps (6..9) widen the raw one-byte B tiles
+constexpr int W8_THREADS = NUM_THREADS + 128;
+constexpr int W8_RING = 2;          // bf16 stages (A + widened B) feeding the MMA
+constexpr int F8_STAGES = 6;        // raw FP8 B tiles in flight
+constexpr int F8_BYTES = BN * BK;   // 256 weight rows x 64 one-byte elements
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = kMaxExperts;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
@@ -82,6 +88,8 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     int ksplit;                // K slices per tile (1: no split)
     float* part[2];            // ksplit > 1: fp32 partials [ksplit][a_rows][part_cols]
     int part_cols[2];          // 2N for SwiGLU (gate half, then up half), N otherwise
+    const float* wscale1[2];   // FP8 weights: per weight-row scale of B1 / B2 (null: bf16 weights)
+    const float* wscale2[2];
     int* status;
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
     int stall_producer;      // test switch: issue no loads, so the consumers' bounded waits run out
@@ -94,6 +102,8 @@ struct SmemTail {
     uint64_t empty[kMaxRing];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
+    uint64_t f8full[F8_STAGES];   // FP8 variant: raw tile landed
+    uint64_t f8empty[F8_STAGES];  // FP8 variant: raw tile widened, slot free
     uint32_t tmem_base;
     int abort_flag;
     int total[2];
@@ -107,9 +117,15 @@ struct SmemTail {
     float stage[4][32][33];
 };
 
-template <int MODE>
+template <int MODE, bool W8>
+constexpr int ring_stages() {
+    return W8 ? W8_RING : StageCfg<MODE>::kStages;
+}
+
+template <int MODE, bool W8>
 constexpr size_t smem_bytes() {
-    return 1024 /*align slack*/ + (size_t)StageCfg<MODE>::kStages * StageCfg<MODE>::kBytes + sizeof(SmemTail);
+    return 1024 /*align slack*/ + (size_t)ring_stages<MODE, W8>() * StageCfg<MODE>::kBytes +
+           (W8 ? (size_t)F8_STAGES * F8_BYTES : 0) + sizeof(SmemTail);
 }
 
 // ---------------------------------------------------------------- PTX helpers
@@ -245,6 +261,56 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Two E4M3 codes (low byte first) -> two bf16 (low half first).  Every E4M3
+// value is a normal fp16 and has at most 4 significant bits, so the hardware
+// E4M3 -> fp16 conversion and the fp16 -> fp32 -> bf16 steps are all exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    uint32_t h2;
+    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(two));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// One raw FP8 B tile (256 rows x 64 bytes, row-major, as the TMA unit wrote
+// it) -> the bf16 K-major 128-byte-swizzled tile the MMA reads (row r at
+// r * 128 bytes, its 16-byte chunk c at chunk c ^ (r % 8)).  128 threads,
+// 16 chunks of 8 elements each; reads and writes are bank-conflict free.
+__device__ __forceinline__ void widen_b_tile(const uint8_t* src, uint8_t* dst, int ctid) {
+#pragma unroll 4
+    for (int q = 0; q < 16; ++q) {
+        const int idx = ctid + q * 128;
+        const int r = idx >> 3, c = idx & 7;
+        const uint2 raw = *reinterpret_cast<const uint2*>(src + r * BK + c * 8);
+        uint4 out;
+        out.x = e4m3x2_to_bf16x2(raw.x & 0xFFFFu);
+        out.y = e4m3x2_to_bf16x2(raw.x >> 16);
+        out.z = e4m3x2_to_bf16x2(raw.y & 0xFFFFu);
+        out.w = e4m3x2_to_bf16x2(raw.y >> 16);
+        *reinterpret_cast<uint4*>(dst + r * (BK * 2) + ((c ^ (r & 7)) << 4)) = out;
+    }
+}
+
+// v[i] *= scale of weight row wrow + i (FP8 weights), for the 32 columns of
+// one tcgen05.ld; rem = columns that exist from wrow on (>= 32: all).
+__device__ __forceinline__ void apply_wscale32(uint32_t (&v)[32], const float* ws, size_t wrow, int rem) {
+    if (rem >= 32) {
+        const float4* p4 = reinterpret_cast<const float4*>(ws + wrow);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 sc = __ldg(p4 + q);
+            v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) * sc.x);
+            v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) * sc.y);
+            v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) * sc.z);
+            v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) * sc.w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            v[i] = __float_as_uint(i < rem ? __uint_as_float(v[i]) * __ldg(ws + wrow + i) : 0.f);
+    }
+}
+
 // ------------------------------------------------------------- tile schedule
 
 struct Tile {
@@ -318,6 +384,12 @@ __device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& 
             col = t.n * BN + c0;
         const int lim = (MODE == kGemmSwiGLU && c0 >= BN / 2) ? 2 * N : N;
         if (!valid || col >= lim) continue;
+        {
+            const bool up_half = MODE == kGemmSwiGLU && c0 >= BN / 2;
+            const float* ws = up_half ? p.wscale2[t.prob] : p.wscale1[t.prob];
+            const int wc = up_half ? col - N : col;  // weight row within the group
+            if (ws) apply_wscale32(v, ws, static_cast<size_t>(t.g) * N + wc, N - wc);
+        }
         float* dst = base + col;
         if (col + 32 <= lim) {
 #pragma unroll
@@ -353,6 +425,11 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             tmem_ld_wait();
             const int col = t.n * (BN / 2) + c0;
             if (!valid || col >= N) continue;
+            if (p.wscale1[t.prob]) {  // FP8 weights: per-channel scales of W1 and W3
+                const size_t wr = static_cast<size_t>(t.g) * N + col;
+                apply_wscale32(g, p.wscale1[t.prob], wr, N - col);
+                apply_wscale32(u, p.wscale2[t.prob], wr, N - col);
+            }
             __nv_bfloat16* dst = out + grow * N + col;
             __nv_bfloat16* dst_lo = out_lo ? out_lo + grow * N + col : nullptr;
             if (col + 32 <= N) {
@@ -403,6 +480,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             tmem_ld_wait();
             const int col = t.n * BN + c0;
             if (col >= N || nvalid <= 0) continue;  // uniform across the warp
+            if (p.wscale1[t.prob]) apply_wscale32(v, p.wscale1[t.prob], static_cast<size_t>(t.g) * N + col, N - col);
 #pragma unroll
             for (int i = 0; i < 32; ++i) stage[lane][i] = scale * __uint_as_float(v[i]);
             __syncwarp();
@@ -416,22 +494,31 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
 
 // ------------------------------------------------------------------ kernel
 
-template <int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const __grid_constant__ TcParams p) {
+template <int MODE, bool W8>
+__global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using SC = StageCfg<MODE>;
-    constexpr int NST = SC::kStages;
-    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)NST * SC::kBytes);
+    constexpr int NST = ring_stages<MODE, W8>();
+    static_assert(!W8 || MODE == kGemmSwiGLU || MODE == kGemmScale, "FP8 weights: SwiGLU and Scale modes only");
+    uint8_t* f8ring = smem + (size_t)NST * SC::kBytes;  // FP8 variant: raw B tiles
+    SmemTail& st = *reinterpret_cast<SmemTail*>(f8ring + (W8 ? (size_t)F8_STAGES * F8_BYTES : 0));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &st.abort_flag;
 
     // ---- prologue: barriers, TMEM, tile prefix ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
-            mbar_init(&st.full[s], 1);
+            // FP8 variant: the A copy's expect_tx plus one arrival per converter warp
+            mbar_init(&st.full[s], W8 ? 5 : 1);
             mbar_init(&st.empty[s], 1);
         }
+        if (W8)
+            for (int j = 0; j < F8_STAGES; ++j) {
+                mbar_init(&st.f8full[j], 1);
+                mbar_init(&st.f8empty[j], 4);
+            }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&st.tmem_full[a], 1);
             mbar_init(&st.tmem_empty[a], 4);
@@ -499,7 +586,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
     const uint32_t tmem_base = st.tmem_base;
     const int total_tiles = st.total[0] + st.total[1];
 
-    if (warp == 0) {
+    if (W8 && warp == 0) {
+        // ---------------- TMA producer, FP8 weights ----------------
+        // Only the raw B tiles: F8_STAGES of them in flight, each freed by the
+        // converter warps once widened (A is loaded by the converters).
+        int j = 0;
+        uint32_t ph8 = 0;
+        uint32_t issued_parity[F8_STAGES];
+        bool used[F8_STAGES];
+        for (int i = 0; i < F8_STAGES; ++i) used[i] = false;
+        bool dead = p.stall_producer != 0;
+        for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
+            const Tile t = decode_tile<MODE>(st, p, id);
+            const int b_row0 = t.g * p.N[t.prob] + t.n * out_cols_per_tile<MODE>();
+            for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                if (!mbar_wait(&st.f8empty[j], ph8 ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
+                    dead = true;
+                    break;
+                }
+                if (lane == 0) {
+                    uint8_t* dst = f8ring + (size_t)j * F8_BYTES;
+                    mbar_expect_tx(&st.f8full[j], F8_BYTES);
+                    tma_load_2d(dst, &p.tmB1[t.prob], kb * BK, b_row0, &st.f8full[j]);
+                    if (MODE == kGemmSwiGLU)
+                        tma_load_2d(dst + F8_BYTES / 2, &p.tmB2[t.prob], kb * BK, b_row0, &st.f8full[j]);
+                }
+                issued_parity[j] = ph8;
+                used[j] = true;
+                if (++j == F8_STAGES) {
+                    j = 0;
+                    ph8 ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            volatile int no_abort = 0;
+            for (int i = 0; i < F8_STAGES; ++i)
+                if (used[i]) mbar_wait(&st.f8full[i], issued_parity[i], &no_abort, nullptr, kDrainLimitNs);
+        }
+    } else if (warp == 0) {
         // ---------------- TMA producer ----------------
         // Lane 0 arms each stage's barrier and loads B (and A when A is a plain
         // tile); when A rows are gathered, every lane loads 4 of the tile's
@@ -606,7 +732,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
                 umma_commit(&st.tmem_full[acc]);
             }
         }
-    } else {
+    } else if (warp < 6) {
         // ---------------- epilogue (warps 2..5) ----------------
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row_in_tile = quarter * 32 + lane;
@@ -622,6 +748,88 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) grouped_gemm_tc_kernel(const _
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.tmem_empty[acc]);
+        }
+    } else if constexpr (W8) {
+        // ---------------- converters (warps 6..9), FP8 weights ----------------
+        // Per k-block: wait for a free bf16 stage; warp 6 starts the A copy
+        // into it (plain tile or gather4, as the bf16 producer does); then all
+        // four warps widen their quarter of the raw B tile into the stage,
+        // make the writes visible to the tensor cores' async proxy, and
+        // arrive -- on the raw slot (free again) and on the stage (one of the
+        // five arrivals the MMA waits for).
+        const int cw = warp - 6;
+        const int ctid = threadIdx.x - NUM_THREADS;  // 0..127
+        int s = 0, j = 0;
+        uint32_t ph = 0, ph8 = 0;
+        uint32_t issued_parity[NST];
+        bool used[NST];
+        for (int i = 0; i < NST; ++i) used[i] = false;
+        bool dead = false;
+        for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
+            const Tile t = decode_tile<MODE>(st, p, id);
+            const int32_t* gidx = p.a_gather[t.prob];
+            int rows4[4] = {0, 0, 0, 0};
+            if (gidx && cw == 0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = lane * 4 + i;
+                    int v = r < t.rows_valid ? __ldg(gidx + t.a_row0 + r) : 0;
+                    if (v < 0 || v >= p.a_src_rows[t.prob]) {
+                        if (r < t.rows_valid) record_status(p.status, kStatusBounds);
+                        v = 0;
+                    }
+                    rows4[i] = v;
+                }
+            }
+            for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                const bool ok_stage = mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok_stage)) {
+                    dead = true;
+                    break;
+                }
+                uint8_t* sa = smem + (size_t)s * SC::kBytes;
+                uint8_t* sb = sa + SC::kBOff;
+                if (cw == 0) {
+                    if (lane == 0) {
+                        const uint32_t a_bytes =
+                            gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : (uint32_t)A_BYTES;
+                        mbar_expect_tx(&st.full[s], a_bytes);
+                        if (!gidx) tma_load_2d(sa, &p.tmA[t.prob], kb * BK, t.a_row0, &st.full[s]);
+                    }
+                    if (gidx && lane * 4 < t.rows_valid)
+                        tma_gather4(sa + lane * 4 * (BK * 2), &p.tmA[t.prob], kb * BK, rows4[0], rows4[1], rows4[2],
+                                    rows4[3], &st.full[s]);
+                    issued_parity[s] = ph;
+                    used[s] = true;
+                }
+                const bool ok_raw = mbar_wait(&st.f8full[j], ph8, abort_flag, p.status, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, ok_raw)) {
+                    dead = true;
+                    break;
+                }
+                widen_b_tile(f8ring + (size_t)j * F8_BYTES, sb, ctid);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&st.f8empty[j]);
+                    mbar_arrive(&st.full[s]);
+                }
+                if (++s == NST) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                if (++j == F8_STAGES) {
+                    j = 0;
+                    ph8 ^= 1u;
+                }
+            }
+        }
+        // warp 6: no A copy may still be landing when the CTA exits
+        __syncwarp();
+        if (cw == 0 && lane == 0) {
+            volatile int no_abort = 0;
+            for (int i = 0; i < NST; ++i)
+                if (used[i]) mbar_wait(&st.full[i], issued_parity[i], &no_abort, nullptr, kDrainLimitNs);
         }
     }
 
@@ -968,7 +1176,21 @@ bool make_tmap(CUtensorMap* tm, const void* base, int rows, int K, int box_rows)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+// 2-D one-byte (FP8 code) tensor [rows][K], box = 64 x box_rows, no swizzle:
+// the converter warps re-lay the tile out for the MMA themselves.
+bool make_tmap_u8(CUtensorMap* tm, const void* base, int rows, int K, int box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, bool W8 = false>
 cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
     // the shared-memory opt-in is per device; remember it for the first 64 ordinals
     static uint64_t attr_set_mask = 0;
@@ -976,14 +1198,19 @@ cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
     cudaGetDevice(&dev);
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (!bit || !(attr_set_mask & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem_bytes<MODE>()));
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, W8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem_bytes<MODE, W8>()));
         if (e != cudaSuccess) return e;
         attr_set_mask |= bit;
     }
-    launch_pdl(grouped_gemm_tc_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), smem_bytes<MODE>(), s, prm);
+    launch_pdl(grouped_gemm_tc_kernel<MODE, W8>, dim3(grid), dim3(W8 ? W8_THREADS : NUM_THREADS),
+               smem_bytes<MODE, W8>(), s, prm);
     return cudaGetLastError();
 }
+
+static_assert(smem_bytes<kGemmSwiGLU, true>() <= 232448, "FP8 SwiGLU kernel exceeds shared memory");
+static_assert(smem_bytes<kGemmScale, true>() <= 232448, "FP8 Scale kernel exceeds shared memory");
 
 template <int MODE>
 cudaError_t launch_pair_mode(const TcParams& prm, int num_sms, cudaStream_t s) {
@@ -1085,6 +1312,58 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         case kGemmScaleSplit: return launch_mode<kGemmScaleSplit>(prm, grid, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
+                              cudaStream_t s, int ksplit) {
+    if (nprob < 1 || nprob > 2 || ksplit < 1) return cudaErrorInvalidValue;
+    if (mode != kGemmSwiGLU && mode != kGemmScale) return cudaErrorInvalidValue;
+    TcParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.ksplit = ksplit;
+    const int b_box = mode == kGemmSwiGLU ? BN / 2 : BN;
+    if (probs[0].G + (nprob > 1 ? probs[1].G : 0) > MAX_GROUPS + 1) return cudaErrorInvalidValue;
+    for (int q = 0; q < nprob; ++q) {
+        const GemmProblem& g = probs[q];
+        if (g.G < 1 || g.G > MAX_GROUPS || g.K % 16 != 0) return cudaErrorInvalidValue;
+        if (!g.wscale1 || (mode == kGemmSwiGLU && !g.wscale2)) return cudaErrorInvalidValue;
+        if (g.a_gather) {
+            if (!make_tmap(&prm.tmA[q], g.A, g.a_src_rows, g.K, 1)) return cudaErrorInvalidValue;
+            prm.a_gather[q] = g.a_gather;
+            prm.a_src_rows[q] = g.a_src_rows;
+        } else if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) {
+            return cudaErrorInvalidValue;
+        }
+        if (!make_tmap_u8(&prm.tmB1[q], g.B1, g.G * g.N, g.K, b_box)) return cudaErrorInvalidValue;
+        if (mode == kGemmSwiGLU && !make_tmap_u8(&prm.tmB2[q], g.B2, g.G * g.N, g.K, b_box))
+            return cudaErrorInvalidValue;
+        if (ksplit > 1) {
+            if (ksplit > (g.K + BK - 1) / BK || g.part == nullptr) return cudaErrorInvalidValue;
+            prm.part[q] = g.part;
+            prm.part_cols[q] = mode == kGemmSwiGLU ? 2 * g.N : g.N;
+        }
+        prm.offsets[q] = g.offsets;
+        prm.out[q] = g.out;
+        prm.out2[q] = g.out2;
+        prm.row_scale[q] = g.row_scale;
+        prm.wscale1[q] = g.wscale1;
+        prm.wscale2[q] = g.wscale2;
+        prm.G[q] = g.G;
+        prm.M[q] = g.M;
+        prm.N[q] = g.N;
+        prm.K[q] = g.K;
+        prm.a_rows[q] = g.a_rows;
+    }
+    prm.nprob = nprob;
+    prm.status = status;
+    prm.wait_limit_ns = kWaitLimitNs;
+    const char* stall = getenv("MOE_TEST_STALL_GEMM");
+    if (stall && stall[0] == '1') {
+        prm.stall_producer = 1;
+        prm.wait_limit_ns = 20000000ull;
+    }
+    const int grid = num_sms > 0 ? num_sms : 148;
+    return mode == kGemmSwiGLU ? launch_mode<kGemmSwiGLU, true>(prm, grid, s) : launch_mode<kGemmScale, true>(prm, grid, s);
 }
 
 }  // namespace moe

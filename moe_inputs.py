@@ -50,6 +50,7 @@ class Workload:
     zipf_s: float = 0.0          # > 0: add Zipf(s) log-probabilities to the logits
     h_split: bool = False        # layer option: keep H as a hi + lo bf16 pair
     routing: str = "token"       # "token": tokens pick top-k experts; "expert": experts pick C tokens
+    weights: str = "same"        # "same": experts stored in `dtype`; "fp8": E4M3 codes + per-row fp32 scales
     seed: int = 0
     notes: str = field(default="", compare=False)
 
@@ -74,6 +75,12 @@ WORKLOADS = {
     # expert-choice routing on the Mixtral prefill shape: every expert takes
     # C = T k / E = 1024 tokens (the same GEMM work as token choice)
     "mixtral_prefill_ec": Workload("mixtral_prefill_ec", T=4096, d=4096, E=8, F=14336, k=2, routing="expert"),
+    # FP8 (E4M3, per-channel scales) expert weights for decode: half the bytes to stream
+    "mixtral_decode_t1_fp8": Workload("mixtral_decode_t1_fp8", T=1, d=4096, E=8, F=14336, k=2, weights="fp8"),
+    "mixtral_decode_t8_fp8": Workload("mixtral_decode_t8_fp8", T=8, d=4096, E=8, F=14336, k=2, weights="fp8"),
+    "mixtral_decode_t32_fp8": Workload("mixtral_decode_t32_fp8", T=32, d=4096, E=8, F=14336, k=2, weights="fp8"),
+    "mixtral_decode_t128_fp8": Workload("mixtral_decode_t128_fp8", T=128, d=4096, E=8, F=14336, k=2,
+                                        weights="fp8"),
     "deepseek_v3": Workload("deepseek_v3", T=8192, d=7168, E=256, F=2048, k=8, n_shared=1, F_s=2048,
                             select_bias=True),
     # the capacity cut leaves most tokens with small outputs and a few with
@@ -165,6 +172,21 @@ def algorithmic_flops(w: Workload, kept_total: int) -> float:
 
 
 def expert_weight_bytes(w: Workload, n_touched: int) -> float:
-    """Bytes of expert weights a call must read: touched routed experts + shared."""
+    """Bytes of expert weights a call must read: touched routed experts + shared
+    (FP8: one byte per weight plus a 4-byte scale per weight row)."""
+    if w.weights == "fp8":
+        rows = lambda d, F: 2 * F + d  # rows of W1, W3 and W2
+        return float(expert_params(w.d, w.F) * n_touched + expert_params(w.d, w.F_s) * w.n_shared
+                     + 4 * (rows(w.d, w.F) * n_touched + rows(w.d, w.F_s) * w.n_shared))
     eb = 2 if w.dtype == "bf16" else 4
     return float(eb * (expert_params(w.d, w.F) * n_touched + expert_params(w.d, w.F_s) * w.n_shared))
+
+
+def up_weight_bytes(w: Workload, n_touched: int) -> float:
+    """Bytes of W1 and W3 (touched experts + shared) the up GEMM must read."""
+    if w.weights == "fp8":
+        per = lambda F: 2 * F * w.d + 4 * 2 * F
+    else:
+        eb = 2 if w.dtype == "bf16" else 4
+        per = lambda F: 2 * F * w.d * eb
+    return float(per(w.F) * n_touched + per(w.F_s) * w.n_shared)

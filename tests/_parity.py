@@ -284,3 +284,90 @@ def check_layer_ec(w: moe_inputs.Workload, n_sample: int | None = None, L: dict 
         and rep["f_max_abs_err"] <= 1e-7 and rep["p_max_abs_err"] <= p_tol
         and rep["L_abs_err"] <= 1e-5 and rep["steps_stats_equal"])
     return rep
+
+
+# ---------------------------------------------------------------- FP8 weights
+
+def check_quantize(w_dev) -> dict:
+    """GPU per-row E4M3 codes and scales vs the oracle's, bit for bit."""
+    q, sc = moe.quantize_fp8(w_dev)
+    oq, osc = oracle.quantize_fp8(moe_inputs.to_numpy(w_dev))
+    gq, gsc = q.cpu().numpy(), sc.cpu().numpy()
+    return dict(codes_equal=bool(np.array_equal(gq, oq)), scales_equal=bool(np.array_equal(gsc, osc)),
+                n_code_mismatch=int((gq != oq).sum()))
+
+
+def _oracle_y_fp8(Ln, q8, w, ids, gates, slot_pos, toks):
+    """Oracle y for the listed tokens with the dequantised FP8 experts, one
+    expert at a time (only experts some listed token uses are dequantised)."""
+    x64 = oracle.widen(Ln["x"])
+    y = np.zeros((len(toks), w.d))
+    sel = np.zeros_like(ids, dtype=bool)
+    sel[toks] = True
+    for e in np.unique(ids[toks][slot_pos[toks] >= 0]):
+        w1 = oracle.dequant_fp8(q8["w1"][e], q8["s1"][e])[None]
+        w3 = oracle.dequant_fp8(q8["w3"][e], q8["s3"][e])[None]
+        w2 = oracle.dequant_fp8(q8["w2"][e], q8["s2"][e])[None]
+        mine = (ids == e) & sel
+        sp = np.where(mine, slot_pos, -1).astype(np.int32)
+        y += oracle.layer_tokens(x64, w1, w3, w2, np.zeros_like(ids), gates, sp, toks)
+    if w.n_shared:
+        sh = tuple(oracle.dequant_fp8(q8[n], q8[s]) for n, s in (("ws1", "ss1"), ("ws3", "ss3"), ("ws2", "ss2")))
+        y += oracle.layer_tokens(x64, sh[0][None], sh[1][None], sh[2][None], np.zeros_like(ids), gates,
+                                 np.full_like(ids, -1), toks, sh)
+    return y
+
+
+def check_layer_fp8(w: moe_inputs.Workload, n_sample: int | None = None) -> dict:
+    """FP8-weight layer: codes and scales bit-exact with the oracle's
+    quantisation of the same bf16 weights; routing as the bf16 layer (the
+    router is unchanged); y (fp32 result) within the bf16 tolerance of the
+    oracle evaluated with the exactly dequantised weights on the GPU's ids;
+    bf16 y = RNE(fp32 y); deterministic."""
+    layer = layer_of(w)
+    L = moe_inputs.make_layer(w, "cuda")
+    names = ["w1", "w3", "w2"] + (["ws1", "ws3", "ws2"] if w.n_shared else [])
+    q8 = moe.quantize_experts_fp8(layer, *(L[n] for n in names))
+    rep = dict(workload=w.name)
+    # quantisation, bit for bit (a row sample of each matrix when large)
+    Ln = moe_inputs.layer_numpy(L)
+    mism = 0
+    for n in names:
+        src = Ln[n].reshape(-1, Ln[n].shape[-1])
+        rows = np.arange(src.shape[0]) if src.shape[0] <= 4096 else \
+            np.random.default_rng(5).choice(src.shape[0], 4096, replace=False)
+        oq, osc = oracle.quantize_fp8(np.ascontiguousarray(src[rows]))
+        gq = q8[n].reshape(-1, src.shape[1]).cpu().numpy()[rows]
+        gs = q8["s" + n[1:]].reshape(-1).cpu().numpy()[rows]
+        mism += int((gq != oq).sum()) + int((gs != osc).sum())
+    rep["quantisation_mismatches"] = mism
+    q8n = {k_: v.cpu().numpy() for k_, v in q8.items()}
+    del Ln["w1"], Ln["w3"], Ln["w2"]
+    # routing ids from the GPU router (the same kernels the fused call runs)
+    ids, gates, _ = moe.route(layer, L["x"], L["w_gate"], L["logit_bias"], L["select_bias"])
+    gids = ids.cpu().numpy()
+    r = oracle.route(Ln["x"], Ln["w_gate"], w.k, Ln["logit_bias"], Ln["select_bias"], w.renormalize)
+    outside = r["margin"] > MARGIN
+    same_set = np.array([set(a) == set(b) for a, b in zip(gids.tolist(), r["ids"].tolist())])
+    rep["ids_mismatch_outside_margin"] = int((~same_set & outside).sum())
+    og = oracle.group(gids, w.E, w.capacity)
+    ogates = oracle.gates_for_ids(r["probs"], gids, w.renormalize)
+    fw = moe.Forward(layer, L["w_gate"], None, None, None, L["logit_bias"], L["select_bias"], fp8=q8)
+    y1 = fw(L["x"])
+    y2 = fw(L["x"])
+    fw32 = moe.Forward(dataclasses.replace(layer, y_fp32=True), L["w_gate"], None, None, None, L["logit_bias"],
+                       L["select_bias"], fp8=q8)
+    y32 = fw32(L["x"])
+    rep["status"] = fw.device_status() | fw32.device_status()
+    toks = sample_tokens(w.T, n_sample if n_sample else w.T)
+    y_or = _oracle_y_fp8(Ln, q8n, w, gids, ogates, og["slot_pos"], toks)
+    y_gpu = y32.cpu().numpy()[toks].astype(np.float64)
+    rms = float(np.sqrt(np.mean(y_or ** 2))) if y_or.size else 0.0
+    err = float(np.abs(y_gpu - y_or).max()) if y_or.size else 0.0
+    rep.update(y_rms=rms, y_rel=err / rms if rms > 0 else err, tol=TOL["bf16"], y_tokens_checked=int(len(toks)))
+    rep["y_stored_is_rne_of_fp32"] = bool(torch.equal(y1, y32.to(y1.dtype)))
+    rep["y_deterministic"] = bool(torch.equal(y1, y2))
+    rep["ok"] = bool(rep["quantisation_mismatches"] == 0 and rep["status"] == 0
+                     and rep["ids_mismatch_outside_margin"] == 0 and rep["y_rel"] <= rep["tol"]
+                     and rep["y_stored_is_rne_of_fp32"] and rep["y_deterministic"])
+    return rep

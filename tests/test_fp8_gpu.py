@@ -1,0 +1,87 @@
+"""FP8 (E4M3, per-channel scale) expert weights on the GPU vs the oracle (GPU only).
+
+The quantisation kernel must reproduce the oracle's codes and scales bit for
+bit (both take the fp32 quotient and round to nearest even); the layer with
+FP8 experts must match the oracle evaluated with the exactly dequantised
+weights, within the bf16 layer's tolerance.  Covers the tensor-core kernel's
+FP8 path in both modes: ragged N and K tails, the shared expert, split-K
+decode batches with gathered rows, expert-choice routing, and the Mixtral
+decode batches the benchmark times.  Comparison rules: tests/_parity.py.
+"""
+import json
+
+import numpy as np
+import pytest
+import torch
+
+from moe_inputs import WORKLOADS, Workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mixture_experts_layer_95_b300 as moe
+    moe.lib()
+    return torch.device("cuda")
+
+
+def _assert_ok(rep):
+    assert rep["ok"], json.dumps(rep, indent=1)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quantize_matches_oracle_bit_for_bit(cuda, dtype):
+    from tests._parity import check_quantize
+    g = torch.Generator(device="cuda").manual_seed(3)
+    w = torch.randn((300, 272), generator=g, device="cuda") * torch.rand((300, 1), generator=g, device="cuda") * 3
+    w[7] = 0.0                              # all-zero row
+    w[9, :] = torch.tensor(1.0)             # constant row: every code 448
+    w[11, ::2] = 2.0 ** -10                 # row maximum 448 below: scale 1, so these are exact
+    w[11, 1::2] = 3 * 2.0 ** -11            # ties and near-ties on the subnormal grid
+    w[11, 0] = 448.0
+    rep = check_quantize(w.to(dtype).contiguous())
+    assert rep["codes_equal"] and rep["scales_equal"], rep
+
+
+SMALL_FP8 = [
+    Workload("fp8_shared_ragged", T=300, d=272, E=8, F=400, k=2, n_shared=1, F_s=208, weights="fp8"),
+    Workload("fp8_many_tiles", T=1000, d=256, E=4, F=640, k=2, weights="fp8"),
+    Workload("fp8_decode_t1", T=1, d=512, E=8, F=512, k=2, weights="fp8"),
+    Workload("fp8_decode_t5_shared", T=5, d=256, E=16, F=320, k=2, n_shared=1, F_s=192, select_bias=True,
+             weights="fp8"),
+    Workload("fp8_gemm_router_capacity", T=520, d=384, E=64, F=256, k=4, capacity=40, weights="fp8"),
+    Workload("fp8_expert_choice", T=300, d=256, E=8, F=384, k=2, routing="expert", weights="fp8"),
+]
+
+
+@pytest.mark.parametrize("w", SMALL_FP8, ids=[w.name for w in SMALL_FP8])
+def test_fp8_layer_matches_oracle(cuda, w):
+    from tests._parity import check_layer_fp8
+    _assert_ok(check_layer_fp8(w))
+
+
+@pytest.mark.parametrize("name", ["mixtral_decode_t1_fp8", "mixtral_decode_t8_fp8"])
+def test_fp8_mixtral_decode(cuda, name):
+    from tests._parity import check_layer_fp8
+    rep = check_layer_fp8(WORKLOADS[name])
+    print(json.dumps(rep))
+    _assert_ok(rep)
+
+
+def test_forward_fp8_rejects_bad_configs(cuda):
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    w = Workload("fp8_bad", T=4, d=264, E=4, F=64, k=2)  # d not a multiple of 16
+    L = moe_inputs.make_layer(w, "cuda")
+    layer = moe.Layer(T=4, d=264, E=4, k=2, d_ff=64)
+    with pytest.raises(moe.MoeError):
+        moe.quantize_fp8(L["w1"])  # 264 columns: not a multiple of 16
+    q8 = {n: torch.zeros(s, dtype=t, device="cuda") for n, s, t in (
+        ("w1", (4, 64, 264), torch.uint8), ("w3", (4, 64, 264), torch.uint8), ("w2", (4, 264, 64), torch.uint8),
+        ("s1", (4, 64), torch.float32), ("s3", (4, 64), torch.float32), ("s2", (4, 264), torch.float32))}
+    fw = moe.Forward(layer, L["w_gate"], None, None, None, fp8=q8)
+    with pytest.raises(moe.MoeError):
+        fw(L["x"])
