@@ -36,7 +36,6 @@
 //    MOE_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded)
 //    for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
-#include <cuda_fp16.h>
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -64,9 +63,10 @@ struct StageCfg {
 constexpr int NUM_THREADS = 192;
 // FP8-weight variant: 4 more warps (6..9) widen the raw one-byte B tiles
 constexpr int W8_THREADS = NUM_THREADS + 128;
-constexpr int W8_RING = 2;          // bf16 stages (A + widened B) feeding the MMA
-constexpr int F8_STAGES = 6;        // raw FP8 B tiles in flight
 constexpr int F8_BYTES = BN * BK;   // 256 weight rows x 64 one-byte elements
+constexpr int W8_RAW = 4;           // TMA stages in flight: bf16 A tile + one-byte B tile
+constexpr int W8_RAW_BYTES = A_BYTES + F8_BYTES;
+constexpr int W8_WIDE = 2;          // widened bf16 B tiles feeding the MMA
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = kMaxExperts;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
@@ -102,8 +102,8 @@ struct SmemTail {
     uint64_t empty[kMaxRing];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
-    uint64_t f8full[F8_STAGES];   // FP8 variant: raw tile landed
-    uint64_t f8empty[F8_STAGES];  // FP8 variant: raw tile widened, slot free
+    uint64_t wfull[W8_WIDE];   // FP8 variant: widened B tile ready for the MMA
+    uint64_t wempty[W8_WIDE];  // FP8 variant: the MMA is done with a widened B tile
     uint32_t tmem_base;
     int abort_flag;
     int total[2];
@@ -119,13 +119,25 @@ struct SmemTail {
 
 template <int MODE, bool W8>
 constexpr int ring_stages() {
-    return W8 ? W8_RING : StageCfg<MODE>::kStages;
+    return W8 ? W8_RAW : StageCfg<MODE>::kStages;
+}
+
+// bytes of one TMA ring stage
+template <int MODE, bool W8>
+constexpr int slot_bytes() {
+    return W8 ? W8_RAW_BYTES : StageCfg<MODE>::kBytes;
+}
+
+// offset of the B tile inside a ring stage
+template <int MODE, bool W8>
+constexpr int slot_b_off() {
+    return W8 ? A_BYTES : StageCfg<MODE>::kBOff;
 }
 
 template <int MODE, bool W8>
 constexpr size_t smem_bytes() {
-    return 1024 /*align slack*/ + (size_t)ring_stages<MODE, W8>() * StageCfg<MODE>::kBytes +
-           (W8 ? (size_t)F8_STAGES * F8_BYTES : 0) + sizeof(SmemTail);
+    return 1024 /*align slack*/ + (size_t)ring_stages<MODE, W8>() * slot_bytes<MODE, W8>() +
+           (W8 ? (size_t)W8_WIDE * B_BYTES : 0) + sizeof(SmemTail);
 }
 
 // ---------------------------------------------------------------- PTX helpers
@@ -261,15 +273,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Two E4M3 codes (low byte first) -> two bf16 (low half first).  Every E4M3
-// value is a normal fp16 and has at most 4 significant bits, so the hardware
-// E4M3 -> fp16 conversion and the fp16 -> fp32 -> bf16 steps are all exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
-    uint32_t h2;
-    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(two));
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-    return *reinterpret_cast<const uint32_t*>(&b);
+// Two E4M3 codes, placed in bytes 1 and 3 of `sp`, -> two bf16 (low half
+// first), exactly, with integer and bf16 ALU operations only (no conversion
+// unit).  The 7 magnitude bits of a code, moved to bits 4..10 of a 16-bit
+// lane, read as a bf16 whose value is the code's value times 2^-120 -- for
+// normal codes (exponent field offset by 127 - 7) and for subnormal ones
+// (m/8 * 2^-6 becomes the bf16 subnormal m/8 * 2^-126) alike; one bf16
+// multiply by +-2^120 (the sign taken from the code) then gives the exact
+// value, a normal bf16 with at most 4 significant bits.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t sp) {
+    const uint32_t mag = (sp >> 4) & 0x07F007F0u;
+    const uint32_t mul = (sp & 0x80008000u) | 0x7B807B80u;  // bf16 +-2^120 per lane
+    const __nv_bfloat162 r =
+        __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&mag), *reinterpret_cast<const __nv_bfloat162*>(&mul));
+    return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // One raw FP8 B tile (256 rows x 64 bytes, row-major, as the TMA unit wrote
@@ -277,16 +294,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
 // r * 128 bytes, its 16-byte chunk c at chunk c ^ (r % 8)).  128 threads,
 // 16 chunks of 8 elements each; reads and writes are bank-conflict free.
 __device__ __forceinline__ void widen_b_tile(const uint8_t* src, uint8_t* dst, int ctid) {
-#pragma unroll 4
+#pragma unroll 8
     for (int q = 0; q < 16; ++q) {
         const int idx = ctid + q * 128;
         const int r = idx >> 3, c = idx & 7;
         const uint2 raw = *reinterpret_cast<const uint2*>(src + r * BK + c * 8);
         uint4 out;
-        out.x = e4m3x2_to_bf16x2(raw.x & 0xFFFFu);
-        out.y = e4m3x2_to_bf16x2(raw.x >> 16);
-        out.z = e4m3x2_to_bf16x2(raw.y & 0xFFFFu);
-        out.w = e4m3x2_to_bf16x2(raw.y >> 16);
+        out.x = e4m3x2_to_bf16x2(__byte_perm(raw.x, 0u, 0x1404));  // codes 0, 1
+        out.y = e4m3x2_to_bf16x2(__byte_perm(raw.x, 0u, 0x3424));  // codes 2, 3
+        out.z = e4m3x2_to_bf16x2(__byte_perm(raw.y, 0u, 0x1404));
+        out.w = e4m3x2_to_bf16x2(__byte_perm(raw.y, 0u, 0x3424));
         *reinterpret_cast<uint4*>(dst + r * (BK * 2) + ((c ^ (r & 7)) << 4)) = out;
     }
 }
@@ -501,23 +518,24 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using SC = StageCfg<MODE>;
     constexpr int NST = ring_stages<MODE, W8>();
+    constexpr int SLOT = slot_bytes<MODE, W8>();
+    constexpr int BOFF = slot_b_off<MODE, W8>();
     static_assert(!W8 || MODE == kGemmSwiGLU || MODE == kGemmScale, "FP8 weights: SwiGLU and Scale modes only");
-    uint8_t* f8ring = smem + (size_t)NST * SC::kBytes;  // FP8 variant: raw B tiles
-    SmemTail& st = *reinterpret_cast<SmemTail*>(f8ring + (W8 ? (size_t)F8_STAGES * F8_BYTES : 0));
+    uint8_t* wide = smem + (size_t)NST * SLOT;  // FP8 variant: widened bf16 B tiles
+    SmemTail& st = *reinterpret_cast<SmemTail*>(wide + (W8 ? (size_t)W8_WIDE * B_BYTES : 0));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &st.abort_flag;
 
     // ---- prologue: barriers, TMEM, tile prefix ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
-            // FP8 variant: the A copy's expect_tx plus one arrival per converter warp
-            mbar_init(&st.full[s], W8 ? 5 : 1);
+            mbar_init(&st.full[s], 1);
             mbar_init(&st.empty[s], 1);
         }
         if (W8)
-            for (int j = 0; j < F8_STAGES; ++j) {
-                mbar_init(&st.f8full[j], 1);
-                mbar_init(&st.f8empty[j], 4);
+            for (int w = 0; w < W8_WIDE; ++w) {
+                mbar_init(&st.wfull[w], 4);  // one arrival per converter warp
+                mbar_init(&st.wempty[w], 1);
             }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&st.tmem_full[a], 1);
@@ -586,50 +604,12 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
     const uint32_t tmem_base = st.tmem_base;
     const int total_tiles = st.total[0] + st.total[1];
 
-    if (W8 && warp == 0) {
-        // ---------------- TMA producer, FP8 weights ----------------
-        // Only the raw B tiles: F8_STAGES of them in flight, each freed by the
-        // converter warps once widened (A is loaded by the converters).
-        int j = 0;
-        uint32_t ph8 = 0;
-        uint32_t issued_parity[F8_STAGES];
-        bool used[F8_STAGES];
-        for (int i = 0; i < F8_STAGES; ++i) used[i] = false;
-        bool dead = p.stall_producer != 0;
-        for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
-            const Tile t = decode_tile<MODE>(st, p, id);
-            const int b_row0 = t.g * p.N[t.prob] + t.n * out_cols_per_tile<MODE>();
-            for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                if (!mbar_wait(&st.f8empty[j], ph8 ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
-                    dead = true;
-                    break;
-                }
-                if (lane == 0) {
-                    uint8_t* dst = f8ring + (size_t)j * F8_BYTES;
-                    mbar_expect_tx(&st.f8full[j], F8_BYTES);
-                    tma_load_2d(dst, &p.tmB1[t.prob], kb * BK, b_row0, &st.f8full[j]);
-                    if (MODE == kGemmSwiGLU)
-                        tma_load_2d(dst + F8_BYTES / 2, &p.tmB2[t.prob], kb * BK, b_row0, &st.f8full[j]);
-                }
-                issued_parity[j] = ph8;
-                used[j] = true;
-                if (++j == F8_STAGES) {
-                    j = 0;
-                    ph8 ^= 1u;
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) {
-            volatile int no_abort = 0;
-            for (int i = 0; i < F8_STAGES; ++i)
-                if (used[i]) mbar_wait(&st.f8full[i], issued_parity[i], &no_abort, nullptr, kDrainLimitNs);
-        }
-    } else if (warp == 0) {
+    if (warp == 0) {
         // ---------------- TMA producer ----------------
         // Lane 0 arms each stage's barrier and loads B (and A when A is a plain
         // tile); when A rows are gathered, every lane loads 4 of the tile's
-        // 128 rows with one gather4 per k-block.
+        // 128 rows with one gather4 per k-block.  FP8 weights: B is the raw
+        // one-byte tile, widened later by the converter warps.
         int s = 0;
         uint32_t ph = 0;
         uint32_t issued_parity[NST];
@@ -658,18 +638,18 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                     dead = true;
                     break;
                 }
-                uint8_t* sa = smem + (size_t)s * SC::kBytes;
-                uint8_t* sb = sa + SC::kBOff;
+                uint8_t* sa = smem + (size_t)s * SLOT;
+                uint8_t* sb = sa + BOFF;
                 if (lane == 0) {
                     // gathered A: only the groups of 4 rows that hold valid rows are
                     // loaded; the other rows of the tile are never stored
                     const uint32_t a_bytes = gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : A_BYTES;
-                    mbar_expect_tx(&st.full[s], SC::kBytes - A_BYTES + a_bytes);
+                    mbar_expect_tx(&st.full[s], SLOT - A_BYTES + a_bytes);
                     if (!gidx) tma_load_2d(sa, &p.tmA[t.prob], kb * BK, t.a_row0, &st.full[s]);
                     if (SC::kSplit) tma_load_2d(sa + A_BYTES, &p.tmA2[t.prob], kb * BK, t.a_row0, &st.full[s]);
                     if (MODE == kGemmSwiGLU) {
                         tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
-                        tma_load_2d(sb + B_BYTES / 2, &p.tmB2[t.prob], kb * BK, b_row0, &st.full[s]);
+                        tma_load_2d(sb + (W8 ? F8_BYTES : B_BYTES) / 2, &p.tmB2[t.prob], kb * BK, b_row0, &st.full[s]);
                     } else {
                         tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
                     }
@@ -696,8 +676,8 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-            int s = 0;
-            uint32_t ph = 0;
+            int s = 0, w = 0;
+            uint32_t ph = 0, pw = 0;
             int it = 0;
             bool dead = false;
             for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x, ++it) {
@@ -712,9 +692,14 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                         dead = true;
                         break;
                     }
+                    // FP8 weights: B comes from the widened tile, not the raw stage
+                    if (W8 && !mbar_wait(&st.wfull[w], pw, abort_flag, p.status, p.wait_limit_ns)) {
+                        dead = true;
+                        break;
+                    }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)s * SC::kBytes);
-                    const uint32_t sb = sa + SC::kBOff;
+                    const uint32_t sa = smem_u32(smem + (size_t)s * SLOT);
+                    const uint32_t sb = W8 ? smem_u32(wide + (size_t)w * B_BYTES) : sa + BOFF;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint64_t bdesc = sdesc_k_sw128(sb + kk * UMMA_K * 2);
@@ -723,6 +708,13 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                         if (SC::kSplit) umma_bf16(dtm, sdesc_k_sw128(sa + A_BYTES + kk * UMMA_K * 2), bdesc, idesc, 1u);
                     }
                     umma_commit(&st.empty[s]);
+                    if (W8) {
+                        umma_commit(&st.wempty[w]);
+                        if (++w == W8_WIDE) {
+                            w = 0;
+                            pw ^= 1u;
+                        }
+                    }
                     if (++s == NST) {
                         s = 0;
                         ph ^= 1u;
@@ -751,85 +743,36 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
         }
     } else if constexpr (W8) {
         // ---------------- converters (warps 6..9), FP8 weights ----------------
-        // Per k-block: wait for a free bf16 stage; warp 6 starts the A copy
-        // into it (plain tile or gather4, as the bf16 producer does); then all
-        // four warps widen their quarter of the raw B tile into the stage,
-        // make the writes visible to the tensor cores' async proxy, and
-        // arrive -- on the raw slot (free again) and on the stage (one of the
-        // five arrivals the MMA waits for).
-        const int cw = warp - 6;
+        // Per k-block: wait for the raw stage (A + one-byte B) to land and for
+        // a free widened tile; each warp widens a quarter of the B tile, makes
+        // its writes visible to the tensor cores' async proxy and arrives.
+        // The raw stage itself is released by the MMA (it also reads A there).
         const int ctid = threadIdx.x - NUM_THREADS;  // 0..127
-        int s = 0, j = 0;
-        uint32_t ph = 0, ph8 = 0;
-        uint32_t issued_parity[NST];
-        bool used[NST];
-        for (int i = 0; i < NST; ++i) used[i] = false;
+        int s = 0, w = 0;
+        uint32_t ph = 0, pw = 0;
         bool dead = false;
         for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
             const Tile t = decode_tile<MODE>(st, p, id);
-            const int32_t* gidx = p.a_gather[t.prob];
-            int rows4[4] = {0, 0, 0, 0};
-            if (gidx && cw == 0) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = lane * 4 + i;
-                    int v = r < t.rows_valid ? __ldg(gidx + t.a_row0 + r) : 0;
-                    if (v < 0 || v >= p.a_src_rows[t.prob]) {
-                        if (r < t.rows_valid) record_status(p.status, kStatusBounds);
-                        v = 0;
-                    }
-                    rows4[i] = v;
-                }
-            }
             for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                const bool ok_stage = mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns);
-                if (!__all_sync(0xffffffffu, ok_stage)) {
-                    dead = true;
-                    break;
-                }
-                uint8_t* sa = smem + (size_t)s * SC::kBytes;
-                uint8_t* sb = sa + SC::kBOff;
-                if (cw == 0) {
-                    if (lane == 0) {
-                        const uint32_t a_bytes =
-                            gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : (uint32_t)A_BYTES;
-                        mbar_expect_tx(&st.full[s], a_bytes);
-                        if (!gidx) tma_load_2d(sa, &p.tmA[t.prob], kb * BK, t.a_row0, &st.full[s]);
-                    }
-                    if (gidx && lane * 4 < t.rows_valid)
-                        tma_gather4(sa + lane * 4 * (BK * 2), &p.tmA[t.prob], kb * BK, rows4[0], rows4[1], rows4[2],
-                                    rows4[3], &st.full[s]);
-                    issued_parity[s] = ph;
-                    used[s] = true;
-                }
-                const bool ok_raw = mbar_wait(&st.f8full[j], ph8, abort_flag, p.status, p.wait_limit_ns);
+                const bool ok_w = mbar_wait(&st.wempty[w], pw ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                const bool ok_raw = ok_w && mbar_wait(&st.full[s], ph, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, ok_raw)) {
                     dead = true;
                     break;
                 }
-                widen_b_tile(f8ring + (size_t)j * F8_BYTES, sb, ctid);
+                widen_b_tile(smem + (size_t)s * SLOT + BOFF, wide + (size_t)w * B_BYTES, ctid);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&st.f8empty[j]);
-                    mbar_arrive(&st.full[s]);
+                if (lane == 0) mbar_arrive(&st.wfull[w]);
+                if (++w == W8_WIDE) {
+                    w = 0;
+                    pw ^= 1u;
                 }
                 if (++s == NST) {
                     s = 0;
                     ph ^= 1u;
                 }
-                if (++j == F8_STAGES) {
-                    j = 0;
-                    ph8 ^= 1u;
-                }
             }
-        }
-        // warp 6: no A copy may still be landing when the CTA exits
-        __syncwarp();
-        if (cw == 0 && lane == 0) {
-            volatile int no_abort = 0;
-            for (int i = 0; i < NST; ++i)
-                if (used[i]) mbar_wait(&st.full[i], issued_parity[i], &no_abort, nullptr, kDrainLimitNs);
         }
     }
 

@@ -318,14 +318,15 @@ def _oracle_y_fp8(Ln, q8, w, ids, gates, slot_pos, toks):
     return y
 
 
-def check_layer_fp8(w: moe_inputs.Workload, n_sample: int | None = None) -> dict:
+def check_layer_fp8(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | None = None) -> dict:
     """FP8-weight layer: codes and scales bit-exact with the oracle's
     quantisation of the same bf16 weights; routing as the bf16 layer (the
     router is unchanged); y (fp32 result) within the bf16 tolerance of the
     oracle evaluated with the exactly dequantised weights on the GPU's ids;
     bf16 y = RNE(fp32 y); deterministic."""
     layer = layer_of(w)
-    L = moe_inputs.make_layer(w, "cuda")
+    if L is None:
+        L = moe_inputs.make_layer(w, "cuda")
     names = ["w1", "w3", "w2"] + (["ws1", "ws3", "ws2"] if w.n_shared else [])
     q8 = moe.quantize_experts_fp8(layer, *(L[n] for n in names))
     rep = dict(workload=w.name)
@@ -343,15 +344,25 @@ def check_layer_fp8(w: moe_inputs.Workload, n_sample: int | None = None) -> dict
     rep["quantisation_mismatches"] = mism
     q8n = {k_: v.cpu().numpy() for k_, v in q8.items()}
     del Ln["w1"], Ln["w3"], Ln["w2"]
-    # routing ids from the GPU router (the same kernels the fused call runs)
-    ids, gates, _ = moe.route(layer, L["x"], L["w_gate"], L["logit_bias"], L["select_bias"])
-    gids = ids.cpu().numpy()
-    r = oracle.route(Ln["x"], Ln["w_gate"], w.k, Ln["logit_bias"], Ln["select_bias"], w.renormalize)
-    outside = r["margin"] > MARGIN
-    same_set = np.array([set(a) == set(b) for a, b in zip(gids.tolist(), r["ids"].tolist())])
-    rep["ids_mismatch_outside_margin"] = int((~same_set & outside).sum())
-    og = oracle.group(gids, w.E, w.capacity)
-    ogates = oracle.gates_for_ids(r["probs"], gids, w.renormalize)
+    # routing from the GPU router (the same kernels the fused call runs)
+    if w.routing == "expert":
+        rt = moe.route_expert_choice(layer, L["x"], L["w_gate"], L["logit_bias"], gather=False)
+        gsel = rt["sorted_token_ids"].cpu().numpy().reshape(w.E, layer.bucket)
+        r = oracle.route(Ln["x"], Ln["w_gate"], 1, Ln["logit_bias"], None, True)
+        own, margin = oracle.ec_select(r["probs"], layer.bucket)
+        same = np.array([np.array_equal(gsel[e], own[e]) for e in range(w.E)])
+        rep["ids_mismatch_outside_margin"] = int((~same & (margin > EC_MARGIN)).sum())
+        sl = oracle.ec_slots(gsel, r["probs"])
+        gids, ogates, og = sl["ids"], sl["gates"], dict(slot_pos=sl["slot_pos"])
+    else:
+        ids, gates, _ = moe.route(layer, L["x"], L["w_gate"], L["logit_bias"], L["select_bias"])
+        gids = ids.cpu().numpy()
+        r = oracle.route(Ln["x"], Ln["w_gate"], w.k, Ln["logit_bias"], Ln["select_bias"], w.renormalize)
+        outside = r["margin"] > MARGIN
+        same_set = np.array([set(a) == set(b) for a, b in zip(gids.tolist(), r["ids"].tolist())])
+        rep["ids_mismatch_outside_margin"] = int((~same_set & outside).sum())
+        og = oracle.group(gids, w.E, w.capacity)
+        ogates = oracle.gates_for_ids(r["probs"], gids, w.renormalize)
     fw = moe.Forward(layer, L["w_gate"], None, None, None, L["logit_bias"], L["select_bias"], fp8=q8)
     y1 = fw(L["x"])
     y2 = fw(L["x"])

@@ -63,6 +63,24 @@ def test_fp8_layer_matches_oracle(cuda, w):
     _assert_ok(check_layer_fp8(w))
 
 
+def test_fp8_subnormal_codes_are_widened_exactly(cuda):
+    """Rows whose maximum sits in a column where x is 0: the up GEMM then sees
+    only the row's small weights, which quantise to subnormal E4M3 codes
+    (|w / scale| < 2^-6), so y depends on widening those codes exactly."""
+    import moe_inputs
+    from tests._parity import check_layer_fp8
+    w = Workload("fp8_subnormal_codes", T=200, d=256, E=4, F=256, k=2, weights="fp8")
+    L = moe_inputs.make_layer(w, "cuda")
+    L["x"][:, 0] = 0
+    for n in ("w1", "w3"):
+        L[n][:, :, 1:] *= 1e-4
+        L[n][:, :, 0] = 1.0  # scale = 1/448: the rest maps below 2^-6
+    q1 = __import__("mixture_experts_layer_95_b300").quantize_fp8(L["w1"])[0]
+    exp_zero = ((q1[:, :, 1:] & 0x78) == 0).float().mean().item()
+    assert exp_zero > 0.9  # almost every code the GEMM uses is subnormal (or zero)
+    _assert_ok(check_layer_fp8(w, L=L))
+
+
 @pytest.mark.parametrize("name", ["mixtral_decode_t1_fp8", "mixtral_decode_t8_fp8"])
 def test_fp8_mixtral_decode(cuda, name):
     from tests._parity import check_layer_fp8
