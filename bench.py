@@ -366,10 +366,12 @@ def run_ours(args):
     plan = moe.plan_describe(layer_of(w).cfg())
     up_kernel = {"tc_pair": "grouped_gemm_tc_pair_kernel<SwiGLU> (up GEMM, CTA pairs)",
                  "tc": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)",
+                 "tc_decode32": "grouped_gemm_decode_kernel<SwiGLU, NT=32> (up GEMM, weights on M)",
+                 "tc_decode64": "grouped_gemm_decode_kernel<SwiGLU, NT=64> (up GEMM, weights on M)",
                  "simt": "grouped_gemm_simt_kernel<SwiGLU> (up GEMM)"}[plan["up"]]
     if q8 is not None:
-        up_kernel = "grouped_gemm_tc_kernel<SwiGLU, FP8 weights> (up GEMM)"
-        plan = dict(plan, up="tc_fp8", down="tc_fp8")
+        up_kernel = up_kernel.replace("<SwiGLU", "<SwiGLU, FP8 weights")
+        plan = dict(plan, weights="fp8_e4m3")
     if tensor_bound:
         achieved = up_flops / (up_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",

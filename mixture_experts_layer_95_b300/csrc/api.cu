@@ -61,6 +61,17 @@ bool use_gather_a(const moe_config& c) {
     return c.dtype == MOE_BF16 && n <= 32 * touched;
 }
 
+// Decode-sized bf16 batches with a single bf16 H: both expert GEMMs put the
+// weights on the MMA's M side (gemm_decode.cu), with 32 token rows per tile
+// when the touched experts average at most 16 rows, else 64.
+bool use_decode_gemm(const moe_config& c) { return c.dtype == MOE_BF16 && !use_h_split(c) && use_gather_a(c); }
+
+int decode_tile_rows(const moe_config& c) {
+    const long long n = perm_rows(c);
+    const long long touched = n < c.E ? n : c.E;
+    return n <= 16 * touched ? 32 : 64;
+}
+
 // ---- split-K for decode-sized batches ----------------------------------------
 // When a grouped GEMM has too few output tiles to keep every SM streaming
 // weights, each tile's K range is split into S slices (fp32 partials, summed
@@ -416,7 +427,15 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     int* status = at<int>(ws, L.status);
     {
         StageScope scope(kStageUp, s);
-        if (w8) {
+        if (use_decode_gemm(c)) {
+            MOE_LAUNCH(launch_gemm_decode(kGemmSwiGLU, up, np, status, sms, s, sp.up, w8 != nullptr,
+                                          decode_tile_rows(c)));
+            if (sp.up > 1) {
+                MOE_LAUNCH(launch_swiglu_finalize(n, offsets + c.E, c.d_ff, sp.up, up[0].part, h, nullptr, s));
+                if (c.n_shared)
+                    MOE_LAUNCH(launch_swiglu_finalize(c.T, nullptr, c.d_ff_shared, sp.up, up[1].part, hs, nullptr, s));
+            }
+        } else if (w8) {
             MOE_LAUNCH(launch_gemm_tc_w8(kGemmSwiGLU, up, np, status, sms, s, sp.up));
             if (sp.up > 1) {
                 MOE_LAUNCH(launch_swiglu_finalize(n, offsets + c.E, c.d_ff, sp.up, up[0].part, h, nullptr, s));
@@ -437,7 +456,15 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     }
     {
         StageScope scope(kStageDown, s);
-        if (w8) {
+        if (use_decode_gemm(c)) {
+            MOE_LAUNCH(launch_gemm_decode(kGemmScale, down, np, status, sms, s, sp.down, w8 != nullptr,
+                                          decode_tile_rows(c)));
+            if (sp.down > 1 && reduce_down) {
+                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
+                if (c.n_shared)
+                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s));
+            }
+        } else if (w8) {
             MOE_LAUNCH(launch_gemm_tc_w8(kGemmScale, down, np, status, sms, s, sp.down));
             if (sp.down > 1 && reduce_down) {
                 MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
@@ -845,7 +872,7 @@ int moe_plan_describe(const moe_config* cfg, char* buf, size_t len) {
     const char* router = use_split_d_router(c.T, c.E) ? "split_d"
                          : use_warp_router(c.E, c.d, c.dtype) ? "warp"
                                                               : "gemm";
-    const char* gemm = c.dtype != MOE_BF16 ? "simt" : "tc";
+    const char* gemm = c.dtype != MOE_BF16 ? "simt" : (use_decode_gemm(c) ? (decode_tile_rows(c) == 32 ? "tc_decode32" : "tc_decode64") : "tc");
     const Splits sp = choose_splits(c);
     const bool gather = use_gather_a(c);
     const bool pair_up = use_pair_gemm(c) && sp.up == 1 && !gather;

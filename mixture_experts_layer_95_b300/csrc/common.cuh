@@ -262,6 +262,12 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
 cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
                               cudaStream_t s, int ksplit = 1);
 
+// Decode-sized batches: the same grouped GEMM with the weights on the MMA's M
+// side (D^T = W X^T; nt = 32 or 64 token rows per tile), bf16 or FP8 (w8)
+// weights, SwiGLU and Scale modes, split-K and gathered token rows; no split H.
+cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
+                               cudaStream_t s, int ksplit, bool w8, int nt);
+
 // Per-row E4M3 quantisation of a [rows][cols] bf16 or fp32 matrix (cols a
 // multiple of 16): q [rows][cols] codes, scale [rows] fp32.
 cudaError_t launch_quantize_fp8(int dtype, long long rows, int cols, const void* w, uint8_t* q, float* scale,

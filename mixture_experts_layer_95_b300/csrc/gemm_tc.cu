@@ -39,14 +39,14 @@
 #include <stdlib.h>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+using namespace tc;
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;  // one 128-byte swizzle row of bf16
-constexpr int UMMA_K = 16;
 constexpr int STAGES = 4;  // ring depth; 3 for the split-A down GEMM (64 KB stages)
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
@@ -69,8 +69,6 @@ constexpr int W8_RAW_BYTES = A_BYTES + F8_BYTES;
 constexpr int W8_WIDE = 2;          // widened bf16 B tiles feeding the MMA
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = kMaxExperts;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
-constexpr uint64_t kDrainLimitNs = 10000000ull;   // 10 ms to drain copies after an abort
 
 struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     CUtensorMap tmA[2];
@@ -138,194 +136,6 @@ template <int MODE, bool W8>
 constexpr size_t smem_bytes() {
     return 1024 /*align slack*/ + (size_t)ring_stages<MODE, W8>() * slot_bytes<MODE, W8>() +
            (W8 ? (size_t)W8_WIDE * B_BYTES : 0) + sizeof(SmemTail);
-}
-
-// ---------------------------------------------------------------- PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for phase `parity` of `bar`.  Returns false when the CTA is
-// aborting (another role gave up) or this wait ran out of time.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                          uint64_t limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > limit_ns) {
-            *abort_flag = 1;
-            record_status(status, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int c0, int c1, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Four rows (r0..r3) x 64 columns starting at column c0 of a 2-D tensor whose
-// map has a one-row box; lands in shared memory as four consecutive 128-byte
-// rows, swizzled like a tiled load to the same address.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, int c0, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-        "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row core groups 1024 bytes apart (SBO); LBO is unused for a
-// swizzled K-major operand whose K extent per instruction (32 bytes) stays
-// inside one swizzle row.  Bits 46-47 hold the descriptor version (1).
-__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(16u >> 4) << 16;
-    d |= static_cast<uint64_t>(1024u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
-    d |= static_cast<uint64_t>(2u) << 61;  // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, dense, M x N.
-constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4)                                  // D format: f32
-           | (1u << 7)                                // A format: bf16
-           | (1u << 10)                               // B format: bf16
-           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
-           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Two E4M3 codes, placed in bytes 1 and 3 of `sp`, -> two bf16 (low half
-// first), exactly, with integer and bf16 ALU operations only (no conversion
-// unit).  The 7 magnitude bits of a code, moved to bits 4..10 of a 16-bit
-// lane, read as a bf16 whose value is the code's value times 2^-120 -- for
-// normal codes (exponent field offset by 127 - 7) and for subnormal ones
-// (m/8 * 2^-6 becomes the bf16 subnormal m/8 * 2^-126) alike; one bf16
-// multiply by +-2^120 (the sign taken from the code) then gives the exact
-// value, a normal bf16 with at most 4 significant bits.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t sp) {
-    const uint32_t mag = (sp >> 4) & 0x07F007F0u;
-    const uint32_t mul = (sp & 0x80008000u) | 0x7B807B80u;  // bf16 +-2^120 per lane
-    const __nv_bfloat162 r =
-        __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&mag), *reinterpret_cast<const __nv_bfloat162*>(&mul));
-    return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// One raw FP8 B tile (256 rows x 64 bytes, row-major, as the TMA unit wrote
-// it) -> the bf16 K-major 128-byte-swizzled tile the MMA reads (row r at
-// r * 128 bytes, its 16-byte chunk c at chunk c ^ (r % 8)).  128 threads,
-// 16 chunks of 8 elements each; reads and writes are bank-conflict free.
-__device__ __forceinline__ void widen_b_tile(const uint8_t* src, uint8_t* dst, int ctid) {
-#pragma unroll 8
-    for (int q = 0; q < 16; ++q) {
-        const int idx = ctid + q * 128;
-        const int r = idx >> 3, c = idx & 7;
-        const uint2 raw = *reinterpret_cast<const uint2*>(src + r * BK + c * 8);
-        uint4 out;
-        out.x = e4m3x2_to_bf16x2(__byte_perm(raw.x, 0u, 0x1404));  // codes 0, 1
-        out.y = e4m3x2_to_bf16x2(__byte_perm(raw.x, 0u, 0x3424));  // codes 2, 3
-        out.z = e4m3x2_to_bf16x2(__byte_perm(raw.y, 0u, 0x1404));
-        out.w = e4m3x2_to_bf16x2(__byte_perm(raw.y, 0u, 0x3424));
-        *reinterpret_cast<uint4*>(dst + r * (BK * 2) + ((c ^ (r & 7)) << 4)) = out;
-    }
-}
-
-// v[i] *= scale of weight row wrow + i (FP8 weights), for the 32 columns of
-// one tcgen05.ld; rem = columns that exist from wrow on (>= 32: all).
-__device__ __forceinline__ void apply_wscale32(uint32_t (&v)[32], const float* ws, size_t wrow, int rem) {
-    if (rem >= 32) {
-        const float4* p4 = reinterpret_cast<const float4*>(ws + wrow);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 sc = __ldg(p4 + q);
-            v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) * sc.x);
-            v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) * sc.y);
-            v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) * sc.z);
-            v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) * sc.w);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            v[i] = __float_as_uint(i < rem ? __uint_as_float(v[i]) * __ldg(ws + wrow + i) : 0.f);
-    }
 }
 
 // ------------------------------------------------------------- tile schedule
@@ -1088,50 +898,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ----------------------------------------------------------------- host side
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// 2-D bf16 tensor [rows][K] (K contiguous), box = 64 x box_rows, 128-byte swizzle.
-bool make_tmap(CUtensorMap* tm, const void* base, int rows, int K, int box_rows) {
-    EncodeTiledFn enc = get_encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 2-D one-byte (FP8 code) tensor [rows][K], box = 64 x box_rows, no swizzle:
-// the converter warps re-lay the tile out for the MMA themselves.
-bool make_tmap_u8(CUtensorMap* tm, const void* base, int rows, int K, int box_rows) {
-    EncodeTiledFn enc = get_encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <int MODE, bool W8 = false>
 cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
