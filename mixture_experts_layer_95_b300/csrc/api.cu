@@ -114,7 +114,7 @@ long long est_row_tiles(const moe_config& c) {
     return by_rows > touched ? by_rows : touched;
 }
 
-Splits choose_splits(const moe_config& c) {
+Splits choose_splits_bf16(const moe_config& c) {
     Splits sp;
     if (c.dtype != MOE_BF16 || c.T == 0) return sp;
     const long long rt = est_row_tiles(c);
@@ -133,6 +133,24 @@ Splits choose_splits(const moe_config& c) {
     const long long p_dn = 8LL * (n + (long long)c.n_shared * c.T) * c.d;
     sp.up = choose_ksplit(up, nk_up, w_up / (10 * p_up));
     sp.down = choose_ksplit(dn, nk_dn, w_dn / (10 * p_dn));
+    return sp;
+}
+
+// With FP8 weights the decode GEMM's stages hold two k-blocks, so a K slice
+// needs at least two; the workspace (sized for bf16) holds either choice.
+bool use_decode_gemm(const moe_config& c);
+
+Splits choose_splits(const moe_config& c, bool w8 = false) {
+    Splits sp = choose_splits_bf16(c);
+    if (w8 && use_decode_gemm(c)) {
+        const int up_max = ceil_div(c.d, 128), dn_max = ceil_div(c.d_ff, 128);
+        const int dn_max_s = c.n_shared ? ceil_div(c.d_ff_shared, 128) : dn_max;
+        sp.up = sp.up < up_max ? sp.up : up_max;
+        sp.down = sp.down < dn_max ? sp.down : dn_max;
+        sp.down = sp.down < dn_max_s ? sp.down : dn_max_s;
+        if (sp.up < 1) sp.up = 1;
+        if (sp.down < 1) sp.down = 1;
+    }
     return sp;
 }
 
@@ -346,7 +364,7 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
                 const float* gates_perm, const void* w1, const void* w3, const void* w2, const void* x,
                 const void* ws1, const void* ws3, const void* ws2, float* y_perm, float* y_shared, int sms,
                 cudaStream_t s, bool reduce_down, const int32_t* gather_idx, const moe_fp8_weights* w8 = nullptr) {
-    const Splits sp = choose_splits(c);
+    const Splits sp = choose_splits(c, w8 != nullptr);
     const int n = (int)perm_rows(c);
     void* h = at<void>(ws, L.h);
     void* hs = at<void>(ws, L.h_shared);
@@ -509,7 +527,7 @@ int forward_tail(const moe_config& c, const Layout& L, void* ws, const void* x, 
     MOE_TRY(enqueue_ffn(c, L, ws, x_perm, offsets, gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared, sms,
                         s, false, gather_idx, w8));
     // combine (straight from the down GEMM's split-K slices when it was split)
-    const Splits sp = choose_splits(c);
+    const Splits sp = choose_splits(c, w8 != nullptr);
     const float* yp = y_perm;
     const float* ys = y_shared;
     size_t yp_stride = 0, ys_stride = 0;

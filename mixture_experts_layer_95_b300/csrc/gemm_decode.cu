@@ -33,8 +33,14 @@ namespace {
 using namespace tc;
 
 constexpr int WR = 256;                  // weight rows per tile (SwiGLU: 128 of W1 + 128 of W3)
-constexpr int WB16 = WR * BK * 2;        // bf16 weight tile bytes
-constexpr int WB8 = WR * BK;             // FP8 weight tile bytes
+constexpr int WB16 = WR * BK * 2;        // bf16 weight tile bytes (one k-block of 64)
+// A stage carries KPS k-blocks: 1 for bf16 weights; 2 for FP8, so that every
+// weight row of a stage is 128 contiguous bytes, as for bf16 (a 64-byte row
+// per TMA request halves the bytes each request brings in).
+template <bool W8>
+constexpr int kps() {
+    return W8 ? 2 : 1;
+}
 constexpr int DEC_THREADS = 192;         // producer, MMA, 4 epilogue warps
 constexpr int DEC_W8_THREADS = 192 + 256;  // + 8 widening warps
 constexpr int DEC_WIDE = 2;              // widened bf16 weight tiles (FP8)
@@ -81,7 +87,7 @@ constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 
 template <bool W8, int NT>
 constexpr int dec_slot_bytes() {
-    return (W8 ? WB8 : WB16) + NT * BK * 2;
+    return WR * 128 + kps<W8>() * NT * BK * 2;  // 256 weight rows x 128 bytes, then KPS token tiles
 }
 
 template <bool W8, int NT>
@@ -99,7 +105,7 @@ constexpr size_t dec_smem_bytes() {
 }
 
 static_assert(dec_stages<false, 32>() >= 4 && dec_stages<false, 64>() >= 4, "bf16 decode ring too shallow");
-static_assert(dec_stages<true, 32>() >= 4 && dec_stages<true, 64>() >= 4, "FP8 decode ring too shallow");
+static_assert(dec_stages<true, 32>() >= 3 && dec_stages<true, 64>() >= 3, "FP8 decode ring too shallow");
 static_assert(dec_smem_bytes<true, 32>() <= kSmemLimit && dec_smem_bytes<false, 64>() <= kSmemLimit &&
                   dec_smem_bytes<true, 64>() <= kSmemLimit && dec_smem_bytes<false, 32>() <= kSmemLimit,
               "decode GEMM exceeds shared memory");
@@ -107,7 +113,7 @@ static_assert(dec_smem_bytes<true, 32>() <= kSmemLimit && dec_smem_bytes<false, 
 struct DTile {
     int prob, g, m, n;
     int x_row0, rows_valid;
-    int ks, kb0, kb1;
+    int ks, kb0, kb1;  // K slice and its range of stages [kb0, kb1) (KPS k-blocks each)
 };
 
 // output columns one tile covers: 128 (the W1/W3 pair) or 256 (W2)
@@ -116,7 +122,7 @@ __device__ __forceinline__ int dec_cols() {
     return MODE == kGemmSwiGLU ? WR / 2 : WR;
 }
 
-template <int MODE, int NT>
+template <int MODE, int NT, int KPS>
 __device__ __forceinline__ DTile dec_tile(const DecTail& st, const DecParams& p, int id) {
     DTile t;
     t.prob = (id < st.total[0]) ? 0 : 1;
@@ -139,7 +145,7 @@ __device__ __forceinline__ DTile dec_tile(const DecTail& st, const DecParams& p,
     t.m = r - t.n * mt;
     t.x_row0 = st.row0[gb + lo] + t.m * NT;
     t.rows_valid = min(NT, rows - t.m * NT);
-    const int nk = (p.K[t.prob] + BK - 1) / BK;
+    const int nk = (p.K[t.prob] + KPS * BK - 1) / (KPS * BK);
     t.kb0 = t.ks * nk / p.ksplit;
     t.kb1 = (t.ks + 1) * nk / p.ksplit;
     return t;
@@ -147,13 +153,14 @@ __device__ __forceinline__ DTile dec_tile(const DecTail& st, const DecParams& p,
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
-// Widening of one FP8 weight tile (256 rows x 64 codes) by `nthreads` threads
-// (the converter warps); layout as widen_b_tile in tc_ptx.cuh.
+// Widening of one k-block (64 codes) of an FP8 stage whose weight rows are
+// 128 bytes apart, by `nthreads` threads (the converter warps), into a bf16
+// K-major 128-byte-swizzled tile; layout as widen_b_tile in tc_ptx.cuh.
 __device__ __forceinline__ void widen_tile(const uint8_t* src, uint8_t* dst, int tid, int nthreads) {
-#pragma unroll 4
+#pragma unroll
     for (int idx = tid; idx < WR * 8; idx += nthreads) {
         const int r = idx >> 3, c = idx & 7;
-        const uint2 raw = *reinterpret_cast<const uint2*>(src + r * BK + c * 8);
+        const uint2 raw = *reinterpret_cast<const uint2*>(src + r * 128 + c * 8);
         uint4 out;
         out.x = e4m3x2_to_bf16x2(__byte_perm(raw.x, 0u, 0x1404));
         out.y = e4m3x2_to_bf16x2(__byte_perm(raw.x, 0u, 0x3424));
@@ -236,7 +243,9 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int NST = dec_stages<W8, NT>();
     constexpr int SLOT = dec_slot_bytes<W8, NT>();
-    constexpr int WBYTES = W8 ? WB8 : WB16;  // weight bytes at the start of a stage; token rows follow
+    constexpr int KPS = kps<W8>();
+    constexpr int WBYTES = WR * 128;   // weight bytes at the start of a stage; KPS token tiles follow
+    constexpr int XBYTES = NT * BK * 2;  // one token tile
     static_assert(MODE == kGemmSwiGLU || MODE == kGemmScale, "decode GEMM: SwiGLU and Scale modes");
     uint8_t* wide = smem + (size_t)NST * SLOT;  // FP8: widened weight tiles
     DecTail& st = *reinterpret_cast<DecTail*>(wide + (W8 ? (size_t)DEC_WIDE * WB16 : 0));
@@ -325,7 +334,7 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
         for (int i = 0; i < NST; ++i) used[i] = false;
         bool dead = p.stall_producer != 0;
         for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
-            const DTile t = dec_tile<MODE, NT>(st, p, id);
+            const DTile t = dec_tile<MODE, NT, KPS>(st, p, id);
             const int w_row0 = t.g * p.N[t.prob] + t.n * dec_cols<MODE>();
             const int32_t* gidx = p.x_gather[t.prob];
             int rows4[4] = {0, 0, 0, 0};
@@ -350,19 +359,24 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
                 uint8_t* sx = sw + WBYTES;
                 if (lane == 0) {
                     const uint32_t x_bytes =
-                        gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : (uint32_t)(NT * BK * 2);
-                    mbar_expect_tx(&st.full[s], WBYTES + x_bytes);
+                        gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : (uint32_t)XBYTES;
+                    mbar_expect_tx(&st.full[s], WBYTES + KPS * x_bytes);
+                    // weight columns of this stage: KPS * 64 elements (bf16: 64, FP8: 128 bytes)
+                    const int wc = kb * KPS * BK;
                     if (MODE == kGemmSwiGLU) {
-                        tma_load_2d(sw, &p.tmW1[t.prob], kb * BK, w_row0, &st.full[s]);
-                        tma_load_2d(sw + WBYTES / 2, &p.tmW2[t.prob], kb * BK, w_row0, &st.full[s]);
+                        tma_load_2d(sw, &p.tmW1[t.prob], wc, w_row0, &st.full[s]);
+                        tma_load_2d(sw + WBYTES / 2, &p.tmW2[t.prob], wc, w_row0, &st.full[s]);
                     } else {
-                        tma_load_2d(sw, &p.tmW1[t.prob], kb * BK, w_row0, &st.full[s]);
+                        tma_load_2d(sw, &p.tmW1[t.prob], wc, w_row0, &st.full[s]);
                     }
-                    if (!gidx) tma_load_2d(sx, &p.tmX[t.prob], kb * BK, t.x_row0, &st.full[s]);
+                    if (!gidx)
+                        for (int h = 0; h < KPS; ++h)
+                            tma_load_2d(sx + h * XBYTES, &p.tmX[t.prob], (kb * KPS + h) * BK, t.x_row0, &st.full[s]);
                 }
                 if (gidx && lane * 4 < t.rows_valid)
-                    tma_gather4(sx + lane * 4 * (BK * 2), &p.tmX[t.prob], kb * BK, rows4[0], rows4[1], rows4[2],
-                                rows4[3], &st.full[s]);
+                    for (int h = 0; h < KPS; ++h)
+                        tma_gather4(sx + h * XBYTES + lane * 4 * (BK * 2), &p.tmX[t.prob], (kb * KPS + h) * BK,
+                                    rows4[0], rows4[1], rows4[2], rows4[3], &st.full[s]);
                 issued_parity[s] = ph;
                 used[s] = true;
                 if (++s == NST) {
@@ -386,7 +400,7 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
             int it = 0;
             bool dead = false;
             for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x, ++it) {
-                const DTile t = dec_tile<MODE, NT>(st, p, id);
+                const DTile t = dec_tile<MODE, NT, KPS>(st, p, id);
                 const int acc = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
                 if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
@@ -397,28 +411,33 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
                         dead = true;
                         break;
                     }
-                    if (W8 && !mbar_wait(&st.wfull[w], pw, abort_flag, p.status, p.wait_limit_ns)) {
-                        dead = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sw = W8 ? smem_u32(wide + (size_t)w * WB16) : smem_u32(smem + (size_t)s * SLOT);
-                    const uint32_t sx = smem_u32(smem + (size_t)s * SLOT + WBYTES);
+                    for (int h = 0; h < KPS && !dead; ++h) {
+                        if (W8 && !mbar_wait(&st.wfull[w], pw, abort_flag, p.status, p.wait_limit_ns)) {
+                            dead = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sw =
+                            W8 ? smem_u32(wide + (size_t)w * WB16) : smem_u32(smem + (size_t)s * SLOT);
+                        const uint32_t sx = smem_u32(smem + (size_t)s * SLOT + WBYTES + h * XBYTES);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t xdesc = sdesc_k_sw128(sx + kk * UMMA_K * 2);
-                        const uint32_t accf = (kb != t.kb0 || kk != 0) ? 1u : 0u;
-                        umma_bf16(dtm, sdesc_k_sw128(sw + kk * UMMA_K * 2), xdesc, idesc, accf);
-                        umma_bf16(dtm + NT, sdesc_k_sw128(sw + 128 * BK * 2 + kk * UMMA_K * 2), xdesc, idesc, accf);
-                    }
-                    umma_commit(&st.empty[s]);
-                    if (W8) {
-                        umma_commit(&st.wempty[w]);
-                        if (++w == DEC_WIDE) {
-                            w = 0;
-                            pw ^= 1u;
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            const uint64_t xdesc = sdesc_k_sw128(sx + kk * UMMA_K * 2);
+                            const uint32_t accf = (kb != t.kb0 || h != 0 || kk != 0) ? 1u : 0u;
+                            umma_bf16(dtm, sdesc_k_sw128(sw + kk * UMMA_K * 2), xdesc, idesc, accf);
+                            umma_bf16(dtm + NT, sdesc_k_sw128(sw + 128 * BK * 2 + kk * UMMA_K * 2), xdesc, idesc,
+                                      accf);
+                        }
+                        if (W8) {
+                            umma_commit(&st.wempty[w]);
+                            if (++w == DEC_WIDE) {
+                                w = 0;
+                                pw ^= 1u;
+                            }
                         }
                     }
+                    if (dead) break;
+                    umma_commit(&st.empty[s]);
                     if (++s == NST) {
                         s = 0;
                         ph ^= 1u;
@@ -434,7 +453,7 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
         const int wrow = quarter * 32 + lane;
         int it = 0;
         for (int id = blockIdx.x; id < total_tiles; id += gridDim.x, ++it) {
-            const DTile t = dec_tile<MODE, NT>(st, p, id);
+            const DTile t = dec_tile<MODE, NT, KPS>(st, p, id);
             const int acc = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status, p.wait_limit_ns)) break;
@@ -453,22 +472,30 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
         uint32_t ph = 0, pw = 0;
         bool dead = false;
         for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
-            const DTile t = dec_tile<MODE, NT>(st, p, id);
+            const DTile t = dec_tile<MODE, NT, KPS>(st, p, id);
             for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                const bool ok_w = mbar_wait(&st.wempty[w], pw ^ 1u, abort_flag, p.status, p.wait_limit_ns);
-                const bool ok_raw = ok_w && mbar_wait(&st.full[s], ph, abort_flag, p.status, p.wait_limit_ns);
+                const bool ok_raw = mbar_wait(&st.full[s], ph, abort_flag, p.status, p.wait_limit_ns);
                 if (!__all_sync(0xffffffffu, ok_raw)) {
                     dead = true;
                     break;
                 }
-                widen_tile(smem + (size_t)s * SLOT, wide + (size_t)w * WB16, ctid, DEC_W8_THREADS - DEC_THREADS);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&st.wfull[w]);
-                if (++w == DEC_WIDE) {
-                    w = 0;
-                    pw ^= 1u;
+                for (int h = 0; h < KPS; ++h) {
+                    const bool ok_w = mbar_wait(&st.wempty[w], pw ^ 1u, abort_flag, p.status, p.wait_limit_ns);
+                    if (!__all_sync(0xffffffffu, ok_w)) {
+                        dead = true;
+                        break;
+                    }
+                    widen_tile(smem + (size_t)s * SLOT + h * BK, wide + (size_t)w * WB16, ctid,
+                               DEC_W8_THREADS - DEC_THREADS);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&st.wfull[w]);
+                    if (++w == DEC_WIDE) {
+                        w = 0;
+                        pw ^= 1u;
+                    }
                 }
+                if (dead) break;
                 if (++s == NST) {
                     s = 0;
                     ph ^= 1u;
@@ -537,16 +564,18 @@ cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, in
         } else if (!make_tmap(&prm.tmX[q], g.A, g.a_rows, g.K, nt)) {
             return cudaErrorInvalidValue;
         }
-        const bool ok1 = w8 ? make_tmap_u8(&prm.tmW1[q], g.B1, g.G * g.N, g.K, w_box)
+        // FP8 stages hold 128 codes (two k-blocks) of every weight row
+        const bool ok1 = w8 ? make_tmap_u8(&prm.tmW1[q], g.B1, g.G * g.N, g.K, w_box, 2 * BK)
                             : make_tmap(&prm.tmW1[q], g.B1, g.G * g.N, g.K, w_box);
         if (!ok1) return cudaErrorInvalidValue;
         if (mode == kGemmSwiGLU) {
-            const bool ok2 = w8 ? make_tmap_u8(&prm.tmW2[q], g.B2, g.G * g.N, g.K, w_box)
+            const bool ok2 = w8 ? make_tmap_u8(&prm.tmW2[q], g.B2, g.G * g.N, g.K, w_box, 2 * BK)
                                 : make_tmap(&prm.tmW2[q], g.B2, g.G * g.N, g.K, w_box);
             if (!ok2) return cudaErrorInvalidValue;
         }
         if (ksplit > 1) {
-            if (ksplit > (g.K + BK - 1) / BK || g.part == nullptr) return cudaErrorInvalidValue;
+            const int kstep = (w8 ? 2 : 1) * BK;
+            if (ksplit > (g.K + kstep - 1) / kstep || g.part == nullptr) return cudaErrorInvalidValue;
             prm.part[q] = g.part;
             prm.part_cols[q] = mode == kGemmSwiGLU ? 2 * g.N : g.N;
         }

@@ -238,12 +238,12 @@ inline bool make_tmap(CUtensorMap* tm, const void* base, int rows, int K, int bo
 
 // 2-D one-byte (FP8 code) tensor [rows][K], box = 64 x box_rows, no swizzle:
 // the converter warps re-lay the tile out for the MMA themselves.
-inline bool make_tmap_u8(CUtensorMap* tm, const void* base, int rows, int K, int box_rows) {
+inline bool make_tmap_u8(CUtensorMap* tm, const void* base, int rows, int K, int box_rows, int box_cols = BK) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
