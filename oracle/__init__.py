@@ -61,11 +61,12 @@ def _L():
         _lib.oracle_e4m3_decode.argtypes = [ip, vp, vp]
         _lib.oracle_quantize_fp8.argtypes = [ll, ip, ip, vp, vp, vp]
         _lib.oracle_dequant_fp8.argtypes = [ll, ip, vp, vp, vp]
+        _lib.oracle_layer_backward.argtypes = [ip] * 8 + [vp] * 11 + [ip, ctypes.c_double, vp, ctypes.c_double] + [vp] * 9
         _lib.oracle_ec_slots.argtypes = [ip, ip, ip, vp, vp, vp, vp, vp, vp]
         for f in ("oracle_route", "oracle_gates_for_ids", "oracle_group", "oracle_layer_tokens",
                   "oracle_load_stats", "oracle_num_threads", "oracle_bias_update", "oracle_ec_select",
                   "oracle_ec_slots", "oracle_load_stats_n", "oracle_e4m3_encode", "oracle_e4m3_decode",
-                  "oracle_quantize_fp8", "oracle_dequant_fp8"):
+                  "oracle_quantize_fp8", "oracle_dequant_fp8", "oracle_layer_backward"):
             getattr(_lib, f).restype = ctypes.c_int
     return _lib
 
@@ -352,4 +353,38 @@ def dequant_fp8(q, scale):
     rows = q.size // cols
     out = np.empty(q.shape, np.float64)
     _check(_L().oracle_dequant_fp8(rows, cols, _p(q), _p(scale), _p(out)), "dequant_fp8")
+    return out
+
+
+# ---------------------------------------------------------------- backward
+
+def backward(layer, k, ids, slot_pos, dy, renormalize=True, alpha=0.01, dL=0.0):
+    """Gradients of <dy, y> + dL * L_balance with respect to x, W_g, W1, W3, W2
+    (and the shared expert's weights), the routing decisions (ids, dropped
+    slots) held fixed and f held constant.  layer: dict as for forward();
+    ids int32 [T, k]; slot_pos int32 [T, k] or None (< 0 = dropped); dy [T, d]
+    (converted to float64).  Returns a dict of float64 arrays: dx, dw_gate,
+    dw1, dw3, dw2, dlogits (and dws1, dws3, dws2 with a shared expert)."""
+    x = _c(layer["x"])
+    dt = _dtype_of(x)
+    wg, w1, w3, w2 = (_c(layer[n]) for n in ("w_gate", "w1", "w3", "w2"))
+    T, d = x.shape
+    E, F, _ = w1.shape
+    ids = _c(ids, np.int32)
+    assert ids.shape == (T, k)
+    sp = _c(slot_pos, np.int32)
+    dy = _c(dy, np.float64)
+    lb = _c(layer.get("logit_bias"), np.float32)
+    shared = layer.get("ws1") is not None
+    s1, s3, s2 = (_c(layer[n]) for n in ("ws1", "ws3", "ws2")) if shared else (None, None, None)
+    Fs = s1.shape[0] if shared else 0
+    out = dict(dx=np.empty((T, d)), dw_gate=np.empty((E, d)), dw1=np.empty((E, F, d)), dw3=np.empty((E, F, d)),
+               dw2=np.empty((E, d, F)), dlogits=np.empty((T, E)))
+    if shared:
+        out.update(dws1=np.empty((Fs, d)), dws3=np.empty((Fs, d)), dws2=np.empty((d, Fs)))
+    _check(_L().oracle_layer_backward(T, d, E, k, F, int(shared), Fs, dt, _p(x), _p(wg), _p(lb), _p(w1), _p(w3),
+                                      _p(w2), _p(s1), _p(s3), _p(s2), _p(ids), _p(sp), int(bool(renormalize)),
+                                      float(alpha), _p(dy), float(dL), _p(out["dx"]), _p(out["dw_gate"]),
+                                      _p(out["dw1"]), _p(out["dw3"]), _p(out["dw2"]), _p(out.get("dws1")),
+                                      _p(out.get("dws3")), _p(out.get("dws2")), _p(out["dlogits"])), "layer_backward")
     return out

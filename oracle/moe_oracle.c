@@ -560,3 +560,264 @@ int oracle_dequant_fp8(long long rows, int cols, const uint8_t *q, const float *
             out[(size_t)r * cols + i] = e4m3_value(q[(size_t)r * cols + i]) * (double)scale[r];
     return 0;
 }
+
+/*
+ * Backward pass of the layer (training; SURVEY's NEXT row, the pages' own
+ * statement of the gradients is the load-balancing one): for the scalar
+ *   Loss = <dy, y> + dL * L_balance,
+ * with the routing decisions (ids, the capacity cut) held fixed -- top-k
+ * selection has no gradient ("MoE Deep Dive", Load Balancing Loss
+ * Derivation: hard selection is non-differentiable) -- and f_i treated as a
+ * constant while p_i carries the gradient (same section: F_i "treated as
+ * constant, no gradient during backprop", P_i differentiable), the gradients
+ * of every input of the forward pass, by the chain rule written out per token:
+ *   kept slot j of token t, expert e, gate g:
+ *     a = W1_e x, b = W3_e x, h = silu(a) b, o = W2_e h        (the expert again)
+ *     dg_j  = <dy_t, o>
+ *     dh    = g W2_e^T dy_t
+ *     da    = dh * b * silu'(a),  silu'(a) = s (1 + a (1 - s)), s = 1/(1+e^-a)
+ *     db    = dh * silu(a)
+ *     dx_t += W1_e^T da + W3_e^T db
+ *     dW1_e += da x^T,  dW3_e += db x^T,  dW2_e += g dy_t h^T
+ *   shared expert: the same with g = 1 (no gate gradient);
+ *   gates -> logits: with renormalisation the gates are the softmax of the
+ *     chosen logits, dl_{e_j} = g_j (dg_j - sum_j' g_j' dg_j'), other
+ *     experts 0; without it g_j = p_{e_j} and dl = p (u - <p, u>), u_{e_j} =
+ *     dg_j (dropped slots have dg_j = 0);
+ *   L_balance = alpha E sum_i f_i (1/T) sum_t p_ti adds
+ *     dl_t += dL (alpha E / T) p_t (f - <p_t, f>),  f_i = counts_i / (T k);
+ *   router: dW_g = sum_t dl_t x_t^T, dx_t += W_g^T dl_t.
+ * dy is fp64 [T][d]; every output is fp64 (dx [T][d], dw_gate [E][d],
+ * dw1/dw3 [E][F][d], dw2 [E][d][F], dws1/dws3 [F_s][d], dws2 [d][F_s] when
+ * n_shared, dlogits [T][E]).  slot_pos < 0 marks a dropped slot.
+ * Pinned: PyTorch autograd in fp64 on the same function; central finite
+ * differences of the forward oracle.
+ */
+static double sigmoid(double a) { return 1.0 / (1.0 + exp(-a)); }
+
+int oracle_layer_backward(int T, int d, int E, int k, int F, int n_shared, int F_s, int dtype, const void *x,
+                          const void *w_gate, const float *logit_bias, const void *w1, const void *w3,
+                          const void *w2, const void *ws1, const void *ws3, const void *ws2, const int32_t *ids,
+                          const int32_t *slot_pos, int renormalize, double alpha, const double *dy, double dL,
+                          double *dx, double *dw_gate, double *dw1, double *dw3, double *dw2, double *dws1,
+                          double *dws3, double *dws2, double *dlogits) {
+    if (T < 1 || E < 1 || k < 1 || k > E || n_shared < 0 || n_shared > 1) return -1;
+    double *gates = (double *)malloc(sizeof(double) * (size_t)T * k);
+    double *fcount = (double *)calloc((size_t)E, sizeof(double));
+    if (!gates || !fcount) {
+        free(gates);
+        free(fcount);
+        return -2;
+    }
+    for (size_t i = 0; i < (size_t)T * k; ++i) {
+        const int e = ids[i];
+        if (e < 0 || e >= E) {
+            free(gates);
+            free(fcount);
+            return -1;
+        }
+        fcount[e] += 1.0 / ((double)T * (double)k);
+    }
+    int bad = 0;
+    const int Fm = F > F_s ? F : F_s;
+    /* phase A, per token: gates, gate gradients, dx, dlogits */
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)d);
+        double *l = (double *)malloc(sizeof(double) * (size_t)E);
+        double *p = (double *)malloc(sizeof(double) * (size_t)E);
+        double *a = (double *)malloc(sizeof(double) * (size_t)Fm);
+        double *b = (double *)malloc(sizeof(double) * (size_t)Fm);
+        double *dh = (double *)malloc(sizeof(double) * (size_t)Fm);
+        double *dg = (double *)malloc(sizeof(double) * (size_t)k);
+        int ok = xt && l && p && a && b && dh && dg;
+#pragma omp for schedule(dynamic, 1)
+        for (int t = 0; t < T; ++t) {
+            if (!ok) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            const double *dyt = dy + (size_t)t * d;
+            double *dxt = dx + (size_t)t * d;
+            for (int i = 0; i < d; ++i) {
+                xt[i] = elem(x, dtype, (size_t)t * d + i);
+                dxt[i] = 0.0;
+            }
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i) acc += elem(w_gate, dtype, (size_t)e * d + i) * xt[i];
+                l[e] = acc + (logit_bias ? (double)logit_bias[e] : 0.0);
+            }
+            double m = l[0], z = 0.0;
+            for (int e = 1; e < E; ++e)
+                if (l[e] > m) m = l[e];
+            for (int e = 0; e < E; ++e) z += (p[e] = exp(l[e] - m));
+            for (int e = 0; e < E; ++e) p[e] /= z;
+            double gsum = 0.0;
+            for (int j = 0; j < k; ++j) gsum += p[ids[(size_t)t * k + j]];
+            for (int j = 0; j < k; ++j) {
+                const double pj = p[ids[(size_t)t * k + j]];
+                gates[(size_t)t * k + j] = renormalize ? pj / gsum : pj;
+            }
+            /* routed experts */
+            for (int j = 0; j < k; ++j) {
+                dg[j] = 0.0;
+                if (slot_pos && slot_pos[(size_t)t * k + j] < 0) continue;
+                const int e = ids[(size_t)t * k + j];
+                const double g = gates[(size_t)t * k + j];
+                const size_t b1 = (size_t)e * F * d, b2 = (size_t)e * d * F;
+                for (int f = 0; f < F; ++f) {
+                    double av = 0.0, bv = 0.0;
+                    for (int i = 0; i < d; ++i) {
+                        av += elem(w1, dtype, b1 + (size_t)f * d + i) * xt[i];
+                        bv += elem(w3, dtype, b1 + (size_t)f * d + i) * xt[i];
+                    }
+                    a[f] = av;
+                    b[f] = bv;
+                }
+                double dgj = 0.0;
+                for (int o = 0; o < d; ++o) {
+                    double ov = 0.0;
+                    for (int f = 0; f < F; ++f) ov += elem(w2, dtype, b2 + (size_t)o * F + f) * (a[f] * sigmoid(a[f]) * b[f]);
+                    dgj += dyt[o] * ov;
+                }
+                dg[j] = dgj;
+                for (int f = 0; f < F; ++f) {
+                    double acc = 0.0;
+                    for (int o = 0; o < d; ++o) acc += elem(w2, dtype, b2 + (size_t)o * F + f) * dyt[o];
+                    dh[f] = g * acc;
+                }
+                for (int f = 0; f < F; ++f) {
+                    const double s = sigmoid(a[f]);
+                    const double da = dh[f] * b[f] * s * (1.0 + a[f] * (1.0 - s));
+                    const double db = dh[f] * a[f] * s;
+                    for (int i = 0; i < d; ++i)
+                        dxt[i] += elem(w1, dtype, b1 + (size_t)f * d + i) * da + elem(w3, dtype, b1 + (size_t)f * d + i) * db;
+                }
+            }
+            /* shared expert */
+            if (n_shared == 1) {
+                for (int f = 0; f < F_s; ++f) {
+                    double av = 0.0, bv = 0.0, acc = 0.0;
+                    for (int i = 0; i < d; ++i) {
+                        av += elem(ws1, dtype, (size_t)f * d + i) * xt[i];
+                        bv += elem(ws3, dtype, (size_t)f * d + i) * xt[i];
+                    }
+                    for (int o = 0; o < d; ++o) acc += elem(ws2, dtype, (size_t)o * F_s + f) * dyt[o];
+                    const double s = sigmoid(av);
+                    const double da = acc * bv * s * (1.0 + av * (1.0 - s));
+                    const double db = acc * av * s;
+                    for (int i = 0; i < d; ++i)
+                        dxt[i] += elem(ws1, dtype, (size_t)f * d + i) * da + elem(ws3, dtype, (size_t)f * d + i) * db;
+                }
+            }
+            /* gates -> logits, plus the balance loss */
+            double *dl = dlogits + (size_t)t * E;
+            for (int e = 0; e < E; ++e) dl[e] = 0.0;
+            if (renormalize) {
+                double s = 0.0;
+                for (int j = 0; j < k; ++j) s += gates[(size_t)t * k + j] * dg[j];
+                for (int j = 0; j < k; ++j) dl[ids[(size_t)t * k + j]] += gates[(size_t)t * k + j] * (dg[j] - s);
+            } else {
+                double s = 0.0;
+                for (int j = 0; j < k; ++j) s += p[ids[(size_t)t * k + j]] * dg[j];
+                for (int e = 0; e < E; ++e) dl[e] -= p[e] * s;
+                for (int j = 0; j < k; ++j) dl[ids[(size_t)t * k + j]] += p[ids[(size_t)t * k + j]] * dg[j];
+            }
+            double pf = 0.0;
+            for (int e = 0; e < E; ++e) pf += p[e] * fcount[e];
+            for (int e = 0; e < E; ++e) dl[e] += dL * alpha * (double)E / (double)T * p[e] * (fcount[e] - pf);
+            for (int i = 0; i < d; ++i) {
+                double acc = 0.0;
+                for (int e = 0; e < E; ++e) acc += elem(w_gate, dtype, (size_t)e * d + i) * dl[e];
+                dxt[i] += acc;
+            }
+        }
+        free(xt);
+        free(l);
+        free(p);
+        free(a);
+        free(b);
+        free(dh);
+        free(dg);
+    }
+    if (bad) {
+        free(gates);
+        free(fcount);
+        return -2;
+    }
+    /* phase B, per expert: weight gradients (each expert's rows belong to one thread) */
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)d);
+        double *a = (double *)malloc(sizeof(double) * (size_t)Fm);
+        double *b = (double *)malloc(sizeof(double) * (size_t)Fm);
+        double *dh = (double *)malloc(sizeof(double) * (size_t)Fm);
+        int ok = xt && a && b && dh;
+#pragma omp for schedule(dynamic, 1)
+        for (int e = 0; e < E + n_shared; ++e) {
+            if (!ok) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            const int shared = e == E;
+            const int Fe = shared ? F_s : F;
+            const void *W1 = shared ? ws1 : w1, *W3 = shared ? ws3 : w3, *W2 = shared ? ws2 : w2;
+            const size_t b1 = shared ? 0 : (size_t)e * F * d, b2 = shared ? 0 : (size_t)e * d * F;
+            double *D1 = shared ? dws1 : dw1 + b1, *D3 = shared ? dws3 : dw3 + b1, *D2 = shared ? dws2 : dw2 + b2;
+            memset(D1, 0, sizeof(double) * (size_t)Fe * d);
+            memset(D3, 0, sizeof(double) * (size_t)Fe * d);
+            memset(D2, 0, sizeof(double) * (size_t)d * Fe);
+            for (int t = 0; t < T; ++t)
+                for (int j = 0; j < (shared ? 1 : k); ++j) {
+                    double g = 1.0;
+                    if (!shared) {
+                        if (ids[(size_t)t * k + j] != e) continue;
+                        if (slot_pos && slot_pos[(size_t)t * k + j] < 0) continue;
+                        g = gates[(size_t)t * k + j];
+                    }
+                    const double *dyt = dy + (size_t)t * d;
+                    for (int i = 0; i < d; ++i) xt[i] = elem(x, dtype, (size_t)t * d + i);
+                    for (int f = 0; f < Fe; ++f) {
+                        double av = 0.0, bv = 0.0, acc = 0.0;
+                        for (int i = 0; i < d; ++i) {
+                            av += elem(W1, dtype, b1 + (size_t)f * d + i) * xt[i];
+                            bv += elem(W3, dtype, b1 + (size_t)f * d + i) * xt[i];
+                        }
+                        for (int o = 0; o < d; ++o) acc += elem(W2, dtype, b2 + (size_t)o * Fe + f) * dyt[o];
+                        a[f] = av;
+                        b[f] = bv;
+                        dh[f] = g * acc;
+                    }
+                    for (int f = 0; f < Fe; ++f) {
+                        const double s = sigmoid(a[f]);
+                        const double da = dh[f] * b[f] * s * (1.0 + a[f] * (1.0 - s));
+                        const double db = dh[f] * a[f] * s;
+                        const double hf = a[f] * s * b[f];
+                        for (int i = 0; i < d; ++i) {
+                            D1[(size_t)f * d + i] += da * xt[i];
+                            D3[(size_t)f * d + i] += db * xt[i];
+                        }
+                        for (int o = 0; o < d; ++o) D2[(size_t)o * Fe + f] += g * dyt[o] * hf;
+                    }
+                }
+        }
+        free(xt);
+        free(a);
+        free(b);
+        free(dh);
+    }
+    /* router weight gradient */
+#pragma omp parallel for schedule(static)
+    for (int e = 0; e < E; ++e)
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += dlogits[(size_t)t * E + e] * elem(x, dtype, (size_t)t * d + i);
+            dw_gate[(size_t)e * d + i] = acc;
+        }
+    free(gates);
+    free(fcount);
+    return bad ? -2 : 0;
+}
