@@ -309,6 +309,37 @@ MOE_API int moe_forward_fp8(const moe_config *cfg, const void *x, const void *w_
                             const float *select_bias, const moe_fp8_weights *w, void *y, const moe_stats *stats,
                             void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---- backward pass ------------------------------------------------------
+ * Gradients of the scalar  <dy, y> + dL * L_balance  with respect to x, W_g,
+ * W1, W3, W2 and the shared expert's weights, the routing decisions (top-k
+ * ids and the capacity cut) held fixed -- hard selection has no gradient --
+ * and f_i held constant while p_i carries the gradient ("MoE Deep Dive", Load
+ * Balancing Loss Derivation: F_i is a constant statistic, P_i the
+ * differentiable soft probability).  Per kept slot (expert e, gate g):
+ *   dg = <dy, W2_e h>,  dh = g W2_e^T dy,  dG = dh U silu'(G),  dU = dh silu(G),
+ *   dx += W1_e^T dG + W3_e^T dU,  dW1_e += dG x^T,  dW3_e += dU x^T,
+ *   dW2_e += g dy h^T;  gates -> logits through the (renormalised) softmax;
+ *   L_balance adds dL alpha E / T  p_t (f - <p_t, f>) to the logits of t;
+ *   dW_g = sum_t dlogits_t x_t^T,  dx += W_g^T dlogits.
+ * The call recomputes the forward routing, grouping and expert activations
+ * (nothing is kept from moe_forward) on the tensor-core GEMMs, with bf16
+ * operands (G, U, dG, dU, h and g*dy rounded to bf16 where they feed a GEMM)
+ * and fp32 accumulation.
+ *   In:  x [T][d], w_gate, w1, w3, w2 (and ws1, ws3, ws2 when n_shared) as for
+ *        moe_forward, logit_bias / select_bias nullable, dy [T][d] (bf16),
+ *        dL (host float, the upstream gradient of L_balance; 0 to ignore it).
+ *   Out (fp32, caller-owned): dx [T][d], dw_gate [E][d], dw1, dw3 [E][F][d],
+ *        dw2 [E][d][F]; dws1, dws3 [F_s][d], dws2 [d][F_s] when n_shared.
+ * Requires cfg->dtype == MOE_BF16 (else MOE_ERR_DTYPE) and token-choice
+ * routing (expert choice: MOE_ERR_SHAPE); ws of moe_backward_workspace_size
+ * bytes (it covers a forward workspace as well). */
+MOE_API size_t moe_backward_workspace_size(const moe_config *cfg);
+MOE_API int moe_backward(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
+                         const float *select_bias, const void *w1, const void *w3, const void *w2, const void *ws1,
+                         const void *ws3, const void *ws2, const void *dy, float dL, float *dx, float *dw_gate,
+                         float *dw1, float *dw3, float *dw2, float *dws1, float *dws3, float *dws2, void *ws,
+                         size_t ws_bytes, moe_stream_t stream);
+
 /* Reads (and clears) the device status word kept in the workspace: MOE_OK,
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  Synchronises `stream` first.
  * Returns MOE_ERR_CUDA if the copy itself fails. */

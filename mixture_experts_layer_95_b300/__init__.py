@@ -27,7 +27,8 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTY
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
             "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static", "moe_bias_update",
-            "moe_plan_describe", "moe_route_expert_choice", "moe_quantize_fp8", "moe_forward_fp8")
+            "moe_plan_describe", "moe_route_expert_choice", "moe_quantize_fp8", "moe_forward_fp8",
+            "moe_backward_workspace_size", "moe_backward")
 STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
 
 
@@ -93,6 +94,10 @@ def lib():
         L.moe_forward_fp8.argtypes = [cfgp, vp, vp, vp, vp, ctypes.POINTER(MoeFp8Weights), vp,
                                       ctypes.POINTER(MoeStats), vp, sz, vp]
         L.moe_forward_fp8.restype = i32
+        L.moe_backward_workspace_size.argtypes = [cfgp]
+        L.moe_backward_workspace_size.restype = sz
+        L.moe_backward.argtypes = [cfgp] + [vp] * 11 + [ctypes.c_float] + [vp] * 8 + [vp, sz, vp]
+        L.moe_backward.restype = i32
         L.moe_route_expert_choice.restype = i32
         L.moe_plan_describe.argtypes = [cfgp, ctypes.c_char_p, sz]
         L.moe_plan_describe.restype = i32
@@ -473,6 +478,46 @@ def quantize_experts_fp8(layer: "Layer", w1, w3, w2, ws1=None, ws3=None, ws2=Non
         q, sc = quantize_fp8(t, stream)
         out[n] = q
         out["s" + n[1:]] = sc  # w1 -> s1, ws1 -> ss1
+    return out
+
+
+def backward(layer: Layer, x, w_gate, w1, w3, w2, dy, logit_bias=None, select_bias=None, ws1=None, ws3=None,
+             ws2=None, dL: float = 0.0, stream=None) -> dict:
+    """moe_backward: gradients (fp32) of <dy, y> + dL * L_balance for every
+    input of the layer, routing held fixed.  Returns a dict with dx, dw_gate,
+    dw1, dw3, dw2 (and dws1, dws3, dws2 with a shared expert)."""
+    dt, dev = layer.torch_dtype, x.device
+    E, F, d, T, Fs = layer.E, layer.d_ff, layer.d, layer.T, layer.d_ff_shared
+    _need(x, (T, d), dt, "x")
+    _need(dy, (T, d), dt, "dy")
+    _need(w_gate, (E, d), dt, "w_gate")
+    _need(w1, (E, F, d), dt, "w1")
+    _need(w3, (E, F, d), dt, "w3")
+    _need(w2, (E, d, F), dt, "w2")
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(dx=torch.empty((T, d), **f32), dw_gate=torch.empty((E, d), **f32),
+               dw1=torch.empty((E, F, d), **f32), dw3=torch.empty((E, F, d), **f32),
+               dw2=torch.empty((E, d, F), **f32))
+    if layer.n_shared:
+        _need(ws1, (Fs, d), dt, "ws1")
+        _need(ws3, (Fs, d), dt, "ws3")
+        _need(ws2, (d, Fs), dt, "ws2")
+        out.update(dws1=torch.empty((Fs, d), **f32), dws3=torch.empty((Fs, d), **f32),
+                   dws2=torch.empty((d, Fs), **f32))
+    c = layer.cfg()
+    nbytes = lib().moe_backward_workspace_size(ctypes.byref(c))
+    if nbytes == 0:
+        raise MoeError(-2, "moe_backward_workspace_size")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _check(lib().moe_workspace_init(ctypes.byref(c), _ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
+    _check(lib().moe_backward(ctypes.byref(c), _ptr(x), _ptr(w_gate), _ptr(logit_bias), _ptr(select_bias), _ptr(w1),
+                              _ptr(w3), _ptr(w2), _ptr(ws1), _ptr(ws3), _ptr(ws2), _ptr(dy), ctypes.c_float(dL),
+                              _ptr(out["dx"]), _ptr(out["dw_gate"]), _ptr(out["dw1"]), _ptr(out["dw3"]),
+                              _ptr(out["dw2"]), _ptr(out.get("dws1")), _ptr(out.get("dws3")), _ptr(out.get("dws2")),
+                              _ptr(ws), ws.numel(), _stream(stream)), "moe_backward")
+    rc = last_device_status(layer, ws, stream)
+    if rc != 0:
+        raise MoeError(rc, "moe_backward (device status)")
     return out
 
 

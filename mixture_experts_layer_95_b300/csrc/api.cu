@@ -212,6 +212,70 @@ Layout layout(const moe_config& c) {
     return l;
 }
 
+// Backward-pass workspace: the forward layout, then these regions.
+struct BLayout {
+    size_t probs, xp, dyp, G, U, D, dGU, Hb, dgp, w2t, w13t, kbase, klen, dGT, dUT, HbT, xpT, dysT, dXp, dlog, R,
+        wg_part, s_off, s_kbase, s_klen, Gs, Us, Ds, dGUs, Hbs, ws2t, ws13t, dGsT, dUsT, HbsT, xT, dyT, dXs, total;
+    int ncols, ncols_s;
+};
+
+constexpr int kWgSplit = 8;  // token chunks of the router weight gradient
+
+BLayout blayout(const moe_config& c) {
+    BLayout b{};
+    const size_t n = (size_t)c.T * c.k, E = c.E, F = c.d_ff, d = c.d, T = c.T, Fs = c.d_ff_shared;
+    b.ncols = (int)(((long long)n + 64LL * c.E + 63) / 64 * 64);  // every expert's window, each rounded up to 64
+    b.ncols_s = (int)((T + 63) / 64 * 64);
+    const size_t nc = (size_t)b.ncols, ncs = (size_t)b.ncols_s;
+    size_t off = layout(c).total;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes);
+        return at;
+    };
+    b.probs = take(4 * T * E);
+    b.xp = take(2 * n * d);
+    b.dyp = take(2 * n * d);
+    b.G = take(4 * n * F);
+    b.U = take(4 * n * F);
+    b.D = take(4 * n * F);
+    b.dGU = take(2 * n * 2 * F);
+    b.Hb = take(2 * n * F);
+    b.dgp = take(4 * n);
+    b.w2t = take(2 * E * F * d);
+    b.w13t = take(2 * E * d * 2 * F);
+    b.kbase = take(4 * E);
+    b.klen = take(4 * E);
+    b.dGT = take(2 * F * nc);
+    b.dUT = take(2 * F * nc);
+    b.HbT = take(2 * F * nc);
+    b.xpT = take(2 * d * nc);
+    b.dysT = take(2 * d * nc);
+    b.dXp = take(4 * n * d);
+    b.dlog = take(4 * T * E);
+    b.R = take(4 * T * d);
+    b.wg_part = take(4 * kWgSplit * E * d);
+    const bool sh = c.n_shared != 0;
+    b.s_off = take(sh ? 8 : 0);
+    b.s_kbase = take(sh ? 4 : 0);
+    b.s_klen = take(sh ? 4 : 0);
+    b.Gs = take(sh ? 4 * T * Fs : 0);
+    b.Us = take(sh ? 4 * T * Fs : 0);
+    b.Ds = take(sh ? 4 * T * Fs : 0);
+    b.dGUs = take(sh ? 2 * T * 2 * Fs : 0);
+    b.Hbs = take(sh ? 2 * T * Fs : 0);
+    b.ws2t = take(sh ? 2 * Fs * d : 0);
+    b.ws13t = take(sh ? 2 * d * 2 * Fs : 0);
+    b.dGsT = take(sh ? 2 * Fs * ncs : 0);
+    b.dUsT = take(sh ? 2 * Fs * ncs : 0);
+    b.HbsT = take(sh ? 2 * Fs * ncs : 0);
+    b.xT = take(sh ? 2 * d * ncs : 0);
+    b.dyT = take(sh ? 2 * d * ncs : 0);
+    b.dXs = take(sh ? 4 * T * d : 0);
+    b.total = off;
+    return b;
+}
+
 template <typename P>
 P* at(void* ws, size_t off) {
     return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off);
@@ -850,6 +914,204 @@ int moe_quantize_fp8(const void* w, int32_t dtype, int64_t rows, int32_t cols, u
     int sms = 0;
     MOE_TRY(device_sms(&sms));
     MOE_LAUNCH(launch_quantize_fp8(dtype, rows, cols, w, q, scale, reinterpret_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
+size_t moe_backward_workspace_size(const moe_config* cfg) {
+    if (check_config(cfg) != MOE_OK || cfg->dtype != MOE_BF16 || expert_choice(*cfg)) return 0;
+    return blayout(*cfg).total;
+}
+
+int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                 const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                 const void* ws3, const void* ws2, const void* dy, float dL, float* dx, float* dw_gate, float* dw1,
+                 float* dw3, float* dw2, float* dws1, float* dws3, float* dws2, void* ws, size_t ws_bytes,
+                 moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (c.dtype != MOE_BF16) return MOE_ERR_DTYPE;
+    if (expert_choice(c)) return MOE_ERR_SHAPE;  // token choice only
+    if (c.T == 0) return MOE_OK;
+    if (!x || !w_gate || !w1 || !w3 || !w2 || !dy || !dx || !dw_gate || !dw1 || !dw3 || !dw2 || !ws)
+        return MOE_ERR_NULL;
+    if (c.n_shared && (!ws1 || !ws3 || !ws2 || !dws1 || !dws3 || !dws2)) return MOE_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign) return MOE_ERR_WORKSPACE;
+    const BLayout B = blayout(c);
+    if (ws_bytes < B.total) return MOE_ERR_WORKSPACE;
+    for (const void* p : {x, w_gate, w1, w3, w2, dy, (const void*)dx, (const void*)dw_gate, (const void*)dw1,
+                          (const void*)dw3, (const void*)dw2})
+        if (!aligned16(p)) return MOE_ERR_ALIGN;
+    if (c.n_shared)
+        for (const void* p : {ws1, ws3, ws2, (const void*)dws1, (const void*)dws3, (const void*)dws2})
+            if (!aligned16(p)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Layout L = layout(c);
+    const int E = c.E, F = c.d_ff, d = c.d, T = c.T, Fs = c.d_ff_shared, n = c.T * c.k;
+    int* status = at<int>(ws, L.status);
+    int32_t* topk_ids = at<int32_t>(ws, L.topk_ids);
+    float* gates = at<float>(ws, L.gates);
+    float* probs = at<float>(ws, B.probs);
+    const int chunk = router_chunk(c.T, c.E, c.d, c.dtype);
+
+    // forward routing and grouping again (the decisions the gradients hold fixed)
+    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates,
+                          at<int32_t>(ws, L.block_hist), sms, s, c.k, probs));
+    GroupOut o{};
+    o.counts = at<int32_t>(ws, L.counts);
+    o.kept = at<int32_t>(ws, L.kept);
+    o.offsets = at<int32_t>(ws, L.offsets);
+    o.sorted_token_ids = at<int32_t>(ws, L.sorted);
+    o.slot_pos = at<int32_t>(ws, L.slot_pos);
+    o.gates_perm = at<float>(ws, L.gates_perm);
+    o.n_dropped = at<int32_t>(ws, L.n_dropped);
+    MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, at<int32_t>(ws, L.block_hist), o,
+                                 status, s));
+    const int32_t* rows_end = o.offsets + E;
+    void* xp = at<void>(ws, B.xp);
+    void* dyp = at<void>(ws, B.dyp);
+    MOE_LAUNCH(launch_gather_rows(MOE_BF16, T, d, n, rows_end, o.sorted_token_ids, x, xp, status, s));
+    MOE_LAUNCH(launch_gather_rows(MOE_BF16, T, d, n, rows_end, o.sorted_token_ids, dy, dyp, status, s));
+    int32_t* kbase = at<int32_t>(ws, B.kbase);
+    int32_t* klen = at<int32_t>(ws, B.klen);
+    MOE_LAUNCH(launch_k_windows(E, o.offsets, kbase, klen, -1, s));
+    int32_t *s_off = nullptr, *s_kbase = nullptr, *s_klen = nullptr;
+    if (c.n_shared) {
+        s_off = at<int32_t>(ws, B.s_off);
+        s_kbase = at<int32_t>(ws, B.s_kbase);
+        s_klen = at<int32_t>(ws, B.s_klen);
+        MOE_LAUNCH(launch_k_windows(1, s_off, s_kbase, s_klen, T, s));
+    }
+
+    // transposed weights: W2^T per expert [F][d]; [W1^T | W3^T] per expert [d][2F]
+    void* w2t = at<void>(ws, B.w2t);
+    void* w13t = at<void>(ws, B.w13t);
+    MOE_LAUNCH(launch_transpose_batched(MOE_BF16, w2, E, d, F, w2t, d, 0, s));
+    MOE_LAUNCH(launch_transpose_batched(MOE_BF16, w1, E, F, d, w13t, 2 * (size_t)F, 0, s));
+    MOE_LAUNCH(launch_transpose_batched(MOE_BF16, w3, E, F, d, w13t, 2 * (size_t)F, F, s));
+    if (c.n_shared) {
+        MOE_LAUNCH(launch_transpose_batched(MOE_BF16, ws2, 1, d, Fs, at<void>(ws, B.ws2t), d, 0, s));
+        MOE_LAUNCH(launch_transpose_batched(MOE_BF16, ws1, 1, Fs, d, at<void>(ws, B.ws13t), 2 * (size_t)Fs, 0, s));
+        MOE_LAUNCH(launch_transpose_batched(MOE_BF16, ws3, 1, Fs, d, at<void>(ws, B.ws13t), 2 * (size_t)Fs, Fs, s));
+    }
+
+    // grouped GEMMs of the routed experts (problem 0) and the shared expert (problem 1)
+    const int np = c.n_shared ? 2 : 1;
+    auto routed = [&](const void* A, int a_rows, const void* Bm, int N, int K, void* out) {
+        GemmProblem g{};
+        g.A = A;
+        g.a_rows = a_rows;
+        g.B1 = Bm;
+        g.offsets = o.offsets;
+        g.G = E;
+        g.N = N;
+        g.K = K;
+        g.out = out;
+        return g;
+    };
+    auto dense = [&](const void* A, int M, const void* Bm, int N, int K, void* out) {
+        GemmProblem g{};
+        g.A = A;
+        g.a_rows = M;
+        g.B1 = Bm;
+        g.G = 1;
+        g.M = M;
+        g.N = N;
+        g.K = K;
+        g.out = out;
+        return g;
+    };
+    auto windows = [&](const void* A, int M, const void* Bm, int N, int K, const int32_t* kb, const int32_t* kl, int G,
+                       void* out) {
+        GemmProblem g{};
+        g.A = A;
+        g.a_rows = M;
+        g.B1 = Bm;
+        g.G = G;
+        g.M = M;
+        g.N = N;
+        g.K = K;
+        g.kbase = kb;
+        g.klen = kl;
+        g.out = out;
+        return g;
+    };
+    float* G = at<float>(ws, B.G);
+    float* U = at<float>(ws, B.U);
+    float* D = at<float>(ws, B.D);
+    {
+        GemmProblem p1[2] = {routed(xp, n, w1, F, d, G), dense(x, T, ws1, Fs, d, at<float>(ws, B.Gs))};
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, p1, np, status, sms, s));
+        GemmProblem p2[2] = {routed(xp, n, w3, F, d, U), dense(x, T, ws3, Fs, d, at<float>(ws, B.Us))};
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, p2, np, status, sms, s));
+        GemmProblem p3[2] = {routed(dyp, n, w2t, F, d, D), dense(dy, T, at<void>(ws, B.ws2t), Fs, d, at<float>(ws, B.Ds))};
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, p3, np, status, sms, s));
+    }
+    void* dGU = at<void>(ws, B.dGU);
+    void* Hb = at<void>(ws, B.Hb);
+    float* dgp = at<float>(ws, B.dgp);
+    MOE_LAUNCH(launch_swiglu_backward(n, rows_end, F, G, U, D, o.gates_perm, dGU, Hb, dgp, s));
+    if (c.n_shared)
+        MOE_LAUNCH(launch_swiglu_backward(T, nullptr, Fs, at<float>(ws, B.Gs), at<float>(ws, B.Us),
+                                          at<float>(ws, B.Ds), nullptr, at<void>(ws, B.dGUs), at<void>(ws, B.Hbs),
+                                          nullptr, s));
+    float* dXp = at<float>(ws, B.dXp);
+    float* dXs = c.n_shared ? at<float>(ws, B.dXs) : nullptr;
+    {
+        GemmProblem p4[2] = {routed(dGU, n, w13t, d, 2 * F, dXp),
+                             dense(at<void>(ws, B.dGUs), T, at<void>(ws, B.ws13t), d, 2 * Fs, dXs)};
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, p4, np, status, sms, s));
+    }
+
+    // weight gradients: per-expert K windows of the transposed activations
+    const int nc = B.ncols, ncs = B.ncols_s;
+    void* dGT = at<void>(ws, B.dGT);
+    void* dUT = at<void>(ws, B.dUT);
+    void* HbT = at<void>(ws, B.HbT);
+    void* xpT = at<void>(ws, B.xpT);
+    void* dysT = at<void>(ws, B.dysT);
+    MOE_LAUNCH(launch_transpose_windows(dGU, 2 * (size_t)F, 0, F, E, o.offsets, kbase, klen, nullptr, dGT, nc, nc, s));
+    MOE_LAUNCH(launch_transpose_windows(dGU, 2 * (size_t)F, F, F, E, o.offsets, kbase, klen, nullptr, dUT, nc, nc, s));
+    MOE_LAUNCH(launch_transpose_windows(Hb, F, 0, F, E, o.offsets, kbase, klen, nullptr, HbT, nc, nc, s));
+    MOE_LAUNCH(launch_transpose_windows(xp, d, 0, d, E, o.offsets, kbase, klen, nullptr, xpT, nc, nc, s));
+    MOE_LAUNCH(launch_transpose_windows(dyp, d, 0, d, E, o.offsets, kbase, klen, o.gates_perm, dysT, nc, nc, s));
+    if (c.n_shared) {
+        void* dGUs = at<void>(ws, B.dGUs);
+        MOE_LAUNCH(launch_transpose_windows(dGUs, 2 * (size_t)Fs, 0, Fs, 1, s_off, s_kbase, s_klen, nullptr,
+                                            at<void>(ws, B.dGsT), ncs, ncs, s));
+        MOE_LAUNCH(launch_transpose_windows(dGUs, 2 * (size_t)Fs, Fs, Fs, 1, s_off, s_kbase, s_klen, nullptr,
+                                            at<void>(ws, B.dUsT), ncs, ncs, s));
+        MOE_LAUNCH(launch_transpose_windows(at<void>(ws, B.Hbs), Fs, 0, Fs, 1, s_off, s_kbase, s_klen, nullptr,
+                                            at<void>(ws, B.HbsT), ncs, ncs, s));
+        MOE_LAUNCH(launch_transpose_windows(x, d, 0, d, 1, s_off, s_kbase, s_klen, nullptr, at<void>(ws, B.xT), ncs,
+                                            ncs, s));
+        MOE_LAUNCH(launch_transpose_windows(dy, d, 0, d, 1, s_off, s_kbase, s_klen, nullptr, at<void>(ws, B.dyT), ncs,
+                                            ncs, s));
+    }
+    {
+        GemmProblem q1[2] = {windows(dGT, F, xpT, d, nc, kbase, klen, E, dw1),
+                             windows(at<void>(ws, B.dGsT), Fs, at<void>(ws, B.xT), d, ncs, s_kbase, s_klen, 1, dws1)};
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, q1, np, status, sms, s));
+        GemmProblem q3[2] = {windows(dUT, F, xpT, d, nc, kbase, klen, E, dw3),
+                             windows(at<void>(ws, B.dUsT), Fs, at<void>(ws, B.xT), d, ncs, s_kbase, s_klen, 1, dws3)};
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, q3, np, status, sms, s));
+        GemmProblem q2[2] = {windows(dysT, d, HbT, F, nc, kbase, klen, E, dw2),
+                             windows(at<void>(ws, B.dyT), d, at<void>(ws, B.HbsT), Fs, ncs, s_kbase, s_klen, 1, dws2)};
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, q2, np, status, sms, s));
+    }
+
+    // router: gate gradients -> logits (+ balance loss) -> W_g and x
+    float* dlog = at<float>(ws, B.dlog);
+    float* R = at<float>(ws, B.R);
+    MOE_LAUNCH(launch_router_backward(T, E, c.k, probs, topk_ids, o.slot_pos, gates, dgp, c.renormalize, o.counts,
+                                      c.alpha, dL, dlog, s));
+    MOE_LAUNCH(launch_router_dx(MOE_BF16, T, E, d, dlog, w_gate, dXs, R, s));
+    float* wgp = at<float>(ws, B.wg_part);
+    MOE_LAUNCH(launch_wgate_grad(MOE_BF16, T, E, d, dlog, x, kWgSplit, wgp, s));
+    MOE_LAUNCH(launch_reduce_partials(E, nullptr, d, kWgSplit, wgp, dw_gate, s));
+    // dx = sum over kept slots of dX rows + router and shared-expert parts
+    MOE_LAUNCH(launch_combine(MOE_F32, T, d, c.k, dXp, o.slot_pos, R, dx, s));
     return MOE_OK;
 }
 

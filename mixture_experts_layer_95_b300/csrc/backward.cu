@@ -1,0 +1,380 @@
+// backward.cu -- the element-wise, transpose and router kernels of the backward
+// pass; its matrix products run on the grouped tensor-core GEMM (gemm_tc.cu).
+//
+// Gradients of <dy, y> + dL * L_balance with the routing decisions held fixed
+// (top-k selection has no gradient) and f_i held constant while p_i carries the
+// gradient ("MoE Deep Dive", Load Balancing Loss Derivation).  Per kept slot
+// (row r of the permuted layout, expert e, gate g), with G = X W1^T, U = X W3^T
+// recomputed and D = dy W2_e (the down projection transposed):
+//   dg_r = sum_f D h,   h = silu(G) U
+//   dh = g D,  dG = dh U silu'(G),  dU = dh silu(G)
+//   dX_r = dG W1_e + dU W3_e,  dW1_e = dG^T X,  dW3_e = dU^T X,  dW2_e = (g dy)^T h
+// The weight gradients contract over each expert's token rows: their operands
+// are transposed per expert into K windows that start on 64-column boundaries
+// (zero-filled to the next boundary), which the GEMM's K-grouped mode reads.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int TT = 64;  // transpose tile
+
+__device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// kbase[e] = sum over e' < e of klen rounded up to 64, klen[e] = rows of expert e.
+// const_len >= 0: a single window of that many rows, and offsets (then an
+// output) = {0, const_len}.
+__global__ void k_windows_kernel(int E, int32_t* __restrict__ offsets, int32_t* __restrict__ kbase,
+                                 int32_t* __restrict__ klen, int const_len) {
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        if (const_len >= 0) {
+            offsets[0] = 0;
+            offsets[1] = const_len;
+            kbase[0] = 0;
+            klen[0] = const_len;
+        } else {
+            int run = 0;
+            for (int e = 0; e < E; ++e) {
+                const int len = max(0, offsets[e + 1] - offsets[e]);
+                kbase[e] = run;
+                klen[e] = len;
+                run += (len + 63) / 64 * 64;
+            }
+        }
+    }
+    __syncthreads();
+    pdl_trigger();
+}
+
+// dst[c][kbase[e] + k] = scale(row) * src[(offsets[e] + k) * ld_src + col0 + c] for
+// k < klen[e], 0 for klen[e] <= k < round64(klen[e]); c < C.  One 64 x 64 tile per
+// block: a block's 64 destination columns lie inside one expert's window.
+__global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloat16* __restrict__ src, size_t ld_src,
+                                                                int col0, int C, int E,
+                                                                const int32_t* __restrict__ offsets,
+                                                                const int32_t* __restrict__ kbase,
+                                                                const int32_t* __restrict__ klen,
+                                                                const float* __restrict__ row_scale,
+                                                                __nv_bfloat16* __restrict__ dst, size_t ld_dst,
+                                                                int ncols) {
+    pdl_wait();
+    __shared__ float tile[TT][TT + 1];
+    const int c_tile = blockIdx.x * TT;  // source column block
+    const int k0 = blockIdx.y * TT;      // destination column block
+    if (k0 < ncols) {
+        int lo = 0, hi = E - 1;  // last expert whose window starts at or before k0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(kbase + mid) <= k0) lo = mid;
+            else hi = mid - 1;
+        }
+        const int e = lo;
+        const int base = __ldg(kbase + e), len = __ldg(klen + e);
+        const int padded = (len + 63) / 64 * 64;
+        if (k0 < base + padded) {  // beyond the last window: nothing to write
+            const int row_base = __ldg(offsets + e) + (k0 - base);
+            // load: threads walk 64 source rows x 64 columns, columns fastest
+            for (int i = threadIdx.x; i < TT * TT; i += blockDim.x) {
+                const int kk = i / TT, cc = i % TT;
+                const int k = k0 - base + kk;
+                float v = 0.f;
+                if (k < len && c_tile + cc < C) {
+                    const size_t r = (size_t)(row_base + kk);
+                    v = bf2f(src[r * ld_src + col0 + c_tile + cc]);
+                    if (row_scale) v *= __ldg(row_scale + r);
+                }
+                tile[kk][cc] = v;
+            }
+            __syncthreads();
+            // store: 64 destination rows (source columns) x 64 columns, columns fastest
+            for (int i = threadIdx.x; i < TT * TT; i += blockDim.x) {
+                const int cc = i / TT, kk = i % TT;
+                if (c_tile + cc < C) dst[(size_t)(c_tile + cc) * ld_dst + k0 + kk] = __float2bfloat16_rn(tile[kk][cc]);
+            }
+        }
+    }
+    __syncthreads();
+    pdl_trigger();
+}
+
+// dst[b][c][col0 + r] = src[b][r][c]: batch of [R][C] matrices (weights) into
+// [C][ld_dst] rows, at column offset col0.
+template <typename T>
+__global__ void __launch_bounds__(256) transpose_batched_kernel(const T* __restrict__ src, int R, int C,
+                                                                __nv_bfloat16* __restrict__ dst, size_t ld_dst,
+                                                                int col0) {
+    pdl_wait();
+    __shared__ float tile[TT][TT + 1];
+    const int b = blockIdx.z;
+    const int c_tile = blockIdx.x * TT, r_tile = blockIdx.y * TT;
+    const T* s = src + (size_t)b * R * C;
+    __nv_bfloat16* d = dst + (size_t)b * C * ld_dst;
+    for (int i = threadIdx.x; i < TT * TT; i += blockDim.x) {
+        const int rr = i / TT, cc = i % TT;
+        float v = 0.f;
+        if (r_tile + rr < R && c_tile + cc < C) {
+            const T w = s[(size_t)(r_tile + rr) * C + c_tile + cc];
+            if constexpr (sizeof(T) == 2) v = bf2f(w);
+            else v = w;
+        }
+        tile[rr][cc] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < TT * TT; i += blockDim.x) {
+        const int cc = i / TT, rr = i % TT;
+        if (r_tile + rr < R && c_tile + cc < C)
+            d[(size_t)(c_tile + cc) * ld_dst + col0 + r_tile + rr] = __float2bfloat16_rn(tile[rr][cc]);
+    }
+    __syncthreads();
+    pdl_trigger();
+}
+
+// One row r of the permuted layout (r < *rows_dev when given, else < rows_max):
+//   h = silu(G) U,  dg_r = sum_f D h,  dh = g D,
+//   dGU[r] = [dh U silu'(G) | dh silu(G)] (bf16),  Hb[r] = bf16(h).
+__global__ void __launch_bounds__(256) swiglu_backward_kernel(int rows_max, const int32_t* __restrict__ rows_dev, int F,
+                                                              const float* __restrict__ G,
+                                                              const float* __restrict__ U,
+                                                              const float* __restrict__ D,
+                                                              const float* __restrict__ gate,
+                                                              __nv_bfloat16* __restrict__ dGU,
+                                                              __nv_bfloat16* __restrict__ Hb,
+                                                              float* __restrict__ dgp) {
+    pdl_wait();
+    __shared__ float s_red[8];
+    const int rows = rows_dev ? min(*rows_dev, rows_max) : rows_max;
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const size_t o = (size_t)r * F;
+        const float g = gate ? __ldg(gate + r) : 1.0f;
+        float part = 0.f;
+        for (int f = threadIdx.x; f < F; f += blockDim.x) {
+            const float a = __ldg(G + o + f), b = __ldg(U + o + f), dd = __ldg(D + o + f);
+            const float s = 1.0f / (1.0f + __expf(-a));
+            const float h = a * s * b;
+            part += dd * h;
+            const float dh = g * dd;
+            dGU[2 * o + f] = __float2bfloat16_rn(dh * b * s * (1.0f + a * (1.0f - s)));
+            dGU[2 * o + F + f] = __float2bfloat16_rn(dh * a * s);
+            Hb[o + f] = __float2bfloat16_rn(h);
+        }
+        part = warp_sum(part);
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = part;
+        __syncthreads();
+        if (threadIdx.x == 0 && dgp) {
+            float acc = 0.f;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) acc += s_red[w];  // fixed order
+            dgp[r] = acc;
+        }
+        __syncthreads();
+    }
+    __syncthreads();
+    pdl_trigger();
+}
+
+// Gates -> logits for token t (one warp per token), plus the balance loss:
+//   renormalised gates:  dl[e_j] = g_j (dg_j - sum_j' g_j' dg_j')
+//   plain gates (p):     dl = p (u - <p, u>), u[e_j] = dg_j
+//   balance loss:        dl += dL alpha E / T  p (f - <p, f>),  f = counts / (T k)
+__global__ void __launch_bounds__(256) router_backward_kernel(int Tn, int E, int k, const float* __restrict__ probs,
+                                                              const int32_t* __restrict__ ids,
+                                                              const int32_t* __restrict__ slot_pos,
+                                                              const float* __restrict__ gates,
+                                                              const float* __restrict__ dgp, int renormalize,
+                                                              const int32_t* __restrict__ counts, float alpha,
+                                                              float dL, float* __restrict__ dlogits) {
+    pdl_wait();
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (t < Tn) {
+        const float* p = probs + (size_t)t * E;
+        float* dl = dlogits + (size_t)t * E;
+        // lane j < k: this token's slot j
+        float dg = 0.f, gj = 0.f, pj = 0.f;
+        int ej = -1;
+        if (lane < k) {
+            ej = __ldg(ids + (size_t)t * k + lane);
+            const int pos = __ldg(slot_pos + (size_t)t * k + lane);
+            dg = pos >= 0 ? __ldg(dgp + pos) : 0.f;
+            gj = __ldg(gates + (size_t)t * k + lane);
+            pj = (ej >= 0 && ej < E) ? __ldg(p + ej) : 0.f;
+        }
+        const float s = warp_sum(renormalize ? gj * dg : pj * dg);
+        const float inv_tk = 1.0f / ((float)Tn * (float)k);
+        float pf = 0.f;
+        for (int e = lane; e < E; e += 32) pf += __ldg(p + e) * ((float)__ldg(counts + e) * inv_tk);
+        pf = warp_sum(pf);
+        const float c = dL * alpha * (float)E / (float)Tn;
+        for (int e = lane; e < E; e += 32) {
+            const float pe = __ldg(p + e);
+            float v = c * pe * ((float)__ldg(counts + e) * inv_tk - pf);
+            if (!renormalize) v -= pe * s;
+            dl[e] = v;
+        }
+        __syncwarp();
+        if (lane < k && ej >= 0 && ej < E) dl[ej] += renormalize ? gj * (dg - s) : pj * dg;
+    }
+    __syncthreads();
+    pdl_trigger();
+}
+
+// R[t][i] = sum_e dl[t][e] W_g[e][i] (+ extra[t][i]): 8 tokens x 256 columns per block.
+template <typename T>
+__global__ void __launch_bounds__(256) router_dx_kernel(int Tn, int E, int d, const float* __restrict__ dlogits,
+                                                        const T* __restrict__ wg, const float* __restrict__ extra,
+                                                        float* __restrict__ R) {
+    pdl_wait();
+    constexpr int TOK = 8;
+    __shared__ float s_dl[TOK][128];
+    const int t0 = blockIdx.y * TOK;
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    float acc[TOK];
+#pragma unroll
+    for (int q = 0; q < TOK; ++q) acc[q] = 0.f;
+    for (int e0 = 0; e0 < E; e0 += 128) {
+        __syncthreads();
+        for (int j = threadIdx.x; j < TOK * 128; j += blockDim.x) {
+            const int q = j / 128, e = e0 + j % 128;
+            s_dl[q][j % 128] = (t0 + q < Tn && e < E) ? __ldg(dlogits + (size_t)(t0 + q) * E + e) : 0.f;
+        }
+        __syncthreads();
+        if (i < d) {
+            const int ne = min(128, E - e0);
+            for (int e = 0; e < ne; ++e) {
+                float w;
+                if constexpr (sizeof(T) == 2) w = bf2f(wg[(size_t)(e0 + e) * d + i]);
+                else w = wg[(size_t)(e0 + e) * d + i];
+#pragma unroll
+                for (int q = 0; q < TOK; ++q) acc[q] = fmaf(s_dl[q][e], w, acc[q]);
+            }
+        }
+    }
+    if (i < d)
+#pragma unroll
+        for (int q = 0; q < TOK; ++q)
+            if (t0 + q < Tn)
+                R[(size_t)(t0 + q) * d + i] = acc[q] + (extra ? __ldg(extra + (size_t)(t0 + q) * d + i) : 0.f);
+    __syncthreads();
+    pdl_trigger();
+}
+
+// part[s][e][i] = sum over tokens t of chunk s of dl[t][e] x[t][i]: 32 experts x
+// 256 columns per block, the tokens split into `nsplit` chunks (summed afterwards
+// in chunk order).
+template <typename T>
+__global__ void __launch_bounds__(256) wgate_grad_kernel(int Tn, int E, int d, const float* __restrict__ dlogits,
+                                                         const T* __restrict__ x, int nsplit,
+                                                         float* __restrict__ part) {
+    pdl_wait();
+    constexpr int EB = 32, TB = 32;
+    __shared__ float s_dl[TB][EB];
+    const int e0 = blockIdx.y * EB;
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    const int s = blockIdx.z;
+    const int tchunk = (Tn + nsplit - 1) / nsplit;
+    const int ta = s * tchunk, tb = min(Tn, ta + tchunk);
+    float acc[EB];
+#pragma unroll
+    for (int q = 0; q < EB; ++q) acc[q] = 0.f;
+    for (int tt = ta; tt < tb; tt += TB) {
+        __syncthreads();
+        for (int j = threadIdx.x; j < TB * EB; j += blockDim.x) {
+            const int q = j / EB, e = e0 + j % EB;
+            s_dl[q][j % EB] = (tt + q < tb && e < E) ? __ldg(dlogits + (size_t)(tt + q) * E + e) : 0.f;
+        }
+        __syncthreads();
+        if (i < d) {
+            const int nt = min(TB, tb - tt);
+            for (int q = 0; q < nt; ++q) {
+                float xv;
+                if constexpr (sizeof(T) == 2) xv = bf2f(x[(size_t)(tt + q) * d + i]);
+                else xv = x[(size_t)(tt + q) * d + i];
+#pragma unroll
+                for (int e = 0; e < EB; ++e) acc[e] = fmaf(s_dl[q][e], xv, acc[e]);
+            }
+        }
+    }
+    if (i < d)
+#pragma unroll
+        for (int e = 0; e < EB; ++e)
+            if (e0 + e < E) part[((size_t)s * E + e0 + e) * d + i] = acc[e];
+    __syncthreads();
+    pdl_trigger();
+}
+
+}  // namespace
+
+cudaError_t launch_k_windows(int E, int32_t* offsets, int32_t* kbase, int32_t* klen, int const_len, cudaStream_t s) {
+    launch_pdl(k_windows_kernel, dim3(1), dim3(32), 0, s, E, offsets, kbase, klen, const_len);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, int C, int E, const int32_t* offsets,
+                                     const int32_t* kbase, const int32_t* klen, const float* row_scale, void* dst,
+                                     size_t ld_dst, int ncols, cudaStream_t s) {
+    if (C == 0 || ncols == 0) return cudaSuccess;
+    const dim3 grid((C + TT - 1) / TT, (ncols + TT - 1) / TT);
+    launch_pdl(transpose_windows_kernel, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), ld_src, col0,
+               C, E, offsets, kbase, klen, row_scale, static_cast<__nv_bfloat16*>(dst), ld_dst, ncols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_batched(int dtype, const void* src, int batch, int R, int C, void* dst, size_t ld_dst,
+                                     int col0, cudaStream_t s) {
+    if (batch == 0 || R == 0 || C == 0) return cudaSuccess;
+    const dim3 grid((C + TT - 1) / TT, (R + TT - 1) / TT, batch);
+    if (dtype == MOE_BF16)
+        launch_pdl(transpose_batched_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
+                   static_cast<const __nv_bfloat16*>(src), R, C, static_cast<__nv_bfloat16*>(dst), ld_dst, col0);
+    else
+        launch_pdl(transpose_batched_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(src), R, C,
+                   static_cast<__nv_bfloat16*>(dst), ld_dst, col0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_backward(int rows_max, const int32_t* rows_dev, int F, const float* G, const float* U,
+                                   const float* D, const float* gate, void* dGU, void* Hb, float* dgp,
+                                   cudaStream_t s) {
+    if (rows_max == 0) return cudaSuccess;
+    const int grid = rows_max < 148 * 16 ? rows_max : 148 * 16;
+    launch_pdl(swiglu_backward_kernel, dim3(grid), dim3(256), 0, s, rows_max, rows_dev, F, G, U, D, gate,
+               static_cast<__nv_bfloat16*>(dGU), static_cast<__nv_bfloat16*>(Hb), dgp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_backward(int T, int E, int k, const float* probs, const int32_t* ids,
+                                   const int32_t* slot_pos, const float* gates, const float* dgp, int renormalize,
+                                   const int32_t* counts, float alpha, float dL, float* dlogits, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    launch_pdl(router_backward_kernel, dim3((T + 7) / 8), dim3(256), 0, s, T, E, k, probs, ids, slot_pos, gates, dgp,
+               renormalize, counts, alpha, dL, dlogits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_dx(int dtype, int T, int E, int d, const float* dlogits, const void* w_gate,
+                             const float* extra, float* R, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const dim3 grid((d + 255) / 256, (T + 7) / 8);
+    if (dtype == MOE_BF16)
+        launch_pdl(router_dx_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, T, E, d, dlogits,
+                   static_cast<const __nv_bfloat16*>(w_gate), extra, R);
+    else
+        launch_pdl(router_dx_kernel<float>, grid, dim3(256), 0, s, T, E, d, dlogits,
+                   static_cast<const float*>(w_gate), extra, R);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wgate_grad(int dtype, int T, int E, int d, const float* dlogits, const void* x, int nsplit,
+                              float* part, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const dim3 grid((d + 255) / 256, (E + 31) / 32, nsplit);
+    if (dtype == MOE_BF16)
+        launch_pdl(wgate_grad_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, T, E, d, dlogits,
+                   static_cast<const __nv_bfloat16*>(x), nsplit, part);
+    else
+        launch_pdl(wgate_grad_kernel<float>, grid, dim3(256), 0, s, T, E, d, dlogits, static_cast<const float*>(x),
+                   nsplit, part);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

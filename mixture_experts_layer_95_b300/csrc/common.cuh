@@ -242,6 +242,12 @@ struct GemmProblem {
     // these the fp32 scale of every weight row ([G*N]), applied per column
     const float* wscale1;
     const float* wscale2;
+    // K-grouped problem (launch_gemm_tc, ksplit 1, no offsets): group g
+    // multiplies A rows [0, M) by B rows [0, N) over the K window
+    // [kbase[g], kbase[g] + klen[g]) and writes output rows g*M .. g*M + M - 1
+    // (weight gradients: a contraction over each expert's token rows)
+    const int32_t* kbase;
+    const int32_t* klen;
 };
 
 // Tensor-core (tcgen05) path, bf16 operands, fp32 accumulate.  Runs up to two
@@ -267,6 +273,35 @@ cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int
 // weights, SwiGLU and Scale modes, split-K and gathered token rows; no split H.
 cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
                                cudaStream_t s, int ksplit, bool w8, int nt);
+
+// ---- backward pass (backward.cu) ----
+// kbase[e] = sum_{e' < e} round64(klen[e']), klen[e] = offsets[e+1] - offsets[e];
+// const_len >= 0: one window of const_len rows, writing offsets = {0, const_len}.
+cudaError_t launch_k_windows(int E, int32_t* offsets, int32_t* kbase, int32_t* klen, int const_len, cudaStream_t s);
+// bf16 rows of expert e (src rows offsets[e] + k, columns col0 .. col0 + C - 1,
+// times row_scale[row] when given) -> dst[c][kbase[e] + k], zero-filled to
+// the next multiple of 64; ncols = columns of dst to cover.
+cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, int C, int E, const int32_t* offsets,
+                                     const int32_t* kbase, const int32_t* klen, const float* row_scale, void* dst,
+                                     size_t ld_dst, int ncols, cudaStream_t s);
+// dst[b][c][col0 + r] = src[b][r][c] (bf16 out), batch of [R][C] matrices.
+cudaError_t launch_transpose_batched(int dtype, const void* src, int batch, int R, int C, void* dst, size_t ld_dst,
+                                     int col0, cudaStream_t s);
+// Per row: dGU = [g D U silu'(G) | g D silu(G)] (bf16), Hb = bf16(silu(G) U),
+// dgp[r] = sum_f D silu(G) U (when dgp != nullptr).
+cudaError_t launch_swiglu_backward(int rows_max, const int32_t* rows_dev, int F, const float* G, const float* U,
+                                   const float* D, const float* gate, void* dGU, void* Hb, float* dgp,
+                                   cudaStream_t s);
+// dlogits [T][E] from the gate gradients (via slot_pos) and the balance loss.
+cudaError_t launch_router_backward(int T, int E, int k, const float* probs, const int32_t* ids,
+                                   const int32_t* slot_pos, const float* gates, const float* dgp, int renormalize,
+                                   const int32_t* counts, float alpha, float dL, float* dlogits, cudaStream_t s);
+// R[t] = dlogits[t] W_g (+ extra[t]).
+cudaError_t launch_router_dx(int dtype, int T, int E, int d, const float* dlogits, const void* w_gate,
+                             const float* extra, float* R, cudaStream_t s);
+// part[s][e][i] = sum over token chunk s of dlogits[t][e] x[t][i].
+cudaError_t launch_wgate_grad(int dtype, int T, int E, int d, const float* dlogits, const void* x, int nsplit,
+                              float* part, cudaStream_t s);
 
 // Per-row E4M3 quantisation of a [rows][cols] bf16 or fp32 matrix (cols a
 // multiple of 16): q [rows][cols] codes, scale [rows] fp32.

@@ -88,6 +88,12 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     int part_cols[2];          // 2N for SwiGLU (gate half, then up half), N otherwise
     const float* wscale1[2];   // FP8 weights: per weight-row scale of B1 / B2 (null: bf16 weights)
     const float* wscale2[2];
+    // K-grouped problem (non-null): every group g multiplies the same A rows
+    // [0, M) by the same B rows [0, N) over its own K window [kbase[g],
+    // kbase[g] + klen[g]) (kbase a multiple of 64; the operands hold zeros up
+    // to the next multiple of 64) and writes output rows g*M .. g*M + M - 1
+    const int32_t* kbase[2];
+    const int32_t* klen[2];
     int* status;
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
     int stall_producer;      // test switch: issue no loads, so the consumers' bounded waits run out
@@ -144,6 +150,8 @@ struct Tile {
     int prob, g, m, n;
     int a_row0, rows_valid;
     int ks, kb0, kb1;  // K slice and its k-block range [kb0, kb1)
+    int out_row0;      // first output row (a_row0 except for K-grouped problems)
+    int k_off;         // K coordinate of k-block 0 (K-grouped problems: the group's window)
 };
 
 template <int MODE>
@@ -174,7 +182,14 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& 
     t.m = r - t.n * mt;
     t.a_row0 = st.row0[gb + lo] + t.m * BM;
     t.rows_valid = min(BM, rows - t.m * BM);
-    const int nk = (p.K[t.prob] + BK - 1) / BK;
+    t.out_row0 = t.a_row0;
+    t.k_off = 0;
+    int nk = (p.K[t.prob] + BK - 1) / BK;
+    if (p.kbase[t.prob]) {  // K-grouped: shared A rows, the group's own K window
+        t.out_row0 = t.g * p.M[t.prob] + t.m * BM;
+        t.k_off = __ldg(p.kbase[t.prob] + t.g);
+        nk = (__ldg(p.klen[t.prob] + t.g) + BK - 1) / BK;
+    }
     t.kb0 = t.ks * nk / p.ksplit;
     t.kb1 = (t.ks + 1) * nk / p.ksplit;
     return t;
@@ -192,7 +207,7 @@ template <int MODE>
 __device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile) {
     const int N = p.N[t.prob];
     const bool valid = row_in_tile < t.rows_valid;
-    const size_t grow = static_cast<size_t>(t.a_row0 + row_in_tile);
+    const size_t grow = static_cast<size_t>(t.out_row0 + row_in_tile);
     const size_t pc = static_cast<size_t>(p.part_cols[t.prob]);
     float* base = p.part[t.prob] + (static_cast<size_t>(t.ks) * p.a_rows[t.prob] + grow) * pc;
     float scale = 1.0f;
@@ -239,7 +254,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
     }
     const int N = p.N[t.prob];
     const bool valid = row_in_tile < t.rows_valid;
-    const size_t grow = static_cast<size_t>(t.a_row0 + row_in_tile);
+    const size_t grow = static_cast<size_t>(t.out_row0 + row_in_tile);
     if (MODE == kGemmSwiGLU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.prob]);
         __nv_bfloat16* out_lo = static_cast<__nv_bfloat16*>(p.out2[t.prob]);
@@ -308,11 +323,13 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             const int col = t.n * BN + c0;
             if (col >= N || nvalid <= 0) continue;  // uniform across the warp
             if (p.wscale1[t.prob]) apply_wscale32(v, p.wscale1[t.prob], static_cast<size_t>(t.g) * N + col, N - col);
+            // a K-grouped tile with an empty window computed nothing: its output is 0
+            const float sc = t.kb1 > t.kb0 ? scale : 0.0f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) stage[lane][i] = scale * __uint_as_float(v[i]);
+            for (int i = 0; i < 32; ++i) stage[lane][i] = t.kb1 > t.kb0 ? sc * __uint_as_float(v[i]) : 0.0f;
             __syncwarp();
             const bool col_ok = col + lane < N;
-            float* dst = out + (size_t)(t.a_row0 + wrow0) * N + col + lane;
+            float* dst = out + (size_t)(t.out_row0 + wrow0) * N + col + lane;
             for (int r = 0; r < nvalid; ++r)
                 if (col_ok) dst[(size_t)r * N] = stage[r][lane];
         }
@@ -428,7 +445,7 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
         bool dead = p.stall_producer != 0;
         for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
             const Tile t = decode_tile<MODE>(st, p, id);
-            const int b_row0 = t.g * p.N[t.prob] + t.n * out_cols_per_tile<MODE>();
+            const int b_row0 = (p.kbase[t.prob] ? 0 : t.g * p.N[t.prob]) + t.n * out_cols_per_tile<MODE>();
             const int32_t* gidx = p.a_gather[t.prob];
             int rows4[4] = {0, 0, 0, 0};
             if (gidx) {
@@ -455,13 +472,14 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                     // loaded; the other rows of the tile are never stored
                     const uint32_t a_bytes = gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : A_BYTES;
                     mbar_expect_tx(&st.full[s], SLOT - A_BYTES + a_bytes);
-                    if (!gidx) tma_load_2d(sa, &p.tmA[t.prob], kb * BK, t.a_row0, &st.full[s]);
-                    if (SC::kSplit) tma_load_2d(sa + A_BYTES, &p.tmA2[t.prob], kb * BK, t.a_row0, &st.full[s]);
+                    const int kc = t.k_off + kb * BK;
+                    if (!gidx) tma_load_2d(sa, &p.tmA[t.prob], kc, t.a_row0, &st.full[s]);
+                    if (SC::kSplit) tma_load_2d(sa + A_BYTES, &p.tmA2[t.prob], kc, t.a_row0, &st.full[s]);
                     if (MODE == kGemmSwiGLU) {
-                        tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
-                        tma_load_2d(sb + (W8 ? F8_BYTES : B_BYTES) / 2, &p.tmB2[t.prob], kb * BK, b_row0, &st.full[s]);
+                        tma_load_2d(sb, &p.tmB1[t.prob], kc, b_row0, &st.full[s]);
+                        tma_load_2d(sb + (W8 ? F8_BYTES : B_BYTES) / 2, &p.tmB2[t.prob], kc, b_row0, &st.full[s]);
                     } else {
-                        tma_load_2d(sb, &p.tmB1[t.prob], kb * BK, b_row0, &st.full[s]);
+                        tma_load_2d(sb, &p.tmB1[t.prob], kc, b_row0, &st.full[s]);
                     }
                 }
                 if (gidx && lane * 4 < t.rows_valid)
@@ -691,6 +709,8 @@ __device__ __forceinline__ Tile decode_tile_pair(const SmemTail& st, const TcPar
     const int first = t.m * 2 * BM + rank * BM;  // this CTA's first row inside the group
     t.a_row0 = st.row0[gb + lo] + first;
     t.rows_valid = min(BM, rows - first);  // may be <= 0 for the upper half of a tail tile
+    t.out_row0 = t.a_row0;
+    t.k_off = 0;
     t.kb0 = 0;
     t.kb1 = (p.K[t.prob] + BK - 1) / BK;
     return t;
@@ -973,8 +993,10 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         } else if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) {
             return cudaErrorInvalidValue;
         }
-        if (!make_tmap(&prm.tmB1[q], g.B1, g.G * g.N, g.K, b_box)) return cudaErrorInvalidValue;
-        if (mode == kGemmSwiGLU && !make_tmap(&prm.tmB2[q], g.B2, g.G * g.N, g.K, b_box))
+        // B rows: one [N][K] matrix per group, or one shared by every group (K-grouped)
+        const int b_rows = g.kbase ? g.N : g.G * g.N;
+        if (!make_tmap(&prm.tmB1[q], g.B1, b_rows, g.K, b_box)) return cudaErrorInvalidValue;
+        if (mode == kGemmSwiGLU && !make_tmap(&prm.tmB2[q], g.B2, b_rows, g.K, b_box))
             return cudaErrorInvalidValue;
         if (mode == kGemmScaleSplit && !make_tmap(&prm.tmA2[q], g.A2, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
         if (ksplit > 1) {
@@ -992,6 +1014,12 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         prm.N[q] = g.N;
         prm.K[q] = g.K;
         prm.a_rows[q] = g.a_rows;
+        if (g.kbase || g.klen) {
+            if (!g.kbase || !g.klen || g.offsets || g.a_gather || ksplit != 1 || pair || mode != kGemmPlain)
+                return cudaErrorInvalidValue;
+            prm.kbase[q] = g.kbase;
+            prm.klen[q] = g.klen;
+        }
     }
     prm.nprob = nprob;
     prm.status = status;

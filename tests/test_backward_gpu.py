@@ -1,0 +1,116 @@
+"""Backward pass on the GPU vs the fp64 oracle's backward, through the C ABI (GPU only).
+
+moe_backward recomputes the routing and grouping with the forward kernels; the
+oracle takes those same ids (and dropped slots) and differentiates the layer in
+fp64 (pinned to autograd and finite differences in test_oracle_backward.py).
+dx and dW_g must satisfy max |g_gpu - g_oracle| <= 2e-2 * RMS(g_oracle), the
+forward pass's bf16 rule.  The expert weight gradients are sums over an
+expert's token rows of products of two operands the GPU rounds to bf16 (dG or
+dU with x; g*dy with h): each term carries up to 2u = 2^-7 relative error, so an
+entry made of few large terms can miss by several percent of the tensor's RMS
+while the tensor as a whole is accurate to ~u/2.  They are therefore checked
+norm-wise, expert by expert: ||g_gpu - g_oracle||_F <= 2e-2 ||g_oracle||_F for
+every expert's block (an expert with no tokens must give exactly 0), which
+still fails on any block computed from wrong rows or windows.  Covers ragged
+tiles and K windows, the shared expert, a capacity cut, selection and logit
+biases, both gate normalisations, the logits-GEMM router and a one-token batch.
+"""
+import json
+
+import numpy as np
+import pytest
+import torch
+
+from moe_inputs import Workload
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+CASES = [
+    Workload("bwd_basic", T=300, d=256, E=8, F=384, k=2),
+    Workload("bwd_shared_capacity_biases", T=200, d=256, E=16, F=256, k=2, n_shared=1, F_s=192, capacity=20,
+             select_bias=True, zipf_s=1.2),
+    Workload("bwd_plain_gates", T=130, d=128, E=4, F=128, k=2, renormalize=False),
+    Workload("bwd_gemm_router", T=300, d=128, E=40, F=128, k=4),
+    Workload("bwd_one_token_shared", T=1, d=256, E=8, F=256, k=2, n_shared=1, F_s=128),
+]
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mixture_experts_layer_95_b300 as moe
+    moe.lib()
+    return torch.device("cuda")
+
+
+def check_backward(w, dL=2.0):
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    import oracle
+    from tests._parity import layer_of
+    layer = layer_of(w)
+    L = moe_inputs.make_layer(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(1234)
+    dy = torch.randn((w.T, w.d), generator=g, device="cuda").to(layer.torch_dtype)
+    G = moe.backward(layer, L["x"], L["w_gate"], L["w1"], L["w3"], L["w2"], dy, L["logit_bias"], L["select_bias"],
+                     L["ws1"], L["ws3"], L["ws2"], dL=dL)
+    ids, gates, _ = moe.route(layer, L["x"], L["w_gate"], L["logit_bias"], L["select_bias"])
+    grp = moe.permute(layer, ids, gates, L["x"])
+    torch.cuda.synchronize()
+    Ln = moe_inputs.layer_numpy(L)
+    ref = oracle.backward(Ln, w.k, ids.cpu().numpy(), grp["slot_pos"].cpu().numpy(),
+                          oracle.widen(moe_inputs.to_numpy(dy)), w.renormalize, w.alpha, dL)
+    rep = dict(workload=w.name, dropped=int(grp["n_dropped"].item()))
+    ok = True
+    for name in G:
+        a = G[name].double().cpu().numpy()
+        b = ref[name]
+        finite = bool(np.isfinite(a).all())
+        if name in ("dx", "dw_gate"):
+            rms = float(np.sqrt(np.mean(b ** 2)))
+            rel = float(np.abs(a - b).max()) / rms if rms > 0 else float(np.abs(a).max())
+            rep[name] = dict(max_rel=rel, finite=finite)
+        else:  # per expert block (the shared expert's matrices are one block)
+            blocks_a = a if name in ("dw1", "dw3", "dw2") else a[None]
+            blocks_b = b if name in ("dw1", "dw3", "dw2") else b[None]
+            rel = 0.0
+            for ea, eb in zip(blocks_a, blocks_b):
+                nb = float(np.linalg.norm(eb))
+                r = float(np.linalg.norm(ea - eb)) / nb if nb > 0 else (0.0 if not ea.any() else float("inf"))
+                rel = max(rel, r)
+            rep[name] = dict(block_fro_rel=rel, finite=finite)
+        ok = ok and rel <= TOL and finite
+    rep["ok"] = bool(ok)
+    return rep
+
+
+@pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
+def test_backward_matches_oracle(cuda, w):
+    rep = check_backward(w)
+    assert rep["ok"], json.dumps(rep, indent=1)
+
+
+def test_backward_is_deterministic(cuda):
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    from tests._parity import layer_of
+    w = CASES[1]
+    layer = layer_of(w)
+    L = moe_inputs.make_layer(w, "cuda")
+    dy = torch.ones((w.T, w.d), device="cuda", dtype=layer.torch_dtype)
+    args = (layer, L["x"], L["w_gate"], L["w1"], L["w3"], L["w2"], dy, L["logit_bias"], L["select_bias"], L["ws1"],
+            L["ws3"], L["ws2"])
+    a = moe.backward(*args, dL=1.0)
+    b = moe.backward(*args, dL=1.0)
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+
+
+def test_backward_rejects_fp32_and_expert_choice(cuda):
+    import mixture_experts_layer_95_b300 as moe
+    for layer in (moe.Layer(T=4, d=64, E=4, k=2, d_ff=64, dtype="f32"),
+                  moe.Layer(T=4, d=64, E=4, k=2, d_ff=64, routing="expert")):
+        assert moe.lib().moe_backward_workspace_size(__import__("ctypes").byref(layer.cfg())) == 0
