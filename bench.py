@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (moe_backward) instead of the forward layer")
     return ap.parse_args(argv)
 
 
@@ -488,10 +490,72 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_backward(args):
+    """Times moe_backward on the workload (one process, this GPU): gradients of
+    <dy, y> + dL * L_balance for every input; reports tokens/s and the
+    backward's algorithmic TFLOP/s (twice the forward's expert FLOPs: the dX and
+    the weight-gradient products; the recomputed forward up projection is not
+    counted as work)."""
+    import torch
+
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    from mixture_experts_layer_95_b300 import _build
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    w = moe_inputs.WORKLOADS[args.workload]
+    layer = layer_of(w)
+    L = moe_inputs.make_layer(w, dev)
+    g = torch.Generator(device=dev).manual_seed(1234)
+    dy = torch.randn((w.T, w.d), generator=g, device=dev).to(layer.torch_dtype)
+    bw = moe.Backward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
+                      L["ws3"], L["ws2"], device=dev)
+    for _ in range(args.warmup):
+        bw(L["x"], dy, 1.0)
+    torch.cuda.synchronize(dev)
+    st = bw.device_status()
+    if st != 0:
+        raise moe.MoeError(st, "backward warm-up device status")
+    launches0 = moe.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        bw(L["x"], dy, 1.0)
+    e1.record()
+    e1.synchronize()
+    launches = moe.launch_count() - launches0
+    ms = e0.elapsed_time(e1) / args.steps
+    st = bw.device_status()
+    if st != 0:
+        raise moe.MoeError(st, "backward device status")
+    kept = w.T * w.k if w.capacity < 0 else None
+    if kept is None:  # count the kept entries the routing actually produced
+        lay = layer
+        ids, gates, _ = moe.route(lay, L["x"], L["w_gate"], L["logit_bias"], L["select_bias"])
+        kept = int(moe.permute(lay, ids, gates, L["x"])["kept"].sum().item())
+    fwd_expert = 2.0 * moe_inputs.expert_params(w.d, w.F) * kept + \
+        2.0 * moe_inputs.expert_params(w.d, w.F_s) * w.T * w.n_shared
+    tflops = 2.0 * fwd_expert / (ms / 1e3) / 1e12
+    peaks, src = load_peaks()
+    out = {"metric": "MoE-layer backward tokens/s on 1 B300 (gradients of every input)", "value": round(w.T / (ms / 1e3), 1),
+           "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+           "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F,
+                      "n_shared": w.n_shared, "capacity": w.capacity},
+           "backward": {"algorithmic_tflop_per_step": round(2.0 * fwd_expert / 1e12, 4), "tflops": round(tflops, 1),
+                        "frac_bf16_peak": round(tflops / peaks["bf16_tflops"], 4), "peak_source": src},
+           "gpu_launches": int(launches)}
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.backward:
+        run_backward(args)
     else:
         run_ours(args)
 

@@ -521,6 +521,44 @@ def backward(layer: Layer, x, w_gate, w1, w3, w2, dy, logit_bias=None, select_bi
     return out
 
 
+class Backward:
+    """Reusable moe_backward call (preallocated workspace and gradient
+    buffers): the form the benchmark times."""
+
+    def __init__(self, layer: Layer, w_gate, w1, w3, w2, logit_bias=None, select_bias=None, ws1=None, ws3=None,
+                 ws2=None, device=None):
+        dev = device or w1.device
+        self.layer, self.cfg = layer, layer.cfg()
+        E, F, d, T, Fs = layer.E, layer.d_ff, layer.d, layer.T, layer.d_ff_shared
+        nbytes = lib().moe_backward_workspace_size(ctypes.byref(self.cfg))
+        if nbytes == 0:
+            raise MoeError(-2, "moe_backward_workspace_size")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        _check(lib().moe_workspace_init(ctypes.byref(self.cfg), _ptr(self.ws), self.ws.numel(), _stream(None)),
+               "moe_workspace_init")
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.grads = dict(dx=torch.empty((T, d), **f32), dw_gate=torch.empty((E, d), **f32),
+                          dw1=torch.empty((E, F, d), **f32), dw3=torch.empty((E, F, d), **f32),
+                          dw2=torch.empty((E, d, F), **f32))
+        if layer.n_shared:
+            self.grads.update(dws1=torch.empty((Fs, d), **f32), dws3=torch.empty((Fs, d), **f32),
+                              dws2=torch.empty((d, Fs), **f32))
+        self.w = (w_gate, logit_bias, select_bias, w1, w3, w2, ws1, ws3, ws2)
+
+    def __call__(self, x, dy, dL: float = 0.0, stream=None):
+        wg, lb, sb, w1, w3, w2, s1, s3, s2 = (_ptr(t) for t in self.w)
+        g = self.grads
+        _check(lib().moe_backward(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(dy),
+                                  ctypes.c_float(dL), _ptr(g["dx"]), _ptr(g["dw_gate"]), _ptr(g["dw1"]),
+                                  _ptr(g["dw3"]), _ptr(g["dw2"]), _ptr(g.get("dws1")), _ptr(g.get("dws3")),
+                                  _ptr(g.get("dws2")), _ptr(self.ws), self.ws.numel(), _stream(stream)),
+               "moe_backward")
+        return g
+
+    def device_status(self, stream=None) -> int:
+        return last_device_status(self.layer, self.ws, stream)
+
+
 class Forward:
     """Reusable moe_forward call: checks the weights once, owns the workspace,
     and enqueues the whole layer per call (the form the benchmark times)."""
