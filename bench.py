@@ -39,7 +39,8 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s on 1 B300; % of bf16 tensor peak or HBM roofline"
 UNIT = "tokens/s"
 FALLBACK = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0)
-TC_SOURCE = os.path.join(ROOT, "mixture_experts_layer_95_b300", "csrc", "gemm_tc.cu")
+# sources of the tensor-core GEMM kernel whose DRAM traffic profiles/traffic.json records
+TC_SOURCES = [os.path.join(ROOT, "mixture_experts_layer_95_b300", "csrc", f) for f in ("gemm_tc.cu", "tc_ptx.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -88,9 +89,12 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
-def source_hash(path=TC_SOURCE):
-    with open(path, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+def source_hash(paths=TC_SOURCES):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload):
