@@ -47,9 +47,31 @@ __global__ void k_windows_kernel(int E, int32_t* __restrict__ offsets, int32_t* 
     pdl_trigger();
 }
 
+// 64 x 64 bf16 tiles are staged in shared memory with a 2-element row pad:
+// loads and stores move 16-byte chunks (8 elements), and the column gathers of
+// the store phase hit distinct banks.
+constexpr int TPAD = TT + 2;
+
+__device__ __forceinline__ void put8(uint16_t* row, const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        row[2 * j] = (uint16_t)(w[j] & 0xFFFFu);
+        row[2 * j + 1] = (uint16_t)(w[j] >> 16);
+    }
+}
+
+__device__ __forceinline__ uint4 gather8(const uint16_t (*tile)[TPAD], int r0, int c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = (uint32_t)tile[r0 + 2 * j][c] | ((uint32_t)tile[r0 + 2 * j + 1][c] << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // dst[c][kbase[e] + k] = scale(row) * src[(offsets[e] + k) * ld_src + col0 + c] for
 // k < klen[e], 0 for klen[e] <= k < round64(klen[e]); c < C.  One 64 x 64 tile per
-// block: a block's 64 destination columns lie inside one expert's window.
+// block: a block's 64 destination columns lie inside one expert's window.  C,
+// ld_src, col0 and ld_dst are multiples of 8 (16-byte chunks).
 __global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloat16* __restrict__ src, size_t ld_src,
                                                                 int col0, int C, int E,
                                                                 const int32_t* __restrict__ offsets,
@@ -59,7 +81,7 @@ __global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloa
                                                                 __nv_bfloat16* __restrict__ dst, size_t ld_dst,
                                                                 int ncols) {
     pdl_wait();
-    __shared__ float tile[TT][TT + 1];
+    __shared__ uint16_t tile[TT][TPAD];
     const int c_tile = blockIdx.x * TT;  // source column block
     const int k0 = blockIdx.y * TT;      // destination column block
     if (k0 < ncols) {
@@ -74,23 +96,33 @@ __global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloa
         const int padded = (len + 63) / 64 * 64;
         if (k0 < base + padded) {  // beyond the last window: nothing to write
             const int row_base = __ldg(offsets + e) + (k0 - base);
-            // load: threads walk 64 source rows x 64 columns, columns fastest
-            for (int i = threadIdx.x; i < TT * TT; i += blockDim.x) {
-                const int kk = i / TT, cc = i % TT;
-                const int k = k0 - base + kk;
-                float v = 0.f;
-                if (k < len && c_tile + cc < C) {
+            // load: 64 source rows x 8 chunks of 8 columns
+            for (int i = threadIdx.x; i < TT * 8; i += blockDim.x) {
+                const int kk = i >> 3, ch = i & 7;
+                const int k = k0 - base + kk, c = c_tile + ch * 8;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (k < len && c < C) {
                     const size_t r = (size_t)(row_base + kk);
-                    v = bf2f(src[r * ld_src + col0 + c_tile + cc]);
-                    if (row_scale) v *= __ldg(row_scale + r);
+                    v = __ldg(reinterpret_cast<const uint4*>(src + r * ld_src + col0 + c));
+                    if (row_scale) {
+                        const float sc = __ldg(row_scale + r);
+                        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 f = __bfloat1622float2(h[j]);
+                            h[j] = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+                        }
+                    }
                 }
-                tile[kk][cc] = v;
+                put8(&tile[kk][ch * 8], v);
             }
             __syncthreads();
-            // store: 64 destination rows (source columns) x 64 columns, columns fastest
-            for (int i = threadIdx.x; i < TT * TT; i += blockDim.x) {
-                const int cc = i / TT, kk = i % TT;
-                if (c_tile + cc < C) dst[(size_t)(c_tile + cc) * ld_dst + k0 + kk] = __float2bfloat16_rn(tile[kk][cc]);
+            // store: 64 destination rows (source columns) x 8 chunks of 8 window columns
+            for (int i = threadIdx.x; i < TT * 8; i += blockDim.x) {
+                const int cc = i >> 3, ch = i & 7;
+                if (c_tile + cc < C)
+                    *reinterpret_cast<uint4*>(dst + (size_t)(c_tile + cc) * ld_dst + k0 + ch * 8) =
+                        gather8(tile, ch * 8, cc);
             }
         }
     }
@@ -98,33 +130,30 @@ __global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloa
     pdl_trigger();
 }
 
-// dst[b][c][col0 + r] = src[b][r][c]: batch of [R][C] matrices (weights) into
-// [C][ld_dst] rows, at column offset col0.
-template <typename T>
-__global__ void __launch_bounds__(256) transpose_batched_kernel(const T* __restrict__ src, int R, int C,
+// dst[b][c][col0 + r] = src[b][r][c]: batch of [R][C] bf16 matrices (weights)
+// into [C][ld_dst] rows at column offset col0; R, C, ld_dst, col0 multiples of 8.
+__global__ void __launch_bounds__(256) transpose_batched_kernel(const __nv_bfloat16* __restrict__ src, int R, int C,
                                                                 __nv_bfloat16* __restrict__ dst, size_t ld_dst,
                                                                 int col0) {
     pdl_wait();
-    __shared__ float tile[TT][TT + 1];
+    __shared__ uint16_t tile[TT][TPAD];
     const int b = blockIdx.z;
     const int c_tile = blockIdx.x * TT, r_tile = blockIdx.y * TT;
-    const T* s = src + (size_t)b * R * C;
+    const __nv_bfloat16* s = src + (size_t)b * R * C;
     __nv_bfloat16* d = dst + (size_t)b * C * ld_dst;
-    for (int i = threadIdx.x; i < TT * TT; i += blockDim.x) {
-        const int rr = i / TT, cc = i % TT;
-        float v = 0.f;
-        if (r_tile + rr < R && c_tile + cc < C) {
-            const T w = s[(size_t)(r_tile + rr) * C + c_tile + cc];
-            if constexpr (sizeof(T) == 2) v = bf2f(w);
-            else v = w;
-        }
-        tile[rr][cc] = v;
+    for (int i = threadIdx.x; i < TT * 8; i += blockDim.x) {
+        const int rr = i >> 3, ch = i & 7;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r_tile + rr < R && c_tile + ch * 8 < C)
+            v = __ldg(reinterpret_cast<const uint4*>(s + (size_t)(r_tile + rr) * C + c_tile + ch * 8));
+        put8(&tile[rr][ch * 8], v);
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < TT * TT; i += blockDim.x) {
-        const int cc = i / TT, rr = i % TT;
-        if (r_tile + rr < R && c_tile + cc < C)
-            d[(size_t)(c_tile + cc) * ld_dst + col0 + r_tile + rr] = __float2bfloat16_rn(tile[rr][cc]);
+    for (int i = threadIdx.x; i < TT * 8; i += blockDim.x) {
+        const int cc = i >> 3, ch = i & 7;
+        if (c_tile + cc < C && r_tile + ch * 8 < R)
+            *reinterpret_cast<uint4*>(d + (size_t)(c_tile + cc) * ld_dst + col0 + r_tile + ch * 8) =
+                gather8(tile, ch * 8, cc);
     }
     __syncthreads();
     pdl_trigger();
@@ -313,6 +342,7 @@ cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, i
                                      const int32_t* kbase, const int32_t* klen, const float* row_scale, void* dst,
                                      size_t ld_dst, int ncols, cudaStream_t s) {
     if (C == 0 || ncols == 0) return cudaSuccess;
+    if (C % 8 || ld_src % 8 || col0 % 8 || ld_dst % 8 || ncols % 64) return cudaErrorInvalidValue;
     const dim3 grid((C + TT - 1) / TT, (ncols + TT - 1) / TT);
     launch_pdl(transpose_windows_kernel, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), ld_src, col0,
                C, E, offsets, kbase, klen, row_scale, static_cast<__nv_bfloat16*>(dst), ld_dst, ncols);
@@ -322,13 +352,10 @@ cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, i
 cudaError_t launch_transpose_batched(int dtype, const void* src, int batch, int R, int C, void* dst, size_t ld_dst,
                                      int col0, cudaStream_t s) {
     if (batch == 0 || R == 0 || C == 0) return cudaSuccess;
+    if (dtype != MOE_BF16 || R % 8 || C % 8 || ld_dst % 8 || col0 % 8) return cudaErrorInvalidValue;
     const dim3 grid((C + TT - 1) / TT, (R + TT - 1) / TT, batch);
-    if (dtype == MOE_BF16)
-        launch_pdl(transpose_batched_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
-                   static_cast<const __nv_bfloat16*>(src), R, C, static_cast<__nv_bfloat16*>(dst), ld_dst, col0);
-    else
-        launch_pdl(transpose_batched_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(src), R, C,
-                   static_cast<__nv_bfloat16*>(dst), ld_dst, col0);
+    launch_pdl(transpose_batched_kernel, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), R, C,
+               static_cast<__nv_bfloat16*>(dst), ld_dst, col0);
     return cudaGetLastError();
 }
 
