@@ -158,7 +158,7 @@ Splits choose_splits(const moe_config& c, bool w8 = false) {
 struct Layout {
     size_t status, topk_ids, gates, p_part, block_hist, counts, kept, offsets, n_dropped, sorted, slot_pos,
         gates_perm, p_mean, f, L, logits, probs, x_perm, h, h_shared, h_lo, h_shared_lo, y_perm, y_shared, part_up,
-        part_up_shared, part_dn, part_dn_shared, total;
+        part_up_shared, part_dn, part_dn_shared, xq, xq_s, hq, hq_s, hsq, hsq_s, total;
 };
 
 Layout layout(const moe_config& c) {
@@ -208,6 +208,15 @@ Layout layout(const moe_config& c) {
     l.part_up_shared = take(c.n_shared ? 4 * su * (size_t)c.T * 2 * c.d_ff_shared : 0);
     l.part_dn = take(4 * sd * n * c.d);
     l.part_dn_shared = take(c.n_shared ? 4 * sd * (size_t)c.T * c.d : 0);
+    // decode-sized batches with FP8 weights: the tokens and H as E4M3 hi/lo
+    // code pairs with a scale per row (the FP8 MMA takes FP8 on both sides)
+    const bool q8 = use_decode_gemm(c);
+    l.xq = take(q8 ? 2 * (size_t)c.T * c.d : 0);
+    l.xq_s = take(q8 ? 4 * (size_t)c.T : 0);
+    l.hq = take(q8 ? 2 * n * c.d_ff : 0);
+    l.hq_s = take(q8 ? 4 * n : 0);
+    l.hsq = take(q8 && c.n_shared ? 2 * (size_t)c.T * c.d_ff_shared : 0);
+    l.hsq_s = take(q8 && c.n_shared ? 4 * (size_t)c.T : 0);
     l.total = off;
     return l;
 }
@@ -507,9 +516,28 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
         down[1].wscale1 = w8->ss2;
     }
     int* status = at<int>(ws, L.status);
+    // FP8 decode GEMMs read the tokens (and H) as E4M3 hi/lo codes: x -> xq
+    // here, H -> hq between the two GEMMs
+    const bool q8 = w8 && use_decode_gemm(c);
+    uint8_t* xq = q8 ? at<uint8_t>(ws, L.xq) : nullptr;
+    uint8_t* hq = q8 ? at<uint8_t>(ws, L.hq) : nullptr;
+    uint8_t* hsq = q8 && c.n_shared ? at<uint8_t>(ws, L.hsq) : nullptr;
+    if (q8) {
+        for (int q = 0; q < np; ++q) {
+            up[q].A = xq;
+            up[q].A2 = xq + (size_t)c.T * c.d;
+            up[q].a_scale = at<float>(ws, L.xq_s);
+            down[q].A = q == 0 ? hq : hsq;
+            down[q].A2 = q == 0 ? hq + (size_t)n * c.d_ff : hsq + (size_t)c.T * c.d_ff_shared;
+            down[q].a_scale = at<float>(ws, q == 0 ? L.hq_s : L.hsq_s);
+        }
+    }
     {
         StageScope scope(kStageUp, s);
         if (use_decode_gemm(c)) {
+            if (q8)
+                MOE_LAUNCH(launch_split_e4m3(c.T, c.d, x, nullptr, xq, xq + (size_t)c.T * c.d, at<float>(ws, L.xq_s),
+                                             s));
             MOE_LAUNCH(launch_gemm_decode(kGemmSwiGLU, up, np, status, sms, s, sp.up, w8 != nullptr,
                                           decode_tile_rows(c)));
             if (sp.up > 1) {
@@ -539,6 +567,13 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     {
         StageScope scope(kStageDown, s);
         if (use_decode_gemm(c)) {
+            if (q8) {
+                MOE_LAUNCH(launch_split_e4m3(n, c.d_ff, h, offsets + c.E, hq, hq + (size_t)n * c.d_ff,
+                                             at<float>(ws, L.hq_s), s));
+                if (c.n_shared)
+                    MOE_LAUNCH(launch_split_e4m3(c.T, c.d_ff_shared, hs, nullptr, hsq,
+                                                 hsq + (size_t)c.T * c.d_ff_shared, at<float>(ws, L.hsq_s), s));
+            }
             MOE_LAUNCH(launch_gemm_decode(kGemmScale, down, np, status, sms, s, sp.down, w8 != nullptr,
                                           decode_tile_rows(c)));
             if (sp.down > 1 && reduce_down) {

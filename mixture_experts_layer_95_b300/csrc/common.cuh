@@ -242,6 +242,10 @@ struct GemmProblem {
     // these the fp32 scale of every weight row ([G*N]), applied per column
     const float* wscale1;
     const float* wscale2;
+    // FP8 tokens (launch_gemm_decode with w8): A holds the hi and A2 the lo
+    // E4M3 codes of every token row, a_scale its power-of-two scale (indexed
+    // like the rows of A, or of the gather source), A row = a_scale * (hi + lo)
+    const float* a_scale;
     // K-grouped problem (launch_gemm_tc, ksplit 1, no offsets): group g
     // multiplies A rows [0, M) by B rows [0, N) over the K window
     // [kbase[g], kbase[g] + klen[g]) and writes output rows g*M .. g*M + M - 1
@@ -307,6 +311,13 @@ cudaError_t launch_wgate_grad(int dtype, int T, int E, int d, const float* dlogi
 // multiple of 16): q [rows][cols] codes, scale [rows] fp32.
 cudaError_t launch_quantize_fp8(int dtype, long long rows, int cols, const void* w, uint8_t* q, float* scale,
                                 cudaStream_t s);
+
+// bf16 rows [rows][K] (K a multiple of 8) -> E4M3 hi and lo code rows and a
+// power-of-two scale per row, row = scale * (hi + lo) (exact for entries
+// within 2^10 of the row's largest magnitude); rows at or beyond *live_rows
+// (nullable) are skipped.  Feeds the FP8 tensor-core path of the decode GEMM.
+cudaError_t launch_split_e4m3(int rows, int K, const void* x, const int32_t* live_rows, uint8_t* hi, uint8_t* lo,
+                              float* scale, cudaStream_t s);
 
 // H[r][f] = silu(sum_s P[s][r][f]) * sum_s P[s][r][N + f] (bf16, and the lo
 // half when h_lo != nullptr) for r < rows, rows = *rows_dev when non-null.

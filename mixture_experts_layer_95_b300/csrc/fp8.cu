@@ -16,6 +16,7 @@
 // quantize_fp8_kernel: one warp per row, 16-byte loads; the row's maximum is
 // a warp reduction, then the same warp re-reads the row (from L1/L2) and
 // writes 8 codes per lane per step.
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -80,7 +81,83 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(long long rows, int c
     pdl_trigger();
 }
 
+// split_e4m3_kernel: one block per row of a bf16 matrix [rows][K] (K a
+// multiple of 8).  The FP8 tensor-core MMA (kind::f8f6f4) takes FP8 on both
+// operands, so a bf16 row x that meets FP8 weights is carried as two E4M3
+// code rows and a power-of-two scale,  x = s * (hi + lo):
+//   s  = 2^(e - 8) with max|x| = m * 2^e, m in [0.5, 1)  (1 for a zero row),
+//        so |x| / s < 256 and the division by s is exact;
+//   hi = E4M3(x / s), lo = E4M3(x / s - hi), both rounded to nearest even.
+// hi keeps the top 4 significant bits of x / s and the remainder has at most
+// 4 more (a bf16 value has 8), so hi + lo == x / s exactly whenever lo stays
+// at or above E4M3's smallest step 2^-9, i.e. for every |x| >= max|x| * 2^-10;
+// smaller entries carry an absolute error of at most s * 2^-10 <= max|x| *
+// 2^-17.  Rows at or beyond *live_rows (when given) are skipped.
+constexpr int kSplitThreads = 256;
+
+__global__ void __launch_bounds__(kSplitThreads) split_e4m3_kernel(int K, const __nv_bfloat16* __restrict__ x,
+                                                                   const int32_t* __restrict__ live_rows,
+                                                                   uint8_t* __restrict__ hi, uint8_t* __restrict__ lo,
+                                                                   float* __restrict__ scale) {
+    __shared__ float s_max[kSplitThreads / 32];
+    pdl_wait();
+    const int row = blockIdx.x;
+    if (!live_rows || row < __ldg(live_rows)) {
+        const __nv_bfloat16* src = x + (size_t)row * K;
+        float amax = 0.f;
+        for (int c = threadIdx.x * 8; c < K; c += kSplitThreads * 8) {
+            float v[8];
+            load8<__nv_bfloat16>(src + c, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        }
+        amax = warp_max(amax);
+        if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = amax;
+        __syncthreads();
+        amax = s_max[0];
+#pragma unroll
+        for (int w = 1; w < kSplitThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
+        int e = 8;  // zero row: s = 1
+        if (amax > 0.f) frexpf(amax, &e);
+        // 1/s = 2^(8 - e) as two factors, each inside the fp32 range
+        const int sh = 8 - e, sh1 = sh / 2, sh2 = sh - sh1;
+        const float f1 = ldexpf(1.0f, sh1), f2 = ldexpf(1.0f, sh2);
+        if (threadIdx.x == 0) scale[row] = ldexpf(1.0f, e - 8);
+        uint8_t* dh = hi + (size_t)row * K;
+        uint8_t* dl = lo + (size_t)row * K;
+        for (int c = threadIdx.x * 8; c < K; c += kSplitThreads * 8) {
+            float v[8];
+            load8<__nv_bfloat16>(src + c, v);
+            uint32_t h[2] = {0u, 0u}, l[2] = {0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const float2 a = make_float2(v[i] * f1 * f2, v[i + 1] * f1 * f2);
+                const __nv_fp8x2_storage_t hc = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hc, __NV_E4M3);
+                const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                const float2 r = make_float2(a.x - hv.x, a.y - hv.y);
+                const __nv_fp8x2_storage_t lc = __nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
+                h[i >> 2] |= (uint32_t)hc << (16 * ((i >> 1) & 1));
+                l[i >> 2] |= (uint32_t)lc << (16 * ((i >> 1) & 1));
+            }
+            *reinterpret_cast<uint2*>(dh + c) = make_uint2(h[0], h[1]);
+            *reinterpret_cast<uint2*>(dl + c) = make_uint2(l[0], l[1]);
+        }
+    }
+    __syncthreads();
+    pdl_trigger();
+}
+
 }  // namespace
+
+cudaError_t launch_split_e4m3(int rows, int K, const void* x, const int32_t* live_rows, uint8_t* hi, uint8_t* lo,
+                              float* scale, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    if (K % 8 != 0) return cudaErrorInvalidValue;
+    launch_pdl(split_e4m3_kernel, dim3((unsigned)rows), dim3(kSplitThreads), 0, s, K,
+               static_cast<const __nv_bfloat16*>(x), live_rows, hi, lo, scale);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_fp8(int dtype, long long rows, int cols, const void* w, uint8_t* q, float* scale,
                                 cudaStream_t s) {

@@ -10,19 +10,26 @@
 // would waste most of every stage on absent rows, so the operands swap:
 // 128-row slices of the weight tile are the MMA's A operand (M = 128 weight
 // rows, one TMEM lane each) and NT token rows its B operand (N = NT), i.e.
-// D^T = W X^T.  A stage then holds a 256-row weight tile (32 KB in bf16, 16 KB
-// as FP8 codes) plus NT token rows (NT * 128 bytes), so 5 to 7 stages -- 160
-// KB of bf16 or 112 KB of FP8 weights -- stay in flight per SM.  The epilogue
-// runs along the weight-row axis: the 32 lanes of a warp hold 32 consecutive
-// output columns, so every store of one token row is one contiguous segment.
+// D^T = W X^T.  A stage then holds a 256-row weight tile with 128-byte rows
+// (32 KB: 64 bf16 or 128 FP8 codes of K per row) plus its NT token rows, so
+// 4 to 6 stages -- 128 to 192 KB of weights -- stay in flight per SM.  The
+// epilogue runs along the weight-row axis: the 32 lanes of a warp hold 32
+// consecutive output columns, so every store of one token row is one
+// contiguous segment.
+//
+// FP8 (E4M3) weights go to the tensor cores as they are (kind::f8f6f4, no
+// widening pass); the token operand then has to be FP8 too, so every bf16
+// token row arrives split as  x = s * (hi + lo)  with hi and lo E4M3 codes and
+// s a power of two per row (split_e4m3 in fp8.cu), and each K step is two MMAs
+// (hi, then lo) into the same accumulator.  The epilogue multiplies column j
+// by s of its token row and row m by the weight row's scale.
 //
 // Roles: warp 0 TMA producer (weight tile + token rows, gathered with
 // tile::gather4 when the rows come straight from the token matrix); warp 1
-// TMEM allocation and the single MMA-issuing thread (two M=128 MMAs per
-// K=16 step, one per half of the weight tile); warps 2-5 epilogue; with FP8
-// weights, warps 6-13 widen each one-byte weight tile into a bf16 tile (two
-// buffers) before the MMA reads it.  Split-K, per-row gates, FP8 per-channel
-// scales and the bounded mbarrier waits are as in gemm_tc.cu.
+// TMEM allocation and the single MMA-issuing thread (two M=128 MMAs per K
+// step, one per half of the weight tile; four with FP8 tokens); warps 2-5
+// epilogue.  Split-K, per-row gates, FP8 per-channel scales and the bounded
+// mbarrier waits are as in gemm_tc.cu.
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -33,23 +40,21 @@ namespace {
 using namespace tc;
 
 constexpr int WR = 256;                  // weight rows per tile (SwiGLU: 128 of W1 + 128 of W3)
-constexpr int WB16 = WR * BK * 2;        // bf16 weight tile bytes (one k-block of 64)
-// A stage carries KPS k-blocks: 1 for bf16 weights; 2 for FP8, so that every
-// weight row of a stage is 128 contiguous bytes, as for bf16 (a 64-byte row
-// per TMA request halves the bytes each request brings in).
+// A stage carries KPS k-blocks of 64: 1 for bf16 weights; 2 for FP8, so that
+// every weight row of a stage is 128 contiguous bytes (one 128-byte swizzle
+// row, one full TMA row request) in both cases.
 template <bool W8>
 constexpr int kps() {
     return W8 ? 2 : 1;
 }
 constexpr int DEC_THREADS = 192;         // producer, MMA, 4 epilogue warps
-constexpr int DEC_W8_THREADS = 192 + 256;  // + 8 widening warps
-constexpr int DEC_WIDE = 2;              // widened bf16 weight tiles (FP8)
 constexpr int DEC_MAX_RING = 8;
 constexpr int DEC_TMEM_COLS = 256;       // two accumulators of 2 x NT columns (NT <= 64)
 constexpr int MAX_GROUPS = kMaxExperts;
 
 struct DecParams {  // CUtensorMap members carry their own 64-byte alignment
-    CUtensorMap tmX[2];   // token rows: a gather map (one-row box) or a tile map (NT-row box)
+    CUtensorMap tmX[2];   // token rows: a gather map (one-row box) or a tile map (NT-row box); FP8: hi codes
+    CUtensorMap tmXlo[2]; // FP8: lo codes, same geometry
     CUtensorMap tmW1[2];  // weights: W1 (SwiGLU) or W2 (down)
     CUtensorMap tmW2[2];  // W3 (SwiGLU)
     const int32_t* offsets[2];
@@ -58,6 +63,7 @@ struct DecParams {  // CUtensorMap members carry their own 64-byte alignment
     const float* wscale1[2];
     const float* wscale2[2];
     const int32_t* x_gather[2];
+    const float* x_scale[2];  // FP8: power-of-two scale of every token row (indexed like the token matrix)
     int G[2], M[2], N[2], K[2], x_rows[2], x_src_rows[2];
     float* part[2];
     int part_cols[2];
@@ -70,8 +76,6 @@ struct DecParams {  // CUtensorMap members carry their own 64-byte alignment
 struct DecTail {
     uint64_t full[DEC_MAX_RING];
     uint64_t empty[DEC_MAX_RING];
-    uint64_t wfull[DEC_WIDE];
-    uint64_t wempty[DEC_WIDE];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
@@ -85,27 +89,29 @@ struct DecTail {
 
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 
+// A stage: the 256-row weight tile (128-byte rows), then the token tile(s):
+// NT rows of 64 bf16, or NT rows of 128 hi codes and NT rows of 128 lo codes.
 template <bool W8, int NT>
 constexpr int dec_slot_bytes() {
-    return WR * 128 + kps<W8>() * NT * BK * 2;  // 256 weight rows x 128 bytes, then KPS token tiles
+    return WR * 128 + (W8 ? 2 : 1) * NT * 128;
 }
+
+constexpr int dec_fixed_bytes() { return 1024 + (int)sizeof(DecTail); }
 
 template <bool W8, int NT>
 constexpr int dec_stages() {
-    return (kSmemLimit - 1024 - (int)sizeof(DecTail) - (W8 ? DEC_WIDE * WB16 : 0)) / dec_slot_bytes<W8, NT>() >
-                   DEC_MAX_RING
+    return (kSmemLimit - dec_fixed_bytes()) / dec_slot_bytes<W8, NT>() > DEC_MAX_RING
                ? DEC_MAX_RING
-               : (kSmemLimit - 1024 - (int)sizeof(DecTail) - (W8 ? DEC_WIDE * WB16 : 0)) / dec_slot_bytes<W8, NT>();
+               : (kSmemLimit - dec_fixed_bytes()) / dec_slot_bytes<W8, NT>();
 }
 
 template <bool W8, int NT>
 constexpr size_t dec_smem_bytes() {
-    return 1024 + (size_t)dec_stages<W8, NT>() * dec_slot_bytes<W8, NT>() + (W8 ? (size_t)DEC_WIDE * WB16 : 0) +
-           sizeof(DecTail);
+    return (size_t)dec_fixed_bytes() + (size_t)dec_stages<W8, NT>() * dec_slot_bytes<W8, NT>();
 }
 
 static_assert(dec_stages<false, 32>() >= 4 && dec_stages<false, 64>() >= 4, "bf16 decode ring too shallow");
-static_assert(dec_stages<true, 32>() >= 3 && dec_stages<true, 64>() >= 3, "FP8 decode ring too shallow");
+static_assert(dec_stages<true, 32>() >= 4 && dec_stages<true, 64>() >= 4, "FP8 decode ring too shallow");
 static_assert(dec_smem_bytes<true, 32>() <= kSmemLimit && dec_smem_bytes<false, 64>() <= kSmemLimit &&
                   dec_smem_bytes<true, 64>() <= kSmemLimit && dec_smem_bytes<false, 32>() <= kSmemLimit,
               "decode GEMM exceeds shared memory");
@@ -153,21 +159,19 @@ __device__ __forceinline__ DTile dec_tile(const DecTail& st, const DecParams& p,
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
-// Widening of one k-block (64 codes) of an FP8 stage whose weight rows are
-// 128 bytes apart, by `nthreads` threads (the converter warps), into a bf16
-// K-major 128-byte-swizzled tile; layout as widen_b_tile in tc_ptx.cuh.
-__device__ __forceinline__ void widen_tile(const uint8_t* src, uint8_t* dst, int tid, int nthreads) {
-#pragma unroll
-    for (int idx = tid; idx < WR * 8; idx += nthreads) {
-        const int r = idx >> 3, c = idx & 7;
-        const uint2 raw = *reinterpret_cast<const uint2*>(src + r * 128 + c * 8);
-        uint4 out;
-        out.x = e4m3x2_to_bf16x2(__byte_perm(raw.x, 0u, 0x1404));
-        out.y = e4m3x2_to_bf16x2(__byte_perm(raw.x, 0u, 0x3424));
-        out.z = e4m3x2_to_bf16x2(__byte_perm(raw.y, 0u, 0x1404));
-        out.w = e4m3x2_to_bf16x2(__byte_perm(raw.y, 0u, 0x3424));
-        *reinterpret_cast<uint4*>(dst + r * (BK * 2) + ((c ^ (r & 7)) << 4)) = out;
+// FP8 tokens: the power-of-two scale of token column j of tile t (its row of
+// the token matrix, through the gather list when there is one); 1 for bf16.
+__device__ __forceinline__ float dec_xscale(const DecParams& p, const DTile& t, int j) {
+    const float* xs = p.x_scale[t.prob];
+    if (!xs) return 1.0f;
+    const int r = t.x_row0 + j;
+    const int32_t* gidx = p.x_gather[t.prob];
+    int src = r;
+    if (gidx) {
+        src = __ldg(gidx + r);
+        if (src < 0 || src >= p.x_src_rows[t.prob]) src = 0;  // recorded by the producer
     }
+    return __ldg(xs + src);
 }
 
 // Epilogue of one tile for this thread's weight row.  The accumulator half h
@@ -197,16 +201,19 @@ __device__ __forceinline__ void dec_epilogue(const DecParams& p, const DTile& t,
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     if (j < jn) {
-                        base[j * pc + f] = s1 * __uint_as_float(g[j]);
-                        base[j * pc + N + f] = s3 * __uint_as_float(u[j]);
+                        const float xs = dec_xscale(p, t, c0 + j);
+                        base[j * pc + f] = s1 * xs * __uint_as_float(g[j]);
+                        base[j * pc + N + f] = s3 * xs * __uint_as_float(u[j]);
                     }
             } else {
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.prob]) + (size_t)(t.x_row0 + c0) * N + f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (j < jn)
-                        out[(size_t)j * N] =
-                            __float2bfloat16_rn(silu_mul(s1 * __uint_as_float(g[j]), s3 * __uint_as_float(u[j])));
+                    if (j < jn) {
+                        const float xs = dec_xscale(p, t, c0 + j);
+                        out[(size_t)j * N] = __float2bfloat16_rn(
+                            silu_mul(s1 * xs * __uint_as_float(g[j]), s3 * xs * __uint_as_float(u[j])));
+                    }
             }
         }
     } else {
@@ -230,25 +237,25 @@ __device__ __forceinline__ void dec_epilogue(const DecParams& p, const DTile& t,
                                  : static_cast<float*>(p.out[t.prob]) + row * N + o;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (j < jn) dst[(size_t)j * N] = (rs ? __ldg(rs + j) : 1.0f) * ws * __uint_as_float(v[j]);
+                    if (j < jn)
+                        dst[(size_t)j * N] =
+                            (rs ? __ldg(rs + j) : 1.0f) * dec_xscale(p, t, c0 + j) * ws * __uint_as_float(v[j]);
             }
         }
     }
 }
 
 template <int MODE, bool W8, int NT>
-__global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
-    grouped_gemm_decode_kernel(const __grid_constant__ DecParams p) {
+__global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(const __grid_constant__ DecParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int NST = dec_stages<W8, NT>();
     constexpr int SLOT = dec_slot_bytes<W8, NT>();
     constexpr int KPS = kps<W8>();
-    constexpr int WBYTES = WR * 128;   // weight bytes at the start of a stage; KPS token tiles follow
-    constexpr int XBYTES = NT * BK * 2;  // one token tile
+    constexpr int WBYTES = WR * 128;  // weight bytes at the start of a stage
+    constexpr int XBYTES = NT * 128;  // one token tile: NT rows of 128 bytes
     static_assert(MODE == kGemmSwiGLU || MODE == kGemmScale, "decode GEMM: SwiGLU and Scale modes");
-    uint8_t* wide = smem + (size_t)NST * SLOT;  // FP8: widened weight tiles
-    DecTail& st = *reinterpret_cast<DecTail*>(wide + (W8 ? (size_t)DEC_WIDE * WB16 : 0));
+    DecTail& st = *reinterpret_cast<DecTail*>(smem + (size_t)NST * SLOT);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &st.abort_flag;
 
@@ -256,10 +263,6 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
         for (int s = 0; s < NST; ++s) {
             mbar_init(&st.full[s], 1);
             mbar_init(&st.empty[s], 1);
-        }
-        for (int w = 0; w < DEC_WIDE; ++w) {
-            mbar_init(&st.wfull[w], 8);  // one arrival per widening warp
-            mbar_init(&st.wempty[w], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&st.tmem_full[a], 1);
@@ -272,6 +275,7 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int q = 0; q < p.nprob; ++q) {
             prefetch_tmap(&p.tmX[q]);
+            if (W8) prefetch_tmap(&p.tmXlo[q]);
             prefetch_tmap(&p.tmW1[q]);
             if (MODE == kGemmSwiGLU) prefetch_tmap(&p.tmW2[q]);
         }
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
     const int total_tiles = st.total[0] + st.total[1];
 
     if (warp == 0) {
-        // ---------------- TMA producer: weight tile + token rows per k-block ----------------
+        // ---------------- TMA producer: weight tile + token rows per stage ----------------
         int s = 0;
         uint32_t ph = 0;
         uint32_t issued_parity[NST];
@@ -350,33 +354,36 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
                     rows4[i] = v;
                 }
             }
+            // token bytes of one tile: gathered rows come in groups of four
+            const uint32_t x_bytes = gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * 128 : (uint32_t)XBYTES;
             for (int kb = t.kb0; kb < t.kb1; ++kb) {
                 if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
                     dead = true;
                     break;
                 }
                 uint8_t* sw = smem + (size_t)s * SLOT;
-                uint8_t* sx = sw + WBYTES;
+                // KPS * 64 elements of K: 64 bf16 or 128 FP8 codes, 128 bytes per row either way
+                const int kc = kb * KPS * BK;
                 if (lane == 0) {
-                    const uint32_t x_bytes =
-                        gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : (uint32_t)XBYTES;
-                    mbar_expect_tx(&st.full[s], WBYTES + KPS * x_bytes);
-                    // weight columns of this stage: KPS * 64 elements (bf16: 64, FP8: 128 bytes)
-                    const int wc = kb * KPS * BK;
+                    mbar_expect_tx(&st.full[s], WBYTES + (W8 ? 2u : 1u) * x_bytes);
                     if (MODE == kGemmSwiGLU) {
-                        tma_load_2d(sw, &p.tmW1[t.prob], wc, w_row0, &st.full[s]);
-                        tma_load_2d(sw + WBYTES / 2, &p.tmW2[t.prob], wc, w_row0, &st.full[s]);
+                        tma_load_2d(sw, &p.tmW1[t.prob], kc, w_row0, &st.full[s]);
+                        tma_load_2d(sw + WBYTES / 2, &p.tmW2[t.prob], kc, w_row0, &st.full[s]);
                     } else {
-                        tma_load_2d(sw, &p.tmW1[t.prob], wc, w_row0, &st.full[s]);
+                        tma_load_2d(sw, &p.tmW1[t.prob], kc, w_row0, &st.full[s]);
                     }
-                    if (!gidx)
-                        for (int h = 0; h < KPS; ++h)
-                            tma_load_2d(sx + h * XBYTES, &p.tmX[t.prob], (kb * KPS + h) * BK, t.x_row0, &st.full[s]);
+                    if (!gidx) {
+                        tma_load_2d(sw + WBYTES, &p.tmX[t.prob], kc, t.x_row0, &st.full[s]);
+                        if (W8) tma_load_2d(sw + WBYTES + XBYTES, &p.tmXlo[t.prob], kc, t.x_row0, &st.full[s]);
+                    }
                 }
-                if (gidx && lane * 4 < t.rows_valid)
-                    for (int h = 0; h < KPS; ++h)
-                        tma_gather4(sx + h * XBYTES + lane * 4 * (BK * 2), &p.tmX[t.prob], (kb * KPS + h) * BK,
-                                    rows4[0], rows4[1], rows4[2], rows4[3], &st.full[s]);
+                if (gidx && lane * 4 < t.rows_valid) {
+                    tma_gather4(sw + WBYTES + lane * 4 * 128, &p.tmX[t.prob], kc, rows4[0], rows4[1], rows4[2],
+                                rows4[3], &st.full[s]);
+                    if (W8)
+                        tma_gather4(sw + WBYTES + XBYTES + lane * 4 * 128, &p.tmXlo[t.prob], kc, rows4[0], rows4[1],
+                                    rows4[2], rows4[3], &st.full[s]);
+                }
                 issued_parity[s] = ph;
                 used[s] = true;
                 if (++s == NST) {
@@ -394,9 +401,9 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
-            int s = 0, w = 0;
-            uint32_t ph = 0, pw = 0;
+            constexpr uint32_t idesc = W8 ? idesc_e4m3_f32(128, NT) : idesc_bf16_f32(128, NT);
+            int s = 0;
+            uint32_t ph = 0;
             int it = 0;
             bool dead = false;
             for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x, ++it) {
@@ -411,32 +418,27 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
                         dead = true;
                         break;
                     }
-                    for (int h = 0; h < KPS && !dead; ++h) {
-                        if (W8 && !mbar_wait(&st.wfull[w], pw, abort_flag, p.status, p.wait_limit_ns)) {
-                            dead = true;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t sw =
-                            W8 ? smem_u32(wide + (size_t)w * WB16) : smem_u32(smem + (size_t)s * SLOT);
-                        const uint32_t sx = smem_u32(smem + (size_t)s * SLOT + WBYTES + h * XBYTES);
+                    tc_fence_after();
+                    const uint32_t sw = smem_u32(smem + (size_t)s * SLOT);
+                    const uint32_t sx = sw + WBYTES;
+                    // four 32-byte K steps per 128-byte row: 16 bf16 or 32 FP8 codes each
 #pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                            const uint64_t xdesc = sdesc_k_sw128(sx + kk * UMMA_K * 2);
-                            const uint32_t accf = (kb != t.kb0 || h != 0 || kk != 0) ? 1u : 0u;
-                            umma_bf16(dtm, sdesc_k_sw128(sw + kk * UMMA_K * 2), xdesc, idesc, accf);
-                            umma_bf16(dtm + NT, sdesc_k_sw128(sw + 128 * BK * 2 + kk * UMMA_K * 2), xdesc, idesc,
-                                      accf);
-                        }
-                        if (W8) {
-                            umma_commit(&st.wempty[w]);
-                            if (++w == DEC_WIDE) {
-                                w = 0;
-                                pw ^= 1u;
-                            }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t accf = (kb != t.kb0 || kk != 0) ? 1u : 0u;
+                        const uint64_t a0 = sdesc_k_sw128(sw + kk * 32);
+                        const uint64_t a1 = sdesc_k_sw128(sw + 128 * 128 + kk * 32);
+                        const uint64_t xh = sdesc_k_sw128(sx + kk * 32);
+                        if constexpr (W8) {  // tokens as hi + lo codes: two MMAs per weight half
+                            const uint64_t xl = sdesc_k_sw128(sx + XBYTES + kk * 32);
+                            umma_e4m3(dtm, a0, xh, idesc, accf);
+                            umma_e4m3(dtm, a0, xl, idesc, 1u);
+                            umma_e4m3(dtm + NT, a1, xh, idesc, accf);
+                            umma_e4m3(dtm + NT, a1, xl, idesc, 1u);
+                        } else {
+                            umma_bf16(dtm, a0, xh, idesc, accf);
+                            umma_bf16(dtm + NT, a1, xh, idesc, accf);
                         }
                     }
-                    if (dead) break;
                     umma_commit(&st.empty[s]);
                     if (++s == NST) {
                         s = 0;
@@ -447,7 +449,7 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
                 umma_commit(&st.tmem_full[acc]);
             }
         }
-    } else if (warp < 6) {
+    } else {
         // ---------------- epilogue (warps 2..5): one weight row per thread ----------------
         const int quarter = warp & 3;
         const int wrow = quarter * 32 + lane;
@@ -464,43 +466,6 @@ __global__ void __launch_bounds__(W8 ? DEC_W8_THREADS : DEC_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.tmem_empty[acc]);
-        }
-    } else if constexpr (W8) {
-        // ---------------- widening warps (6..13), FP8 weights ----------------
-        const int ctid = threadIdx.x - DEC_THREADS;  // 0..255
-        int s = 0, w = 0;
-        uint32_t ph = 0, pw = 0;
-        bool dead = false;
-        for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
-            const DTile t = dec_tile<MODE, NT, KPS>(st, p, id);
-            for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                const bool ok_raw = mbar_wait(&st.full[s], ph, abort_flag, p.status, p.wait_limit_ns);
-                if (!__all_sync(0xffffffffu, ok_raw)) {
-                    dead = true;
-                    break;
-                }
-                for (int h = 0; h < KPS; ++h) {
-                    const bool ok_w = mbar_wait(&st.wempty[w], pw ^ 1u, abort_flag, p.status, p.wait_limit_ns);
-                    if (!__all_sync(0xffffffffu, ok_w)) {
-                        dead = true;
-                        break;
-                    }
-                    widen_tile(smem + (size_t)s * SLOT + h * BK, wide + (size_t)w * WB16, ctid,
-                               DEC_W8_THREADS - DEC_THREADS);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&st.wfull[w]);
-                    if (++w == DEC_WIDE) {
-                        w = 0;
-                        pw ^= 1u;
-                    }
-                }
-                if (dead) break;
-                if (++s == NST) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
         }
     }
 
@@ -532,7 +497,7 @@ cudaError_t launch_dec(const DecParams& prm, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set_mask |= bit;
     }
-    launch_pdl(grouped_gemm_decode_kernel<MODE, W8, NT>, dim3(grid), dim3(W8 ? DEC_W8_THREADS : DEC_THREADS),
+    launch_pdl(grouped_gemm_decode_kernel<MODE, W8, NT>, dim3(grid), dim3(DEC_THREADS),
                dec_smem_bytes<W8, NT>(), s, prm);
     return cudaGetLastError();
 }
@@ -555,23 +520,29 @@ cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, in
     if (probs[0].G + (nprob > 1 ? probs[1].G : 0) > MAX_GROUPS + 1) return cudaErrorInvalidValue;
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
-        if (g.G < 1 || g.G > MAX_GROUPS || g.out2 || g.A2) return cudaErrorInvalidValue;
-        if (w8 && (g.K % 16 != 0 || !g.wscale1 || (mode == kGemmSwiGLU && !g.wscale2))) return cudaErrorInvalidValue;
+        if (g.G < 1 || g.G > MAX_GROUPS || g.out2) return cudaErrorInvalidValue;
+        // FP8: A holds the hi codes of the tokens, A2 the lo codes, a_scale the row scales
+        if (w8 && (g.K % 16 != 0 || !g.wscale1 || (mode == kGemmSwiGLU && !g.wscale2) || !g.A2 || !g.a_scale))
+            return cudaErrorInvalidValue;
+        if (!w8 && (g.A2 || g.a_scale)) return cudaErrorInvalidValue;
+        const int x_src = g.a_gather ? g.a_src_rows : g.a_rows;
+        const int x_box = g.a_gather ? 1 : nt;  // gather maps: one-row box
+        if (w8) {  // FP8 stages hold 128 codes (two k-blocks) of every weight and token row
+            if (!make_tmap_u8(&prm.tmX[q], g.A, x_src, g.K, x_box, 2 * BK, true) ||
+                !make_tmap_u8(&prm.tmXlo[q], g.A2, x_src, g.K, x_box, 2 * BK, true) ||
+                !make_tmap_u8(&prm.tmW1[q], g.B1, g.G * g.N, g.K, w_box, 2 * BK, true) ||
+                (mode == kGemmSwiGLU && !make_tmap_u8(&prm.tmW2[q], g.B2, g.G * g.N, g.K, w_box, 2 * BK, true)))
+                return cudaErrorInvalidValue;
+            prm.x_scale[q] = g.a_scale;
+        } else {
+            if (!make_tmap(&prm.tmX[q], g.A, x_src, g.K, x_box) ||
+                !make_tmap(&prm.tmW1[q], g.B1, g.G * g.N, g.K, w_box) ||
+                (mode == kGemmSwiGLU && !make_tmap(&prm.tmW2[q], g.B2, g.G * g.N, g.K, w_box)))
+                return cudaErrorInvalidValue;
+        }
         if (g.a_gather) {
-            if (!make_tmap(&prm.tmX[q], g.A, g.a_src_rows, g.K, 1)) return cudaErrorInvalidValue;
             prm.x_gather[q] = g.a_gather;
             prm.x_src_rows[q] = g.a_src_rows;
-        } else if (!make_tmap(&prm.tmX[q], g.A, g.a_rows, g.K, nt)) {
-            return cudaErrorInvalidValue;
-        }
-        // FP8 stages hold 128 codes (two k-blocks) of every weight row
-        const bool ok1 = w8 ? make_tmap_u8(&prm.tmW1[q], g.B1, g.G * g.N, g.K, w_box, 2 * BK)
-                            : make_tmap(&prm.tmW1[q], g.B1, g.G * g.N, g.K, w_box);
-        if (!ok1) return cudaErrorInvalidValue;
-        if (mode == kGemmSwiGLU) {
-            const bool ok2 = w8 ? make_tmap_u8(&prm.tmW2[q], g.B2, g.G * g.N, g.K, w_box, 2 * BK)
-                                : make_tmap(&prm.tmW2[q], g.B2, g.G * g.N, g.K, w_box);
-            if (!ok2) return cudaErrorInvalidValue;
         }
         if (ksplit > 1) {
             const int kstep = (w8 ? 2 : 1) * BK;

@@ -130,6 +130,25 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0
+// for both), fp32 accumulator, both K-major, dense, M x N.  One MMA covers
+// K = 32 codes, i.e. the same 32 bytes of a 128-byte swizzle row as a bf16
+// kind::f16 MMA.
+constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                                  // D format: f32
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
@@ -236,9 +255,11 @@ inline bool make_tmap(CUtensorMap* tm, const void* base, int rows, int K, int bo
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D one-byte (FP8 code) tensor [rows][K], box = 64 x box_rows, no swizzle:
-// the converter warps re-lay the tile out for the MMA themselves.
-inline bool make_tmap_u8(CUtensorMap* tm, const void* base, int rows, int K, int box_rows, int box_cols = BK) {
+// 2-D one-byte (FP8 code) tensor [rows][K], box = box_cols x box_rows.  No
+// swizzle (the converter warps re-lay the tile out for the MMA themselves),
+// or, with sw128 and 128 columns, the 128-byte swizzle the MMA reads directly.
+inline bool make_tmap_u8(CUtensorMap* tm, const void* base, int rows, int K, int box_rows, int box_cols = BK,
+                         bool sw128 = false) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
@@ -246,7 +267,8 @@ inline bool make_tmap_u8(CUtensorMap* tm, const void* base, int rows, int K, int
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -318,12 +318,17 @@ def _oracle_y_fp8(Ln, q8, w, ids, gates, slot_pos, toks):
     return y
 
 
-def check_layer_fp8(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | None = None) -> dict:
+def check_layer_fp8(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | None = None,
+                    per_token: bool = False) -> dict:
     """FP8-weight layer: codes and scales bit-exact with the oracle's
     quantisation of the same bf16 weights; routing as the bf16 layer (the
     router is unchanged); y (fp32 result) within the bf16 tolerance of the
     oracle evaluated with the exactly dequantised weights on the GPU's ids;
-    bf16 y = RNE(fp32 y); deterministic."""
+    bf16 y = RNE(fp32 y); deterministic.  per_token=True holds every token
+    to the tolerance against its own RMS instead, for inputs whose token rows
+    differ in scale by many orders of magnitude: there the RMS over all
+    tokens is one token's RMS / sqrt(T), which would hold that token to a
+    sqrt(T) tighter bound than any other layer call gets."""
     layer = layer_of(w)
     if L is None:
         L = moe_inputs.make_layer(w, "cuda")
@@ -376,9 +381,15 @@ def check_layer_fp8(w: moe_inputs.Workload, n_sample: int | None = None, L: dict
     rms = float(np.sqrt(np.mean(y_or ** 2))) if y_or.size else 0.0
     err = float(np.abs(y_gpu - y_or).max()) if y_or.size else 0.0
     rep.update(y_rms=rms, y_rel=err / rms if rms > 0 else err, tol=TOL["bf16"], y_tokens_checked=int(len(toks)))
+    if y_or.size:  # worst token against its own RMS (a zero row must come out exactly zero)
+        t_rms = np.sqrt(np.mean(y_or ** 2, axis=1))
+        t_err = np.abs(y_gpu - y_or).max(axis=1)
+        rel = np.where(t_rms > 0, t_err / np.where(t_rms > 0, t_rms, 1.0), np.where(t_err > 0, np.inf, 0.0))
+        rep["y_rel_worst_token"] = float(rel.max())
     rep["y_stored_is_rne_of_fp32"] = bool(torch.equal(y1, y32.to(y1.dtype)))
     rep["y_deterministic"] = bool(torch.equal(y1, y2))
     rep["ok"] = bool(rep["quantisation_mismatches"] == 0 and rep["status"] == 0
-                     and rep["ids_mismatch_outside_margin"] == 0 and rep["y_rel"] <= rep["tol"]
+                     and rep["ids_mismatch_outside_margin"] == 0
+                     and (rep.get("y_rel_worst_token", 0.0) if per_token else rep["y_rel"]) <= rep["tol"]
                      and rep["y_stored_is_rne_of_fp32"] and rep["y_deterministic"])
     return rep

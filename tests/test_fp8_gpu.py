@@ -81,6 +81,29 @@ def test_fp8_subnormal_codes_are_widened_exactly(cuda):
     _assert_ok(check_layer_fp8(w, L=L))
 
 
+@pytest.mark.parametrize("T", [3, 40])
+def test_fp8_decode_tokens_of_very_different_scales(cuda, T):
+    """Decode-sized batches carry the bf16 token rows (and H) to the FP8 MMA
+    as E4M3 hi + lo codes with a power-of-two scale per row.  Rows scaled by
+    2^-40 and 2^+30, a zero row and a row with one entry 2^12 above the rest
+    (whose small entries fall below the lo codes' range) must each stay
+    within tolerance against their own RMS; the zero row gives exactly 0."""
+    import moe_inputs
+    from tests._parity import check_layer_fp8
+    w = Workload(f"fp8_decode_scales_t{T}", T=T, d=256, E=8, F=384, k=2, n_shared=1, F_s=128, weights="fp8")
+    L = moe_inputs.make_layer(w, "cuda")
+    x = L["x"].float()
+    x[0] *= 2.0 ** -40
+    x[1] *= 2.0 ** 30
+    x[2] = 0.0
+    if T > 3:
+        x[3, 5] = 4096.0
+    L["x"] = x.to(L["x"].dtype).contiguous()
+    rep = check_layer_fp8(w, L=L, per_token=True)
+    print(json.dumps(rep))
+    _assert_ok(rep)
+
+
 @pytest.mark.parametrize("name", ["mixtral_decode_t1_fp8", "mixtral_decode_t8_fp8"])
 def test_fp8_mixtral_decode(cuda, name):
     from tests._parity import check_layer_fp8
