@@ -12,9 +12,12 @@ max-over-ranks of the timed region.
 
 `value` is whole-job tokens/s.  `roofline` describes the dominant kernel (the
 up-projection grouped GEMM with the fused SwiGLU), timed live with the
-library's per-stage CUDA events inside the timed region.  `e2e` repeats the
-measurement through the public Python API with the token batch copied from
-pinned host memory each step and the output copied back.  `cpu_baseline`
+library's per-stage CUDA events inside the timed region; its roof is the
+one that binds it (tensor time of its FLOPs vs HBM time of its algorithmic
+bytes).  `e2e` repeats the measurement through the public Python API
+(HostPipeline) with each step's token batch copied in from pinned host
+memory and its output copied back, those copies overlapped with the
+neighbouring steps' layer calls as a serving loop would.  `cpu_baseline`
 times the fp64 CPU oracle on a bounded sample of the same workload.
 
 --impl reference times that oracle (the only reference implementation this
@@ -39,8 +42,11 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s on 1 B300; % of bf16 tensor peak or HBM roofline"
 UNIT = "tokens/s"
 FALLBACK = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0)
-# sources of the tensor-core GEMM kernel whose DRAM traffic profiles/traffic.json records
-TC_SOURCES = [os.path.join(ROOT, "mixture_experts_layer_95_b300", "csrc", f) for f in ("gemm_tc.cu", "tc_ptx.cuh")]
+# profiles/traffic.json: per workload, the up GEMM's DRAM bytes per launch from
+# an ncu capture, with the kernel sources it was taken on ("sources", default
+# the prefill GEMM's) and their hash; a changed source voids the figure
+CSRC = os.path.join(ROOT, "mixture_experts_layer_95_b300", "csrc")
+TC_SOURCES = ("gemm_tc.cu", "tc_ptx.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -89,10 +95,10 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
-def source_hash(paths=TC_SOURCES):
+def source_hash(names=TC_SOURCES):
     h = hashlib.sha256()
-    for path in paths:
-        with open(path, "rb") as fh:
+    for name in names:
+        with open(os.path.join(CSRC, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -105,7 +111,7 @@ def recorded_traffic(workload):
     with open(TRAFFIC_FILE) as fh:
         d = json.load(fh)
     e = d.get(workload)
-    if not e or e.get("source_sha256_16") != source_hash():
+    if not e or e.get("source_sha256_16") != source_hash(e.get("sources", TC_SOURCES)):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -368,7 +374,9 @@ def run_ours(args):
     up_ms = up_ms_live["up_gemm"] / up_n["up_gemm"]  # live, inside the timed region
     layer_flops = moe_inputs.algorithmic_flops(w, kept_total)
     wbytes = moe_inputs.expert_weight_bytes(w, touched)
-    tensor_bound = w.T * w.k >= 512  # below that the GEMMs stream weights from HBM
+    # the up GEMM's binding roof: tensor time of its FLOPs vs HBM time of its bytes
+    up_bytes = moe_inputs.up_gemm_bytes(w, touched, kept_total)
+    tensor_bound = up_flops / (peaks["bf16_tflops"] * 1e12) >= up_bytes / (peaks["hbm_gbs"] * 1e9)
     plan = moe.plan_describe(layer_of(w).cfg())
     up_kernel = {"tc_pair": "grouped_gemm_tc_pair_kernel<SwiGLU> (up GEMM, CTA pairs)",
                  "tc": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)",
@@ -385,38 +393,39 @@ def run_ours(args):
                 "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4),
                 "traffic": recorded_traffic(args.workload),
                 "kernel": up_kernel, "peak_source": f"{peak_src} bf16 burst",
-                "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4)}
+                "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4),
+                "frac_of_hbm": round(up_bytes / (up_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                "algorithmic_bytes_per_launch": up_bytes}
     else:
-        up_bytes = moe_inputs.up_weight_bytes(w, touched)
         achieved = up_bytes / (up_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": recorded_traffic(args.workload),
                 "kernel": up_kernel, "peak_source": f"{peak_src} HBM copy",
-                "algorithmic_bytes_per_launch": up_bytes, "launch_ms": round(up_ms, 4)}
+                "algorithmic_bytes_per_launch": up_bytes, "launch_ms": round(up_ms, 4),
+                "frac_of_bf16_peak": round(up_flops / (up_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4)}
 
-    # end to end through the public API: host batch in, host result out
+    # end to end through the public API: every step copies its batch in from
+    # pinned host memory and its result back out (HostPipeline overlaps those
+    # copies with the neighbouring steps' layer calls, as a serving loop would)
     x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     x_h.copy_(x)
-    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-    x_dev = torch.empty_like(x)
-    for _ in range(2):
-        x_dev.copy_(x_h, non_blocking=True)
-        fw(x_dev, y)
-        y_h.copy_(y, non_blocking=True)
+    y_h = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
+    pipe = moe.HostPipeline(fw, dev)
+    pipe.run([x_h] * 2, y_h, stream)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        x_dev.copy_(x_h, non_blocking=True)
-        fw(x_dev, y)
-        y_h.copy_(y, non_blocking=True)
+    pipe.run([x_h] * args.steps, [y_h[i % 2] for i in range(args.steps)], stream)
     e1.record(stream)
     e1.synchronize()
+    if not torch.equal(y_h[(args.steps - 1) % 2].to(dev), y):
+        raise RuntimeError("end-to-end result differs from the device-timed call's")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     clocks.stop()
     e2e = {"value": round(job_throughput(w.T, world, args.steps, e2e_ms), 1), "unit": UNIT,
            "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
-           "d2h_bytes_per_step": y_h.numel() * y_h.element_size()}
+           "d2h_bytes_per_step": y_h[0].numel() * y_h[0].element_size(),
+           "copies": "pinned host, own streams, overlapped with the neighbouring steps' layer calls"}
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,

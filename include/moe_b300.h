@@ -279,8 +279,15 @@ MOE_API int moe_forward(const moe_config *cfg, const void *x, const void *w_gate
  *   q_ri    = E4M3(w_ri / scale_r)  (IEEE fp32 quotient, round to nearest
  *             even, saturating), and the layer uses w~_ri = value(q_ri) scale_r.
  * The expert GEMMs stream the one-byte codes (half the bytes of bf16 weights:
- * the decode-time bound), widen them exactly to bf16 in shared memory and
- * apply scale_r to the fp32 accumulator of output channel r. */
+ * the decode-time bound) and apply scale_r to the fp32 accumulator of output
+ * channel r.  Prefill-sized batches widen the codes exactly to bf16 in shared
+ * memory (bf16 x bf16 MMAs).  Decode-sized batches (at most 32 rows per
+ * touched expert on average) feed the codes to the FP8 tensor cores as they
+ * are; that MMA takes FP8 on both sides, so every bf16 row of x and of H is
+ * first split into two E4M3 code rows and a power-of-two scale,
+ * row = s (hi + lo), which reproduces every entry within a factor 2^10 of the
+ * row's largest magnitude exactly (smaller entries: absolute error at most
+ * 2^-17 times that magnitude).  Both products then accumulate in fp32. */
 
 /* Quantises a [rows][cols] matrix (dtype MOE_BF16 or MOE_F32; cols a multiple
  * of 16) row by row: q [rows][cols] uint8 codes, scale [rows] fp32.  Device
@@ -350,8 +357,10 @@ MOE_API int moe_last_device_status(const moe_config *cfg, void *ws, moe_stream_t
  * events[2*s] on its stream just before the launches of stage s and
  * events[2*s+1] just after them, for s = 0 router (logits, softmax, top-k),
  * 1 grouping scan (ranks, offsets, permutation; includes the histogram
- * kernel of moe_permute), 2 row gather (x_perm), 3 up GEMM (SwiGLU), 4 down
- * GEMM, 5 combine.  `events` holds n (<= 12) cudaEvent_t handles owned by
+ * kernel of moe_permute), 2 token rows for the up GEMM (the x_perm gather;
+ * with FP8 weights on decode-sized batches, the E4M3 hi/lo split of x),
+ * 3 up GEMM (SwiGLU, and its split-K finalize), 4 down GEMM (with FP8 weights
+ * on decode-sized batches, after the E4M3 hi/lo split of H), 5 combine.  `events` holds n (<= 12) cudaEvent_t handles owned by
  * the caller; NULL entries are skipped.  Pass events = NULL to clear.
  * Returns MOE_OK, or MOE_ERR_SHAPE if n is out of range. */
 MOE_API int moe_set_stage_events(void *const *events, int n);

@@ -637,6 +637,71 @@ class Forward:
         return last_device_status(self.layer, self.ws, stream)
 
 
+class HostPipeline:
+    """Feeds a Forward with batches that live in pinned host memory, the way a
+    serving loop does: two device slots for x and y; batch i's host-to-device
+    copy runs on a copy stream while batch i-1 computes, and its result goes
+    back to the host on a second copy stream while batch i+1 computes.  Events
+    order each slot's copy-in, layer call and copy-out; every kernel is the
+    Forward's own, on the compute stream."""
+
+    def __init__(self, fw: Forward, device=None):
+        L = fw.layer
+        dev = torch.device(device) if device is not None else fw.ws.device
+        self.fw = fw
+        self.device = dev
+        self.x = [torch.empty((L.T, L.d), dtype=L.torch_dtype, device=dev) for _ in range(2)]
+        self.y = [torch.empty((L.T, L.d), dtype=L.y_dtype, device=dev) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.copied_in = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.copied_out = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+
+    def run(self, x_host, y_host, stream=None):
+        """Enqueues one layer call per (x_host[i], y_host[i]) pair of pinned
+        host tensors ([T][d], the layer's input and output dtypes) and returns
+        without waiting; once `stream` (default: the current stream) has
+        drained, every y_host[i] holds its result.  The host tensors must stay
+        alive and untouched until then."""
+        L = self.fw.layer
+        comp = stream or torch.cuda.current_stream(self.device)
+        start = torch.cuda.Event()
+        start.record(comp)  # copies begin after the work already on `stream`
+        self.h2d.wait_stream(comp)
+        last = None
+        for i, (xh, yh) in enumerate(zip(x_host, y_host)):
+            _need_host(xh, (L.T, L.d), L.torch_dtype, "x_host")
+            _need_host(yh, (L.T, L.d), L.y_dtype, "y_host")
+            s = i % 2
+            if self.used[s]:
+                self.h2d.wait_event(self.computed[s])   # the call that last read x[s] is done
+                comp.wait_event(self.copied_out[s])     # y[s] is back on the host
+            with torch.cuda.stream(self.h2d):
+                self.x[s].copy_(xh, non_blocking=True)
+            self.copied_in[s].record(self.h2d)
+            comp.wait_event(self.copied_in[s])
+            self.fw(self.x[s], self.y[s], stream=comp)
+            self.computed[s].record(comp)
+            self.d2h.wait_event(self.computed[s])
+            with torch.cuda.stream(self.d2h):
+                yh.copy_(self.y[s], non_blocking=True)
+            self.copied_out[s].record(self.d2h)
+            self.used[s] = True
+            last = s
+        if last is not None:
+            comp.wait_event(self.copied_out[last])  # draining `stream` covers every copy-out
+
+
+def _need_host(t, shape, dtype, name):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu" or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned host tensor")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+    return t
+
+
 def forward(layer: Layer, x, w_gate, w1, w3, w2, logit_bias=None, select_bias=None, ws1=None, ws3=None, ws2=None,
             stats: bool = False, stream=None):
     """One moe_forward call; returns y (and the statistics dict when stats=True)."""

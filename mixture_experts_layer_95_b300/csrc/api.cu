@@ -532,12 +532,13 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
             down[q].a_scale = at<float>(ws, q == 0 ? L.hq_s : L.hsq_s);
         }
     }
+    if (q8) {  // token rows for the up GEMM, timed with the gather step
+        StageScope scope(kStageGather, s);
+        MOE_LAUNCH(launch_split_e4m3(c.T, c.d, x, nullptr, xq, xq + (size_t)c.T * c.d, at<float>(ws, L.xq_s), s));
+    }
     {
         StageScope scope(kStageUp, s);
         if (use_decode_gemm(c)) {
-            if (q8)
-                MOE_LAUNCH(launch_split_e4m3(c.T, c.d, x, nullptr, xq, xq + (size_t)c.T * c.d, at<float>(ws, L.xq_s),
-                                             s));
             MOE_LAUNCH(launch_gemm_decode(kGemmSwiGLU, up, np, status, sms, s, sp.up, w8 != nullptr,
                                           decode_tile_rows(c)));
             if (sp.up > 1) {

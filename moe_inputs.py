@@ -182,6 +182,14 @@ def expert_weight_bytes(w: Workload, n_touched: int) -> float:
     return float(eb * (expert_params(w.d, w.F) * n_touched + expert_params(w.d, w.F_s) * w.n_shared))
 
 
+def up_gemm_bytes(w: Workload, n_touched: int, kept_total: int) -> float:
+    """Algorithmic HBM bytes of one up-GEMM launch: W1 and W3 of the touched
+    experts and the shared expert (up_weight_bytes), every kept token row read
+    once and every row of H written once (activations in the layer's dtype)."""
+    ab = 4 if w.dtype == "f32" else 2
+    return up_weight_bytes(w, n_touched) + float(ab * (kept_total * (w.d + w.F) + w.T * w.n_shared * (w.d + w.F_s)))
+
+
 def up_weight_bytes(w: Workload, n_touched: int) -> float:
     """Bytes of W1 and W3 (touched experts + shared) the up GEMM must read."""
     if w.weights == "fp8":
