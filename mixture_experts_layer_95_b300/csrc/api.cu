@@ -223,8 +223,8 @@ Layout layout(const moe_config& c) {
 
 // Backward-pass workspace: the forward layout, then these regions.
 struct BLayout {
-    size_t probs, xp, dyp, G, U, D, dGU, Hb, dgp, w2t, w13t, kbase, klen, dGT, dUT, HbT, xpT, dysT, dXp, dlog, R,
-        wg_part, s_off, s_kbase, s_klen, Gs, Us, Ds, dGUs, Hbs, ws2t, ws13t, dGsT, dUsT, HbsT, xT, dyT, dXs, total;
+    size_t probs, xp, dyp, G, U, D, dGU, Hb, dgp, kbase, klen, dGT, dUT, HbT, xpT, dysT, dXp, dlog, R,
+        wg_part, s_off, s_kbase, s_klen, Gs, Us, Ds, dGUs, Hbs, dGsT, dUsT, HbsT, xT, dyT, dXs, total;
     int ncols, ncols_s;
 };
 
@@ -251,8 +251,6 @@ BLayout blayout(const moe_config& c) {
     b.dGU = take(2 * n * 2 * F);
     b.Hb = take(2 * n * F);
     b.dgp = take(4 * n);
-    b.w2t = take(2 * E * F * d);
-    b.w13t = take(2 * E * d * 2 * F);
     b.kbase = take(4 * E);
     b.klen = take(4 * E);
     b.dGT = take(2 * F * nc);
@@ -273,8 +271,6 @@ BLayout blayout(const moe_config& c) {
     b.Ds = take(sh ? 4 * T * Fs : 0);
     b.dGUs = take(sh ? 2 * T * 2 * Fs : 0);
     b.Hbs = take(sh ? 2 * T * Fs : 0);
-    b.ws2t = take(sh ? 2 * Fs * d : 0);
-    b.ws13t = take(sh ? 2 * d * 2 * Fs : 0);
     b.dGsT = take(sh ? 2 * Fs * ncs : 0);
     b.dUsT = take(sh ? 2 * Fs * ncs : 0);
     b.HbsT = take(sh ? 2 * Fs * ncs : 0);
@@ -1020,18 +1016,6 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
         MOE_LAUNCH(launch_k_windows(1, s_off, s_kbase, s_klen, T, s));
     }
 
-    // transposed weights: W2^T per expert [F][d]; [W1^T | W3^T] per expert [d][2F]
-    void* w2t = at<void>(ws, B.w2t);
-    void* w13t = at<void>(ws, B.w13t);
-    MOE_LAUNCH(launch_transpose_batched(MOE_BF16, w2, E, d, F, w2t, d, 0, s));
-    MOE_LAUNCH(launch_transpose_batched(MOE_BF16, w1, E, F, d, w13t, 2 * (size_t)F, 0, s));
-    MOE_LAUNCH(launch_transpose_batched(MOE_BF16, w3, E, F, d, w13t, 2 * (size_t)F, F, s));
-    if (c.n_shared) {
-        MOE_LAUNCH(launch_transpose_batched(MOE_BF16, ws2, 1, d, Fs, at<void>(ws, B.ws2t), d, 0, s));
-        MOE_LAUNCH(launch_transpose_batched(MOE_BF16, ws1, 1, Fs, d, at<void>(ws, B.ws13t), 2 * (size_t)Fs, 0, s));
-        MOE_LAUNCH(launch_transpose_batched(MOE_BF16, ws3, 1, Fs, d, at<void>(ws, B.ws13t), 2 * (size_t)Fs, Fs, s));
-    }
-
     // grouped GEMMs of the routed experts (problem 0) and the shared expert (problem 1)
     const int np = c.n_shared ? 2 : 1;
     auto routed = [&](const void* A, int a_rows, const void* Bm, int N, int K, void* out) {
@@ -1058,6 +1042,13 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
         g.out = out;
         return g;
     };
+    // products with W^T read the weights as they are stored: MN-major B
+    auto transposed = [&](GemmProblem g, const void* b2, int kpart) {
+        g.b_mn = 1;
+        g.B2 = b2;
+        g.kpart = kpart;
+        return g;
+    };
     auto windows = [&](const void* A, int M, const void* Bm, int N, int K, const int32_t* kb, const int32_t* kl, int G,
                        void* out) {
         GemmProblem g{};
@@ -1076,13 +1067,19 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
     float* G = at<float>(ws, B.G);
     float* U = at<float>(ws, B.U);
     float* D = at<float>(ws, B.D);
+    // large segments: the row-indexed products run on CTA pairs (Scale mode
+    // without gates is the plain product)
+    const bool pair = use_pair_gemm(c);
+    const int pm = pair ? kGemmScale : kGemmPlain;
     {
         GemmProblem p1[2] = {routed(xp, n, w1, F, d, G), dense(x, T, ws1, Fs, d, at<float>(ws, B.Gs))};
-        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, p1, np, status, sms, s));
+        MOE_LAUNCH(launch_gemm_tc(pm, p1, np, status, sms, s, 1, pair));
         GemmProblem p2[2] = {routed(xp, n, w3, F, d, U), dense(x, T, ws3, Fs, d, at<float>(ws, B.Us))};
-        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, p2, np, status, sms, s));
-        GemmProblem p3[2] = {routed(dyp, n, w2t, F, d, D), dense(dy, T, at<void>(ws, B.ws2t), Fs, d, at<float>(ws, B.Ds))};
-        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, p3, np, status, sms, s));
+        MOE_LAUNCH(launch_gemm_tc(pm, p2, np, status, sms, s, 1, pair));
+        // D = dy W2 (W2 stored [d][F]: B^T of this product)
+        GemmProblem p3[2] = {transposed(routed(dyp, n, w2, F, d, D), nullptr, 0),
+                             transposed(dense(dy, T, ws2, Fs, d, at<float>(ws, B.Ds)), nullptr, 0)};
+        MOE_LAUNCH(launch_gemm_tc(pm, p3, np, status, sms, s, 1, pair));
     }
     void* dGU = at<void>(ws, B.dGU);
     void* Hb = at<void>(ws, B.Hb);
@@ -1095,9 +1092,10 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
     float* dXp = at<float>(ws, B.dXp);
     float* dXs = c.n_shared ? at<float>(ws, B.dXs) : nullptr;
     {
-        GemmProblem p4[2] = {routed(dGU, n, w13t, d, 2 * F, dXp),
-                             dense(at<void>(ws, B.dGUs), T, at<void>(ws, B.ws13t), d, 2 * Fs, dXs)};
-        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, p4, np, status, sms, s));
+        // dX = dG W1 + dU W3: K in two parts (dG with W1, dU with W3), W1 and W3 stored [F][d]
+        GemmProblem p4[2] = {transposed(routed(dGU, n, w1, d, 2 * F, dXp), w3, F),
+                             transposed(dense(at<void>(ws, B.dGUs), T, ws1, d, 2 * Fs, dXs), ws3, Fs)};
+        MOE_LAUNCH(launch_gemm_tc(pm, p4, np, status, sms, s, 1, pair));
     }
 
     // weight gradients: per-expert K windows of the transposed activations

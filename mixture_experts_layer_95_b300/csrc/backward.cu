@@ -5,7 +5,8 @@
 // (top-k selection has no gradient) and f_i held constant while p_i carries the
 // gradient ("MoE Deep Dive", Load Balancing Loss Derivation).  Per kept slot
 // (row r of the permuted layout, expert e, gate g), with G = X W1^T, U = X W3^T
-// recomputed and D = dy W2_e (the down projection transposed):
+// recomputed and D = dy W2_e (the down projection transposed; the GEMM reads
+// W2_e, W1_e and W3_e as stored, as MN-major B operands):
 //   dg_r = sum_f D h,   h = silu(G) U
 //   dh = g D,  dG = dh U silu'(G),  dU = dh silu(G)
 //   dX_r = dG W1_e + dU W3_e,  dW1_e = dG^T X,  dW3_e = dU^T X,  dW2_e = (g dy)^T h
@@ -125,35 +126,6 @@ __global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloa
                         gather8(tile, ch * 8, cc);
             }
         }
-    }
-    __syncthreads();
-    pdl_trigger();
-}
-
-// dst[b][c][col0 + r] = src[b][r][c]: batch of [R][C] bf16 matrices (weights)
-// into [C][ld_dst] rows at column offset col0; R, C, ld_dst, col0 multiples of 8.
-__global__ void __launch_bounds__(256) transpose_batched_kernel(const __nv_bfloat16* __restrict__ src, int R, int C,
-                                                                __nv_bfloat16* __restrict__ dst, size_t ld_dst,
-                                                                int col0) {
-    pdl_wait();
-    __shared__ uint16_t tile[TT][TPAD];
-    const int b = blockIdx.z;
-    const int c_tile = blockIdx.x * TT, r_tile = blockIdx.y * TT;
-    const __nv_bfloat16* s = src + (size_t)b * R * C;
-    __nv_bfloat16* d = dst + (size_t)b * C * ld_dst;
-    for (int i = threadIdx.x; i < TT * 8; i += blockDim.x) {
-        const int rr = i >> 3, ch = i & 7;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r_tile + rr < R && c_tile + ch * 8 < C)
-            v = __ldg(reinterpret_cast<const uint4*>(s + (size_t)(r_tile + rr) * C + c_tile + ch * 8));
-        put8(&tile[rr][ch * 8], v);
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < TT * 8; i += blockDim.x) {
-        const int cc = i >> 3, ch = i & 7;
-        if (c_tile + cc < C && r_tile + ch * 8 < R)
-            *reinterpret_cast<uint4*>(d + (size_t)(c_tile + cc) * ld_dst + col0 + r_tile + ch * 8) =
-                gather8(tile, ch * 8, cc);
     }
     __syncthreads();
     pdl_trigger();
@@ -346,16 +318,6 @@ cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, i
     const dim3 grid((C + TT - 1) / TT, (ncols + TT - 1) / TT);
     launch_pdl(transpose_windows_kernel, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), ld_src, col0,
                C, E, offsets, kbase, klen, row_scale, static_cast<__nv_bfloat16*>(dst), ld_dst, ncols);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_batched(int dtype, const void* src, int batch, int R, int C, void* dst, size_t ld_dst,
-                                     int col0, cudaStream_t s) {
-    if (batch == 0 || R == 0 || C == 0) return cudaSuccess;
-    if (dtype != MOE_BF16 || R % 8 || C % 8 || ld_dst % 8 || col0 % 8) return cudaErrorInvalidValue;
-    const dim3 grid((C + TT - 1) / TT, (R + TT - 1) / TT, batch);
-    launch_pdl(transpose_batched_kernel, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), R, C,
-               static_cast<__nv_bfloat16*>(dst), ld_dst, col0);
     return cudaGetLastError();
 }
 

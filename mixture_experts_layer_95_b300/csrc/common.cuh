@@ -252,6 +252,13 @@ struct GemmProblem {
     // (weight gradients: a contraction over each expert's token rows)
     const int32_t* kbase;
     const int32_t* klen;
+    // MN-major B (launch_gemm_tc, Plain / Scale modes, ksplit 1, plain A): B1
+    // holds B^T per group, [G][K][N] (N a multiple of 8), read without a
+    // transposed copy.  kpart > 0: K = 2 kpart in two parts, A = [rows][2 kpart]
+    // (part 0 then part 1 of every row), B1 = part 0 of B^T [G][kpart][N], B2
+    // = part 1; each part is padded to whole 64-deep k-blocks with zeros.
+    int b_mn;
+    int kpart;
 };
 
 // Tensor-core (tcgen05) path, bf16 operands, fp32 accumulate.  Runs up to two
@@ -288,9 +295,6 @@ cudaError_t launch_k_windows(int E, int32_t* offsets, int32_t* kbase, int32_t* k
 cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, int C, int E, const int32_t* offsets,
                                      const int32_t* kbase, const int32_t* klen, const float* row_scale, void* dst,
                                      size_t ld_dst, int ncols, cudaStream_t s);
-// dst[b][c][col0 + r] = src[b][r][c] (bf16 out), batch of [R][C] matrices.
-cudaError_t launch_transpose_batched(int dtype, const void* src, int batch, int R, int C, void* dst, size_t ld_dst,
-                                     int col0, cudaStream_t s);
 // Per row: dGU = [g D U silu'(G) | g D silu(G)] (bf16), Hb = bf16(silu(G) U),
 // dgp[r] = sum_f D silu(G) U (when dgp != nullptr).
 cudaError_t launch_swiglu_backward(int rows_max, const int32_t* rows_dev, int F, const float* G, const float* U,

@@ -520,7 +520,7 @@ cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, in
     if (probs[0].G + (nprob > 1 ? probs[1].G : 0) > MAX_GROUPS + 1) return cudaErrorInvalidValue;
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
-        if (g.G < 1 || g.G > MAX_GROUPS || g.out2) return cudaErrorInvalidValue;
+        if (g.G < 1 || g.G > MAX_GROUPS || g.out2 || g.b_mn) return cudaErrorInvalidValue;
         // FP8: A holds the hi codes of the tokens, A2 the lo codes, a_scale the row scales
         if (w8 && (g.K % 16 != 0 || !g.wscale1 || (mode == kGemmSwiGLU && !g.wscale2) || !g.A2 || !g.a_scale))
             return cudaErrorInvalidValue;

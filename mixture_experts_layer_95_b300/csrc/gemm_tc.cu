@@ -94,6 +94,13 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     // to the next multiple of 64) and writes output rows g*M .. g*M + M - 1
     const int32_t* kbase[2];
     const int32_t* klen[2];
+    // MN-major B (Plain and Scale modes): tmB1 / tmB2 are 3-D maps {N, K, G}
+    // of matrices stored [G][K][N] (B^T per group), loaded as 64x64 boxes.
+    // kpart[q] > 0 splits K into two parts of kpart[q] each, every part padded
+    // to whole k-blocks: part 0 reads A part 0 and tmB1, part 1 A part 1 and
+    // tmB2, where tmA is then a 3-D map {kpart, 2, rows} of A = [rows][2 kpart].
+    int b_mn;
+    int kpart[2];
     int* status;
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
     int stall_producer;      // test switch: issue no loads, so the consumers' bounded waits run out
@@ -159,6 +166,26 @@ __device__ __forceinline__ int out_cols_per_tile() {
     return MODE == kGemmSwiGLU ? BN / 2 : BN;
 }
 
+// 64-deep k-blocks of one tile's K range (two padded parts when kpart is set)
+__device__ __forceinline__ int k_blocks(const TcParams& p, int prob) {
+    return p.kpart[prob] ? 2 * ((p.kpart[prob] + BK - 1) / BK) : (p.K[prob] + BK - 1) / BK;
+}
+
+// MN-major B: loads k-block kb of a tile -- A (BM rows, plain or part-split)
+// and nblk 64-column blocks of B^T starting at column n0 of group g -- onto
+// `bar`.  load3 / load2 issue one 3-D / 2-D TMA copy.
+template <typename Load3, typename Load2>
+__device__ __forceinline__ void load_kblock_bmn(const TcParams& p, int prob, int kb, int a_row0, int n0, int g,
+                                                int nblk, uint8_t* sa, uint8_t* sb, Load3 load3, Load2 load2) {
+    const int nkp = p.kpart[prob] ? (p.kpart[prob] + BK - 1) / BK : 1 << 30;
+    const int part = kb >= nkp ? 1 : 0;
+    const int k0 = (kb - part * nkp) * BK;
+    if (p.kpart[prob]) load3(sa, &p.tmA[prob], k0, part, a_row0);
+    else load2(sa, &p.tmA[prob], k0, a_row0);
+    const CUtensorMap* tb = part ? &p.tmB2[prob] : &p.tmB1[prob];
+    for (int j = 0; j < nblk; ++j) load3(sb + j * (BK * BK * 2), tb, n0 + j * BK, k0, g);
+}
+
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& p, int id) {
     Tile t;
@@ -184,7 +211,7 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& 
     t.rows_valid = min(BM, rows - t.m * BM);
     t.out_row0 = t.a_row0;
     t.k_off = 0;
-    int nk = (p.K[t.prob] + BK - 1) / BK;
+    int nk = k_blocks(p, t.prob);
     if (p.kbase[t.prob]) {  // K-grouped: shared A rows, the group's own K window
         t.out_row0 = t.g * p.M[t.prob] + t.m * BM;
         t.k_off = __ldg(p.kbase[t.prob] + t.g);
@@ -473,13 +500,24 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                     const uint32_t a_bytes = gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : A_BYTES;
                     mbar_expect_tx(&st.full[s], SLOT - A_BYTES + a_bytes);
                     const int kc = t.k_off + kb * BK;
-                    if (!gidx) tma_load_2d(sa, &p.tmA[t.prob], kc, t.a_row0, &st.full[s]);
-                    if (SC::kSplit) tma_load_2d(sa + A_BYTES, &p.tmA2[t.prob], kc, t.a_row0, &st.full[s]);
-                    if (MODE == kGemmSwiGLU) {
-                        tma_load_2d(sb, &p.tmB1[t.prob], kc, b_row0, &st.full[s]);
-                        tma_load_2d(sb + (W8 ? F8_BYTES : B_BYTES) / 2, &p.tmB2[t.prob], kc, b_row0, &st.full[s]);
+                    if (!W8 && MODE != kGemmSwiGLU && !SC::kSplit && p.b_mn) {  // B^T as 64-column blocks
+                        uint64_t* bar = &st.full[s];
+                        load_kblock_bmn(
+                            p, t.prob, kb, t.a_row0, t.n * BN, t.g, BN / BK, sa, sb,
+                            [bar](void* d, const CUtensorMap* tm, int c0, int c1, int c2) {
+                                tma_load_3d(d, tm, c0, c1, c2, bar);
+                            },
+                            [bar](void* d, const CUtensorMap* tm, int c0, int c1) { tma_load_2d(d, tm, c0, c1, bar); });
                     } else {
-                        tma_load_2d(sb, &p.tmB1[t.prob], kc, b_row0, &st.full[s]);
+                        if (!gidx) tma_load_2d(sa, &p.tmA[t.prob], kc, t.a_row0, &st.full[s]);
+                        if (SC::kSplit) tma_load_2d(sa + A_BYTES, &p.tmA2[t.prob], kc, t.a_row0, &st.full[s]);
+                        if (MODE == kGemmSwiGLU) {
+                            tma_load_2d(sb, &p.tmB1[t.prob], kc, b_row0, &st.full[s]);
+                            tma_load_2d(sb + (W8 ? F8_BYTES : B_BYTES) / 2, &p.tmB2[t.prob], kc, b_row0,
+                                        &st.full[s]);
+                        } else {
+                            tma_load_2d(sb, &p.tmB1[t.prob], kc, b_row0, &st.full[s]);
+                        }
                     }
                 }
                 if (gidx && lane * 4 < t.rows_valid)
@@ -503,7 +541,8 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            const bool bmn = !W8 && MODE != kGemmSwiGLU && !SC::kSplit && p.b_mn;
+            const uint32_t idesc = idesc_bf16_f32(BM, BN) | (bmn ? kIdescBMnMajor : 0u);
             int s = 0, w = 0;
             uint32_t ph = 0, pw = 0;
             int it = 0;
@@ -530,7 +569,8 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                     const uint32_t sb = W8 ? smem_u32(wide + (size_t)w * B_BYTES) : sa + BOFF;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t bdesc = sdesc_k_sw128(sb + kk * UMMA_K * 2);
+                        const uint64_t bdesc = bmn ? sdesc_mn_sw128(sb + kk * UMMA_K * 128, BK * BK * 2)
+                                                   : sdesc_k_sw128(sb + kk * UMMA_K * 2);
                         umma_bf16(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2), bdesc, idesc,
                                   (kb != t.kb0 || kk != 0) ? 1u : 0u);
                         if (SC::kSplit) umma_bf16(dtm, sdesc_k_sw128(sa + A_BYTES + kk * UMMA_K * 2), bdesc, idesc, 1u);
@@ -663,6 +703,15 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* t
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* tm, int c0, int c1, int c2,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+        "%3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                uint32_t accumulate) {
     asm volatile(
@@ -712,7 +761,7 @@ __device__ __forceinline__ Tile decode_tile_pair(const SmemTail& st, const TcPar
     t.out_row0 = t.a_row0;
     t.k_off = 0;
     t.kb0 = 0;
-    t.kb1 = (p.K[t.prob] + BK - 1) / BK;
+    t.kb1 = k_blocks(p, t.prob);
     return t;
 }
 
@@ -826,8 +875,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     uint8_t* sb = sa + A_BYTES;
                     const uint32_t full_leader = leader_addr(&st.full[s]);
                     if (leader) mbar_expect_tx(&st.full[s], 2 * PAIR_STAGE_BYTES);
-                    tma_load_2d_pair(sa, &p.tmA[t.prob], kb * BK, t.a_row0, full_leader);
-                    tma_load_2d_pair(sb, tmb, kb * BK, b_row, full_leader);
+                    if (MODE != kGemmSwiGLU && p.b_mn) {  // this CTA's 128 columns: two 64-column blocks
+                        load_kblock_bmn(
+                            p, t.prob, kb, t.a_row0, t.n * BN + rank * (BN / 2), t.g, BN / 2 / BK, sa, sb,
+                            [full_leader](void* d, const CUtensorMap* tm, int c0, int c1, int c2) {
+                                tma_load_3d_pair(d, tm, c0, c1, c2, full_leader);
+                            },
+                            [full_leader](void* d, const CUtensorMap* tm, int c0, int c1) {
+                                tma_load_2d_pair(d, tm, c0, c1, full_leader);
+                            });
+                    } else {
+                        tma_load_2d_pair(sa, &p.tmA[t.prob], kb * BK, t.a_row0, full_leader);
+                        tma_load_2d_pair(sb, tmb, kb * BK, b_row, full_leader);
+                    }
                     issued_parity[s] = ph;
                     used[s] = true;
                     if (++s == NST) {
@@ -847,7 +907,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+            const bool bmn = MODE != kGemmSwiGLU && p.b_mn;
+            const uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | (bmn ? kIdescBMnMajor : 0u);
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -869,7 +930,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                        umma_bf16_pair(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2), sdesc_k_sw128(sb + kk * UMMA_K * 2),
+                        umma_bf16_pair(dtm, sdesc_k_sw128(sa + kk * UMMA_K * 2),
+                                       bmn ? sdesc_mn_sw128(sb + kk * UMMA_K * 128, BK * BK * 2)
+                                           : sdesc_k_sw128(sb + kk * UMMA_K * 2),
                                        idesc, (kb != t.kb0 || kk != 0) ? 1u : 0u);
                     umma_commit_pair(&st.empty[s]);
                     if (++s == NST) {
@@ -985,19 +1048,39 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
         if (g.G < 1 || g.G > MAX_GROUPS) return cudaErrorInvalidValue;
-        if (g.a_gather) {
-            // A rows are gathered from a [a_src_rows][K] tensor, 4 rows per load
-            if (!make_tmap(&prm.tmA[q], g.A, g.a_src_rows, g.K, 1)) return cudaErrorInvalidValue;
-            prm.a_gather[q] = g.a_gather;
-            prm.a_src_rows[q] = g.a_src_rows;
-        } else if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) {
-            return cudaErrorInvalidValue;
+        if (q > 0 && g.b_mn != probs[0].b_mn) return cudaErrorInvalidValue;
+        if (g.b_mn) {
+            // B^T tiles of 64 K-rows x 64 columns; A plain, or split in two K parts
+            if ((mode != kGemmPlain && mode != kGemmScale) || g.a_gather || g.kbase || g.klen || ksplit != 1 ||
+                g.N % 8 != 0 || (g.kpart && (g.kpart % 8 != 0 || g.K != 2 * g.kpart || !g.B2)))
+                return cudaErrorInvalidValue;
+            const uint64_t N = (uint64_t)g.N, kp = (uint64_t)(g.kpart ? g.kpart : g.K);
+            if (!make_tmap_3d(&prm.tmB1[q], g.B1, N, kp, (uint64_t)g.G, N * 2, kp * N * 2, BK, BK, 1))
+                return cudaErrorInvalidValue;
+            if (g.kpart) {
+                if (!make_tmap_3d(&prm.tmB2[q], g.B2, N, kp, (uint64_t)g.G, N * 2, kp * N * 2, BK, BK, 1) ||
+                    !make_tmap_3d(&prm.tmA[q], g.A, kp, 2, (uint64_t)g.a_rows, kp * 2, 2 * kp * 2, BK, 1, BM))
+                    return cudaErrorInvalidValue;
+                prm.kpart[q] = g.kpart;
+            } else if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) {
+                return cudaErrorInvalidValue;
+            }
+            prm.b_mn = 1;
+        } else {
+            if (g.a_gather) {
+                // A rows are gathered from a [a_src_rows][K] tensor, 4 rows per load
+                if (!make_tmap(&prm.tmA[q], g.A, g.a_src_rows, g.K, 1)) return cudaErrorInvalidValue;
+                prm.a_gather[q] = g.a_gather;
+                prm.a_src_rows[q] = g.a_src_rows;
+            } else if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) {
+                return cudaErrorInvalidValue;
+            }
+            // B rows: one [N][K] matrix per group, or one shared by every group (K-grouped)
+            const int b_rows = g.kbase ? g.N : g.G * g.N;
+            if (!make_tmap(&prm.tmB1[q], g.B1, b_rows, g.K, b_box)) return cudaErrorInvalidValue;
+            if (mode == kGemmSwiGLU && !make_tmap(&prm.tmB2[q], g.B2, b_rows, g.K, b_box))
+                return cudaErrorInvalidValue;
         }
-        // B rows: one [N][K] matrix per group, or one shared by every group (K-grouped)
-        const int b_rows = g.kbase ? g.N : g.G * g.N;
-        if (!make_tmap(&prm.tmB1[q], g.B1, b_rows, g.K, b_box)) return cudaErrorInvalidValue;
-        if (mode == kGemmSwiGLU && !make_tmap(&prm.tmB2[q], g.B2, b_rows, g.K, b_box))
-            return cudaErrorInvalidValue;
         if (mode == kGemmScaleSplit && !make_tmap(&prm.tmA2[q], g.A2, g.a_rows, g.K, BM)) return cudaErrorInvalidValue;
         if (ksplit > 1) {
             // every slice needs at least one k-block
@@ -1071,6 +1154,7 @@ cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int
         } else if (!make_tmap(&prm.tmA[q], g.A, g.a_rows, g.K, BM)) {
             return cudaErrorInvalidValue;
         }
+        if (g.b_mn) return cudaErrorInvalidValue;
         if (!make_tmap_u8(&prm.tmB1[q], g.B1, g.G * g.N, g.K, b_box)) return cudaErrorInvalidValue;
         if (mode == kGemmSwiGLU && !make_tmap_u8(&prm.tmB2[q], g.B2, g.G * g.N, g.K, b_box))
             return cudaErrorInvalidValue;

@@ -78,6 +78,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int c0, int c1, int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Four rows (r0..r3) x 64 columns starting at column c0 of a 2-D tensor whose
 // map has a one-row box; lands in shared memory as four consecutive 128-byte
 // rows, swizzled like a tiled load to the same address.
@@ -110,6 +118,25 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(2u) << 61;  // 128-byte swizzle
     return d;
 }
+
+// Shared-memory matrix descriptor: MN-major operand, 128-byte swizzle.  Each
+// 128-byte row holds 64 consecutive M (or N) elements of one K index; 8
+// K-rows form a 1024-byte swizzle atom and consecutive atoms along K are SBO
+// = 1024 bytes apart; the next 64 M (N) elements start LBO = mn_block_bytes
+// further on.  One kind::f16 MMA consumes 16 K-rows (two atoms), so the K
+// steps of a 64-deep block advance the start address by 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_block_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor bit: B is MN-major (transposed) in shared memory.
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 
 // Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, dense, M x N.
@@ -251,6 +278,23 @@ inline bool make_tmap(CUtensorMap* tm, const void* base, int rows, int K, int bo
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor with dims {d0 (contiguous), d1, d2} and byte strides s1, s2
+// of dims 1 and 2; box = b0 x b1 x b2, 128-byte swizzle (b0 = 64).  Used for
+// MN-major operand tiles (64 M/N elements x 64 K-rows of one group) and for
+// K ranges padded per part (coordinates past a dim's extent read as zero).
+inline bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                         uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {d0, d1 > 0 ? d1 : 1, d2 > 0 ? d2 : 1};
+    const cuuint64_t strides[2] = {s1, s2};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -34,6 +34,8 @@ CASES = [
     Workload("bwd_plain_gates", T=130, d=128, E=4, F=128, k=2, renormalize=False),
     Workload("bwd_gemm_router", T=300, d=128, E=40, F=128, k=4),
     Workload("bwd_one_token_shared", T=1, d=256, E=8, F=256, k=2, n_shared=1, F_s=128),
+    # >= 512 rows per expert: the row-indexed products run on CTA pairs (ragged N and K)
+    Workload("bwd_pair_shared", T=1100, d=272, E=4, F=400, k=2, n_shared=1, F_s=208),
 ]
 
 
