@@ -1067,8 +1067,8 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
     float* G = at<float>(ws, B.G);
     float* U = at<float>(ws, B.U);
     float* D = at<float>(ws, B.D);
-    // large segments: the row-indexed products run on CTA pairs (Scale mode
-    // without gates is the plain product)
+    // large segments: every product runs on CTA pairs (Scale mode without
+    // gates is the plain product)
     const bool pair = use_pair_gemm(c);
     const int pm = pair ? kGemmScale : kGemmPlain;
     {
@@ -1126,13 +1126,13 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
     {
         GemmProblem q1[2] = {windows(dGT, F, xpT, d, nc, kbase, klen, E, dw1),
                              windows(at<void>(ws, B.dGsT), Fs, at<void>(ws, B.xT), d, ncs, s_kbase, s_klen, 1, dws1)};
-        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, q1, np, status, sms, s));
+        MOE_LAUNCH(launch_gemm_tc(pm, q1, np, status, sms, s, 1, pair));
         GemmProblem q3[2] = {windows(dUT, F, xpT, d, nc, kbase, klen, E, dw3),
                              windows(at<void>(ws, B.dUsT), Fs, at<void>(ws, B.xT), d, ncs, s_kbase, s_klen, 1, dws3)};
-        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, q3, np, status, sms, s));
+        MOE_LAUNCH(launch_gemm_tc(pm, q3, np, status, sms, s, 1, pair));
         GemmProblem q2[2] = {windows(dysT, d, HbT, F, nc, kbase, klen, E, dw2),
                              windows(at<void>(ws, B.dyT), d, at<void>(ws, B.HbsT), Fs, ncs, s_kbase, s_klen, 1, dws2)};
-        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, q2, np, status, sms, s));
+        MOE_LAUNCH(launch_gemm_tc(pm, q2, np, status, sms, s, 1, pair));
     }
 
     // router: gate gradients -> logits (+ balance loss) -> W_g and x

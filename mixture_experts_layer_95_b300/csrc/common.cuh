@@ -246,7 +246,8 @@ struct GemmProblem {
     // E4M3 codes of every token row, a_scale its power-of-two scale (indexed
     // like the rows of A, or of the gather source), A row = a_scale * (hi + lo)
     const float* a_scale;
-    // K-grouped problem (launch_gemm_tc, ksplit 1, no offsets): group g
+    // K-grouped problem (launch_gemm_tc, ksplit 1, no offsets; Plain mode, or
+    // Scale mode without row scales on CTA pairs): group g
     // multiplies A rows [0, M) by B rows [0, N) over the K window
     // [kbase[g], kbase[g] + klen[g]) and writes output rows g*M .. g*M + M - 1
     // (weight gradients: a contraction over each expert's token rows)

@@ -762,6 +762,11 @@ __device__ __forceinline__ Tile decode_tile_pair(const SmemTail& st, const TcPar
     t.k_off = 0;
     t.kb0 = 0;
     t.kb1 = k_blocks(p, t.prob);
+    if (p.kbase[t.prob]) {  // K-grouped: shared A rows, the group's own K window
+        t.out_row0 = t.g * p.M[t.prob] + first;
+        t.k_off = __ldg(p.kbase[t.prob] + t.g);
+        t.kb1 = (__ldg(p.klen[t.prob] + t.g) + BK - 1) / BK;
+    }
     return t;
 }
 
@@ -862,8 +867,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 if (MODE == kGemmSwiGLU) {  // rank 0: the W1 (gate) rows, rank 1: the W3 (up) rows
                     b_row = t.g * p.N[t.prob] + t.n * (BN / 2);
                     tmb = rank == 0 ? &p.tmB1[t.prob] : &p.tmB2[t.prob];
-                } else {
-                    b_row = t.g * p.N[t.prob] + t.n * BN + rank * (BN / 2);
+                } else {  // K-grouped problems share one B matrix
+                    b_row = (p.kbase[t.prob] ? 0 : t.g * p.N[t.prob]) + t.n * BN + rank * (BN / 2);
                     tmb = &p.tmB1[t.prob];
                 }
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
@@ -885,8 +890,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                                 tma_load_2d_pair(d, tm, c0, c1, full_leader);
                             });
                     } else {
-                        tma_load_2d_pair(sa, &p.tmA[t.prob], kb * BK, t.a_row0, full_leader);
-                        tma_load_2d_pair(sb, tmb, kb * BK, b_row, full_leader);
+                        tma_load_2d_pair(sa, &p.tmA[t.prob], t.k_off + kb * BK, t.a_row0, full_leader);
+                        tma_load_2d_pair(sb, tmb, t.k_off + kb * BK, b_row, full_leader);
                     }
                     issued_parity[s] = ph;
                     used[s] = true;
@@ -1098,8 +1103,9 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         prm.K[q] = g.K;
         prm.a_rows[q] = g.a_rows;
         if (g.kbase || g.klen) {
-            if (!g.kbase || !g.klen || g.offsets || g.a_gather || ksplit != 1 || pair || mode != kGemmPlain)
-                return cudaErrorInvalidValue;
+            // 1-CTA: Plain mode; CTA pairs: Scale mode without row scales (the same product)
+            const bool mode_ok = pair ? (mode == kGemmScale && !g.row_scale) : mode == kGemmPlain;
+            if (!g.kbase || !g.klen || g.offsets || g.a_gather || ksplit != 1 || !mode_ok) return cudaErrorInvalidValue;
             prm.kbase[q] = g.kbase;
             prm.klen[q] = g.klen;
         }
