@@ -115,11 +115,15 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
     // 1. global counts, this block's prefix, capacity cut
     for (int e = threadIdx.x; e < E; e += kScanThreads) {
         int tot = 0, before = 0;
-#pragma unroll 8
-        for (int b = 0; b < a.nblk; ++b) {  // independent loads: keep several in flight
-            const int v = __ldg(a.block_hist + (size_t)b * E + e);
-            before += (b < (int)blockIdx.x) ? v : 0;
-            tot += v;
+        for (int b0 = 0; b0 < a.nblk; b0 += 32) {  // 32 independent loads in flight per batch
+            int v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = b0 + j < a.nblk ? __ldg(a.block_hist + (size_t)(b0 + j) * E + e) : 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                before += (b0 + j < (int)blockIdx.x) ? v[j] : 0;
+                tot += v[j];
+            }
         }
         s_before[e] = before;
         s_kept[e] = (a.capacity >= 0 && tot > a.capacity) ? a.capacity : tot;
@@ -140,9 +144,16 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
             // load statistics: f = counts/(T k), p = mean softmax row, L = alpha E sum f p
             float part = 0.f;
             for (int e = threadIdx.x; e < E; e += kScanThreads) {
-                float ps = 0.f;
-#pragma unroll 8
-                for (int b = 0; b < a.o.p_nblk; ++b) ps += __ldg(a.o.p_part + (size_t)b * E + e);
+                float ps = 0.f;  // row order, as moe_load_stats sums it; 32 loads in flight
+                for (int b0 = 0; b0 < a.o.p_nblk; b0 += 32) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = b0 + j < a.o.p_nblk ? __ldg(a.o.p_part + (size_t)(b0 + j) * E + e) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (b0 + j < a.o.p_nblk) ps += v[j];
+                }
                 const float pm = ps / (float)a.T;
                 const float f = (float)s_wcnt[e] / ((float)a.T * (float)a.k);
                 if (a.o.p_mean) a.o.p_mean[e] = pm;
