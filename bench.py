@@ -42,6 +42,7 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s on 1 B300; % of bf16 tensor peak or HBM roofline"
 UNIT = "tokens/s"
 FALLBACK = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0)
+FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12  # CUDA-core fp32 FMA peak at the maximum SM clock
 # profiles/traffic.json: per workload, the up GEMM's DRAM bytes per launch from
 # an ncu capture, with the kernel sources it was taken on ("sources", default
 # the prefill GEMM's) and their hash; a changed source voids the figure
@@ -386,7 +387,16 @@ def run_ours(args):
     if q8 is not None:
         up_kernel = up_kernel.replace("<SwiGLU", "<SwiGLU, FP8 weights")
         plan = dict(plan, weights="fp8_e4m3")
-    if tensor_bound:
+    if plan["up"] == "simt":
+        # fp32 layers run on the CUDA cores: FMA-pipe bound (fp32 FMA peak from
+        # unit counts and the maximum SM clock: 148 SMs x 128 lanes x 2 FLOP x
+        # 2.032 GHz = 77.0 TFLOP/s)
+        achieved = up_flops / (up_ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_FMA_TFLOPS, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / round(FP32_FMA_TFLOPS, 1), 4), "traffic": None, "kernel": up_kernel,
+                "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2.032 GHz",
+                "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4)}
+    elif tensor_bound:
         achieved = up_flops / (up_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
