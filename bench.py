@@ -385,7 +385,8 @@ def run_ours(args):
                  "tc_decode64": "grouped_gemm_decode_kernel<SwiGLU, NT=64> (up GEMM, weights on M)",
                  "simt": "grouped_gemm_simt_kernel<SwiGLU> (up GEMM)"}[plan["up"]]
     if q8 is not None:
-        up_kernel = up_kernel.replace("<SwiGLU", "<SwiGLU, FP8 weights")
+        # with FP8 weights the decode GEMM takes 48 token rows where bf16 takes 64
+        up_kernel = up_kernel.replace("<SwiGLU", "<SwiGLU, FP8 weights").replace("NT=64", "NT=48")
         plan = dict(plan, weights="fp8_e4m3")
     if plan["up"] == "simt":
         # fp32 layers run on the CUDA cores: FMA-pipe bound (fp32 FMA peak from

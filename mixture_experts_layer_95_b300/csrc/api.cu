@@ -66,10 +66,12 @@ bool use_gather_a(const moe_config& c) {
 // when the touched experts average at most 16 rows, else 64.
 bool use_decode_gemm(const moe_config& c) { return c.dtype == MOE_BF16 && !use_h_split(c) && use_gather_a(c); }
 
-int decode_tile_rows(const moe_config& c) {
+int decode_tile_rows(const moe_config& c, bool w8 = false) {
     const long long n = perm_rows(c);
     const long long touched = n < c.E ? n : c.E;
-    return n <= 16 * touched ? 32 : 64;
+    // FP8: a 64-row tile's hi and lo token codes (16 KB) leave room for four
+    // 32 KB weight stages only; 48 rows keep five
+    return n <= 16 * touched ? 32 : (w8 ? 48 : 64);
 }
 
 // ---- split-K for decode-sized batches ----------------------------------------
@@ -158,7 +160,7 @@ Splits choose_splits(const moe_config& c, bool w8 = false) {
 struct Layout {
     size_t status, topk_ids, gates, p_part, block_hist, counts, kept, offsets, n_dropped, sorted, slot_pos,
         gates_perm, p_mean, f, L, logits, probs, x_perm, h, h_shared, h_lo, h_shared_lo, y_perm, y_shared, part_up,
-        part_up_shared, part_dn, part_dn_shared, xq, xq_s, hq, hq_s, hsq, hsq_s, total;
+        part_up_shared, part_dn, part_dn_shared, xq, xq_s, xsq, xsq_s, hq, hq_s, hsq, hsq_s, total;
 };
 
 Layout layout(const moe_config& c) {
@@ -211,8 +213,10 @@ Layout layout(const moe_config& c) {
     // decode-sized batches with FP8 weights: the tokens and H as E4M3 hi/lo
     // code pairs with a scale per row (the FP8 MMA takes FP8 on both sides)
     const bool q8 = use_decode_gemm(c);
-    l.xq = take(q8 ? 2 * (size_t)c.T * c.d : 0);
-    l.xq_s = take(q8 ? 4 * (size_t)c.T : 0);
+    l.xq = take(q8 ? 2 * n * c.d : 0);  // token rows in expert order
+    l.xq_s = take(q8 ? 4 * n : 0);
+    l.xsq = take(q8 && c.n_shared ? 2 * (size_t)c.T * c.d : 0);  // every token, for the shared expert
+    l.xsq_s = take(q8 && c.n_shared ? 4 * (size_t)c.T : 0);
     l.hq = take(q8 ? 2 * n * c.d_ff : 0);
     l.hq_s = take(q8 ? 4 * n : 0);
     l.hsq = take(q8 && c.n_shared ? 2 * (size_t)c.T * c.d_ff_shared : 0);
@@ -513,16 +517,27 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     }
     int* status = at<int>(ws, L.status);
     // FP8 decode GEMMs read the tokens (and H) as E4M3 hi/lo codes: x -> xq
-    // here, H -> hq between the two GEMMs
+    // (rows already in expert order, so the up GEMM loads plain tiles instead
+    // of gathering twice as many code rows) and xsq (the shared expert's) here,
+    // H -> hq between the two GEMMs
     const bool q8 = w8 && use_decode_gemm(c);
     uint8_t* xq = q8 ? at<uint8_t>(ws, L.xq) : nullptr;
+    uint8_t* xsq = q8 && c.n_shared ? at<uint8_t>(ws, L.xsq) : nullptr;
     uint8_t* hq = q8 ? at<uint8_t>(ws, L.hq) : nullptr;
     uint8_t* hsq = q8 && c.n_shared ? at<uint8_t>(ws, L.hsq) : nullptr;
+    if (q8 && !gather_idx) return MOE_ERR_SHAPE;  // the fused layer always passes the expert order
     if (q8) {
+        up[0].A = xq;
+        up[0].A2 = xq + (size_t)n * c.d;
+        up[0].a_scale = at<float>(ws, L.xq_s);
+        up[0].a_gather = nullptr;
+        up[0].a_rows = n;
+        if (c.n_shared) {
+            up[1].A = xsq;
+            up[1].A2 = xsq + (size_t)c.T * c.d;
+            up[1].a_scale = at<float>(ws, L.xsq_s);
+        }
         for (int q = 0; q < np; ++q) {
-            up[q].A = xq;
-            up[q].A2 = xq + (size_t)c.T * c.d;
-            up[q].a_scale = at<float>(ws, L.xq_s);
             down[q].A = q == 0 ? hq : hsq;
             down[q].A2 = q == 0 ? hq + (size_t)n * c.d_ff : hsq + (size_t)c.T * c.d_ff_shared;
             down[q].a_scale = at<float>(ws, q == 0 ? L.hq_s : L.hsq_s);
@@ -530,13 +545,17 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     }
     if (q8) {  // token rows for the up GEMM, timed with the gather step
         StageScope scope(kStageGather, s);
-        MOE_LAUNCH(launch_split_e4m3(c.T, c.d, x, nullptr, xq, xq + (size_t)c.T * c.d, at<float>(ws, L.xq_s), s));
+        MOE_LAUNCH(launch_split_e4m3(n, c.d, x, c.T, gather_idx, offsets + c.E, xq, xq + (size_t)n * c.d,
+                                     at<float>(ws, L.xq_s), s));
+        if (c.n_shared)
+            MOE_LAUNCH(launch_split_e4m3(c.T, c.d, x, c.T, nullptr, nullptr, xsq, xsq + (size_t)c.T * c.d,
+                                         at<float>(ws, L.xsq_s), s));
     }
     {
         StageScope scope(kStageUp, s);
         if (use_decode_gemm(c)) {
             MOE_LAUNCH(launch_gemm_decode(kGemmSwiGLU, up, np, status, sms, s, sp.up, w8 != nullptr,
-                                          decode_tile_rows(c)));
+                                          decode_tile_rows(c, w8 != nullptr)));
             if (sp.up > 1) {
                 MOE_LAUNCH(launch_swiglu_finalize(n, offsets + c.E, c.d_ff, sp.up, up[0].part, h, nullptr, s));
                 if (c.n_shared)
@@ -565,14 +584,14 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
         StageScope scope(kStageDown, s);
         if (use_decode_gemm(c)) {
             if (q8) {
-                MOE_LAUNCH(launch_split_e4m3(n, c.d_ff, h, offsets + c.E, hq, hq + (size_t)n * c.d_ff,
+                MOE_LAUNCH(launch_split_e4m3(n, c.d_ff, h, n, nullptr, offsets + c.E, hq, hq + (size_t)n * c.d_ff,
                                              at<float>(ws, L.hq_s), s));
                 if (c.n_shared)
-                    MOE_LAUNCH(launch_split_e4m3(c.T, c.d_ff_shared, hs, nullptr, hsq,
+                    MOE_LAUNCH(launch_split_e4m3(c.T, c.d_ff_shared, hs, c.T, nullptr, nullptr, hsq,
                                                  hsq + (size_t)c.T * c.d_ff_shared, at<float>(ws, L.hsq_s), s));
             }
             MOE_LAUNCH(launch_gemm_decode(kGemmScale, down, np, status, sms, s, sp.down, w8 != nullptr,
-                                          decode_tile_rows(c)));
+                                          decode_tile_rows(c, w8 != nullptr)));
             if (sp.down > 1 && reduce_down) {
                 MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
                 if (c.n_shared)

@@ -281,7 +281,8 @@ cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int
                               cudaStream_t s, int ksplit = 1);
 
 // Decode-sized batches: the same grouped GEMM with the weights on the MMA's M
-// side (D^T = W X^T; nt = 32 or 64 token rows per tile), bf16 or FP8 (w8)
+// side (D^T = W X^T; nt = 32 or 64 token rows per tile, or 48 with FP8
+// weights, which keeps five stages in flight), bf16 or FP8 (w8)
 // weights, SwiGLU and Scale modes, split-K and gathered token rows; no split H.
 cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
                                cudaStream_t s, int ksplit, bool w8, int nt);
@@ -317,12 +318,14 @@ cudaError_t launch_wgate_grad(int dtype, int T, int E, int d, const float* dlogi
 cudaError_t launch_quantize_fp8(int dtype, long long rows, int cols, const void* w, uint8_t* q, float* scale,
                                 cudaStream_t s);
 
-// bf16 rows [rows][K] (K a multiple of 8) -> E4M3 hi and lo code rows and a
+// bf16 rows (K a multiple of 8) -> E4M3 hi and lo code rows [rows][K] and a
 // power-of-two scale per row, row = scale * (hi + lo) (exact for entries
-// within 2^10 of the row's largest magnitude); rows at or beyond *live_rows
-// (nullable) are skipped.  Feeds the FP8 tensor-core path of the decode GEMM.
-cudaError_t launch_split_e4m3(int rows, int K, const void* x, const int32_t* live_rows, uint8_t* hi, uint8_t* lo,
-                              float* scale, cudaStream_t s);
+// within 2^10 of the row's largest magnitude).  Output row r is row
+// gather[r] of x ([x_rows][K]) when gather is given, else row r; rows at or
+// beyond *live_rows (nullable) are skipped.  Feeds the FP8 tensor-core path
+// of the decode GEMM.
+cudaError_t launch_split_e4m3(int rows, int K, const void* x, int x_rows, const int32_t* gather,
+                              const int32_t* live_rows, uint8_t* hi, uint8_t* lo, float* scale, cudaStream_t s);
 
 // H[r][f] = silu(sum_s P[s][r][f]) * sum_s P[s][r][N + f] (bf16, and the lo
 // half when h_lo != nullptr) for r < rows, rows = *rows_dev when non-null.

@@ -92,18 +92,26 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(long long rows, int c
 // 4 more (a bf16 value has 8), so hi + lo == x / s exactly whenever lo stays
 // at or above E4M3's smallest step 2^-9, i.e. for every |x| >= max|x| * 2^-10;
 // smaller entries carry an absolute error of at most s * 2^-10 <= max|x| *
-// 2^-17.  Rows at or beyond *live_rows (when given) are skipped.
+// 2^-17.  Row r of the output is row gather[r] of x when gather is given
+// (token rows in expert order); rows at or beyond *live_rows (when given)
+// are skipped.
 constexpr int kSplitThreads = 256;
 
 __global__ void __launch_bounds__(kSplitThreads) split_e4m3_kernel(int K, const __nv_bfloat16* __restrict__ x,
+                                                                   int x_rows, const int32_t* __restrict__ gather,
                                                                    const int32_t* __restrict__ live_rows,
                                                                    uint8_t* __restrict__ hi, uint8_t* __restrict__ lo,
                                                                    float* __restrict__ scale) {
     __shared__ float s_max[kSplitThreads / 32];
     pdl_wait();
     const int row = blockIdx.x;
-    if (!live_rows || row < __ldg(live_rows)) {
-        const __nv_bfloat16* src = x + (size_t)row * K;
+    int src_row = row;
+    if (gather) {
+        src_row = __ldg(gather + row);
+        if (src_row < 0 || src_row >= x_rows) src_row = -1;  // the grouping scan wrote it; never taken
+    }
+    if ((!live_rows || row < __ldg(live_rows)) && src_row >= 0) {
+        const __nv_bfloat16* src = x + (size_t)src_row * K;
         float amax = 0.f;
         for (int c = threadIdx.x * 8; c < K; c += kSplitThreads * 8) {
             float v[8];
@@ -150,12 +158,12 @@ __global__ void __launch_bounds__(kSplitThreads) split_e4m3_kernel(int K, const 
 
 }  // namespace
 
-cudaError_t launch_split_e4m3(int rows, int K, const void* x, const int32_t* live_rows, uint8_t* hi, uint8_t* lo,
-                              float* scale, cudaStream_t s) {
+cudaError_t launch_split_e4m3(int rows, int K, const void* x, int x_rows, const int32_t* gather,
+                              const int32_t* live_rows, uint8_t* hi, uint8_t* lo, float* scale, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     if (K % 8 != 0) return cudaErrorInvalidValue;
     launch_pdl(split_e4m3_kernel, dim3((unsigned)rows), dim3(kSplitThreads), 0, s, K,
-               static_cast<const __nv_bfloat16*>(x), live_rows, hi, lo, scale);
+               static_cast<const __nv_bfloat16*>(x), x_rows, gather, live_rows, hi, lo, scale);
     return cudaGetLastError();
 }
 

@@ -82,9 +82,7 @@ struct DecTail {
     int abort_flag;
     int total[2];
     int gbase[2];
-    int tile_start[MAX_GROUPS + 1];
-    int row0[MAX_GROUPS + 1];
-    int rows[MAX_GROUPS + 1];
+    int tile_start[MAX_GROUPS + 1];  // a group's rows come from the offsets (grp_rows)
 };
 
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
@@ -112,6 +110,8 @@ constexpr size_t dec_smem_bytes() {
 
 static_assert(dec_stages<false, 32>() >= 4 && dec_stages<false, 64>() >= 4, "bf16 decode ring too shallow");
 static_assert(dec_stages<true, 32>() >= 4 && dec_stages<true, 64>() >= 4, "FP8 decode ring too shallow");
+static_assert(dec_stages<true, 48>() >= 5 && dec_smem_bytes<true, 48>() <= kSmemLimit,
+              "FP8 decode with 48 token rows: five stages");
 static_assert(dec_smem_bytes<true, 32>() <= kSmemLimit && dec_smem_bytes<false, 64>() <= kSmemLimit &&
                   dec_smem_bytes<true, 64>() <= kSmemLimit && dec_smem_bytes<false, 32>() <= kSmemLimit,
               "decode GEMM exceeds shared memory");
@@ -128,6 +128,18 @@ __device__ __forceinline__ int dec_cols() {
     return MODE == kGemmSwiGLU ? WR / 2 : WR;
 }
 
+// Rows [lo, hi) of group g of problem q: its offsets, or all M rows; a range
+// that does not fit the token matrix is empty (the tile scan records it).
+__device__ __forceinline__ void grp_rows(const DecParams& p, int q, int g, int& lo, int& hi) {
+    lo = 0;
+    hi = p.M[q];
+    if (p.offsets[q]) {
+        lo = __ldg(p.offsets[q] + g);
+        hi = __ldg(p.offsets[q] + g + 1);
+    }
+    if (lo < 0 || hi < lo || hi > p.x_rows[q]) lo = hi = 0;
+}
+
 template <int MODE, int NT, int KPS>
 __device__ __forceinline__ DTile dec_tile(const DecTail& st, const DecParams& p, int id) {
     DTile t;
@@ -142,14 +154,16 @@ __device__ __forceinline__ DTile dec_tile(const DecTail& st, const DecParams& p,
         else hi = mid - 1;
     }
     t.g = lo;
-    const int rows = st.rows[gb + lo];
+    int row0, row1;
+    grp_rows(p, t.prob, lo, row0, row1);
+    const int rows = row1 - row0;
     const int mt = (rows + NT - 1) / NT;
     int r = local - ts[lo];
     t.ks = r % p.ksplit;  // K slices of one output tile are adjacent, then token chunks
     r /= p.ksplit;
     t.n = r / mt;
     t.m = r - t.n * mt;
-    t.x_row0 = st.row0[gb + lo] + t.m * NT;
+    t.x_row0 = row0 + t.m * NT;
     t.rows_valid = min(NT, rows - t.m * NT);
     const int nk = (p.K[t.prob] + KPS * BK - 1) / (KPS * BK);
     t.kb0 = t.ks * nk / p.ksplit;
@@ -174,6 +188,15 @@ __device__ __forceinline__ float dec_xscale(const DecParams& p, const DTile& t, 
     return __ldg(xs + src);
 }
 
+// 32 accumulator columns from c0 on, or the last 16 when NT is not a
+// multiple of 32 (NT = 48), so that a load never crosses into the next
+// accumulator half.
+template <int NT>
+__device__ __forceinline__ void dec_tmem_ld(uint32_t taddr, int c0, uint32_t (&r)[32]) {
+    if (NT % 32 != 0 && NT - c0 < 32) tmem_ld16(taddr, r);
+    else tmem_ld32(taddr, r);
+}
+
 // Epilogue of one tile for this thread's weight row.  The accumulator half h
 // (TMEM columns h*NT .. h*NT+NT-1) holds, per token column j, the dot product
 // of token row x_row0 + j with weight row  (tile row h*128 + lane).
@@ -190,8 +213,8 @@ __device__ __forceinline__ void dec_epilogue(const DecParams& p, const DTile& t,
         for (int c0 = 0; c0 < NT; c0 += 32) {
             uint32_t g[32], u[32];
             __syncwarp();
-            tmem_ld32(tacc + c0, g);
-            tmem_ld32(tacc + NT + c0, u);
+            dec_tmem_ld<NT>(tacc + c0, c0, g);
+            dec_tmem_ld<NT>(tacc + NT + c0, c0, u);
             tmem_ld_wait();
             if (!live) continue;
             const int jn = min(32, t.rows_valid - c0);
@@ -226,7 +249,7 @@ __device__ __forceinline__ void dec_epilogue(const DecParams& p, const DTile& t,
             for (int c0 = 0; c0 < NT; c0 += 32) {
                 uint32_t v[32];
                 __syncwarp();
-                tmem_ld32(tacc + h * NT + c0, v);
+                dec_tmem_ld<NT>(tacc + h * NT + c0, c0, v);
                 tmem_ld_wait();
                 if (!live) continue;
                 const int jn = min(32, t.rows_valid - c0);
@@ -297,17 +320,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
                     const int g = base + lane;
                     int tiles = 0;
                     if (g < p.G[q]) {
-                        int lo = 0, hi = p.M[q];
-                        if (p.offsets[q]) {
-                            lo = p.offsets[q][g];
-                            hi = p.offsets[q][g + 1];
+                        int lo, hi;
+                        grp_rows(p, q, g, lo, hi);
+                        if (p.offsets[q]) {  // report a range grp_rows emptied
+                            const int a = p.offsets[q][g], b = p.offsets[q][g + 1];
+                            if (a < 0 || b < a || b > p.x_rows[q]) record_status(p.status, kStatusBounds);
                         }
-                        if (lo < 0 || hi < lo || hi > p.x_rows[q]) {
-                            record_status(p.status, kStatusBounds);
-                            lo = hi = 0;
-                        }
-                        st.row0[gb + g] = lo;
-                        st.rows[gb + g] = hi - lo;
                         tiles = ((hi - lo + NT - 1) / NT) * ncb * p.ksplit;
                     }
                     int incl = tiles;
@@ -504,6 +522,7 @@ cudaError_t launch_dec(const DecParams& prm, int grid, cudaStream_t s) {
 
 template <int MODE, bool W8>
 cudaError_t launch_dec_nt(const DecParams& prm, int nt, int grid, cudaStream_t s) {
+    if (nt == 48) return W8 ? launch_dec<MODE, true, 48>(prm, grid, s) : cudaErrorInvalidValue;
     return nt == 32 ? launch_dec<MODE, W8, 32>(prm, grid, s) : launch_dec<MODE, W8, 64>(prm, grid, s);
 }
 
@@ -511,7 +530,8 @@ cudaError_t launch_dec_nt(const DecParams& prm, int nt, int grid, cudaStream_t s
 
 cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
                                cudaStream_t s, int ksplit, bool w8, int nt) {
-    if (nprob < 1 || nprob > 2 || ksplit < 1 || (nt != 32 && nt != 64)) return cudaErrorInvalidValue;
+    if (nprob < 1 || nprob > 2 || ksplit < 1 || (nt != 32 && nt != 64 && !(nt == 48 && w8)))
+        return cudaErrorInvalidValue;
     if (mode != kGemmSwiGLU && mode != kGemmScale) return cudaErrorInvalidValue;
     DecParams prm;
     memset(&prm, 0, sizeof(prm));

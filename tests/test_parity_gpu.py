@@ -39,6 +39,8 @@ SMALL = [
     Workload("split_k_shared_t3_bf16", T=3, d=256, E=16, F=320, k=2, n_shared=1, F_s=192, select_bias=True,
              h_split=True),
     Workload("decode_like_t5_bf16", T=5, d=512, E=8, F=512, k=2),
+    # 17..32 rows per touched expert: 64-row token tiles of the decode GEMM
+    Workload("decode_64rows_shared_bf16", T=100, d=256, E=8, F=320, k=2, n_shared=1, F_s=192),
     Workload("many_tiles_bf16", T=1000, d=256, E=4, F=640, k=2),
     # >= 512 rows per expert: both GEMMs run on CTA pairs (256-row tiles whose
     # upper half may be empty at a segment end; N tail of 64 in the down GEMM)
