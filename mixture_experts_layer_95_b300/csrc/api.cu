@@ -53,9 +53,8 @@ bool use_pair_gemm(const moe_config& c) {
     return c.dtype == MOE_BF16 && c.h_split == 0 && n >= 512 * touched;
 }
 
-// Decode-sized bf16 batches (at most 32 rows per touched expert on average):
-// the up GEMM gathers x rows itself, so the layer skips the permuted copy.
-bool use_gather_a(const moe_config& c) {
+// Decode-sized bf16 batches: at most 32 rows per touched expert on average.
+bool decode_sized(const moe_config& c) {
     const long long n = perm_rows(c);
     const long long touched = n < c.E ? n : c.E;
     return c.dtype == MOE_BF16 && n <= 32 * touched;
@@ -64,7 +63,18 @@ bool use_gather_a(const moe_config& c) {
 // Decode-sized bf16 batches with a single bf16 H: both expert GEMMs put the
 // weights on the MMA's M side (gemm_decode.cu), with 32 token rows per tile
 // when the touched experts average at most 16 rows, else 64.
-bool use_decode_gemm(const moe_config& c) { return c.dtype == MOE_BF16 && !use_h_split(c) && use_gather_a(c); }
+bool use_decode_gemm(const moe_config& c) { return decode_sized(c) && !use_h_split(c); }
+
+// The up GEMM gathers x rows itself (TMA gather4, 4 rows per load), so the
+// layer skips the permuted copy: decode-sized batches, except that the
+// decode GEMM with 64-row token tiles reads an explicit copy as plain tiles
+// (16 gather4 loads per stage would limit its weight stream).
+bool use_gather_a(const moe_config& c) {
+    if (!decode_sized(c)) return false;
+    const long long n = perm_rows(c);
+    const long long touched = n < c.E ? n : c.E;
+    return !use_decode_gemm(c) || n <= 16 * touched;
+}
 
 int decode_tile_rows(const moe_config& c, bool w8 = false) {
     const long long n = perm_rows(c);
@@ -629,7 +639,8 @@ int forward_tail(const moe_config& c, const Layout& L, void* ws, const void* x, 
     int* status = at<int>(ws, L.status);
     void* x_perm = nullptr;
     const int32_t* gather_idx = nullptr;
-    if (use_gather_a(c)) {
+    // FP8 decode batches: the E4M3 split of x puts the rows in expert order itself
+    if (use_gather_a(c) || (w8 && use_decode_gemm(c))) {
         gather_idx = sorted;
     } else {
         x_perm = at<void>(ws, L.x_perm);
