@@ -167,6 +167,11 @@ class StageTimer:
         self._arr = (ctypes.c_void_p * len(ev))(*handles)  # kept alive while set
         _check(lib().moe_set_stage_events(self._arr, len(ev)), "moe_set_stage_events")
 
+    def skip_call(self):
+        """The next library call records no events (its launches keep their
+        programmatic overlap)."""
+        _check(lib().moe_set_stage_events(None, 0), "moe_set_stage_events")
+
     def __enter__(self):
         return self
 

@@ -115,6 +115,7 @@ int choose_ksplit(long long est_tiles, int nk, long long max_s) {
 
 struct Splits {
     int up = 1, down = 1;
+    bool up_balanced = false;  // decode up GEMM: 2 slices cut where each CTA's equal share ends
 };
 
 // Tiles a grouped GEMM will have at least: every touched expert owns one or
@@ -154,6 +155,21 @@ bool use_decode_gemm(const moe_config& c);
 
 Splits choose_splits(const moe_config& c, bool w8 = false) {
     Splits sp = choose_splits_bf16(c);
+    // FP8 decode-sized up GEMMs with one to four waves of tiles and no shared
+    // expert: instead of S uniform slices (whose tile count rarely divides
+    // into whole waves), every CTA streams an equal contiguous share of all
+    // tiles' k-blocks; a share of at least one tile leaves each tile in at
+    // most two pieces, so two slices hold every partial sum.  (Measured on
+    // one box: one token, FP8 0.0966 -> 0.0954 ms; with bf16 weights the
+    // uniform slices stay faster, 0.1404 vs 0.1422 ms.)
+    if (w8 && use_decode_gemm(c) && c.n_shared == 0 && sp.up > 1) {
+        const long long up_tiles = est_row_tiles(c) * ceil_div(c.d_ff, 128);
+        if (up_tiles >= kNominalSms && up_tiles < 4LL * kNominalSms) {
+            sp.up = 2;
+            sp.up_balanced = true;
+            return sp;
+        }
+    }
     if (w8 && use_decode_gemm(c)) {
         const int up_max = ceil_div(c.d, 128), dn_max = ceil_div(c.d_ff, 128);
         const int dn_max_s = c.n_shared ? ceil_div(c.d_ff_shared, 128) : dn_max;
@@ -565,7 +581,7 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
         StageScope scope(kStageUp, s);
         if (use_decode_gemm(c)) {
             MOE_LAUNCH(launch_gemm_decode(kGemmSwiGLU, up, np, status, sms, s, sp.up, w8 != nullptr,
-                                          decode_tile_rows(c, w8 != nullptr)));
+                                          decode_tile_rows(c, w8 != nullptr), sp.up_balanced));
             if (sp.up > 1) {
                 MOE_LAUNCH(launch_swiglu_finalize(n, offsets + c.E, c.d_ff, sp.up, up[0].part, h, nullptr, s));
                 if (c.n_shared)

@@ -284,8 +284,11 @@ cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int
 // side (D^T = W X^T; nt = 32 or 64 token rows per tile, or 48 with FP8
 // weights, which keeps five stages in flight), bf16 or FP8 (w8)
 // weights, SwiGLU and Scale modes, split-K and gathered token rows; no split H.
+// balanced (ksplit 2, one problem): every CTA takes an equal contiguous
+// share of all tiles' k-blocks (slice 0 = a tile's part from k-block 0,
+// slice 1 = the rest, zeros when one CTA covered the whole tile).
 cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
-                               cudaStream_t s, int ksplit, bool w8, int nt);
+                               cudaStream_t s, int ksplit, bool w8, int nt, bool balanced = false);
 
 // ---- backward pass (backward.cu) ----
 // kbase[e] = sum_{e' < e} round64(klen[e']), klen[e] = offsets[e+1] - offsets[e];

@@ -68,6 +68,11 @@ struct DecParams {  // CUtensorMap members carry their own 64-byte alignment
     float* part[2];
     int part_cols[2];
     int nprob, ksplit;
+    // balanced split-K (ksplit 2, one problem): every CTA takes an equal,
+    // contiguous share of all tiles' k-blocks, cut at tile boundaries; a
+    // tile's part that starts at k-block 0 is slice 0, the rest slice 1 (a
+    // tile one CTA covers whole writes zeros to slice 1)
+    int balanced;
     int* status;
     uint64_t wait_limit_ns;
     int stall_producer;
@@ -120,6 +125,7 @@ struct DTile {
     int prob, g, m, n;
     int x_row0, rows_valid;
     int ks, kb0, kb1;  // K slice and its range of stages [kb0, kb1) (KPS k-blocks each)
+    bool whole;        // balanced split-K: this CTA covers the whole K range (slice 1 gets zeros)
 };
 
 // output columns one tile covers: 128 (the W1/W3 pair) or 256 (W2)
@@ -159,16 +165,63 @@ __device__ __forceinline__ DTile dec_tile(const DecTail& st, const DecParams& p,
     const int rows = row1 - row0;
     const int mt = (rows + NT - 1) / NT;
     int r = local - ts[lo];
-    t.ks = r % p.ksplit;  // K slices of one output tile are adjacent, then token chunks
-    r /= p.ksplit;
+    const int units = p.balanced ? 1 : p.ksplit;  // tile-list entries per output tile
+    t.ks = r % units;  // K slices of one output tile are adjacent, then token chunks
+    r /= units;
     t.n = r / mt;
     t.m = r - t.n * mt;
     t.x_row0 = row0 + t.m * NT;
     t.rows_valid = min(NT, rows - t.m * NT);
     const int nk = (p.K[t.prob] + KPS * BK - 1) / (KPS * BK);
-    t.kb0 = t.ks * nk / p.ksplit;
-    t.kb1 = (t.ks + 1) * nk / p.ksplit;
+    t.kb0 = t.ks * nk / units;
+    t.kb1 = (t.ks + 1) * nk / units;
+    t.whole = p.balanced != 0;
     return t;
+}
+
+// This CTA's work items, the same sequence for every role: tiles round-robin
+// over the grid, or (balanced split-K, when every CTA's share is at least one
+// whole tile) contiguous shares of the flattened (tile, k-block) space.
+struct DecWork {
+    long long pos, end;  // balanced: flat k-block positions; else pos = next tile id
+    int nk;              // stages per tile (balanced)
+    bool flat;
+};
+
+template <int KPS>
+__device__ __forceinline__ DecWork dec_work_begin(const DecParams& p, int total_tiles) {
+    DecWork w;
+    w.nk = (p.K[0] + KPS * BK - 1) / (KPS * BK);
+    const long long W = (long long)total_tiles * w.nk;
+    w.flat = p.balanced && w.nk > 0 && W / gridDim.x >= w.nk;
+    if (w.flat) {
+        w.pos = (long long)blockIdx.x * W / gridDim.x;
+        w.end = (long long)(blockIdx.x + 1) * W / gridDim.x;
+    } else {
+        w.pos = blockIdx.x;
+        w.end = total_tiles;
+    }
+    return w;
+}
+
+template <int MODE, int NT, int KPS>
+__device__ __forceinline__ bool dec_work_next(const DecTail& st, const DecParams& p, DecWork& w, DTile& t) {
+    if (w.pos >= w.end) return false;
+    if (!w.flat) {
+        t = dec_tile<MODE, NT, KPS>(st, p, (int)w.pos);
+        w.pos += gridDim.x;
+        return true;
+    }
+    const int id = (int)(w.pos / w.nk);
+    const int kb = (int)(w.pos - (long long)id * w.nk);
+    const long long seg_end = min(w.end, (long long)(id + 1) * w.nk);
+    t = dec_tile<MODE, NT, KPS>(st, p, id);
+    t.kb0 = kb;
+    t.kb1 = kb + (int)(seg_end - w.pos);
+    t.ks = kb == 0 ? 0 : 1;
+    t.whole = kb == 0 && t.kb1 == w.nk;
+    w.pos = seg_end;
+    return true;
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
@@ -221,12 +274,19 @@ __device__ __forceinline__ void dec_epilogue(const DecParams& p, const DTile& t,
             if (p.ksplit > 1) {
                 const size_t pc = static_cast<size_t>(p.part_cols[t.prob]);
                 float* base = p.part[t.prob] + (static_cast<size_t>(t.ks) * p.x_rows[t.prob] + t.x_row0 + c0) * pc;
+                float* zero = t.whole && p.balanced
+                                  ? p.part[t.prob] + ((size_t)p.x_rows[t.prob] + t.x_row0 + c0) * pc
+                                  : nullptr;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     if (j < jn) {
                         const float xs = dec_xscale(p, t, c0 + j);
                         base[j * pc + f] = s1 * xs * __uint_as_float(g[j]);
                         base[j * pc + N + f] = s3 * xs * __uint_as_float(u[j]);
+                        if (zero) {
+                            zero[j * pc + f] = 0.f;
+                            zero[j * pc + N + f] = 0.f;
+                        }
                     }
             } else {
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.prob]) + (size_t)(t.x_row0 + c0) * N + f;
@@ -258,11 +318,16 @@ __device__ __forceinline__ void dec_epilogue(const DecParams& p, const DTile& t,
                 float* dst = p.ksplit > 1
                                  ? p.part[t.prob] + (static_cast<size_t>(t.ks) * p.x_rows[t.prob] + row) * N + o
                                  : static_cast<float*>(p.out[t.prob]) + row * N + o;
+                float* zero = p.ksplit > 1 && t.whole && p.balanced
+                                  ? p.part[t.prob] + ((size_t)p.x_rows[t.prob] + row) * N + o
+                                  : nullptr;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (j < jn)
+                    if (j < jn) {
                         dst[(size_t)j * N] =
                             (rs ? __ldg(rs + j) : 1.0f) * dec_xscale(p, t, c0 + j) * ws * __uint_as_float(v[j]);
+                        if (zero) zero[(size_t)j * N] = 0.f;
+                    }
             }
         }
     }
@@ -326,7 +391,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
                             const int a = p.offsets[q][g], b = p.offsets[q][g + 1];
                             if (a < 0 || b < a || b > p.x_rows[q]) record_status(p.status, kStatusBounds);
                         }
-                        tiles = ((hi - lo + NT - 1) / NT) * ncb * p.ksplit;
+                        tiles = ((hi - lo + NT - 1) / NT) * ncb * (p.balanced ? 1 : p.ksplit);
                     }
                     int incl = tiles;
 #pragma unroll
@@ -355,8 +420,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
         bool used[NST];
         for (int i = 0; i < NST; ++i) used[i] = false;
         bool dead = p.stall_producer != 0;
-        for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
-            const DTile t = dec_tile<MODE, NT, KPS>(st, p, id);
+        DecWork work = dec_work_begin<KPS>(p, total_tiles);
+        DTile t;
+        while (!dead && dec_work_next<MODE, NT, KPS>(st, p, work, t)) {
             const int w_row0 = t.g * p.N[t.prob] + t.n * dec_cols<MODE>();
             const int32_t* gidx = p.x_gather[t.prob];
             int rows4[4] = {0, 0, 0, 0};
@@ -424,8 +490,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
             uint32_t ph = 0;
             int it = 0;
             bool dead = false;
-            for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x, ++it) {
-                const DTile t = dec_tile<MODE, NT, KPS>(st, p, id);
+            DecWork work = dec_work_begin<KPS>(p, total_tiles);
+            DTile t;
+            for (; !dead && dec_work_next<MODE, NT, KPS>(st, p, work, t); ++it) {
                 const int acc = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
                 if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
@@ -472,8 +539,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
         const int quarter = warp & 3;
         const int wrow = quarter * 32 + lane;
         int it = 0;
-        for (int id = blockIdx.x; id < total_tiles; id += gridDim.x, ++it) {
-            const DTile t = dec_tile<MODE, NT, KPS>(st, p, id);
+        DecWork work = dec_work_begin<KPS>(p, total_tiles);
+        DTile t;
+        for (; dec_work_next<MODE, NT, KPS>(st, p, work, t); ++it) {
             const int acc = it & 1;
             const uint32_t use = static_cast<uint32_t>(it >> 1);
             if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status, p.wait_limit_ns)) break;
@@ -529,7 +597,8 @@ cudaError_t launch_dec_nt(const DecParams& prm, int nt, int grid, cudaStream_t s
 }  // namespace
 
 cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
-                               cudaStream_t s, int ksplit, bool w8, int nt) {
+                               cudaStream_t s, int ksplit, bool w8, int nt, bool balanced) {
+    if (balanced && (ksplit != 2 || nprob != 1)) return cudaErrorInvalidValue;
     if (nprob < 1 || nprob > 2 || ksplit < 1 || (nt != 32 && nt != 64 && !(nt == 48 && w8)))
         return cudaErrorInvalidValue;
     if (mode != kGemmSwiGLU && mode != kGemmScale) return cudaErrorInvalidValue;
@@ -582,6 +651,7 @@ cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, in
         prm.x_rows[q] = g.a_rows;
     }
     prm.nprob = nprob;
+    prm.balanced = balanced ? 1 : 0;
     prm.status = status;
     prm.wait_limit_ns = kWaitLimitNs;
     const char* stall = getenv("MOE_TEST_STALL_GEMM");

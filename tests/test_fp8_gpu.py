@@ -54,6 +54,8 @@ SMALL_FP8 = [
              weights="fp8"),
     Workload("fp8_gemm_router_capacity", T=520, d=384, E=64, F=256, k=4, capacity=40, weights="fp8"),
     Workload("fp8_expert_choice", T=300, d=256, E=8, F=384, k=2, routing="expert", weights="fp8"),
+    # one token, 160 up-GEMM tiles: balanced split-K with FP8 stages (two k-blocks each)
+    Workload("fp8_decode_balanced_splitk_t1", T=1, d=384, E=8, F=10240, k=2, weights="fp8"),
     # 17..32 rows per touched expert: the FP8 decode GEMM's 48-row token tiles (shared expert: 48, 48, 4)
     Workload("fp8_decode_48rows_shared", T=100, d=256, E=8, F=320, k=2, n_shared=1, F_s=192, weights="fp8"),
 ]
