@@ -254,7 +254,7 @@ Layout layout(const moe_config& c) {
 // Backward-pass workspace: the forward layout, then these regions.
 struct BLayout {
     size_t probs, xp, dyp, G, U, D, dGU, Hb, dgp, kbase, klen, dGT, dUT, HbT, xpT, dysT, dXp, dlog, R,
-        wg_part, s_off, s_kbase, s_klen, Gs, Us, Ds, dGUs, Hbs, dGsT, dUsT, HbsT, xT, dyT, dXs, total;
+        wg_part, s_off, s_kbase, s_klen, Gs, Us, dGUs, Hbs, dGsT, dUsT, HbsT, xT, dyT, dXs, total;
     int ncols, ncols_s;
 };
 
@@ -277,10 +277,10 @@ BLayout blayout(const moe_config& c) {
     b.dyp = take(2 * n * d);
     b.G = take(4 * n * F);
     b.U = take(4 * n * F);
-    b.D = take(4 * n * F);
+    b.D = take(4 * ((F + 255) / 256) * ((n + 3) / 4 * 4));  // the gate-gradient partials of the D GEMM
     b.dGU = take(2 * n * 2 * F);
     b.Hb = take(2 * n * F);
-    b.dgp = take(4 * n);
+    b.dgp = take(4 * ((n + 3) / 4 * 4));
     b.kbase = take(4 * E);
     b.klen = take(4 * E);
     b.dGT = take(2 * F * nc);
@@ -298,7 +298,6 @@ BLayout blayout(const moe_config& c) {
     b.s_klen = take(sh ? 4 : 0);
     b.Gs = take(sh ? 4 * T * Fs : 0);
     b.Us = take(sh ? 4 * T * Fs : 0);
-    b.Ds = take(sh ? 4 * T * Fs : 0);
     b.dGUs = take(sh ? 2 * T * 2 * Fs : 0);
     b.Hbs = take(sh ? 2 * T * Fs : 0);
     b.dGsT = take(sh ? 2 * Fs * ncs : 0);
@@ -1122,19 +1121,33 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
         MOE_LAUNCH(launch_gemm_tc(pm, p1, np, status, sms, s, 1, pair));
         GemmProblem p2[2] = {routed(xp, n, w3, F, d, U), dense(x, T, ws3, Fs, d, at<float>(ws, B.Us))};
         MOE_LAUNCH(launch_gemm_tc(pm, p2, np, status, sms, s, 1, pair));
-        // D = dy W2 (W2 stored [d][F]: B^T of this product)
-        GemmProblem p3[2] = {transposed(routed(dyp, n, w2, F, d, D), nullptr, 0),
-                             transposed(dense(dy, T, ws2, Fs, d, at<float>(ws, B.Ds)), nullptr, 0)};
-        MOE_LAUNCH(launch_gemm_tc(pm, p3, np, status, sms, s, 1, pair));
     }
+    // D = dy W2 (W2 stored [d][F]: B^T of this product), consumed in the GEMM's
+    // epilogue by the SwiGLU backward: dGU = [dG | dU], Hb = bf16(h), and the
+    // gate gradients dg = sum_f D h as one partial per 256-column tile (the D
+    // region holds them), summed in tile order below
     void* dGU = at<void>(ws, B.dGU);
     void* Hb = at<void>(ws, B.Hb);
     float* dgp = at<float>(ws, B.dgp);
-    MOE_LAUNCH(launch_swiglu_backward(n, rows_end, F, G, U, D, o.gates_perm, dGU, Hb, dgp, s));
-    if (c.n_shared)
-        MOE_LAUNCH(launch_swiglu_backward(T, nullptr, Fs, at<float>(ws, B.Gs), at<float>(ws, B.Us),
-                                          at<float>(ws, B.Ds), nullptr, at<void>(ws, B.dGUs), at<void>(ws, B.Hbs),
-                                          nullptr, s));
+    const int dg_ld = (n + 3) / 4 * 4;
+    const int dg_tiles = (F + 255) / 256;
+    {
+        GemmProblem p3[2] = {transposed(routed(dyp, n, w2, F, d, nullptr), nullptr, 0),
+                             transposed(dense(dy, T, ws2, Fs, d, nullptr), nullptr, 0)};
+        p3[0].row_scale = o.gates_perm;
+        p3[0].bwd_G = G;
+        p3[0].bwd_U = U;
+        p3[0].bwd_dGU = dGU;
+        p3[0].bwd_Hb = Hb;
+        p3[0].bwd_dgp_part = D;
+        p3[0].bwd_dgp_ld = dg_ld;
+        p3[1].bwd_G = at<float>(ws, B.Gs);
+        p3[1].bwd_U = at<float>(ws, B.Us);
+        p3[1].bwd_dGU = at<void>(ws, B.dGUs);
+        p3[1].bwd_Hb = at<void>(ws, B.Hbs);
+        MOE_LAUNCH(launch_gemm_tc(kGemmSwigluBwd, p3, np, status, sms, s, 1, pair));
+        MOE_LAUNCH(launch_reduce_partials(1, nullptr, dg_ld, dg_tiles, D, dgp, s));
+    }
     float* dXp = at<float>(ws, B.dXp);
     float* dXs = c.n_shared ? at<float>(ws, B.dXs) : nullptr;
     {

@@ -1,4 +1,4 @@
-// backward.cu -- the element-wise, transpose and router kernels of the backward
+// backward.cu -- the transpose and router kernels of the backward
 // pass; its matrix products run on the grouped tensor-core GEMM (gemm_tc.cu).
 //
 // Gradients of <dy, y> + dL * L_balance with the routing decisions held fixed
@@ -10,9 +10,11 @@
 //   dg_r = sum_f D h,   h = silu(G) U
 //   dh = g D,  dG = dh U silu'(G),  dU = dh silu(G)
 //   dX_r = dG W1_e + dU W3_e,  dW1_e = dG^T X,  dW3_e = dU^T X,  dW2_e = (g dy)^T h
-// The weight gradients contract over each expert's token rows: their operands
-// are transposed per expert into K windows that start on 64-column boundaries
-// (zero-filled to the next boundary), which the GEMM's K-grouped mode reads.
+// The element-wise part (h, dh, dG, dU, dg) runs in the epilogue of the D
+// GEMM (kGemmSwigluBwd).  The weight gradients contract over each expert's
+// token rows: their operands are transposed per expert into K windows that
+// start on 64-column boundaries (zero-filled to the next boundary), which the
+// GEMM's K-grouped mode reads.
 #include "common.cuh"
 
 namespace moe {
@@ -126,48 +128,6 @@ __global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloa
                         gather8(tile, ch * 8, cc);
             }
         }
-    }
-    __syncthreads();
-    pdl_trigger();
-}
-
-// One row r of the permuted layout (r < *rows_dev when given, else < rows_max):
-//   h = silu(G) U,  dg_r = sum_f D h,  dh = g D,
-//   dGU[r] = [dh U silu'(G) | dh silu(G)] (bf16),  Hb[r] = bf16(h).
-__global__ void __launch_bounds__(256) swiglu_backward_kernel(int rows_max, const int32_t* __restrict__ rows_dev, int F,
-                                                              const float* __restrict__ G,
-                                                              const float* __restrict__ U,
-                                                              const float* __restrict__ D,
-                                                              const float* __restrict__ gate,
-                                                              __nv_bfloat16* __restrict__ dGU,
-                                                              __nv_bfloat16* __restrict__ Hb,
-                                                              float* __restrict__ dgp) {
-    pdl_wait();
-    __shared__ float s_red[8];
-    const int rows = rows_dev ? min(*rows_dev, rows_max) : rows_max;
-    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-        const size_t o = (size_t)r * F;
-        const float g = gate ? __ldg(gate + r) : 1.0f;
-        float part = 0.f;
-        for (int f = threadIdx.x; f < F; f += blockDim.x) {
-            const float a = __ldg(G + o + f), b = __ldg(U + o + f), dd = __ldg(D + o + f);
-            const float s = 1.0f / (1.0f + __expf(-a));
-            const float h = a * s * b;
-            part += dd * h;
-            const float dh = g * dd;
-            dGU[2 * o + f] = __float2bfloat16_rn(dh * b * s * (1.0f + a * (1.0f - s)));
-            dGU[2 * o + F + f] = __float2bfloat16_rn(dh * a * s);
-            Hb[o + f] = __float2bfloat16_rn(h);
-        }
-        part = warp_sum(part);
-        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = part;
-        __syncthreads();
-        if (threadIdx.x == 0 && dgp) {
-            float acc = 0.f;
-            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) acc += s_red[w];  // fixed order
-            dgp[r] = acc;
-        }
-        __syncthreads();
     }
     __syncthreads();
     pdl_trigger();
@@ -318,16 +278,6 @@ cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, i
     const dim3 grid((C + TT - 1) / TT, (ncols + TT - 1) / TT);
     launch_pdl(transpose_windows_kernel, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), ld_src, col0,
                C, E, offsets, kbase, klen, row_scale, static_cast<__nv_bfloat16*>(dst), ld_dst, ncols);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_swiglu_backward(int rows_max, const int32_t* rows_dev, int F, const float* G, const float* U,
-                                   const float* D, const float* gate, void* dGU, void* Hb, float* dgp,
-                                   cudaStream_t s) {
-    if (rows_max == 0) return cudaSuccess;
-    const int grid = rows_max < 148 * 16 ? rows_max : 148 * 16;
-    launch_pdl(swiglu_backward_kernel, dim3(grid), dim3(256), 0, s, rows_max, rows_dev, F, G, U, D, gate,
-               static_cast<__nv_bfloat16*>(dGU), static_cast<__nv_bfloat16*>(Hb), dgp);
     return cudaGetLastError();
 }
 

@@ -216,6 +216,7 @@ enum GemmMode : int {
     kGemmScale = 1,   // out(fp32)  = row_scale[row] * (A B^T)  (row_scale may be null: 1)
     kGemmPlain = 2,   // out(fp32)  = A B^T
     kGemmScaleSplit = 3,  // out(fp32) = row_scale[row] * ((A + A2) B^T), A and A2 bf16 (hi and lo halves)
+    kGemmSwigluBwd = 4,   // D = A B^T consumed in the epilogue by the SwiGLU backward (bwd_* fields)
 };
 
 // One grouped problem: rows of A are split into groups by offsets (G+1
@@ -260,6 +261,18 @@ struct GemmProblem {
     // = part 1; each part is padded to whole 64-deep k-blocks with zeros.
     int b_mn;
     int kpart;
+    // kGemmSwigluBwd (launch_gemm_tc, ksplit 1): the product D = A B^T [rows][N]
+    // is not stored; with G, U the recomputed up projections [rows][N] fp32 and
+    // g = row_scale[row] (null: 1), the epilogue writes per element
+    //   h = silu(G) U,  dh = g D,  dG = dh U silu'(G),  dU = dh silu(G)
+    // as bf16 dGU [rows][2N] (dG, then dU) and Hb = bf16(h) [rows][N], and, per
+    // 256-column tile n, dgp_part[n * dgp_ld + row] = sum over its columns of D h
+    const float* bwd_G;
+    const float* bwd_U;
+    void* bwd_dGU;
+    void* bwd_Hb;
+    float* bwd_dgp_part;
+    int bwd_dgp_ld;
 };
 
 // Tensor-core (tcgen05) path, bf16 operands, fp32 accumulate.  Runs up to two
@@ -300,11 +313,6 @@ cudaError_t launch_k_windows(int E, int32_t* offsets, int32_t* kbase, int32_t* k
 cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, int C, int E, const int32_t* offsets,
                                      const int32_t* kbase, const int32_t* klen, const float* row_scale, void* dst,
                                      size_t ld_dst, int ncols, cudaStream_t s);
-// Per row: dGU = [g D U silu'(G) | g D silu(G)] (bf16), Hb = bf16(silu(G) U),
-// dgp[r] = sum_f D silu(G) U (when dgp != nullptr).
-cudaError_t launch_swiglu_backward(int rows_max, const int32_t* rows_dev, int F, const float* G, const float* U,
-                                   const float* D, const float* gate, void* dGU, void* Hb, float* dgp,
-                                   cudaStream_t s);
 // dlogits [T][E] from the gate gradients (via slot_pos) and the balance loss.
 cudaError_t launch_router_backward(int T, int E, int k, const float* probs, const int32_t* ids,
                                    const int32_t* slot_pos, const float* gates, const float* dgp, int renormalize,

@@ -20,6 +20,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "fp8_split.cuh"
 
 namespace moe {
 namespace {
@@ -82,19 +83,10 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(long long rows, int c
 }
 
 // split_e4m3_kernel: one block per row of a bf16 matrix [rows][K] (K a
-// multiple of 8).  The FP8 tensor-core MMA (kind::f8f6f4) takes FP8 on both
-// operands, so a bf16 row x that meets FP8 weights is carried as two E4M3
-// code rows and a power-of-two scale,  x = s * (hi + lo):
-//   s  = 2^(e - 8) with max|x| = m * 2^e, m in [0.5, 1)  (1 for a zero row),
-//        so |x| / s < 256 and the division by s is exact;
-//   hi = E4M3(x / s), lo = E4M3(x / s - hi), both rounded to nearest even.
-// hi keeps the top 4 significant bits of x / s and the remainder has at most
-// 4 more (a bf16 value has 8), so hi + lo == x / s exactly whenever lo stays
-// at or above E4M3's smallest step 2^-9, i.e. for every |x| >= max|x| * 2^-10;
-// smaller entries carry an absolute error of at most s * 2^-10 <= max|x| *
-// 2^-17.  Row r of the output is row gather[r] of x when gather is given
-// (token rows in expert order); rows at or beyond *live_rows (when given)
-// are skipped.
+// multiple of 8) -> the E4M3 hi/lo code rows and power-of-two scale of
+// fp8_split.cuh.  Row r of the output is row gather[r] of x when gather is
+// given (token rows in expert order); rows at or beyond *live_rows (when
+// given) are skipped.
 constexpr int kSplitThreads = 256;
 
 __global__ void __launch_bounds__(kSplitThreads) split_e4m3_kernel(int K, const __nv_bfloat16* __restrict__ x,
@@ -125,31 +117,17 @@ __global__ void __launch_bounds__(kSplitThreads) split_e4m3_kernel(int K, const 
         amax = s_max[0];
 #pragma unroll
         for (int w = 1; w < kSplitThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
-        int e = 8;  // zero row: s = 1
-        if (amax > 0.f) frexpf(amax, &e);
-        // 1/s = 2^(8 - e) as two factors, each inside the fp32 range
-        const int sh = 8 - e, sh1 = sh / 2, sh2 = sh - sh1;
-        const float f1 = ldexpf(1.0f, sh1), f2 = ldexpf(1.0f, sh2);
-        if (threadIdx.x == 0) scale[row] = ldexpf(1.0f, e - 8);
+        const E4m3RowScale sc = e4m3_row_scale(amax);
+        if (threadIdx.x == 0) scale[row] = sc.s;
         uint8_t* dh = hi + (size_t)row * K;
         uint8_t* dl = lo + (size_t)row * K;
         for (int c = threadIdx.x * 8; c < K; c += kSplitThreads * 8) {
             float v[8];
             load8<__nv_bfloat16>(src + c, v);
-            uint32_t h[2] = {0u, 0u}, l[2] = {0u, 0u};
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                const float2 a = make_float2(v[i] * f1 * f2, v[i + 1] * f1 * f2);
-                const __nv_fp8x2_storage_t hc = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
-                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hc, __NV_E4M3);
-                const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-                const float2 r = make_float2(a.x - hv.x, a.y - hv.y);
-                const __nv_fp8x2_storage_t lc = __nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
-                h[i >> 2] |= (uint32_t)hc << (16 * ((i >> 1) & 1));
-                l[i >> 2] |= (uint32_t)lc << (16 * ((i >> 1) & 1));
-            }
-            *reinterpret_cast<uint2*>(dh + c) = make_uint2(h[0], h[1]);
-            *reinterpret_cast<uint2*>(dl + c) = make_uint2(l[0], l[1]);
+            uint2 h, l;
+            e4m3_split8(v, sc, h, l);
+            *reinterpret_cast<uint2*>(dh + c) = h;
+            *reinterpret_cast<uint2*>(dl + c) = l;
         }
     }
     __syncthreads();

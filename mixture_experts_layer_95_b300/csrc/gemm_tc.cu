@@ -101,6 +101,13 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     // tmB2, where tmA is then a 3-D map {kpart, 2, rows} of A = [rows][2 kpart].
     int b_mn;
     int kpart[2];
+    // kGemmSwigluBwd epilogue operands (GemmProblem::bwd_*)
+    const float* bwd_G[2];
+    const float* bwd_U[2];
+    __nv_bfloat16* bwd_dGU[2];
+    __nv_bfloat16* bwd_Hb[2];
+    float* bwd_dgp_part[2];
+    int bwd_dgp_ld[2];
     int* status;
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
     int stall_producer;      // test switch: issue no loads, so the consumers' bounded waits run out
@@ -330,6 +337,79 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
                 }
             }
         }
+    } else if (MODE == kGemmSwigluBwd) {
+        // SwiGLU backward on D (this thread's row, 32 columns at a time)
+        const float g = (valid && p.row_scale[t.prob]) ? __ldg(p.row_scale[t.prob] + grow) : 1.0f;
+        const float* Gr = p.bwd_G[t.prob] + grow * N;
+        const float* Ur = p.bwd_U[t.prob] + grow * N;
+        __nv_bfloat16* dGr = p.bwd_dGU[t.prob] + grow * 2 * N;
+        __nv_bfloat16* Hr = p.bwd_Hb[t.prob] + grow * N;
+        float part = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            __syncwarp();
+            tmem_ld32(tacc + c0, v);
+            tmem_ld_wait();
+            const int col = t.n * BN + c0;
+            if (!valid || col >= N) continue;
+            const int nc = min(32, N - col);
+#pragma unroll
+            for (int q = 0; q < 32; q += 8) {
+                if (q >= nc) continue;  // (fully unrolled: v is indexed with constants only)
+                float a[8], b[8];
+                if (q + 8 <= nc) {
+                    const float4 a0 = __ldg(reinterpret_cast<const float4*>(Gr + col + q));
+                    const float4 a1 = __ldg(reinterpret_cast<const float4*>(Gr + col + q + 4));
+                    const float4 b0 = __ldg(reinterpret_cast<const float4*>(Ur + col + q));
+                    const float4 b1 = __ldg(reinterpret_cast<const float4*>(Ur + col + q + 4));
+                    a[0] = a0.x, a[1] = a0.y, a[2] = a0.z, a[3] = a0.w, a[4] = a1.x, a[5] = a1.y, a[6] = a1.z, a[7] = a1.w;
+                    b[0] = b0.x, b[1] = b0.y, b[2] = b0.z, b[3] = b0.w, b[4] = b1.x, b[5] = b1.y, b[6] = b1.z, b[7] = b1.w;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        a[i] = q + i < nc ? __ldg(Gr + col + q + i) : 0.f;
+                        b[i] = q + i < nc ? __ldg(Ur + col + q + i) : 0.f;
+                    }
+                }
+                float dG[8], dU[8], hh[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float dd = __uint_as_float(v[q + i]);
+                    const float sg = 1.0f / (1.0f + __expf(-a[i]));
+                    hh[i] = a[i] * sg * b[i];
+                    if (q + i < nc) part += dd * hh[i];
+                    const float dh = g * dd;
+                    dG[i] = dh * b[i] * sg * (1.0f + a[i] * (1.0f - sg));
+                    dU[i] = dh * a[i] * sg;
+                }
+                if (q + 8 <= nc) {
+                    uint4 pg, pu, ph;
+                    uint32_t* wg = reinterpret_cast<uint32_t*>(&pg);
+                    uint32_t* wu = reinterpret_cast<uint32_t*>(&pu);
+                    uint32_t* wh = reinterpret_cast<uint32_t*>(&ph);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        __nv_bfloat162 x = __floats2bfloat162_rn(dG[2 * i], dG[2 * i + 1]);
+                        __nv_bfloat162 y = __floats2bfloat162_rn(dU[2 * i], dU[2 * i + 1]);
+                        __nv_bfloat162 z = __floats2bfloat162_rn(hh[2 * i], hh[2 * i + 1]);
+                        wg[i] = *reinterpret_cast<uint32_t*>(&x);
+                        wu[i] = *reinterpret_cast<uint32_t*>(&y);
+                        wh[i] = *reinterpret_cast<uint32_t*>(&z);
+                    }
+                    *reinterpret_cast<uint4*>(dGr + col + q) = pg;
+                    *reinterpret_cast<uint4*>(dGr + N + col + q) = pu;
+                    *reinterpret_cast<uint4*>(Hr + col + q) = ph;
+                } else {
+                    for (int i = 0; i < 8 && q + i < nc; ++i) {
+                        dGr[col + q + i] = __float2bfloat16_rn(dG[i]);
+                        dGr[N + col + q + i] = __float2bfloat16_rn(dU[i]);
+                        Hr[col + q + i] = __float2bfloat16_rn(hh[i]);
+                    }
+                }
+            }
+        }
+        if (valid && p.bwd_dgp_part[t.prob]) p.bwd_dgp_part[t.prob][(size_t)t.n * p.bwd_dgp_ld[t.prob] + grow] = part;
     } else {
         // fp32 output: each 32x32 block of the warp's rows goes through shared
         // memory (thread = row on the way in, lane = column on the way out), so
@@ -1056,7 +1136,8 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         if (q > 0 && g.b_mn != probs[0].b_mn) return cudaErrorInvalidValue;
         if (g.b_mn) {
             // B^T tiles of 64 K-rows x 64 columns; A plain, or split in two K parts
-            if ((mode != kGemmPlain && mode != kGemmScale) || g.a_gather || g.kbase || g.klen || ksplit != 1 ||
+            if ((mode != kGemmPlain && mode != kGemmScale && mode != kGemmSwigluBwd) || g.a_gather || g.kbase || g.klen ||
+                ksplit != 1 ||
                 g.N % 8 != 0 || (g.kpart && (g.kpart % 8 != 0 || g.K != 2 * g.kpart || !g.B2)))
                 return cudaErrorInvalidValue;
             const uint64_t N = (uint64_t)g.N, kp = (uint64_t)(g.kpart ? g.kpart : g.K);
@@ -1093,6 +1174,17 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
             prm.part[q] = g.part;
             prm.part_cols[q] = mode == kGemmSwiGLU ? 2 * g.N : g.N;
         }
+        if (mode == kGemmSwigluBwd) {
+            if (!g.bwd_G || !g.bwd_U || !g.bwd_dGU || !g.bwd_Hb || ksplit != 1 || g.kbase || g.N % 8 != 0 ||
+                (g.bwd_dgp_part && g.bwd_dgp_ld < g.a_rows))
+                return cudaErrorInvalidValue;
+            prm.bwd_G[q] = g.bwd_G;
+            prm.bwd_U[q] = g.bwd_U;
+            prm.bwd_dGU[q] = static_cast<__nv_bfloat16*>(g.bwd_dGU);
+            prm.bwd_Hb[q] = static_cast<__nv_bfloat16*>(g.bwd_Hb);
+            prm.bwd_dgp_part[q] = g.bwd_dgp_part;
+            prm.bwd_dgp_ld[q] = g.bwd_dgp_ld;
+        }
         prm.offsets[q] = g.offsets;
         prm.out[q] = g.out;
         prm.out2[q] = g.out2;
@@ -1128,6 +1220,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         switch (mode) {
             case kGemmSwiGLU: return launch_pair_mode<kGemmSwiGLU>(prm, grid, s);
             case kGemmScale: return launch_pair_mode<kGemmScale>(prm, grid, s);
+            case kGemmSwigluBwd: return launch_pair_mode<kGemmSwigluBwd>(prm, grid, s);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -1135,6 +1228,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
         case kGemmSwiGLU: return launch_mode<kGemmSwiGLU>(prm, grid, s);
         case kGemmScale: return launch_mode<kGemmScale>(prm, grid, s);
         case kGemmPlain: return launch_mode<kGemmPlain>(prm, grid, s);
+        case kGemmSwigluBwd: return launch_mode<kGemmSwigluBwd>(prm, grid, s);
         case kGemmScaleSplit: return launch_mode<kGemmScaleSplit>(prm, grid, s);
         default: return cudaErrorInvalidValue;
     }
