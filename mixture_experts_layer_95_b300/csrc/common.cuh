@@ -91,6 +91,24 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Column sums over the per-chunk rows of the router's statistics (p and the
+// expert histograms), for layers with at most kWarpColumnMaxE experts: one
+// warp per column, lane j taking rows j, j+32, ... in ascending order, then
+// the 32 lane sums added in lane order.  Every kernel that sums these columns
+// uses this one order, so their floats agree bit for bit.
+constexpr int kWarpColumnMaxE = 32;
+
+__device__ __forceinline__ float warp_column_sum(const float* __restrict__ m, int nrows, int ld, int col) {
+    const int lane = threadIdx.x & 31;
+    float s = 0.f;
+#pragma unroll 4
+    for (int b = lane; b < nrows; b += 32) s += __ldg(m + (size_t)b * ld + col);
+    float tot = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) tot += __shfl_sync(0xffffffffu, s, j);
+    return tot;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -112,26 +112,52 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = a.T * a.k;
 
-    // 1. global counts, this block's prefix, capacity cut
-    for (int e = threadIdx.x; e < E; e += kScanThreads) {
-        int tot = 0, before = 0;
-        for (int b0 = 0; b0 < a.nblk; b0 += 32) {  // 32 independent loads in flight per batch
-            int v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = b0 + j < a.nblk ? __ldg(a.block_hist + (size_t)(b0 + j) * E + e) : 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                before += (b0 + j < (int)blockIdx.x) ? v[j] : 0;
-                tot += v[j];
+    // 1. global counts, this block's prefix, capacity cut: one warp per expert
+    // (all its histogram rows in flight at once) for small E, else one thread
+    // per expert
+    if (E <= kWarpColumnMaxE) {
+        for (int e = warp; e < E; e += kScanWarps) {
+            int tot = 0, before = 0;
+#pragma unroll 4
+            for (int b = lane; b < a.nblk; b += 32) {
+                const int v = __ldg(a.block_hist + (size_t)b * E + e);
+                tot += v;
+                before += b < (int)blockIdx.x ? v : 0;
+            }
+            tot = __reduce_add_sync(0xffffffffu, tot);
+            before = __reduce_add_sync(0xffffffffu, before);
+            if (lane == 0) {
+                s_before[e] = before;
+                s_kept[e] = (a.capacity >= 0 && tot > a.capacity) ? a.capacity : tot;
+                if (blockIdx.x == 0) {
+                    a.o.counts[e] = tot;
+                    a.o.kept[e] = s_kept[e];
+                }
+                s_wcnt[e] = tot;
             }
         }
-        s_before[e] = before;
-        s_kept[e] = (a.capacity >= 0 && tot > a.capacity) ? a.capacity : tot;
-        if (blockIdx.x == 0) {
-            a.o.counts[e] = tot;
-            a.o.kept[e] = s_kept[e];
+    } else {
+        for (int e = threadIdx.x; e < E; e += kScanThreads) {
+            int tot = 0, before = 0;
+            for (int b0 = 0; b0 < a.nblk; b0 += 32) {  // 32 independent loads in flight per batch
+                int v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = b0 + j < a.nblk ? __ldg(a.block_hist + (size_t)(b0 + j) * E + e) : 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    before += (b0 + j < (int)blockIdx.x) ? v[j] : 0;
+                    tot += v[j];
+                }
+            }
+            s_before[e] = before;
+            s_kept[e] = (a.capacity >= 0 && tot > a.capacity) ? a.capacity : tot;
+            if (blockIdx.x == 0) {
+                a.o.counts[e] = tot;
+                a.o.kept[e] = s_kept[e];
+            }
+            s_wcnt[e] = tot;  // scratch: counts for the statistics below
         }
-        s_wcnt[e] = tot;  // scratch: counts for the statistics below
     }
     __syncthreads();
     // 2. expert offsets
@@ -140,7 +166,28 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
     if (blockIdx.x == 0) {
         for (int e = threadIdx.x; e <= E; e += kScanThreads) a.o.offsets[e] = s_off[e];
         if (threadIdx.x == 0) *a.o.n_dropped = n - total;
-        if (a.o.p_part) {
+        if (a.o.p_part && E <= kWarpColumnMaxE) {
+            // load statistics: f = counts/(T k), p = mean softmax row, L = alpha E sum f p
+            // (p: the column-sum order moe_load_stats uses; L: terms added in expert order)
+            s_red[threadIdx.x] = 0.f;
+            __syncthreads();
+            for (int e = warp; e < E; e += kScanWarps) {
+                const float ps = warp_column_sum(a.o.p_part, a.o.p_nblk, E, e);
+                if (lane == 0) {
+                    const float pm = ps / (float)a.T;
+                    const float f = (float)s_wcnt[e] / ((float)a.T * (float)a.k);
+                    if (a.o.p_mean) a.o.p_mean[e] = pm;
+                    if (a.o.f) a.o.f[e] = f;
+                    s_red[e] = f * pm;
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                float acc = 0.f;
+                for (int i = 0; i < kScanThreads; ++i) acc += s_red[i];
+                if (a.o.L) *a.o.L = a.o.alpha * (float)E * acc;
+            }
+        } else if (a.o.p_part) {
             // load statistics: f = counts/(T k), p = mean softmax row, L = alpha E sum f p
             float part = 0.f;
             for (int e = threadIdx.x; e < E; e += kScanThreads) {

@@ -314,8 +314,17 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
     pdl_trigger();
 }
 
+// Column means of the router's p rows, in the order the fused grouping scan
+// sums them (warp_column_sum for small E, row order otherwise).
 __global__ void p_mean_kernel(int Tn, int E, int nblk, const float* __restrict__ p_part, float* __restrict__ p_mean) {
     pdl_wait();
+    if (E <= kWarpColumnMaxE) {
+        const int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // one warp per expert
+        if (e >= E) return;
+        const float s = warp_column_sum(p_part, nblk, E, e);
+        if ((threadIdx.x & 31) == 0) p_mean[e] = Tn > 0 ? s / (float)Tn : 0.f;
+        return;
+    }
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E) return;
     float s = 0.f;
@@ -400,7 +409,8 @@ cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, 
 }
 
 cudaError_t launch_p_mean(int T, int E, int nblk, const float* p_part, float* p_mean, cudaStream_t s) {
-    launch_pdl(p_mean_kernel, dim3((E + 255) / 256), dim3(256), 0, s, T, E, nblk, p_part, p_mean);
+    const int threads = E <= kWarpColumnMaxE ? 32 * E : E;
+    launch_pdl(p_mean_kernel, dim3((threads + 255) / 256), dim3(256), 0, s, T, E, nblk, p_part, p_mean);
     return cudaGetLastError();
 }
 
