@@ -62,7 +62,8 @@ bool decode_sized(const moe_config& c) {
 
 // Decode-sized bf16 batches with a single bf16 H: both expert GEMMs put the
 // weights on the MMA's M side (gemm_decode.cu), with 32 token rows per tile
-// when the touched experts average at most 16 rows, else 64.
+// when the touched experts average at most 16 rows, else 64 (48 with FP8
+// weights, decode_tile_rows).
 bool use_decode_gemm(const moe_config& c) { return decode_sized(c) && !use_h_split(c); }
 
 // The up GEMM gathers x rows itself (TMA gather4, 4 rows per load), so the
