@@ -64,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (moe_backward) instead of the forward layer")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step: moe_forward_train, then moe_backward_saved on its activations")
     return ap.parse_args(argv)
 
 
@@ -542,21 +544,39 @@ def run_backward(args):
     dy = torch.randn((w.T, w.d), generator=g, device=dev).to(layer.torch_dtype)
     bw = moe.Backward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
                       L["ws3"], L["ws2"], device=dev)
+    y = torch.empty((w.T, w.d), dtype=layer.y_dtype, device=dev)
+    # train: one step = the forward that keeps its activations + the backward on them;
+    # an event between the two splits the step
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if args.train else []
+
+    def step(i=None):
+        if args.train:
+            bw.forward_train(L["x"], y)
+            if i is not None:
+                mids[i].record()
+            bw(L["x"], dy, 1.0, saved=True)
+        else:
+            bw(L["x"], dy, 1.0)
+
     for _ in range(args.warmup):
-        bw(L["x"], dy, 1.0)
+        step()
     torch.cuda.synchronize(dev)
     st = bw.device_status()
     if st != 0:
         raise moe.MoeError(st, "backward warm-up device status")
     launches0 = moe.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if args.train else []
     e0.record()
-    for _ in range(args.steps):
-        bw(L["x"], dy, 1.0)
+    for i in range(args.steps):
+        if args.train:
+            starts[i].record()
+        step(i)
     e1.record()
     e1.synchronize()
     launches = moe.launch_count() - launches0
     ms = e0.elapsed_time(e1) / args.steps
+    fwd_ms = sum(a.elapsed_time(b) for a, b in zip(starts, mids)) / args.steps if args.train else None
     st = bw.device_status()
     if st != 0:
         raise moe.MoeError(st, "backward device status")
@@ -567,16 +587,21 @@ def run_backward(args):
         kept = int(moe.permute(lay, ids, gates, L["x"])["kept"].sum().item())
     fwd_expert = 2.0 * moe_inputs.expert_params(w.d, w.F) * kept + \
         2.0 * moe_inputs.expert_params(w.d, w.F_s) * w.T * w.n_shared
-    tflops = 2.0 * fwd_expert / (ms / 1e3) / 1e12
+    mult = 3.0 if args.train else 2.0  # the training step adds the forward's expert FLOPs
+    tflops = mult * fwd_expert / (ms / 1e3) / 1e12
     peaks, src = load_peaks()
-    out = {"metric": "MoE-layer backward tokens/s on 1 B300 (gradients of every input)", "value": round(w.T / (ms / 1e3), 1),
+    metric = ("MoE-layer training step tokens/s on 1 B300 (forward + gradients of every input)" if args.train
+              else "MoE-layer backward tokens/s on 1 B300 (gradients of every input)")
+    out = {"metric": metric, "value": round(w.T / (ms / 1e3), 1),
            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
            "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F,
                       "n_shared": w.n_shared, "capacity": w.capacity},
-           "backward": {"algorithmic_tflop_per_step": round(2.0 * fwd_expert / 1e12, 4), "tflops": round(tflops, 1),
+           "backward": {"algorithmic_tflop_per_step": round(mult * fwd_expert / 1e12, 4), "tflops": round(tflops, 1),
                         "frac_bf16_peak": round(tflops / peaks["bf16_tflops"], 4), "peak_source": src},
            "gpu_launches": int(launches)}
+    if args.train:
+        out["train"] = {"forward_train_ms": round(fwd_ms, 4), "backward_saved_ms": round(ms - fwd_ms, 4)}
     print(json.dumps(out), flush=True)
 
 
@@ -584,7 +609,7 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
-    elif args.backward:
+    elif args.backward or args.train:
         run_backward(args)
     else:
         run_ours(args)

@@ -347,6 +347,37 @@ MOE_API int moe_backward(const moe_config *cfg, const void *x, const void *w_gat
                          float *dw1, float *dw3, float *dw2, float *dws1, float *dws3, float *dws2, void *ws,
                          size_t ws_bytes, moe_stream_t stream);
 
+/* ---- training step: forward that keeps its activations ------------------
+ * moe_forward_train computes y and the statistics as moe_forward does (for
+ * decode-sized batches it keeps the large-batch GEMMs, so y may differ from
+ * moe_forward's in rounding), and leaves in ws -- a moe_backward_workspace_size workspace -- what the
+ * backward pass would otherwise recompute: the softmax rows, the top-k ids,
+ * gates and grouping, x in expert order, and the fp32 pre-activations
+ * G = x W1^T, U = x W3^T of every kept slot (and of the shared expert).  The
+ * up GEMM writes G and U from the same accumulators that give h = silu(G) U,
+ * so moe_backward_saved on that workspace returns the gradients moe_backward
+ * returns, bit for bit, without the routing, grouping and two of the seven
+ * expert GEMMs (the FLOPs of the forward up GEMM).  The gradients are those
+ * of "MoE Deep Dive", Load Balancing Loss Derivation (see moe_backward).
+ *   moe_forward_train: arguments and outputs as moe_forward (bf16, token
+ *   choice, cfg->h_split 0; else MOE_ERR_DTYPE / MOE_ERR_SHAPE), ws of
+ *   moe_backward_workspace_size bytes (MOE_ERR_WORKSPACE if smaller).
+ *   moe_backward_saved: arguments, outputs and errors as moe_backward; the
+ *   caller passes the cfg, x, weights, biases and ws of the last
+ *   moe_forward_train on that ws, with no other call on ws in between.  The
+ *   library cannot check this, and not every index it reads back from ws is
+ *   re-checked on the device: any other workspace content is a caller error
+ *   with undefined results.  Both are asynchronous on `stream`. */
+MOE_API int moe_forward_train(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
+                              const float *select_bias, const void *w1, const void *w3, const void *w2,
+                              const void *ws1, const void *ws3, const void *ws2, void *y, const moe_stats *stats,
+                              void *ws, size_t ws_bytes, moe_stream_t stream);
+MOE_API int moe_backward_saved(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
+                               const float *select_bias, const void *w1, const void *w3, const void *w2,
+                               const void *ws1, const void *ws3, const void *ws2, const void *dy, float dL,
+                               float *dx, float *dw_gate, float *dw1, float *dw3, float *dw2, float *dws1,
+                               float *dws3, float *dws2, void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Reads (and clears) the device status word kept in the workspace: MOE_OK,
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_BOUNDS.  Synchronises `stream` first.
  * Returns MOE_ERR_CUDA if the copy itself fails. */

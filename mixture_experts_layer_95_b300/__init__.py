@@ -28,7 +28,7 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permut
             "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
             "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static", "moe_bias_update",
             "moe_plan_describe", "moe_route_expert_choice", "moe_quantize_fp8", "moe_forward_fp8",
-            "moe_backward_workspace_size", "moe_backward")
+            "moe_backward_workspace_size", "moe_backward", "moe_forward_train", "moe_backward_saved")
 STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
 
 
@@ -98,6 +98,10 @@ def lib():
         L.moe_backward_workspace_size.restype = sz
         L.moe_backward.argtypes = [cfgp] + [vp] * 11 + [ctypes.c_float] + [vp] * 8 + [vp, sz, vp]
         L.moe_backward.restype = i32
+        L.moe_backward_saved.argtypes = L.moe_backward.argtypes
+        L.moe_backward_saved.restype = i32
+        L.moe_forward_train.argtypes = L.moe_forward.argtypes
+        L.moe_forward_train.restype = i32
         L.moe_route_expert_choice.restype = i32
         L.moe_plan_describe.argtypes = [cfgp, ctypes.c_char_p, sz]
         L.moe_plan_describe.restype = i32
@@ -550,14 +554,30 @@ class Backward:
                               dws2=torch.empty((d, Fs), **f32))
         self.w = (w_gate, logit_bias, select_bias, w1, w3, w2, ws1, ws3, ws2)
 
-    def __call__(self, x, dy, dL: float = 0.0, stream=None):
+    def forward_train(self, x, y=None, stream=None):
+        """moe_forward_train: y of the layer, with the activations the next
+        __call__(..., saved=True) reads kept in this object's workspace."""
+        L = self.layer
+        _need(x, (L.T, L.d), L.torch_dtype, "x")
+        if y is None:
+            y = torch.empty((L.T, L.d), dtype=L.y_dtype, device=x.device)
+        else:
+            _need(y, (L.T, L.d), L.y_dtype, "y")
+        wg, lb, sb, w1, w3, w2, s1, s3, s2 = (_ptr(t) for t in self.w)
+        _check(lib().moe_forward_train(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(y),
+                                       None, _ptr(self.ws), self.ws.numel(), _stream(stream)), "moe_forward_train")
+        return y
+
+    def __call__(self, x, dy, dL: float = 0.0, stream=None, saved: bool = False):
+        """saved=True: moe_backward_saved on the activations of the last
+        forward_train(x) (same x); otherwise moe_backward recomputes them."""
         wg, lb, sb, w1, w3, w2, s1, s3, s2 = (_ptr(t) for t in self.w)
         g = self.grads
-        _check(lib().moe_backward(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(dy),
-                                  ctypes.c_float(dL), _ptr(g["dx"]), _ptr(g["dw_gate"]), _ptr(g["dw1"]),
-                                  _ptr(g["dw3"]), _ptr(g["dw2"]), _ptr(g.get("dws1")), _ptr(g.get("dws3")),
-                                  _ptr(g.get("dws2")), _ptr(self.ws), self.ws.numel(), _stream(stream)),
-               "moe_backward")
+        fn, name = (lib().moe_backward_saved, "moe_backward_saved") if saved else (lib().moe_backward, "moe_backward")
+        _check(fn(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(dy), ctypes.c_float(dL),
+                  _ptr(g["dx"]), _ptr(g["dw_gate"]), _ptr(g["dw1"]), _ptr(g["dw3"]), _ptr(g["dw2"]),
+                  _ptr(g.get("dws1")), _ptr(g.get("dws3")), _ptr(g.get("dws2")), _ptr(self.ws), self.ws.numel(),
+                  _stream(stream)), name)
         return g
 
     def device_status(self, stream=None) -> int:

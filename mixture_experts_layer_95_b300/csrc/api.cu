@@ -1000,11 +1000,14 @@ size_t moe_backward_workspace_size(const moe_config* cfg) {
     return blayout(*cfg).total;
 }
 
-int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
-                 const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
-                 const void* ws3, const void* ws2, const void* dy, float dL, float* dx, float* dw_gate, float* dw1,
-                 float* dw3, float* dw2, float* dws1, float* dws3, float* dws2, void* ws, size_t ws_bytes,
-                 moe_stream_t stream) {
+// moe_backward and moe_backward_saved: saved = the routing, grouping, x rows
+// in expert order, softmax rows and G, U of the layer call are the ones
+// moe_forward_train left in ws, so they are not recomputed.
+static int backward_impl(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                         const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                         const void* ws3, const void* ws2, const void* dy, float dL, float* dx, float* dw_gate,
+                         float* dw1, float* dw3, float* dw2, float* dws1, float* dws3, float* dws2, void* ws,
+                         size_t ws_bytes, moe_stream_t stream, bool saved) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
     if (c.dtype != MOE_BF16) return MOE_ERR_DTYPE;
@@ -1034,8 +1037,9 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
     const int chunk = router_chunk(c.T, c.E, c.d, c.dtype);
 
     // forward routing and grouping again (the decisions the gradients hold fixed)
-    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates,
-                          at<int32_t>(ws, L.block_hist), sms, s, c.k, probs));
+    if (!saved)
+        MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates,
+                              at<int32_t>(ws, L.block_hist), sms, s, c.k, probs));
     GroupOut o{};
     o.counts = at<int32_t>(ws, L.counts);
     o.kept = at<int32_t>(ws, L.kept);
@@ -1044,12 +1048,13 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
     o.slot_pos = at<int32_t>(ws, L.slot_pos);
     o.gates_perm = at<float>(ws, L.gates_perm);
     o.n_dropped = at<int32_t>(ws, L.n_dropped);
-    MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, at<int32_t>(ws, L.block_hist), o,
-                                 status, s));
+    if (!saved)
+        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates,
+                                     at<int32_t>(ws, L.block_hist), o, status, s));
     const int32_t* rows_end = o.offsets + E;
     void* xp = at<void>(ws, B.xp);
     void* dyp = at<void>(ws, B.dyp);
-    MOE_LAUNCH(launch_gather_rows(MOE_BF16, T, d, n, rows_end, o.sorted_token_ids, x, xp, status, s));
+    if (!saved) MOE_LAUNCH(launch_gather_rows(MOE_BF16, T, d, n, rows_end, o.sorted_token_ids, x, xp, status, s));
     MOE_LAUNCH(launch_gather_rows(MOE_BF16, T, d, n, rows_end, o.sorted_token_ids, dy, dyp, status, s));
     int32_t* kbase = at<int32_t>(ws, B.kbase);
     int32_t* klen = at<int32_t>(ws, B.klen);
@@ -1117,7 +1122,7 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
     // gates is the plain product)
     const bool pair = use_pair_gemm(c);
     const int pm = pair ? kGemmScale : kGemmPlain;
-    {
+    if (!saved) {
         GemmProblem p1[2] = {routed(xp, n, w1, F, d, G), dense(x, T, ws1, Fs, d, at<float>(ws, B.Gs))};
         MOE_LAUNCH(launch_gemm_tc(pm, p1, np, status, sms, s, 1, pair));
         GemmProblem p2[2] = {routed(xp, n, w3, F, d, U), dense(x, T, ws3, Fs, d, at<float>(ws, B.Us))};
@@ -1207,6 +1212,143 @@ int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const
     // dx = sum over kept slots of dX rows + router and shared-expert parts
     MOE_LAUNCH(launch_combine(MOE_F32, T, d, c.k, dXp, o.slot_pos, R, dx, s));
     return MOE_OK;
+}
+
+int moe_forward_train(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                      const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                      const void* ws3, const void* ws2, void* y, const moe_stats* stats, void* ws, size_t ws_bytes,
+                      moe_stream_t stream) {
+    MOE_TRY(check_config(cfg));
+    const moe_config& c = *cfg;
+    if (c.dtype != MOE_BF16) return MOE_ERR_DTYPE;
+    if (expert_choice(c) || c.h_split) return MOE_ERR_SHAPE;  // token choice, single bf16 H
+    if (c.T == 0) return MOE_OK;
+    if (!x || !w_gate || !w1 || !w3 || !w2 || !y || !ws) return MOE_ERR_NULL;
+    if (c.n_shared && (!ws1 || !ws3 || !ws2)) return MOE_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign) return MOE_ERR_WORKSPACE;
+    const BLayout B = blayout(c);
+    if (ws_bytes < B.total) return MOE_ERR_WORKSPACE;
+    for (const void* p : {x, w_gate, w1, w3, w2, (const void*)y})
+        if (!aligned16(p)) return MOE_ERR_ALIGN;
+    if (c.n_shared)
+        for (const void* p : {ws1, ws3, ws2})
+            if (!aligned16(p)) return MOE_ERR_ALIGN;
+    int sms = 0;
+    MOE_TRY(device_sms(&sms));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const Layout L = layout(c);
+    const int E = c.E, F = c.d_ff, d = c.d, T = c.T, Fs = c.d_ff_shared, n = c.T * c.k;
+    int* status = at<int>(ws, L.status);
+    int32_t* topk_ids = at<int32_t>(ws, L.topk_ids);
+    float* gates = at<float>(ws, L.gates);
+    const int chunk = router_chunk(c.T, c.E, c.d, c.dtype);
+    const int nblk = (c.T + chunk - 1) / chunk;
+
+    // 1-4: routing (softmax rows kept) and grouping, into the workspace regions
+    // moe_backward_saved reads
+    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates,
+                          at<int32_t>(ws, L.block_hist), sms, s, c.k, at<float>(ws, B.probs)));
+    GroupOut o{};
+    o.counts = at<int32_t>(ws, L.counts);
+    o.kept = at<int32_t>(ws, L.kept);
+    o.offsets = at<int32_t>(ws, L.offsets);
+    o.sorted_token_ids = at<int32_t>(ws, L.sorted);
+    o.slot_pos = at<int32_t>(ws, L.slot_pos);
+    o.gates_perm = at<float>(ws, L.gates_perm);
+    o.n_dropped = at<int32_t>(ws, L.n_dropped);
+    if (stats && (stats->f || stats->p || stats->L)) {
+        o.p_part = at<float>(ws, L.p_part);
+        o.p_nblk = nblk;
+        o.f = stats->f;
+        o.p_mean = stats->p;
+        o.L = stats->L;
+        o.alpha = c.alpha;
+    }
+    MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, at<int32_t>(ws, L.block_hist), o,
+                                 status, s));
+    if (stats) {  // the counts stay in the workspace for the backward; copies for the caller
+        if (stats->counts && cudaMemcpyAsync(stats->counts, o.counts, 4 * (size_t)E, cudaMemcpyDeviceToDevice, s))
+            return MOE_ERR_CUDA;
+        if (stats->kept && cudaMemcpyAsync(stats->kept, o.kept, 4 * (size_t)E, cudaMemcpyDeviceToDevice, s))
+            return MOE_ERR_CUDA;
+        if (stats->n_dropped && cudaMemcpyAsync(stats->n_dropped, o.n_dropped, 4, cudaMemcpyDeviceToDevice, s))
+            return MOE_ERR_CUDA;
+    }
+    // 5: x rows in expert order
+    void* xp = at<void>(ws, B.xp);
+    MOE_LAUNCH(launch_gather_rows(MOE_BF16, T, d, n, o.offsets + E, o.sorted_token_ids, x, xp, status, s));
+    // 6: expert FFNs; the up GEMM also keeps G and U (fp32) for the backward
+    const bool pair = use_pair_gemm(c);
+    const int np = c.n_shared ? 2 : 1;
+    void* h = at<void>(ws, L.h);
+    void* hs = at<void>(ws, L.h_shared);
+    float* y_perm = at<float>(ws, L.y_perm);
+    float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
+    GemmProblem up[2] = {}, down[2] = {};
+    up[0].A = xp;
+    up[0].a_rows = n;
+    up[0].B1 = w1;
+    up[0].B2 = w3;
+    up[0].offsets = o.offsets;
+    up[0].G = E;
+    up[0].N = F;
+    up[0].K = d;
+    up[0].out = h;
+    up[0].out_g = at<float>(ws, B.G);
+    up[0].out_u = at<float>(ws, B.U);
+    down[0].A = h;
+    down[0].a_rows = n;
+    down[0].B1 = w2;
+    down[0].offsets = o.offsets;
+    down[0].G = E;
+    down[0].N = d;
+    down[0].K = F;
+    down[0].out = y_perm;
+    down[0].row_scale = o.gates_perm;
+    if (c.n_shared) {
+        up[1].A = x;
+        up[1].a_rows = T;
+        up[1].B1 = ws1;
+        up[1].B2 = ws3;
+        up[1].G = 1;
+        up[1].M = T;
+        up[1].N = Fs;
+        up[1].K = d;
+        up[1].out = hs;
+        up[1].out_g = at<float>(ws, B.Gs);
+        up[1].out_u = at<float>(ws, B.Us);
+        down[1].A = hs;
+        down[1].a_rows = T;
+        down[1].B1 = ws2;
+        down[1].G = 1;
+        down[1].M = T;
+        down[1].N = d;
+        down[1].K = Fs;
+        down[1].out = y_shared;
+    }
+    MOE_LAUNCH(launch_gemm_tc(kGemmSwiGLU, up, np, status, sms, s, 1, pair));
+    MOE_LAUNCH(launch_gemm_tc(kGemmScale, down, np, status, sms, s, 1, pair));
+    // 7: combine
+    MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, T, d, c.k, y_perm, o.slot_pos, y_shared, y, s, nullptr));
+    return MOE_OK;
+}
+
+int moe_backward(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                 const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                 const void* ws3, const void* ws2, const void* dy, float dL, float* dx, float* dw_gate, float* dw1,
+                 float* dw3, float* dw2, float* dws1, float* dws3, float* dws2, void* ws, size_t ws_bytes,
+                 moe_stream_t stream) {
+    return backward_impl(cfg, x, w_gate, logit_bias, select_bias, w1, w3, w2, ws1, ws3, ws2, dy, dL, dx, dw_gate, dw1,
+                         dw3, dw2, dws1, dws3, dws2, ws, ws_bytes, stream, false);
+}
+
+int moe_backward_saved(const moe_config* cfg, const void* x, const void* w_gate, const float* logit_bias,
+                       const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
+                       const void* ws3, const void* ws2, const void* dy, float dL, float* dx, float* dw_gate,
+                       float* dw1, float* dw3, float* dw2, float* dws1, float* dws3, float* dws2, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+    return backward_impl(cfg, x, w_gate, logit_bias, select_bias, w1, w3, w2, ws1, ws3, ws2, dy, dL, dx, dw_gate, dw1,
+                         dw3, dw2, dws1, dws3, dws2, ws, ws_bytes, stream, true);
 }
 
 int moe_last_device_status(const moe_config* cfg, void* ws, moe_stream_t stream) {

@@ -279,6 +279,10 @@ struct GemmProblem {
     // = part 1; each part is padded to whole 64-deep k-blocks with zeros.
     int b_mn;
     int kpart;
+    // kGemmSwiGLU (launch_gemm_tc, bf16 weights, ksplit 1): when non-null, the
+    // fp32 pre-activations G = A W1^T and U = A W3^T [rows][N] are written too
+    float* out_g;
+    float* out_u;
     // kGemmSwigluBwd (launch_gemm_tc, ksplit 1): the product D = A B^T [rows][N]
     // is not stored; with G, U the recomputed up projections [rows][N] fp32 and
     // g = row_scale[row] (null: 1), the epilogue writes per element

@@ -101,6 +101,9 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     // tmB2, where tmA is then a 3-D map {kpart, 2, rows} of A = [rows][2 kpart].
     int b_mn;
     int kpart[2];
+    // SwiGLU mode: when non-null, the fp32 G and U ([rows][N] each) go here too
+    float* out_g[2];
+    float* out_u[2];
     // kGemmSwigluBwd epilogue operands (GemmProblem::bwd_*)
     const float* bwd_G[2];
     const float* bwd_U[2];
@@ -308,6 +311,26 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             }
             __nv_bfloat16* dst = out + grow * N + col;
             __nv_bfloat16* dst_lo = out_lo ? out_lo + grow * N + col : nullptr;
+            if (p.out_g[t.prob]) {  // the pre-activation G and U as well (kept for the backward)
+                float* gd = p.out_g[t.prob] + grow * N + col;
+                float* ud = p.out_u[t.prob] + grow * N + col;
+                if (col + 32 <= N) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        reinterpret_cast<float4*>(gd)[q] =
+                            make_float4(__uint_as_float(g[4 * q]), __uint_as_float(g[4 * q + 1]),
+                                        __uint_as_float(g[4 * q + 2]), __uint_as_float(g[4 * q + 3]));
+                        reinterpret_cast<float4*>(ud)[q] =
+                            make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
+                                        __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3]));
+                    }
+                } else {
+                    for (int i = 0; i < 32 && col + i < N; ++i) {
+                        gd[i] = __uint_as_float(g[i]);
+                        ud[i] = __uint_as_float(u[i]);
+                    }
+                }
+            }
             if (col + 32 <= N) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -1184,6 +1207,11 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
             prm.bwd_Hb[q] = static_cast<__nv_bfloat16*>(g.bwd_Hb);
             prm.bwd_dgp_part[q] = g.bwd_dgp_part;
             prm.bwd_dgp_ld[q] = g.bwd_dgp_ld;
+        }
+        if (g.out_g || g.out_u) {
+            if (mode != kGemmSwiGLU || !g.out_g || !g.out_u || ksplit != 1 || g.N % 4 != 0) return cudaErrorInvalidValue;
+            prm.out_g[q] = g.out_g;
+            prm.out_u[q] = g.out_u;
         }
         prm.offsets[q] = g.offsets;
         prm.out[q] = g.out;

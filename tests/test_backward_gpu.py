@@ -116,3 +116,44 @@ def test_backward_rejects_fp32_and_expert_choice(cuda):
     for layer in (moe.Layer(T=4, d=64, E=4, k=2, d_ff=64, dtype="f32"),
                   moe.Layer(T=4, d=64, E=4, k=2, d_ff=64, routing="expert")):
         assert moe.lib().moe_backward_workspace_size(__import__("ctypes").byref(layer.cfg())) == 0
+
+
+SAVED_CASES = [CASES[0], CASES[1], CASES[4], CASES[5]]
+
+
+@pytest.mark.parametrize("w", SAVED_CASES, ids=[w.name for w in SAVED_CASES])
+def test_backward_saved_equals_recompute(cuda, w):
+    """moe_forward_train + moe_backward_saved give moe_backward's gradients
+    bit for bit (G and U come from the same accumulators either way), and
+    the training forward's y passes the forward's bf16 rule against
+    moe_forward's y."""
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    from tests._parity import layer_of
+    layer = layer_of(w)
+    L = moe_inputs.make_layer(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(99)
+    dy = torch.randn((w.T, w.d), generator=g, device="cuda").to(layer.torch_dtype)
+    bw = moe.Backward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
+                      L["ws3"], L["ws2"])
+    y_train = bw.forward_train(L["x"]).clone()
+    saved = {n: t.clone() for n, t in bw(L["x"], dy, dL=1.5, saved=True).items()}
+    assert bw.device_status() == 0
+    recomputed = bw(L["x"], dy, dL=1.5)
+    assert bw.device_status() == 0
+    for n in saved:
+        assert torch.equal(saved[n], recomputed[n]), n
+    y = moe.forward(layer, L["x"], L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"],
+                    L["ws1"], L["ws3"], L["ws2"])
+    a, b = y_train.double(), y.double()
+    rms = float(b.pow(2).mean().sqrt())
+    assert float((a - b).abs().max()) <= TOL * rms
+
+
+def test_forward_train_rejects_expert_choice(cuda):
+    import ctypes
+    import mixture_experts_layer_95_b300 as moe
+    layer = moe.Layer(T=4, d=64, E=4, k=2, d_ff=64, routing="expert")
+    c = layer.cfg()
+    rc = moe.lib().moe_forward_train(ctypes.byref(c), *([None] * 11), None, None, 0, None)
+    assert rc == -2
