@@ -155,7 +155,10 @@ MOE_API int moe_workspace_init(const moe_config *cfg, void *ws, size_t ws_bytes,
  *   (added to the logits for the top-k choice only).
  *   Outputs: topk_ids int32 [T][k] (descending selection score, ties to the lower
  *   expert index), gates fp32 [T][k] (unbiased softmax at those ids, renormalised
- *   when cfg->renormalize), p_mean fp32 [E] or NULL (mean softmax row). */
+ *   when cfg->renormalize), p_mean fp32 [E] or NULL (mean softmax row).
+ *   A NaN selection score ranks below every other score (as -inf), so a token
+ *   with non-finite inputs still gets k distinct valid ids; its gates, and the
+ *   layer's output row for it, are then NaN.  Other tokens are unaffected. */
 MOE_API int moe_route(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
               const float *select_bias, int32_t *topk_ids, float *gates, float *p_mean, void *ws,
               size_t ws_bytes, moe_stream_t stream);

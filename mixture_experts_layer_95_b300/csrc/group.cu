@@ -267,6 +267,10 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
         if (i < whi) {
             int pos = -1;
             if (e >= 0 && (a.capacity < 0 || rank < a.capacity)) pos = s_off[e] + rank;
+            if (pos >= 0 && pos >= s_off[e + 1]) {  // ids that disagree with the histogram rows
+                record_status(a.status, kStatusBounds);
+                pos = -1;
+            }
             a.o.slot_pos[i] = pos;
             if (pos >= 0) {
                 a.o.sorted_token_ids[pos] = i / a.k;

@@ -63,6 +63,10 @@ __device__ __forceinline__ void softmax_topk(int t, int E, int k, const float (&
         psum[j] += p[j];
         if (probs_out && e < E) probs_out[(size_t)t * E + e] = p[j];
         s[j] = (e < E) ? l[j] + (select_bias ? __ldg(select_bias + e) : 0.f) : -FLT_MAX;
+        // a NaN score selects as -inf: the comparisons below then form a total
+        // order (value, then lower index), so every lane agrees on each choice
+        // and the ids match the histogram counted from them
+        if (isnan(s[j])) s[j] = -INFINITY;
     }
     uint32_t taken = 0;
     float gsum = 0.f;
