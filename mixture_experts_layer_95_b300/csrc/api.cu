@@ -259,7 +259,6 @@ struct BLayout {
     int ncols, ncols_s;
 };
 
-constexpr int kWgSplit = 8;  // token chunks of the router weight gradient
 
 BLayout blayout(const moe_config& c) {
     BLayout b{};
@@ -292,7 +291,7 @@ BLayout blayout(const moe_config& c) {
     b.dXp = take(4 * n * d);
     b.dlog = take(4 * T * E);
     b.R = take(4 * T * d);
-    b.wg_part = take(4 * kWgSplit * E * d);
+    b.wg_part = take(4 * (size_t)wgate_grad_split(c.E, c.d) * E * d);
     const bool sh = c.n_shared != 0;
     b.s_off = take(sh ? 8 : 0);
     b.s_kbase = take(sh ? 4 : 0);
@@ -1207,8 +1206,9 @@ static int backward_impl(const moe_config* cfg, const void* x, const void* w_gat
                                       c.alpha, dL, dlog, s));
     MOE_LAUNCH(launch_router_dx(MOE_BF16, T, E, d, dlog, w_gate, dXs, R, s));
     float* wgp = at<float>(ws, B.wg_part);
-    MOE_LAUNCH(launch_wgate_grad(MOE_BF16, T, E, d, dlog, x, kWgSplit, wgp, s));
-    MOE_LAUNCH(launch_reduce_partials(E, nullptr, d, kWgSplit, wgp, dw_gate, s));
+    const int wg_split = wgate_grad_split(E, d);
+    MOE_LAUNCH(launch_wgate_grad(MOE_BF16, T, E, d, dlog, x, wg_split, wgp, s));
+    MOE_LAUNCH(launch_reduce_partials(E, nullptr, d, wg_split, wgp, dw_gate, s));
     // dx = sum over kept slots of dX rows + router and shared-expert parts
     MOE_LAUNCH(launch_combine(MOE_F32, T, d, c.k, dXp, o.slot_pos, R, dx, s));
     return MOE_OK;

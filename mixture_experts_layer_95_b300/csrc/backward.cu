@@ -219,24 +219,26 @@ __global__ void __launch_bounds__(256) router_dx_kernel(int Tn, int E, int d, co
     pdl_trigger();
 }
 
-// part[s][e][i] = sum over tokens t of chunk s of dl[t][e] x[t][i]: 32 experts x
-// 256 columns per block, the tokens split into `nsplit` chunks (summed afterwards
-// in chunk order).
-template <typename T>
+// part[s][e][i] = sum over tokens t of chunk s of dl[t][e] x[t][i]: EB experts x
+// 512 columns per block (two adjacent columns per thread), the tokens split into
+// `nsplit` chunks (summed afterwards in chunk order).  Each thread loads the x
+// values of 32 tokens before it multiplies any of them, so the loads of a batch
+// are in flight together; within a chunk the tokens are added in index order.
+template <typename T, int EB>
 __global__ void __launch_bounds__(256) wgate_grad_kernel(int Tn, int E, int d, const float* __restrict__ dlogits,
                                                          const T* __restrict__ x, int nsplit,
                                                          float* __restrict__ part) {
     pdl_wait();
-    constexpr int EB = 32, TB = 32;
+    constexpr int TB = 32;
     __shared__ float s_dl[TB][EB];
     const int e0 = blockIdx.y * EB;
-    const int i = blockIdx.x * 256 + threadIdx.x;
+    const int i = (blockIdx.x * 256 + threadIdx.x) * 2;  // columns i and i + 1 (d is even)
     const int s = blockIdx.z;
     const int tchunk = (Tn + nsplit - 1) / nsplit;
-    const int ta = s * tchunk, tb = min(Tn, ta + tchunk);
-    float acc[EB];
+    const int ta = min(Tn, s * tchunk), tb = min(Tn, ta + tchunk);
+    float acc0[EB], acc1[EB];
 #pragma unroll
-    for (int q = 0; q < EB; ++q) acc[q] = 0.f;
+    for (int q = 0; q < EB; ++q) acc0[q] = acc1[q] = 0.f;
     for (int tt = ta; tt < tb; tt += TB) {
         __syncthreads();
         for (int j = threadIdx.x; j < TB * EB; j += blockDim.x) {
@@ -245,22 +247,58 @@ __global__ void __launch_bounds__(256) wgate_grad_kernel(int Tn, int E, int d, c
         }
         __syncthreads();
         if (i < d) {
-            const int nt = min(TB, tb - tt);
-            for (int q = 0; q < nt; ++q) {
-                float xv;
-                if constexpr (sizeof(T) == 2) xv = bf2f(x[(size_t)(tt + q) * d + i]);
-                else xv = x[(size_t)(tt + q) * d + i];
+            float x0[TB], x1[TB];
 #pragma unroll
-                for (int e = 0; e < EB; ++e) acc[e] = fmaf(s_dl[q][e], xv, acc[e]);
+            for (int q = 0; q < TB; ++q) {
+                x0[q] = x1[q] = 0.f;
+                if (tt + q < tb) {
+                    const size_t at = (size_t)(tt + q) * d + i;
+                    if constexpr (sizeof(T) == 2) {
+                        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + at));
+                        x0[q] = v.x;
+                        x1[q] = v.y;
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2*>(x + at);
+                        x0[q] = v.x;
+                        x1[q] = v.y;
+                    }
+                }
             }
+#pragma unroll
+            for (int q = 0; q < TB; ++q)
+#pragma unroll
+                for (int e = 0; e < EB; ++e) {
+                    acc0[e] = fmaf(s_dl[q][e], x0[q], acc0[e]);
+                    acc1[e] = fmaf(s_dl[q][e], x1[q], acc1[e]);
+                }
         }
     }
     if (i < d)
 #pragma unroll
         for (int e = 0; e < EB; ++e)
-            if (e0 + e < E) part[((size_t)s * E + e0 + e) * d + i] = acc[e];
+            if (e0 + e < E)
+                *reinterpret_cast<float2*>(part + ((size_t)s * E + e0 + e) * d + i) = make_float2(acc0[e], acc1[e]);
     __syncthreads();
     pdl_trigger();
+}
+
+int wgate_expert_block(int E) { return E <= 8 ? 8 : (E <= 16 ? 16 : 32); }
+
+template <typename T, int EB>
+void launch_wgate_eb(dim3 grid, cudaStream_t s, int T_, int E, int d, const float* dlogits, const void* x, int nsplit,
+                     float* part) {
+    launch_pdl(wgate_grad_kernel<T, EB>, grid, dim3(256), 0, s, T_, E, d, dlogits, static_cast<const T*>(x), nsplit,
+               part);
+}
+
+template <typename T>
+void launch_wgate_t(dim3 grid, cudaStream_t s, int T_, int E, int d, const float* dlogits, const void* x, int nsplit,
+                    float* part) {
+    switch (wgate_expert_block(E)) {
+        case 8: launch_wgate_eb<T, 8>(grid, s, T_, E, d, dlogits, x, nsplit, part); break;
+        case 16: launch_wgate_eb<T, 16>(grid, s, T_, E, d, dlogits, x, nsplit, part); break;
+        default: launch_wgate_eb<T, 32>(grid, s, T_, E, d, dlogits, x, nsplit, part); break;
+    }
 }
 
 }  // namespace
@@ -303,16 +341,23 @@ cudaError_t launch_router_dx(int dtype, int T, int E, int d, const float* dlogit
     return cudaGetLastError();
 }
 
+int wgate_grad_split(int E, int d) {
+    // about two waves of blocks on 148 SMs, at most 32 token chunks
+    const long long blocks = (long long)((d + 511) / 512) * ((E + wgate_expert_block(E) - 1) / wgate_expert_block(E));
+    long long sp = (2LL * 148 + blocks - 1) / blocks;
+    return (int)(sp < 1 ? 1 : (sp > 32 ? 32 : sp));
+}
+
 cudaError_t launch_wgate_grad(int dtype, int T, int E, int d, const float* dlogits, const void* x, int nsplit,
                               float* part, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const dim3 grid((d + 255) / 256, (E + 31) / 32, nsplit);
+    if (d % 2 || nsplit < 1) return cudaErrorInvalidValue;
+    const int eb = wgate_expert_block(E);
+    const dim3 grid((d + 511) / 512, (E + eb - 1) / eb, nsplit);
     if (dtype == MOE_BF16)
-        launch_pdl(wgate_grad_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, T, E, d, dlogits,
-                   static_cast<const __nv_bfloat16*>(x), nsplit, part);
+        launch_wgate_t<__nv_bfloat16>(grid, s, T, E, d, dlogits, x, nsplit, part);
     else
-        launch_pdl(wgate_grad_kernel<float>, grid, dim3(256), 0, s, T, E, d, dlogits, static_cast<const float*>(x),
-                   nsplit, part);
+        launch_wgate_t<float>(grid, s, T, E, d, dlogits, x, nsplit, part);
     return cudaGetLastError();
 }
 

@@ -343,6 +343,9 @@ cudaError_t launch_router_backward(int T, int E, int k, const float* probs, cons
 cudaError_t launch_router_dx(int dtype, int T, int E, int d, const float* dlogits, const void* w_gate,
                              const float* extra, float* R, cudaStream_t s);
 // part[s][e][i] = sum over token chunk s of dlogits[t][e] x[t][i].
+// Token chunks launch_wgate_grad is given for E experts and d columns (the
+// partial buffer holds that many [E][d] slices).
+int wgate_grad_split(int E, int d);
 cudaError_t launch_wgate_grad(int dtype, int T, int E, int d, const float* dlogits, const void* x, int nsplit,
                               float* part, cudaStream_t s);
 

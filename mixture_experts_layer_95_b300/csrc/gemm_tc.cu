@@ -361,12 +361,34 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             }
         }
     } else if (MODE == kGemmSwigluBwd) {
-        // SwiGLU backward on D (this thread's row, 32 columns at a time)
+        // SwiGLU backward on D (this thread's row, 32 columns at a time).  The
+        // G and U values of the next 32 columns are loaded while this chunk is
+        // computed, so each chunk waits for at most one round trip to memory.
         const float g = (valid && p.row_scale[t.prob]) ? __ldg(p.row_scale[t.prob] + grow) : 1.0f;
         const float* Gr = p.bwd_G[t.prob] + grow * N;
         const float* Ur = p.bwd_U[t.prob] + grow * N;
         __nv_bfloat16* dGr = p.bwd_dGU[t.prob] + grow * 2 * N;
         __nv_bfloat16* Hr = p.bwd_Hb[t.prob] + grow * N;
+        auto load_gu = [&](int col, float (&ga)[32], float (&ub)[32]) {
+            const int nc = valid ? min(32, N - col) : 0;
+            if (nc == 32) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 a4 = __ldg(reinterpret_cast<const float4*>(Gr + col) + q);
+                    const float4 b4 = __ldg(reinterpret_cast<const float4*>(Ur + col) + q);
+                    ga[4 * q] = a4.x, ga[4 * q + 1] = a4.y, ga[4 * q + 2] = a4.z, ga[4 * q + 3] = a4.w;
+                    ub[4 * q] = b4.x, ub[4 * q + 1] = b4.y, ub[4 * q + 2] = b4.z, ub[4 * q + 3] = b4.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    ga[i] = i < nc ? __ldg(Gr + col + i) : 0.f;
+                    ub[i] = i < nc ? __ldg(Ur + col + i) : 0.f;
+                }
+            }
+        };
+        float ga[32], ub[32];
+        load_gu(t.n * BN, ga, ub);
         float part = 0.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -375,61 +397,54 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             tmem_ld32(tacc + c0, v);
             tmem_ld_wait();
             const int col = t.n * BN + c0;
-            if (!valid || col >= N) continue;
-            const int nc = min(32, N - col);
+            float gn[32], un[32];
+            if (c0 + 32 < BN) load_gu(col + 32, gn, un);
+            if (valid && col < N) {
+                const int nc = min(32, N - col);
 #pragma unroll
-            for (int q = 0; q < 32; q += 8) {
-                if (q >= nc) continue;  // (fully unrolled: v is indexed with constants only)
-                float a[8], b[8];
-                if (q + 8 <= nc) {
-                    const float4 a0 = __ldg(reinterpret_cast<const float4*>(Gr + col + q));
-                    const float4 a1 = __ldg(reinterpret_cast<const float4*>(Gr + col + q + 4));
-                    const float4 b0 = __ldg(reinterpret_cast<const float4*>(Ur + col + q));
-                    const float4 b1 = __ldg(reinterpret_cast<const float4*>(Ur + col + q + 4));
-                    a[0] = a0.x, a[1] = a0.y, a[2] = a0.z, a[3] = a0.w, a[4] = a1.x, a[5] = a1.y, a[6] = a1.z, a[7] = a1.w;
-                    b[0] = b0.x, b[1] = b0.y, b[2] = b0.z, b[3] = b0.w, b[4] = b1.x, b[5] = b1.y, b[6] = b1.z, b[7] = b1.w;
-                } else {
+                for (int q = 0; q < 32; q += 8) {
+                    if (q >= nc) continue;  // (fully unrolled: v, ga, ub are indexed with constants only)
+                    float dG[8], dU[8], hh[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        a[i] = q + i < nc ? __ldg(Gr + col + q + i) : 0.f;
-                        b[i] = q + i < nc ? __ldg(Ur + col + q + i) : 0.f;
+                        const float a = ga[q + i], b = ub[q + i];
+                        const float dd = __uint_as_float(v[q + i]);
+                        const float sg = 1.0f / (1.0f + __expf(-a));
+                        hh[i] = a * sg * b;
+                        if (q + i < nc) part += dd * hh[i];
+                        const float dh = g * dd;
+                        dG[i] = dh * b * sg * (1.0f + a * (1.0f - sg));
+                        dU[i] = dh * a * sg;
                     }
-                }
-                float dG[8], dU[8], hh[8];
+                    if (q + 8 <= nc) {
+                        uint4 pg, pu, ph;
+                        uint32_t* wg = reinterpret_cast<uint32_t*>(&pg);
+                        uint32_t* wu = reinterpret_cast<uint32_t*>(&pu);
+                        uint32_t* wh = reinterpret_cast<uint32_t*>(&ph);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float dd = __uint_as_float(v[q + i]);
-                    const float sg = 1.0f / (1.0f + __expf(-a[i]));
-                    hh[i] = a[i] * sg * b[i];
-                    if (q + i < nc) part += dd * hh[i];
-                    const float dh = g * dd;
-                    dG[i] = dh * b[i] * sg * (1.0f + a[i] * (1.0f - sg));
-                    dU[i] = dh * a[i] * sg;
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat162 x = __floats2bfloat162_rn(dG[2 * i], dG[2 * i + 1]);
+                            __nv_bfloat162 y = __floats2bfloat162_rn(dU[2 * i], dU[2 * i + 1]);
+                            __nv_bfloat162 z = __floats2bfloat162_rn(hh[2 * i], hh[2 * i + 1]);
+                            wg[i] = *reinterpret_cast<uint32_t*>(&x);
+                            wu[i] = *reinterpret_cast<uint32_t*>(&y);
+                            wh[i] = *reinterpret_cast<uint32_t*>(&z);
+                        }
+                        *reinterpret_cast<uint4*>(dGr + col + q) = pg;
+                        *reinterpret_cast<uint4*>(dGr + N + col + q) = pu;
+                        *reinterpret_cast<uint4*>(Hr + col + q) = ph;
+                    } else {
+                        for (int i = 0; i < 8 && q + i < nc; ++i) {
+                            dGr[col + q + i] = __float2bfloat16_rn(dG[i]);
+                            dGr[N + col + q + i] = __float2bfloat16_rn(dU[i]);
+                            Hr[col + q + i] = __float2bfloat16_rn(hh[i]);
+                        }
+                    }
                 }
-                if (q + 8 <= nc) {
-                    uint4 pg, pu, ph;
-                    uint32_t* wg = reinterpret_cast<uint32_t*>(&pg);
-                    uint32_t* wu = reinterpret_cast<uint32_t*>(&pu);
-                    uint32_t* wh = reinterpret_cast<uint32_t*>(&ph);
+            }
+            if (c0 + 32 < BN) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        __nv_bfloat162 x = __floats2bfloat162_rn(dG[2 * i], dG[2 * i + 1]);
-                        __nv_bfloat162 y = __floats2bfloat162_rn(dU[2 * i], dU[2 * i + 1]);
-                        __nv_bfloat162 z = __floats2bfloat162_rn(hh[2 * i], hh[2 * i + 1]);
-                        wg[i] = *reinterpret_cast<uint32_t*>(&x);
-                        wu[i] = *reinterpret_cast<uint32_t*>(&y);
-                        wh[i] = *reinterpret_cast<uint32_t*>(&z);
-                    }
-                    *reinterpret_cast<uint4*>(dGr + col + q) = pg;
-                    *reinterpret_cast<uint4*>(dGr + N + col + q) = pu;
-                    *reinterpret_cast<uint4*>(Hr + col + q) = ph;
-                } else {
-                    for (int i = 0; i < 8 && q + i < nc; ++i) {
-                        dGr[col + q + i] = __float2bfloat16_rn(dG[i]);
-                        dGr[N + col + q + i] = __float2bfloat16_rn(dU[i]);
-                        Hr[col + q + i] = __float2bfloat16_rn(hh[i]);
-                    }
-                }
+                for (int i = 0; i < 32; ++i) ga[i] = gn[i], ub[i] = un[i];
             }
         }
         if (valid && p.bwd_dgp_part[t.prob]) p.bwd_dgp_part[t.prob][(size_t)t.n * p.bwd_dgp_ld[t.prob] + grow] = part;
@@ -444,24 +459,49 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
         const int lane = threadIdx.x & 31;
         const int wrow0 = row_in_tile - lane;  // first tile row of this warp
         const int nvalid = min(32, t.rows_valid - wrow0);  // rows of this warp that exist
+        // a K-grouped tile with an empty window computed nothing: its output is 0
+        const bool computed = t.kb1 > t.kb0;
+        // the next 32 accumulator columns are read from TMEM while this chunk's
+        // rows are stored; a full 32 x 32 block is read from shared memory into
+        // registers before any of its 32 row stores is issued
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(tacc, v);
+        tmem_ld_wait();
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            __syncwarp();
-            tmem_ld32(tacc + c0, v);
-            tmem_ld_wait();
             const int col = t.n * BN + c0;
-            if (col >= N || nvalid <= 0) continue;  // uniform across the warp
-            if (p.wscale1[t.prob]) apply_wscale32(v, p.wscale1[t.prob], static_cast<size_t>(t.g) * N + col, N - col);
-            // a K-grouped tile with an empty window computed nothing: its output is 0
-            const float sc = t.kb1 > t.kb0 ? scale : 0.0f;
+            const bool live = col < N && nvalid > 0;  // uniform across the warp
+            if (live) {
+                if (p.wscale1[t.prob])
+                    apply_wscale32(v, p.wscale1[t.prob], static_cast<size_t>(t.g) * N + col, N - col);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) stage[lane][i] = t.kb1 > t.kb0 ? sc * __uint_as_float(v[i]) : 0.0f;
+                for (int i = 0; i < 32; ++i) stage[lane][i] = computed ? scale * __uint_as_float(v[i]) : 0.0f;
+            }
             __syncwarp();
-            const bool col_ok = col + lane < N;
-            float* dst = out + (size_t)(t.out_row0 + wrow0) * N + col + lane;
-            for (int r = 0; r < nvalid; ++r)
-                if (col_ok) dst[(size_t)r * N] = stage[r][lane];
+            const bool more = c0 + 32 < BN;
+            uint32_t vn[32];
+            if (more) tmem_ld32(tacc + c0 + 32, vn);
+            if (live) {
+                float* dst = out + (size_t)(t.out_row0 + wrow0) * N + col + lane;
+                if (nvalid == 32 && col + 32 <= N) {
+                    float rv[32];
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) rv[r] = stage[r][lane];
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) dst[(size_t)r * N] = rv[r];
+                } else {
+                    const bool col_ok = col + lane < N;
+                    for (int r = 0; r < nvalid; ++r)
+                        if (col_ok) dst[(size_t)r * N] = stage[r][lane];
+                }
+            }
+            if (more) {
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = vn[i];
+            }
+            __syncwarp();  // the stage block is read before the next chunk overwrites it
         }
     }
 }
