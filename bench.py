@@ -27,6 +27,7 @@ method has) on the same workload, a bounded token sample per step.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -122,12 +123,14 @@ def recorded_traffic(workload):
 
 
 class ClockSampler:
-    """SM clock, power and throttle reasons sampled every 50 ms on a thread.
+    """SM clock, power and throttle reasons sampled every 20 ms on a thread.
 
     Uses NVML in-process (read-only queries; no GPU setting is touched).  It
     is started before the warm-up so that its set-up never overlaps the timed
-    region; `mark` records the timed window and `summary` keeps the samples
-    inside it.  Falls back to `nvidia-smi -lms 50` when NVML is unavailable.
+    region; `mark` records the timed window (epoch seconds) and `summary`
+    keeps the samples inside it.  Falls back to `nvidia-smi -lms 20` when NVML
+    is unavailable; each of its lines carries nvidia-smi's own timestamp, since
+    lines read from a pipe arrive in bursts long after they were sampled.
     """
 
     REASONS = {"hw_slowdown": "nvmlClocksEventReasonHwSlowdown",
@@ -135,7 +138,7 @@ class ClockSampler:
                "sw_thermal_slowdown": "nvmlClocksEventReasonSwThermalSlowdown",
                "sw_power_cap": "nvmlClocksEventReasonSwPowerCap"}
 
-    def __init__(self, gpu_uuid, pci_bus_id=None, period_s=0.05):
+    def __init__(self, gpu_uuid, pci_bus_id=None, period_s=0.02):
         self.samples = []  # (time, sm_mhz, max_mhz, power_w, reasons)
         self.window = None
         self.proc = None
@@ -161,7 +164,7 @@ class ClockSampler:
             self.source = "nvidia-smi"
             try:
                 self.proc = subprocess.Popen(
-                    ["nvidia-smi", "-i", gpu_uuid, "--query-gpu=clocks.sm,clocks.max.sm,power.draw,"
+                    ["nvidia-smi", "-i", gpu_uuid, "--query-gpu=timestamp,clocks.sm,clocks.max.sm,power.draw,"
                      "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                      "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                      "--format=csv,noheader,nounits", "-lms", str(int(period_s * 1000))],
@@ -180,7 +183,7 @@ class ClockSampler:
                 pw = nv.nvmlDeviceGetPowerUsage(self._h) / 1000.0
                 bits = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
                 reasons = [k for k, m in self._masks.items() if bits & m]
-                self.samples.append((time.monotonic(), sm, self._max, pw, reasons))
+                self.samples.append((time.time(), sm, self._max, pw, reasons))
             except Exception:
                 pass
             self._stop.wait(period_s)
@@ -189,11 +192,12 @@ class ClockSampler:
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.proc.stdout:
             p = [x.strip() for x in line.split(",")]
-            if len(p) < 7:
+            if len(p) < 8:
                 continue
             try:
-                self.samples.append((time.monotonic(), float(p[0]), float(p[1]), float(p[2]),
-                                     [n for n, v in zip(names, p[3:7]) if v.lower() in ("active", "1", "yes")]))
+                at = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                self.samples.append((at, float(p[1]), float(p[2]), float(p[3]),
+                                     [n for n, v in zip(names, p[4:8]) if v.lower() in ("active", "1", "yes")]))
             except ValueError:
                 pass
 
@@ -337,7 +341,7 @@ def run_ours(args):
     barrier()
     launches0 = moe.launch_count()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    wall0 = time.monotonic()
+    wall0 = time.time()
     # timed region: the dominant kernel (up GEMM) is bracketed by events in
     # every EVENT_EVERY-th step only (an event between two kernels removes
     # their programmatic overlap); every other launch keeps it
@@ -351,7 +355,7 @@ def run_ours(args):
             fw(x, y)
         end.record(stream)
     end.synchronize()
-    wall1 = time.monotonic()
+    wall1 = time.time()
     barrier()
     clocks.mark(wall0, wall1)
     launches = moe.launch_count() - launches0  # kernels launched inside the timed region

@@ -93,3 +93,26 @@ def test_clock_summary_keeps_samples_inside_the_timed_window():
     s = cs.summary()
     assert s["samples"] == 3 and s["sm_mhz"] == 1900.0 and s["sm_max_mhz"] == 2032.0
     assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 950.0
+
+
+def test_clock_sampler_places_smi_lines_by_their_own_timestamps():
+    """Lines from `nvidia-smi -lms` reach the pipe in bursts; each sample must
+    be placed at the time nvidia-smi took it, not when the line was read."""
+    import datetime
+    import io
+    sys.path.insert(0, ROOT)
+    import bench
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.source, cs.error, cs.samples = "nvidia-smi", None, []
+    lines = ["2026/12/03 04:55:37.107, 1222, 2032, 590.57, Not Active, Not Active, Not Active, Active\n",
+             "2026/12/03 04:55:37.127, 1230, 2032, 600.00, Not Active, Not Active, Not Active, Active\n",
+             "garbage line\n"]
+    cs.proc = type("P", (), {"stdout": io.StringIO("".join(lines))})()
+    cs._read_smi()
+    assert len(cs.samples) == 2
+    t0 = datetime.datetime(2026, 12, 3, 4, 55, 37, 107000).timestamp()
+    assert abs(cs.samples[0][0] - t0) < 1e-3 and abs(cs.samples[1][0] - t0 - 0.02) < 1e-3
+    assert cs.samples[0][1:4] == (1222.0, 2032.0, 590.57) and cs.samples[0][4] == ["sw_power_cap"]
+    cs.window = (t0 - 0.001, t0 + 0.05)
+    s = cs.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 1226.0 and s["reasons"] == ["sw_power_cap"]
