@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
     const int nv = d / VE;  // vectors per row
     {
         const uint4* src = reinterpret_cast<const uint4*>(wg);
+#pragma unroll 8
         for (int i = threadIdx.x; i < NE * nv; i += blockDim.x)
             s_w[i] = (i < E * nv) ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
     }
@@ -194,18 +195,34 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
     for (int q = 0; q < kTpw; ++q)
 #pragma unroll
         for (int e = 0; e < NE; ++e) acc[q][e] = 0.f;
-    for (int v = lane; v < nv; v += 32) {
-        float xv[kTpw][VE];
+    // U of the lane's vectors per token are loaded before any is used, so
+    // U * kTpw loads are in flight per lane; they are added in the same order
+    // (v = lane, lane + 32, ...) as one at a time.  (U = 2 for 16 experts keeps
+    // the accumulators within the 128 registers of a 512-thread block.)
+    constexpr int U = NE <= 8 ? 4 : 2;
+    for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+        uint4 raw[U][kTpw];
 #pragma unroll
-        for (int q = 0; q < kTpw; ++q) widen(__ldg(xr[q] + v), xv[q], static_cast<const T*>(nullptr));
-#pragma unroll
-        for (int e = 0; e < NE; ++e) {
-            float wv[VE];
-            widen(s_w[e * nv + v], wv, static_cast<const T*>(nullptr));
+        for (int u = 0; u < U; ++u)
 #pragma unroll
             for (int q = 0; q < kTpw; ++q)
+                raw[u][q] = v0 + 32 * u < nv ? __ldg(xr[q] + v0 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                for (int i = 0; i < VE; ++i) acc[q][e] = fmaf(xv[q][i], wv[i], acc[q][e]);
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + 32 * u;
+            if (v >= nv) break;  // v rises with u
+            float xv[kTpw][VE];
+#pragma unroll
+            for (int q = 0; q < kTpw; ++q) widen(raw[u][q], xv[q], static_cast<const T*>(nullptr));
+#pragma unroll
+            for (int e = 0; e < NE; ++e) {
+                float wv[VE];
+                widen(s_w[e * nv + v], wv, static_cast<const T*>(nullptr));
+#pragma unroll
+                for (int q = 0; q < kTpw; ++q)
+#pragma unroll
+                    for (int i = 0; i < VE; ++i) acc[q][e] = fmaf(xv[q][i], wv[i], acc[q][e]);
+            }
         }
     }
     float psum[1] = {0.f};
