@@ -554,19 +554,30 @@ class Backward:
                               dws2=torch.empty((d, Fs), **f32))
         self.w = (w_gate, logit_bias, select_bias, w1, w3, w2, ws1, ws3, ws2)
 
-    def forward_train(self, x, y=None, stream=None):
+    def forward_train(self, x, y=None, stream=None, stats: bool = False):
         """moe_forward_train: y of the layer, with the activations the next
-        __call__(..., saved=True) reads kept in this object's workspace."""
+        __call__(..., saved=True) reads kept in this object's workspace.
+        stats=True returns (y, stats) with the same statistics as Forward."""
         L = self.layer
         _need(x, (L.T, L.d), L.torch_dtype, "x")
         if y is None:
             y = torch.empty((L.T, L.d), dtype=L.y_dtype, device=x.device)
         else:
             _need(y, (L.T, L.d), L.y_dtype, "y")
+        st, st_struct = None, None
+        if stats:
+            i32 = dict(dtype=torch.int32, device=x.device)
+            f32 = dict(dtype=torch.float32, device=x.device)
+            E = L.E
+            st = dict(counts=torch.zeros(E, **i32), kept=torch.zeros(E, **i32), f=torch.zeros(E, **f32),
+                      p=torch.zeros(E, **f32), L=torch.zeros(1, **f32), n_dropped=torch.zeros(1, **i32))
+            st_struct = MoeStats(st["counts"].data_ptr(), st["kept"].data_ptr(), st["f"].data_ptr(),
+                                 st["p"].data_ptr(), st["L"].data_ptr(), st["n_dropped"].data_ptr())
         wg, lb, sb, w1, w3, w2, s1, s3, s2 = (_ptr(t) for t in self.w)
         _check(lib().moe_forward_train(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(y),
-                                       None, _ptr(self.ws), self.ws.numel(), _stream(stream)), "moe_forward_train")
-        return y
+                                       ctypes.byref(st_struct) if st_struct is not None else None, _ptr(self.ws),
+                                       self.ws.numel(), _stream(stream)), "moe_forward_train")
+        return (y, st) if stats else y
 
     def __call__(self, x, dy, dL: float = 0.0, stream=None, saved: bool = False):
         """saved=True: moe_backward_saved on the activations of the last

@@ -157,3 +157,25 @@ def test_forward_train_rejects_expert_choice(cuda):
     c = layer.cfg()
     rc = moe.lib().moe_forward_train(ctypes.byref(c), *([None] * 11), None, None, 0, None)
     assert rc == -2
+
+
+def test_forward_train_statistics_equal_the_forward(cuda):
+    """moe_forward_train's load statistics are moe_forward's, bit for bit (the
+    same router and grouping scan; the counts are copied out of the
+    workspace, where the backward reads them)."""
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    from tests._parity import layer_of
+    w = CASES[1]  # shared expert, capacity cut, selection bias
+    layer = layer_of(w)
+    L = moe_inputs.make_layer(w, "cuda")
+    bw = moe.Backward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
+                      L["ws3"], L["ws2"])
+    _, st_train = bw.forward_train(L["x"], stats=True)
+    fw = moe.Forward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
+                     L["ws3"], L["ws2"], stats=True)
+    fw(L["x"])
+    torch.cuda.synchronize()
+    assert int(st_train["n_dropped"].item()) > 0
+    for n in ("counts", "kept", "f", "p", "L", "n_dropped"):
+        assert torch.equal(st_train[n], fw.stats[n]), n
