@@ -562,8 +562,8 @@ int oracle_dequant_fp8(long long rows, int cols, const uint8_t *q, const float *
 }
 
 /*
- * Backward pass of the layer (training; SURVEY's NEXT row, the pages' own
- * statement of the gradients is the load-balancing one): for the scalar
+ * Backward pass of the layer (training; the pages' own statement of the
+ * gradients is the load-balancing one): for the scalar
  *   Loss = <dy, y> + dL * L_balance,
  * with the routing decisions (ids, the capacity cut) held fixed -- top-k
  * selection has no gradient ("MoE Deep Dive", Load Balancing Loss

@@ -2,7 +2,8 @@
 
 Small workloads span several 128-row tiles, ragged segment ends, K and N
 tails, empty experts, dropped entries and every routing variant; the
-BASELINE-sized workloads are checked on every routing and grouping output and
+full-size benchmark workloads (Mixtral, DeepSeek-V3, skewed) are checked on every
+routing and grouping output and
 on a seeded sample of output rows, in the same launch configuration the
 benchmark times.  See tests/_parity.py for the comparison rules.
 """
