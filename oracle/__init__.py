@@ -61,7 +61,7 @@ def _L():
         _lib.oracle_e4m3_decode.argtypes = [ip, vp, vp]
         _lib.oracle_quantize_fp8.argtypes = [ll, ip, ip, vp, vp, vp]
         _lib.oracle_dequant_fp8.argtypes = [ll, ip, vp, vp, vp]
-        _lib.oracle_layer_backward.argtypes = [ip] * 8 + [vp] * 11 + [ip, ctypes.c_double, vp, ctypes.c_double] + [vp] * 9
+        _lib.oracle_layer_backward.argtypes = [ip] * 8 + [vp] * 11 + [ip, ctypes.c_double, vp, ctypes.c_double] + [vp] * 15
         _lib.oracle_ec_slots.argtypes = [ip, ip, ip, vp, vp, vp, vp, vp, vp]
         for f in ("oracle_route", "oracle_gates_for_ids", "oracle_group", "oracle_layer_tokens",
                   "oracle_load_stats", "oracle_num_threads", "oracle_bias_update", "oracle_ec_select",
@@ -358,13 +358,17 @@ def dequant_fp8(q, scale):
 
 # ---------------------------------------------------------------- backward
 
-def backward(layer, k, ids, slot_pos, dy, renormalize=True, alpha=0.01, dL=0.0):
+def backward(layer, k, ids, slot_pos, dy, renormalize=True, alpha=0.01, dL=0.0, magnitudes=False):
     """Gradients of <dy, y> + dL * L_balance with respect to x, W_g, W1, W3, W2
     (and the shared expert's weights), the routing decisions (ids, dropped
     slots) held fixed and f held constant.  layer: dict as for forward();
     ids int32 [T, k]; slot_pos int32 [T, k] or None (< 0 = dropped); dy [T, d]
     (converted to float64).  Returns a dict of float64 arrays: dx, dw_gate,
-    dw1, dw3, dw2, dlogits (and dws1, dws3, dws2 with a shared expert)."""
+    dw1, dw3, dw2, dlogits (and dws1, dws3, dws2 with a shared expert).
+    magnitudes=True adds, for every weight gradient "dwX", "sum_abs_dwX": the
+    sum over the same terms of the products of absolute values (|da| |x|,
+    |db| |x|, |g dy| |h|), the per-entry scale for comparing gradients
+    computed from rounded operands."""
     x = _c(layer["x"])
     dt = _dtype_of(x)
     wg, w1, w3, w2 = (_c(layer[n]) for n in ("w_gate", "w1", "w3", "w2"))
@@ -382,9 +386,14 @@ def backward(layer, k, ids, slot_pos, dy, renormalize=True, alpha=0.01, dL=0.0):
                dw2=np.empty((E, d, F)), dlogits=np.empty((T, E)))
     if shared:
         out.update(dws1=np.empty((Fs, d)), dws3=np.empty((Fs, d)), dws2=np.empty((d, Fs)))
+    if magnitudes:
+        for n in [n for n in out if n.startswith("dw") and n != "dw_gate"]:
+            out["sum_abs_" + n] = np.empty_like(out[n])
     _check(_L().oracle_layer_backward(T, d, E, k, F, int(shared), Fs, dt, _p(x), _p(wg), _p(lb), _p(w1), _p(w3),
                                       _p(w2), _p(s1), _p(s3), _p(s2), _p(ids), _p(sp), int(bool(renormalize)),
                                       float(alpha), _p(dy), float(dL), _p(out["dx"]), _p(out["dw_gate"]),
                                       _p(out["dw1"]), _p(out["dw3"]), _p(out["dw2"]), _p(out.get("dws1")),
-                                      _p(out.get("dws3")), _p(out.get("dws2")), _p(out["dlogits"])), "layer_backward")
+                                      _p(out.get("dws3")), _p(out.get("dws2")), _p(out["dlogits"]),
+                                      *(_p(out.get("sum_abs_" + n)) for n in ("dw1", "dw3", "dw2", "dws1", "dws3", "dws2"))),
+           "layer_backward")
     return out

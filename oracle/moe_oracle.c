@@ -590,8 +590,16 @@ int oracle_dequant_fp8(long long rows, int cols, const uint8_t *q, const float *
  * dy is fp64 [T][d]; every output is fp64 (dx [T][d], dw_gate [E][d],
  * dw1/dw3 [E][F][d], dw2 [E][d][F], dws1/dws3 [F_s][d], dws2 [d][F_s] when
  * n_shared, dlogits [T][E]).  slot_pos < 0 marks a dropped slot.
+ * Optional magnitude sums (nullable, same shapes as dw1/dw3/dw2 and the
+ * shared expert's): sw1 = sum |da| |x|^T, sw3 = sum |db| |x|^T and
+ * sw2 = sum |g dy| |h|^T over the same terms as the gradient entries -- the
+ * scale against which a gradient computed from rounded operands is judged
+ * entry by entry (rounding each factor perturbs every term in proportion
+ * to its own magnitude, so the error of an entry is bounded by a multiple
+ * of its magnitude sum, not of the entry itself).
  * Pinned: PyTorch autograd in fp64 on the same function; central finite
- * differences of the forward oracle.
+ * differences of the forward oracle; the magnitude sums equal |gradient|
+ * for a single term and bound it (triangle inequality) otherwise.
  */
 static double sigmoid(double a) { return 1.0 / (1.0 + exp(-a)); }
 
@@ -600,7 +608,8 @@ int oracle_layer_backward(int T, int d, int E, int k, int F, int n_shared, int F
                           const void *w2, const void *ws1, const void *ws3, const void *ws2, const int32_t *ids,
                           const int32_t *slot_pos, int renormalize, double alpha, const double *dy, double dL,
                           double *dx, double *dw_gate, double *dw1, double *dw3, double *dw2, double *dws1,
-                          double *dws3, double *dws2, double *dlogits) {
+                          double *dws3, double *dws2, double *dlogits, double *sw1, double *sw3, double *sw2,
+                          double *sws1, double *sws3, double *sws2) {
     if (T < 1 || E < 1 || k < 1 || k > E || n_shared < 0 || n_shared > 1) return -1;
     double *gates = (double *)malloc(sizeof(double) * (size_t)T * k);
     double *fcount = (double *)calloc((size_t)E, sizeof(double));
@@ -770,6 +779,12 @@ int oracle_layer_backward(int T, int d, int E, int k, int F, int n_shared, int F
             memset(D1, 0, sizeof(double) * (size_t)Fe * d);
             memset(D3, 0, sizeof(double) * (size_t)Fe * d);
             memset(D2, 0, sizeof(double) * (size_t)d * Fe);
+            double *S1 = shared ? sws1 : (sw1 ? sw1 + b1 : NULL);
+            double *S3 = shared ? sws3 : (sw3 ? sw3 + b1 : NULL);
+            double *S2 = shared ? sws2 : (sw2 ? sw2 + b2 : NULL);
+            if (S1) memset(S1, 0, sizeof(double) * (size_t)Fe * d);
+            if (S3) memset(S3, 0, sizeof(double) * (size_t)Fe * d);
+            if (S2) memset(S2, 0, sizeof(double) * (size_t)d * Fe);
             for (int t = 0; t < T; ++t)
                 for (int j = 0; j < (shared ? 1 : k); ++j) {
                     double g = 1.0;
@@ -801,6 +816,12 @@ int oracle_layer_backward(int T, int d, int E, int k, int F, int n_shared, int F
                             D3[(size_t)f * d + i] += db * xt[i];
                         }
                         for (int o = 0; o < d; ++o) D2[(size_t)o * Fe + f] += g * dyt[o] * hf;
+                        if (S1)
+                            for (int i = 0; i < d; ++i) S1[(size_t)f * d + i] += fabs(da) * fabs(xt[i]);
+                        if (S3)
+                            for (int i = 0; i < d; ++i) S3[(size_t)f * d + i] += fabs(db) * fabs(xt[i]);
+                        if (S2)
+                            for (int o = 0; o < d; ++o) S2[(size_t)o * Fe + f] += fabs(g * dyt[o]) * fabs(hf);
                     }
                 }
         }

@@ -13,7 +13,9 @@ the very same tensors and returns a report of every comparison:
   the oracle's own grouping when no token is inside the margin.
 * x_perm: bit-exact row gather.
 * y: max |y_gpu - y_oracle| <= tol * RMS(y_oracle) over the checked tokens
-  (all tokens, or a seeded sample for the large workloads), with tol = 2e-2
+  (all tokens, or for the large workloads a seeded sample plus the tokens at
+  the first and last row of every 64-row block of every expert segment, so
+  every output tile of the launch has checked rows), with tol = 2e-2
   for bf16 and 1e-4 for fp32; the oracle evaluates y with the GPU's ids.
   For bf16 layers the tolerance applies to the layer's fp32 result (the
   library's y_fp32 output): rounding the output itself to bf16 costs up to
@@ -52,6 +54,21 @@ def sample_tokens(T: int, n: int, seed: int = 1234, must=()) -> np.ndarray:
     rng = np.random.default_rng(seed)
     pick = set(rng.choice(T, n, replace=False).tolist()) | {0, T - 1} | set(int(t) for t in must if 0 <= t < T)
     return np.array(sorted(pick), dtype=np.int32)
+
+
+def tile_cover_tokens(offsets, sorted_token_ids, step: int = 64) -> np.ndarray:
+    """Tokens whose rows are the first and the last row of every `step`-row
+    block of every expert segment.  The GEMMs cut each segment into 128-row
+    (1-CTA), 256-row (CTA-pair) or 64-row tiles that all start on a multiple of
+    64 rows from the segment start, so a 64-row cover puts a checked output row
+    in every tile of every expert, whichever kernel ran."""
+    rows = []
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for b in range(lo, hi, step):
+            rows += [b, min(b + step, hi) - 1]
+    return np.unique(np.asarray(sorted_token_ids, np.int64)[np.asarray(rows, np.int64)]) if rows else \
+        np.zeros(0, np.int64)
 
 
 def run_gpu(w: moe_inputs.Workload, L: dict, layer: moe.Layer):
@@ -129,7 +146,12 @@ def check_layer(w: moe_inputs.Workload, n_sample: int | None = None, L: dict | N
     rep["n_dropped"] = og["n_dropped"]
 
     # ---- layer output ----
-    must = np.nonzero((og["slot_pos"] < 0).any(1))[0][:8] if og["n_dropped"] else ()
+    # a sampled check also covers every (expert, row tile) of the launch
+    must = np.nonzero((og["slot_pos"] < 0).any(1))[0][:8] if og["n_dropped"] else np.zeros(0, np.int64)
+    if n_sample:
+        must = np.concatenate([must, tile_cover_tokens(og["offsets"], og["sorted_token_ids"])])
+        if w.n_shared:  # the shared expert's problem has one row per token
+            must = np.concatenate([must, tile_cover_tokens([0, w.T], np.arange(w.T))])
     toks = sample_tokens(w.T, n_sample if n_sample else w.T, must=must)
     y_or = oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], gids, ogates_for_gpu, og["slot_pos"], toks,
                                (Ln["ws1"], Ln["ws3"], Ln["ws2"]) if w.n_shared else None)
@@ -251,7 +273,8 @@ def check_layer_ec(w: moe_inputs.Workload, n_sample: int | None = None, L: dict 
     src = L["x"][torch.from_numpy(R["sorted_token_ids"].astype(np.int64)).to(xp.device)]
     rep["x_perm_bit_exact"] = bool(torch.equal(xp, src))
 
-    toks = sample_tokens(w.T, n_sample if n_sample else w.T)
+    must = tile_cover_tokens(R["offsets"], R["sorted_token_ids"]) if n_sample else ()
+    toks = sample_tokens(w.T, n_sample if n_sample else w.T, must=must)
     y_or = oracle.layer_tokens(Ln["x"], Ln["w1"], Ln["w3"], Ln["w2"], sl["ids"], sl["gates"], sl["slot_pos"], toks,
                                (Ln["ws1"], Ln["ws3"], Ln["ws2"]) if w.n_shared else None)
     y_gpu = G["y32"].cpu().numpy()[toks].astype(np.float64)

@@ -108,7 +108,11 @@ def test_fp8_decode_tokens_of_very_different_scales(cuda, T):
     _assert_ok(rep)
 
 
-@pytest.mark.parametrize("name", ["mixtral_decode_t1_fp8", "mixtral_decode_t8_fp8"])
+# 1, 8 and 32 tokens (at most 16 rows per touched expert on average): 32-row
+# token tiles; 128 tokens: 48-row tiles over the token codes split in expert
+# order; each at the size the benchmark times
+@pytest.mark.parametrize("name", ["mixtral_decode_t1_fp8", "mixtral_decode_t8_fp8", "mixtral_decode_t32_fp8",
+                                  "mixtral_decode_t128_fp8"])
 def test_fp8_mixtral_decode(cuda, name):
     from tests._parity import check_layer_fp8
     rep = check_layer_fp8(WORKLOADS[name])

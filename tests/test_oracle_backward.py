@@ -65,7 +65,7 @@ def _torch_loss(L, ids, slot_pos, dy, renorm, alpha, dL, k):
     Lb = alpha * E * (f * p.mean(dim=0)).sum()
     loss = (torch.tensor(dy) * y).sum() + dL * Lb
     loss.backward()
-    return {n: v.grad.numpy() for n, v in t.items()}
+    return {n: (v.grad.numpy() if v.grad is not None else np.zeros(v.shape)) for n, v in t.items()}
 
 
 @pytest.mark.parametrize("renorm,shared,capacity,lb", [(True, False, -1, False), (False, False, -1, True),
@@ -127,3 +127,27 @@ def test_balance_loss_gradient_pushes_overloaded_experts_down():
     g = oracle.backward(L, k, ids, None, np.zeros((T, d)), True, 1.0, 1.0)
     # descent direction -dl raises logits of idle experts relative to expert 0
     assert np.all(g["dlogits"][:, 0] > 0) and np.all(g["dlogits"][:, 1:] < 0)
+
+
+def test_magnitude_sums_are_per_token_absolute_gradients_summed():
+    """The weight gradients' magnitude sums (the per-entry scale of the GPU
+    comparison) equal, for every entry, the sum over tokens of |that token's
+    own gradient of the entry| taken from autograd on the one-token layer:
+    each token adds one term per expert block, so its absolute gradient is the
+    product of absolute values.  They also bound |gradient| entry by entry."""
+    rng = np.random.default_rng(70)
+    T, d, E, F, k = 6, 8, 3, 7, 2
+    L = _layer(rng, T, d, E, F, shared=True)
+    fw = oracle.forward(L, k, capacity=3)
+    dy = rng.standard_normal((T, d))
+    got = oracle.backward(L, k, fw["ids"], fw["slot_pos"], dy, True, 0.01, 0.0, magnitudes=True)
+    acc = {n: 0.0 for n in ("w1", "w3", "w2", "ws1", "ws3", "ws2")}
+    for t in range(T):
+        Lt = dict(L, x=L["x"][t:t + 1])
+        ref = _torch_loss(Lt, fw["ids"][t:t + 1], fw["slot_pos"][t:t + 1], dy[t:t + 1], True, 0.01, 0.0, k)
+        for n in acc:
+            acc[n] = acc[n] + np.abs(ref[n])
+    for n in acc:
+        np.testing.assert_allclose(got["sum_abs_d" + n], acc[n], rtol=1e-9, atol=1e-13, err_msg=n)
+        assert np.all(got["sum_abs_d" + n] >= np.abs(got["d" + n]) * (1 - 1e-12)), n
+    assert (fw["slot_pos"] < 0).any()

@@ -122,6 +122,70 @@ def test_softmax_matches_scipy_and_topk_then_softmax_form():
     np.testing.assert_allclose(r["gates"].sum(1), 1.0, rtol=0, atol=1e-14)
 
 
+# gates_for_ids evaluates the gates of ids chosen elsewhere (the GPU's, for a
+# token inside the top-k margin); every parity comparison of y uses it.
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_gates_for_ids_reproduces_route_gates(renorm):
+    """On the router's own ids the gates are the router's, bit for bit
+    (logit and selection biases on, so the ids are not just the top-k of p)."""
+    rng = np.random.default_rng(21)
+    T, d, E, k = 64, 24, 16, 4
+    x = _f32(rng.standard_normal((T, d)))
+    wg = _f32(rng.standard_normal((E, d)) / math.sqrt(d))
+    r = oracle.route(x, wg, k, logit_bias=_f32(rng.standard_normal(E)),
+                     select_bias=_f32(rng.uniform(-0.5, 0.5, E)), renormalize=renorm)
+    np.testing.assert_array_equal(oracle.gates_for_ids(r["probs"], r["ids"], renorm), r["gates"])
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_gates_for_ids_follow_the_ids_not_the_slots(renorm):
+    """Permuting a token's ids permutes its gates the same way (up to the
+    rounding of the renormalising sum, whose order follows the slots)."""
+    rng = np.random.default_rng(22)
+    T, E, k = 50, 10, 3
+    probs = scipy.special.softmax(rng.standard_normal((T, E)), axis=1)
+    ids = np.array([rng.choice(E, k, replace=False) for _ in range(T)], np.int32)
+    g = oracle.gates_for_ids(probs, ids, renorm)
+    perm = np.array([rng.permutation(k) for _ in range(T)])
+    gp = oracle.gates_for_ids(probs, np.take_along_axis(ids, perm, axis=1), renorm)
+    np.testing.assert_allclose(gp, np.take_along_axis(g, perm, axis=1), rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_gates_for_ids_equal_softmax_of_the_chosen_logits(renorm):
+    """For any k distinct ids (not only the top k): renormalised gates are the
+    softmax over the chosen logits alone ("MoE Architecture" route()), plain
+    gates are the full softmax at those ids; both written with scipy from the
+    logits, not from p.  Renormalising over all E, or taking p by slot, fails."""
+    rng = np.random.default_rng(23)
+    T, E, k = 40, 12, 5
+    logits = rng.standard_normal((T, E)) * 2.0
+    probs = scipy.special.softmax(logits, axis=1)
+    ids = np.array([rng.choice(E, k, replace=False) for _ in range(T)], np.int32)
+    g = oracle.gates_for_ids(probs, ids, renorm)
+    sel = np.take_along_axis(logits, ids.astype(np.int64), axis=1)
+    ref = scipy.special.softmax(sel, axis=1) if renorm else \
+        np.take_along_axis(scipy.special.softmax(logits, axis=1), ids.astype(np.int64), axis=1)
+    np.testing.assert_allclose(g, ref, rtol=1e-12, atol=0)
+
+
+def test_gates_for_ids_worked_example():
+    """Deep Dive, Weighted Sum Output: 0.55 and 0.3 become 0.55/0.85 and 0.3/0.85,
+    in either slot order; without renormalisation they stay 0.55 and 0.3."""
+    gd = _golden.load("deepdive_weighted_sum.txt")
+    probs = np.asarray([gd["probs"]], np.float64)
+    a, b = gd["selected"]
+    g = oracle.gates_for_ids(probs, np.array([[a, b]], np.int32), True)
+    np.testing.assert_allclose(g[0], gd["gates"], rtol=1e-15)
+    g = oracle.gates_for_ids(probs, np.array([[b, a]], np.int32), True)
+    np.testing.assert_allclose(g[0], gd["gates"][::-1], rtol=1e-15)
+    g = oracle.gates_for_ids(probs, np.array([[a, b]], np.int32), False)
+    np.testing.assert_array_equal(g[0], [gd["probs"][a], gd["probs"][b]])
+    with pytest.raises(RuntimeError):
+        oracle.gates_for_ids(probs, np.array([[a, len(gd["probs"])]], np.int32), True)
+
+
 def test_bf16_inputs_are_widened_exactly():
     rng = np.random.default_rng(3)
     T, d, E, F, k = 6, 16, 4, 8, 2
