@@ -21,6 +21,16 @@ memory and its output copied back, those copies overlapped with the
 neighbouring steps' layer calls as a serving loop would.  `cpu_baseline`
 times the fp64 CPU oracle on a bounded sample of the same workload.
 
+At N = 1 (unless --no-workloads) the same line also carries `workloads`: every
+other configuration of the layer (decode batches of 1-128 tokens with bf16
+and FP8 experts, the DeepSeek-V3 shape, the skewed layer with a capacity cut,
+the fp32 layer, expert choice), each timed the same way (200 calls for the
+decode-sized and fp32 layers, 20 for the others) with its dominant kernel's
+roofline fraction, the layer's fractions and the SM clock seen; and
+`sustained`: the headline layer called back to back for 1.5 s, long enough
+for the board to reach its power cap, reported against the measured
+sustained bf16 peak with the clock it ran at.
+
 --impl reference times that oracle (the only reference implementation this
 method has) on the same workload, a bounded token sample per step.
 """
@@ -62,6 +72,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="mixtral_prefill")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the sustained loop and the other workloads (N=1 only runs them)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (moe_backward) instead of the forward layer")
@@ -288,6 +300,182 @@ def layer_of(w):
                      routing=w.routing)
 
 
+def up_kernel_name(plan, fp8):
+    name = {"tc_pair": "grouped_gemm_tc_pair_kernel<SwiGLU> (up GEMM, CTA pairs)",
+            "tc": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)",
+            "tc_decode32": "grouped_gemm_decode_kernel<SwiGLU, NT=32> (up GEMM, weights on M)",
+            "tc_decode64": "grouped_gemm_decode_kernel<SwiGLU, NT=64> (up GEMM, weights on M)",
+            "simt": "grouped_gemm_simt_kernel<SwiGLU> (up GEMM)"}[plan["up"]]
+    if fp8:
+        # with FP8 weights the decode GEMM takes 48 token rows where bf16 takes 64
+        name = name.replace("<SwiGLU", "<SwiGLU, FP8 weights").replace("NT=64", "NT=48")
+    return name
+
+
+def config_of(w, world):
+    """The `config` object of the JSON line (both arms print the same one)."""
+    import moe_inputs
+    stored = moe_inputs.expert_weight_bytes(w, w.E)
+    return {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F, "n_shared": w.n_shared,
+            "d_ff_shared": w.F_s, "capacity": w.capacity, "routing": w.routing,
+            "expert_weights": "fp8 e4m3 + fp32 row scales" if w.weights == "fp8" else w.dtype,
+            "parallelism": f"replicas x{world}",
+            "l2": ("working set larger than L2 (expert weights %.2f GB stored)" % (stored / 1e9)) if stored > 126e6
+            else "working set %.1f MB, within L2 (latency-reported)" % (stored / 1e6)}
+
+
+class Bench:
+    """One workload's layer on this GPU: inputs drawn and weights quantised
+    once, then any number of timed loops."""
+
+    def __init__(self, w, dev):
+        import torch
+
+        import mixture_experts_layer_95_b300 as moe
+        import moe_inputs
+        self.w, self.dev = w, dev
+        self.layer = layer_of(w)
+        self.L = moe_inputs.make_layer(w, dev)
+        self.q8 = None
+        if w.weights == "fp8":  # E4M3 experts, quantised on the device before timing
+            names = ["w1", "w3", "w2"] + (["ws1", "ws3", "ws2"] if w.n_shared else [])
+            self.q8 = moe.quantize_experts_fp8(self.layer, *(self.L[n] for n in names))
+        L = self.L
+        self.fw = moe.Forward(self.layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"],
+                              L["ws1"], L["ws3"], L["ws2"], stats=True, device=dev, fp8=self.q8)
+        self.x = L["x"]
+        self.y = torch.empty_like(self.x)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def warm(self, n):
+        import torch
+
+        import mixture_experts_layer_95_b300 as moe
+        for _ in range(n):
+            self.fw(self.x, self.y)
+        torch.cuda.synchronize(self.dev)
+        st = self.fw.device_status()
+        if st != 0:
+            raise moe.MoeError(st, "warm-up device status")
+
+    def timed(self, steps, barrier):
+        """`steps` back-to-back layer calls timed with events on the launching
+        stream; the up GEMM is bracketed in every EVENT_EVERY-th call.
+        Returns (total ms, up-GEMM ms per launch, launches, (wall0, wall1))."""
+        import torch
+
+        import mixture_experts_layer_95_b300 as moe
+        barrier()
+        launches0 = moe.launch_count()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.time()
+        # an event between two kernels removes their programmatic overlap, so
+        # the other calls' launches keep it
+        with moe.StageTimer(steps // EVENT_EVERY + 1, stages=("up_gemm",)) as timer:
+            start.record(self.stream)
+            for i in range(steps):
+                if i % EVENT_EVERY == 0:
+                    timer.begin_call()
+                else:
+                    timer.skip_call()
+                self.fw(self.x, self.y)
+            end.record(self.stream)
+        end.synchronize()
+        wall1 = time.time()
+        barrier()
+        launches = moe.launch_count() - launches0
+        up_ms, up_n = timer.ms()
+        timer.close()
+        st = self.fw.device_status()
+        if st != 0:
+            raise moe.MoeError(st, "timed-region device status")
+        return start.elapsed_time(end), up_ms["up_gemm"] / up_n["up_gemm"], launches, (wall0, wall1)
+
+    def stages(self, steps):
+        """Per-stage breakdown in a separate loop (every stage bracketed)."""
+        import mixture_experts_layer_95_b300 as moe
+        with moe.StageTimer(steps) as br:
+            for _ in range(steps):
+                br.begin_call()
+                self.fw(self.x, self.y)
+        stage_ms, stage_n = br.ms()
+        br.close()
+        return {s: (round(stage_ms[s] / stage_n[s], 4) if stage_n[s] else None) for s in moe.STAGES}
+
+    def accounting(self, ms_per_step, up_ms, peaks, peak_src):
+        """Roofline of the dominant kernel (the up GEMM with the fused SwiGLU)
+        and of the whole layer, from the kept entries the routing produced."""
+        import mixture_experts_layer_95_b300 as moe
+        import moe_inputs
+        w, st = self.w, self.fw.stats
+        kept_total = int(st["kept"].sum().item())
+        n_dropped = int(st["n_dropped"].item())
+        touched = int((st["counts"] > 0).sum().item())
+        up_flops = 2.0 * kept_total * w.d * 2 * w.F + 2.0 * w.T * w.d * 2 * w.F_s * w.n_shared
+        layer_flops = moe_inputs.algorithmic_flops(w, kept_total)
+        wbytes = moe_inputs.expert_weight_bytes(w, touched)
+        # the up GEMM's binding roof: tensor time of its FLOPs vs HBM time of its bytes
+        up_bytes = moe_inputs.up_gemm_bytes(w, touched, kept_total)
+        tensor_bound = up_flops / (peaks["bf16_tflops"] * 1e12) >= up_bytes / (peaks["hbm_gbs"] * 1e9)
+        plan = moe.plan_describe(self.layer.cfg())
+        kernel = up_kernel_name(plan, self.q8 is not None)
+        if self.q8 is not None:
+            plan = dict(plan, weights="fp8_e4m3")
+        if plan["up"] == "simt":
+            # fp32 layers run on the CUDA cores: FMA-pipe bound (fp32 FMA peak from
+            # unit counts and the maximum SM clock: 148 SMs x 128 lanes x 2 FLOP x
+            # 2.032 GHz = 77.0 TFLOP/s)
+            achieved = up_flops / (up_ms / 1e3) / 1e12
+            roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_FMA_TFLOPS, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / round(FP32_FMA_TFLOPS, 1), 4), "traffic": None,
+                    "kernel": kernel, "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2.032 GHz",
+                    "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4)}
+        elif tensor_bound:
+            achieved = up_flops / (up_ms / 1e3) / 1e12
+            roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                    "traffic": recorded_traffic(w.name), "kernel": kernel,
+                    "peak_source": f"{peak_src} bf16 burst", "algorithmic_flop_per_launch": up_flops,
+                    "launch_ms": round(up_ms, 4),
+                    "frac_of_hbm": round(up_bytes / (up_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "algorithmic_bytes_per_launch": up_bytes}
+        else:
+            achieved = up_bytes / (up_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": recorded_traffic(w.name),
+                    "kernel": kernel, "peak_source": f"{peak_src} HBM copy",
+                    "algorithmic_bytes_per_launch": up_bytes, "launch_ms": round(up_ms, 4),
+                    "frac_of_bf16_peak": round(up_flops / (up_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4)}
+        s = ms_per_step / 1e3
+        layer = {"algorithmic_tflop_per_step": round(layer_flops / 1e12, 4),
+                 "tflops": round(layer_flops / s / 1e12, 1),
+                 "frac_bf16_peak": round(layer_flops / s / 1e12 / peaks["bf16_tflops"], 4),
+                 "expert_weight_gbs": round(wbytes / s / 1e9, 1),
+                 "frac_hbm": round(wbytes / s / 1e9 / peaks["hbm_gbs"], 4),
+                 "kept_entries": kept_total, "experts_touched": touched,
+                 ("tokens_without_expert" if w.routing == "expert" else "dropped_entries"): n_dropped,
+                 "plan": plan}
+        return roof, layer
+
+    def close(self):
+        import torch
+        self.fw = self.L = self.q8 = self.x = self.y = None
+        torch.cuda.empty_cache()
+
+
+# workloads measured after the headline, each with its own step count (decode
+# and the latency-bound fp32 layer take 200 calls, the others 20)
+SIDE_WORKLOADS = ("mixtral_decode_t1", "mixtral_decode_t8", "mixtral_decode_t32", "mixtral_decode_t128",
+                  "mixtral_decode_t1_fp8", "mixtral_decode_t8_fp8", "mixtral_decode_t32_fp8",
+                  "mixtral_decode_t128_fp8", "deepseek_v3", "skewed_capacity", "tiny_f32", "mixtral_prefill_ec")
+SUSTAINED_S = 1.5  # length of the back-to-back loop of the sustained figure
+
+
+def side_steps(w):
+    return (200, 10) if (w.T <= 256) else (20, 5)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -303,17 +491,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     _build.build()
     w = moe_inputs.WORKLOADS[args.workload]
-    layer = layer_of(w)
-    L = moe_inputs.make_layer(w, dev)
-    q8 = None
-    if w.weights == "fp8":  # E4M3 experts, quantised on the device before timing
-        names = ["w1", "w3", "w2"] + (["ws1", "ws3", "ws2"] if w.n_shared else [])
-        q8 = moe.quantize_experts_fp8(layer, *(L[n] for n in names))
-    fw = moe.Forward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"], L["ws1"],
-                     L["ws3"], L["ws2"], stats=True, device=dev, fp8=q8)
-    x = L["x"]
-    y = torch.empty_like(x)
-    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
 
     props = torch.cuda.get_device_properties(dev)
     try:  # NVML numbers GPUs physically; the UUID names ours regardless of CUDA_VISIBLE_DEVICES
@@ -326,114 +504,30 @@ def run_ours(args):
         pci = None
     clocks = ClockSampler(gpu_id, pci)  # started before the warm-up: its set-up never overlaps the timed region
 
-    for _ in range(args.warmup):
-        fw(x, y)
-    torch.cuda.synchronize(dev)
-    st = fw.device_status()
-    if st != 0:
-        raise moe.MoeError(st, "warm-up device status")
-
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    barrier()
-    launches0 = moe.launch_count()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    wall0 = time.time()
-    # timed region: the dominant kernel (up GEMM) is bracketed by events in
-    # every EVENT_EVERY-th step only (an event between two kernels removes
-    # their programmatic overlap); every other launch keeps it
-    with moe.StageTimer(args.steps, stages=("up_gemm",)) as timer:
-        start.record(stream)
-        for i in range(args.steps):
-            if i % EVENT_EVERY == 0:
-                timer.begin_call()
-            else:
-                timer.skip_call()
-            fw(x, y)
-        end.record(stream)
-    end.synchronize()
-    wall1 = time.time()
-    barrier()
-    clocks.mark(wall0, wall1)
-    launches = moe.launch_count() - launches0  # kernels launched inside the timed region
-    up_ms_live, up_n = timer.ms()
-    timer.close()
-    # per-stage breakdown in a separate loop (every stage bracketed)
-    with moe.StageTimer(args.steps) as br:
-        for _ in range(args.steps):
-            br.begin_call()
-            fw(x, y)
-    stage_ms, stage_n = br.ms()
-    br.close()
-    ms = max_over_ranks(start.elapsed_time(end), world, dev)
-    st = fw.device_status()
-    if st != 0:
-        raise moe.MoeError(st, "timed-region device status")
-    kept_total = int(fw.stats["kept"].sum().item())
-    n_dropped = int(fw.stats["n_dropped"].item())
-    touched = int((fw.stats["counts"] > 0).sum().item())
-
+    b = Bench(w, dev)
+    b.warm(args.warmup)
+    ms, up_ms, launches, window = b.timed(args.steps, barrier)
+    clocks.mark(*window)
+    ms = max_over_ranks(ms, world, dev)
     ms_per_step = ms / args.steps
     value = job_throughput(w.T, world, args.steps, ms)
-
-    # roofline of the dominant kernel (up GEMM + fused SwiGLU)
-    peaks, peak_src = load_peaks()
-    up_flops = 2.0 * kept_total * w.d * 2 * w.F + 2.0 * w.T * w.d * 2 * w.F_s * w.n_shared
-    down_flops = 2.0 * kept_total * w.d * w.F + 2.0 * w.T * w.d * w.F_s * w.n_shared
-    per = {s: (stage_ms[s] / stage_n[s] if stage_n[s] else None) for s in moe.STAGES}
-    up_ms = up_ms_live["up_gemm"] / up_n["up_gemm"]  # live, inside the timed region
-    layer_flops = moe_inputs.algorithmic_flops(w, kept_total)
-    wbytes = moe_inputs.expert_weight_bytes(w, touched)
-    # the up GEMM's binding roof: tensor time of its FLOPs vs HBM time of its bytes
-    up_bytes = moe_inputs.up_gemm_bytes(w, touched, kept_total)
-    tensor_bound = up_flops / (peaks["bf16_tflops"] * 1e12) >= up_bytes / (peaks["hbm_gbs"] * 1e9)
-    plan = moe.plan_describe(layer_of(w).cfg())
-    up_kernel = {"tc_pair": "grouped_gemm_tc_pair_kernel<SwiGLU> (up GEMM, CTA pairs)",
-                 "tc": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)",
-                 "tc_decode32": "grouped_gemm_decode_kernel<SwiGLU, NT=32> (up GEMM, weights on M)",
-                 "tc_decode64": "grouped_gemm_decode_kernel<SwiGLU, NT=64> (up GEMM, weights on M)",
-                 "simt": "grouped_gemm_simt_kernel<SwiGLU> (up GEMM)"}[plan["up"]]
-    if q8 is not None:
-        # with FP8 weights the decode GEMM takes 48 token rows where bf16 takes 64
-        up_kernel = up_kernel.replace("<SwiGLU", "<SwiGLU, FP8 weights").replace("NT=64", "NT=48")
-        plan = dict(plan, weights="fp8_e4m3")
-    if plan["up"] == "simt":
-        # fp32 layers run on the CUDA cores: FMA-pipe bound (fp32 FMA peak from
-        # unit counts and the maximum SM clock: 148 SMs x 128 lanes x 2 FLOP x
-        # 2.032 GHz = 77.0 TFLOP/s)
-        achieved = up_flops / (up_ms / 1e3) / 1e12
-        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(FP32_FMA_TFLOPS, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / round(FP32_FMA_TFLOPS, 1), 4), "traffic": None, "kernel": up_kernel,
-                "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2.032 GHz",
-                "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4)}
-    elif tensor_bound:
-        achieved = up_flops / (up_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "frac_of_sustained_peak": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                "traffic": recorded_traffic(args.workload),
-                "kernel": up_kernel, "peak_source": f"{peak_src} bf16 burst",
-                "algorithmic_flop_per_launch": up_flops, "launch_ms": round(up_ms, 4),
-                "frac_of_hbm": round(up_bytes / (up_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                "algorithmic_bytes_per_launch": up_bytes}
-    else:
-        achieved = up_bytes / (up_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": recorded_traffic(args.workload),
-                "kernel": up_kernel, "peak_source": f"{peak_src} HBM copy",
-                "algorithmic_bytes_per_launch": up_bytes, "launch_ms": round(up_ms, 4),
-                "frac_of_bf16_peak": round(up_flops / (up_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4)}
+    roof, layer = b.accounting(ms_per_step, up_ms, peaks, peak_src)
+    layer["stage_ms"] = b.stages(args.steps)
+    head_clocks = clocks.summary()
 
     # end to end through the public API: every step copies its batch in from
     # pinned host memory and its result back out (HostPipeline overlaps those
     # copies with the neighbouring steps' layer calls, as a serving loop would)
+    x, y, stream = b.x, b.y, b.stream
     x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     x_h.copy_(x)
     y_h = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
-    pipe = moe.HostPipeline(fw, dev)
+    pipe = moe.HostPipeline(b.fw, dev)
     pipe.run([x_h] * 2, y_h, stream)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -444,7 +538,6 @@ def run_ours(args):
     if not torch.equal(y_h[(args.steps - 1) % 2].to(dev), y):
         raise RuntimeError("end-to-end result differs from the device-timed call's")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    clocks.stop()
     e2e = {"value": round(job_throughput(w.T, world, args.steps, e2e_ms), 1), "unit": UNIT,
            "h2d_bytes_per_step": x_h.numel() * x_h.element_size(),
            "d2h_bytes_per_step": y_h[0].numel() * y_h[0].element_size(),
@@ -454,32 +547,61 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded, N(0,1) tokens, N(0,1/fan_in) weights)",
-        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F, "n_shared": w.n_shared,
-                   "d_ff_shared": w.F_s, "capacity": w.capacity, "routing": w.routing,
-                   "expert_weights": "fp8 e4m3 + fp32 row scales" if w.weights == "fp8" else w.dtype,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "working set larger than L2 (expert weights %.2f GB)" % (wbytes / 1e9)},
+        "config": config_of(w, world),
         "roofline": roof,
-        "layer": {"algorithmic_tflop_per_step": round(layer_flops / 1e12, 4),
-                  "tflops": round(layer_flops / (ms_per_step / 1e3) / 1e12, 1),
-                  "frac_bf16_peak": round(layer_flops / (ms_per_step / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
-                  "expert_weight_gbs": round(wbytes / (ms_per_step / 1e3) / 1e9, 1),
-                  "frac_hbm": round(wbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                  "stage_ms": {s: (round(v, 4) if v is not None else None) for s, v in per.items()},
-                  "kept_entries": kept_total, "experts_touched": touched,
-                  ("tokens_without_expert" if w.routing == "expert" else "dropped_entries"): n_dropped,
-                  "plan": plan},
+        "layer": layer,
         "e2e": e2e,
         "gpu_launches": int(launches),
-        "clocks": clocks.summary(),
+        "clocks": head_clocks,
     }
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        Ln = moe_inputs.layer_numpy(L)
+        Ln = moe_inputs.layer_numpy(b.L)  # the very tensors the GPU arm ran on
         tps, info = time_oracle(w, Ln, args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(tps, 3), "unit": UNIT, "cores": info["cores"], "kind": "oracle",
                                "sample": f"full routing+grouping of {w.T} tokens, expert FFNs of the first "
                                          f"{info['n_tokens']} tokens, extrapolated to {w.T}",
                                "cpu": cpu_model(), **{k: v for k, v in info.items() if k != "cores"}}
+        del Ln
+    if world == 1 and not args.no_workloads:
+        out["workloads"] = {}
+        for name in SIDE_WORKLOADS:
+            ws = moe_inputs.WORKLOADS[name]
+            steps, warm = side_steps(ws)
+            sb = Bench(ws, dev)
+            sb.warm(warm)
+            s_ms, s_up, s_launch, s_win = sb.timed(steps, barrier)
+            clocks.mark(*s_win)
+            s_roof, s_layer = sb.accounting(s_ms / steps, s_up, peaks, peak_src)
+            c = clocks.summary()
+            out["workloads"][name] = {
+                "steps": steps, "ms_per_step": round(s_ms / steps, 4), "value": round(ws.T * steps / (s_ms / 1e3), 1),
+                "unit": UNIT, "kernel": s_roof["kernel"], "kernel_bound": s_roof["bound"],
+                "kernel_frac": s_roof["frac"], "kernel_ms": s_roof["launch_ms"],
+                "layer_frac_bf16_peak": s_layer["frac_bf16_peak"], "layer_frac_hbm": s_layer["frac_hbm"],
+                "kept_entries": s_layer["kept_entries"], "experts_touched": s_layer["experts_touched"],
+                "gpu_launches_per_step": round(s_launch / steps, 2),
+                "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
+            sb.close()
+    if world == 1 and not args.no_workloads:
+        # sustained (last, after the other workloads): the headline layer back
+        # to back for SUSTAINED_S seconds, the regime a continuous caller sees
+        # once the board reaches its power cap
+        n = max(args.steps, int(SUSTAINED_S / (ms_per_step / 1e3)))
+        s_ms, s_up, _, s_win = b.timed(n, barrier)
+        clocks.mark(*s_win)
+        s_roof, s_layer = b.accounting(s_ms / n, s_up, peaks, peak_src)
+        out["sustained"] = {
+            "steps": n, "seconds": round(s_ms / 1e3, 3), "ms_per_step": round(s_ms / n, 4),
+            "value": round(w.T * n / (s_ms / 1e3), 1), "unit": UNIT,
+            "layer_tflops": s_layer["tflops"],
+            "layer_frac_of_sustained_peak": round(s_layer["tflops"] / peaks["bf16_tflops_sustained"], 4),
+            "layer_frac_of_burst_peak": s_layer["frac_bf16_peak"],
+            "up_gemm_ms": s_roof["launch_ms"], "up_gemm_frac_of_sustained_peak": s_roof.get("frac_of_sustained_peak"),
+            "up_gemm_frac_of_burst_peak": s_roof["frac"] if s_roof["bound"] == "tensor" else None,
+            "peak_sustained": peaks["bf16_tflops_sustained"], "clocks": clocks.summary()}
+    b.close()
+    clocks.stop()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -518,8 +640,7 @@ def run_reference(args):
     out = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(1e3 * elapsed / args.steps, 1), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-           "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F,
-                      "n_shared": w.n_shared, "capacity": w.capacity},
+           "config": config_of(w, world),
            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": info["cores"], "kind": "oracle",
                             "sample": sample, "cpu": cpu_model()},
            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -415,6 +415,15 @@ MOE_API const char *moe_strerror(int status);
  * MOE_ERR_NULL (buf NULL or len 0) or a configuration error. */
 MOE_API int moe_plan_describe(const moe_config *cfg, char *buf, size_t len);
 
+/* Test switch for failure detection (no counterpart on the pages): with
+ * on != 0, every tensor-core GEMM launched afterwards in this process (any
+ * thread, any device) issues no operand loads and bounds its waits at 20 ms
+ * instead of 2 s, so its consumers give up, record MOE_ERR_TIMEOUT in the
+ * workspace status word, free their tensor memory and return, leaving the
+ * context usable; on = 0 restores normal launches.  Nothing faults or hangs
+ * either way.  Off at load.  Returns the previous setting (0 or 1). */
+MOE_API int moe_test_stall_gemm(int on);
+
 /* Library version as "major.minor.patch". */
 MOE_API const char *moe_version(void);
 

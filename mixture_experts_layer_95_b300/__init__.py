@@ -28,7 +28,8 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_permut
             "moe_combine", "moe_load_stats", "moe_forward", "moe_last_device_status", "moe_strerror",
             "moe_version", "moe_set_stage_events", "moe_launch_count", "moe_permute_static", "moe_bias_update",
             "moe_plan_describe", "moe_route_expert_choice", "moe_quantize_fp8", "moe_forward_fp8",
-            "moe_backward_workspace_size", "moe_backward", "moe_forward_train", "moe_backward_saved")
+            "moe_backward_workspace_size", "moe_backward", "moe_forward_train", "moe_backward_saved",
+            "moe_test_stall_gemm")
 STAGES = ("router", "group_scan", "gather", "up_gemm", "down_gemm", "combine")
 
 
@@ -88,6 +89,8 @@ def lib():
         L.moe_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         L.moe_set_stage_events.restype = i32
         L.moe_launch_count.restype = ctypes.c_uint64
+        L.moe_test_stall_gemm.argtypes = [i32]
+        L.moe_test_stall_gemm.restype = i32
         L.moe_route_expert_choice.argtypes = [cfgp] + [vp] * 10 + [vp, sz, vp]
         L.moe_quantize_fp8.argtypes = [vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, vp, vp, vp]
         L.moe_quantize_fp8.restype = i32
@@ -131,6 +134,13 @@ def plan_describe(cfg: MoeConfig) -> dict:
 def launch_count() -> int:
     """Kernels launched by the library in this process so far."""
     return int(lib().moe_launch_count())
+
+
+def test_stall_gemm(on: bool) -> bool:
+    """moe_test_stall_gemm: the failure-detection test switch (tensor-core GEMMs
+    launched while it is on issue no loads and time out after 20 ms).
+    Returns the previous setting."""
+    return bool(lib().moe_test_stall_gemm(1 if on else 0))
 
 
 class StageTimer:

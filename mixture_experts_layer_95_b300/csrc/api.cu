@@ -376,6 +376,7 @@ constexpr int kStageEvents = 12;
 thread_local cudaEvent_t g_stage_events[kStageEvents] = {};
 thread_local int g_stage_n = 0;
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_test_stall{0};
 
 enum Stage { kStageRouter = 0, kStageScan = 1, kStageGather = 2, kStageUp = 3, kStageDown = 4, kStageCombine = 5 };
 
@@ -714,6 +715,9 @@ int forward_expert_choice(const moe_config& c, const Layout& L, void* ws, const 
 }
 
 }  // namespace
+
+bool test_stall_gemm() { return g_test_stall.load(std::memory_order_relaxed) != 0; }
+
 }  // namespace moe
 
 using namespace moe;
@@ -1412,5 +1416,7 @@ int moe_set_stage_events(void* const* events, int n) {
 }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_test_stall_gemm(int on) { return g_test_stall.exchange(on != 0 ? 1 : 0, std::memory_order_relaxed); }
 
 }  // extern "C"

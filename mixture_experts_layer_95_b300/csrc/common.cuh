@@ -307,6 +307,12 @@ struct GemmProblem {
 cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
                            cudaStream_t s, int ksplit = 1, bool pair = false);
 
+// Failure-detection test switch (moe_test_stall_gemm): when set, the
+// tensor-core GEMM launchers make the producer issue no loads and bound every
+// wait at kStallWaitLimitNs, so the kernels report MOE_ERR_TIMEOUT and return.
+bool test_stall_gemm();
+constexpr uint64_t kStallWaitLimitNs = 20000000ull;  // 20 ms
+
 // Same grouped GEMM with FP8 (E4M3) B operands: raw one-byte tiles stream in
 // through a deep TMA ring, four converter warps widen them (exactly) to the
 // bf16 swizzled layout the MMA reads, and the epilogue multiplies column n by

@@ -30,7 +30,6 @@
 // step, one per half of the weight tile; four with FP8 tokens); warps 2-5
 // epilogue.  Split-K, per-row gates, FP8 per-channel scales and the bounded
 // mbarrier waits are as in gemm_tc.cu.
-#include <stdlib.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -654,10 +653,9 @@ cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, in
     prm.balanced = balanced ? 1 : 0;
     prm.status = status;
     prm.wait_limit_ns = kWaitLimitNs;
-    const char* stall = getenv("MOE_TEST_STALL_GEMM");
-    if (stall && stall[0] == '1') {
+    if (test_stall_gemm()) {
         prm.stall_producer = 1;
-        prm.wait_limit_ns = 20000000ull;
+        prm.wait_limit_ns = kStallWaitLimitNs;
     }
     const int grid = num_sms > 0 ? num_sms : 148;
     if (mode == kGemmSwiGLU)

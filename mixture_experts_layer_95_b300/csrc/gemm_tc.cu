@@ -36,7 +36,6 @@
 //    MOE_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded)
 //    for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
-#include <stdlib.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -1273,13 +1272,11 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     prm.nprob = nprob;
     prm.status = status;
     prm.wait_limit_ns = kWaitLimitNs;
-    // Test switch for the failure path: MOE_TEST_STALL_GEMM=1 makes the
-    // producer issue no loads; every CTA with work then gives up after a
-    // short bounded wait and reports MOE_ERR_TIMEOUT in the status word.
-    const char* stall = getenv("MOE_TEST_STALL_GEMM");
-    if (stall && stall[0] == '1') {
+    // failure-path test switch: the producer issues no loads, so every CTA
+    // with work gives up after a short bounded wait and reports MOE_ERR_TIMEOUT
+    if (test_stall_gemm()) {
         prm.stall_producer = 1;
-        prm.wait_limit_ns = 20000000ull;  // 20 ms
+        prm.wait_limit_ns = kStallWaitLimitNs;
     }
     const int grid = num_sms > 0 ? num_sms : 148;
     if (pair) {
@@ -1346,10 +1343,9 @@ cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int
     prm.nprob = nprob;
     prm.status = status;
     prm.wait_limit_ns = kWaitLimitNs;
-    const char* stall = getenv("MOE_TEST_STALL_GEMM");
-    if (stall && stall[0] == '1') {
+    if (test_stall_gemm()) {
         prm.stall_producer = 1;
-        prm.wait_limit_ns = 20000000ull;
+        prm.wait_limit_ns = kStallWaitLimitNs;
     }
     const int grid = num_sms > 0 ? num_sms : 148;
     return mode == kGemmSwiGLU ? launch_mode<kGemmSwiGLU, true>(prm, grid, s) : launch_mode<kGemmScale, true>(prm, grid, s);

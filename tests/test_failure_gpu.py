@@ -1,10 +1,14 @@
 """Failure detection on the GPU without a fault (GPU only).
 
-The tensor-core GEMM bounds every mbarrier wait.  The host-side test switch
-MOE_TEST_STALL_GEMM=1 makes its producer issue no loads, so the consumer
-warps' waits run out (20 ms in that mode): the kernel must record
-MOE_ERR_TIMEOUT in the workspace status word, free its TMEM and return, and
-the context must stay usable for the next, normal call.
+Every mbarrier wait of the tensor-core GEMMs is bounded.  The library's test
+switch moe_test_stall_gemm(1) makes their producers issue no loads, so the
+consumer warps' waits run out (20 ms in that mode): each kernel must record
+MOE_ERR_TIMEOUT in the workspace status word, free its TMEM and return, and the
+context must stay usable for the next, normal call.  One case per GEMM kernel:
+the 1-CTA kernel (75 rows per expert), the CTA-pair kernel (550 rows per
+expert: both CTAs of a pair give up and meet at the final cluster barrier) and
+the decode kernel with the weights on the MMA's M side, with bf16 and with FP8
+weights (2 rows per expert).
 """
 import pytest
 import torch
@@ -15,6 +19,13 @@ pytestmark = pytest.mark.gpu
 
 MOE_ERR_TIMEOUT = -7
 
+CASES = [
+    (Workload("stall_tc_bf16", T=300, d=256, E=8, F=256, k=2), "tc"),
+    (Workload("stall_pair_bf16", T=1100, d=256, E=4, F=256, k=2), "tc_pair"),
+    (Workload("stall_decode_bf16", T=8, d=256, E=8, F=256, k=2), "tc_decode32"),
+    (Workload("stall_decode_fp8", T=8, d=256, E=8, F=256, k=2, weights="fp8"), "tc_decode32"),
+]
+
 
 @pytest.fixture(scope="module")
 def cuda():
@@ -23,20 +34,29 @@ def cuda():
     return torch.device("cuda")
 
 
-def test_bounded_wait_times_out_and_the_context_survives(cuda, monkeypatch):
+@pytest.mark.parametrize("w,up_kernel", CASES, ids=[w.name for w, _ in CASES])
+def test_bounded_wait_times_out_and_the_context_survives(cuda, w, up_kernel):
     import mixture_experts_layer_95_b300 as moe
     import moe_inputs
-    from tests._parity import check_layer, layer_of
-    w = Workload("stall_bf16", T=300, d=256, E=8, F=256, k=2)
+    from tests._parity import check_layer, check_layer_fp8, layer_of
+    layer = layer_of(w)
+    assert moe.plan_describe(layer.cfg())["up"] == up_kernel
     L = moe_inputs.make_layer(w, "cuda")
-    fw = moe.Forward(layer_of(w), L["w_gate"], L["w1"], L["w3"], L["w2"])
-    monkeypatch.setenv("MOE_TEST_STALL_GEMM", "1")
-    fw(L["x"])
+    q8 = None
+    if w.weights == "fp8":
+        q8 = moe.quantize_experts_fp8(layer, L["w1"], L["w3"], L["w2"])
+    fw = moe.Forward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], fp8=q8)
+    torch.cuda.synchronize()
+    assert moe.test_stall_gemm(True) is False
+    try:
+        fw(L["x"])
+        torch.cuda.synchronize()
+    finally:
+        moe.test_stall_gemm(False)
     assert fw.device_status() == MOE_ERR_TIMEOUT
     assert fw.device_status() == 0  # read-and-clear
-    monkeypatch.delenv("MOE_TEST_STALL_GEMM")
     fw(L["x"])
     torch.cuda.synchronize()
     assert fw.device_status() == 0
-    rep = check_layer(w, L=L)
+    rep = check_layer_fp8(w, L=L) if q8 is not None else check_layer(w, L=L)
     assert rep["ok"], rep
