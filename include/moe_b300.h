@@ -210,6 +210,10 @@ MOE_API int moe_permute(const moe_config *cfg, const int32_t *topk_ids, const fl
  *   The call allocates nothing and calls no allocating routine.  Its first
  *   call on a device looks up the array's device address (once per device,
  *   with that device current); make that first call before any stream capture.
+ *   With the CUDA runtime's lazy module loading (the default), that first call
+ *   is also when the library's device code, and with it the array, is loaded
+ *   onto the device: a caller whose runtime forbids device allocation after
+ *   start-up makes its first call on each device during start-up.
  *   All calls on a device share the one array and each call overwrites what
  *   the previous one left there, so calls whose kernels overlap on the GPU
  *   (different streams without ordering) race and give wrong results;

@@ -12,7 +12,12 @@
 //
 // The array is a device symbol: host code cannot use its name as a device
 // address, so the first call on each device looks the address up with
-// cudaGetSymbolAddress (with that device current) and caches it.
+// cudaGetSymbolAddress (with that device current) and caches it.  Under the
+// CUDA runtime's lazy module loading that first call is also when the
+// library's device code, the array included, is put on the device, so a
+// caller that must not allocate later makes its first call at start-up.
+#include <atomic>
+
 #include "common.cuh"
 
 // Room for one E-wide histogram per 64-token block: ceil(T / 64) * E int32
@@ -29,7 +34,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 // Device address of the scratch array on each device, filled on first use.
-int32_t* g_scratch_addr[kMaxDevices] = {};
+// Host threads may call concurrently: every writer stores the same address,
+// and the atomics make those racing stores and loads well defined.
+std::atomic<int32_t*> g_scratch_addr[kMaxDevices] = {};
 
 int static_check(const moe_config* c) {
     if (!c) return MOE_ERR_NULL;
@@ -66,13 +73,14 @@ extern "C" int moe_permute_static(const moe_config* cfg, const int32_t* topk_ids
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (major != 10 || minor != 3) return MOE_ERR_DEVICE;
-    if (!g_scratch_addr[dev]) {
+    int32_t* block_hist = g_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!block_hist) {
         // one-time set-up on this device (it is current here)
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-        g_scratch_addr[dev] = static_cast<int32_t*>(p);
+        block_hist = static_cast<int32_t*>(p);
+        g_scratch_addr[dev].store(block_hist, std::memory_order_relaxed);
     }
-    int32_t* block_hist = g_scratch_addr[dev];
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     // The histogram kernel rewrites every entry of block_hist that the scan

@@ -60,3 +60,45 @@ def test_static_scratch_permute_refuses_sizes_beyond_its_scratch(cuda):
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
     rc = lib.moe_permute_static(ctypes.byref(c), *([fake] * 11), None)
     assert rc == -2  # MOE_ERR_SHAPE
+
+
+def test_static_scratch_permute_at_its_exact_limit(cuda):
+    """ceil(T/64) * E == 65,536 (T = 16384, E = 256) is accepted and matches moe_permute."""
+    import mixture_experts_layer_95_b300 as moe
+    layer = moe.Layer(T=16384, d=64, E=256, k=8, d_ff=64)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    ids = torch.argsort(torch.rand((layer.T, layer.E), generator=g, device="cuda"), dim=1)[:, :layer.k]
+    ids = ids.to(torch.int32).contiguous()
+    gates = torch.rand((layer.T, layer.k), generator=g, device="cuda")
+    x = torch.randn((layer.T, layer.d), generator=g, device="cuda").to(torch.bfloat16)
+    ref = moe.permute(layer, ids, gates, x)
+    got = moe.permute_static(layer, ids, gates, x)
+    torch.cuda.synchronize()
+    for name in ("counts", "kept", "offsets", "sorted_token_ids", "slot_pos", "gates_perm", "n_dropped"):
+        assert torch.equal(got[name], ref[name]), name
+    assert torch.equal(got["x_perm"], ref["x_perm"])
+
+
+def test_static_scratch_permute_skips_out_of_range_ids(cuda):
+    """Ids equal to E or negative get no position and are not counted, exactly as
+    in moe_permute (which also records them in its workspace status word)."""
+    import mixture_experts_layer_95_b300 as moe
+    layer = moe.Layer(T=200, d=64, E=8, k=2, d_ff=64)
+    g = torch.Generator(device="cuda").manual_seed(8)
+    ids = torch.argsort(torch.rand((layer.T, layer.E), generator=g, device="cuda"), dim=1)[:, :layer.k]
+    ids = ids.to(torch.int32).contiguous()
+    bad = [(3, 0, layer.E), (50, 1, -1), (199, 0, layer.E + 5)]
+    for t, j, v in bad:
+        ids[t, j] = v
+    gates = torch.rand((layer.T, layer.k), generator=g, device="cuda")
+    x = torch.randn((layer.T, layer.d), generator=g, device="cuda").to(torch.bfloat16)
+    ref = moe.permute(layer, ids, gates, x)
+    got = moe.permute_static(layer, ids, gates, x)
+    torch.cuda.synchronize()
+    for name in ("counts", "kept", "offsets", "sorted_token_ids", "slot_pos", "gates_perm", "n_dropped"):
+        assert torch.equal(got[name], ref[name]), name
+    valid = (ids >= 0) & (ids < layer.E)
+    assert int(got["counts"].sum().item()) == int(valid.sum().item())
+    for t, j, _ in bad:
+        assert int(got["slot_pos"][t, j].item()) == -1
+    assert bool((got["slot_pos"][valid] >= 0).all())
