@@ -143,9 +143,11 @@ typedef struct moe_stats {
  * Returns 0 when cfg is invalid.  The workspace needs 256-byte alignment. */
 MOE_API size_t moe_workspace_size(const moe_config *cfg);
 
-/* Prepares a freshly allocated workspace: zeroes its device status word
- * (enqueued on `stream`).  Call once per workspace before the first entry
- * point; moe_last_device_status clears the word again after reading it.
+/* Prepares a freshly allocated workspace: zeroes its device status word and
+ * the completion counters some kernels keep in it (enqueued on `stream`).
+ * Call once per workspace before the first entry point; every kernel leaves
+ * its counters at zero again, and moe_last_device_status clears the word (and,
+ * after a device error, the counters) again after reading it.
  * Errors: MOE_ERR_NULL, MOE_ERR_WORKSPACE, MOE_ERR_CUDA. */
 MOE_API int moe_workspace_init(const moe_config *cfg, void *ws, size_t ws_bytes, moe_stream_t stream);
 
@@ -398,8 +400,12 @@ MOE_API int moe_last_device_status(const moe_config *cfg, void *ws, moe_stream_t
  * kernel of moe_permute), 2 token rows for the up GEMM (the x_perm gather;
  * with FP8 weights on decode-sized batches, the E4M3 hi/lo split of x),
  * 3 up GEMM (SwiGLU, and its split-K finalize), 4 down GEMM (with FP8 weights
- * on decode-sized batches, after the E4M3 hi/lo split of H), 5 combine.  `events` holds n (<= 12) cudaEvent_t handles owned by
- * the caller; NULL entries are skipped.  Pass events = NULL to clear.
+ * on decode-sized batches, after the E4M3 hi/lo split of H), 5 combine (a
+ * decode-sized batch is grouped inside the router launch, so stage 1 records
+ * nothing there).  `events` holds n (<= 12) cudaEvent_t handles owned by
+ * the caller; NULL entries are skipped.  Pass events = NULL to clear.  On a
+ * stream that is being captured into a CUDA graph the events are recorded
+ * as external event nodes, so every replay of the graph records them.
  * Returns MOE_OK, or MOE_ERR_SHAPE if n is out of range. */
 MOE_API int moe_set_stage_events(void *const *events, int n);
 

@@ -143,6 +143,11 @@ def test_stall_gemm(on: bool) -> bool:
     return bool(lib().moe_test_stall_gemm(1 if on else 0))
 
 
+# True while a StageTimer has stage events set for the next library calls
+# (Forward then enqueues eagerly, so that the events record this call).
+_STAGE_EVENTS_SET = [False]
+
+
 class StageTimer:
     """Per-stage CUDA-event timing of the library's launches (diagnostics).
 
@@ -173,6 +178,7 @@ class StageTimer:
         return ev
 
     def begin_call(self):
+        _STAGE_EVENTS_SET[0] = True
         if self._used == len(self._events):
             self._events.append(self._new_set())
         ev = self._events[self._used]
@@ -185,12 +191,14 @@ class StageTimer:
         """The next library call records no events (its launches keep their
         programmatic overlap)."""
         _check(lib().moe_set_stage_events(None, 0), "moe_set_stage_events")
+        _STAGE_EVENTS_SET[0] = False
 
     def __enter__(self):
         return self
 
     def __exit__(self, *exc):
         lib().moe_set_stage_events(None, 0)
+        _STAGE_EVENTS_SET[0] = False
         return False
 
     def ms(self):
@@ -607,12 +615,24 @@ class Backward:
 
 class Forward:
     """Reusable moe_forward call: checks the weights once, owns the workspace,
-    and enqueues the whole layer per call (the form the benchmark times)."""
+    and enqueues the whole layer per call (the form the benchmark times).
+
+    graph=True replays the layer from a CUDA graph: the first call on a given
+    pair of x / y buffers runs eagerly and records the library's launches
+    (every pointer, the workspace and the statistics buffers included) into a
+    graph; later calls on the same buffers only replay it, which costs the
+    host one graph launch instead of the library's argument checks, tensor
+    map set-up and one launch per kernel.  The layer's configuration and
+    weights are fixed per Forward, so a replay computes exactly what an eager
+    call would."""
 
     def __init__(self, layer: Layer, w_gate, w1, w3, w2, logit_bias=None, select_bias=None, ws1=None, ws3=None,
-                 ws2=None, stats: bool = False, device=None, stream=None, fp8: dict | None = None):
+                 ws2=None, stats: bool = False, device=None, stream=None, fp8: dict | None = None,
+                 graph: bool = False):
         """fp8: an FP8 weight set from quantize_experts_fp8 (then w1/w3/w2 and
         ws1/ws3/ws2 are ignored and may be None; the call is moe_forward_fp8)."""
+        self.graph = graph
+        self._graphs = {}
         dt = layer.torch_dtype
         self.layer = layer
         self.cfg = layer.cfg()
@@ -668,16 +688,60 @@ class Forward:
             y = torch.empty((L.T, L.d), dtype=L.y_dtype, device=x.device)
         else:
             _need(y, (L.T, L.d), L.y_dtype, "y")
+        if self.graph and not _STAGE_EVENTS_SET[0]:
+            key = (x.data_ptr(), y.data_ptr())
+            g = self._graphs.get(key)
+            if g is None:
+                if len(self._graphs) >= 8:
+                    self._graphs.clear()
+                self._graphs[key] = self.capture(x, y, stream=stream)  # (its eager call computed this y)
+                return y
+            if stream is not None:
+                with torch.cuda.stream(stream):
+                    g.replay()
+            else:
+                g.replay()
+            return y
+        self._enqueue(x, y, stream)
+        return y
+
+    def capture(self, x, y, stage_timer=None, stream=None):
+        """Runs one layer call on (x, y) eagerly, then records the same call as
+        a CUDA graph and returns it (torch.cuda.CUDAGraph: .replay() enqueues
+        the whole layer on the current stream).  With stage_timer, that
+        timer's next event set is recorded inside the graph, so each replay
+        records it again."""
+        dev = x.device
+        cur = stream or torch.cuda.current_stream(dev)
+        events_were_set = _STAGE_EVENTS_SET[0]
+        if events_were_set:
+            lib().moe_set_stage_events(None, 0)
+            _STAGE_EVENTS_SET[0] = False
+        self._enqueue(x, y, cur)  # the library's one-time per-device set-up happens outside the capture
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(cur)
+        with torch.cuda.graph(g, stream=side, capture_error_mode="relaxed"):
+            if stage_timer is not None:
+                stage_timer.begin_call()
+            try:
+                self._enqueue(x, y, side)
+            finally:
+                if stage_timer is not None:
+                    stage_timer.skip_call()
+        cur.wait_stream(side)
+        return g
+
+    def _enqueue(self, x, y, stream):
         wg, lb, sb, w1, w3, w2, s1, s3, s2 = self._args
         st = ctypes.byref(self._stats_struct) if self._stats_struct is not None else None
         if self.fp8 is not None:
             _check(lib().moe_forward_fp8(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, ctypes.byref(self._fp8_struct),
                                          _ptr(y), st, _ptr(self.ws), self.ws.numel(), _stream(stream)),
                    "moe_forward_fp8")
-            return y
+            return
         _check(lib().moe_forward(ctypes.byref(self.cfg), _ptr(x), wg, lb, sb, w1, w3, w2, s1, s3, s2, _ptr(y), st,
                                  _ptr(self.ws), self.ws.numel(), _stream(stream)), "moe_forward")
-        return y
 
     def device_status(self, stream=None) -> int:
         return last_device_status(self.layer, self.ws, stream)

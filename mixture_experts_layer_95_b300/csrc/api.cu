@@ -44,13 +44,18 @@ long long perm_rows(const moe_config& c) { return expert_choice(c) ? (long long)
 int slots_per_token(const moe_config& c) { return expert_choice(c) ? c.E : c.k; }
 
 // Large expert segments (at least 512 rows per touched expert on average,
-// bf16, a single bf16 H): both grouped GEMMs run on CTA pairs with 256-row
-// tiles (2-SM tensor-core MMAs).  Smaller segments keep 128-row tiles, which
-// waste fewer rows at segment ends.
+// bf16, a single bf16 H): both grouped GEMMs run on CTA pairs (2-SM
+// tensor-core MMAs) with 256-row tiles, a segment's last tile shrinking to
+// 128 rows (64 per SM) when that covers its remainder.  A pair reads 32 KB of
+// operands per SM and k-block where a 1-SM 128-row tile reads 48 KB for the
+// same MMA work.  Smaller segments keep the 1-SM kernel's 128-row tiles: at
+// ~256 rows per expert (the DeepSeek-V3 shape) the pairs measured slower
+// (8.06 against 7.51 ms per layer call, same box, same clocks).
+constexpr int kPairMinRowsPerExpert = 512;
 bool use_pair_gemm(const moe_config& c) {
     const long long n = perm_rows(c);
     const long long touched = n < c.E ? n : c.E;
-    return c.dtype == MOE_BF16 && c.h_split == 0 && n >= 512 * touched;
+    return c.dtype == MOE_BF16 && c.h_split == 0 && n >= kPairMinRowsPerExpert * touched;
 }
 
 // Decode-sized bf16 batches: at most 32 rows per touched expert on average.
@@ -128,6 +133,14 @@ long long est_row_tiles(const moe_config& c) {
     return by_rows > touched ? by_rows : touched;
 }
 
+// K slices of the router's logits GEMM (bf16, large E): enough 128-token x
+// 256-expert tiles to fill the SMs; the slices are added by the softmax pass.
+int router_ksplit(const moe_config& c) {
+    if (c.dtype != MOE_BF16 || !use_gemm_router(c) || c.T == 0) return 1;
+    const long long tiles = (long long)ceil_div(c.T, 128) * ceil_div(c.E, 256);
+    return choose_ksplit(tiles, ceil_div(c.d, 64), 4);
+}
+
 Splits choose_splits_bf16(const moe_config& c) {
     Splits sp;
     if (c.dtype != MOE_BF16 || c.T == 0) return sp;
@@ -187,8 +200,20 @@ Splits choose_splits(const moe_config& c, bool w8 = false) {
 struct Layout {
     size_t status, topk_ids, gates, p_part, block_hist, counts, kept, offsets, n_dropped, sorted, slot_pos,
         gates_perm, p_mean, f, L, logits, probs, x_perm, h, h_shared, h_lo, h_shared_lo, y_perm, y_shared, part_up,
-        part_up_shared, part_dn, part_dn_shared, xq, xq_s, xsq, xsq_s, hq, hq_s, hsq, hsq_s, total;
+        part_up_shared, part_dn, part_dn_shared, xq, xq_s, xsq, xsq_s, hq, hq_s, hsq, hsq_s, up_sync, up_sync_bytes,
+        total;
 };
+
+// Output tiles of a decode-sized split-K up GEMM, at most: every touched
+// group's rows in 32-row token tiles (one partial tile per group) times the
+// 128-channel column blocks, plus the shared expert's.
+size_t decode_up_tiles(const moe_config& c) {
+    const long long n = perm_rows(c);
+    const long long touched = n < c.E ? n : c.E;
+    const long long routed = ((n + 31) / 32 + touched) * ((c.d_ff + 127) / 128);
+    const long long shared = c.n_shared ? ((long long)(c.T + 31) / 32) * ((c.d_ff_shared + 127) / 128) : 0;
+    return (size_t)(routed + shared);
+}
 
 Layout layout(const moe_config& c) {
     Layout l{};
@@ -206,7 +231,7 @@ Layout layout(const moe_config& c) {
         off = align_up(off + bytes);
         return at;
     };
-    l.status = take(16);
+    l.status = take(16);  // [0] device status word, [1] grouping counter of the one-block-per-token router
     l.topk_ids = take(4 * nk);
     l.gates = take(4 * nk);
     l.p_part = take(4 * nblk * E);
@@ -221,7 +246,7 @@ Layout layout(const moe_config& c) {
     l.p_mean = take(4 * E);
     l.f = take(4 * E);
     l.L = take(4);
-    l.logits = take(use_gemm_router(c) ? 4 * (size_t)c.T * E : 0);
+    l.logits = take(use_gemm_router(c) ? 4 * (size_t)router_ksplit(c) * c.T * E : 0);
     l.probs = take(expert_choice(c) ? 4 * (size_t)c.T * E : 0);
     l.x_perm = take(use_gather_a(c) ? 0 : n * c.d * esize(c));  // not needed when the up GEMM gathers x
     l.h = take(n * c.d_ff * esize(c));
@@ -248,6 +273,10 @@ Layout layout(const moe_config& c) {
     l.hq_s = take(q8 ? 4 * n : 0);
     l.hsq = take(q8 && c.n_shared ? 2 * (size_t)c.T * c.d_ff_shared : 0);
     l.hsq_s = take(q8 && c.n_shared ? 4 * (size_t)c.T : 0);
+    // split-K decode up GEMM: per-output-tile slice counters (zeroed by
+    // moe_workspace_init, zero again after every launch)
+    l.up_sync_bytes = use_decode_gemm(c) && sp.up > 1 ? 4 * decode_up_tiles(c) : 0;
+    l.up_sync = take(l.up_sync_bytes);
     l.total = off;
     return l;
 }
@@ -381,7 +410,14 @@ std::atomic<int> g_test_stall{0};
 enum Stage { kStageRouter = 0, kStageScan = 1, kStageGather = 2, kStageUp = 3, kStageDown = 4, kStageCombine = 5 };
 
 void stage_mark(int idx, cudaStream_t s) {
-    if (idx < g_stage_n && g_stage_events[idx]) cudaEventRecord(g_stage_events[idx], s);
+    if (idx >= g_stage_n || !g_stage_events[idx]) return;
+    // under stream capture the event becomes a record node of the graph, so
+    // that every replay records it (a plain record would only order the capture)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(g_stage_events[idx], s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(g_stage_events[idx], s);
 }
 
 // Records the stage's start event on construction and its stop event on scope exit.
@@ -435,12 +471,39 @@ int enqueue_route(const moe_config& c, const Layout& L, void* ws, const void* x,
     g.N = c.E;
     g.K = c.d;
     g.out = logits;
+    const int rs = router_ksplit(c);
+    if (rs > 1) g.part = logits;  // K slices [rs][T][E]
     if (c.dtype == MOE_BF16)
-        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, &g, 1, at<int>(ws, L.status), sms, s));
+        MOE_LAUNCH(launch_gemm_tc(kGemmPlain, &g, 1, at<int>(ws, L.status), sms, s, rs));
     else
         MOE_LAUNCH(launch_gemm_simt_f32(kGemmPlain, &g, 1, s));
     MOE_LAUNCH(launch_router_from_logits(c.T, c.E, k, logits, logit_bias, select_bias, c.renormalize, topk_ids,
-                                       gates, p_part, block_hist, s, probs));
+                                       gates, p_part, block_hist, s, probs, rs));
+    return MOE_OK;
+}
+
+// Router, softmax, top-k, then the grouping into `o` (statistics too when
+// o.p_part is set).  Decode-sized batches (the one-block-per-token router)
+// group inside the router launch: its last block to finish does it, counted
+// in on the workspace word after the status word.  Otherwise the grouping
+// scan follows as its own launch.
+int enqueue_route_group(const moe_config& c, const Layout& L, void* ws, const void* x, const void* w_gate,
+                        const float* logit_bias, const float* select_bias, int32_t* topk_ids, float* gates,
+                        const GroupOut& o, int sms, cudaStream_t s, float* probs = nullptr) {
+    int* status = at<int>(ws, L.status);
+    int32_t* block_hist = at<int32_t>(ws, L.block_hist);
+    if (use_split_d_router(c.T, c.E)) {
+        StageScope scope(kStageRouter, s);
+        MOE_LAUNCH(launch_router_split_d(c.dtype, c.T, c.d, c.E, c.k, x, w_gate, logit_bias, select_bias,
+                                         c.renormalize, topk_ids, gates, at<float>(ws, L.p_part), block_hist, s, probs,
+                                         &o, c.capacity, reinterpret_cast<unsigned int*>(status + 1), status));
+        return MOE_OK;
+    }
+    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, block_hist, sms, s, c.k,
+                          probs));
+    const int chunk = router_chunk(c.T, c.E, c.d, c.dtype);
+    StageScope scope(kStageScan, s);
+    MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, block_hist, o, status, s));
     return MOE_OK;
 }
 
@@ -580,13 +643,10 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     {
         StageScope scope(kStageUp, s);
         if (use_decode_gemm(c)) {
+            // split-K: the CTA that writes a tile's last K slice applies the SwiGLU itself
             MOE_LAUNCH(launch_gemm_decode(kGemmSwiGLU, up, np, status, sms, s, sp.up, w8 != nullptr,
-                                          decode_tile_rows(c, w8 != nullptr), sp.up_balanced));
-            if (sp.up > 1) {
-                MOE_LAUNCH(launch_swiglu_finalize(n, offsets + c.E, c.d_ff, sp.up, up[0].part, h, nullptr, s));
-                if (c.n_shared)
-                    MOE_LAUNCH(launch_swiglu_finalize(c.T, nullptr, c.d_ff_shared, sp.up, up[1].part, hs, nullptr, s));
-            }
+                                          decode_tile_rows(c, w8 != nullptr), sp.up_balanced,
+                                          sp.up > 1 ? at<unsigned int>(ws, L.up_sync) : nullptr));
         } else if (w8) {
             MOE_LAUNCH(launch_gemm_tc_w8(kGemmSwiGLU, up, np, status, sms, s, sp.up));
             if (sp.up > 1) {
@@ -734,6 +794,8 @@ int moe_workspace_init(const moe_config* cfg, void* ws, size_t ws_bytes, moe_str
     MOE_TRY(check_ws(cfg, ws, ws_bytes));
     const Layout L = layout(*cfg);
     MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.status), 0, 16, reinterpret_cast<cudaStream_t>(stream)));
+    if (L.up_sync_bytes)
+        MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.up_sync), 0, L.up_sync_bytes, reinterpret_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 
@@ -909,10 +971,8 @@ static int forward_body(const moe_config& c, const void* x, const void* w_gate, 
         return forward_expert_choice(c, L, ws, x, w_gate, logit_bias, w1, w3, w2, ws1, ws3, ws2, y, stats, nblk,
                                      sms, s, w8);
 
-    // 1-3: router, softmax, top-k; the router blocks also emit their id histograms
-    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, block_hist, sms, s, c.k));
-
-    // 4: grouping (+ load statistics from the router's partial sums)
+    // 1-4: router, softmax, top-k (the router blocks also emit their id
+    // histograms), grouping (+ load statistics from the router's partial sums)
     GroupOut o{};
     o.counts = (stats && stats->counts) ? stats->counts : at<int32_t>(ws, L.counts);
     o.kept = (stats && stats->kept) ? stats->kept : at<int32_t>(ws, L.kept);
@@ -929,10 +989,7 @@ static int forward_body(const moe_config& c, const void* x, const void* w_gate, 
         o.L = stats->L;
         o.alpha = c.alpha;
     }
-    {
-        StageScope scope(kStageScan, s);
-        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, block_hist, o, status, s));
-    }
+    MOE_TRY(enqueue_route_group(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, o, sms, s));
     // 5-6: rows in expert order (decode-sized bf16 batches: the up GEMM
     // gathers x rows itself with TMA gather4), expert FFNs (routed groups +
     // shared expert in the same launches), combine
@@ -1040,9 +1097,6 @@ static int backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     const int chunk = router_chunk(c.T, c.E, c.d, c.dtype);
 
     // forward routing and grouping again (the decisions the gradients hold fixed)
-    if (!saved)
-        MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates,
-                              at<int32_t>(ws, L.block_hist), sms, s, c.k, probs));
     GroupOut o{};
     o.counts = at<int32_t>(ws, L.counts);
     o.kept = at<int32_t>(ws, L.kept);
@@ -1052,8 +1106,7 @@ static int backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     o.gates_perm = at<float>(ws, L.gates_perm);
     o.n_dropped = at<int32_t>(ws, L.n_dropped);
     if (!saved)
-        MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates,
-                                     at<int32_t>(ws, L.block_hist), o, status, s));
+        MOE_TRY(enqueue_route_group(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, o, sms, s, probs));
     const int32_t* rows_end = o.offsets + E;
     void* xp = at<void>(ws, B.xp);
     void* dyp = at<void>(ws, B.dyp);
@@ -1250,8 +1303,6 @@ int moe_forward_train(const moe_config* cfg, const void* x, const void* w_gate, 
 
     // 1-4: routing (softmax rows kept) and grouping, into the workspace regions
     // moe_backward_saved reads
-    MOE_TRY(enqueue_route(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates,
-                          at<int32_t>(ws, L.block_hist), sms, s, c.k, at<float>(ws, B.probs)));
     GroupOut o{};
     o.counts = at<int32_t>(ws, L.counts);
     o.kept = at<int32_t>(ws, L.kept);
@@ -1268,8 +1319,8 @@ int moe_forward_train(const moe_config* cfg, const void* x, const void* w_gate, 
         o.L = stats->L;
         o.alpha = c.alpha;
     }
-    MOE_LAUNCH(launch_group_scan(c.T, c.E, c.k, chunk, c.capacity, topk_ids, gates, at<int32_t>(ws, L.block_hist), o,
-                                 status, s));
+    MOE_TRY(enqueue_route_group(c, L, ws, x, w_gate, logit_bias, select_bias, topk_ids, gates, o, sms, s,
+                                at<float>(ws, B.probs)));
     if (stats) {  // the counts stay in the workspace for the backward; copies for the caller
         if (stats->counts && cudaMemcpyAsync(stats->counts, o.counts, 4 * (size_t)E, cudaMemcpyDeviceToDevice, s))
             return MOE_ERR_CUDA;
@@ -1363,7 +1414,12 @@ int moe_last_device_status(const moe_config* cfg, void* ws, moe_stream_t stream)
     int v = 0;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemcpy(&v, at<int>(ws, L.status), sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-    if (v != 0 && cudaMemset(at<int>(ws, L.status), 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (v != 0) {
+        // a kernel that gave up may have left its counters mid-count: clear them with the word
+        if (cudaMemset(at<int>(ws, L.status), 0, 16) != cudaSuccess) return MOE_ERR_CUDA;
+        if (L.up_sync_bytes && cudaMemset(at<int>(ws, L.up_sync), 0, L.up_sync_bytes) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     return v;
 }
 

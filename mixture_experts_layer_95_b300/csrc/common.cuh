@@ -160,17 +160,25 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
 
 // Router for T <= kSplitDRouterMaxT and E <= 32: one block per token, same
 // outputs with one histogram row per token.
+// group != nullptr (T <= 256, E <= 32): the last block to finish also groups
+// the batch into *group (as launch_group_scan with one token per histogram
+// row, statistics included when group->p_part is set); `counter` is a
+// workspace word that is zero before the launch and zero again after it.
+struct GroupOut;
 cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
                                   const float* logit_bias, const float* select_bias, int renormalize,
                                   int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
-                                  cudaStream_t s, float* probs = nullptr);
+                                  cudaStream_t s, float* probs = nullptr, const GroupOut* group = nullptr,
+                                  int capacity = -1, unsigned int* counter = nullptr, int* status = nullptr);
 
 // Softmax / top-k over precomputed fp32 logits [T][E] (any E <= kMaxExperts);
 // same outputs as the fused router.
+// nsplit > 1: logits holds nsplit fp32 K slices [nsplit][T][E] of the
+// logits GEMM, added in slice order.
 cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, const float* logit_bias,
                                       const float* select_bias, int renormalize, int32_t* topk_ids,
                                       float* gates, float* p_part, int32_t* block_hist, cudaStream_t s,
-                                      float* probs = nullptr);
+                                      float* probs = nullptr, int nsplit = 1);
 
 // p_mean[e] = (sum over blocks of p_part[b][e]) / T, fixed order.
 cudaError_t launch_p_mean(int T, int E, int nblk, const float* p_part, float* p_mean, cudaStream_t s);
@@ -328,8 +336,12 @@ cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int
 // balanced (ksplit 2, one problem): every CTA takes an equal contiguous
 // share of all tiles' k-blocks (slice 0 = a tile's part from k-block 0,
 // slice 1 = the rest, zeros when one CTA covered the whole tile).
+// tile_sync (SwiGLU, ksplit > 1): one zeroed counter per output tile
+// (decode_tile_sync_words); the kernel then finishes the SwiGLU itself (no
+// launch_swiglu_finalize) and leaves the counters zero again.
 cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
-                               cudaStream_t s, int ksplit, bool w8, int nt, bool balanced = false);
+                               cudaStream_t s, int ksplit, bool w8, int nt, bool balanced = false,
+                               unsigned int* tile_sync = nullptr);
 
 // ---- backward pass (backward.cu) ----
 // kbase[e] = sum_{e' < e} round64(klen[e']), klen[e] = offsets[e+1] - offsets[e];

@@ -72,6 +72,10 @@ struct DecParams {  // CUtensorMap members carry their own 64-byte alignment
     // tile's part that starts at k-block 0 is slice 0, the rest slice 1 (a
     // tile one CTA covers whole writes zeros to slice 1)
     int balanced;
+    // SwiGLU with split-K (non-null): one counter per output tile (zero
+    // before the launch); the CTA that writes a tile's last K slice sums the
+    // slices, applies SwiGLU and writes H itself, and resets the counter
+    unsigned int* tile_sync;
     int* status;
     uint64_t wait_limit_ns;
     int stall_producer;
@@ -84,12 +88,17 @@ struct DecTail {
     uint64_t tmem_empty[2];
     uint32_t tmem_base;
     int abort_flag;
+    int fix_last;  // epilogue: this CTA wrote the current tile's last K slice
     int total[2];
     int gbase[2];
     int tile_start[MAX_GROUPS + 1];  // a group's rows come from the offsets (grp_rows)
 };
 
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
+// The producer asks L2 for the weight tile of the stage this many stages past
+// the one it loads (into the CTA's next work item at an item's end), so that
+// a freed stage refills from L2 instead of waiting on HBM.
+constexpr int kDecL2Prefetch = 4;
 
 // A stage: the 256-row weight tile (128-byte rows), then the token tile(s):
 // NT rows of 64 bf16, or NT rows of 128 hi codes and NT rows of 128 lo codes.
@@ -125,6 +134,7 @@ struct DTile {
     int x_row0, rows_valid;
     int ks, kb0, kb1;  // K slice and its range of stages [kb0, kb1) (KPS k-blocks each)
     bool whole;        // balanced split-K: this CTA covers the whole K range (slice 1 gets zeros)
+    int out_id;        // output tile (the tile-list entries of its K slices share it)
 };
 
 // output columns one tile covers: 128 (the W1/W3 pair) or 256 (W2)
@@ -175,6 +185,7 @@ __device__ __forceinline__ DTile dec_tile(const DecTail& st, const DecParams& p,
     t.kb0 = t.ks * nk / units;
     t.kb1 = (t.ks + 1) * nk / units;
     t.whole = p.balanced != 0;
+    t.out_id = id / units;  // every group's and problem's entry count is a multiple of units
     return t;
 }
 
@@ -332,6 +343,31 @@ __device__ __forceinline__ void dec_epilogue(const DecParams& p, const DTile& t,
     }
 }
 
+// Split-K SwiGLU finished by the CTA that wrote an output tile's last K
+// slice: for this thread's hidden channel f, every token row of the tile sums
+// its K slices in slice order (the other CTAs' partials read through L2) and
+// becomes silu(g) * u in bf16 -- the arithmetic of swiglu_finalize_kernel, in
+// the same order, so H is bit-identical to the separate pass it replaces.
+template <int NT>
+__device__ __forceinline__ void dec_swiglu_fixup(const DecParams& p, const DTile& t, int wrow) {
+    const int N = p.N[t.prob];
+    const int f = t.n * (WR / 2) + wrow;
+    if (f >= N) return;
+    const size_t pc = static_cast<size_t>(p.part_cols[t.prob]);
+    const size_t stride = static_cast<size_t>(p.x_rows[t.prob]) * pc;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.prob]);
+    for (int j = 0; j < t.rows_valid; ++j) {
+        const size_t row = static_cast<size_t>(t.x_row0 + j);
+        const float* gp = p.part[t.prob] + row * pc + f;
+        float g = __ldcg(gp), u = __ldcg(gp + N);
+        for (int sl = 1; sl < p.ksplit; ++sl) {
+            g += __ldcg(gp + sl * stride);
+            u += __ldcg(gp + sl * stride + N);
+        }
+        out[row * N + f] = __float2bfloat16_rn(g / (1.0f + __expf(-g)) * u);
+    }
+}
+
 template <int MODE, bool W8, int NT>
 __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(const __grid_constant__ DecParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -423,6 +459,15 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
         DTile t;
         while (!dead && dec_work_next<MODE, NT, KPS>(st, p, work, t)) {
             const int w_row0 = t.g * p.N[t.prob] + t.n * dec_cols<MODE>();
+            // the next work item (the same sequence, advanced on a copy), for the L2 prefetch
+            DecWork peek = work;
+            DTile nt;
+            const bool has_next = kDecL2Prefetch > 0 && dec_work_next<MODE, NT, KPS>(st, p, peek, nt);
+            auto prefetch_stage = [&](const DTile& q, int kb) {
+                const int row = q.g * p.N[q.prob] + q.n * dec_cols<MODE>();
+                tma_prefetch_2d(&p.tmW1[q.prob], kb * KPS * BK, row);
+                if (MODE == kGemmSwiGLU) tma_prefetch_2d(&p.tmW2[q.prob], kb * KPS * BK, row);
+            };
             const int32_t* gidx = p.x_gather[t.prob];
             int rows4[4] = {0, 0, 0, 0};
             if (gidx) {
@@ -458,6 +503,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
                     if (!gidx) {
                         tma_load_2d(sw + WBYTES, &p.tmX[t.prob], kc, t.x_row0, &st.full[s]);
                         if (W8) tma_load_2d(sw + WBYTES + XBYTES, &p.tmXlo[t.prob], kc, t.x_row0, &st.full[s]);
+                    }
+                    if (kDecL2Prefetch > 0) {
+                        const int pk = kb + kDecL2Prefetch;
+                        if (pk < t.kb1) prefetch_stage(t, pk);
+                        else if (has_next && pk - t.kb1 + nt.kb0 < nt.kb1) prefetch_stage(nt, pk - t.kb1 + nt.kb0);
                     }
                 }
                 if (gidx && lane * 4 < t.rows_valid) {
@@ -551,6 +601,26 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.tmem_empty[acc]);
+            if (MODE == kGemmSwiGLU && p.tile_sync) {
+                // count this slice in once all four epilogue warps have written it
+                __threadfence();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (warp == 2 && lane == 0) {
+                    const unsigned int mine = (p.balanced && t.whole) ? 2u : 1u;  // slices this CTA wrote
+                    int last = 1;
+                    if (mine < (unsigned int)p.ksplit) {
+                        const unsigned int before = atomicAdd(p.tile_sync + t.out_id, mine);
+                        last = before + mine == (unsigned int)p.ksplit;
+                        if (last) p.tile_sync[t.out_id] = 0u;  // every slice is in: ready for the next launch
+                    }
+                    st.fix_last = last;
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (st.fix_last) {
+                    __threadfence();
+                    dec_swiglu_fixup<NT>(p, t, wrow);
+                }
+            }
         }
     }
 
@@ -596,8 +666,9 @@ cudaError_t launch_dec_nt(const DecParams& prm, int nt, int grid, cudaStream_t s
 }  // namespace
 
 cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, int* status, int num_sms,
-                               cudaStream_t s, int ksplit, bool w8, int nt, bool balanced) {
+                               cudaStream_t s, int ksplit, bool w8, int nt, bool balanced, unsigned int* tile_sync) {
     if (balanced && (ksplit != 2 || nprob != 1)) return cudaErrorInvalidValue;
+    if (tile_sync && (mode != kGemmSwiGLU || ksplit < 2)) return cudaErrorInvalidValue;
     if (nprob < 1 || nprob > 2 || ksplit < 1 || (nt != 32 && nt != 64 && !(nt == 48 && w8)))
         return cudaErrorInvalidValue;
     if (mode != kGemmSwiGLU && mode != kGemmScale) return cudaErrorInvalidValue;
@@ -651,6 +722,7 @@ cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, in
     }
     prm.nprob = nprob;
     prm.balanced = balanced ? 1 : 0;
+    prm.tile_sync = tile_sync;
     prm.status = status;
     prm.wait_limit_ns = kWaitLimitNs;
     if (test_stall_gemm()) {

@@ -68,6 +68,10 @@ constexpr int W8_RAW_BYTES = A_BYTES + F8_BYTES;
 constexpr int W8_WIDE = 2;          // widened bf16 B tiles feeding the MMA
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = kMaxExperts;
+// The 1-SM producer asks L2 for the operand tiles of the k-block this many
+// blocks past the one it loads (into the next tile at a tile's end), so that
+// a shared-memory stage, once free, refills from L2 instead of waiting on HBM.
+constexpr int kL2Prefetch = 4;
 
 struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     CUtensorMap tmA[2];
@@ -113,6 +117,11 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     int* status;
     uint64_t wait_limit_ns;  // bound on every mbarrier wait
     int stall_producer;      // test switch: issue no loads, so the consumers' bounded waits run out
+    // CTA pairs: a group's last tile, when it holds at most 128 rows, is an
+    // M = 128 MMA (64 rows per CTA) instead of M = 256.  One SM: a tile of at
+    // most 64 rows is an M = 64 MMA instead of M = 128.
+    int pair_half;
+    int m64;
 };
 
 constexpr int kMaxRing = 6;  // deepest ring of any kernel here (the 2-SM kernel)
@@ -168,6 +177,7 @@ struct Tile {
     int ks, kb0, kb1;  // K slice and its k-block range [kb0, kb1)
     int out_row0;      // first output row (a_row0 except for K-grouped problems)
     int k_off;         // K coordinate of k-block 0 (K-grouped problems: the group's window)
+    int half;          // CTA-pair tail tile of M = 128 (64 rows per CTA) instead of 256
 };
 
 template <int MODE>
@@ -220,6 +230,7 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& 
     t.rows_valid = min(BM, rows - t.m * BM);
     t.out_row0 = t.a_row0;
     t.k_off = 0;
+    t.half = (p.m64 && t.rows_valid <= BM / 2) ? 1 : 0;
     int nk = k_blocks(p, t.prob);
     if (p.kbase[t.prob]) {  // K-grouped: shared A rows, the group's own K window
         t.out_row0 = t.g * p.M[t.prob] + t.m * BM;
@@ -281,9 +292,20 @@ __device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& 
     }
 }
 
+// The thread's accumulator row covers output columns [col_lo, col_lo + ncols)
+// of the tile, at TMEM columns [0, ncols): the whole 256-column tile, or one
+// half of it in a CTA-pair M = 128 tile, whose rows hold the first half of
+// the columns in TMEM lanes 0-63 and the second half in lanes 64-127.
+// ilv (CTA pairs, SwiGLU): the tile's columns are [W1 | W3] per 64 features,
+// i.e. G of features 0-63, U of 0-63, G of 64-127, U of 64-127, so that
+// either column half holds G and U of the same features.
+// warp_row0 >= 0: the warp's rows are warp_row0 .. warp_row0 + warp_rows - 1,
+// held by its lanes 0 .. warp_rows - 1 (an M = 64 tile keeps 16 rows in each
+// 32-lane quarter of TMEM); otherwise the warp holds 32 consecutive rows.
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile,
-                                              float (*stage)[33]) {
+                                              float (*stage)[33], int col_lo = 0, int ncols = BN, bool ilv = false,
+                                              int warp_row0 = -1, int warp_rows = 32) {
     if (p.ksplit > 1) {
         epilogue_partial<MODE>(p, t, tacc, row_in_tile);
         return;
@@ -294,14 +316,25 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
     if (MODE == kGemmSwiGLU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.prob]);
         __nv_bfloat16* out_lo = static_cast<__nv_bfloat16*>(p.out2[t.prob]);
+        const int nchunks = ilv ? ncols / 64 : BN / 2 / 32;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+        for (int ch = 0; ch < nchunks; ++ch) {
+            int gcol, ucol, col;  // TMEM columns of G and U, first output feature
+            if (ilv) {
+                const int b = (ch >> 1) * 128, c0 = (ch & 1) * 32;
+                gcol = b + c0;
+                ucol = b + 64 + c0;
+                col = t.n * (BN / 2) + ((col_lo + b) >> 1) + c0;
+            } else {
+                gcol = ch * 32;
+                ucol = BN / 2 + ch * 32;
+                col = t.n * (BN / 2) + ch * 32;
+            }
             uint32_t g[32], u[32];
             __syncwarp();  // tcgen05.ld is warp-aligned: reconverge after the per-lane stores
-            tmem_ld32(tacc + c0, g);
-            tmem_ld32(tacc + BN / 2 + c0, u);
+            tmem_ld32(tacc + gcol, g);
+            tmem_ld32(tacc + ucol, u);
             tmem_ld_wait();
-            const int col = t.n * (BN / 2) + c0;
             if (!valid || col >= N) continue;
             if (p.wscale1[t.prob]) {  // FP8 weights: per-channel scales of W1 and W3
                 const size_t wr = static_cast<size_t>(t.g) * N + col;
@@ -456,8 +489,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
         if ((MODE == kGemmScale || MODE == kGemmScaleSplit) && valid && p.row_scale[t.prob] != nullptr)
             scale = __ldg(p.row_scale[t.prob] + grow);
         const int lane = threadIdx.x & 31;
-        const int wrow0 = row_in_tile - lane;  // first tile row of this warp
-        const int nvalid = min(32, t.rows_valid - wrow0);  // rows of this warp that exist
+        const int wrow0 = warp_row0 >= 0 ? warp_row0 : row_in_tile - lane;  // first tile row of this warp
+        const int nvalid = min(warp_rows, t.rows_valid - wrow0);  // rows of this warp that exist
         // a K-grouped tile with an empty window computed nothing: its output is 0
         const bool computed = t.kb1 > t.kb0;
         // the next 32 accumulator columns are read from TMEM while this chunk's
@@ -468,8 +501,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
         tmem_ld32(tacc, v);
         tmem_ld_wait();
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            const int col = t.n * BN + c0;
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+            const int col = t.n * BN + col_lo + c0;
             const bool live = col < N && nvalid > 0;  // uniform across the warp
             if (live) {
                 if (p.wscale1[t.prob])
@@ -478,7 +511,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
                 for (int i = 0; i < 32; ++i) stage[lane][i] = computed ? scale * __uint_as_float(v[i]) : 0.0f;
             }
             __syncwarp();
-            const bool more = c0 + 32 < BN;
+            const bool more = c0 + 32 < ncols;
             uint32_t vn[32];
             if (more) tmem_ld32(tacc + c0 + 32, vn);
             if (live) {
@@ -612,8 +645,21 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
         bool used[NST];
         for (int i = 0; i < NST; ++i) used[i] = false;
         bool dead = p.stall_producer != 0;
+        // L2 prefetch of plain K-major tiles: A (unless gathered), the split A
+        // half, and B (W1 and W3 for SwiGLU)
+        const bool l2pf = kL2Prefetch > 0 && !p.b_mn;
+        auto prefetch_kblock = [&](const Tile& q, int kb) {
+            const int kc = q.k_off + kb * BK;
+            const int br = (p.kbase[q.prob] ? 0 : q.g * p.N[q.prob]) + q.n * out_cols_per_tile<MODE>();
+            if (!p.a_gather[q.prob]) tma_prefetch_2d(&p.tmA[q.prob], kc, q.a_row0);
+            if (SC::kSplit) tma_prefetch_2d(&p.tmA2[q.prob], kc, q.a_row0);
+            tma_prefetch_2d(&p.tmB1[q.prob], kc, br);
+            if (MODE == kGemmSwiGLU) tma_prefetch_2d(&p.tmB2[q.prob], kc, br);
+        };
         for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
             const Tile t = decode_tile<MODE>(st, p, id);
+            const bool has_next = l2pf && id + (int)gridDim.x < total_tiles;
+            const Tile nt = has_next ? decode_tile<MODE>(st, p, id + gridDim.x) : t;
             const int b_row0 = (p.kbase[t.prob] ? 0 : t.g * p.N[t.prob]) + t.n * out_cols_per_tile<MODE>();
             const int32_t* gidx = p.a_gather[t.prob];
             int rows4[4] = {0, 0, 0, 0};
@@ -661,6 +707,11 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                             tma_load_2d(sb, &p.tmB1[t.prob], kc, b_row0, &st.full[s]);
                         }
                     }
+                    if (l2pf) {
+                        const int pk = kb + kL2Prefetch;
+                        if (pk < t.kb1) prefetch_kblock(t, pk);
+                        else if (has_next && pk - t.kb1 + nt.kb0 < nt.kb1) prefetch_kblock(nt, pk - t.kb1 + nt.kb0);
+                    }
                 }
                 if (gidx && lane * 4 < t.rows_valid)
                     tma_gather4(sa + lane * 4 * (BK * 2), &p.tmA[t.prob], kb * BK, rows4[0], rows4[1], rows4[2],
@@ -684,13 +735,15 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const bool bmn = !W8 && MODE != kGemmSwiGLU && !SC::kSplit && p.b_mn;
-            const uint32_t idesc = idesc_bf16_f32(BM, BN) | (bmn ? kIdescBMnMajor : 0u);
+            const uint32_t idesc_full = idesc_bf16_f32(BM, BN) | (bmn ? kIdescBMnMajor : 0u);
+            const uint32_t idesc_m64 = idesc_bf16_f32(BM / 2, BN) | (bmn ? kIdescBMnMajor : 0u);
             int s = 0, w = 0;
             uint32_t ph = 0, pw = 0;
             int it = 0;
             bool dead = false;
             for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x, ++it) {
                 const Tile t = decode_tile<MODE>(st, p, id);
+                const uint32_t idesc = t.half ? idesc_m64 : idesc_full;
                 const int acc = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
                 if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
@@ -746,7 +799,11 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
             if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status, p.wait_limit_ns)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_tile<MODE>(p, t, tacc, row_in_tile, st.stage[quarter]);
+            if (MODE != kGemmSwigluBwd && t.half)  // M = 64: rows 16q .. 16q + 15 in lanes 0-15 of quarter q
+                epilogue_tile<MODE>(p, t, tacc, lane < 16 ? quarter * 16 + lane : BM, st.stage[quarter], 0, BN, false,
+                                    quarter * 16, 16);
+            else
+                epilogue_tile<MODE>(p, t, tacc, row_in_tile, st.stage[quarter]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.tmem_empty[acc]);
@@ -897,9 +954,12 @@ __device__ __forceinline__ Tile decode_tile_pair(const SmemTail& st, const TcPar
     t.ks = 0;
     t.n = r / mt;
     t.m = r - t.n * mt;
-    const int first = t.m * 2 * BM + rank * BM;  // this CTA's first row inside the group
+    // a last tile of at most 128 rows is an M = 128 MMA: 64 rows per CTA
+    t.half = (p.pair_half && rows - t.m * 2 * BM <= BM) ? 1 : 0;
+    const int per = t.half ? BM / 2 : BM;
+    const int first = t.m * 2 * BM + rank * per;  // this CTA's first row inside the group
     t.a_row0 = st.row0[gb + lo] + first;
-    t.rows_valid = min(BM, rows - first);  // may be <= 0 for the upper half of a tail tile
+    t.rows_valid = min(per, rows - first);  // may be <= 0 for the upper CTA of a tail tile
     t.out_row0 = t.a_row0;
     t.k_off = 0;
     t.kb0 = 0;
@@ -1004,15 +1064,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             bool dead = p.stall_producer != 0;
             for (int id = cluster_id; id < total_tiles && !dead; id += nclusters) {
                 const Tile t = decode_tile_pair<MODE>(st, p, id, rank);
-                int b_row;  // this CTA's half of the B tile
-                const CUtensorMap* tmb;
-                if (MODE == kGemmSwiGLU) {  // rank 0: the W1 (gate) rows, rank 1: the W3 (up) rows
-                    b_row = t.g * p.N[t.prob] + t.n * (BN / 2);
-                    tmb = rank == 0 ? &p.tmB1[t.prob] : &p.tmB2[t.prob];
-                } else {  // K-grouped problems share one B matrix
+                // this CTA's half of the B tile.  SwiGLU: 64 W1 (gate) rows and
+                // the same 64 features' W3 (up) rows, so the tile's columns run
+                // [G 0-63 | U 0-63 | G 64-127 | U 64-127] over its 128 features
+                int b_row;
+                const CUtensorMap* tmb = &p.tmB1[t.prob];
+                if (MODE == kGemmSwiGLU)
+                    b_row = t.g * p.N[t.prob] + t.n * (BN / 2) + rank * (BN / 4);
+                else  // K-grouped problems share one B matrix
                     b_row = (p.kbase[t.prob] ? 0 : t.g * p.N[t.prob]) + t.n * BN + rank * (BN / 2);
-                    tmb = &p.tmB1[t.prob];
-                }
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(&st.empty[s], ph ^ 1u, abort_flag, p.status, p.wait_limit_ns)) {
                         dead = true;
@@ -1033,7 +1093,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                             });
                     } else {
                         tma_load_2d_pair(sa, &p.tmA[t.prob], t.k_off + kb * BK, t.a_row0, full_leader);
-                        tma_load_2d_pair(sb, tmb, t.k_off + kb * BK, b_row, full_leader);
+                        if (MODE == kGemmSwiGLU) {  // two 64-row boxes
+                            tma_load_2d_pair(sb, &p.tmB1[t.prob], t.k_off + kb * BK, b_row, full_leader);
+                            tma_load_2d_pair(sb + B_BYTES / 4, &p.tmB2[t.prob], t.k_off + kb * BK, b_row, full_leader);
+                        } else {
+                            tma_load_2d_pair(sb, tmb, t.k_off + kb * BK, b_row, full_leader);
+                        }
                     }
                     issued_parity[s] = ph;
                     used[s] = true;
@@ -1055,13 +1120,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             const bool bmn = MODE != kGemmSwiGLU && p.b_mn;
-            const uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | (bmn ? kIdescBMnMajor : 0u);
+            const uint32_t idesc_full = idesc_bf16_f32(2 * BM, BN) | (bmn ? kIdescBMnMajor : 0u);
+            const uint32_t idesc_half = idesc_bf16_f32(BM, BN) | (bmn ? kIdescBMnMajor : 0u);
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
             bool dead = false;
             for (int id = cluster_id; id < total_tiles && !dead; id += nclusters, ++it) {
                 const Tile t = decode_tile_pair<MODE>(st, p, id, 0);
+                const uint32_t idesc = t.half ? idesc_half : idesc_full;
                 const int acc = it & 1;
                 const uint32_t use = static_cast<uint32_t>(it >> 1);
                 if (!mbar_wait(&st.tmem_empty[acc], (use & 1u) ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
@@ -1103,7 +1170,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t tacc =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_tile<MODE>(p, t, tacc, row_in_tile, st.stage[quarter]);
+            // M = 128 tile: lanes 0-63 hold this CTA's 64 rows x the first 128
+            // columns, lanes 64-127 the same rows x the other 128
+            const int row = t.half ? (quarter & 1) * 32 + lane : row_in_tile;
+            const int col_lo = t.half ? (quarter >> 1) * (BN / 2) : 0;
+            epilogue_tile<MODE>(p, t, tacc, row, st.stage[quarter], col_lo, t.half ? BN / 2 : BN, MODE == kGemmSwiGLU);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(leader_addr(&st.tmem_empty[acc]));
@@ -1190,7 +1261,8 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     prm.ksplit = ksplit;
     // rows of B per TMA box: half the tile for SwiGLU (the W1 / W3 halves) and,
     // in either mode, on a CTA pair (each CTA holds half of the N columns)
-    const int b_box = (mode == kGemmSwiGLU || pair) ? BN / 2 : BN;
+    // (SwiGLU on CTA pairs: two 64-row boxes per CTA, W1 and W3 of the same features)
+    const int b_box = (mode == kGemmSwiGLU && pair) ? BN / 4 : (mode == kGemmSwiGLU || pair) ? BN / 2 : BN;
     if (probs[0].G + (nprob > 1 ? probs[1].G : 0) > MAX_GROUPS + 1) return cudaErrorInvalidValue;
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
@@ -1272,6 +1344,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     prm.nprob = nprob;
     prm.status = status;
     prm.wait_limit_ns = kWaitLimitNs;
+    prm.m64 = (pair || mode == kGemmSwigluBwd) ? 0 : 1;  // (the SwiGLU backward keeps 128-row tiles)
     // failure-path test switch: the producer issues no loads, so every CTA
     // with work gives up after a short bounded wait and reports MOE_ERR_TIMEOUT
     if (test_stall_gemm()) {
@@ -1282,6 +1355,8 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     if (pair) {
         // 2-SM tiles: plain A tiles only (no split-K, no gathered or split A)
         if (ksplit != 1 || prm.a_gather[0] || prm.a_gather[1]) return cudaErrorInvalidValue;
+        // M = 128 tail tiles in every mode whose epilogue takes a column half
+        prm.pair_half = mode != kGemmSwigluBwd ? 1 : 0;
         switch (mode) {
             case kGemmSwiGLU: return launch_pair_mode<kGemmSwiGLU>(prm, grid, s);
             case kGemmScale: return launch_pair_mode<kGemmScale>(prm, grid, s);
@@ -1342,6 +1417,7 @@ cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int
     }
     prm.nprob = nprob;
     prm.status = status;
+    prm.m64 = 1;
     prm.wait_limit_ns = kWaitLimitNs;
     if (test_stall_gemm()) {
         prm.stall_producer = 1;

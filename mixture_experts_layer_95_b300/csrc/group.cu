@@ -26,6 +26,10 @@ namespace {
 
 constexpr int kScanThreads = 256;
 constexpr int kScanWarps = kScanThreads / 32;
+// up to this many experts the global counts are summed one warp per expert
+// (each lane's histogram rows in flight at once); the load statistics keep
+// the order moe_load_stats uses (warp columns only up to kWarpColumnMaxE)
+constexpr int kScanWarpCountMaxE = 64;
 
 __global__ void __launch_bounds__(kRouterThreads) group_hist_kernel(int Tn, int E, int k, int chunk,
                                                                      const int32_t* __restrict__ ids,
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
     // 1. global counts, this block's prefix, capacity cut: one warp per expert
     // (all its histogram rows in flight at once) for small E, else one thread
     // per expert
-    if (E <= kWarpColumnMaxE) {
+    if (E <= kScanWarpCountMaxE) {
         for (int e = warp; e < E; e += kScanWarps) {
             int tot = 0, before = 0;
 #pragma unroll 4
@@ -324,7 +328,8 @@ cudaError_t launch_group_scan(int T, int E, int k, int chunk, int capacity, cons
     ScanArgs a{T, E, k, chunk, capacity, nblk, topk_ids, gates, block_hist, o, status};
     const size_t smem = sizeof(int) * ((size_t)3 * E + 1 + (size_t)kScanWarps * E + kScanWarps + 1) +
                         sizeof(float) * kScanThreads;
-    cudaFuncSetAttribute(group_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (smem > 48 * 1024)  // (at most 46 KB for the largest E the library takes)
+        cudaFuncSetAttribute(group_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     launch_pdl(group_scan_kernel, dim3(nblk), dim3(kScanThreads), smem, s, a);
     return cudaGetLastError();
 }
@@ -333,9 +338,16 @@ cudaError_t launch_gather_rows(int dtype, int T, int d, int rows_max, const int3
                                const int32_t* sorted_token_ids, const void* x, void* x_perm, int* status,
                                cudaStream_t s) {
     if (rows_max == 0) return cudaSuccess;
+    // SM count of the current device, remembered per device ordinal
+    static int sms_of[64] = {0};
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < 64 && sms_of[dev] > 0) {
+        sms = sms_of[dev];
+    } else if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && dev >= 0 &&
+               dev < 64) {
+        sms_of[dev] = sms;
+    }
     const int want = (rows_max + 7) / 8;  // 8 warps per block, one row per warp
     const int grid = want < sms * 8 ? want : sms * 8;
     if (dtype == MOE_BF16)

@@ -243,6 +243,149 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
     pdl_trigger();  // after this block's last global write
 }
 
+// Grouping of a decode-sized batch inside the router launch (T <= 256,
+// E <= 32): the last router block to finish -- every block counts itself in
+// on a workspace counter after its writes, so the one that sees the count
+// reach the grid size knows every token is routed -- groups all T k entries
+// ("Mixture of experts (MoE)" handbook, Implementation: stable sort by
+// expert, counts, running starts; capacity as in the notes and "MoE
+// Architecture" s2) and writes the load statistics, which saves the separate
+// grouping launch and its dependency wait.  A token picks each expert at most
+// once, so an entry's rank inside its expert is the number of earlier tokens
+// that picked that expert: a prefix sum down one column of the per-token id
+// histogram.  Results equal group_scan_kernel's bit for bit (integers; the
+// statistics add in the same order).
+struct SmallGroup {
+    GroupOut o;
+    int capacity;
+    unsigned int* counter;  // zero before the launch; wraps back to zero after it
+    int* status;
+};
+
+constexpr int kSmallGroupMaxT = kSplitDRouterMaxT;
+constexpr int kSmallGroupMaxE = 32;
+
+// Same order of additions as warp_column_sum, through L2 (the rows were
+// written by other blocks of this launch).
+__device__ __forceinline__ float warp_column_sum_cg(const float* m, int nrows, int ld, int col) {
+    const int lane = threadIdx.x & 31;
+    float s = 0.f;
+#pragma unroll 4
+    for (int b = lane; b < nrows; b += 32) s += __ldcg(m + (size_t)b * ld + col);
+    float tot = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) tot += __shfl_sync(0xffffffffu, s, j);
+    return tot;
+}
+
+// Runs in one block of kSplitDThreads threads.  ids, gates [T][k], hist and
+// p_part [T][E] hold every token's row.
+__device__ void group_small_batch(const SmallGroup& g, int Tn, int E, int k, const int32_t* ids, const float* gates,
+                                  const int32_t* hist, const float* p_part) {
+    __shared__ int s_rank[kSmallGroupMaxT][kSmallGroupMaxE];  // earlier tokens that picked each expert
+    __shared__ int s_cnt[kSmallGroupMaxE], s_off[kSmallGroupMaxE + 1];
+    __shared__ float s_fp[kSmallGroupMaxE];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kW = kSplitDThreads / 32;
+    const int n = Tn * k;
+    // 1. per expert: exclusive prefix of its histogram column over tokens
+    //    (lane l owns tokens [8 l, 8 l + 8))
+    for (int e = warp; e < E; e += kW) {
+        int v[8], loc = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = lane * 8 + i;
+            v[i] = t < Tn ? __ldcg(hist + (size_t)t * E + e) : 0;
+            loc += v[i];
+        }
+        int incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - loc;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = lane * 8 + i;
+            if (t < Tn) s_rank[t][e] = run;
+            run += v[i];
+        }
+        if (lane == 31) s_cnt[e] = incl;
+    }
+    __syncthreads();
+    // 2. capacity cut and expert offsets (warp 0, one lane per expert)
+    if (warp == 0) {
+        const int cnt = lane < E ? s_cnt[lane] : 0;
+        const int kept = (g.capacity >= 0 && cnt > g.capacity) ? g.capacity : cnt;
+        int incl = kept;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane < E) {
+            s_off[lane] = incl - kept;
+            g.o.counts[lane] = cnt;
+            g.o.kept[lane] = kept;
+            g.o.offsets[lane] = incl - kept;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (lane == 0) {
+            s_off[E] = total;
+            g.o.offsets[E] = total;
+            *g.o.n_dropped = n - total;
+        }
+    }
+    // 3. load statistics: f = counts / (T k), p = mean softmax row, L = alpha E sum f p
+    //    (the additions of group_scan_kernel and moe_load_stats, in their order)
+    if (g.o.p_part) {
+        for (int e = warp; e < E; e += kW) {
+            const float ps = warp_column_sum_cg(p_part, Tn, E, e);
+            if (lane == 0) {
+                const float pm = ps / (float)Tn;
+                const float f = (float)s_cnt[e] / ((float)Tn * (float)k);
+                if (g.o.p_mean) g.o.p_mean[e] = pm;
+                if (g.o.f) g.o.f[e] = f;
+                s_fp[e] = f * pm;
+            }
+        }
+    }
+    __syncthreads();
+    if (g.o.p_part && g.o.L && threadIdx.x == 0) {
+        float acc = 0.f;
+        for (int e = 0; e < E; ++e) acc += s_fp[e];
+        *g.o.L = g.o.alpha * (float)E * acc;
+    }
+    // 4. positions: entries in flat order; positions past the kept total get
+    //    sorted_token_ids = -1, gates_perm = 0
+    const int total = s_off[E];
+    for (int pos = total + threadIdx.x; pos < n; pos += blockDim.x) {
+        g.o.sorted_token_ids[pos] = -1;
+        g.o.gates_perm[pos] = 0.f;
+    }
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int t = i / k;
+        const int e = __ldcg(ids + i);
+        int pos = -1;
+        if (e < 0 || e >= E) {
+            record_status(g.status, kStatusBounds);
+        } else {
+            const int rank = s_rank[t][e];
+            if (g.capacity < 0 || rank < g.capacity) pos = s_off[e] + rank;
+            if (pos >= s_off[e + 1]) {  // ids that disagree with the histogram rows
+                record_status(g.status, kStatusBounds);
+                pos = -1;
+            }
+        }
+        g.o.slot_pos[i] = pos;
+        if (pos >= 0) {
+            g.o.sorted_token_ids[pos] = t;
+            g.o.gates_perm[pos] = __ldcg(gates + i);
+        }
+    }
+}
+
 // Router for decode-sized batches: one block per token, the d dimension split
 // over the block's threads (each thread owns 16-byte vectors v = tid,
 // tid + 256, ...), W_g read straight from L2/L1.  The E partial dots are
@@ -253,11 +396,12 @@ __global__ void __launch_bounds__(kSplitDThreads) router_split_d_kernel(
     int Tn, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ wg,
     const float* __restrict__ logit_bias, const float* __restrict__ select_bias, int renormalize,
     int32_t* __restrict__ topk_ids, float* __restrict__ gates, float* __restrict__ p_part,
-    int32_t* __restrict__ block_hist, float* __restrict__ probs) {
+    int32_t* __restrict__ block_hist, float* __restrict__ probs, const SmallGroup group) {
     pdl_wait();
     constexpr int VE = Vec<T>::kElems;
     constexpr int kW = kSplitDThreads / 32;
     __shared__ float s_red[kW][NE];
+    __shared__ int s_last;
     const int t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nv = d / VE;
@@ -285,20 +429,30 @@ __global__ void __launch_bounds__(kSplitDThreads) router_split_d_kernel(
         if (lane == 0) s_red[warp][e] = v;
     }
     __syncthreads();
-    if (warp != 0) return;
-    float l[1] = {-FLT_MAX};
-    if (lane < E) {
-        float v = 0.f;
-        for (int q = 0; q < kW; ++q) v += s_red[q][lane];  // fixed order
-        l[0] = v + (logit_bias ? __ldg(logit_bias + lane) : 0.f);
+    if (warp == 0) {
+        float l[1] = {-FLT_MAX};
+        if (lane < E) {
+            float v = 0.f;
+            for (int q = 0; q < kW; ++q) v += s_red[q][lane];  // fixed order
+            l[0] = v + (logit_bias ? __ldg(logit_bias + lane) : 0.f);
+        }
+        float psum[1] = {0.f};
+        int hcnt[1] = {0};
+        softmax_topk<1>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
+        if (lane < E) {
+            if (p_part) p_part[(size_t)t * E + lane] = psum[0];
+            if (block_hist) block_hist[(size_t)t * E + lane] = hcnt[0];
+        }
     }
-    float psum[1] = {0.f};
-    int hcnt[1] = {0};
-    softmax_topk<1>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
-    if (lane < E) {
-        if (p_part) p_part[(size_t)t * E + lane] = psum[0];
-        if (block_hist) block_hist[(size_t)t * E + lane] = hcnt[0];
-    }
+    if (group.counter == nullptr) return;  // routing only
+    // count this block in after its writes; the last one groups the batch
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicInc(group.counter, gridDim.x - 1) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    group_small_batch(group, Tn, E, k, topk_ids, gates, block_hist, p_part);
 }
 
 template <int NJ>
@@ -306,7 +460,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
     int Tn, int E, int k, const float* __restrict__ logits, const float* __restrict__ logit_bias,
     const float* __restrict__ select_bias, int renormalize, int32_t* __restrict__ topk_ids,
     float* __restrict__ gates, float* __restrict__ p_part, int32_t* __restrict__ block_hist,
-    float* __restrict__ probs) {
+    float* __restrict__ probs, int nsplit) {
     pdl_wait();
     extern __shared__ float s_dyn[];
     float* s_p = s_dyn;
@@ -326,7 +480,13 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             const int e = lane + 32 * j;
-            l[j] = (e < E) ? logits[(size_t)t * E + e] + (logit_bias ? __ldg(logit_bias + e) : 0.f) : -FLT_MAX;
+            float v = -FLT_MAX;
+            if (e < E) {  // the logits GEMM's K slices, added in slice order
+                v = logits[(size_t)t * E + e];
+                for (int sl = 1; sl < nsplit; ++sl) v += logits[((size_t)sl * Tn + t) * E + e];
+                v += logit_bias ? __ldg(logit_bias + e) : 0.f;
+            }
+            l[j] = v;
         }
         softmax_topk<NJ>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
     }
@@ -388,13 +548,24 @@ cudaError_t launch_router_warp(int dtype, int T, int d, int E, int k, const void
 cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const void* x, const void* w_gate,
                                   const float* logit_bias, const float* select_bias, int renormalize,
                                   int32_t* topk_ids, float* gates, float* p_part, int32_t* block_hist,
-                                  cudaStream_t s, float* probs) {
+                                  cudaStream_t s, float* probs, const GroupOut* group, int capacity,
+                                  unsigned int* counter, int* status) {
     if (T == 0) return cudaSuccess;
+    SmallGroup sg{};
+    if (group) {
+        // grouping in the last block: every token's ids, gates, p row and histogram row are needed
+        if (!counter || !block_hist || !p_part || !topk_ids || !gates || T > kSmallGroupMaxT || E > kSmallGroupMaxE)
+            return cudaErrorInvalidValue;
+        sg.o = *group;
+        sg.capacity = capacity;
+        sg.counter = counter;
+        sg.status = status;
+    }
 #define MOE_SPLITD_CASE(TY, NE)                                                                              \
     launch_pdl(router_split_d_kernel<TY, NE>, dim3(T), dim3(kSplitDThreads), 0, s, T, d, E, k, static_cast<const TY*>(x),       \
                                                                static_cast<const TY*>(w_gate), logit_bias,  \
                                                                select_bias, renormalize, topk_ids, gates,  \
-                                                               p_part, block_hist, probs)
+                                                               p_part, block_hist, probs, sg)
     if (dtype == MOE_BF16) {
         if (E <= 8) MOE_SPLITD_CASE(__nv_bfloat16, 8);
         else if (E <= 16) MOE_SPLITD_CASE(__nv_bfloat16, 16);
@@ -411,7 +582,8 @@ cudaError_t launch_router_split_d(int dtype, int T, int d, int E, int k, const v
 cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, const float* logit_bias,
                                       const float* select_bias, int renormalize, int32_t* topk_ids,
                                       float* gates, float* p_part, int32_t* block_hist, cudaStream_t s,
-                                      float* probs) {
+                                      float* probs, int nsplit) {
+    if (nsplit < 1) return cudaErrorInvalidValue;
     const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
     if (nblk == 0) return cudaSuccess;
     const size_t smem = (size_t)kWarps * E * (sizeof(float) + sizeof(int));
@@ -420,7 +592,8 @@ cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, 
     do {                                                                                                     \
         cudaFuncSetAttribute(router_logits_kernel<NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
         launch_pdl(router_logits_kernel<NJ>, dim3(grid), dim3(block), smem, s, T, E, k, logits, logit_bias, select_bias,       \
-                                                           renormalize, topk_ids, gates, p_part, block_hist, probs); \
+                                                           renormalize, topk_ids, gates, p_part, block_hist, probs, \
+                                                           nsplit);                                          \
     } while (0)
     if (E <= 64) MOE_LOGITS_CASE(2);
     else if (E <= 256) MOE_LOGITS_CASE(8);

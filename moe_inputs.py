@@ -83,6 +83,10 @@ WORKLOADS = {
                                         weights="fp8"),
     "deepseek_v3": Workload("deepseek_v3", T=8192, d=7168, E=256, F=2048, k=8, n_shared=1, F_s=2048,
                             select_bias=True),
+    # the DeepSeek-V3 expert shape and rows per expert (~256) at an eighth of
+    # the weights (32 experts, 1024 tokens): the case profiled with ncu --set full
+    "deepseek_v3_e32": Workload("deepseek_v3_e32", T=1024, d=7168, E=32, F=2048, k=8, n_shared=1, F_s=2048,
+                                select_bias=True),
     # the capacity cut leaves most tokens with small outputs and a few with
     # outputs ~12x RMS(y); a bf16 H then costs ~2% of RMS(y) at those tokens,
     # so this layer keeps H as a hi + lo pair

@@ -40,6 +40,9 @@ CASES = [
     Workload("bwd_one_token_shared", T=1, d=256, E=8, F=256, k=2, n_shared=1, F_s=128),
     # >= 512 rows per expert: the row-indexed products run on CTA pairs (ragged N and K)
     Workload("bwd_pair_shared", T=1100, d=272, E=4, F=400, k=2, n_shared=1, F_s=208),
+    # ~300 rows per expert: CTA pairs with M = 128 tail tiles (the SwiGLU
+    # backward's D product keeps 256-row tiles)
+    Workload("bwd_pair_half_shared", T=600, d=272, E=4, F=400, k=2, n_shared=1, F_s=208, select_bias=True),
 ]
 
 
@@ -130,7 +133,7 @@ def test_backward_rejects_fp32_and_expert_choice(cuda):
         assert moe.lib().moe_backward_workspace_size(__import__("ctypes").byref(layer.cfg())) == 0
 
 
-SAVED_CASES = [CASES[0], CASES[1], CASES[4], CASES[5]]
+SAVED_CASES = [CASES[0], CASES[1], CASES[4], CASES[5], CASES[6]]
 
 
 @pytest.mark.parametrize("w", SAVED_CASES, ids=[w.name for w in SAVED_CASES])

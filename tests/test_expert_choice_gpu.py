@@ -36,6 +36,9 @@ SMALL_EC = [
     # tokens, so the layer keeps H as a hi + lo pair (as the skewed token-choice layer does)
     Workload("ec_zipf_empty_tokens_bf16", T=400, d=256, E=16, F=128, k=1, zipf_s=1.2, h_split=True,
              routing="expert"),
+    # decode-sized buckets (C = 2 of 16 tokens): the down GEMM runs the combine, and
+    # counts the tokens no expert took, in its last CTA per column block
+    Workload("ec_decode_empty_tokens_bf16", T=16, d=256, E=8, F=256, k=1, zipf_s=1.2, routing="expert"),
 ]
 
 

@@ -46,10 +46,14 @@ SMALL = [
     # >= 512 rows per expert: both GEMMs run on CTA pairs (256-row tiles whose
     # upper half may be empty at a segment end; N tail of 64 in the down GEMM)
     Workload("pair_tiles_shared_bf16", T=1100, d=320, E=4, F=384, k=2, n_shared=1, F_s=256),
-    # a few hundred rows per expert (DeepSeek-V3-like segments): 128-row tiles with
-    # ragged segment ends, ragged N and K, shared expert in the same launches
+    # a few hundred rows per expert (DeepSeek-V3-like segments): CTA pairs whose
+    # last tile of a segment is an M = 128 tile (64 rows per SM, the upper SM's
+    # rows partly or wholly absent) when at most 128 rows remain; ragged N and
+    # K; shared expert (600 rows: 256 + 256 + 88) in the same launches
     Workload("wide_chunks_shared_ragged_bf16", T=600, d=272, E=4, F=400, k=2, n_shared=1, F_s=208, select_bias=True),
     Workload("wide_chunks_e16_bf16", T=2000, d=256, E=16, F=256, k=2),
+    # 128-191 rows per expert: the 1-SM kernel's 128-row tiles
+    Workload("one_sm_160rows_bf16", T=640, d=256, E=8, F=264, k=2),
 ]
 
 
