@@ -5,8 +5,7 @@
 
 A step is one full layer call (router, top-k, grouping, both grouped expert
 GEMMs, combine, load statistics) over one batch of synthetic tokens whose
-inputs are resident in HBM, replayed from the layer's CUDA graph (the public
-API's graph mode, which spares the host the per-call launch work).  N > 1 runs under torchrun as N independent
+inputs are resident in HBM.  N > 1 runs under torchrun as N independent
 replicas (one per GPU, weak scaling): the layer's token batch has no exchange
 step on one GPU, so the only collectives are the harness's barrier and the
 max-over-ranks of the timed region.
@@ -343,7 +342,7 @@ class Bench:
             self.q8 = moe.quantize_experts_fp8(self.layer, *(self.L[n] for n in names))
         L = self.L
         self.fw = moe.Forward(self.layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"],
-                              L["ws1"], L["ws3"], L["ws2"], stats=True, device=dev, fp8=self.q8, graph=True)
+                              L["ws1"], L["ws3"], L["ws2"], stats=True, device=dev, fp8=self.q8)
         self.x = L["x"]
         self.y = torch.empty_like(self.x)
         self.stream = torch.cuda.current_stream(dev)
@@ -359,63 +358,54 @@ class Bench:
         if st != 0:
             raise moe.MoeError(st, "warm-up device status")
 
-    def launches_per_call(self):
-        """Kernels one layer call launches (counted by the library on an eager call)."""
-        import torch
-
-        import mixture_experts_layer_95_b300 as moe
-        n0 = moe.launch_count()
-        self.fw._enqueue(self.x, self.y, None)
-        torch.cuda.synchronize(self.dev)
-        return moe.launch_count() - n0
-
     def timed(self, steps, barrier):
         """`steps` back-to-back layer calls timed with events on the launching
-        stream, each a replay of the layer's CUDA graph (the public API's
-        graph mode); the up GEMM is bracketed by events in every
-        EVENT_EVERY-th call (a graph of its own per such call, recording that
-        call's event pair).  Returns (total ms, up-GEMM ms per launch, kernels
-        launched, (wall0, wall1))."""
+        stream; the up GEMM is bracketed in every EVENT_EVERY-th call.
+        Returns (total ms, up-GEMM ms per launch, launches, (wall0, wall1))."""
         import torch
 
         import mixture_experts_layer_95_b300 as moe
-        n_ev = (steps + EVENT_EVERY - 1) // EVENT_EVERY
-        # an event between two kernels removes their programmatic overlap, so
-        # the other calls' launches keep it
-        with moe.StageTimer(n_ev, stages=("up_gemm",)) as timer:
-            ev_graphs = [self.fw.capture(self.x, self.y, stage_timer=timer) for _ in range(n_ev)]
-        plain = self.fw.capture(self.x, self.y)
-        per_call = self.launches_per_call()
-        for _ in range(2):  # the graphs' first replays
-            plain.replay()
         barrier()
+        launches0 = moe.launch_count()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         wall0 = time.time()
-        start.record(self.stream)
-        for i in range(steps):
-            (ev_graphs[i // EVENT_EVERY] if i % EVENT_EVERY == 0 else plain).replay()
-        end.record(self.stream)
+        # an event between two kernels removes their programmatic overlap, so
+        # the other calls' launches keep it
+        with moe.StageTimer(steps // EVENT_EVERY + 1, stages=("up_gemm",)) as timer:
+            start.record(self.stream)
+            for i in range(steps):
+                if i % EVENT_EVERY == 0:
+                    timer.begin_call()
+                else:
+                    timer.skip_call()
+                self.fw(self.x, self.y)
+            end.record(self.stream)
         end.synchronize()
         wall1 = time.time()
         barrier()
+        launches = moe.launch_count() - launches0
         up_ms, up_n = timer.ms()
         timer.close()
-        del ev_graphs, plain
         st = self.fw.device_status()
         if st != 0:
             raise moe.MoeError(st, "timed-region device status")
-        return start.elapsed_time(end), up_ms["up_gemm"] / up_n["up_gemm"], per_call * steps, (wall0, wall1)
+        return start.elapsed_time(end), up_ms["up_gemm"] / up_n["up_gemm"], launches, (wall0, wall1)
 
-    def timed_eager(self, steps):
-        """The same loop enqueued call by call (no graph): ms per step."""
+    def timed_graph(self, steps):
+        """The same loop as replays of the layer's CUDA graph (Forward's graph
+        mode): ms per step, for comparison."""
         import torch
+        g = self.fw.capture(self.x, self.y)
+        for _ in range(2):
+            g.replay()
         torch.cuda.synchronize(self.dev)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(self.stream)
         for _ in range(steps):
-            self.fw._enqueue(self.x, self.y, None)
+            g.replay()
         end.record(self.stream)
         end.synchronize()
+        del g
         return start.elapsed_time(end) / steps
 
     def stages(self, steps):
@@ -546,7 +536,7 @@ def run_ours(args):
     value = job_throughput(w.T, world, args.steps, ms)
     roof, layer = b.accounting(ms_per_step, up_ms, peaks, peak_src)
     layer["stage_ms"] = b.stages(args.steps)
-    layer["eager_ms_per_step"] = round(b.timed_eager(args.steps), 4)  # call by call, for comparison
+    layer["graph_ms_per_step"] = round(b.timed_graph(args.steps), 4)  # CUDA-graph replays, for comparison
     head_clocks = clocks.summary()
 
     # end to end through the public API: every step copies its batch in from
@@ -581,8 +571,8 @@ def run_ours(args):
         "layer": layer,
         "e2e": e2e,
         "gpu_launches": int(launches),
-        "launch": "every timed call replays the layer's CUDA graph (Forward(graph=True)); "
-                  "layer.eager_ms_per_step is the same loop enqueued call by call",
+        "launch": "every timed call enqueues the layer through Forward (programmatic dependent launch "
+                  "chains consecutive calls); layer.graph_ms_per_step is the same loop as CUDA-graph replays",
         "clocks": head_clocks,
     }
 
@@ -614,7 +604,7 @@ def run_ours(args):
                 "kept_entries": s_layer["kept_entries"], "experts_touched": s_layer["experts_touched"],
                 "gpu_launches_per_step": round(s_launch / steps, 2),
                 "sm_mhz": c["sm_mhz"], "reasons": c["reasons"], "stage_ms": sb.stages(min(steps, 50)),
-                "eager_ms_per_step": round(sb.timed_eager(steps), 4)}
+                "graph_ms_per_step": round(sb.timed_graph(steps), 4)}
             sb.close()
     if world == 1 and not args.no_workloads:
         # sustained (last, after the other workloads): the headline layer back

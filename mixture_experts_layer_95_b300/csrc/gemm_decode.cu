@@ -95,10 +95,6 @@ struct DecTail {
 };
 
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
-// The producer asks L2 for the weight tile of the stage this many stages past
-// the one it loads (into the CTA's next work item at an item's end), so that
-// a freed stage refills from L2 instead of waiting on HBM.
-constexpr int kDecL2Prefetch = 4;
 
 // A stage: the 256-row weight tile (128-byte rows), then the token tile(s):
 // NT rows of 64 bf16, or NT rows of 128 hi codes and NT rows of 128 lo codes.
@@ -459,15 +455,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
         DTile t;
         while (!dead && dec_work_next<MODE, NT, KPS>(st, p, work, t)) {
             const int w_row0 = t.g * p.N[t.prob] + t.n * dec_cols<MODE>();
-            // the next work item (the same sequence, advanced on a copy), for the L2 prefetch
-            DecWork peek = work;
-            DTile nt;
-            const bool has_next = kDecL2Prefetch > 0 && dec_work_next<MODE, NT, KPS>(st, p, peek, nt);
-            auto prefetch_stage = [&](const DTile& q, int kb) {
-                const int row = q.g * p.N[q.prob] + q.n * dec_cols<MODE>();
-                tma_prefetch_2d(&p.tmW1[q.prob], kb * KPS * BK, row);
-                if (MODE == kGemmSwiGLU) tma_prefetch_2d(&p.tmW2[q.prob], kb * KPS * BK, row);
-            };
             const int32_t* gidx = p.x_gather[t.prob];
             int rows4[4] = {0, 0, 0, 0};
             if (gidx) {
@@ -503,11 +490,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) grouped_gemm_decode_kernel(con
                     if (!gidx) {
                         tma_load_2d(sw + WBYTES, &p.tmX[t.prob], kc, t.x_row0, &st.full[s]);
                         if (W8) tma_load_2d(sw + WBYTES + XBYTES, &p.tmXlo[t.prob], kc, t.x_row0, &st.full[s]);
-                    }
-                    if (kDecL2Prefetch > 0) {
-                        const int pk = kb + kDecL2Prefetch;
-                        if (pk < t.kb1) prefetch_stage(t, pk);
-                        else if (has_next && pk - t.kb1 + nt.kb0 < nt.kb1) prefetch_stage(nt, pk - t.kb1 + nt.kb0);
                     }
                 }
                 if (gidx && lane * 4 < t.rows_valid) {

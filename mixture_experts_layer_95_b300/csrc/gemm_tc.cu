@@ -68,10 +68,6 @@ constexpr int W8_RAW_BYTES = A_BYTES + F8_BYTES;
 constexpr int W8_WIDE = 2;          // widened bf16 B tiles feeding the MMA
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int MAX_GROUPS = kMaxExperts;
-// The 1-SM producer asks L2 for the operand tiles of the k-block this many
-// blocks past the one it loads (into the next tile at a tile's end), so that
-// a shared-memory stage, once free, refills from L2 instead of waiting on HBM.
-constexpr int kL2Prefetch = 4;
 
 struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     CUtensorMap tmA[2];
@@ -645,21 +641,8 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
         bool used[NST];
         for (int i = 0; i < NST; ++i) used[i] = false;
         bool dead = p.stall_producer != 0;
-        // L2 prefetch of plain K-major tiles: A (unless gathered), the split A
-        // half, and B (W1 and W3 for SwiGLU)
-        const bool l2pf = kL2Prefetch > 0 && !p.b_mn;
-        auto prefetch_kblock = [&](const Tile& q, int kb) {
-            const int kc = q.k_off + kb * BK;
-            const int br = (p.kbase[q.prob] ? 0 : q.g * p.N[q.prob]) + q.n * out_cols_per_tile<MODE>();
-            if (!p.a_gather[q.prob]) tma_prefetch_2d(&p.tmA[q.prob], kc, q.a_row0);
-            if (SC::kSplit) tma_prefetch_2d(&p.tmA2[q.prob], kc, q.a_row0);
-            tma_prefetch_2d(&p.tmB1[q.prob], kc, br);
-            if (MODE == kGemmSwiGLU) tma_prefetch_2d(&p.tmB2[q.prob], kc, br);
-        };
         for (int id = blockIdx.x; id < total_tiles && !dead; id += gridDim.x) {
             const Tile t = decode_tile<MODE>(st, p, id);
-            const bool has_next = l2pf && id + (int)gridDim.x < total_tiles;
-            const Tile nt = has_next ? decode_tile<MODE>(st, p, id + gridDim.x) : t;
             const int b_row0 = (p.kbase[t.prob] ? 0 : t.g * p.N[t.prob]) + t.n * out_cols_per_tile<MODE>();
             const int32_t* gidx = p.a_gather[t.prob];
             int rows4[4] = {0, 0, 0, 0};
@@ -706,11 +689,6 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                         } else {
                             tma_load_2d(sb, &p.tmB1[t.prob], kc, b_row0, &st.full[s]);
                         }
-                    }
-                    if (l2pf) {
-                        const int pk = kb + kL2Prefetch;
-                        if (pk < t.kb1) prefetch_kblock(t, pk);
-                        else if (has_next && pk - t.kb1 + nt.kb0 < nt.kb1) prefetch_kblock(nt, pk - t.kb1 + nt.kb0);
                     }
                 }
                 if (gidx && lane * 4 < t.rows_valid)

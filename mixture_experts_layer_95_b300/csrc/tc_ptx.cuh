@@ -98,14 +98,6 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, in
         : "memory");
 }
 
-// Hint: bring the box at (c0, c1) of a 2-D tensor map into L2 (no shared
-// memory, no barrier).  Coordinates outside the tensor prefetch nothing.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
