@@ -297,7 +297,7 @@ def layer_of(w):
     import mixture_experts_layer_95_b300 as moe
     return moe.Layer(T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.F, n_shared=w.n_shared, d_ff_shared=w.F_s, dtype=w.dtype,
                      renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha, h_split=w.h_split,
-                     routing=w.routing)
+                     routing=w.routing, yperm_bf16=w.yperm_bf16)
 
 
 def up_kernel_name(plan, fp8):

@@ -124,6 +124,14 @@ typedef struct moe_config {
                             to [1, T]; renormalize and select_bias have no
                             effect (a per-expert constant does not change an
                             expert's ranking of the tokens).                   */
+    int32_t yperm_bf16;  /* bf16 layers: 1 stores each expert row of the down
+                            GEMM (y_perm, after its gate) and the shared
+                            expert's rows (y_shared) in bf16 instead of fp32,
+                            rounded once per row after its K slices are summed,
+                            halving the combine's reads; the combine still adds
+                            them in fp32.  For layers with many experts per
+                            token, whose rows are each a small part of y.
+                            0 for fp32 layers.                                 */
 } moe_config;
 
 /* Optional statistics outputs of moe_forward (device pointers, each nullable). */
@@ -230,24 +238,26 @@ MOE_API int moe_permute_static(const moe_config *cfg, const int32_t *topk_ids, c
  *   x_perm [T*k][d] and offsets [E+1] as produced by moe_permute (expert
  *   choice: [E*C][d] from moe_route_expert_choice); gates_perm fp32
  *   [T*k]; w1, w3 [E][F][d], w2 [E][d][F] (dtype).
- *   y_perm fp32 [T*k][d]: row pos = gates_perm[pos] * W2_e(silu(W1_e x) * W3_e x)
- *   for pos < offsets[E] (rows past the end are left untouched).
+ *   y_perm [T*k][d] (fp32, or bf16 when cfg->yperm_bf16): row pos =
+ *   gates_perm[pos] * W2_e(silu(W1_e x) * W3_e x) for pos < offsets[E] (rows
+ *   past the end are left untouched).
  *   Shared expert (when cfg->n_shared == 1): x [T][d], ws1, ws3 [F_s][d],
- *   ws2 [d][F_s] and y_shared fp32 [T][d] = Shared(x) (gate 1) are required;
- *   when n_shared == 0 those five may be NULL. */
+ *   ws2 [d][F_s] and y_shared [T][d] (as y_perm) = Shared(x) (gate 1) are
+ *   required; when n_shared == 0 those five may be NULL. */
 MOE_API int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets,
                    const float *gates_perm, const void *w1, const void *w3, const void *w2,
-                   const void *x, const void *ws1, const void *ws3, const void *ws2, float *y_perm,
-                   float *y_shared, void *ws, size_t ws_bytes, moe_stream_t stream);
+                   const void *x, const void *ws1, const void *ws3, const void *ws2, void *y_perm,
+                   void *y_shared, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Combine (step 6): y[t] = sum over j = 0..k-1 with slot_pos[t][j] >= 0 of
  * y_perm[slot_pos[t][j]], in that order, plus y_shared[t] when y_shared is
  * non-NULL; accumulated in fp32 and stored in cfg->dtype (round to nearest
- * even for bf16), or in fp32 when cfg->y_fp32.  A token whose entries were
- * all dropped gets only its shared row (or 0).  Under expert choice slot_pos
- * is [T][E] and the sum runs over j = 0..E-1. */
-MOE_API int moe_combine(const moe_config *cfg, const float *y_perm, const int32_t *slot_pos,
-                const float *y_shared, void *y, moe_stream_t stream);
+ * even for bf16), or in fp32 when cfg->y_fp32.  y_perm and y_shared are fp32,
+ * or bf16 when cfg->yperm_bf16 (as moe_expert_ffn writes them).  A token whose
+ * entries were all dropped gets only its shared row (or 0).  Under expert
+ * choice slot_pos is [T][E] and the sum runs over j = 0..E-1. */
+MOE_API int moe_combine(const moe_config *cfg, const void *y_perm, const int32_t *slot_pos,
+                const void *y_shared, void *y, moe_stream_t stream);
 
 /* Load statistics (step 7) from counts [E] (moe_permute) and p_mean [E]
  * (moe_route): f [E] = counts/(T k), L [1] = alpha * E * sum f p_mean.

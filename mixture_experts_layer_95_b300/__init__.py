@@ -44,7 +44,7 @@ class MoeConfig(ctypes.Structure):
                 ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("capacity", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("y_fp32", ctypes.c_int32), ("h_split", ctypes.c_int32),
-                ("routing", ctypes.c_int32)]
+                ("routing", ctypes.c_int32), ("yperm_bf16", ctypes.c_int32)]
 
 
 class MoeFp8Weights(ctypes.Structure):
@@ -246,6 +246,7 @@ class Layer:
     y_fp32: bool = False  # return y in fp32 (before rounding to the layer dtype)
     h_split: bool = False  # bf16: keep H as a hi + lo bf16 pair (heavy-tailed layers)
     routing: str = "token"  # "token": tokens choose top-k experts; "expert": experts choose C tokens
+    yperm_bf16: bool = False  # bf16: keep the expert rows (y_perm, y_shared) in bf16 for the combine
 
     def cfg(self) -> MoeConfig:
         if self.routing not in ("token", "expert"):
@@ -253,7 +254,13 @@ class Layer:
         return MoeConfig(self.T, self.d, self.E, self.k, self.d_ff, self.n_shared, self.d_ff_shared,
                          MOE_BF16 if self.dtype == "bf16" else MOE_F32, int(bool(self.renormalize)),
                          int(self.capacity), float(self.alpha), int(bool(self.y_fp32)), int(bool(self.h_split)),
-                         MOE_ROUTE_EXPERT_CHOICE if self.routing == "expert" else MOE_ROUTE_TOKEN_CHOICE)
+                         MOE_ROUTE_EXPERT_CHOICE if self.routing == "expert" else MOE_ROUTE_TOKEN_CHOICE,
+                         int(bool(self.yperm_bf16)))
+
+    @property
+    def yperm_dtype(self):
+        """Storage of the expert rows y_perm / y_shared of the step API."""
+        return torch.bfloat16 if self.yperm_bf16 else torch.float32
 
     @property
     def bucket(self) -> int:
@@ -418,8 +425,8 @@ def permute_static(layer: Layer, topk_ids, gates, x, stream=None):
 
 def expert_ffn(layer: Layer, x_perm, offsets, gates_perm, w1, w3, w2, x=None, ws1=None, ws3=None, ws2=None,
                ws=None, stream=None):
-    """moe_expert_ffn: returns (y_perm fp32 [rows, d], y_shared fp32 [T, d] or None);
-    rows = T*k (token choice) or E*C (expert choice)."""
+    """moe_expert_ffn: returns (y_perm [rows, d], y_shared [T, d] or None), fp32 or,
+    with layer.yperm_bf16, bf16; rows = T*k (token choice) or E*C (expert choice)."""
     dt, dev = layer.torch_dtype, x_perm.device
     n = layer.perm_rows
     _need(x_perm, (n, layer.d), dt, "x_perm")
@@ -434,9 +441,9 @@ def expert_ffn(layer: Layer, x_perm, offsets, gates_perm, w1, w3, w2, x=None, ws
         _need(ws1, (layer.d_ff_shared, layer.d), dt, "ws1")
         _need(ws3, (layer.d_ff_shared, layer.d), dt, "ws3")
         _need(ws2, (layer.d, layer.d_ff_shared), dt, "ws2")
-        y_shared = torch.empty((layer.T, layer.d), dtype=torch.float32, device=dev)
+        y_shared = torch.empty((layer.T, layer.d), dtype=layer.yperm_dtype, device=dev)
     ws = ws if ws is not None else workspace(layer, dev, stream)
-    y_perm = torch.empty((n, layer.d), dtype=torch.float32, device=dev)
+    y_perm = torch.empty((n, layer.d), dtype=layer.yperm_dtype, device=dev)
     c = layer.cfg()
     _check(lib().moe_expert_ffn(ctypes.byref(c), _ptr(x_perm), _ptr(offsets), _ptr(gates_perm), _ptr(w1), _ptr(w3),
                                 _ptr(w2), _ptr(x), _ptr(ws1), _ptr(ws3), _ptr(ws2), _ptr(y_perm), _ptr(y_shared),
@@ -447,10 +454,10 @@ def expert_ffn(layer: Layer, x_perm, offsets, gates_perm, w1, w3, w2, x=None, ws
 def combine(layer: Layer, y_perm, slot_pos, y_shared=None, stream=None):
     """moe_combine: returns y [T, d] in the layer dtype."""
     dev = y_perm.device
-    _need(y_perm, (layer.perm_rows, layer.d), torch.float32, "y_perm")
+    _need(y_perm, (layer.perm_rows, layer.d), layer.yperm_dtype, "y_perm")
     _need(slot_pos, (layer.T, layer.slots), torch.int32, "slot_pos")
     if y_shared is not None:
-        _need(y_shared, (layer.T, layer.d), torch.float32, "y_shared")
+        _need(y_shared, (layer.T, layer.d), layer.yperm_dtype, "y_shared")
     y = torch.empty((layer.T, layer.d), dtype=layer.y_dtype, device=dev)
     c = layer.cfg()
     _check(lib().moe_combine(ctypes.byref(c), _ptr(y_perm), _ptr(slot_pos), _ptr(y_shared), _ptr(y),

@@ -254,8 +254,9 @@ Layout layout(const moe_config& c) {
     const bool split = use_h_split(c);
     l.h_lo = take(split ? n * c.d_ff * esize(c) : 0);
     l.h_shared_lo = take(split && c.n_shared ? (size_t)c.T * c.d_ff_shared * esize(c) : 0);
-    l.y_perm = take(4 * n * c.d);
-    l.y_shared = take(c.n_shared ? 4 * (size_t)c.T * c.d : 0);
+    const size_t yb = c.yperm_bf16 ? 2 : 4;  // expert rows in bf16 or fp32
+    l.y_perm = take(yb * n * c.d);
+    l.y_shared = take(c.n_shared ? yb * (size_t)c.T * c.d : 0);
     const Splits sp = choose_splits(c);
     const size_t su = sp.up > 1 ? sp.up : 0, sd = sp.down > 1 ? sp.down : 0;
     l.part_up = take(4 * su * n * 2 * c.d_ff);
@@ -359,6 +360,7 @@ int check_config(const moe_config* c) {
     if (c->y_fp32 != 0 && c->y_fp32 != 1) return MOE_ERR_DTYPE;
     if (c->h_split != 0 && c->h_split != 1) return MOE_ERR_DTYPE;
     if (c->routing != MOE_ROUTE_TOKEN_CHOICE && c->routing != MOE_ROUTE_EXPERT_CHOICE) return MOE_ERR_SHAPE;
+    if (c->yperm_bf16 != 0 && (c->yperm_bf16 != 1 || c->dtype != MOE_BF16)) return MOE_ERR_DTYPE;
     if (c->routing == MOE_ROUTE_EXPERT_CHOICE) {
         if ((long long)c->T * c->E >= (1LL << 31)) return MOE_ERR_SHAPE;
         if ((long long)c->E * ec_bucket(*c) >= (1LL << 31)) return MOE_ERR_SHAPE;
@@ -524,7 +526,7 @@ int enqueue_route_ec(const moe_config& c, const Layout& L, void* ws, const void*
 // left in the workspace for the split-aware combine (moe_forward).
 int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_perm, const int32_t* offsets,
                 const float* gates_perm, const void* w1, const void* w3, const void* w2, const void* x,
-                const void* ws1, const void* ws3, const void* ws2, float* y_perm, float* y_shared, int sms,
+                const void* ws1, const void* ws3, const void* ws2, void* y_perm, void* y_shared, int sms,
                 cudaStream_t s, bool reduce_down, const int32_t* gather_idx, const moe_fp8_weights* w8 = nullptr) {
     const Splits sp = choose_splits(c, w8 != nullptr);
     const int n = (int)perm_rows(c);
@@ -558,6 +560,7 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
     down[0].N = c.d;
     down[0].K = c.d_ff;
     down[0].out = y_perm;
+    down[0].out_bf16 = c.yperm_bf16;
     down[0].row_scale = gates_perm;
     int np = 1;
     if (c.n_shared) {
@@ -580,6 +583,7 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
         down[1].N = c.d;
         down[1].K = c.d_ff_shared;
         down[1].out = y_shared;
+        down[1].out_bf16 = c.yperm_bf16;
         np = 2;
     }
     if (sp.up > 1) {
@@ -679,24 +683,24 @@ int enqueue_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_pe
             MOE_LAUNCH(launch_gemm_decode(kGemmScale, down, np, status, sms, s, sp.down, w8 != nullptr,
                                           decode_tile_rows(c, w8 != nullptr)));
             if (sp.down > 1 && reduce_down) {
-                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
+                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s, c.yperm_bf16 != 0));
                 if (c.n_shared)
-                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s));
+                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s, c.yperm_bf16 != 0));
             }
         } else if (w8) {
             MOE_LAUNCH(launch_gemm_tc_w8(kGemmScale, down, np, status, sms, s, sp.down));
             if (sp.down > 1 && reduce_down) {
-                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
+                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s, c.yperm_bf16 != 0));
                 if (c.n_shared)
-                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s));
+                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s, c.yperm_bf16 != 0));
             }
         } else if (c.dtype == MOE_BF16) {
             MOE_LAUNCH(launch_gemm_tc(split ? kGemmScaleSplit : kGemmScale, down, np, status, sms, s, sp.down,
                                       use_pair_gemm(c) && sp.down == 1));
             if (sp.down > 1 && reduce_down) {
-                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s));
+                MOE_LAUNCH(launch_reduce_partials(n, offsets + c.E, c.d, sp.down, down[0].part, y_perm, s, c.yperm_bf16 != 0));
                 if (c.n_shared)
-                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s));
+                    MOE_LAUNCH(launch_reduce_partials(c.T, nullptr, c.d, sp.down, down[1].part, y_shared, s, c.yperm_bf16 != 0));
             }
         } else {
             MOE_LAUNCH(launch_gemm_simt_f32(kGemmScale, down, np, s));
@@ -724,26 +728,23 @@ int forward_tail(const moe_config& c, const Layout& L, void* ws, const void* x, 
         MOE_LAUNCH(launch_gather_rows(c.dtype, c.T, c.d, (int)perm_rows(c), offsets + c.E, sorted, x, x_perm,
                                       status, s));
     }
-    float* y_perm = at<float>(ws, L.y_perm);
-    float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
+    void* y_perm = at<void>(ws, L.y_perm);
+    void* y_shared = c.n_shared ? at<void>(ws, L.y_shared) : nullptr;
     MOE_TRY(enqueue_ffn(c, L, ws, x_perm, offsets, gates_perm, w1, w3, w2, x, ws1, ws3, ws2, y_perm, y_shared, sms,
                         s, false, gather_idx, w8));
-    // combine (straight from the down GEMM's split-K slices when it was split)
+    // combine (straight from the down GEMM's split-K slices when it was split;
+    // a layer that keeps its expert rows in bf16 rounds each entry's slice sum
+    // as the reduction into a bf16 row would)
     const Splits sp = choose_splits(c, w8 != nullptr);
-    const float* yp = y_perm;
-    const float* ys = y_shared;
-    size_t yp_stride = 0, ys_stride = 0;
-    if (sp.down > 1) {
-        yp = at<float>(ws, L.part_dn);
-        yp_stride = (size_t)perm_rows(c) * c.d;
-        if (c.n_shared) {
-            ys = at<float>(ws, L.part_dn_shared);
-            ys_stride = (size_t)c.T * c.d;
-        }
-    }
+    const int ydt = c.y_fp32 ? MOE_F32 : c.dtype;
     StageScope scope(kStageCombine, s);
-    MOE_LAUNCH(launch_combine_split(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, slots, yp, yp_stride, sp.down, slot_pos,
-                                    ys, ys_stride, sp.down, y, s, n_empty));
+    if (sp.down > 1) {
+        MOE_LAUNCH(launch_combine_split(ydt, c.T, c.d, slots, at<float>(ws, L.part_dn), (size_t)perm_rows(c) * c.d,
+                                        sp.down, slot_pos, c.n_shared ? at<float>(ws, L.part_dn_shared) : nullptr,
+                                        (size_t)c.T * c.d, sp.down, y, s, n_empty, c.yperm_bf16 != 0));
+    } else {
+        MOE_LAUNCH(launch_combine(ydt, c.T, c.d, slots, y_perm, slot_pos, y_shared, y, s, n_empty, c.yperm_bf16 != 0));
+    }
     return MOE_OK;
 }
 
@@ -894,7 +895,7 @@ int moe_permute(const moe_config* cfg, const int32_t* topk_ids, const float* gat
 
 int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets, const float* gates_perm,
                    const void* w1, const void* w3, const void* w2, const void* x, const void* ws1, const void* ws3,
-                   const void* ws2, float* y_perm, float* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                   const void* ws2, void* y_perm, void* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
     if (c.T == 0) return MOE_OK;
@@ -913,7 +914,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* off
                        reinterpret_cast<cudaStream_t>(stream), true, nullptr);
 }
 
-int moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_pos, const float* y_shared, void* y,
+int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot_pos, const void* y_shared, void* y,
                 moe_stream_t stream) {
     MOE_TRY(check_config(cfg));
     const moe_config& c = *cfg;
@@ -924,7 +925,7 @@ int moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* slot_
     MOE_TRY(device_sms(&sms));
     StageScope scope(kStageCombine, reinterpret_cast<cudaStream_t>(stream));
     MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, c.T, c.d, slots_per_token(c), y_perm, slot_pos, y_shared, y,
-                              reinterpret_cast<cudaStream_t>(stream)));
+                              reinterpret_cast<cudaStream_t>(stream), nullptr, c.yperm_bf16 != 0));
     return MOE_OK;
 }
 
@@ -1337,8 +1338,8 @@ int moe_forward_train(const moe_config* cfg, const void* x, const void* w_gate, 
     const int np = c.n_shared ? 2 : 1;
     void* h = at<void>(ws, L.h);
     void* hs = at<void>(ws, L.h_shared);
-    float* y_perm = at<float>(ws, L.y_perm);
-    float* y_shared = c.n_shared ? at<float>(ws, L.y_shared) : nullptr;
+    void* y_perm = at<void>(ws, L.y_perm);
+    void* y_shared = c.n_shared ? at<void>(ws, L.y_shared) : nullptr;
     GemmProblem up[2] = {}, down[2] = {};
     up[0].A = xp;
     up[0].a_rows = n;
@@ -1384,7 +1385,8 @@ int moe_forward_train(const moe_config* cfg, const void* x, const void* w_gate, 
     MOE_LAUNCH(launch_gemm_tc(kGemmSwiGLU, up, np, status, sms, s, 1, pair));
     MOE_LAUNCH(launch_gemm_tc(kGemmScale, down, np, status, sms, s, 1, pair));
     // 7: combine
-    MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, T, d, c.k, y_perm, o.slot_pos, y_shared, y, s, nullptr));
+    MOE_LAUNCH(launch_combine(c.y_fp32 ? MOE_F32 : c.dtype, T, d, c.k, y_perm, o.slot_pos, y_shared, y, s, nullptr,
+                              c.yperm_bf16 != 0));
     return MOE_OK;
 }
 

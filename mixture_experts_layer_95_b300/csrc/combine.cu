@@ -41,6 +41,29 @@ __device__ __forceinline__ void add4(float4& a, const float4& b) {
     a.w += b.w;
 }
 
+// 8 consecutive values of a row (16-byte aligned) as two float4: fp32 rows,
+// or bf16 rows widened exactly
+__device__ __forceinline__ void load8(const float* p, float4& a, float4& b) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float4& a, float4& b) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.z));
+    const float2 f3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.w));
+    a = make_float4(f0.x, f0.y, f1.x, f1.y);
+    b = make_float4(f2.x, f2.y, f3.x, f3.y);
+}
+
+// v rounded to bf16 and back (what storing it as a bf16 row would keep)
+__device__ __forceinline__ float4 round_bf16(float4 v) {
+    const float2 a = __bfloat1622float2(__floats2bfloat162_rn(v.x, v.y));
+    const float2 b = __bfloat1622float2(__floats2bfloat162_rn(v.z, v.w));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // One warp per (token, 256-column chunk), so that even a single token is
 // spread over d/256 warps.  The warp reads the token's k slot positions 32 at
 // a time (lane j holds slot j of the batch), finds the live ones (>= 0) with
@@ -52,13 +75,17 @@ __device__ __forceinline__ void add4(float4& a, const float4& b) {
 // each entry's slices are summed in slice order first, then the entries in
 // fixed j order, then the shared row -- the same order in which a reduction
 // of the slices followed by the plain combine adds them.
-template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, const float* __restrict__ y_perm,
+// TIN: the rows' storage (fp32, or bf16 for layers that keep them in bf16).
+// round_rows (fp32 split-K slices of a layer whose rows are bf16): each
+// entry's slice sum is rounded to bf16 before it is added, exactly as if the
+// slices had been reduced into a bf16 row first.
+template <typename T, typename TIN>
+__global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, const TIN* __restrict__ y_perm,
                                                       size_t perm_stride, int nsplit,
                                                       const int32_t* __restrict__ slot_pos,
-                                                      const float* __restrict__ y_shared, size_t shared_stride,
+                                                      const TIN* __restrict__ y_shared, size_t shared_stride,
                                                       int shared_nsplit, T* __restrict__ y,
-                                                      int32_t* __restrict__ n_empty) {
+                                                      int32_t* __restrict__ n_empty, int round_rows) {
     pdl_wait();
     const int chunks = (d + 255) / 256;
     const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -78,13 +105,18 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
             live &= live - 1u;
             const int pos = __shfl_sync(0xffffffffu, my_pos, j);
             if (!active) continue;
-            const float4* src = reinterpret_cast<const float4*>(y_perm + (size_t)pos * d + c);
-            float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+            float4 p0, p1;
+            load8(y_perm + (size_t)pos * d + c, p0, p1);
 #pragma unroll 8
             for (int sl = 1; sl < nsplit; ++sl) {  // independent loads: keep them in flight together
-                const float4* q = reinterpret_cast<const float4*>(y_perm + sl * perm_stride + (size_t)pos * d + c);
-                add4(p0, __ldg(q));
-                add4(p1, __ldg(q + 1));
+                float4 q0, q1;
+                load8(y_perm + sl * perm_stride + (size_t)pos * d + c, q0, q1);
+                add4(p0, q0);
+                add4(p1, q1);
+            }
+            if (round_rows) {
+                p0 = round_bf16(p0);
+                p1 = round_bf16(p1);
             }
             add4(a0, p0);
             add4(a1, p1);
@@ -93,13 +125,18 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
     if (n_empty && !any && lane == 0 && c == 0) atomicAdd(n_empty, 1);  // a token no expert took
     if (!active) return;
     if (y_shared) {
-        const float4* src = reinterpret_cast<const float4*>(y_shared + (size_t)t * d + c);
-        float4 p0 = __ldg(src), p1 = __ldg(src + 1);
+        float4 p0, p1;
+        load8(y_shared + (size_t)t * d + c, p0, p1);
 #pragma unroll 8
         for (int sl = 1; sl < shared_nsplit; ++sl) {
-            const float4* q = reinterpret_cast<const float4*>(y_shared + sl * shared_stride + (size_t)t * d + c);
-            add4(p0, __ldg(q));
-            add4(p1, __ldg(q + 1));
+            float4 q0, q1;
+            load8(y_shared + sl * shared_stride + (size_t)t * d + c, q0, q1);
+            add4(p0, q0);
+            add4(p1, q1);
+        }
+        if (round_rows) {
+            p0 = round_bf16(p0);
+            p1 = round_bf16(p1);
         }
         add4(a0, p0);
         add4(a1, p1);
@@ -150,10 +187,12 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(int rows_max, cons
     pdl_trigger();
 }
 
-// out[r][c] = sum over slices of part[s][r][c], slices in order.
+// out[r][c] = sum over slices of part[s][r][c], slices in order (stored as
+// fp32, or rounded to bf16).
+template <typename TO>
 __global__ void __launch_bounds__(256) reduce_partials_kernel(int rows_max, const int32_t* __restrict__ rows_dev,
                                                               int N, int ksplit, const float* __restrict__ part,
-                                                              float* __restrict__ out) {
+                                                              TO* __restrict__ out) {
     pdl_wait();
     const int rows = rows_dev ? min(*rows_dev, rows_max) : rows_max;
     const size_t stride = (size_t)rows_max * N;
@@ -166,7 +205,7 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(int rows_max, cons
 #pragma unroll 8
         for (int sl = 1; sl < ksplit; ++sl)
             add4(acc, __ldg(reinterpret_cast<const float4*>(part + sl * stride + r * N + c)));
-        *reinterpret_cast<float4*>(out + r * N + c) = acc;
+        store4<TO>(out + r * N + c, acc);
     }
     __syncthreads();
     pdl_trigger();
@@ -215,23 +254,38 @@ cudaError_t launch_bias_update(int T, int E, int k, const int32_t* counts, float
 
 cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_perm, size_t perm_stride,
                                  int nsplit, const int32_t* slot_pos, const float* y_shared, size_t shared_stride,
-                                 int shared_nsplit, void* y, cudaStream_t s, int32_t* n_empty) {
+                                 int shared_nsplit, void* y, cudaStream_t s, int32_t* n_empty, bool round_rows) {
     if (T == 0) return cudaSuccess;
     const long long warps = (long long)T * ((d + 255) / 256);
     const int grid = (int)((warps + 7) / 8);
+    const int rr = round_rows ? 1 : 0;
     if (dtype == MOE_BF16)
-        launch_pdl(combine_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
-                                                           shared_stride, shared_nsplit,
-                                                           static_cast<__nv_bfloat16*>(y), n_empty);
+        launch_pdl(combine_kernel<__nv_bfloat16, float>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride,
+                   nsplit, slot_pos, y_shared, shared_stride, shared_nsplit, static_cast<__nv_bfloat16*>(y), n_empty,
+                   rr);
     else
-        launch_pdl(combine_kernel<float>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared,
-                                                   shared_stride, shared_nsplit, static_cast<float*>(y), n_empty);
+        launch_pdl(combine_kernel<float, float>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride, nsplit,
+                   slot_pos, y_shared, shared_stride, shared_nsplit, static_cast<float*>(y), n_empty, rr);
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, const int32_t* slot_pos,
-                           const float* y_shared, void* y, cudaStream_t s, int32_t* n_empty) {
-    return launch_combine_split(dtype, T, d, k, y_perm, 0, 1, slot_pos, y_shared, 0, 1, y, s, n_empty);
+cudaError_t launch_combine(int dtype, int T, int d, int k, const void* y_perm, const int32_t* slot_pos,
+                           const void* y_shared, void* y, cudaStream_t s, int32_t* n_empty, bool rows_bf16) {
+    if (T == 0) return cudaSuccess;
+    if (!rows_bf16)
+        return launch_combine_split(dtype, T, d, k, static_cast<const float*>(y_perm), 0, 1, slot_pos,
+                                    static_cast<const float*>(y_shared), 0, 1, y, s, n_empty, false);
+    const long long warps = (long long)T * ((d + 255) / 256);
+    const int grid = (int)((warps + 7) / 8);
+    const __nv_bfloat16* yp = static_cast<const __nv_bfloat16*>(y_perm);
+    const __nv_bfloat16* ys = static_cast<const __nv_bfloat16*>(y_shared);
+    if (dtype == MOE_BF16)
+        launch_pdl(combine_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(grid), dim3(256), 0, s, T, d, k, yp, (size_t)0, 1,
+                   slot_pos, ys, (size_t)0, 1, static_cast<__nv_bfloat16*>(y), n_empty, 0);
+    else
+        launch_pdl(combine_kernel<float, __nv_bfloat16>, dim3(grid), dim3(256), 0, s, T, d, k, yp, (size_t)0, 1,
+                   slot_pos, ys, (size_t)0, 1, static_cast<float*>(y), n_empty, 0);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_swiglu_finalize(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
@@ -243,10 +297,15 @@ cudaError_t launch_swiglu_finalize(int rows_max, const int32_t* rows_dev, int N,
 }
 
 cudaError_t launch_reduce_partials(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
-                                   float* out, cudaStream_t s) {
+                                   void* out, cudaStream_t s, bool out_bf16) {
     if (rows_max == 0) return cudaSuccess;
-    launch_pdl(reduce_partials_kernel, dim3(grid_for((size_t)rows_max * (N / 4), 256)), dim3(256), 0, s, rows_max, rows_dev, N, ksplit,
-                                                                                     part, out);
+    const dim3 grid(grid_for((size_t)rows_max * (N / 4), 256));
+    if (out_bf16)
+        launch_pdl(reduce_partials_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, rows_max, rows_dev, N, ksplit, part,
+                   static_cast<__nv_bfloat16*>(out));
+    else
+        launch_pdl(reduce_partials_kernel<float>, grid, dim3(256), 0, s, rows_max, rows_dev, N, ksplit, part,
+                   static_cast<float*>(out));
     return cudaGetLastError();
 }
 

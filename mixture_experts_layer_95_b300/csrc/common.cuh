@@ -215,9 +215,11 @@ cudaError_t launch_gather_rows(int dtype, int T, int d, int rows_max, const int3
                                const int32_t* sorted_token_ids, const void* x, void* x_perm, int* status,
                                cudaStream_t s);
 
-// y[t] = sum_j y_perm[slot_pos[t][j]] (slot_pos >= 0) + y_shared[t].
-cudaError_t launch_combine(int dtype, int T, int d, int k, const float* y_perm, const int32_t* slot_pos,
-                           const float* y_shared, void* y, cudaStream_t s, int32_t* n_empty = nullptr);
+// y[t] = sum_j y_perm[slot_pos[t][j]] (slot_pos >= 0) + y_shared[t]; the
+// rows are fp32, or bf16 when rows_bf16.
+cudaError_t launch_combine(int dtype, int T, int d, int k, const void* y_perm, const int32_t* slot_pos,
+                           const void* y_shared, void* y, cudaStream_t s, int32_t* n_empty = nullptr,
+                           bool rows_bf16 = false);
 
 // Expert-choice routing: expert e takes the C tokens with the largest
 // probs[t][e] (ties to the lower token index), in ascending token order, as
@@ -259,6 +261,7 @@ struct GemmProblem {
     int N;
     int K;
     void* out;            // [rows][N]
+    int out_bf16;         // Scale / ScaleSplit modes: out holds bf16 rows (else fp32)
     const float* row_scale;
     const void* A2;       // kGemmScaleSplit: the lo half of A, same layout
     void* out2;           // kGemmSwiGLU: optional lo half of H (H - bf16(H)), same layout as out
@@ -386,14 +389,18 @@ cudaError_t launch_split_e4m3(int rows, int K, const void* x, int x_rows, const 
 cudaError_t launch_swiglu_finalize(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
                                    void* h, void* h_lo, cudaStream_t s);
 
-// out[r][c] = sum_s P[s][r][c] (fp32) for r < rows (rows_dev as above).
+// out[r][c] = sum_s P[s][r][c] for r < rows (rows_dev as above), stored as
+// fp32 or, with out_bf16, rounded to bf16.
 cudaError_t launch_reduce_partials(int rows_max, const int32_t* rows_dev, int N, int ksplit, const float* part,
-                                   float* out, cudaStream_t s);
+                                   void* out, cudaStream_t s, bool out_bf16 = false);
 
-// Combine over split-K partials: y[t] = sum_j (sum_s Yp[s][pos_j]) + sum_s Ys[s][t].
+// Combine over split-K partials: y[t] = sum_j (sum_s Yp[s][pos_j]) + sum_s Ys[s][t];
+// round_rows rounds each entry's slice sum to bf16 before adding it (the
+// layer keeps its rows in bf16).
 cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_perm, size_t perm_stride,
                                  int nsplit, const int32_t* slot_pos, const float* y_shared, size_t shared_stride,
-                                 int shared_nsplit, void* y, cudaStream_t s, int32_t* n_empty = nullptr);
+                                 int shared_nsplit, void* y, cudaStream_t s, int32_t* n_empty = nullptr,
+                                 bool round_rows = false);
 
 // CUDA-core fp32 path with the same semantics (dtype MOE_F32).
 cudaError_t launch_gemm_simt_f32(int mode, const GemmProblem* probs, int nprob, cudaStream_t s);

@@ -58,6 +58,7 @@ struct DecParams {  // CUtensorMap members carry their own 64-byte alignment
     CUtensorMap tmW2[2];  // W3 (SwiGLU)
     const int32_t* offsets[2];
     void* out[2];
+    int out_bf16[2];  // Scale mode without split-K: out holds bf16 rows
     const float* row_scale[2];
     const float* wscale1[2];
     const float* wscale2[2];
@@ -321,6 +322,15 @@ __device__ __forceinline__ void dec_epilogue(const DecParams& p, const DTile& t,
                 const int jn = min(32, t.rows_valid - c0);
                 const size_t row = (size_t)(t.x_row0 + c0);
                 const float* rs = p.row_scale[t.prob] ? p.row_scale[t.prob] + row : nullptr;
+                if (p.ksplit == 1 && p.out_bf16[t.prob]) {  // bf16 rows
+                    __nv_bfloat16* db = static_cast<__nv_bfloat16*>(p.out[t.prob]) + row * N + o;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn)
+                            db[(size_t)j * N] = __float2bfloat16_rn(
+                                (rs ? __ldg(rs + j) : 1.0f) * dec_xscale(p, t, c0 + j) * ws * __uint_as_float(v[j]));
+                    continue;
+                }
                 float* dst = p.ksplit > 1
                                  ? p.part[t.prob] + (static_cast<size_t>(t.ks) * p.x_rows[t.prob] + row) * N + o
                                  : static_cast<float*>(p.out[t.prob]) + row * N + o;
@@ -691,8 +701,10 @@ cudaError_t launch_gemm_decode(int mode, const GemmProblem* probs, int nprob, in
             prm.part[q] = g.part;
             prm.part_cols[q] = mode == kGemmSwiGLU ? 2 * g.N : g.N;
         }
+        if (g.out_bf16 && mode != kGemmScale) return cudaErrorInvalidValue;
         prm.offsets[q] = g.offsets;
         prm.out[q] = g.out;
+        prm.out_bf16[q] = g.out_bf16;
         prm.row_scale[q] = g.row_scale;
         prm.wscale1[q] = w8 ? g.wscale1 : nullptr;
         prm.wscale2[q] = w8 ? g.wscale2 : nullptr;

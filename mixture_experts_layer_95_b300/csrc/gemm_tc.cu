@@ -76,6 +76,7 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     CUtensorMap tmB2[2];
     const int32_t* offsets[2];
     void* out[2];
+    int out_bf16[2];  // fp32-accumulator modes: out holds bf16 rows
     void* out2[2];  // SwiGLU: when non-null, the lo half of H (H - bf16(H)) goes here
     const float* row_scale[2];
     int G[2], M[2], N[2], K[2], a_rows[2];
@@ -510,7 +511,21 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             const bool more = c0 + 32 < ncols;
             uint32_t vn[32];
             if (more) tmem_ld32(tacc + c0 + 32, vn);
-            if (live) {
+            if (live && p.out_bf16[t.prob]) {  // bf16 rows: lane = column, 64-byte row segments
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[t.prob]) +
+                                     (size_t)(t.out_row0 + wrow0) * N + col + lane;
+                const bool col_ok = col + lane < N;
+                if (nvalid == 32 && col + 32 <= N) {
+                    float rv[32];
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) rv[r] = stage[r][lane];
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) dst[(size_t)r * N] = __float2bfloat16_rn(rv[r]);
+                } else {
+                    for (int r = 0; r < nvalid; ++r)
+                        if (col_ok) dst[(size_t)r * N] = __float2bfloat16_rn(stage[r][lane]);
+                }
+            } else if (live) {
                 float* dst = out + (size_t)(t.out_row0 + wrow0) * N + col + lane;
                 if (nvalid == 32 && col + 32 <= N) {
                     float rv[32];
@@ -1302,8 +1317,10 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
             prm.out_g[q] = g.out_g;
             prm.out_u[q] = g.out_u;
         }
+        if (g.out_bf16 && mode != kGemmScale && mode != kGemmScaleSplit) return cudaErrorInvalidValue;
         prm.offsets[q] = g.offsets;
         prm.out[q] = g.out;
+        prm.out_bf16[q] = g.out_bf16;
         prm.out2[q] = g.out2;
         prm.row_scale[q] = g.row_scale;
         prm.G[q] = g.G;
@@ -1381,8 +1398,10 @@ cudaError_t launch_gemm_tc_w8(int mode, const GemmProblem* probs, int nprob, int
             prm.part[q] = g.part;
             prm.part_cols[q] = mode == kGemmSwiGLU ? 2 * g.N : g.N;
         }
+        if (g.out_bf16 && mode != kGemmScale) return cudaErrorInvalidValue;
         prm.offsets[q] = g.offsets;
         prm.out[q] = g.out;
+        prm.out_bf16[q] = g.out_bf16;
         prm.out2[q] = g.out2;
         prm.row_scale[q] = g.row_scale;
         prm.wscale1[q] = g.wscale1;

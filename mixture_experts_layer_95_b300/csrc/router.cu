@@ -28,9 +28,14 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = kRouterThreads / 32;
 constexpr int kSplitDThreads = 512;  // one-block-per-token router: d split over 512 threads
-constexpr int kTokensPerWarp = kRouterTokensPerBlock / kWarps;
+// softmax / top-k pass over precomputed logits: 16 warps share a block's 64
+// tokens (8 when each lane holds 32 experts' logits), so that a top-8 over 256
+// experts (k sequential warp reductions per token) keeps enough warps in flight
+template <int NJ>
+constexpr int logits_warps() {
+    return NJ >= 32 ? 8 : 16;
+}
 
 // Softmax, top-k and gate epilogue shared by both kernels.  Lane L holds the
 // logit (already including logit_bias) of experts L + 32*j in l[j]; absent
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(kSplitDThreads) router_split_d_kernel(
 }
 
 template <int NJ>
-__global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
+__global__ void __launch_bounds__(32 * logits_warps<NJ>()) router_logits_kernel(
     int Tn, int E, int k, const float* __restrict__ logits, const float* __restrict__ logit_bias,
     const float* __restrict__ select_bias, int renormalize, int32_t* __restrict__ topk_ids,
     float* __restrict__ gates, float* __restrict__ p_part, int32_t* __restrict__ block_hist,
@@ -464,7 +469,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
     pdl_wait();
     extern __shared__ float s_dyn[];
     float* s_p = s_dyn;
-    int* s_h = reinterpret_cast<int*>(s_dyn + kWarps * E);
+    constexpr int kW = logits_warps<NJ>();
+    constexpr int kTokensPerWarp = kRouterTokensPerBlock / kW;
+    int* s_h = reinterpret_cast<int*>(s_dyn + kW * E);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float psum[NJ];
     int hcnt[NJ];
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(
         }
         softmax_topk<NJ>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
     }
-    block_epilogue<NJ, kWarps>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
+    block_epilogue<NJ, kW>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
     __syncthreads();
     pdl_trigger();
 }
@@ -586,11 +593,13 @@ cudaError_t launch_router_from_logits(int T, int E, int k, const float* logits, 
     if (nsplit < 1) return cudaErrorInvalidValue;
     const int nblk = (T + kRouterTokensPerBlock - 1) / kRouterTokensPerBlock;
     if (nblk == 0) return cudaSuccess;
-    const size_t smem = (size_t)kWarps * E * (sizeof(float) + sizeof(int));
-    const dim3 grid(nblk), block(kRouterThreads);
+    const dim3 grid(nblk);
 #define MOE_LOGITS_CASE(NJ)                                                                                  \
     do {                                                                                                     \
-        cudaFuncSetAttribute(router_logits_kernel<NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        const size_t smem = (size_t)logits_warps<NJ>() * E * (sizeof(float) + sizeof(int));                 \
+        const dim3 block(32 * logits_warps<NJ>());                                                           \
+        if (smem > 48 * 1024)                                                                                \
+            cudaFuncSetAttribute(router_logits_kernel<NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
         launch_pdl(router_logits_kernel<NJ>, dim3(grid), dim3(block), smem, s, T, E, k, logits, logit_bias, select_bias,       \
                                                            renormalize, topk_ids, gates, p_part, block_hist, probs, \
                                                            nsplit);                                          \

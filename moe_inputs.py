@@ -51,6 +51,7 @@ class Workload:
     h_split: bool = False        # layer option: keep H as a hi + lo bf16 pair
     routing: str = "token"       # "token": tokens pick top-k experts; "expert": experts pick C tokens
     weights: str = "same"        # "same": experts stored in `dtype`; "fp8": E4M3 codes + per-row fp32 scales
+    yperm_bf16: bool = False     # layer option: expert rows of the down GEMM kept in bf16 for the combine
     seed: int = 0
     notes: str = field(default="", compare=False)
 
@@ -81,12 +82,14 @@ WORKLOADS = {
     "mixtral_decode_t32_fp8": Workload("mixtral_decode_t32_fp8", T=32, d=4096, E=8, F=14336, k=2, weights="fp8"),
     "mixtral_decode_t128_fp8": Workload("mixtral_decode_t128_fp8", T=128, d=4096, E=8, F=14336, k=2,
                                         weights="fp8"),
+    # nine expert rows per token (eight routed, one shared), each a small part of
+    # y: the layer keeps them in bf16 for the combine (half of its 2.1 GB of reads)
     "deepseek_v3": Workload("deepseek_v3", T=8192, d=7168, E=256, F=2048, k=8, n_shared=1, F_s=2048,
-                            select_bias=True),
+                            select_bias=True, yperm_bf16=True),
     # the DeepSeek-V3 expert shape and rows per expert (~256) at an eighth of
     # the weights (32 experts, 1024 tokens): the case profiled with ncu --set full
     "deepseek_v3_e32": Workload("deepseek_v3_e32", T=1024, d=7168, E=32, F=2048, k=8, n_shared=1, F_s=2048,
-                                select_bias=True),
+                                select_bias=True, yperm_bf16=True),
     # the capacity cut leaves most tokens with small outputs and a few with
     # outputs ~12x RMS(y); a bf16 H then costs ~2% of RMS(y) at those tokens,
     # so this layer keeps H as a hi + lo pair

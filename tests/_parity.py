@@ -45,7 +45,7 @@ TOL = {"bf16": 2e-2, "f32": 1e-4}
 def layer_of(w: moe_inputs.Workload) -> moe.Layer:
     return moe.Layer(T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.F, n_shared=w.n_shared, d_ff_shared=w.F_s, dtype=w.dtype,
                      renormalize=w.renormalize, capacity=w.capacity, alpha=w.alpha, h_split=w.h_split,
-                     routing=w.routing)
+                     routing=w.routing, yperm_bf16=w.yperm_bf16)
 
 
 def sample_tokens(T: int, n: int, seed: int = 1234, must=()) -> np.ndarray:

@@ -54,6 +54,13 @@ SMALL = [
     Workload("wide_chunks_e16_bf16", T=2000, d=256, E=16, F=256, k=2),
     # 128-191 rows per expert: the 1-SM kernel's 128-row tiles
     Workload("one_sm_160rows_bf16", T=640, d=256, E=8, F=264, k=2),
+    # expert rows kept in bf16 for the combine: 1-SM tiles (k = 8 + shared), CTA
+    # pairs, and decode-sized split-K (the combine rounds each entry's slice sum)
+    Workload("yperm_bf16_k8_shared", T=300, d=256, E=32, F=128, k=8, n_shared=1, F_s=192, select_bias=True,
+             yperm_bf16=True),
+    Workload("yperm_bf16_pairs", T=1100, d=256, E=4, F=384, k=2, yperm_bf16=True),
+    Workload("yperm_bf16_split_k_t3", T=3, d=256, E=16, F=320, k=2, n_shared=1, F_s=192, yperm_bf16=True),
+    Workload("yperm_bf16_decode_64rows", T=100, d=256, E=8, F=320, k=2, n_shared=1, F_s=192, yperm_bf16=True),
 ]
 
 
