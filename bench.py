@@ -348,15 +348,20 @@ class Bench:
         self.stream = torch.cuda.current_stream(dev)
 
     def warm(self, n):
+        """`n` untimed layer calls; returns the wall-clock ms per call."""
         import torch
 
         import mixture_experts_layer_95_b300 as moe
+        torch.cuda.synchronize(self.dev)
+        t0 = time.perf_counter()
         for _ in range(n):
             self.fw(self.x, self.y)
         torch.cuda.synchronize(self.dev)
+        ms = (time.perf_counter() - t0) * 1e3 / max(n, 1)
         st = self.fw.device_status()
         if st != 0:
             raise moe.MoeError(st, "warm-up device status")
+        return ms
 
     def timed(self, steps, barrier):
         """`steps` back-to-back layer calls timed with events on the launching
@@ -488,6 +493,7 @@ SIDE_WORKLOADS = ("mixtral_decode_t1", "mixtral_decode_t8", "mixtral_decode_t32"
                   "mixtral_decode_t128_fp8", "deepseek_v3", "skewed_capacity", "tiny_f32", "mixtral_prefill_ec")
 SUSTAINED_S = 1.5  # length of the back-to-back loop of the sustained figure
 SIDE_IDLE_S = 1.0  # idle time before each of the other workloads' timed loops
+SIDE_REWARM_S = 0.02  # untimed calls between that idle time and the timed loop
 
 
 def side_steps(w):
@@ -590,8 +596,12 @@ def run_ours(args):
             ws = moe_inputs.WORKLOADS[name]
             steps, warm = side_steps(ws)
             sb = Bench(ws, dev)
-            sb.warm(warm)
-            time.sleep(SIDE_IDLE_S)  # each workload starts from an idle board, as the headline does
+            call_ms = sb.warm(warm)
+            time.sleep(SIDE_IDLE_S)  # each workload starts from a cool board, as the headline does
+            # ... but not from idle clocks: a short loop (about SIDE_REWARM_S,
+            # too short to heat the board) brings the SM clock back up before
+            # the timed calls, which at one decode token last only 30 ms
+            sb.warm(max(3, int(SIDE_REWARM_S * 1e3 / max(call_ms, 1e-3))))
             s_ms, s_up, s_launch, s_win = sb.timed(steps, barrier)
             clocks.mark(*s_win)
             s_roof, s_layer = sb.accounting(s_ms / steps, s_up, peaks, peak_src)
