@@ -305,10 +305,12 @@ def up_kernel_name(plan, fp8):
             "tc": "grouped_gemm_tc_kernel<SwiGLU> (up GEMM)",
             "tc_decode32": "grouped_gemm_decode_kernel<SwiGLU, NT=32> (up GEMM, weights on M)",
             "tc_decode64": "grouped_gemm_decode_kernel<SwiGLU, NT=64> (up GEMM, weights on M)",
-            "simt": "grouped_gemm_simt_kernel<SwiGLU> (up GEMM)"}[plan["up"]]
+            "simt": "grouped_gemm_simt_kernel<SwiGLU> (up GEMM)",
+            "fused": "fused_up_kernel<NT> (router + up projection + SwiGLU, small batches)"}[plan["up"]]
     if fp8:
         # with FP8 weights the decode GEMM takes 48 token rows where bf16 takes 64
-        name = name.replace("<SwiGLU", "<SwiGLU, FP8 weights").replace("NT=64", "NT=48")
+        name = name.replace("<SwiGLU", "<SwiGLU, FP8 weights").replace("NT=64", "NT=48").replace(
+            "<NT>", "<FP8 weights, NT>")
     return name
 
 

@@ -282,7 +282,15 @@ MOE_API int moe_bias_update(const moe_config *cfg, const int32_t *counts, float 
 /* The whole layer (steps 1-7) in one call, fused where the steps allow.
  *   y [T][d] (dtype, or fp32 when cfg->y_fp32) receives the layer output; stats (host struct, nullable)
  *   names optional device outputs.  ws1/ws3/ws2 are the shared expert's weights
- *   (required iff cfg->n_shared == 1). */
+ *   (required iff cfg->n_shared == 1).
+ *   Token-choice bf16 one-token batches (T = 1) with E <= 32, k <= 16 and a
+ *   single bf16 H run as two kernels (moe_plan_describe: up=fused): every CTA
+ *   routes the batch itself (the one-block-per-token router's arithmetic, so
+ *   ids, gates and statistics are bit for bit those of moe_route), the first
+ *   kernel streams W1/W3 rows and writes H, the second streams W2 rows and
+ *   writes y with the gates and the shared expert applied.  The expert dots
+ *   run on the CUDA cores with fp32 accumulation, so y agrees with
+ *   the step-by-step entry points to rounding, not bit for bit. */
 MOE_API int moe_forward(const moe_config *cfg, const void *x, const void *w_gate, const float *logit_bias,
                 const float *select_bias, const void *w1, const void *w3, const void *w2,
                 const void *ws1, const void *ws3, const void *ws2, void *y, const moe_stats *stats,
@@ -300,9 +308,10 @@ MOE_API int moe_forward(const moe_config *cfg, const void *x, const void *w_gate
  * The expert GEMMs stream the one-byte codes (half the bytes of bf16 weights:
  * the decode-time bound) and apply scale_r to the fp32 accumulator of output
  * channel r.  Prefill-sized batches widen the codes exactly to bf16 in shared
- * memory (bf16 x bf16 MMAs).  Decode-sized batches (at most 32 rows per
- * touched expert on average) feed the codes to the FP8 tensor cores as they
- * are; that MMA takes FP8 on both sides, so every bf16 row of x and of H is
+ * memory (bf16 x bf16 MMAs).  Batches the two fused small-batch kernels take
+ * (see moe_forward) widen the codes exactly to fp32 on the CUDA cores, against
+ * bf16 x and H.  Other decode-sized batches (at most 32 rows per touched
+ * expert on average) feed the codes to the FP8 tensor cores as they are; that MMA takes FP8 on both sides, so every bf16 row of x and of H is
  * first split into two E4M3 code rows and a power-of-two scale,
  * row = s (hi + lo), which reproduces every entry within a factor 2^10 of the
  * row's largest magnitude exactly (smaller entries: absolute error at most
@@ -427,8 +436,11 @@ MOE_API const char *moe_strerror(int status);
 
 /* Diagnostic: the kernels moe_forward picks for this configuration, as one
  * line of "key=value" words written into buf (NUL-terminated, truncated to
- * len bytes): router=split_d|warp|gemm, up=/down= tc|tc_pair|simt (tc_pair =
- * CTA-pair tensor-core GEMM with 256-row tiles), ksplit_up=/ksplit_down= the
+ * len bytes): router=split_d|warp|gemm|fused, up=/down=
+ * tc|tc_pair|tc_decode32|tc_decode64|simt|fused (tc_pair = CTA-pair
+ * tensor-core GEMM with 256-row tiles; tc_decode = weights on the MMA's M side
+ * with 32 or 64 token rows; fused = the two small-batch kernels, with bf16
+ * weights), ksplit_up=/ksplit_down= the
  * split-K factor, gather_a=1 when the up GEMM gathers x rows itself, h= the
  * storage of the SwiGLU output.  The choice depends on the configuration
  * only, never on the data.  No counterpart on the pages.  Returns MOE_OK,

@@ -956,6 +956,66 @@ int moe_bias_update(const moe_config* cfg, const int32_t* counts, float gamma, f
     return MOE_OK;
 }
 
+// Steps 1-7 for batches the two fused decode kernels take (decode_fused.cu):
+// every CTA routes the batch itself, so the router, the grouping, the x gather
+// and the combine have no launch of their own.  H goes through the workspace.
+static int forward_fused_decode(const moe_config& c, const FusedPlan& fp, const Layout& L, void* ws, const void* x,
+                                const void* w_gate, const float* logit_bias, const float* select_bias,
+                                const void* w1, const void* w3, const void* w2, const void* ws1, const void* ws3,
+                                const void* ws2, const moe_fp8_weights* w8, void* y, const moe_stats* stats,
+                                cudaStream_t s) {
+    FusedDecodeArgs a{};
+    a.T = c.T;
+    a.d = c.d;
+    a.E = c.E;
+    a.k = c.k;
+    a.F = c.d_ff;
+    a.Fs = c.n_shared ? c.d_ff_shared : 0;
+    a.n_shared = c.n_shared;
+    a.renormalize = c.renormalize;
+    a.capacity = c.capacity;
+    a.y_fp32 = c.y_fp32;
+    a.fp8 = w8 != nullptr;
+    a.alpha = c.alpha;
+    a.x = x;
+    a.wg = w_gate;
+    a.logit_bias = logit_bias;
+    a.select_bias = select_bias;
+    a.w1 = w1;
+    a.w3 = w3;
+    a.w2 = w2;
+    a.ws1 = ws1;
+    a.ws3 = ws3;
+    a.ws2 = ws2;
+    if (w8) {
+        a.s1 = w8->s1;
+        a.s3 = w8->s3;
+        a.s2 = w8->s2;
+        a.ss1 = w8->ss1;
+        a.ss3 = w8->ss3;
+        a.ss2 = w8->ss2;
+    }
+    a.h = at<void>(ws, L.h);
+    a.h_shared = c.n_shared ? at<void>(ws, L.h_shared) : nullptr;
+    a.y = y;
+    if (stats) {
+        a.counts = stats->counts;
+        a.kept = stats->kept;
+        a.n_dropped = stats->n_dropped;
+        a.f = stats->f;
+        a.p = stats->p;
+        a.L = stats->L;
+    }
+    a.status = at<int>(ws, L.status);
+    {
+        StageScope scope(kStageUp, s);
+        MOE_LAUNCH(launch_fused_up(a, fp, s));
+    }
+    StageScope scope(kStageDown, s);
+    MOE_LAUNCH(launch_fused_down(a, fp, s));
+    return MOE_OK;
+}
+
 // Steps 1-7 after argument checks; w8 != nullptr: FP8 expert weights.
 static int forward_body(const moe_config& c, const void* x, const void* w_gate, const float* logit_bias,
                         const float* select_bias, const void* w1, const void* w3, const void* w2, const void* ws1,
@@ -971,6 +1031,10 @@ static int forward_body(const moe_config& c, const void* x, const void* w_gate, 
     if (expert_choice(c))
         return forward_expert_choice(c, L, ws, x, w_gate, logit_bias, w1, w3, w2, ws1, ws3, ws2, y, stats, nblk,
                                      sms, s, w8);
+    const FusedPlan fp = fused_decode_plan(c, w8 != nullptr, sms);
+    if (fp.ok)
+        return forward_fused_decode(c, fp, L, ws, x, w_gate, logit_bias, select_bias, w1, w3, w2, ws1, ws3, ws2, w8,
+                                    y, stats, s);
 
     // 1-4: router, softmax, top-k (the router blocks also emit their id
     // histograms), grouping (+ load statistics from the router's partial sums)
@@ -1450,6 +1514,11 @@ int moe_plan_describe(const moe_config* cfg, char* buf, size_t len) {
     const char* router = use_split_d_router(c.T, c.E) ? "split_d"
                          : use_warp_router(c.E, c.d, c.dtype) ? "warp"
                                                               : "gemm";
+    if (fused_decode_plan(c, false, kNominalSms).ok) {
+        snprintf(buf, len, "routing=token_choice router=fused up=fused ksplit_up=1 down=fused ksplit_down=1 "
+                           "gather_a=0 h=bf16");
+        return MOE_OK;
+    }
     const char* gemm = c.dtype != MOE_BF16 ? "simt" : (use_decode_gemm(c) ? (decode_tile_rows(c) == 32 ? "tc_decode32" : "tc_decode64") : "tc");
     const Splits sp = choose_splits(c);
     const bool gather = use_gather_a(c);

@@ -405,4 +405,42 @@ cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_
 // CUDA-core fp32 path with the same semantics (dtype MOE_F32).
 cudaError_t launch_gemm_simt_f32(int mode, const GemmProblem* probs, int nprob, cudaStream_t s);
 
+// ---- decode_fused.cu: the whole token-choice layer for batches of at most
+// kFusedMaxT tokens on routers of at most kFusedMaxE experts, in two launches
+// (router + up projection + SwiGLU; down projection + gates + shared expert).
+constexpr int kFusedMaxT = 1;
+constexpr int kFusedMaxE = 32;
+constexpr int kFusedMaxEntries = 16;  // T k routing decisions
+
+struct FusedDecodeArgs {
+    int T, d, E, k, F, Fs, n_shared, renormalize, capacity, y_fp32, fp8;
+    float alpha;
+    const void *x, *wg;                           // bf16 [T][d], [E][d]
+    const float *logit_bias, *select_bias;        // [E], nullable
+    const void *w1, *w3, *w2, *ws1, *ws3, *ws2;   // bf16 weights or E4M3 codes
+    const float *s1, *s3, *s2, *ss1, *ss3, *ss2;  // FP8 row scales (fp8 = 1)
+    void *h, *h_shared;                           // bf16 H [T k][F], [T][Fs] (workspace)
+    void* y;                                      // [T][d] bf16, or fp32 when y_fp32
+    int32_t *counts, *kept, *n_dropped;           // statistics, each nullable
+    float *f, *p, *L;
+    int* status;
+};
+
+// Shared-memory and grid plan of the two kernels for one layer; ok is false
+// when the layer is not one they take (routing, dtype, sizes) or does not fit.
+struct FusedPlan {
+    bool ok;
+    int up_rows, up_wslice, up_stages;      // a stage: up_rows whole W1 and W3 rows; d elements per consumer warp
+    int dn_wslice, dn_wslice_s, dn_stages;  // per consumer warp: F (F_s) elements of each W2 row
+    int dn_rows_stage;                      // a stage: this many whole consecutive W2 rows (1 or 2)
+    int up_pv, dn_pv;                       // activation vectors per lane and token (2 or 4)
+    int dn_rows, dn_cols;                   // output channels per CTA (at most); partial columns (at most)
+    int grid_up, grid_dn;
+    size_t up_part_bytes, up_smem;                   // partial dots, then the ring
+    size_t dn_stage_bytes, dn_part_bytes, dn_smem;   // partial dots, then the ring
+};
+FusedPlan fused_decode_plan(const moe_config& c, bool fp8, int sms);
+cudaError_t launch_fused_up(const FusedDecodeArgs& a, const FusedPlan& p, cudaStream_t s);
+cudaError_t launch_fused_down(const FusedDecodeArgs& a, const FusedPlan& p, cudaStream_t s);
+
 }  // namespace moe

@@ -24,91 +24,18 @@
 #include <float.h>
 
 #include "common.cuh"
+#include "route_math.cuh"
 
 namespace moe {
 namespace {
+using namespace route_math;
 
-constexpr int kSplitDThreads = 512;  // one-block-per-token router: d split over 512 threads
 // softmax / top-k pass over precomputed logits: 16 warps share a block's 64
 // tokens (8 when each lane holds 32 experts' logits), so that a top-8 over 256
 // experts (k sequential warp reductions per token) keeps enough warps in flight
 template <int NJ>
 constexpr int logits_warps() {
     return NJ >= 32 ? 8 : 16;
-}
-
-// Softmax, top-k and gate epilogue shared by both kernels.  Lane L holds the
-// logit (already including logit_bias) of experts L + 32*j in l[j]; absent
-// experts hold -inf and index < 0.  Writes ids/gates for token t, adds p into
-// the lane's running column sums and counts the chosen experts.
-template <int NJ>
-__device__ __forceinline__ void softmax_topk(int t, int E, int k, const float (&l)[NJ], const float* select_bias,
-                                             int renormalize, int32_t* topk_ids, float* gates, float (&psum)[NJ],
-                                             int (&hcnt)[NJ], float* probs_out) {
-    const int lane = threadIdx.x & 31;
-    float m = -FLT_MAX;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j)
-        if (lane + 32 * j < E) m = fmaxf(m, l[j]);
-    m = warp_max(m);
-    float ex[NJ];
-    float z = 0.f;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        ex[j] = (lane + 32 * j < E) ? expf(l[j] - m) : 0.f;
-        z += ex[j];
-    }
-    z = warp_sum(z);
-    const float inv_z = 1.f / z;
-    float p[NJ], s[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        const int e = lane + 32 * j;
-        p[j] = ex[j] * inv_z;
-        psum[j] += p[j];
-        if (probs_out && e < E) probs_out[(size_t)t * E + e] = p[j];
-        s[j] = (e < E) ? l[j] + (select_bias ? __ldg(select_bias + e) : 0.f) : -FLT_MAX;
-        // a NaN score selects as -inf: the comparisons below then form a total
-        // order (value, then lower index), so every lane agrees on each choice
-        // and the ids match the histogram counted from them
-        if (isnan(s[j])) s[j] = -INFINITY;
-    }
-    uint32_t taken = 0;
-    float gsum = 0.f;
-    float my_gate = 0.f;  // lane r keeps the r-th choice (k <= 32)
-    int my_id = -1;
-    for (int r = 0; r < k; ++r) {
-        float bv = -FLT_MAX;
-        int bi = -1;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && !(taken >> j & 1u) && (bi < 0 || s[j] > bv)) {
-                bv = s[j];
-                bi = e;
-            }
-        }
-        warp_argmax(bv, bi);
-        // the owner lane marks it taken and publishes its probability
-        float pw = 0.f;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j)
-            if (bi == lane + 32 * j) {
-                taken |= 1u << j;
-                pw = p[j];
-                hcnt[j] += 1;
-            }
-        pw = __shfl_sync(0xffffffffu, pw, bi & 31);
-        gsum += pw;
-        if (lane == r) {
-            my_gate = pw;
-            my_id = bi;
-        }
-    }
-    if (lane < k) {
-        topk_ids[(size_t)t * k + lane] = my_id;
-        gates[(size_t)t * k + lane] = renormalize ? my_gate / gsum : my_gate;
-    }
 }
 
 // Writes the per-block partial sums of p and the per-block id histogram.
@@ -135,29 +62,6 @@ __device__ __forceinline__ void block_epilogue(int E, const float (&psum)[NJ], c
         if (p_part) p_part[(size_t)blockIdx.x * E + e] = ps;
         if (block_hist) block_hist[(size_t)blockIdx.x * E + e] = hs;
     }
-}
-
-// 16-byte vector of T: 8 bf16 or 4 fp32.
-template <typename T>
-struct Vec {
-    static constexpr int kElems = 16 / sizeof(T);
-};
-
-__device__ __forceinline__ void widen(const uint4& u, float (&v)[8], const __nv_bfloat16*) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        v[2 * i] = f.x;
-        v[2 * i + 1] = f.y;
-    }
-}
-
-__device__ __forceinline__ void widen(const uint4& u, float (&v)[4], const float*) {
-    v[0] = __uint_as_float(u.x);
-    v[1] = __uint_as_float(u.y);
-    v[2] = __uint_as_float(u.z);
-    v[3] = __uint_as_float(u.w);
 }
 
 // Fused router for E <= NE.  W_g is copied once per block into shared memory

@@ -8,7 +8,8 @@ context must stay usable for the next, normal call.  One case per GEMM kernel:
 the 1-CTA kernel (75 rows per expert), the CTA-pair kernel (550 rows per
 expert: both CTAs of a pair give up and meet at the final cluster barrier) and
 the decode kernel with the weights on the MMA's M side, with bf16 and with FP8
-weights (2 rows per expert).
+weights (2 rows per expert), and the two fused small-batch kernels (one
+token; every warp's own ring), with bf16 and with FP8 weights.
 """
 import pytest
 import torch
@@ -24,6 +25,8 @@ CASES = [
     (Workload("stall_pair_bf16", T=1100, d=256, E=4, F=256, k=2), "tc_pair"),
     (Workload("stall_decode_bf16", T=8, d=256, E=8, F=256, k=2), "tc_decode32"),
     (Workload("stall_decode_fp8", T=8, d=256, E=8, F=256, k=2, weights="fp8"), "tc_decode32"),
+    (Workload("stall_fused_bf16", T=1, d=256, E=8, F=256, k=2, n_shared=1, F_s=128), "fused"),
+    (Workload("stall_fused_fp8", T=1, d=256, E=8, F=256, k=2, weights="fp8"), "fused"),
 ]
 
 
@@ -43,9 +46,10 @@ def test_bounded_wait_times_out_and_the_context_survives(cuda, w, up_kernel):
     assert moe.plan_describe(layer.cfg())["up"] == up_kernel
     L = moe_inputs.make_layer(w, "cuda")
     q8 = None
+    shared = (L["ws1"], L["ws3"], L["ws2"]) if w.n_shared else (None, None, None)
     if w.weights == "fp8":
-        q8 = moe.quantize_experts_fp8(layer, L["w1"], L["w3"], L["w2"])
-    fw = moe.Forward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], fp8=q8)
+        q8 = moe.quantize_experts_fp8(layer, L["w1"], L["w3"], L["w2"], *shared)
+    fw = moe.Forward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], None, None, *shared, fp8=q8)
     torch.cuda.synchronize()
     assert moe.test_stall_gemm(True) is False
     try:

@@ -54,8 +54,18 @@ SMALL_FP8 = [
              weights="fp8"),
     Workload("fp8_gemm_router_capacity", T=520, d=384, E=64, F=256, k=4, capacity=40, weights="fp8"),
     Workload("fp8_expert_choice", T=300, d=256, E=8, F=384, k=2, routing="expert", weights="fp8"),
-    # one token, 160 up-GEMM tiles: balanced split-K with FP8 stages (two k-blocks each)
-    Workload("fp8_decode_balanced_splitk_t1", T=1, d=384, E=8, F=10240, k=2, weights="fp8"),
+    # one token, 160 up-GEMM tiles: balanced split-K with FP8 stages (two k-blocks
+    # each); 40 experts keep it off the fused small-batch kernels
+    Workload("fp8_decode_balanced_splitk_t1_e40", T=1, d=384, E=40, F=10240, k=2, weights="fp8"),
+    # the fused small-batch kernels with FP8 codes (one token): ragged slices,
+    # shared expert, selection bias; 8 decisions over 32 experts
+    Workload("fp8_fused_t1_shared_ragged", T=1, d=272, E=8, F=400, k=2, n_shared=1, F_s=208, select_bias=True,
+             weights="fp8"),
+    Workload("fp8_fused_t1_k8_e32", T=1, d=512, E=32, F=512, k=8, zipf_s=1.2, weights="fp8"),
+    # two tokens, the general FP8 decode path: shared expert, capacity cut
+    Workload("fp8_small_t2_shared_ragged", T=2, d=272, E=8, F=400, k=2, n_shared=1, F_s=208, select_bias=True,
+             weights="fp8"),
+    Workload("fp8_small_t2_capacity", T=2, d=512, E=16, F=512, k=4, capacity=1, zipf_s=1.2, weights="fp8"),
     # 17..32 rows per touched expert: the FP8 decode GEMM's 48-row token tiles (shared expert: 48, 48, 4)
     Workload("fp8_decode_48rows_shared", T=100, d=256, E=8, F=320, k=2, n_shared=1, F_s=192, weights="fp8"),
 ]
@@ -83,6 +93,31 @@ def test_fp8_subnormal_codes_are_widened_exactly(cuda):
     exp_zero = ((q1[:, :, 1:] & 0x78) == 0).float().mean().item()
     assert exp_zero > 0.9  # almost every code the GEMM uses is subnormal (or zero)
     _assert_ok(check_layer_fp8(w, L=L))
+
+
+@pytest.mark.parametrize("how", ["tiny", "huge", "zero", "outlier"])
+def test_fp8_fused_one_token_of_extreme_scale(cuda, how):
+    """The fused one-token kernels meet E4M3 codes with f16 activations scaled
+    by a power of two per warp slice (x, then H): a token scaled by 2^-40 or
+    2^+30, a zero token (y exactly 0) and one entry 2^12 above the rest must
+    each stay within tolerance."""
+    import moe_inputs
+    from tests._parity import check_layer_fp8
+    w = Workload(f"fp8_fused_scale_{how}", T=1, d=256, E=8, F=384, k=2, n_shared=1, F_s=128, weights="fp8")
+    L = moe_inputs.make_layer(w, "cuda")
+    x = L["x"].float()
+    if how == "tiny":
+        x *= 2.0 ** -40
+    elif how == "huge":
+        x *= 2.0 ** 30
+    elif how == "zero":
+        x[:] = 0.0
+    else:
+        x[0, 5] = 4096.0
+    L["x"] = x.to(L["x"].dtype).contiguous()
+    rep = check_layer_fp8(w, L=L, per_token=True)
+    print(json.dumps(rep))
+    _assert_ok(rep)
 
 
 @pytest.mark.parametrize("T", [3, 40])

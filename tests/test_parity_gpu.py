@@ -61,6 +61,28 @@ SMALL = [
     Workload("yperm_bf16_pairs", T=1100, d=256, E=4, F=384, k=2, yperm_bf16=True),
     Workload("yperm_bf16_split_k_t3", T=3, d=256, E=16, F=320, k=2, n_shared=1, F_s=192, yperm_bf16=True),
     Workload("yperm_bf16_decode_64rows", T=100, d=256, E=8, F=320, k=2, n_shared=1, F_s=192, yperm_bf16=True),
+    # one token on a router too wide for the fused small-batch kernels: the
+    # decode GEMM with split-K
+    Workload("decode_t1_e40_bf16", T=1, d=512, E=40, F=512, k=2),
+    # one token, E <= 32: the two fused small-batch kernels.  Ragged hidden
+    # slices (F / 16 not a multiple of 8; the last warps' slices shorter or
+    # empty), a d that is not a multiple of 16, shared expert, biases, both
+    # gate normalisations, capacity 0 (every routed entry dropped), 8 routing
+    # decisions over 32 experts
+    Workload("fused_t1_ragged", T=1, d=520, E=8, F=1000, k=2),
+    Workload("fused_t1_k8_shared_long_d", T=1, d=4104, E=32, F=520, k=8, n_shared=1, F_s=264),
+    Workload("fused_t1_shared_selectbias_plain", T=1, d=1024, E=16, F=2056, k=4, n_shared=1, F_s=776,
+             select_bias=True, renormalize=False),
+    Workload("fused_t1_capacity_zero_shared", T=1, d=256, E=4, F=128, k=2, capacity=0, n_shared=1, F_s=64),
+    Workload("fused_t1_capacity_zero", T=1, d=256, E=4, F=128, k=2, capacity=0),
+    Workload("fused_t1_tiny_f_empty_warps", T=1, d=128, E=6, F=40, k=3, zipf_s=1.2),
+    # two tokens: the general decode path (the fused kernels take one), with
+    # the same features
+    Workload("small_t2_shared_selectbias", T=2, d=1024, E=16, F=2056, k=4, n_shared=1, F_s=776, select_bias=True),
+    Workload("small_t2_capacity_shared", T=2, d=256, E=4, F=256, k=3, capacity=1, n_shared=1, F_s=128),
+    Workload("small_t2_k8_plain_gates_e32", T=2, d=384, E=32, F=384, k=8, renormalize=False),
+    # three tokens: the general decode path
+    Workload("decode_t3_shared_capacity", T=3, d=256, E=4, F=256, k=2, capacity=1, n_shared=1, F_s=128),
 ]
 
 
