@@ -55,6 +55,10 @@ METRIC = "MoE-layer tokens/s on 1 B300; % of bf16 tensor peak or HBM roofline"
 UNIT = "tokens/s"
 FALLBACK = dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0)
 EVENT_EVERY = 4  # timed steps per up-GEMM event pair
+# decode-sized side workloads: an event pair costs the bracketed call its
+# programmatic overlap with its neighbours (~15 us of a 0.1 ms call), so they
+# bracket one call in 20
+EVENT_EVERY_DECODE = 20
 FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12  # CUDA-core fp32 FMA peak at the maximum SM clock
 # profiles/traffic.json: per workload, the up GEMM's DRAM bytes per launch from
 # an ncu capture, with the kernel sources it was taken on ("sources", default
@@ -365,9 +369,9 @@ class Bench:
             raise moe.MoeError(st, "warm-up device status")
         return ms
 
-    def timed(self, steps, barrier):
+    def timed(self, steps, barrier, event_every=EVENT_EVERY):
         """`steps` back-to-back layer calls timed with events on the launching
-        stream; the up GEMM is bracketed in every EVENT_EVERY-th call.
+        stream; the up GEMM is bracketed in every event_every-th call.
         Returns (total ms, up-GEMM ms per launch, launches, (wall0, wall1))."""
         import torch
 
@@ -378,10 +382,10 @@ class Bench:
         wall0 = time.time()
         # an event between two kernels removes their programmatic overlap, so
         # the other calls' launches keep it
-        with moe.StageTimer(steps // EVENT_EVERY + 1, stages=("up_gemm",)) as timer:
+        with moe.StageTimer(steps // event_every + 1, stages=("up_gemm",)) as timer:
             start.record(self.stream)
             for i in range(steps):
-                if i % EVENT_EVERY == 0:
+                if i % event_every == 0:
                     timer.begin_call()
                 else:
                     timer.skip_call()
@@ -604,12 +608,13 @@ def run_ours(args):
             # too short to heat the board) brings the SM clock back up before
             # the timed calls, which at one decode token last only 30 ms
             sb.warm(max(3, int(SIDE_REWARM_S * 1e3 / max(call_ms, 1e-3))))
-            s_ms, s_up, s_launch, s_win = sb.timed(steps, barrier)
+            ev = EVENT_EVERY_DECODE if ws.T <= 256 else EVENT_EVERY
+            s_ms, s_up, s_launch, s_win = sb.timed(steps, barrier, ev)
             clocks.mark(*s_win)
             s_roof, s_layer = sb.accounting(s_ms / steps, s_up, peaks, peak_src)
             c = clocks.summary()
             out["workloads"][name] = {
-                "steps": steps, "ms_per_step": round(s_ms / steps, 4), "value": round(ws.T * steps / (s_ms / 1e3), 1),
+                "steps": steps, "event_every": ev, "ms_per_step": round(s_ms / steps, 4), "value": round(ws.T * steps / (s_ms / 1e3), 1),
                 "unit": UNIT, "kernel": s_roof["kernel"], "kernel_bound": s_roof["bound"],
                 "kernel_frac": s_roof["frac"], "kernel_ms": s_roof["launch_ms"],
                 "layer_frac_bf16_peak": s_layer["frac_bf16_peak"], "layer_frac_hbm": s_layer["frac_hbm"],
