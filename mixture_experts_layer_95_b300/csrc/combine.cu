@@ -64,22 +64,49 @@ __device__ __forceinline__ float4 round_bf16(float4 v) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
-// One warp per (token, 256-column chunk), so that even a single token is
-// spread over d/256 warps.  The warp reads the token's k slot positions 32 at
-// a time (lane j holds slot j of the batch), finds the live ones (>= 0) with
-// a ballot and broadcasts them in ascending slot order; each lane owns 8
-// consecutive columns.  k is the top-k of token choice, or E for expert
-// choice (slot e live iff expert e took the token; n_empty, when given,
-// counts the tokens with no live slot).  Rows of y_perm (and
-// y_shared) may be split into `nsplit` fp32 slices `stride` elements apart:
-// each entry's slices are summed in slice order first, then the entries in
-// fixed j order, then the shared row -- the same order in which a reduction
-// of the slices followed by the plain combine adds them.
+// One warp per (token, CH 256-column chunks), so that even a single token is
+// spread over d/(256 CH) warps.  The warp reads the token's k slot positions
+// 32 at a time (lane j holds slot j of the batch), finds the live ones (>= 0)
+// with a ballot and takes them NB at a time in ascending slot order, so that
+// those rows' loads for every chunk are in flight together; each lane owns 8
+// consecutive columns of each chunk.  Measured (same box, A/B): CH = 2,
+// NB = 2 for k <= 2 without split-K slices (skewed layer 43 -> 32 us,
+// Mixtral prefill 48 -> 36 us); one chunk and one row at a time otherwise,
+// where the larger shapes cost more in warps per SM than they gain
+// (DeepSeek-V3 shape, k = 8: 0.34 -> 0.36 ms; 128 decode tokens with slices:
+// 15 -> 21 us).  k is the top-k of
+// token choice, or E for expert choice (slot e live iff expert e took the
+// token; n_empty, when given, counts the tokens with no live slot).  Rows of
+// y_perm (and y_shared) may be split into `nsplit` fp32 slices `stride`
+// elements apart: each entry's slices are summed in slice order first, then
+// the entries in ascending j order, then the shared row -- the same order in
+// which a reduction of the slices followed by the plain combine adds them.
 // TIN: the rows' storage (fp32, or bf16 for layers that keep them in bf16).
 // round_rows (fp32 split-K slices of a layer whose rows are bf16): each
 // entry's slice sum is rounded to bf16 before it is added, exactly as if the
 // slices had been reduced into a bf16 row first.
-template <typename T, typename TIN>
+
+// One entry's 8 columns at c of row `pos`: its slices summed in slice order,
+// rounded to bf16 when the layer keeps its rows in bf16.
+template <bool SPLIT, typename TIN>
+__device__ __forceinline__ void entry8(const TIN* __restrict__ rows, size_t stride, int nsplit, size_t pos, int d,
+                                       int c, int round_rows, float4& p0, float4& p1) {
+    load8(rows + pos * d + c, p0, p1);
+    if (!SPLIT) return;
+#pragma unroll 8
+    for (int sl = 1; sl < nsplit; ++sl) {  // independent loads: keep them in flight together
+        float4 q0, q1;
+        load8(rows + sl * stride + pos * d + c, q0, q1);
+        add4(p0, q0);
+        add4(p1, q1);
+    }
+    if (round_rows) {
+        p0 = round_bf16(p0);
+        p1 = round_bf16(p1);
+    }
+}
+
+template <typename T, typename TIN, int CH, int NB, bool SPLIT>
 __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, const TIN* __restrict__ y_perm,
                                                       size_t perm_stride, int nsplit,
                                                       const int32_t* __restrict__ slot_pos,
@@ -88,61 +115,68 @@ __global__ void __launch_bounds__(256) combine_kernel(int Tn, int d, int k, cons
                                                       int32_t* __restrict__ n_empty, int round_rows) {
     pdl_wait();
     const int chunks = (d + 255) / 256;
+    const int groups = (chunks + CH - 1) / CH;
     const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (item >= Tn * chunks) return;
-    const int t = item / chunks;
-    const int c = (item - t * chunks) * 256 + lane * 8;
-    const bool active = c < d;  // d is a multiple of 8: an active lane owns 8 columns
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    if (item >= Tn * groups) return;
+    const int t = item / groups;
+    const int g0 = (item - t * groups) * CH;
+    int c[CH];
+    bool act[CH];  // d is a multiple of 8: an active lane owns 8 columns of the chunk
+#pragma unroll
+    for (int h = 0; h < CH; ++h) {
+        c[h] = (g0 + h) * 256 + lane * 8;
+        act[h] = c[h] < d;
+    }
+    float4 acc[CH][2];
+#pragma unroll
+    for (int h = 0; h < CH; ++h) acc[h][0] = acc[h][1] = make_float4(0.f, 0.f, 0.f, 0.f);
     bool any = false;
     for (int j0 = 0; j0 < k; j0 += 32) {  // 32 slots at a time; live ones in ascending j
         const int my_pos = j0 + lane < k ? __ldg(slot_pos + (size_t)t * k + j0 + lane) : -1;
         unsigned live = __ballot_sync(0xffffffffu, my_pos >= 0);
         any |= live != 0u;
-        while (live) {
-            const int j = __ffs(live) - 1;
-            live &= live - 1u;
-            const int pos = __shfl_sync(0xffffffffu, my_pos, j);
-            if (!active) continue;
+        while (live) {  // warp-uniform
+            int pos[NB];
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                pos[u] = -1;
+                if (live) {
+                    pos[u] = __shfl_sync(0xffffffffu, my_pos, __ffs(live) - 1);
+                    live &= live - 1u;
+                }
+            }
+            float4 q[NB][CH][2];
+#pragma unroll
+            for (int u = 0; u < NB; ++u)
+#pragma unroll
+                for (int h = 0; h < CH; ++h)
+                    if (act[h] && pos[u] >= 0)
+                        entry8<SPLIT>(y_perm, perm_stride, nsplit, (size_t)pos[u], d, c[h], round_rows, q[u][h][0],
+                                      q[u][h][1]);
+#pragma unroll
+            for (int u = 0; u < NB; ++u)
+#pragma unroll
+                for (int h = 0; h < CH; ++h)
+                    if (act[h] && pos[u] >= 0) {
+                        add4(acc[h][0], q[u][h][0]);
+                        add4(acc[h][1], q[u][h][1]);
+                    }
+        }
+    }
+    if (n_empty && !any && lane == 0 && g0 == 0) atomicAdd(n_empty, 1);  // a token no expert took
+#pragma unroll
+    for (int h = 0; h < CH; ++h) {
+        if (!act[h]) continue;
+        if (y_shared) {
             float4 p0, p1;
-            load8(y_perm + (size_t)pos * d + c, p0, p1);
-#pragma unroll 8
-            for (int sl = 1; sl < nsplit; ++sl) {  // independent loads: keep them in flight together
-                float4 q0, q1;
-                load8(y_perm + sl * perm_stride + (size_t)pos * d + c, q0, q1);
-                add4(p0, q0);
-                add4(p1, q1);
-            }
-            if (round_rows) {
-                p0 = round_bf16(p0);
-                p1 = round_bf16(p1);
-            }
-            add4(a0, p0);
-            add4(a1, p1);
+            entry8<SPLIT>(y_shared, shared_stride, shared_nsplit, (size_t)t, d, c[h], round_rows, p0, p1);
+            add4(acc[h][0], p0);
+            add4(acc[h][1], p1);
         }
+        store4<T>(y + (size_t)t * d + c[h], acc[h][0]);
+        store4<T>(y + (size_t)t * d + c[h] + 4, acc[h][1]);
     }
-    if (n_empty && !any && lane == 0 && c == 0) atomicAdd(n_empty, 1);  // a token no expert took
-    if (!active) return;
-    if (y_shared) {
-        float4 p0, p1;
-        load8(y_shared + (size_t)t * d + c, p0, p1);
-#pragma unroll 8
-        for (int sl = 1; sl < shared_nsplit; ++sl) {
-            float4 q0, q1;
-            load8(y_shared + sl * shared_stride + (size_t)t * d + c, q0, q1);
-            add4(p0, q0);
-            add4(p1, q1);
-        }
-        if (round_rows) {
-            p0 = round_bf16(p0);
-            p1 = round_bf16(p1);
-        }
-        add4(a0, p0);
-        add4(a1, p1);
-    }
-    store4<T>(y + (size_t)t * d + c, a0);
-    store4<T>(y + (size_t)t * d + c + 4, a1);
 }
 
 // SwiGLU over split-K partials of the up GEMM: one thread per 4 columns.
@@ -252,20 +286,33 @@ cudaError_t launch_bias_update(int T, int E, int k, const int32_t* counts, float
     return cudaGetLastError();
 }
 
+template <typename T, typename TIN>
+void launch_combine_kernel(int T_, int d, int k, const TIN* y_perm, size_t perm_stride, int nsplit,
+                           const int32_t* slot_pos, const TIN* y_shared, size_t shared_stride, int shared_nsplit,
+                           T* y, int32_t* n_empty, int round_rows, cudaStream_t s) {
+    const int chunks = (d + 255) / 256;
+    const bool split = nsplit > 1 || shared_nsplit > 1 || round_rows;
+    const long long w2 = (long long)T_ * ((chunks + 1) / 2), w1 = (long long)T_ * chunks;
+#define MOE_COMBINE(CH, NB, SP, W)                                                                              \
+    launch_pdl(combine_kernel<T, TIN, CH, NB, SP>, dim3((int)(((W) + 7) / 8)), dim3(256), 0, s, T_, d, k, y_perm, \
+               perm_stride, nsplit, slot_pos, y_shared, shared_stride, shared_nsplit, y, n_empty, round_rows)
+    if (k <= 2 && !split) MOE_COMBINE(2, 2, false, w2);
+    else if (split) MOE_COMBINE(1, 1, true, w1);
+    else MOE_COMBINE(1, 1, false, w1);
+#undef MOE_COMBINE
+}
+
 cudaError_t launch_combine_split(int dtype, int T, int d, int k, const float* y_perm, size_t perm_stride,
                                  int nsplit, const int32_t* slot_pos, const float* y_shared, size_t shared_stride,
                                  int shared_nsplit, void* y, cudaStream_t s, int32_t* n_empty, bool round_rows) {
     if (T == 0) return cudaSuccess;
-    const long long warps = (long long)T * ((d + 255) / 256);
-    const int grid = (int)((warps + 7) / 8);
     const int rr = round_rows ? 1 : 0;
     if (dtype == MOE_BF16)
-        launch_pdl(combine_kernel<__nv_bfloat16, float>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride,
-                   nsplit, slot_pos, y_shared, shared_stride, shared_nsplit, static_cast<__nv_bfloat16*>(y), n_empty,
-                   rr);
+        launch_combine_kernel(T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared, shared_stride, shared_nsplit,
+                              static_cast<__nv_bfloat16*>(y), n_empty, rr, s);
     else
-        launch_pdl(combine_kernel<float, float>, dim3(grid), dim3(256), 0, s, T, d, k, y_perm, perm_stride, nsplit,
-                   slot_pos, y_shared, shared_stride, shared_nsplit, static_cast<float*>(y), n_empty, rr);
+        launch_combine_kernel(T, d, k, y_perm, perm_stride, nsplit, slot_pos, y_shared, shared_stride, shared_nsplit,
+                              static_cast<float*>(y), n_empty, rr, s);
     return cudaGetLastError();
 }
 
@@ -275,16 +322,14 @@ cudaError_t launch_combine(int dtype, int T, int d, int k, const void* y_perm, c
     if (!rows_bf16)
         return launch_combine_split(dtype, T, d, k, static_cast<const float*>(y_perm), 0, 1, slot_pos,
                                     static_cast<const float*>(y_shared), 0, 1, y, s, n_empty, false);
-    const long long warps = (long long)T * ((d + 255) / 256);
-    const int grid = (int)((warps + 7) / 8);
     const __nv_bfloat16* yp = static_cast<const __nv_bfloat16*>(y_perm);
     const __nv_bfloat16* ys = static_cast<const __nv_bfloat16*>(y_shared);
     if (dtype == MOE_BF16)
-        launch_pdl(combine_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(grid), dim3(256), 0, s, T, d, k, yp, (size_t)0, 1,
-                   slot_pos, ys, (size_t)0, 1, static_cast<__nv_bfloat16*>(y), n_empty, 0);
+        launch_combine_kernel(T, d, k, yp, (size_t)0, 1, slot_pos, ys, (size_t)0, 1, static_cast<__nv_bfloat16*>(y),
+                              n_empty, 0, s);
     else
-        launch_pdl(combine_kernel<float, __nv_bfloat16>, dim3(grid), dim3(256), 0, s, T, d, k, yp, (size_t)0, 1,
-                   slot_pos, ys, (size_t)0, 1, static_cast<float*>(y), n_empty, 0);
+        launch_combine_kernel(T, d, k, yp, (size_t)0, 1, slot_pos, ys, (size_t)0, 1, static_cast<float*>(y), n_empty,
+                              0, s);
     return cudaGetLastError();
 }
 

@@ -26,10 +26,8 @@ namespace {
 
 constexpr int kScanThreads = 256;
 constexpr int kScanWarps = kScanThreads / 32;
-// up to this many experts the global counts are summed one warp per expert
-// (each lane's histogram rows in flight at once); the load statistics keep
-// the order moe_load_stats uses (warp columns only up to kWarpColumnMaxE)
-constexpr int kScanWarpCountMaxE = 64;
+// The load statistics keep the order moe_load_stats uses (warp columns only
+// up to kWarpColumnMaxE).
 
 __global__ void __launch_bounds__(kRouterThreads) group_hist_kernel(int Tn, int E, int k, int chunk,
                                                                      const int32_t* __restrict__ ids,
@@ -94,8 +92,13 @@ __device__ void block_exclusive_scan(const int* v, int* out, int n, int* s_warp)
     __syncthreads();
 }
 
+// The statistics block stages the p rows in shared memory (one coalesced
+// pass) when they fit this many floats, then adds each column in row order.
+constexpr int kScanStageFloats = 16384;
+
 struct ScanArgs {
     int T, E, k, chunk, capacity, nblk;
+    int p_stage;  // 1: stage o.p_part ([o.p_nblk][E]) in shared memory for the statistics
     const int32_t* ids;
     const float* gates;
     const int32_t* block_hist;
@@ -113,32 +116,51 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
     int* s_wcnt = s_off + E + 1;           // [kScanWarps][E]
     int* s_warp = s_wcnt + kScanWarps * E; // [kScanWarps + 1]
     float* s_red = reinterpret_cast<float*>(s_warp + kScanWarps + 1);  // [kScanThreads]
+    int* s_pb = reinterpret_cast<int*>(s_red + kScanThreads);           // [kScanWarps][E]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = a.T * a.k;
 
-    // 1. global counts, this block's prefix, capacity cut: one warp per expert
-    // (all its histogram rows in flight at once) for small E, else one thread
-    // per expert
-    if (E <= kScanWarpCountMaxE) {
-        for (int e = warp; e < E; e += kScanWarps) {
+    // 1. global counts, this block's prefix, capacity cut.  Up to kScanThreads
+    // experts: thread t = e + E j (j < cpt) sums column e over rows j, j + cpt,
+    // ..., so consecutive threads read consecutive columns of a row and every
+    // thread keeps 32 rows in flight; the cpt partial sums per column are then
+    // added through shared memory (integers: any order gives the same counts).
+    // More experts: one thread per expert walking all rows.
+    if (E <= kScanThreads) {
+        const int cpt = kScanThreads / E < kScanWarps ? kScanThreads / E : kScanWarps;
+        if ((int)threadIdx.x < cpt * E) {
+            const int e = threadIdx.x % E, j = threadIdx.x / E;
             int tot = 0, before = 0;
-#pragma unroll 4
-            for (int b = lane; b < a.nblk; b += 32) {
-                const int v = __ldg(a.block_hist + (size_t)b * E + e);
-                tot += v;
-                before += b < (int)blockIdx.x ? v : 0;
-            }
-            tot = __reduce_add_sync(0xffffffffu, tot);
-            before = __reduce_add_sync(0xffffffffu, before);
-            if (lane == 0) {
-                s_before[e] = before;
-                s_kept[e] = (a.capacity >= 0 && tot > a.capacity) ? a.capacity : tot;
-                if (blockIdx.x == 0) {
-                    a.o.counts[e] = tot;
-                    a.o.kept[e] = s_kept[e];
+            for (int b0 = j; b0 < a.nblk; b0 += 32 * cpt) {
+                int v[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int b = b0 + u * cpt;
+                    v[u] = b < a.nblk ? __ldg(a.block_hist + (size_t)b * E + e) : 0;
                 }
-                s_wcnt[e] = tot;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    tot += v[u];
+                    before += (b0 + u * cpt < (int)blockIdx.x) ? v[u] : 0;
+                }
             }
+            s_wcnt[j * E + e] = tot;
+            s_pb[j * E + e] = before;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += kScanThreads) {
+            int tot = 0, before = 0;
+            for (int j = 0; j < cpt; ++j) {
+                tot += s_wcnt[j * E + e];
+                before += s_pb[j * E + e];
+            }
+            s_before[e] = before;
+            s_kept[e] = (a.capacity >= 0 && tot > a.capacity) ? a.capacity : tot;
+            if (blockIdx.x == 0) {
+                a.o.counts[e] = tot;
+                a.o.kept[e] = s_kept[e];
+            }
+            s_wcnt[e] = tot;  // scratch: counts for the statistics below (only this thread's column)
         }
     } else {
         for (int e = threadIdx.x; e < E; e += kScanThreads) {
@@ -193,17 +215,28 @@ __global__ void __launch_bounds__(kScanThreads) group_scan_kernel(const ScanArgs
             }
         } else if (a.o.p_part) {
             // load statistics: f = counts/(T k), p = mean softmax row, L = alpha E sum f p
+            float* s_p = reinterpret_cast<float*>(s_pb + kScanWarps * E);  // [p_nblk][E] when staged
+            if (a.p_stage) {
+                const int n = a.o.p_nblk * E;
+#pragma unroll 16
+                for (int i = threadIdx.x; i < n; i += kScanThreads) s_p[i] = __ldg(a.o.p_part + i);
+                __syncthreads();
+            }
             float part = 0.f;
             for (int e = threadIdx.x; e < E; e += kScanThreads) {
                 float ps = 0.f;  // row order, as moe_load_stats sums it; 32 loads in flight
-                for (int b0 = 0; b0 < a.o.p_nblk; b0 += 32) {
-                    float v[32];
+                if (a.p_stage) {
+                    for (int b = 0; b < a.o.p_nblk; ++b) ps += s_p[b * E + e];
+                } else {
+                    for (int b0 = 0; b0 < a.o.p_nblk; b0 += 32) {
+                        float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = b0 + j < a.o.p_nblk ? __ldg(a.o.p_part + (size_t)(b0 + j) * E + e) : 0.f;
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = b0 + j < a.o.p_nblk ? __ldg(a.o.p_part + (size_t)(b0 + j) * E + e) : 0.f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (b0 + j < a.o.p_nblk) ps += v[j];
+                        for (int j = 0; j < 32; ++j)
+                            if (b0 + j < a.o.p_nblk) ps += v[j];
+                    }
                 }
                 const float pm = ps / (float)a.T;
                 const float f = (float)s_wcnt[e] / ((float)a.T * (float)a.k);
@@ -325,10 +358,12 @@ cudaError_t launch_group_scan(int T, int E, int k, int chunk, int capacity, cons
                               cudaStream_t s) {
     const int nblk = (T + chunk - 1) / chunk;
     if (nblk == 0) return cudaSuccess;
-    ScanArgs a{T, E, k, chunk, capacity, nblk, topk_ids, gates, block_hist, o, status};
+    const int p_stage = o.p_part && E > kWarpColumnMaxE && (long long)o.p_nblk * E <= kScanStageFloats ? 1 : 0;
+    ScanArgs a{T, E, k, chunk, capacity, nblk, p_stage, topk_ids, gates, block_hist, o, status};
     const size_t smem = sizeof(int) * ((size_t)3 * E + 1 + (size_t)kScanWarps * E + kScanWarps + 1) +
-                        sizeof(float) * kScanThreads;
-    if (smem > 48 * 1024)  // (at most 46 KB for the largest E the library takes)
+                        sizeof(float) * kScanThreads + sizeof(int) * (size_t)kScanWarps * E +
+                        (p_stage ? sizeof(float) * (size_t)o.p_nblk * E : 0);
+    if (smem > 48 * 1024)  // (at most 78 KB for the largest E the library takes, 64 KB more when staging p)
         cudaFuncSetAttribute(group_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     launch_pdl(group_scan_kernel, dim3(nblk), dim3(kScanThreads), smem, s, a);
     return cudaGetLastError();
