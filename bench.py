@@ -771,6 +771,29 @@ def run_backward(args):
            "gpu_launches": int(launches)}
     if args.train:
         out["train"] = {"forward_train_ms": round(fwd_ms, 4), "backward_saved_ms": round(ms - fwd_ms, 4)}
+    else:
+        # the same gradients from the activations a training forward keeps
+        # (moe_forward_train before each call, outside the bracket): what a
+        # training step's backward costs, without recomputing G and U
+        bsum = 0.0
+        for i in range(args.warmup + args.steps):
+            bw.forward_train(L["x"], y)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            bw(L["x"], dy, 1.0, saved=True)
+            b.record()
+            b.synchronize()
+            if i >= args.warmup:
+                bsum += a.elapsed_time(b)
+        st = bw.device_status()
+        if st != 0:
+            raise moe.MoeError(st, "backward_saved device status")
+        s_ms = bsum / args.steps
+        s_tf = 2.0 * fwd_expert / (s_ms / 1e3) / 1e12
+        out["from_saved_activations"] = {
+            "ms_per_step": round(s_ms, 4), "tokens_per_s": round(w.T / (s_ms / 1e3), 1), "tflops": round(s_tf, 1),
+            "frac_bf16_peak": round(s_tf / peaks["bf16_tflops"], 4),
+            "how": "moe_backward_saved after moe_forward_train, each call bracketed by events"}
     print(json.dumps(out), flush=True)
 
 
