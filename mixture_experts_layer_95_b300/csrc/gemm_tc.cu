@@ -37,6 +37,8 @@
 //    for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -104,7 +106,15 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     // SwiGLU mode: when non-null, the fp32 G and U ([rows][N] each) go here too
     float* out_g[2];
     float* out_u[2];
-    // kGemmSwigluBwd epilogue operands (GemmProblem::bwd_*)
+    // kGemmSwigluBwd epilogue operands (GemmProblem::bwd_*); on CTA pairs G and
+    // U also come in through tmG / tmU (fp32 [rows][N], 32 x 32 boxes, 128-byte swizzle)
+    CUtensorMap tmG[2];
+    CUtensorMap tmU[2];
+    // ... and dG, dU, H go out through tmdG / tmdU / tmH (bf16 rows of bwd_dGU and
+    // bwd_Hb, 32 x 32 boxes, 64-byte swizzle)
+    CUtensorMap tmdG[2];
+    CUtensorMap tmdU[2];
+    CUtensorMap tmH[2];
     const float* bwd_G[2];
     const float* bwd_U[2];
     __nv_bfloat16* bwd_dGU[2];
@@ -123,7 +133,8 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
 
 constexpr int kMaxRing = 6;  // deepest ring of any kernel here (the 2-SM kernel)
 
-struct SmemTail {
+template <int NG>
+struct SmemTailT {
     uint64_t full[kMaxRing];
     uint64_t empty[kMaxRing];
     uint64_t tmem_full[2];
@@ -134,10 +145,15 @@ struct SmemTail {
     int abort_flag;
     int total[2];
     int gbase[2];  // first entry of each problem's groups in the arrays below
-    // per group (both problems back to back; the launcher keeps G0 + G1 <= MAX_GROUPS + 1)
-    int tile_start[MAX_GROUPS + 1];
-    int row0[MAX_GROUPS + 1];
-    int rows[MAX_GROUPS + 1];
+    // per group (both problems back to back; the launcher keeps G0 + G1 <= NG)
+    int tile_start[NG];
+    int row0[NG];
+    int rows[NG];
+    // CTA-pair SwiGLU backward: each epilogue warp's two G/U staging slots
+    uint64_t gu_full[4][2];
+};
+using SmemTailCore = SmemTailT<MAX_GROUPS + 1>;
+struct SmemTail : SmemTailCore {
     // epilogue staging: each epilogue warp transposes 32 rows x 32 fp32 columns
     // so that its global stores are whole 128-byte row segments
     float stage[4][32][33];
@@ -203,7 +219,7 @@ __device__ __forceinline__ void load_kblock_bmn(const TcParams& p, int prob, int
 }
 
 template <int MODE>
-__device__ __forceinline__ Tile decode_tile(const SmemTail& st, const TcParams& p, int id) {
+__device__ __forceinline__ Tile decode_tile(const SmemTailCore& st, const TcParams& p, int id) {
     Tile t;
     t.prob = (id < st.total[0]) ? 0 : 1;
     const int local = id - (t.prob ? st.total[0] : 0);
@@ -286,6 +302,57 @@ __device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& 
         } else {
             for (int i = 0; i < 32 && col + i < lim; ++i) dst[i] = scale * __uint_as_float(v[i]);
         }
+    }
+}
+
+// SwiGLU backward of one row's 32 columns: with a = G, b = U, s = sigmoid(a)
+// and dd = D (the upstream gradient of H), H = a s b, dG = g dd b s (1 + a (1 - s))
+// and dU = g dd a s, packed as bf16 pairs (8 columns per uint4); the gate
+// gradient's partial sum gains dd H over the first nc (<= 32) columns.
+__device__ __forceinline__ void swiglu_bwd_pack(const float (&ga)[32], const float (&ub)[32], const uint32_t (&v)[32],
+                                                int nc, float g, uint4 (&pg)[4], uint4 (&pu)[4], uint4 (&ph)[4],
+                                                float& part) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float dG[8], dU[8], hh[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float a = ga[8 * q + i], b = ub[8 * q + i];
+            const float dd = __uint_as_float(v[8 * q + i]);
+            const float sg = 1.0f / (1.0f + __expf(-a));
+            hh[i] = a * sg * b;
+            if (8 * q + i < nc) part += dd * hh[i];
+            const float dh = g * dd;
+            dG[i] = dh * b * sg * (1.0f + a * (1.0f - sg));
+            dU[i] = dh * a * sg;
+        }
+        uint32_t* wg = reinterpret_cast<uint32_t*>(&pg[q]);
+        uint32_t* wu = reinterpret_cast<uint32_t*>(&pu[q]);
+        uint32_t* wh = reinterpret_cast<uint32_t*>(&ph[q]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 x = __floats2bfloat162_rn(dG[2 * i], dG[2 * i + 1]);
+            __nv_bfloat162 y = __floats2bfloat162_rn(dU[2 * i], dU[2 * i + 1]);
+            __nv_bfloat162 z = __floats2bfloat162_rn(hh[2 * i], hh[2 * i + 1]);
+            wg[i] = *reinterpret_cast<uint32_t*>(&x);
+            wu[i] = *reinterpret_cast<uint32_t*>(&y);
+            wh[i] = *reinterpret_cast<uint32_t*>(&z);
+        }
+    }
+}
+
+// The first nc (<= 32) of 32 packed bf16 values to out (16-byte aligned when nc == 32).
+__device__ __forceinline__ void store_bf16_row(const uint4 (&w)[4], int nc, __nv_bfloat16* out) {
+    if (nc == 32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(out)[q] = w[q];
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        if (i >= nc) break;
+        const uint32_t word = (&w[i >> 3].x)[(i & 7) >> 1];
+        out[i] = __ushort_as_bfloat16(static_cast<unsigned short>((i & 1) ? word >> 16 : word & 0xffffu));
     }
 }
 
@@ -430,46 +497,11 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             if (c0 + 32 < BN) load_gu(col + 32, gn, un);
             if (valid && col < N) {
                 const int nc = min(32, N - col);
-#pragma unroll
-                for (int q = 0; q < 32; q += 8) {
-                    if (q >= nc) continue;  // (fully unrolled: v, ga, ub are indexed with constants only)
-                    float dG[8], dU[8], hh[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float a = ga[q + i], b = ub[q + i];
-                        const float dd = __uint_as_float(v[q + i]);
-                        const float sg = 1.0f / (1.0f + __expf(-a));
-                        hh[i] = a * sg * b;
-                        if (q + i < nc) part += dd * hh[i];
-                        const float dh = g * dd;
-                        dG[i] = dh * b * sg * (1.0f + a * (1.0f - sg));
-                        dU[i] = dh * a * sg;
-                    }
-                    if (q + 8 <= nc) {
-                        uint4 pg, pu, ph;
-                        uint32_t* wg = reinterpret_cast<uint32_t*>(&pg);
-                        uint32_t* wu = reinterpret_cast<uint32_t*>(&pu);
-                        uint32_t* wh = reinterpret_cast<uint32_t*>(&ph);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            __nv_bfloat162 x = __floats2bfloat162_rn(dG[2 * i], dG[2 * i + 1]);
-                            __nv_bfloat162 y = __floats2bfloat162_rn(dU[2 * i], dU[2 * i + 1]);
-                            __nv_bfloat162 z = __floats2bfloat162_rn(hh[2 * i], hh[2 * i + 1]);
-                            wg[i] = *reinterpret_cast<uint32_t*>(&x);
-                            wu[i] = *reinterpret_cast<uint32_t*>(&y);
-                            wh[i] = *reinterpret_cast<uint32_t*>(&z);
-                        }
-                        *reinterpret_cast<uint4*>(dGr + col + q) = pg;
-                        *reinterpret_cast<uint4*>(dGr + N + col + q) = pu;
-                        *reinterpret_cast<uint4*>(Hr + col + q) = ph;
-                    } else {
-                        for (int i = 0; i < 8 && q + i < nc; ++i) {
-                            dGr[col + q + i] = __float2bfloat16_rn(dG[i]);
-                            dGr[N + col + q + i] = __float2bfloat16_rn(dU[i]);
-                            Hr[col + q + i] = __float2bfloat16_rn(hh[i]);
-                        }
-                    }
-                }
+                uint4 pg[4], pu[4], ph[4];
+                swiglu_bwd_pack(ga, ub, v, nc, g, pg, pu, ph, part);
+                store_bf16_row(pg, nc, dGr + col);
+                store_bf16_row(pu, nc, dGr + N + col);
+                store_bf16_row(ph, nc, Hr + col);
             }
             if (c0 + 32 < BN) {
 #pragma unroll
@@ -865,10 +897,35 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
 // the leader's stage barrier, MMA completion is multicast to both CTAs, and
 // both CTAs' epilogue warps release the accumulator on the leader's barrier.
 
-constexpr int PAIR_STAGES = kMaxRing;
 constexpr int PAIR_STAGE_BYTES = A_BYTES + B_BYTES / 2;  // this CTA's 128 rows of A + half of B
-
-constexpr size_t pair_smem_bytes() { return 1024 + (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + sizeof(SmemTail); }
+// The SwiGLU backward's epilogue reads two fp32 tensors (G, U) and writes
+// three bf16 ones (dG, dU, H), each as large as its output: its ring keeps 4
+// stages, and the freed shared memory stages those tiles for TMA (each
+// epilogue warp: 2 slots of a 32 x 32 G box and a 32 x 32 U box, and one
+// 32 x 32 box of each output, with 64-byte swizzle); the fp32 transpose
+// buffer of the other epilogues is left out.
+constexpr int GU_SLOT_BYTES = 32 * 32 * 4;
+constexpr int GU_BYTES = 4 * 2 * 2 * GU_SLOT_BYTES;  // 4 warps x 2 slots x (G, U)
+constexpr int OUT_BOX_BYTES = 32 * 32 * 2;
+constexpr int OUT_BYTES = 4 * 3 * OUT_BOX_BYTES;  // 4 warps x (dG, dU, H)
+// groups of both problems the CTA-pair SwiGLU backward takes (its shared
+// memory holds no more); the launcher runs larger ones on single CTAs
+constexpr int kPairBwdGroups = 512;
+template <int MODE>
+using PairTail =
+    typename std::conditional<MODE == kGemmSwigluBwd, SmemTailT<kPairBwdGroups + 1>, SmemTail>::type;
+template <int MODE>
+constexpr int pair_stages() {
+    return MODE == kGemmSwigluBwd ? 4 : kMaxRing;
+}
+template <int MODE>
+constexpr size_t pair_gu_bytes() {
+    return MODE == kGemmSwigluBwd ? (size_t)(GU_BYTES + OUT_BYTES) : 0;
+}
+template <int MODE>
+constexpr size_t pair_smem_bytes() {
+    return 1024 + (size_t)pair_stages<MODE>() * PAIR_STAGE_BYTES + pair_gu_bytes<MODE>() + sizeof(PairTail<MODE>);
+}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -927,8 +984,8 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
 }
 
 // Pair tile: 256 rows of one group (128 per CTA) x 256 accumulator columns.
-template <int MODE>
-__device__ __forceinline__ Tile decode_tile_pair(const SmemTail& st, const TcParams& p, int id, int rank) {
+template <int MODE, class TailT>
+__device__ __forceinline__ Tile decode_tile_pair(const TailT& st, const TcParams& p, int id, int rank) {
     Tile t;
     t.prob = (id < st.total[0]) ? 0 : 1;
     const int local = id - (t.prob ? st.total[0] : 0);
@@ -970,8 +1027,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_pair_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int NST = PAIR_STAGES;
-    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)NST * PAIR_STAGE_BYTES);
+    constexpr int NST = pair_stages<MODE>();
+    uint8_t* gu_stage = smem + (size_t)NST * PAIR_STAGE_BYTES;  // 1024-aligned (stages are 32 KB)
+    PairTail<MODE>& st = *reinterpret_cast<PairTail<MODE>*>(gu_stage + pair_gu_bytes<MODE>());
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)cluster_rank();
     const bool leader = rank == 0;
@@ -987,6 +1045,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&st.tmem_full[a], 1);
             mbar_init(&st.tmem_empty[a], 8);  // leader: 4 epilogue warps in each CTA
         }
+        for (int w = 0; w < 4; ++w)
+            for (int sl = 0; sl < 2; ++sl) mbar_init(&st.gu_full[w][sl], 1);
         st.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -995,6 +1055,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             prefetch_tmap(&p.tmA[q]);
             prefetch_tmap(&p.tmB1[q]);
             if (MODE == kGemmSwiGLU) prefetch_tmap(&p.tmB2[q]);
+            if (MODE == kGemmSwigluBwd) {
+                prefetch_tmap(&p.tmG[q]);
+                prefetch_tmap(&p.tmU[q]);
+                prefetch_tmap(&p.tmdG[q]);
+                prefetch_tmap(&p.tmdU[q]);
+                prefetch_tmap(&p.tmH[q]);
+            }
         }
     }
     if (warp == 1) {  // both CTAs of the pair allocate together
@@ -1151,6 +1218,115 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 umma_commit_pair(&st.tmem_full[acc]);
             }
         }
+    } else if constexpr (MODE == kGemmSwigluBwd) {
+        // SwiGLU backward.  G and U of this warp's 32 rows come in by TMA, 32
+        // columns per box, into two slots per tensor: the next chunk's loads
+        // are in flight while one is computed, and a tile's first two chunks
+        // are requested before its accumulator is ready.  dG, dU and H leave
+        // through one 32 x 32 box each, stored by TMA, when all 32 rows of the
+        // warp belong to the tile's group (a box must not spill into the next
+        // group's rows); otherwise each thread stores its own row.
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // full 128-row tiles: TMEM lane = tile row
+        float* gu = reinterpret_cast<float*>(gu_stage) + quarter * (GU_BYTES / 4 / 4);  // [slot][G | U][32][32]
+        uint8_t* ob = gu_stage + GU_BYTES + quarter * (3 * OUT_BOX_BYTES);             // [dG | dU | H][32][64 B]
+        uint64_t* gbar = st.gu_full[quarter];
+        // 16-byte chunk j of this lane's output row, 64-byte swizzle
+        const int o_row = lane * 64, o_sw = (lane >> 1) & 3;
+        uint32_t seq = 0;  // chunks this warp has requested before the current tile
+        int it = 0;
+        bool ok = true;
+        for (int id = cluster_id; ok && id < total_tiles; id += nclusters, ++it) {
+            const Tile t = decode_tile_pair<MODE>(st, p, id, rank);
+            const int r0 = t.out_row0 + quarter * 32;
+            auto request = [&](int c) {  // chunk c of this tile into slot (seq + c) & 1
+                if (lane == 0) {
+                    const uint32_t slot = (seq + c) & 1u;
+                    float* dst = gu + slot * (2 * 32 * 32);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(&gbar[slot], 2 * GU_SLOT_BYTES);
+                    tma_load_2d(dst, &p.tmG[t.prob], t.n * BN + c * 32, r0, &gbar[slot]);
+                    tma_load_2d(dst + 32 * 32, &p.tmU[t.prob], t.n * BN + c * 32, r0, &gbar[slot]);
+                }
+            };
+            request(0);
+            request(1);
+            const int acc = it & 1;
+            const uint32_t use = static_cast<uint32_t>(it >> 1);
+            if (!mbar_wait(&st.tmem_full[acc], use & 1u, abort_flag, p.status, p.wait_limit_ns)) break;
+            tc_fence_after();
+            const uint32_t tacc =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            const int N = p.N[t.prob];
+            const bool valid = row < t.rows_valid;
+            const bool box_rows = t.rows_valid - quarter * 32 >= 32;  // (uniform across the warp)
+            const size_t grow = static_cast<size_t>(t.out_row0 + row);
+            const float g = (valid && p.row_scale[t.prob]) ? __ldg(p.row_scale[t.prob] + grow) : 1.0f;
+            __nv_bfloat16* dGr = p.bwd_dGU[t.prob] + grow * 2 * N;
+            __nv_bfloat16* Hr = p.bwd_Hb[t.prob] + grow * N;
+            float part = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                __syncwarp();
+                tmem_ld32(tacc + c * 32, v);
+                tmem_ld_wait();
+                const uint32_t slot = (seq + c) & 1u;
+                if (!mbar_wait(&gbar[slot], ((seq + c) >> 1) & 1u, abort_flag, p.status, p.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                // box row `lane`: 16-byte chunk j sits at chunk j ^ (lane & 7) of its 128-byte row
+                const float* gs = gu + slot * (2 * 32 * 32) + lane * 32;
+                float ga[32], ub[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int o = (j ^ (lane & 7)) * 4;
+                    const float4 a4 = *reinterpret_cast<const float4*>(gs + o);
+                    const float4 b4 = *reinterpret_cast<const float4*>(gs + 32 * 32 + o);
+                    ga[4 * j] = a4.x, ga[4 * j + 1] = a4.y, ga[4 * j + 2] = a4.z, ga[4 * j + 3] = a4.w;
+                    ub[4 * j] = b4.x, ub[4 * j + 1] = b4.y, ub[4 * j + 2] = b4.z, ub[4 * j + 3] = b4.w;
+                }
+                __syncwarp();  // every lane has read the slot before it is requested again
+                if (c + 2 < BN / 32) request(c + 2);
+                const int col = t.n * BN + c * 32;
+                if (col >= N) continue;  // (uniform across the warp)
+                const int nc = min(32, N - col);
+                uint4 pg[4], pu[4], ph[4];
+                if (box_rows) {
+                    swiglu_bwd_pack(ga, ub, v, nc, g, pg, pu, ph, part);
+                    if (lane == 0) bulk_wait_read<0>();  // the previous boxes have left shared memory
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int o = o_row + ((j ^ o_sw) << 4);
+                        *reinterpret_cast<uint4*>(ob + o) = pg[j];
+                        *reinterpret_cast<uint4*>(ob + OUT_BOX_BYTES + o) = pu[j];
+                        *reinterpret_cast<uint4*>(ob + 2 * OUT_BOX_BYTES + o) = ph[j];
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {  // columns past N are clipped by the tensor maps
+                        tma_store_2d(&p.tmdG[t.prob], col, r0, ob);
+                        tma_store_2d(&p.tmdU[t.prob], col, r0, ob + OUT_BOX_BYTES);
+                        tma_store_2d(&p.tmH[t.prob], col, r0, ob + 2 * OUT_BOX_BYTES);
+                        bulk_commit();
+                    }
+                } else if (valid) {
+                    swiglu_bwd_pack(ga, ub, v, nc, g, pg, pu, ph, part);
+                    store_bf16_row(pg, nc, dGr + col);
+                    store_bf16_row(pu, nc, dGr + N + col);
+                    store_bf16_row(ph, nc, Hr + col);
+                }
+            }
+            if (!ok) break;
+            seq += BN / 32;
+            if (valid && p.bwd_dgp_part[t.prob]) p.bwd_dgp_part[t.prob][(size_t)t.n * p.bwd_dgp_ld[t.prob] + grow] = part;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_addr(&st.tmem_empty[acc]));
+        }
+        if (lane == 0) bulk_wait<0>();  // every box is written before the CTA leaves
     } else {
         const int quarter = warp & 3;
         const int row_in_tile = quarter * 32 + lane;
@@ -1214,6 +1390,9 @@ cudaError_t launch_mode(const TcParams& prm, int grid, cudaStream_t s) {
 
 static_assert(smem_bytes<kGemmSwiGLU, true>() <= 232448, "FP8 SwiGLU kernel exceeds shared memory");
 static_assert(smem_bytes<kGemmScale, true>() <= 232448, "FP8 Scale kernel exceeds shared memory");
+static_assert(pair_smem_bytes<kGemmSwiGLU>() <= 232448 && pair_smem_bytes<kGemmScale>() <= 232448 &&
+                  pair_smem_bytes<kGemmSwigluBwd>() <= 232448,
+              "CTA-pair kernel exceeds shared memory");
 
 template <int MODE>
 cudaError_t launch_pair_mode(const TcParams& prm, int num_sms, cudaStream_t s) {
@@ -1225,13 +1404,13 @@ cudaError_t launch_pair_mode(const TcParams& prm, int num_sms, cudaStream_t s) {
     if (!bit || !(attr_set_mask & bit)) {
         cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_pair_kernel<MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(pair_smem_bytes()));
+                                             static_cast<int>(pair_smem_bytes<MODE>()));
         if (e != cudaSuccess) return e;
         // persistent grid: only as many pairs as can be resident at once
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (num_sms / 2));
         cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = pair_smem_bytes();
+        cfg.dynamicSmemBytes = pair_smem_bytes<MODE>();
         int nc = 0;
         e = cudaOccupancyMaxActiveClusters(&nc, grouped_gemm_tc_pair_kernel<MODE>, &cfg);
         if (e != cudaSuccess || nc < 1) return e != cudaSuccess ? e : cudaErrorLaunchOutOfResources;
@@ -1240,7 +1419,7 @@ cudaError_t launch_pair_mode(const TcParams& prm, int num_sms, cudaStream_t s) {
     }
     const int nc = dev < 64 ? max_clusters[dev] : 1;
     const int clusters = nc < num_sms / 2 ? nc : num_sms / 2;
-    launch_pdl(grouped_gemm_tc_pair_kernel<MODE>, dim3(2 * clusters), dim3(NUM_THREADS), pair_smem_bytes(), s, prm);
+    launch_pdl(grouped_gemm_tc_pair_kernel<MODE>, dim3(2 * clusters), dim3(NUM_THREADS), pair_smem_bytes<MODE>(), s, prm);
     return cudaGetLastError();
 }
 
@@ -1255,6 +1434,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     // rows of B per TMA box: half the tile for SwiGLU (the W1 / W3 halves) and,
     // in either mode, on a CTA pair (each CTA holds half of the N columns)
     // (SwiGLU on CTA pairs: two 64-row boxes per CTA, W1 and W3 of the same features)
+    if (pair && mode == kGemmSwigluBwd && probs[0].G + (nprob > 1 ? probs[1].G : 0) > kPairBwdGroups + 1) pair = false;
     const int b_box = (mode == kGemmSwiGLU && pair) ? BN / 4 : (mode == kGemmSwiGLU || pair) ? BN / 2 : BN;
     if (probs[0].G + (nprob > 1 ? probs[1].G : 0) > MAX_GROUPS + 1) return cudaErrorInvalidValue;
     for (int q = 0; q < nprob; ++q) {
@@ -1311,6 +1491,19 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
             prm.bwd_Hb[q] = static_cast<__nv_bfloat16*>(g.bwd_Hb);
             prm.bwd_dgp_part[q] = g.bwd_dgp_part;
             prm.bwd_dgp_ld[q] = g.bwd_dgp_ld;
+            if (pair) {
+                // N % 8 == 0: every row stride and dU's column offset are multiples of 16 bytes
+                const uint64_t N = (uint64_t)g.N;
+                __nv_bfloat16* dGU = static_cast<__nv_bfloat16*>(g.bwd_dGU);
+                if ((reinterpret_cast<uintptr_t>(g.bwd_G) | reinterpret_cast<uintptr_t>(g.bwd_U) |
+                     reinterpret_cast<uintptr_t>(g.bwd_dGU) | reinterpret_cast<uintptr_t>(g.bwd_Hb)) % 16 != 0 ||
+                    !make_tmap_f32(&prm.tmG[q], g.bwd_G, g.a_rows, g.N) ||
+                    !make_tmap_f32(&prm.tmU[q], g.bwd_U, g.a_rows, g.N) ||
+                    !make_tmap_bf16_box32(&prm.tmdG[q], dGU, g.a_rows, g.N, 4 * N) ||
+                    !make_tmap_bf16_box32(&prm.tmdU[q], dGU + N, g.a_rows, g.N, 4 * N) ||
+                    !make_tmap_bf16_box32(&prm.tmH[q], g.bwd_Hb, g.a_rows, g.N, 2 * N))
+                    return cudaErrorInvalidValue;
+            }
         }
         if (g.out_g || g.out_u) {
             if (mode != kGemmSwiGLU || !g.out_g || !g.out_u || ksplit != 1 || g.N % 4 != 0) return cudaErrorInvalidValue;

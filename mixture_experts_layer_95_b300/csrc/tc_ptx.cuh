@@ -86,6 +86,26 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, in
         : "memory");
 }
 
+// Shared -> global tensor store of one box at (c0, c1); elements outside the
+// tensor's extent are not written.  Completion is tracked per thread in bulk
+// groups: bulk_commit() closes a group, bulk_wait_read<n>() waits until at most
+// n groups still read shared memory, bulk_wait<n>() until their writes are done.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int c0, int c1, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Four rows (r0..r3) x 64 columns starting at column c0 of a 2-D tensor whose
 // map has a one-row box; lands in shared memory as four consecutive 128-byte
 // rows, swizzled like a tiled load to the same address.
@@ -351,6 +371,27 @@ inline bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t d0, uint64_
     const cuuint64_t strides[2] = {s1, s2};
     const cuuint32_t box[3] = {b0, b1, b2};
     return encode_cached(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// 2-D fp32 tensor [rows][cols] (cols contiguous, a multiple of 4), box = 32
+// columns (128 bytes) x 32 rows, 128-byte swizzle: 16-byte chunk j of box row r
+// lands at r * 128 + ((j ^ (r & 7)) << 4) of a 1024-byte-aligned destination.
+inline bool make_tmap_f32(CUtensorMap* tm, const void* base, int rows, int cols) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    return encode_cached(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// 2-D bf16 tensor of `cols` columns per row, rows `row_bytes` apart (a multiple
+// of 16), box = 32 columns (64 bytes) x 32 rows, 64-byte swizzle: 16-byte chunk
+// j of box row r sits at r * 64 + ((j ^ ((r >> 1) & 3)) << 4) of a
+// 512-byte-aligned shared buffer.
+inline bool make_tmap_bf16_box32(CUtensorMap* tm, const void* base, int rows, int cols, uint64_t row_bytes) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {32, 32};
+    return encode_cached(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // 2-D one-byte (FP8 code) tensor [rows][K], box = box_cols x box_rows.  No
