@@ -319,7 +319,7 @@ __device__ __forceinline__ void swiglu_bwd_pack(const float (&ga)[32], const flo
         for (int i = 0; i < 8; ++i) {
             const float a = ga[8 * q + i], b = ub[8 * q + i];
             const float dd = __uint_as_float(v[8 * q + i]);
-            const float sg = 1.0f / (1.0f + __expf(-a));
+            const float sg = __fdividef(1.0f, 1.0f + __expf(-a));  // (0 once exp(-a) passes 2^126)
             hh[i] = a * sg * b;
             if (8 * q + i < nc) part += dd * hh[i];
             const float dh = g * dd;
