@@ -32,7 +32,7 @@
 //    warps' partial dots in a fixed order and writes
 //    H[entry][f] = silu(x W1^T) * (x W3^T) in bf16 (and H_shared).
 //  * fused_down_kernel: a CTA owns a block of output channels r and streams
-//    W2[e][r] for every touched expert e (expert by expert; one or two rows a
+//    W2[e][r] for every touched expert e (expert by expert; up to four rows a
 //    stage), the lanes holding the expert's H values at their positions; it
 //    then adds the warps' slices, the row scale (FP8) and the gates in a
 //    fixed order and writes y: no Y_perm and no combine launch.
@@ -67,6 +67,7 @@ constexpr int kFW = 16;  // consumer warps per CTA, both kernels (warp kFW is th
 constexpr int kFThreads = 32 * kFW;
 constexpr int kFThreadsP = kFThreads + 32;
 constexpr int kFMaxStages = 16;
+constexpr int kDnMaxRows = 4;    // W2 rows of one down-kernel stage, at most
 // dynamic shared memory of either kernel, at most (the static part -- routing,
 // barriers -- stays under 5 KB of the 227 KB a CTA may hold)
 constexpr size_t kFSmemBudget = 216 * 1024;
@@ -228,7 +229,8 @@ __device__ void fused_stats(const FusedDecodeArgs& a, const FusedRoute& r) {
 // ---------------------------------------------------------------- the rings
 // One CTA-wide ring of shared-memory stages per kernel.  Warp kFW (the
 // producer) fills each stage with one or two 1-D bulk copies of whole weight
-// rows, up to 32 KB each: measured, the copies' cost is per copy (2-4 KB
+// rows, up to 32 KB each (64 KB for the down kernel's single copy): measured,
+// the copies' cost is per copy (2-4 KB
 // copies held an SM to ~7 million a second; one row of a 4096-wide bf16
 // matrix per stage instead of two ran the up kernel 1.5x slower).  The kFW
 // consumer warps each read their own slice of every stage and release it on
@@ -577,8 +579,8 @@ __global__ void __launch_bounds__(kFThreadsP, 1)
 // ---------------------------------------------------------------- down kernel
 
 // The down kernel's work list for one CTA's output channels r0..r1: expert
-// slot es (n_exp: the shared expert), then channels, dn_rows_stage (1 or 2)
-// whole consecutive W2 rows per stage (one bulk copy).  Consumer warp w takes
+// slot es (n_exp: the shared expert), then channels, dn_rows_stage (1 to
+// kDnMaxRows) whole consecutive W2 rows per stage (one bulk copy).  Consumer warp w takes
 // slice [w cs, w cs + cs) of every row, its lanes the same positions in each,
 // so the expert's tokens' H values there are loaded into registers once per
 // expert.
@@ -668,31 +670,32 @@ __global__ void __launch_bounds__(kFThreadsP, 1)
             }
             if (!mbar_wait(&g.full[s], ph, &g.abort_flag, a.status, wait_ns)) break;
             const int rows = nr - row < R2 ? nr - row : R2;
-            float acc[2][NT][PV];  // [row of the stage][token][vector]
+            float acc[kDnMaxRows][NT][PV];  // [row of the stage][token][vector]
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj)
+            for (int jj = 0; jj < kDnMaxRows; ++jj)
 #pragma unroll
                 for (int i = 0; i < NT; ++i)
 #pragma unroll
                     for (int v = 0; v < PV; ++v) acc[jj][i][v] = 0.f;
             if (nvec > 0) {
                 const uint8_t* st = ring + (size_t)s * stage_bytes + (size_t)a0 * WB;
-                slice_dots<W8, NT, PV>(st, nvec, h, ntok, acc[0]);
-                if (rows > 1) slice_dots<W8, NT, PV>(st + (size_t)Fe * WB, nvec, h, ntok, acc[1]);
+#pragma unroll
+                for (int jj = 0; jj < kDnMaxRows; ++jj)
+                    if (jj < rows) slice_dots<W8, NT, PV>(st + (size_t)jj * Fe * WB, nvec, h, ntok, acc[jj]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&g.empty[s]);
-            float vals[2 * NT];  // (row, token) dots
+            float vals[kDnMaxRows * NT];  // (row, token) dots
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj)
+            for (int jj = 0; jj < kDnMaxRows; ++jj)
 #pragma unroll
                 for (int i = 0; i < NT; ++i) {
                     vals[jj * NT + i] = 0.f;
 #pragma unroll
                     for (int v = 0; v < PV; ++v) vals[jj * NT + i] += acc[jj][i][v];
                 }
-            const float tot = warp_sum_multi<2 * NT>(vals);
-            constexpr int kPer = 32 / (2 * NT);  // lanes per value
+            const float tot = warp_sum_multi<kDnMaxRows * NT>(vals);
+            constexpr int kPer = 32 / (kDnMaxRows * NT);  // lanes per value
             const int vi = lane / kPer, jj = vi / NT, ti = vi % NT;
             if (lane % kPer == 0 && jj < rows && ti < ntok) part[((size_t)warp * nr + row + jj) * ncols + col0 + ti] = tot;
             row += R2;
@@ -794,7 +797,8 @@ FusedPlan fused_decode_plan(const moe_config& c, bool fp8, int sms) {
     if (sms < 1) return p;
     const int wb = fp8 ? 1 : 2, ve = fp8 ? 16 : 8;  // bytes per weight; elements per 16-byte vector
     const int T = c.T;
-    const int kCopy = 32768;                       // bytes of one bulk copy, at most (unless one row is longer)
+    // bytes of one bulk copy (one stage), at most, unless one row is longer
+    const int kCopyUp = 32768, kCopyDn = 65536;
     // activation vectors per lane for a warp slice: 2 or 4, within kLaneWords registers
     auto pv_of = [&](int slice) {
         const int v = (slice + 32 * ve - 1) / (32 * ve);
@@ -806,7 +810,7 @@ FusedPlan fused_decode_plan(const moe_config& c, bool fp8, int sms) {
     // rows of W1 and of W3
     auto wslice = [&](int rows) { return round_up((c.d + kFW / rows - 1) / (kFW / rows), ve); };
     p.up_rows = 1;
-    while (p.up_rows * 2 <= kFW && (long long)p.up_rows * 2 * c.d * wb <= kCopy && pv_of(wslice(p.up_rows * 2)))
+    while (p.up_rows * 2 <= kFW && (long long)p.up_rows * 2 * c.d * wb <= kCopyUp && pv_of(wslice(p.up_rows * 2)))
         p.up_rows *= 2;
     p.up_wslice = wslice(p.up_rows);
     p.up_pv = pv_of(p.up_wslice);
@@ -831,7 +835,9 @@ FusedPlan fused_decode_plan(const moe_config& c, bool fp8, int sms) {
     p.dn_pv = pv_of(p.dn_wslice > p.dn_wslice_s ? p.dn_wslice : p.dn_wslice_s);
     if (!p.dn_pv) return p;
     const int fmax = c.n_shared && c.d_ff_shared > c.d_ff ? c.d_ff_shared : c.d_ff;
-    p.dn_rows_stage = (long long)2 * fmax * wb <= kCopy ? 2 : 1;
+    p.dn_rows_stage = 1;
+    while (p.dn_rows_stage * 2 <= kDnMaxRows && (long long)p.dn_rows_stage * 2 * fmax * wb <= kCopyDn)
+        p.dn_rows_stage *= 2;
     p.dn_stage_bytes = align128((size_t)p.dn_rows_stage * fmax * wb);
     p.grid_dn = sms < c.d ? sms : c.d;
     p.dn_rows = (c.d + p.grid_dn - 1) / p.grid_dn;
