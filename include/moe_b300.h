@@ -309,8 +309,11 @@ MOE_API int moe_forward(const moe_config *cfg, const void *x, const void *w_gate
  * the decode-time bound) and apply scale_r to the fp32 accumulator of output
  * channel r.  Prefill-sized batches widen the codes exactly to bf16 in shared
  * memory (bf16 x bf16 MMAs).  Batches the two fused small-batch kernels take
- * (see moe_forward) widen the codes exactly to fp32 on the CUDA cores, against
- * bf16 x and H.  Other decode-sized batches (at most 32 rows per touched
+ * (see moe_forward) convert the codes exactly to f16 on the CUDA cores and
+ * multiply them by x and H held as f16, each warp's slice of a row scaled by
+ * a power of two that puts its largest magnitude in [0.5, 1): the 16 products
+ * of each 16-code vector are summed as two f16 partial sums of eight, which
+ * then join an fp32 accumulator.  Other decode-sized batches (at most 32 rows per touched
  * expert on average) feed the codes to the FP8 tensor cores as they are; that MMA takes FP8 on both sides, so every bf16 row of x and of H is
  * first split into two E4M3 code rows and a power-of-two scale,
  * row = s (hi + lo), which reproduces every entry within a factor 2^10 of the

@@ -26,7 +26,8 @@
 //    registers: shared memory carries each weight byte once and nothing else.
 //    The dots run on the CUDA cores with fp32 accumulation (at one token the
 //    MMA's N side would be padding): bf16 weights through mixed-precision
-//    bf16 FMAs, E4M3 codes widened exactly to fp32.
+//    bf16 FMAs; E4M3 codes converted exactly to f16 pairs and multiplied by
+//    f16 activation pairs, 16 products summed in f16 before they join fp32.
 //  * fused_up_kernel: a stage is up_rows consecutive hidden features of one
 //    touched expert (their W1 rows and W3 rows, two copies); the CTA sums its
 //    warps' partial dots in a fixed order and writes
@@ -268,9 +269,11 @@ __device__ __forceinline__ void ring_drain(Ring& g, int S, int issued) {
 // of its warp's slice), so the x (or H) values those meet are loaded once
 // per token (per expert, in the down kernel) and shared memory carries
 // only the weights -- one read of each byte.  Against bf16 weights they stay
-// bf16 pairs, multiplied by mixed-precision FMAs; against E4M3 codes they are
-// fp32 and the codes are widened.  A lane holds PV (2 or 4) vectors per
-// token, at most kLaneWords registers.
+// bf16 pairs, multiplied by mixed-precision FMAs; against E4M3 codes they
+// become f16 pairs scaled by a power of two per warp slice (the slice's
+// largest magnitude lands in [0.5, 1)), multiplied with the codes as f16
+// pairs.  A lane holds PV (2 or 4) vectors per token, at most kLaneWords
+// registers.
 constexpr int kLaneWords = 64;
 
 // acc += a.lo b.lo, then + a.hi b.hi: mixed-precision FMAs on bf16 operands
@@ -286,29 +289,20 @@ __device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float acc) {
         : "r"(a), "r"(b));
     return acc;
 }
-// 16 E4M3 codes -> 16 floats, exactly (E4M3 values are f16 values).
-__device__ __forceinline__ void widen_e4m3x16(const uint4& u, float (&v)[16]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const __half2_raw hr =
-                __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * h)), __NV_E4M3);
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            v[4 * i + 2 * h] = f.x;
-            v[4 * i + 2 * h + 1] = f.y;
-        }
-    }
+
+// Two E4M3 codes (the low 16 bits) -> an f16 pair, exactly (E4M3 values are f16 values).
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+    return *reinterpret_cast<const __half2*>(&hr);
 }
 
 // Activation registers per 16-byte weight vector: 4 bf16 pairs against bf16
-// weights, 16 floats against E4M3 codes.
+// weights, 8 f16 pairs against E4M3 codes.
 template <bool W8>
-using act_t = std::conditional_t<W8, float, uint32_t>;
+using act_t = uint32_t;
 template <bool W8>
 constexpr int act_n() {
-    return W8 ? 16 : 4;
+    return W8 ? 8 : 4;
 }
 
 // Sums V values (1, 2 or 4) over the warp's 32 lanes at once: each butterfly
@@ -317,6 +311,7 @@ constexpr int act_n() {
 // lane returns the sum of its value.  Fixed order: deterministic.
 template <int V>
 __device__ __forceinline__ float warp_sum_multi(const float (&x)[V]) {
+
     static_assert(V == 1 || V == 2 || V == 4, "1, 2 or 4 values");
     const int lane = threadIdx.x & 31;
     float v;
@@ -336,38 +331,67 @@ __device__ __forceinline__ float warp_sum_multi(const float (&x)[V]) {
     return v;
 }
 
-// One token's activations at this lane's positions of a warp slice of a
-// bf16 row starting at element a0, n elements long: vectors v = lane + 32 i
-// (i < PV), zero past the slice; bf16 pairs as they are (bf16 weights) or
-// widened to fp32 (E4M3 weights).
+// The lane's activations of one token row at its PV vectors (v = lane + 32 i,
+// i < PV) of the slice [a0, a0 + n), zero past the slice; bf16 pairs as they
+// are against bf16 weights.  FP8: returned as f16 pairs of x 2^-e, e chosen for the whole
+// warp so that the slice's largest magnitude lands in [0.5, 1) (e = 0 for an
+// all-zero slice); the return value is 2^e, which the warp's dots are
+// multiplied by (exactly: a power of two).  Must be called by whole warps.
 template <bool W8, int PV>
-__device__ __forceinline__ void load_act(const bf16* row, int a0, int n, act_t<W8> (&out)[PV][act_n<W8>()]) {
+__device__ __forceinline__ float load_act(const bf16* row, int a0, int n, act_t<W8> (&out)[PV][act_n<W8>()]) {
     constexpr int VE = W8 ? 16 : 8;
     const int lane = threadIdx.x & 31;
+    if constexpr (W8) {
+        float xv[PV][16];
+        uint32_t mx = 0;  // largest |x| of the lane, as bits (same order as the values)
 #pragma unroll
-    for (int i = 0; i < PV; ++i) {
-        const int v = lane + 32 * i;
+        for (int i = 0; i < PV; ++i) {
+            const int v = lane + 32 * i;
 #pragma unroll
-        for (int h = 0; h < VE / 8; ++h) {
-            uint4 u = make_uint4(0u, 0u, 0u, 0u);
-            if (v * VE < n) u = __ldcg(reinterpret_cast<const uint4*>(row + a0 + v * VE) + h);
-            if constexpr (W8) {
+            for (int h = 0; h < 2; ++h) {
+                uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                if (v * VE < n) u = __ldcg(reinterpret_cast<const uint4*>(row + a0 + v * VE) + h);
                 float f8[8];
                 widen(u, f8, static_cast<const __nv_bfloat16*>(nullptr));
 #pragma unroll
-                for (int e = 0; e < 8; ++e) out[i][8 * h + e] = f8[e];
-            } else {
-                out[i][0] = u.x;
-                out[i][1] = u.y;
-                out[i][2] = u.z;
-                out[i][3] = u.w;
+                for (int e = 0; e < 8; ++e) {
+                    xv[i][8 * h + e] = f8[e];
+                    mx = max(mx, __float_as_uint(fabsf(f8[e])));
+                }
             }
         }
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        int ex = 0;
+        if (mx != 0) frexpf(__uint_as_float(mx), &ex);  // max = m 2^ex, m in [0.5, 1)
+        const float scale = ldexpf(1.0f, -ex);
+#pragma unroll
+        for (int i = 0; i < PV; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const __half2 p2 = __floats2half2_rn(xv[i][2 * e] * scale, xv[i][2 * e + 1] * scale);
+                out[i][e] = *reinterpret_cast<const uint32_t*>(&p2);
+            }
+        return ldexpf(1.0f, ex);
+    } else {
+#pragma unroll
+        for (int i = 0; i < PV; ++i) {
+            const int v = lane + 32 * i;
+            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+            if (v * VE < n) u = __ldcg(reinterpret_cast<const uint4*>(row + a0 + v * VE));
+            out[i][0] = u.x;
+            out[i][1] = u.y;
+            out[i][2] = u.z;
+            out[i][3] = u.w;
+        }
+        return 1.0f;
     }
 }
 
 // acc[q][i] += <activations of token q, 16-byte weight vector lane + 32 i of
-// the slice at `w`> for the vectors below nvec.
+// the slice at `w`> for the vectors below nvec.  E4M3 codes: the 16 products
+// of a vector are summed as f16 pairs (two partial sums of 8 products each,
+// |sum| < 8 x 448 with activations below 1), which then join the fp32
+// accumulator.
 template <bool W8, int NT, int PV>
 __device__ __forceinline__ void slice_dots(const uint8_t* w, int nvec, const act_t<W8> (&act)[NT][PV][act_n<W8>()],
                                            int ntok, float (&acc)[NT][PV]) {
@@ -378,17 +402,25 @@ __device__ __forceinline__ void slice_dots(const uint8_t* w, int nvec, const act
         const int v = lane + 32 * i;
         if (v < nvec) {
             const uint4 u = wv[v];
+            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
             if constexpr (W8) {
-                float wf[16];
-                widen_e4m3x16(u, wf);
+                __half2 wh[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    wh[2 * j] = e4m3x2_to_half2(wd[j]);
+                    wh[2 * j + 1] = e4m3x2_to_half2(wd[j] >> 16);
+                }
 #pragma unroll
                 for (int q = 0; q < NT; ++q)
                     if (q < ntok) {
+                        __half2 s2 = __float2half2_rn(0.0f);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) acc[q][i] = fmaf(act[q][i][e], wf[e], acc[q][i]);
+                        for (int e = 0; e < 8; ++e)
+                            s2 = __hfma2(wh[e], *reinterpret_cast<const __half2*>(&act[q][i][e]), s2);
+                        const float2 f = __half22float2(s2);
+                        acc[q][i] += f.x + f.y;
                     }
             } else {
-                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int q = 0; q < NT; ++q)
                     if (q < ntok) {
@@ -485,10 +517,12 @@ __global__ void __launch_bounds__(kFThreadsP, 1)
         const int n = d - a0 < pl.up_wslice ? (d - a0 > 0 ? d - a0 : 0) : pl.up_wslice;
         const int nvec = n / VE;
         act_t<W8> xr[NT][PV][act_n<W8>()];  // every token's x at this lane's positions
+        float xs[NT];                        // ... and the factor its dots take (FP8: 2^e)
 #pragma unroll
         for (int q = 0; q < NT; ++q) {
+            xs[q] = 1.0f;
             if (q < a.T) {
-                load_act<W8, PV>(static_cast<const bf16*>(a.x) + (size_t)q * d, a0, n, xr[q]);
+                xs[q] = load_act<W8, PV>(static_cast<const bf16*>(a.x) + (size_t)q * d, a0, n, xr[q]);
             } else {
 #pragma unroll
                 for (int i = 0; i < PV; ++i)
@@ -529,9 +563,12 @@ __global__ void __launch_bounds__(kFThreadsP, 1)
                         vals[2 * q + 1] += uacc[q][i];
                     }
                 }
-                const float tot = warp_sum_multi<2 * NT>(vals);
+                float tot = warp_sum_multi<2 * NT>(vals);
                 constexpr int kPer = 32 / (2 * NT);  // lanes per value
                 const int vi = lane / kPer;
+#pragma unroll
+                for (int q = 0; q < NT; ++q)
+                    if (q == (vi >> 1)) tot *= xs[q];
                 if (lane % kPer == 0 && (vi >> 1) < a.T)
                     part[((((size_t)bl * R + j) * wpr + sub) * a.T + (vi >> 1)) * 2 + (vi & 1)] = tot;
             }
@@ -646,6 +683,7 @@ __global__ void __launch_bounds__(kFThreadsP, 1)
         for (int i = lane; i < nr * ncols; i += 32) part[(size_t)warp * nr * ncols + i] = 0.f;
         pdl_wait();  // H from here on
         act_t<W8> h[NT][PV][act_n<W8>()];  // the current expert's tokens' H at this lane's positions
+        float hs[NT];                       // ... and the factor their dots take (FP8: 2^e)
         int es = 0, row = 0, s = 0, cur_es = -1, ntok = 0, col0 = 0, a0 = 0, nvec = 0, Fe = 0;
         uint32_t ph = 0;
         for (int q = 0; q < n_items; ++q) {
@@ -661,10 +699,11 @@ __global__ void __launch_bounds__(kFThreadsP, 1)
                 nvec = n / VE;
 #pragma unroll
                 for (int i = 0; i < NT; ++i) {
+                    hs[i] = 1.0f;
                     if (i < ntok) {
                         const bf16* hrow = routed ? static_cast<const bf16*>(a.h) + (size_t)r.ent[es][i] * F
                                                   : static_cast<const bf16*>(a.h_shared) + (size_t)i * Fs;
-                        load_act<W8, PV>(hrow, a0, n, h[i]);
+                        hs[i] = load_act<W8, PV>(hrow, a0, n, h[i]);
                     }
                 }
             }
@@ -694,9 +733,12 @@ __global__ void __launch_bounds__(kFThreadsP, 1)
 #pragma unroll
                     for (int v = 0; v < PV; ++v) vals[jj * NT + i] += acc[jj][i][v];
                 }
-            const float tot = warp_sum_multi<kDnMaxRows * NT>(vals);
+            float tot = warp_sum_multi<kDnMaxRows * NT>(vals);
             constexpr int kPer = 32 / (kDnMaxRows * NT);  // lanes per value
             const int vi = lane / kPer, jj = vi / NT, ti = vi % NT;
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+                if (i == ti) tot *= hs[i];
             if (lane % kPer == 0 && jj < rows && ti < ntok) part[((size_t)warp * nr + row + jj) * ncols + col0 + ti] = tot;
             row += R2;
             if (row >= nr) {
@@ -803,7 +845,7 @@ FusedPlan fused_decode_plan(const moe_config& c, bool fp8, int sms) {
     auto pv_of = [&](int slice) {
         const int v = (slice + 32 * ve - 1) / (32 * ve);
         const int pv = v <= 2 ? 2 : 4;
-        return v <= 4 && T * pv * (fp8 ? 16 : 4) <= kLaneWords ? pv : 0;
+        return v <= 4 && T * pv * (fp8 ? 8 : 4) <= kLaneWords ? pv : 0;
     };
     auto round_up = [](int v, int m) { return (v + m - 1) / m * m; };
     // up kernel: the partial dots, then the ring; a stage holds up_rows whole
