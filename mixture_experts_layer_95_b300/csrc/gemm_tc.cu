@@ -115,6 +115,10 @@ struct TcParams {  // CUtensorMap members carry their own 64-byte alignment
     CUtensorMap tmdG[2];
     CUtensorMap tmdU[2];
     CUtensorMap tmH[2];
+    // columns of the MMA and of the B tile in Plain mode: BN, or 64 for a
+    // product with N <= 64 (the router's logits GEMM), whose B box is then
+    // 64 rows high
+    int mma_n;
     const float* bwd_G[2];
     const float* bwd_U[2];
     __nv_bfloat16* bwd_dGU[2];
@@ -264,7 +268,8 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 // sums the slices in slice order.  For SwiGLU the gate half lands in columns
 // [0, N) and the up half in [N, 2N).
 template <int MODE>
-__device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile) {
+__device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile,
+                                                 int ncols = BN) {
     const int N = p.N[t.prob];
     const bool valid = row_in_tile < t.rows_valid;
     const size_t grow = static_cast<size_t>(t.out_row0 + row_in_tile);
@@ -274,7 +279,7 @@ __device__ __forceinline__ void epilogue_partial(const TcParams& p, const Tile& 
     if ((MODE == kGemmScale || MODE == kGemmScaleSplit) && valid && p.row_scale[t.prob] != nullptr)
         scale = __ldg(p.row_scale[t.prob] + grow);
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
+    for (int c0 = 0; c0 < ncols; c0 += 32) {
         uint32_t v[32];
         __syncwarp();
         tmem_ld32(tacc + c0, v);
@@ -370,8 +375,9 @@ template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile,
                                               float (*stage)[33], int col_lo = 0, int ncols = BN, bool ilv = false,
                                               int warp_row0 = -1, int warp_rows = 32) {
+    if (MODE == kGemmPlain && p.mma_n < ncols) ncols = p.mma_n;  // (columns past mma_n hold nothing)
     if (p.ksplit > 1) {
-        epilogue_partial<MODE>(p, t, tacc, row_in_tile);
+        epilogue_partial<MODE>(p, t, tacc, row_in_tile, ncols);
         return;
     }
     const int N = p.N[t.prob];
@@ -716,7 +722,9 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
                     // gathered A: only the groups of 4 rows that hold valid rows are
                     // loaded; the other rows of the tile are never stored
                     const uint32_t a_bytes = gidx ? (uint32_t)((t.rows_valid + 3) / 4) * 4 * (BK * 2) : A_BYTES;
-                    mbar_expect_tx(&st.full[s], SLOT - A_BYTES + a_bytes);
+                    const uint32_t b_bytes =
+                        (MODE == kGemmPlain && p.mma_n != BN) ? (uint32_t)(p.mma_n * BK * 2) : (uint32_t)(SLOT - A_BYTES);
+                    mbar_expect_tx(&st.full[s], b_bytes + a_bytes);
                     const int kc = t.k_off + kb * BK;
                     if (!W8 && MODE != kGemmSwiGLU && !SC::kSplit && p.b_mn) {  // B^T as 64-column blocks
                         uint64_t* bar = &st.full[s];
@@ -760,8 +768,9 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const bool bmn = !W8 && MODE != kGemmSwiGLU && !SC::kSplit && p.b_mn;
-            const uint32_t idesc_full = idesc_bf16_f32(BM, BN) | (bmn ? kIdescBMnMajor : 0u);
-            const uint32_t idesc_m64 = idesc_bf16_f32(BM / 2, BN) | (bmn ? kIdescBMnMajor : 0u);
+            const int mn = MODE == kGemmPlain ? p.mma_n : BN;
+            const uint32_t idesc_full = idesc_bf16_f32(BM, mn) | (bmn ? kIdescBMnMajor : 0u);
+            const uint32_t idesc_m64 = idesc_bf16_f32(BM / 2, mn) | (bmn ? kIdescBMnMajor : 0u);
             int s = 0, w = 0;
             uint32_t ph = 0, pw = 0;
             int it = 0;
@@ -1435,7 +1444,10 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     // in either mode, on a CTA pair (each CTA holds half of the N columns)
     // (SwiGLU on CTA pairs: two 64-row boxes per CTA, W1 and W3 of the same features)
     if (pair && mode == kGemmSwigluBwd && probs[0].G + (nprob > 1 ? probs[1].G : 0) > kPairBwdGroups + 1) pair = false;
-    const int b_box = (mode == kGemmSwiGLU && pair) ? BN / 4 : (mode == kGemmSwiGLU || pair) ? BN / 2 : BN;
+    // a plain product with few columns (the router's logits): 64-column MMAs and B tiles
+    const bool narrow = mode == kGemmPlain && !pair && nprob == 1 && probs[0].N <= 64 && !probs[0].b_mn &&
+                        !probs[0].kbase && !probs[0].klen && !probs[0].a_gather;
+    const int b_box = narrow ? 64 : (mode == kGemmSwiGLU && pair) ? BN / 4 : (mode == kGemmSwiGLU || pair) ? BN / 2 : BN;
     if (probs[0].G + (nprob > 1 ? probs[1].G : 0) > MAX_GROUPS + 1) return cudaErrorInvalidValue;
     for (int q = 0; q < nprob; ++q) {
         const GemmProblem& g = probs[q];
@@ -1533,6 +1545,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem* probs, int nprob, int* s
     prm.status = status;
     prm.wait_limit_ns = kWaitLimitNs;
     prm.m64 = (pair || mode == kGemmSwigluBwd) ? 0 : 1;  // (the SwiGLU backward keeps 128-row tiles)
+    prm.mma_n = narrow ? 64 : BN;
     // failure-path test switch: the producer issues no loads, so every CTA
     // with work gives up after a short bounded wait and reports MOE_ERR_TIMEOUT
     if (test_stall_gemm()) {

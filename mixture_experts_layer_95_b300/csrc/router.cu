@@ -384,22 +384,39 @@ __global__ void __launch_bounds__(32 * logits_warps<NJ>()) router_logits_kernel(
         psum[j] = 0.f;
         hcnt[j] = 0;
     }
-    for (int i = 0; i < kTokensPerWarp; ++i) {
-        const int t = blockIdx.x * kRouterTokensPerBlock + warp * kTokensPerWarp + i;
-        if (t >= Tn) break;
-        float l[NJ];
+    // the logits of kPre tokens at a time (at most 64 registers) are loaded
+    // before their softmax / top-k, so the warp waits for memory once per
+    // group instead of once per token
+    constexpr int kPre = kTokensPerWarp * NJ <= 64 ? kTokensPerWarp : (64 / NJ > 0 ? 64 / NJ : 1);
+    for (int i0 = 0; i0 < kTokensPerWarp; i0 += kPre) {
+        const int t0 = blockIdx.x * kRouterTokensPerBlock + warp * kTokensPerWarp + i0;
+        if (t0 >= Tn) break;
+        float l[kPre][NJ];
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const int e = lane + 32 * j;
-            float v = -FLT_MAX;
-            if (e < E) {  // the logits GEMM's K slices, added in slice order
-                v = logits[(size_t)t * E + e];
-                for (int sl = 1; sl < nsplit; ++sl) v += logits[((size_t)sl * Tn + t) * E + e];
-                v += logit_bias ? __ldg(logit_bias + e) : 0.f;
+        for (int i = 0; i < kPre; ++i)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int e = lane + 32 * j;
+                l[i][j] = (t0 + i < Tn && e < E) ? logits[(size_t)(t0 + i) * E + e] : -FLT_MAX;
             }
-            l[j] = v;
+        for (int sl = 1; sl < nsplit; ++sl)  // the logits GEMM's K slices, added in slice order
+#pragma unroll
+            for (int i = 0; i < kPre; ++i)
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int e = lane + 32 * j;
+                    if (t0 + i < Tn && e < E) l[i][j] += logits[((size_t)sl * Tn + t0 + i) * E + e];
+                }
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) {
+            if (i0 + i >= kTokensPerWarp || t0 + i >= Tn) break;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int e = lane + 32 * j;
+                if (e < E) l[i][j] += logit_bias ? __ldg(logit_bias + e) : 0.f;
+            }
+            softmax_topk<NJ>(t0 + i, E, k, l[i], select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
         }
-        softmax_topk<NJ>(t, E, k, l, select_bias, renormalize, topk_ids, gates, psum, hcnt, probs);
     }
     block_epilogue<NJ, kW>(E, psum, hcnt, p_part, block_hist, s_p, s_h);
     __syncthreads();
