@@ -9,7 +9,10 @@ the 1-CTA kernel (75 rows per expert), the CTA-pair kernel (550 rows per
 expert: both CTAs of a pair give up and meet at the final cluster barrier) and
 the decode kernel with the weights on the MMA's M side, with bf16 and with FP8
 weights (2 rows per expert), and the two fused small-batch kernels (one
-token; every warp's own ring), with bf16 and with FP8 weights.
+token; every warp's own ring), with bf16 and with FP8 weights.  The backward
+on CTA pairs (recomputed G and U, the SwiGLU backward whose epilogue has G and
+U loads and dG / dU / H stores of its own in flight, dX and the K-grouped
+weight gradients) gets the same treatment.
 """
 import pytest
 import torch
@@ -63,4 +66,37 @@ def test_bounded_wait_times_out_and_the_context_survives(cuda, w, up_kernel):
     torch.cuda.synchronize()
     assert fw.device_status() == 0
     rep = check_layer_fp8(w, L=L) if q8 is not None else check_layer(w, L=L)
+    assert rep["ok"], rep
+
+
+def test_backward_bounded_wait_times_out_and_the_context_survives(cuda):
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    from tests._parity import layer_of
+    from tests.test_backward_gpu import check_backward
+    w = Workload("stall_backward_pair", T=1100, d=256, E=4, F=256, k=2, n_shared=1, F_s=128)
+    layer = layer_of(w)
+    assert moe.plan_describe(layer.cfg())["up"] == "tc_pair"
+    L = moe_inputs.make_layer(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(1234)
+    dy = torch.randn((w.T, w.d), generator=g, device="cuda").to(layer.torch_dtype)
+    bw = moe.Backward(layer, L["w_gate"], L["w1"], L["w3"], L["w2"], L["logit_bias"], L["select_bias"],
+                      L["ws1"], L["ws3"], L["ws2"])
+    torch.cuda.synchronize()
+    assert moe.test_stall_gemm(True) is False
+    try:
+        bw(L["x"], dy, dL=2.0)
+        torch.cuda.synchronize()
+    finally:
+        moe.test_stall_gemm(False)
+    assert bw.device_status() == MOE_ERR_TIMEOUT
+    assert bw.device_status() == 0  # read-and-clear
+    got = {n: t.clone() for n, t in bw(L["x"], dy, dL=2.0).items()}
+    torch.cuda.synchronize()
+    assert bw.device_status() == 0
+    fresh = moe.backward(layer, L["x"], L["w_gate"], L["w1"], L["w3"], L["w2"], dy, L["logit_bias"],
+                         L["select_bias"], L["ws1"], L["ws3"], L["ws2"], dL=2.0)
+    for n in fresh:
+        assert torch.equal(got[n], fresh[n]), n
+    rep = check_backward(w)
     assert rep["ok"], rep
