@@ -3,9 +3,10 @@
 // Same problems and epilogues as gemm_tc.cu (see there for the sources), for
 // layers stored in fp32.  The tensor cores offer fp32 inputs only as TF32,
 // whose 10-bit mantissa cannot meet an fp32 layer's tolerance, so fp32 layers
-// use plain FMA tiles: 64x64 output tiles, K staged through shared memory 16
-// at a time, 256 threads with a 4x4 register tile each (two accumulator sets
-// for the paired W1/W3 SwiGLU tile).  Tiles are enumerated on the device from
+// use plain FMA tiles: 64x64 output tiles, K staged through shared memory 32
+// at a time (the next 32 loaded into registers while the current ones are
+// multiplied), 256 threads with a 4x4 register tile each (two accumulator
+// sets for the paired W1/W3 SwiGLU tile).  Tiles are enumerated on the device from
 // the group offsets; blocks beyond the real tile count exit at once.
 #include "common.cuh"
 
@@ -13,7 +14,7 @@ namespace moe {
 namespace {
 
 constexpr int SB = 64;    // tile rows and output columns
-constexpr int SK = 16;    // K slab
+constexpr int SK = 32;    // K slab
 constexpr int SMAXG = kMaxExperts;
 
 struct SimtParams {
@@ -27,31 +28,35 @@ struct SimtParams {
     int nprob;
 };
 
+// Rows [lo, hi) of group g of problem q: its offsets, or all M rows; a range
+// that does not fit the A matrix is empty.
+__device__ __forceinline__ void simt_grp_rows(const SimtParams& p, int q, int g, int& lo, int& hi) {
+    lo = 0;
+    hi = p.M[q];
+    if (p.offsets[q]) {
+        lo = __ldg(p.offsets[q] + g);
+        hi = __ldg(p.offsets[q] + g + 1);
+    }
+    if (lo < 0 || hi < lo || hi > p.a_rows[q]) lo = hi = 0;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams p) {
     pdl_wait();
     __shared__ int s_start[2][SMAXG + 1];
-    __shared__ int s_row0[2][SMAXG];
-    __shared__ int s_rows[2][SMAXG];
     __shared__ int s_total[2];
-    __shared__ float sA[SK][SB + 4];
-    __shared__ float sB1[SK][SB + 4];
-    __shared__ float sB2[SK][SB + 4];
+    __shared__ __align__(16) float sA[SK][SB + 4];
+    __shared__ __align__(16) float sB1[SK][SB + 4];
+    __shared__ __align__(16) float sB2[SK][SB + 4];
     if (threadIdx.x == 0) {
         for (int q = 0; q < 2; ++q) {
             int run = 0;
             if (q < p.nprob) {
                 const int ncb = (p.N[q] + SB - 1) / SB;
                 for (int g = 0; g < p.G[q]; ++g) {
-                    int lo = 0, hi = p.M[q];
-                    if (p.offsets[q]) {
-                        lo = p.offsets[q][g];
-                        hi = p.offsets[q][g + 1];
-                    }
-                    if (lo < 0 || hi < lo || hi > p.a_rows[q]) lo = hi = 0;
+                    int lo, hi;
+                    simt_grp_rows(p, q, g, lo, hi);
                     s_start[q][g] = run;
-                    s_row0[q][g] = lo;
-                    s_rows[q][g] = hi - lo;
                     run += ((hi - lo + SB - 1) / SB) * ncb;
                 }
             }
@@ -64,11 +69,13 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams
         const int local = id - (q ? s_total[0] : 0);
         int g = 0;
         while (g + 1 < p.G[q] && s_start[q][g + 1] <= local) ++g;
-        const int mt = (s_rows[q][g] + SB - 1) / SB;
+        int glo, ghi;
+        simt_grp_rows(p, q, g, glo, ghi);
+        const int mt = (ghi - glo + SB - 1) / SB;
         const int r = local - s_start[q][g];
         const int n = r / mt, m = r - (r / mt) * mt;
-        const int row0 = s_row0[q][g] + m * SB;
-        const int rows_valid = min(SB, s_rows[q][g] - m * SB);
+        const int row0 = glo + m * SB;
+        const int rows_valid = min(SB, ghi - glo - m * SB);
         const int N = p.N[q], K = p.K[q];
         const int col0 = n * SB;
         const float* A = p.A[q];
@@ -76,24 +83,72 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams
         const float* B2 = (MODE == kGemmSwiGLU) ? p.B2[q] + (size_t)g * N * K : nullptr;
         const int tr = threadIdx.x / 16, tc = threadIdx.x % 16;
         float acc1[4][4] = {}, acc2[4][4] = {};
-        for (int k0 = 0; k0 < K; k0 += SK) {
-            for (int i = threadIdx.x; i < SB * SK; i += 256) {
-                const int rr = i / SK, kk = i % SK;
-                const int kg = k0 + kk;
-                sA[kk][rr] = (rr < rows_valid && kg < K) ? A[(size_t)(row0 + rr) * K + kg] : 0.f;
-                const bool bv = (col0 + rr < N) && kg < K;
-                sB1[kk][rr] = bv ? B1[(size_t)(col0 + rr) * K + kg] : 0.f;
-                if (MODE == kGemmSwiGLU) sB2[kk][rr] = bv ? B2[(size_t)(col0 + rr) * K + kg] : 0.f;
+        // Loader role: thread t brings row t / 4 of the A, B1 (and B2) slabs,
+        // the four-element groups t % 4 and t % 4 + 4 of the slab's eight (one
+        // 16-byte load each when K % 4 == 0).  The next slab is loaded into
+        // these registers while the current one is multiplied, so each slab
+        // waits for its loads at most once.
+        constexpr int NQ = SK / 16;  // four-element groups per thread and operand
+        const int lr = threadIdx.x >> 2, lq = threadIdx.x & 3;
+        // 16-byte loads need K % 4 == 0 and 16-byte aligned operand bases (the
+        // entry points reject other pointers and sizes; checked here as well so
+        // that the kernel stays safe on its own)
+        const uintptr_t bases = reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(p.B1[q]) |
+                                (MODE == kGemmSwiGLU ? reinterpret_cast<uintptr_t>(p.B2[q]) : 0);
+        const bool vec = (K & 3) == 0 && (bases & 15) == 0;
+        const bool a_ok = lr < rows_valid, b_ok = col0 + lr < N;
+        const float* a_row = A + (size_t)(row0 + (a_ok ? lr : 0)) * K;
+        const float* b1_row = B1 + (size_t)(col0 + (b_ok ? lr : 0)) * K;
+        const float* b2_row = (MODE == kGemmSwiGLU) ? B2 + (size_t)(col0 + (b_ok ? lr : 0)) * K : nullptr;
+        float ra[NQ][4], rb1[NQ][4], rb2[NQ][4];
+        auto fetch = [&](int k0) {
+#pragma unroll
+            for (int h = 0; h < NQ; ++h) {
+                const int kg = k0 + (lq + 4 * h) * 4;
+                if (vec && kg < K) {  // K % 4 == 0: the four elements are all in range or all out
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 va = a_ok ? __ldg(reinterpret_cast<const float4*>(a_row + kg)) : z;
+                    const float4 vb = b_ok ? __ldg(reinterpret_cast<const float4*>(b1_row + kg)) : z;
+                    ra[h][0] = va.x, ra[h][1] = va.y, ra[h][2] = va.z, ra[h][3] = va.w;
+                    rb1[h][0] = vb.x, rb1[h][1] = vb.y, rb1[h][2] = vb.z, rb1[h][3] = vb.w;
+                    if (MODE == kGemmSwiGLU) {
+                        const float4 vc = b_ok ? __ldg(reinterpret_cast<const float4*>(b2_row + kg)) : z;
+                        rb2[h][0] = vc.x, rb2[h][1] = vc.y, rb2[h][2] = vc.z, rb2[h][3] = vc.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const bool kv = kg + e < K;
+                        ra[h][e] = (a_ok && kv) ? __ldg(a_row + kg + e) : 0.f;
+                        rb1[h][e] = (b_ok && kv) ? __ldg(b1_row + kg + e) : 0.f;
+                        if (MODE == kGemmSwiGLU) rb2[h][e] = (b_ok && kv) ? __ldg(b2_row + kg + e) : 0.f;
+                    }
+                }
             }
+        };
+        fetch(0);
+        for (int k0 = 0; k0 < K; k0 += SK) {
+#pragma unroll
+            for (int h = 0; h < NQ; ++h)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int kk = (lq + 4 * h) * 4 + e;
+                    sA[kk][lr] = ra[h][e];
+                    sB1[kk][lr] = rb1[h][e];
+                    if (MODE == kGemmSwiGLU) sB2[kk][lr] = rb2[h][e];
+                }
             __syncthreads();
+            if (k0 + SK < K) fetch(k0 + SK);
 #pragma unroll
             for (int kk = 0; kk < SK; ++kk) {
-                float a[4], b1[4], b2[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    a[i] = sA[kk][tr * 4 + i];
-                    b1[i] = sB1[kk][tc * 4 + i];
-                    if (MODE == kGemmSwiGLU) b2[i] = sB2[kk][tc * 4 + i];
+                const float4 a4 = *reinterpret_cast<const float4*>(&sA[kk][tr * 4]);
+                const float4 b4 = *reinterpret_cast<const float4*>(&sB1[kk][tc * 4]);
+                const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+                const float b1[4] = {b4.x, b4.y, b4.z, b4.w};
+                float b2[4] = {0.f, 0.f, 0.f, 0.f};
+                if (MODE == kGemmSwiGLU) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(&sB2[kk][tc * 4]);
+                    b2[0] = c4.x, b2[1] = c4.y, b2[2] = c4.z, b2[3] = c4.w;
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
