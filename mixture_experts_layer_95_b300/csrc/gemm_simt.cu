@@ -3,17 +3,19 @@
 // Same problems and epilogues as gemm_tc.cu (see there for the sources), for
 // layers stored in fp32.  The tensor cores offer fp32 inputs only as TF32,
 // whose 10-bit mantissa cannot meet an fp32 layer's tolerance, so fp32 layers
-// use plain FMA tiles: 64x64 output tiles, K staged through shared memory 32
-// at a time (the next 32 loaded into registers while the current ones are
-// multiplied), 256 threads with a 4x4 register tile each (two accumulator
-// sets for the paired W1/W3 SwiGLU tile).  Tiles are enumerated on the device from
-// the group offsets; blocks beyond the real tile count exit at once.
+// use plain FMA tiles: 64x64 output tiles (32x64 when 64-row tiles would not
+// give every SM one), K staged through shared memory 32 at a time (the next
+// 32 loaded into registers while the current ones are multiplied), one 4x4
+// register tile per thread (256 or 128 threads; two accumulator sets for the
+// paired W1/W3 SwiGLU tile).  Every output still sums its K products in
+// order.  Tiles are enumerated on the device from the group offsets; blocks
+// beyond the real tile count exit at once.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int SB = 64;    // tile rows and output columns
+constexpr int SB = 64;    // output columns of a tile (and its rows, unless a launch takes 32-row tiles)
 constexpr int SK = 32;    // K slab
 constexpr int SMAXG = kMaxExperts;
 
@@ -40,12 +42,13 @@ __device__ __forceinline__ void simt_grp_rows(const SimtParams& p, int q, int g,
     if (lo < 0 || hi < lo || hi > p.a_rows[q]) lo = hi = 0;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams p) {
+// TM: tile rows, 64 or 32 (4 TM threads: TM / 4 row groups x 16 column groups)
+template <int MODE, int TM>
+__global__ void __launch_bounds__(4 * TM) grouped_gemm_simt_kernel(const SimtParams p) {
     pdl_wait();
     __shared__ int s_start[2][SMAXG + 1];
     __shared__ int s_total[2];
-    __shared__ __align__(16) float sA[SK][SB + 4];
+    __shared__ __align__(16) float sA[SK][TM + 4];
     __shared__ __align__(16) float sB1[SK][SB + 4];
     __shared__ __align__(16) float sB2[SK][SB + 4];
     if (threadIdx.x == 0) {
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams
                     int lo, hi;
                     simt_grp_rows(p, q, g, lo, hi);
                     s_start[q][g] = run;
-                    run += ((hi - lo + SB - 1) / SB) * ncb;
+                    run += ((hi - lo + TM - 1) / TM) * ncb;
                 }
             }
             s_total[q] = run;
@@ -71,11 +74,11 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams
         while (g + 1 < p.G[q] && s_start[q][g + 1] <= local) ++g;
         int glo, ghi;
         simt_grp_rows(p, q, g, glo, ghi);
-        const int mt = (ghi - glo + SB - 1) / SB;
+        const int mt = (ghi - glo + TM - 1) / TM;
         const int r = local - s_start[q][g];
         const int n = r / mt, m = r - (r / mt) * mt;
-        const int row0 = glo + m * SB;
-        const int rows_valid = min(SB, ghi - glo - m * SB);
+        const int row0 = glo + m * TM;
+        const int rows_valid = min(TM, ghi - glo - m * TM);
         const int N = p.N[q], K = p.K[q];
         const int col0 = n * SB;
         const float* A = p.A[q];
@@ -83,12 +86,14 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams
         const float* B2 = (MODE == kGemmSwiGLU) ? p.B2[q] + (size_t)g * N * K : nullptr;
         const int tr = threadIdx.x / 16, tc = threadIdx.x % 16;
         float acc1[4][4] = {}, acc2[4][4] = {};
-        // Loader role: thread t brings row t / 4 of the A, B1 (and B2) slabs,
-        // the four-element groups t % 4 and t % 4 + 4 of the slab's eight (one
-        // 16-byte load each when K % 4 == 0).  The next slab is loaded into
-        // these registers while the current one is multiplied, so each slab
-        // waits for its loads at most once.
-        constexpr int NQ = SK / 16;  // four-element groups per thread and operand
+        // Loader role: thread t brings row t / 4 of the A slab and rows t / 4 +
+        // TM j of the B1 (and B2) slabs (j < 64 / TM), the four-element groups
+        // t % 4 and t % 4 + 4 of each slab row's eight (one 16-byte load each
+        // when K % 4 == 0).  The next slab is loaded into these registers while
+        // the current one is multiplied, so each slab waits for its loads at
+        // most once.
+        constexpr int NQ = SK / 16;  // four-element groups per thread and row
+        constexpr int PB = SB / TM;  // B rows per thread
         const int lr = threadIdx.x >> 2, lq = threadIdx.x & 3;
         // 16-byte loads need K % 4 == 0 and 16-byte aligned operand bases (the
         // entry points reject other pointers and sizes; checked here as well so
@@ -96,33 +101,37 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams
         const uintptr_t bases = reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(p.B1[q]) |
                                 (MODE == kGemmSwiGLU ? reinterpret_cast<uintptr_t>(p.B2[q]) : 0);
         const bool vec = (K & 3) == 0 && (bases & 15) == 0;
-        const bool a_ok = lr < rows_valid, b_ok = col0 + lr < N;
+        const bool a_ok = lr < rows_valid;
         const float* a_row = A + (size_t)(row0 + (a_ok ? lr : 0)) * K;
-        const float* b1_row = B1 + (size_t)(col0 + (b_ok ? lr : 0)) * K;
-        const float* b2_row = (MODE == kGemmSwiGLU) ? B2 + (size_t)(col0 + (b_ok ? lr : 0)) * K : nullptr;
-        float ra[NQ][4], rb1[NQ][4], rb2[NQ][4];
+        bool b_ok[PB];
+        const float* b1_row[PB];
+        const float* b2_row[PB];
+#pragma unroll
+        for (int j = 0; j < PB; ++j) {
+            const int br = lr + TM * j;
+            b_ok[j] = col0 + br < N;
+            b1_row[j] = B1 + (size_t)(col0 + (b_ok[j] ? br : 0)) * K;
+            b2_row[j] = (MODE == kGemmSwiGLU) ? B2 + (size_t)(col0 + (b_ok[j] ? br : 0)) * K : nullptr;
+        }
+        float ra[NQ][4], rb1[PB][NQ][4], rb2[PB][NQ][4];
+        auto load4 = [&](const float* row, bool ok, int kg, float (&v)[4]) {
+            if (vec && kg < K) {  // K % 4 == 0: the four elements are all in range or all out
+                const float4 x = ok ? __ldg(reinterpret_cast<const float4*>(row + kg)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = (ok && kg + e < K) ? __ldg(row + kg + e) : 0.f;
+            }
+        };
         auto fetch = [&](int k0) {
 #pragma unroll
             for (int h = 0; h < NQ; ++h) {
                 const int kg = k0 + (lq + 4 * h) * 4;
-                if (vec && kg < K) {  // K % 4 == 0: the four elements are all in range or all out
-                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float4 va = a_ok ? __ldg(reinterpret_cast<const float4*>(a_row + kg)) : z;
-                    const float4 vb = b_ok ? __ldg(reinterpret_cast<const float4*>(b1_row + kg)) : z;
-                    ra[h][0] = va.x, ra[h][1] = va.y, ra[h][2] = va.z, ra[h][3] = va.w;
-                    rb1[h][0] = vb.x, rb1[h][1] = vb.y, rb1[h][2] = vb.z, rb1[h][3] = vb.w;
-                    if (MODE == kGemmSwiGLU) {
-                        const float4 vc = b_ok ? __ldg(reinterpret_cast<const float4*>(b2_row + kg)) : z;
-                        rb2[h][0] = vc.x, rb2[h][1] = vc.y, rb2[h][2] = vc.z, rb2[h][3] = vc.w;
-                    }
-                } else {
+                load4(a_row, a_ok, kg, ra[h]);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const bool kv = kg + e < K;
-                        ra[h][e] = (a_ok && kv) ? __ldg(a_row + kg + e) : 0.f;
-                        rb1[h][e] = (b_ok && kv) ? __ldg(b1_row + kg + e) : 0.f;
-                        if (MODE == kGemmSwiGLU) rb2[h][e] = (b_ok && kv) ? __ldg(b2_row + kg + e) : 0.f;
-                    }
+                for (int j = 0; j < PB; ++j) {
+                    load4(b1_row[j], b_ok[j], kg, rb1[j][h]);
+                    if (MODE == kGemmSwiGLU) load4(b2_row[j], b_ok[j], kg, rb2[j][h]);
                 }
             }
         };
@@ -134,8 +143,11 @@ __global__ void __launch_bounds__(256) grouped_gemm_simt_kernel(const SimtParams
                 for (int e = 0; e < 4; ++e) {
                     const int kk = (lq + 4 * h) * 4 + e;
                     sA[kk][lr] = ra[h][e];
-                    sB1[kk][lr] = rb1[h][e];
-                    if (MODE == kGemmSwiGLU) sB2[kk][lr] = rb2[h][e];
+#pragma unroll
+                    for (int j = 0; j < PB; ++j) {
+                        sB1[kk][lr + TM * j] = rb1[j][h][e];
+                        if (MODE == kGemmSwiGLU) sB2[kk][lr + TM * j] = rb2[j][h][e];
+                    }
                 }
             __syncthreads();
             if (k0 + SK < K) fetch(k0 + SK);
@@ -211,11 +223,34 @@ cudaError_t launch_gemm_simt_f32(int mode, const GemmProblem* probs, int nprob, 
     }
     prm.nprob = nprob;
     if (tiles_max == 0) return cudaSuccess;
+    // fewer 64-row tiles than SMs: 32-row tiles (half the work each, twice as many)
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool small = tiles_max < sms;
+    if (small) {
+        tiles_max = 0;
+        for (int q = 0; q < nprob; ++q) {
+            const GemmProblem& g = probs[q];
+            const long long rows = g.offsets ? g.a_rows : g.M;
+            tiles_max += ((rows + 31) / 32 + (g.offsets ? g.G : 0)) * ((g.N + SB - 1) / SB);
+        }
+    }
     const int grid = static_cast<int>(tiles_max < 65535 ? tiles_max : 65535);
+    const dim3 block(small ? 128 : 256);
     switch (mode) {
-        case kGemmSwiGLU: launch_pdl(grouped_gemm_simt_kernel<kGemmSwiGLU>, dim3(grid), dim3(256), 0, s, prm); break;
-        case kGemmScale: launch_pdl(grouped_gemm_simt_kernel<kGemmScale>, dim3(grid), dim3(256), 0, s, prm); break;
-        case kGemmPlain: launch_pdl(grouped_gemm_simt_kernel<kGemmPlain>, dim3(grid), dim3(256), 0, s, prm); break;
+        case kGemmSwiGLU:
+            if (small) launch_pdl(grouped_gemm_simt_kernel<kGemmSwiGLU, 32>, dim3(grid), block, 0, s, prm);
+            else launch_pdl(grouped_gemm_simt_kernel<kGemmSwiGLU, 64>, dim3(grid), block, 0, s, prm);
+            break;
+        case kGemmScale:
+            if (small) launch_pdl(grouped_gemm_simt_kernel<kGemmScale, 32>, dim3(grid), block, 0, s, prm);
+            else launch_pdl(grouped_gemm_simt_kernel<kGemmScale, 64>, dim3(grid), block, 0, s, prm);
+            break;
+        case kGemmPlain:
+            if (small) launch_pdl(grouped_gemm_simt_kernel<kGemmPlain, 32>, dim3(grid), block, 0, s, prm);
+            else launch_pdl(grouped_gemm_simt_kernel<kGemmPlain, 64>, dim3(grid), block, 0, s, prm);
+            break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
