@@ -76,6 +76,7 @@ bool use_decode_gemm(const moe_config& c) { return decode_sized(c) && !use_h_spl
 // decode GEMM with 64-row token tiles reads an explicit copy as plain tiles
 // (16 gather4 loads per stage would limit its weight stream).
 bool use_gather_a(const moe_config& c) {
+    if (c.dtype == MOE_F32) return true;  // the CUDA-core up GEMM reads x rows through the row order
     if (!decode_sized(c)) return false;
     const long long n = perm_rows(c);
     const long long touched = n < c.E ? n : c.E;

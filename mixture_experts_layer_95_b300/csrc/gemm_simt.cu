@@ -7,8 +7,9 @@
 // give every SM one), K staged through shared memory 32 at a time (the next
 // 32 loaded into registers while the current ones are multiplied), one 4x4
 // register tile per thread (256 or 128 threads; two accumulator sets for the
-// paired W1/W3 SwiGLU tile).  Every output still sums its K products in
-// order.  Tiles are enumerated on the device from the group offsets; blocks
+// paired W1/W3 SwiGLU tile).  The up GEMM reads its token rows straight
+// from x through the grouping's row order.  Every output still sums its K
+// products in order.  Tiles are enumerated on the device from the group offsets; blocks
 // beyond the real tile count exit at once.
 #include "common.cuh"
 
@@ -21,6 +22,8 @@ constexpr int SMAXG = kMaxExperts;
 
 struct SimtParams {
     const float* A[2];
+    const int32_t* a_gather[2];  // non-null: A row r is row a_gather[r] of A ([a_src_rows][K])
+    int a_src_rows[2];
     const float* B1[2];
     const float* B2[2];
     const int32_t* offsets[2];
@@ -102,7 +105,12 @@ __global__ void __launch_bounds__(4 * TM) grouped_gemm_simt_kernel(const SimtPar
                                 (MODE == kGemmSwiGLU ? reinterpret_cast<uintptr_t>(p.B2[q]) : 0);
         const bool vec = (K & 3) == 0 && (bases & 15) == 0;
         const bool a_ok = lr < rows_valid;
-        const float* a_row = A + (size_t)(row0 + (a_ok ? lr : 0)) * K;
+        int a_src = row0 + (a_ok ? lr : 0);
+        if (p.a_gather[q]) {  // rows straight from the token matrix, in expert order
+            a_src = a_ok ? __ldg(p.a_gather[q] + a_src) : 0;
+            if (a_src < 0 || a_src >= p.a_src_rows[q]) a_src = 0;
+        }
+        const float* a_row = A + (size_t)a_src * K;
         bool b_ok[PB];
         const float* b1_row[PB];
         const float* b2_row[PB];
@@ -208,6 +216,8 @@ cudaError_t launch_gemm_simt_f32(int mode, const GemmProblem* probs, int nprob, 
         const GemmProblem& g = probs[q];
         if (g.G < 1 || g.G > SMAXG) return cudaErrorInvalidValue;
         prm.A[q] = static_cast<const float*>(g.A);
+        prm.a_gather[q] = g.a_gather;
+        prm.a_src_rows[q] = g.a_src_rows;
         prm.B1[q] = static_cast<const float*>(g.B1);
         prm.B2[q] = static_cast<const float*>(g.B2);
         prm.offsets[q] = g.offsets;
