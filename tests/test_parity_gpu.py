@@ -30,6 +30,9 @@ SMALL = [
              h_split=True),
     Workload("gemm_router_f32", T=300, d=128, E=20, F=96, k=3, dtype="f32"),
     Workload("warp_router_f32", T=300, d=264, E=8, F=96, k=2, dtype="f32"),
+    # enough rows that both CUDA-core GEMMs take 64-row tiles (the small cases
+    # above take 32-row tiles), with a shared expert and a ragged F
+    Workload("many_tiles_shared_f32", T=1024, d=256, E=8, F=520, k=2, n_shared=1, F_s=264, dtype="f32"),
     Workload("shared_selectbias_bf16", T=200, d=256, E=32, F=128, k=8, n_shared=1, F_s=192, select_bias=True),
     Workload("dense_limit_bf16", T=64, d=128, E=8, F=128, k=8, renormalize=False),
     Workload("single_expert_bf16", T=130, d=128, E=1, F=256, k=1),
