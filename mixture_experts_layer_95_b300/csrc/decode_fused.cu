@@ -335,7 +335,7 @@ __device__ __forceinline__ float warp_sum_multi(const float (&x)[V]) {
 // i < PV) of the slice [a0, a0 + n), zero past the slice; bf16 pairs as they
 // are against bf16 weights.  FP8: returned as f16 pairs of x 2^-e, e chosen for the whole
 // warp so that the slice's largest magnitude lands in [0.5, 1) (e = 0 for an
-// all-zero slice); the return value is 2^e, which the warp's dots are
+// all-zero slice; e kept in [-125, 126]); the return value is 2^e, which the warp's dots are
 // multiplied by (exactly: a power of two).  Must be called by whole warps.
 template <bool W8, int PV>
 __device__ __forceinline__ float load_act(const bf16* row, int a0, int n, act_t<W8> (&out)[PV][act_n<W8>()]) {
@@ -363,6 +363,10 @@ __device__ __forceinline__ float load_act(const bf16* row, int a0, int n, act_t<
         mx = __reduce_max_sync(0xffffffffu, mx);
         int ex = 0;
         if (mx != 0) frexpf(__uint_as_float(mx), &ex);  // max = m 2^ex, m in [0.5, 1)
+        // both 2^-ex and 2^ex stay finite fp32 values: at the ends of the bf16
+        // range the slice's largest magnitude then lands below 4 (f16 sums of
+        // eight products stay below 8 x 448 x 4) or below 0.5
+        ex = ex < -125 ? -125 : (ex > 126 ? 126 : ex);
         const float scale = ldexpf(1.0f, -ex);
 #pragma unroll
         for (int i = 0; i < PV; ++i)

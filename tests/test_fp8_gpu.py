@@ -120,6 +120,29 @@ def test_fp8_fused_one_token_of_extreme_scale(cuda, how):
     _assert_ok(rep)
 
 
+def test_fp8_fused_one_token_of_subnormal_scale(cuda):
+    """A token of bf16 subnormals (x scaled by 2^-130): the slice scale 2^-e
+    would overflow fp32 there, so it is held at 2^125.  H (about x^2)
+    underflows fp32 on every path, so y must come out finite and negligible
+    -- not NaN from 0 x inf."""
+    import mixture_experts_layer_95_b300 as moe
+    import moe_inputs
+    from tests._parity import layer_of
+    w = Workload("fp8_fused_scale_subnormal", T=1, d=256, E=8, F=384, k=2, n_shared=1, F_s=128, weights="fp8")
+    layer = layer_of(w)
+    assert moe.plan_describe(layer.cfg())["up"] == "fused"
+    L = moe_inputs.make_layer(w, "cuda")
+    x = (L["x"].float() * 2.0 ** -130).to(L["x"].dtype).contiguous()
+    assert int((x != 0).sum()) > 200  # subnormal, not flushed
+    q8 = moe.quantize_experts_fp8(layer, L["w1"], L["w3"], L["w2"], L["ws1"], L["ws3"], L["ws2"])
+    fw = moe.Forward(layer, L["w_gate"], None, None, None, L["logit_bias"], L["select_bias"], fp8=q8)
+    y = fw(x)
+    torch.cuda.synchronize()
+    assert fw.device_status() == 0
+    assert bool(torch.isfinite(y.float()).all())
+    assert float(y.float().abs().max()) < 1e-30
+
+
 @pytest.mark.parametrize("T", [3, 40])
 def test_fp8_decode_tokens_of_very_different_scales(cuda, T):
     """Decode-sized batches carry the bf16 token rows (and H) to the FP8 MMA
