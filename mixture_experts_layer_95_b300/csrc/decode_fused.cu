@@ -127,15 +127,16 @@ __device__ void fused_route(const FusedDecodeArgs& a, FusedRoute& r, float (*s_r
             // the producer warp (threads kFThreads..) only meets the barriers
             const int v_end = warp < kFW ? nv : 0;
             for (int v = threadIdx.x + kFThreads * h; v < v_end; v += kSplitDThreads) {
-                float xv[8];
-                widen(__ldcg(xr + v), xv, static_cast<const __nv_bfloat16*>(nullptr));
+                // bf16 pairs into mixed-precision FMAs: the router's sums, bit for bit
+                const uint4 x4 = __ldcg(xr + v);
+                const uint32_t xd[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
                 for (int e = 0; e < NE; ++e) {
                     if (e < a.E) {
-                        float wv[8];
-                        widen(__ldg(w + (size_t)e * nv + v), wv, static_cast<const __nv_bfloat16*>(nullptr));
+                        const uint4 w4 = __ldg(w + (size_t)e * nv + v);
+                        const uint32_t wd[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[h][e] = fmaf(xv[i], wv[i], acc[h][e]);
+                        for (int j = 0; j < 4; ++j) acc[h][e] = fma2_bf16(xd[j], wd[j], acc[h][e]);
                     }
                 }
             }
@@ -275,20 +276,6 @@ __device__ __forceinline__ void ring_drain(Ring& g, int S, int issued) {
 // pairs.  A lane holds PV (2 or 4) vectors per token, at most kLaneWords
 // registers.
 constexpr int kLaneWords = 64;
-
-// acc += a.lo b.lo, then + a.hi b.hi: mixed-precision FMAs on bf16 operands
-// into an fp32 accumulator.  A product of two bf16 values is exact in fp32,
-// so each step rounds only the addition, as fmaf on the widened values would.
-__device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float acc) {
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
-        "mov.b32 {al, ah}, %1;\n\t"
-        "mov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
-        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(a), "r"(b));
-    return acc;
-}
 
 // Two E4M3 codes (the low 16 bits) -> an f16 pair, exactly (E4M3 values are f16 values).
 __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {

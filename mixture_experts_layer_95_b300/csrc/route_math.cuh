@@ -28,6 +28,21 @@ struct Vec {
     static constexpr int kElems = 16 / sizeof(T);
 };
 
+// acc += a.lo b.lo, then + a.hi b.hi: mixed-precision FMAs on bf16 operands
+// into an fp32 accumulator.  A product of two bf16 values is exact in fp32,
+// so each step rounds only the addition, as fmaf on the widened values would
+// (the same result in one instruction, without widening either operand).
+__device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+
 __device__ __forceinline__ void widen(const uint4& u, float (&v)[8], const __nv_bfloat16*) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll

@@ -23,6 +23,8 @@
 //    tensor-core GEMM (large E); lane owns experts lane, lane+32, ...
 #include <float.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "route_math.cuh"
 
@@ -120,17 +122,33 @@ __global__ void __launch_bounds__(kWarpRouterThreads) router_warp_kernel(
         for (int u = 0; u < U; ++u) {
             const int v = v0 + 32 * u;
             if (v >= nv) break;  // v rises with u
-            float xv[kTpw][VE];
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                // bf16 pairs straight into mixed-precision FMAs: the same sums
+                // as widening both operands, element by element in order
 #pragma unroll
-            for (int q = 0; q < kTpw; ++q) widen(raw[u][q], xv[q], static_cast<const T*>(nullptr));
+                for (int e = 0; e < NE; ++e) {
+                    const uint4 w4 = s_w[e * nv + v];
+                    const uint32_t wd[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-            for (int e = 0; e < NE; ++e) {
-                float wv[VE];
-                widen(s_w[e * nv + v], wv, static_cast<const T*>(nullptr));
+                    for (int q = 0; q < kTpw; ++q) {
+                        const uint32_t xd[4] = {raw[u][q].x, raw[u][q].y, raw[u][q].z, raw[u][q].w};
 #pragma unroll
-                for (int q = 0; q < kTpw; ++q)
+                        for (int j = 0; j < 4; ++j) acc[q][e] = fma2_bf16(xd[j], wd[j], acc[q][e]);
+                    }
+                }
+            } else {
+                float xv[kTpw][VE];
 #pragma unroll
-                    for (int i = 0; i < VE; ++i) acc[q][e] = fmaf(xv[q][i], wv[i], acc[q][e]);
+                for (int q = 0; q < kTpw; ++q) widen(raw[u][q], xv[q], static_cast<const T*>(nullptr));
+#pragma unroll
+                for (int e = 0; e < NE; ++e) {
+                    float wv[VE];
+                    widen(s_w[e * nv + v], wv, static_cast<const T*>(nullptr));
+#pragma unroll
+                    for (int q = 0; q < kTpw; ++q)
+#pragma unroll
+                        for (int i = 0; i < VE; ++i) acc[q][e] = fmaf(xv[q][i], wv[i], acc[q][e]);
+                }
             }
         }
     }
@@ -320,15 +338,29 @@ __global__ void __launch_bounds__(kSplitDThreads) router_split_d_kernel(
 #pragma unroll
     for (int e = 0; e < NE; ++e) acc[e] = 0.f;
     for (int v = threadIdx.x; v < nv; v += kSplitDThreads) {
-        float xv[VE];
-        widen(__ldg(xr + v), xv, static_cast<const T*>(nullptr));
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) {  // (the same sums as widening, in order)
+            const uint4 x4 = __ldg(xr + v);
+            const uint32_t xd[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-        for (int e = 0; e < NE; ++e) {
-            if (e < E) {
-                float wv[VE];
-                widen(__ldg(w + (size_t)e * nv + v), wv, static_cast<const T*>(nullptr));
+            for (int e = 0; e < NE; ++e) {
+                if (e < E) {
+                    const uint4 w4 = __ldg(w + (size_t)e * nv + v);
+                    const uint32_t wd[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                for (int i = 0; i < VE; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+                    for (int j = 0; j < 4; ++j) acc[e] = fma2_bf16(xd[j], wd[j], acc[e]);
+                }
+            }
+        } else {
+            float xv[VE];
+            widen(__ldg(xr + v), xv, static_cast<const T*>(nullptr));
+#pragma unroll
+            for (int e = 0; e < NE; ++e) {
+                if (e < E) {
+                    float wv[VE];
+                    widen(__ldg(w + (size_t)e * nv + v), wv, static_cast<const T*>(nullptr));
+#pragma unroll
+                    for (int i = 0; i < VE; ++i) acc[e] = fmaf(xv[i], wv[i], acc[e]);
+                }
             }
         }
     }
