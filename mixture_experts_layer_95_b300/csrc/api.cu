@@ -314,8 +314,8 @@ BLayout blayout(const moe_config& c) {
     b.dgp = take(4 * ((n + 3) / 4 * 4));
     b.kbase = take(4 * E);
     b.klen = take(4 * E);
-    b.dGT = take(2 * F * nc);
-    b.dUT = take(2 * F * nc);
+    b.dGT = take(2 * 2 * F * nc);  // dG^T windows, then dU^T (one transpose of the dG|dU rows writes both)
+    b.dUT = b.dGT + 2 * F * nc;
     b.HbT = take(2 * F * nc);
     b.xpT = take(2 * d * nc);
     b.dysT = take(2 * d * nc);
@@ -331,8 +331,8 @@ BLayout blayout(const moe_config& c) {
     b.Us = take(sh ? 4 * T * Fs : 0);
     b.dGUs = take(sh ? 2 * T * 2 * Fs : 0);
     b.Hbs = take(sh ? 2 * T * Fs : 0);
-    b.dGsT = take(sh ? 2 * Fs * ncs : 0);
-    b.dUsT = take(sh ? 2 * Fs * ncs : 0);
+    b.dGsT = take(sh ? 2 * 2 * Fs * ncs : 0);
+    b.dUsT = b.dGsT + 2 * Fs * ncs;
     b.HbsT = take(sh ? 2 * Fs * ncs : 0);
     b.xT = take(sh ? 2 * d * ncs : 0);
     b.dyT = take(sh ? 2 * d * ncs : 0);
@@ -1292,17 +1292,16 @@ static int backward_impl(const moe_config* cfg, const void* x, const void* w_gat
     void* HbT = at<void>(ws, B.HbT);
     void* xpT = at<void>(ws, B.xpT);
     void* dysT = at<void>(ws, B.dysT);
-    MOE_LAUNCH(launch_transpose_windows(dGU, 2 * (size_t)F, 0, F, E, o.offsets, kbase, klen, nullptr, dGT, nc, nc, s));
-    MOE_LAUNCH(launch_transpose_windows(dGU, 2 * (size_t)F, F, F, E, o.offsets, kbase, klen, nullptr, dUT, nc, nc, s));
+    // the dG|dU rows in one pass: source column c < F lands in dG^T's row c, c >= F in dU^T's row c - F
+    MOE_LAUNCH(launch_transpose_windows(dGU, 2 * (size_t)F, 0, 2 * F, E, o.offsets, kbase, klen, nullptr, dGT, nc, nc,
+                                        s));
     MOE_LAUNCH(launch_transpose_windows(Hb, F, 0, F, E, o.offsets, kbase, klen, nullptr, HbT, nc, nc, s));
     MOE_LAUNCH(launch_transpose_windows(xp, d, 0, d, E, o.offsets, kbase, klen, nullptr, xpT, nc, nc, s));
     MOE_LAUNCH(launch_transpose_windows(dyp, d, 0, d, E, o.offsets, kbase, klen, o.gates_perm, dysT, nc, nc, s));
     if (c.n_shared) {
         void* dGUs = at<void>(ws, B.dGUs);
-        MOE_LAUNCH(launch_transpose_windows(dGUs, 2 * (size_t)Fs, 0, Fs, 1, s_off, s_kbase, s_klen, nullptr,
+        MOE_LAUNCH(launch_transpose_windows(dGUs, 2 * (size_t)Fs, 0, 2 * Fs, 1, s_off, s_kbase, s_klen, nullptr,
                                             at<void>(ws, B.dGsT), ncs, ncs, s));
-        MOE_LAUNCH(launch_transpose_windows(dGUs, 2 * (size_t)Fs, Fs, Fs, 1, s_off, s_kbase, s_klen, nullptr,
-                                            at<void>(ws, B.dUsT), ncs, ncs, s));
         MOE_LAUNCH(launch_transpose_windows(at<void>(ws, B.Hbs), Fs, 0, Fs, 1, s_off, s_kbase, s_klen, nullptr,
                                             at<void>(ws, B.HbsT), ncs, ncs, s));
         MOE_LAUNCH(launch_transpose_windows(x, d, 0, d, 1, s_off, s_kbase, s_klen, nullptr, at<void>(ws, B.xT), ncs,

@@ -50,32 +50,30 @@ __global__ void k_windows_kernel(int E, int32_t* __restrict__ offsets, int32_t* 
     pdl_trigger();
 }
 
-// 64 x 64 bf16 tiles are staged in shared memory with a 2-element row pad:
-// loads and stores move 16-byte chunks (8 elements), and the column gathers of
-// the store phase hit distinct banks.
-constexpr int TPAD = TT + 2;
+// A block moves 64 window columns (source rows) x 128 source columns.  The
+// tile is staged in shared memory as 32-bit words, word w of source column c
+// holding rows 2w and 2w+1 (the bf16 pair that lands side by side in the
+// destination row), so both phases move whole words: the load phase pairs
+// two rows' 16-byte chunks with byte permutes, the store phase reads 16-byte
+// runs of a column.  Word w of column c sits at w ^ tile_swizzle(c), which
+// puts the 32 word stores of a load-phase warp on 32 banks and keeps each
+// 16-byte run of the store phase in one 4-word group (its two halves swapped
+// when bit 1 of the swizzle is set).  All of a thread's loads are issued
+// before the first shared-memory store, so each SM keeps up to 128 KB of
+// reads in flight.
+constexpr int TC = 128;  // source columns per block
+constexpr int TW = TT / 2;  // words per staged column
 
-__device__ __forceinline__ void put8(uint16_t* row, const uint4 v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        row[2 * j] = (uint16_t)(w[j] & 0xFFFFu);
-        row[2 * j + 1] = (uint16_t)(w[j] >> 16);
-    }
-}
-
-__device__ __forceinline__ uint4 gather8(const uint16_t (*tile)[TPAD], int r0, int c) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = (uint32_t)tile[r0 + 2 * j][c] | ((uint32_t)tile[r0 + 2 * j + 1][c] << 16);
-    return make_uint4(w[0], w[1], w[2], w[3]);
+__device__ __forceinline__ int tile_swizzle(int c) {
+    const int ch = c >> 3;  // the 8-column chunk of the source row
+    return ((ch & 7) << 2) | ((ch >> 3) << 1);
 }
 
 // dst[c][kbase[e] + k] = scale(row) * src[(offsets[e] + k) * ld_src + col0 + c] for
-// k < klen[e], 0 for klen[e] <= k < round64(klen[e]); c < C.  One 64 x 64 tile per
-// block: a block's 64 destination columns lie inside one expert's window.  C,
-// ld_src, col0 and ld_dst are multiples of 8 (16-byte chunks).
-__global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloat16* __restrict__ src, size_t ld_src,
+// k < klen[e], 0 for klen[e] <= k < round64(klen[e]); c < C.  A block's 64
+// destination columns lie inside one expert's window.  C, ld_src, col0 and
+// ld_dst are multiples of 8 (16-byte chunks).
+__global__ void __launch_bounds__(256, 8) transpose_windows_kernel(const __nv_bfloat16* __restrict__ src, size_t ld_src,
                                                                 int col0, int C, int E,
                                                                 const int32_t* __restrict__ offsets,
                                                                 const int32_t* __restrict__ kbase,
@@ -84,8 +82,8 @@ __global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloa
                                                                 __nv_bfloat16* __restrict__ dst, size_t ld_dst,
                                                                 int ncols) {
     pdl_wait();
-    __shared__ uint16_t tile[TT][TPAD];
-    const int c_tile = blockIdx.x * TT;  // source column block
+    __shared__ __align__(16) uint32_t tile[TC * TW];
+    const int c_tile = blockIdx.x * TC;  // source column block
     const int k0 = blockIdx.y * TT;      // destination column block
     if (k0 < ncols) {
         int lo = 0, hi = E - 1;  // last expert whose window starts at or before k0
@@ -99,33 +97,61 @@ __global__ void __launch_bounds__(256) transpose_windows_kernel(const __nv_bfloa
         const int padded = (len + 63) / 64 * 64;
         if (k0 < base + padded) {  // beyond the last window: nothing to write
             const int row_base = __ldg(offsets + e) + (k0 - base);
-            // load: 64 source rows x 8 chunks of 8 columns
-            for (int i = threadIdx.x; i < TT * 8; i += blockDim.x) {
-                const int kk = i >> 3, ch = i & 7;
-                const int k = k0 - base + kk, c = c_tile + ch * 8;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (k < len && c < C) {
-                    const size_t r = (size_t)(row_base + kk);
-                    v = __ldg(reinterpret_cast<const uint4*>(src + r * ld_src + col0 + c));
-                    if (row_scale) {
-                        const float sc = __ldg(row_scale + r);
-                        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+            // load: 32 row pairs x 16 chunks of 8 columns, two (pair, chunk) items per thread
+            constexpr int kItems = (TW * (TC / 8)) / 256;
+            uint4 v[kItems][2];
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int i = threadIdx.x + it * 256;
+                const int ch = i & (TC / 8 - 1), p = i / (TC / 8);
+                const int c = c_tile + ch * 8;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int kk = 2 * p + h;
+                    v[it][h] = make_uint4(0u, 0u, 0u, 0u);
+                    if (k0 - base + kk < len && c < C)
+                        v[it][h] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(row_base + kk) * ld_src + col0 + c));
+                }
+            }
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int i = threadIdx.x + it * 256;
+                const int ch = i & (TC / 8 - 1), p = i / (TC / 8);
+                if (row_scale) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int kk = 2 * p + h;
+                        if (k0 - base + kk >= len) continue;
+                        const float sc = __ldg(row_scale + row_base + kk);
+                        __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&v[it][h]);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const float2 f = __bfloat1622float2(h[j]);
-                            h[j] = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+                            const float2 f = __bfloat1622float2(b[j]);
+                            b[j] = __floats2bfloat162_rn(f.x * sc, f.y * sc);
                         }
                     }
                 }
-                put8(&tile[kk][ch * 8], v);
+                const uint32_t a[4] = {v[it][0].x, v[it][0].y, v[it][0].z, v[it][0].w};
+                const uint32_t b[4] = {v[it][1].x, v[it][1].y, v[it][1].z, v[it][1].w};
+                const int sw = tile_swizzle(ch * 8);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = ch * 8 + 2 * j;  // source columns c (low halves) and c + 1 (high halves)
+                    tile[c * TW + (p ^ sw)] = __byte_perm(a[j], b[j], 0x5410);
+                    tile[(c + 1) * TW + (p ^ sw)] = __byte_perm(a[j], b[j], 0x7632);
+                }
             }
             __syncthreads();
-            // store: 64 destination rows (source columns) x 8 chunks of 8 window columns
-            for (int i = threadIdx.x; i < TT * 8; i += blockDim.x) {
-                const int cc = i >> 3, ch = i & 7;
-                if (c_tile + cc < C)
-                    *reinterpret_cast<uint4*>(dst + (size_t)(c_tile + cc) * ld_dst + k0 + ch * 8) =
-                        gather8(tile, ch * 8, cc);
+            // store: 128 destination rows (source columns) x 8 runs of 8 window columns
+#pragma unroll
+            for (int it = 0; it < (TC * 8) / 256; ++it) {
+                const int i = threadIdx.x + it * 256;
+                const int cc = i >> 3, q = i & 7;
+                if (c_tile + cc >= C) continue;
+                const int sw = tile_swizzle(cc);
+                uint4 w = *reinterpret_cast<const uint4*>(&tile[cc * TW + 4 * (q ^ (sw >> 2))]);
+                if (sw & 2) w = make_uint4(w.z, w.w, w.x, w.y);
+                *reinterpret_cast<uint4*>(dst + (size_t)(c_tile + cc) * ld_dst + k0 + q * 8) = w;
             }
         }
     }
@@ -313,7 +339,7 @@ cudaError_t launch_transpose_windows(const void* src, size_t ld_src, int col0, i
                                      size_t ld_dst, int ncols, cudaStream_t s) {
     if (C == 0 || ncols == 0) return cudaSuccess;
     if (C % 8 || ld_src % 8 || col0 % 8 || ld_dst % 8 || ncols % 64) return cudaErrorInvalidValue;
-    const dim3 grid((C + TT - 1) / TT, (ncols + TT - 1) / TT);
+    const dim3 grid((C + TC - 1) / TC, (ncols + TT - 1) / TT);
     launch_pdl(transpose_windows_kernel, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), ld_src, col0,
                C, E, offsets, kbase, klen, row_scale, static_cast<__nv_bfloat16*>(dst), ld_dst, ncols);
     return cudaGetLastError();
