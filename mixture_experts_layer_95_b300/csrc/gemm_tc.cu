@@ -158,9 +158,9 @@ struct SmemTailT {
 };
 using SmemTailCore = SmemTailT<MAX_GROUPS + 1>;
 struct SmemTail : SmemTailCore {
-    // epilogue staging: each epilogue warp transposes 32 rows x 32 fp32 columns
-    // so that its global stores are whole 128-byte row segments
-    float stage[4][32][33];
+    // epilogue staging: each epilogue warp passes 32 rows x 32 fp32 columns
+    // through its block so that its global stores cover whole row segments
+    alignas(16) float stage[4][32][33];
 };
 
 template <int MODE, bool W8>
@@ -516,9 +516,14 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
         }
         if (valid && p.bwd_dgp_part[t.prob]) p.bwd_dgp_part[t.prob][(size_t)t.n * p.bwd_dgp_ld[t.prob] + grow] = part;
     } else {
-        // fp32 output: each 32x32 block of the warp's rows goes through shared
-        // memory (thread = row on the way in, lane = column on the way out), so
-        // that every store instruction writes one 128-byte row segment.
+        // fp32 (or bf16) rows out: each 32x32 block of the warp's rows goes
+        // through shared memory, written row by row (thread = row, 16-byte
+        // chunks) and read back with 8 lanes per row, so that every store
+        // instruction writes 4 whole row segments (measured against one 32-bit
+        // store per row segment: the saved-activation backward's weight-gradient
+        // GEMMs, 6.00 -> 5.85 ms per backward call on the Mixtral prefill shape;
+        // a TMA store of each block, which shares the copy engine with the
+        // operand loads, was slower: 6.50 ms).
         float* out = static_cast<float*>(p.out[t.prob]);
         float scale = 1.0f;
         if ((MODE == kGemmScale || MODE == kGemmScaleSplit) && valid && p.row_scale[t.prob] != nullptr)
@@ -528,9 +533,13 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
         const int nvalid = min(warp_rows, t.rows_valid - wrow0);  // rows of this warp that exist
         // a K-grouped tile with an empty window computed nothing: its output is 0
         const bool computed = t.kb1 > t.kb0;
-        // the next 32 accumulator columns are read from TMEM while this chunk's
-        // rows are stored; a full 32 x 32 block is read from shared memory into
-        // registers before any of its 32 row stores is issued
+        // The next 32 accumulator columns are read from TMEM while this chunk's
+        // rows are stored.  The 32 x 32 block in shared memory: row r's 16-byte
+        // chunk j at float r * 32 + ((j ^ (r & 7)) << 2), so that both the
+        // row-wise 16-byte writes and the 16-byte reads of 8 lanes per row hit
+        // distinct banks.
+        float* sb = &stage[0][0];
+        auto sidx = [](int r, int c) { return r * 32 + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); };
         uint32_t v[32];
         __syncwarp();
         tmem_ld32(tacc, v);
@@ -543,38 +552,54 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
                 if (p.wscale1[t.prob])
                     apply_wscale32(v, p.wscale1[t.prob], static_cast<size_t>(t.g) * N + col, N - col);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) stage[lane][i] = computed ? scale * __uint_as_float(v[i]) : 0.0f;
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(sb + lane * 32 + ((j ^ (lane & 7)) << 2)) =
+                        computed ? make_float4(scale * __uint_as_float(v[4 * j]), scale * __uint_as_float(v[4 * j + 1]),
+                                               scale * __uint_as_float(v[4 * j + 2]), scale * __uint_as_float(v[4 * j + 3]))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             __syncwarp();
             const bool more = c0 + 32 < ncols;
             uint32_t vn[32];
             if (more) tmem_ld32(tacc + c0 + 32, vn);
-            if (live && p.out_bf16[t.prob]) {  // bf16 rows: lane = column, 64-byte row segments
-                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[t.prob]) +
-                                     (size_t)(t.out_row0 + wrow0) * N + col + lane;
-                const bool col_ok = col + lane < N;
-                if (nvalid == 32 && col + 32 <= N) {
-                    float rv[32];
+            if (live) {
+                const size_t row0 = (size_t)(t.out_row0 + wrow0);
+                if (nvalid == 32 && col + 32 <= N && (N & 3) == 0) {
+                    // 8 lanes per row, 4 rows per instruction: 16-byte reads, whole row segments out
+                    const int rq = lane >> 3, jj = lane & 7;
+                    float4 q[8];
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) rv[r] = stage[r][lane];
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + rq;
+                        q[i] = *reinterpret_cast<const float4*>(sb + rr * 32 + ((jj ^ (rr & 7)) << 2));
+                    }
+                    if (p.out_bf16[t.prob]) {
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[t.prob]) + row0 * N + col + 4 * jj;
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) dst[(size_t)r * N] = __float2bfloat16_rn(rv[r]);
-                } else {
-                    for (int r = 0; r < nvalid; ++r)
-                        if (col_ok) dst[(size_t)r * N] = __float2bfloat16_rn(stage[r][lane]);
-                }
-            } else if (live) {
-                float* dst = out + (size_t)(t.out_row0 + wrow0) * N + col + lane;
-                if (nvalid == 32 && col + 32 <= N) {
-                    float rv[32];
+                        for (int i = 0; i < 8; ++i) {
+                            __nv_bfloat162 a = __floats2bfloat162_rn(q[i].x, q[i].y);
+                            __nv_bfloat162 b = __floats2bfloat162_rn(q[i].z, q[i].w);
+                            uint2 u;
+                            u.x = *reinterpret_cast<uint32_t*>(&a);
+                            u.y = *reinterpret_cast<uint32_t*>(&b);
+                            *reinterpret_cast<uint2*>(dst + (size_t)(4 * i + rq) * N) = u;
+                        }
+                    } else {
+                        float* dst = out + row0 * N + col + 4 * jj;
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) rv[r] = stage[r][lane];
-#pragma unroll
-                    for (int r = 0; r < 32; ++r) dst[(size_t)r * N] = rv[r];
+                        for (int i = 0; i < 8; ++i) *reinterpret_cast<float4*>(dst + (size_t)(4 * i + rq) * N) = q[i];
+                    }
                 } else {
                     const bool col_ok = col + lane < N;
-                    for (int r = 0; r < nvalid; ++r)
-                        if (col_ok) dst[(size_t)r * N] = stage[r][lane];
+                    if (p.out_bf16[t.prob]) {
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[t.prob]) + row0 * N + col + lane;
+                        for (int r = 0; r < nvalid; ++r)
+                            if (col_ok) dst[(size_t)r * N] = __float2bfloat16_rn(sb[sidx(r, lane)]);
+                    } else {
+                        float* dst = out + row0 * N + col + lane;
+                        for (int r = 0; r < nvalid; ++r)
+                            if (col_ok) dst[(size_t)r * N] = sb[sidx(r, lane)];
+                    }
                 }
             }
             if (more) {
