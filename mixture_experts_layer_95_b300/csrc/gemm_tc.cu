@@ -371,6 +371,38 @@ __device__ __forceinline__ void store_bf16_row(const uint4 (&w)[4], int nc, __nv
 // warp_row0 >= 0: the warp's rows are warp_row0 .. warp_row0 + warp_rows - 1,
 // held by its lanes 0 .. warp_rows - 1 (an M = 64 tile keeps 16 rows in each
 // 32-lane quarter of TMEM); otherwise the warp holds 32 consecutive rows.
+// The warp's 32 rows x 32 fp32 columns (x: this thread's row, as bits) to
+// dst + r * ld for the rows r < nvalid that exist and the columns c < ncv,
+// through the warp's 32 x 32 shared block: row r's 16-byte chunk j sits at
+// float r * 32 + ((j ^ (r & 7)) << 2), so that the row-wise 16-byte writes
+// and the 16-byte reads of 8 lanes per row hit distinct banks and every store
+// instruction covers 4 whole row segments.
+__device__ __forceinline__ void stage_rows_f32(float* sb, const uint32_t (&x)[32], float* dst, size_t ld, int nvalid,
+                                               int ncv) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(sb + lane * 32 + ((j ^ (lane & 7)) << 2)) =
+            make_float4(__uint_as_float(x[4 * j]), __uint_as_float(x[4 * j + 1]), __uint_as_float(x[4 * j + 2]),
+                        __uint_as_float(x[4 * j + 3]));
+    __syncwarp();
+    if (nvalid == 32 && ncv >= 32 && (ld & 3) == 0) {
+        const int rq = lane >> 3, jj = lane & 7;
+        float4 q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + rq;
+            q[i] = *reinterpret_cast<const float4*>(sb + rr * 32 + ((jj ^ (rr & 7)) << 2));
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) *reinterpret_cast<float4*>(dst + (size_t)(4 * i + rq) * ld + 4 * jj) = q[i];
+    } else if (lane < ncv) {
+        for (int r = 0; r < nvalid; ++r)
+            dst[(size_t)r * ld + lane] = sb[r * 32 + (((lane >> 2) ^ (r & 7)) << 2) + (lane & 3)];
+    }
+    __syncwarp();  // the block is read before it is written again
+}
+
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile,
                                               float (*stage)[33], int col_lo = 0, int ncols = BN, bool ilv = false,
@@ -387,6 +419,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[t.prob]);
         __nv_bfloat16* out_lo = static_cast<__nv_bfloat16*>(p.out2[t.prob]);
         const int nchunks = ilv ? ncols / 64 : BN / 2 / 32;
+        const int wrow0 = warp_row0 >= 0 ? warp_row0 : row_in_tile - (int)(threadIdx.x & 31);  // first row of this warp
+        const int nvalid = min(warp_rows, t.rows_valid - wrow0);                                 // its rows that exist
 #pragma unroll 1
         for (int ch = 0; ch < nchunks; ++ch) {
             int gcol, ucol, col;  // TMEM columns of G and U, first output feature
@@ -405,34 +439,20 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
             tmem_ld32(tacc + gcol, g);
             tmem_ld32(tacc + ucol, u);
             tmem_ld_wait();
-            if (!valid || col >= N) continue;
+            if (col >= N) continue;  // (uniform across the warp)
             if (p.wscale1[t.prob]) {  // FP8 weights: per-channel scales of W1 and W3
                 const size_t wr = static_cast<size_t>(t.g) * N + col;
                 apply_wscale32(g, p.wscale1[t.prob], wr, N - col);
                 apply_wscale32(u, p.wscale2[t.prob], wr, N - col);
             }
+            if (p.out_g[t.prob] && nvalid > 0) {  // the pre-activation G and U as well (kept for the backward)
+                const size_t r0 = static_cast<size_t>(t.out_row0 + wrow0) * N + col;
+                stage_rows_f32(&stage[0][0], g, p.out_g[t.prob] + r0, N, nvalid, N - col);
+                stage_rows_f32(&stage[0][0], u, p.out_u[t.prob] + r0, N, nvalid, N - col);
+            }
+            if (!valid) continue;
             __nv_bfloat16* dst = out + grow * N + col;
             __nv_bfloat16* dst_lo = out_lo ? out_lo + grow * N + col : nullptr;
-            if (p.out_g[t.prob]) {  // the pre-activation G and U as well (kept for the backward)
-                float* gd = p.out_g[t.prob] + grow * N + col;
-                float* ud = p.out_u[t.prob] + grow * N + col;
-                if (col + 32 <= N) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        reinterpret_cast<float4*>(gd)[q] =
-                            make_float4(__uint_as_float(g[4 * q]), __uint_as_float(g[4 * q + 1]),
-                                        __uint_as_float(g[4 * q + 2]), __uint_as_float(g[4 * q + 3]));
-                        reinterpret_cast<float4*>(ud)[q] =
-                            make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
-                                        __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3]));
-                    }
-                } else {
-                    for (int i = 0; i < 32 && col + i < N; ++i) {
-                        gd[i] = __uint_as_float(g[i]);
-                        ud[i] = __uint_as_float(u[i]);
-                    }
-                }
-            }
             if (col + 32 <= N) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
