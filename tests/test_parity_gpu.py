@@ -64,6 +64,9 @@ SMALL = [
     Workload("yperm_bf16_pairs", T=1100, d=256, E=4, F=384, k=2, yperm_bf16=True),
     Workload("yperm_bf16_split_k_t3", T=3, d=256, E=16, F=320, k=2, n_shared=1, F_s=192, yperm_bf16=True),
     Workload("yperm_bf16_decode_64rows", T=100, d=256, E=8, F=320, k=2, n_shared=1, F_s=192, yperm_bf16=True),
+    # the logits GEMM with rows of 18 fp32 logits (72 bytes, not whole 16-byte
+    # chunks): its epilogue stores element by element
+    Workload("gemm_router_e18_bf16", T=300, d=256, E=18, F=128, k=3),
     # one token on a router too wide for the fused small-batch kernels: the
     # decode GEMM with split-K
     Workload("decode_t1_e40_bf16", T=1, d=512, E=40, F=512, k=2),
