@@ -403,7 +403,8 @@ __device__ __forceinline__ void stage_rows_f32(float* sb, const uint32_t (&x)[32
     __syncwarp();  // the block is read before it is written again
 }
 
-template <int MODE>
+// W8: the FP8-weight kernel, which never keeps G and U (no out_g / out_u)
+template <int MODE, bool W8 = false>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, uint32_t tacc, int row_in_tile,
                                               float (*stage)[33], int col_lo = 0, int ncols = BN, bool ilv = false,
                                               int warp_row0 = -1, int warp_rows = 32) {
@@ -445,7 +446,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const Tile& t, 
                 apply_wscale32(g, p.wscale1[t.prob], wr, N - col);
                 apply_wscale32(u, p.wscale2[t.prob], wr, N - col);
             }
-            if (p.out_g[t.prob] && nvalid > 0) {  // the pre-activation G and U as well (kept for the backward)
+            if (!W8 && p.out_g[t.prob] && nvalid > 0) {  // the pre-activation G and U as well (kept for the backward)
                 const size_t r0 = static_cast<size_t>(t.out_row0 + wrow0) * N + col;
                 stage_rows_f32(&stage[0][0], g, p.out_g[t.prob] + r0, N, nvalid, N - col);
                 stage_rows_f32(&stage[0][0], u, p.out_u[t.prob] + r0, N, nvalid, N - col);
@@ -879,10 +880,10 @@ __global__ void __launch_bounds__(W8 ? W8_THREADS : NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
             if (MODE != kGemmSwigluBwd && t.half)  // M = 64: rows 16q .. 16q + 15 in lanes 0-15 of quarter q
-                epilogue_tile<MODE>(p, t, tacc, lane < 16 ? quarter * 16 + lane : BM, st.stage[quarter], 0, BN, false,
+                epilogue_tile<MODE, W8>(p, t, tacc, lane < 16 ? quarter * 16 + lane : BM, st.stage[quarter], 0, BN, false,
                                     quarter * 16, 16);
             else
-                epilogue_tile<MODE>(p, t, tacc, row_in_tile, st.stage[quarter]);
+                epilogue_tile<MODE, W8>(p, t, tacc, row_in_tile, st.stage[quarter]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.tmem_empty[acc]);
