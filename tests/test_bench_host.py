@@ -116,3 +116,23 @@ def test_clock_sampler_places_smi_lines_by_their_own_timestamps():
     cs.window = (t0 - 0.001, t0 + 0.05)
     s = cs.summary()
     assert s["samples"] == 2 and s["sm_mhz"] == 1226.0 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_recorded_traffic_is_dropped_once_the_kernel_source_changes(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu capture only while the kernel
+    source it was taken on is unchanged: a stale hash reads as no figure."""
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "csrc"
+    csrc.mkdir()
+    (csrc / "k.cu").write_text("__global__ void k() {}\n")
+    monkeypatch.setattr(bench, "CSRC", str(csrc))
+    entry = {"sources": ["k.cu"], "dram_bytes_per_launch": 12345, "source_sha256_16": bench.source_hash(["k.cu"])}
+    tf = tmp_path / "traffic.json"
+    tf.write_text(json.dumps({"w": entry}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tf))
+    assert bench.recorded_traffic("w") == 12345
+    assert bench.recorded_traffic("other") is None
+    (csrc / "k.cu").write_text("__global__ void k() { /* changed */ }\n")
+    assert bench.recorded_traffic("w") is None
+
